@@ -1,0 +1,405 @@
+"""Benchmark: chunkwise delta-rule prefill tokens/s (headline) and decode
+state-GB/s, against the GB300 roofline, with the fp64 oracle timed on the
+host cores beside them.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Headline step: one ``la_prefill_delta`` call on the GPT-2-small-shaped
+workload (8 sequences x 2048 tokens, 12 heads of 64, bf16, k L2-normalised,
+beta = sigmoid(N(0,1)), no gate, chunk 64, fp32 state), inputs resident in
+HBM.  L2 is flushed (a 256 MiB write) before every timed step; kernel time is
+taken with CUDA events on the launching stream.  The same JSON line carries
+the decode step (256 x 32 heads of 128x128 fp32 state, 64 steps), the gated
+(4 x 8192, 32 heads of 128) and packed varlen (65536 tokens, 16 heads of 128)
+prefills, an end-to-end number through the public API with pinned host
+buffers, the roofline of the dominant kernel and the oracle's CPU throughput.
+
+Multi-GPU (torchrun): every rank runs its own independent batch (weak
+scaling, no data-path collective); the timed region is bracketed by a barrier
+and the slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+L2_FLUSH_BYTES = 256 << 20
+HEADLINE = "gpt2_prefill"
+METRIC = "prefill tokens/s & decode state GB/s (delta-rule attn), % of GB300 roofline"
+
+
+# ------------------------------------------------------------------ helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def prefill_algo(w: wl.Workload, chunk=64, final_states=False):
+    """Algorithmic bytes and contraction FLOPs of one delta-rule prefill.
+
+    Bytes: q, k, v read and o written once in the I/O dtype, beta logits
+    (one per token and head), gate logits (dk per token and head) when gated,
+    final states (fp32) when returned.  FLOPs per token and head:
+    10 C d + 6 d^2 (dense C x C tiles: K K^T, T K, T V, Q K^T, A u; and
+    W S, Q S, K^T u), with d = dk = dv."""
+    esz = torch.tensor([], dtype=w.dtype).element_size()
+    th = w.ntok * w.H
+    per = esz * (2 * w.dk + 2 * w.dv) + esz + (esz * w.dk if w.gated else 0)
+    nbytes = th * per + (len(w.lengths) * w.H * w.dk * w.dv * 4 if final_states else 0)
+    d = w.dk
+    flops = th * (10 * chunk * d + 6 * d * d)
+    return nbytes, flops
+
+
+def decode_state_bytes(w: wl.Workload):
+    return 8 * w.n_seq * w.H * w.dk * w.dv   # fp32 state read + written once per step
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "delta_rule_recurrent_chunkwise_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key: str):
+    """Per-launch DRAM bytes from the committed ncu summary, or None when the
+    summary is missing or was taken on different kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        e = t[kernel_key]
+        if e.get("source_hash") != kernel_source_hash():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_gpu{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        except Exception:
+            return None
+        if not rows:
+            return None
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]
+                          and "Not" not in r[5 + i]})
+        loaded = [s for s in sm if mx and s >= 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# --------------------------------------------------------------- GPU timing
+
+class Prefill:
+    """Device-resident inputs and one la_prefill_delta call per step."""
+
+    def __init__(self, la, w: wl.Workload, seed: int, dev, final_states=False):
+        self.la, self.w = la, w
+        inp = wl.inputs_for(w, seed=seed)
+        self.host = inp
+        self.t = {n: (None if inp[n] is None else inp[n].to(dev))
+                  for n in ("q", "k", "v", "beta_logits", "gate_logits", "cu_seqlens")}
+        self.o = torch.empty((w.ntok, w.H, w.dv), dtype=w.dtype, device=dev)
+        self.fS = (torch.empty((len(w.lengths), w.H, w.dk, w.dv), device=dev)
+                   if final_states else None)
+        nbytes = la.la_prefill_delta_workspace_size(len(w.lengths), w.ntok, w.H, w.dk, w.dv)
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
+        self.cu_host = inp["cu_seqlens"]
+
+    def step(self, stream):
+        t = self.t
+        self.la.la_prefill_delta(t["q"], t["k"], t["v"], t["beta_logits"], t["gate_logits"],
+                                 self.o, t["cu_seqlens"], final_S=self.fS, workspace=self.ws,
+                                 cu_seqlens_host=self.cu_host, stream=stream)
+
+
+def time_steps(step_fn, steps, warmup, flush, stream, barrier=None):
+    """Per-step CUDA-event durations (ms) on `stream`, L2 flushed between steps."""
+    for _ in range(warmup):
+        step_fn()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    for i in range(steps):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        step_fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def run_ours(args, rank, world, dev, dist):
+    import delta_rule_recurrent_chunkwise_gb300 as la
+    la.build()
+    la.library()
+    pk = peaks()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    barrier = (lambda: dist.barrier()) if dist is not None else None
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    result = {}
+    with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
+        # ---- headline: GPT-2-shaped delta prefill
+        w = wl.workload(HEADLINE)
+        pf = Prefill(la, w, seed=rank, dev=dev)
+        ms = time_steps(lambda: pf.step(stream), args.steps, args.warmup, flush, stream, barrier)
+        total_ms = max_over_ranks(sum(ms))
+        tokens = w.ntok * world * args.steps
+        value = tokens / (total_ms / 1e3)
+        kern_ms = sum(ms) / len(ms)
+        nbytes, flops = prefill_algo(w)
+        achieved = nbytes / (kern_ms / 1e3) / 1e9
+        traffic = ncu_traffic("delta_prefill:" + HEADLINE)
+        result.update(
+            value=value, ms_per_step=total_ms / args.steps, gpu_launches=args.steps,
+            roofline={"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                      "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
+                      "kernel": "la_prefill_delta (chunkwise delta rule)",
+                      "algorithmic_bytes_per_launch": nbytes,
+                      "tensor_tflops": flops / (kern_ms / 1e3) / 1e12,
+                      "tensor_frac": flops / (kern_ms / 1e3) / 1e12 / pk["bf16_tflops"],
+                      "peak_source": pk["source"]})
+        # ---- end to end through the public API with pinned host buffers
+        host = {n: (None if pf.host[n] is None else pf.host[n].pin_memory())
+                for n in ("q", "k", "v", "beta_logits")}
+        o_host = torch.empty(pf.o.shape, dtype=pf.o.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+        d2h = o_host.numel() * o_host.element_size()
+
+        def e2e_step():
+            for n, t in host.items():
+                pf.t[n].copy_(t, non_blocking=True)
+            pf.step(stream)
+            o_host.copy_(pf.o, non_blocking=True)
+
+        e2e_ms = time_steps(e2e_step, max(3, args.steps // 2), 2, None, stream, barrier)
+        e2e_total = max_over_ranks(sum(e2e_ms))
+        result["e2e"] = {"value": w.ntok * world * len(e2e_ms) / (e2e_total / 1e3),
+                         "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        del pf
+
+        if not args.headline_only:
+            extra = {}
+            # ---- decode: 64 consecutive steps on 256 x 32 states
+            dw = wl.workload("decode")
+            d = wl.inputs_for(dw, seed=rank)
+            toks = {n: (None if d[n] is None else d[n].to(dev))
+                    for n in ("q", "k", "v", "beta_logits", "gate_logits")}
+            state = d["state"].to(dev)
+            od = torch.empty((dw.n_seq, dw.H, dw.dv), dtype=dw.dtype, device=dev)
+
+            def decode_64():
+                for s in range(dw.steps):
+                    la.la_decode_step(toks["q"][s], toks["k"][s], toks["v"][s],
+                                      toks["beta_logits"][s], toks["gate_logits"][s], od, state,
+                                      stream=stream)
+
+            dms = time_steps(decode_64, max(2, args.steps // 4), 1, None, stream, barrier)
+            d_ms = max_over_ranks(sum(dms)) / len(dms)
+            sb = decode_state_bytes(dw) * dw.steps
+            gbs = sb / (d_ms / 1e3) / 1e9
+            extra["decode"] = {"workload": "256 seq x 32 heads, dk=dv=128, fp32 state, 64 steps",
+                               "state_GBps": gbs * world, "ms_per_64_steps": d_ms,
+                               "us_per_step": d_ms * 1e3 / dw.steps,
+                               "frac_of_hbm": gbs / pk["hbm_gbs"],
+                               "state_bytes_per_step": decode_state_bytes(dw)}
+            del toks, state, d
+            # ---- gated and varlen prefills
+            for name in ("gated_prefill", "varlen_prefill"):
+                gw = wl.workload(name, seed=0)
+                fs = name == "varlen_prefill"
+                p = Prefill(la, gw, seed=rank, dev=dev, final_states=fs)
+                gms = time_steps(lambda: p.step(stream), max(3, args.steps // 4), 2, flush,
+                                 stream, barrier)
+                g_ms = max_over_ranks(sum(gms)) / len(gms)
+                nb, fl = prefill_algo(gw, final_states=fs)
+                extra[name] = {"tokens_per_s": gw.ntok * world / (g_ms / 1e3), "ms": g_ms,
+                               "hbm_frac": nb / (g_ms / 1e3) / 1e9 / pk["hbm_gbs"],
+                               "tensor_frac": fl / (g_ms / 1e3) / 1e12 / pk["bf16_tflops"]}
+                if name == "varlen_prefill":
+                    extra[name]["lengths"] = list(gw.lengths)
+                del p
+            result["secondary"] = extra
+    result["clocks"] = clocks.summary()
+    return result
+
+
+# --------------------------------------------------------------- CPU oracle
+
+def cpu_oracle_throughput(w: wl.Workload, target_s: float, nseq=None):
+    """Time the oracle as it stands on a bounded sample of the workload."""
+    import oracle
+    oracle.build()
+    lens = list(w.lengths[:nseq] if nseq else w.lengths)
+    inp = wl.prefill_inputs(lens, w.H, w.dk, w.dv, w.dtype, w.gated, seed=0)
+    f = lambda t: None if t is None else t.double().numpy()
+    args = [f(inp[n]) for n in ("q", "k", "v", "beta_logits", "gate_logits")]
+    cu = inp["cu_seqlens"].numpy()
+    threads = min(oracle.default_threads(), len(lens) * w.H)
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        oracle.delta(*args, cu, nthreads=threads)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= target_s or passes >= 50:
+            break
+    tokens = sum(lens) * passes
+    return {"value": tokens / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(lens)} of {len(w.lengths)} sequences x {w.H} heads x "
+                      f"{lens[0]} tokens, {passes} pass(es), {el:.1f} s, fp64"}
+
+
+# --------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = wl.workload(HEADLINE)
+    config = {"workload": f"{HEADLINE}: B=8 x T=2048 tokens, H=12, d=64, bf16, delta rule "
+                          "without gate, k L2-normalised, chunk 64, fp32 state",
+              "global_batch": 8 * world, "seq_len": 2048, "heads": 12, "head_dim": 64,
+              "chunk": 64, "parallelism": f"independent batches x{world}",
+              "l2": "flushed (256 MiB write) before every timed step"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        cb = cpu_oracle_throughput(w, target_s=min(20.0, 3.0 * args.cpu_seconds), nseq=2)
+        line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "tokens/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": w.ntok / cb["value"] * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": config, "cpu_baseline": cb,
+                "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        dist = tdist
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    r = run_ours(args, rank, world, dev, dist)
+    if rank == 0:
+        line = {"metric": METRIC, "value": r["value"], "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32", "data": "synthetic (seeded; shapes of the page's "
+                "GPT-2-small-shaped model)", "config": config,
+                "roofline": r["roofline"], "e2e": r["e2e"], "gpu_launches": r["gpu_launches"],
+                "clocks": r["clocks"]}
+        if "secondary" in r:
+            line["secondary"] = r["secondary"]
+        if world == 1:
+            line["cpu_baseline"] = cpu_oracle_throughput(w, target_s=args.cpu_seconds, nseq=2)
+        print(json.dumps(line))
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

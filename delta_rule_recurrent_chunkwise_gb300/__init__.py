@@ -1,0 +1,180 @@
+"""GB300 (sm_103a) causal linear / delta-rule attention: thin Python binding.
+
+The product is the C-ABI library ``_lib/liblinattn.so`` declared in
+``include/linattn.h``.  This module only marshals torch tensors (device
+pointers, sizes, the current CUDA stream) into those calls; every step of the
+computation runs in the library's CUDA kernels.  There is no CPU fallback: if
+the library is not built, the first call raises.
+
+Functions (same names as the C ABI):
+  la_prefill_linear, la_prefill_delta, la_prefill_delta_workspace_size,
+  la_decode_step, la_check_device, la_status_string.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB_PATH, build  # noqa: F401  (build needs no GPU)
+
+LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT = 0, 1, 2, 3, 4
+LA_F32, LA_BF16 = 0, 1
+LA_L2NORM_K, LA_L2NORM_Q, LA_SILU_QK = 1, 2, 4
+
+EXPORTED = ("la_prefill_linear", "la_prefill_delta", "la_prefill_delta_workspace_size",
+            "la_decode_step", "la_check_device", "la_status_string")
+
+
+class LinAttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {la_status_string(status)}")
+
+
+_lib = None
+
+
+def library():
+    """Load the in-tree CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CUDA library missing at {LIB_PATH}: build it with "
+                               "delta_rule_recurrent_chunkwise_gb300.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, ip, fp = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        u, sz = ctypes.c_uint, ctypes.c_size_t
+        lib.la_prefill_linear.argtypes = [vp, vp, vp, vp, ip, vp, vp, ip, ip, ip, ip,
+                                          vp, vp, vp, vp, vp]
+        lib.la_prefill_delta.argtypes = [vp, vp, vp, vp, vp, vp, ip, vp, vp, ip, ip, ip, ip, ip,
+                                         fp, u, vp, vp, vp, sz, vp]
+        lib.la_prefill_delta_workspace_size.argtypes = [ip, ip, ip, ip, ip, ip, ip]
+        lib.la_prefill_delta_workspace_size.restype = sz
+        lib.la_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, ip, ip, ip, ip, ip, fp, u, vp, vp]
+        lib.la_check_device.argtypes = [vp]
+        lib.la_status_string.argtypes = [ip]
+        lib.la_status_string.restype = ctypes.c_char_p
+        for f in ("la_prefill_linear", "la_prefill_delta", "la_decode_step", "la_check_device"):
+            getattr(lib, f).restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def la_status_string(status: int) -> str:
+    return library().la_status_string(int(status)).decode()
+
+
+# ---------------------------------------------------------------- marshalling
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _io(t):
+    import torch
+    if t.dtype == torch.float32:
+        return LA_F32
+    if t.dtype == torch.bfloat16:
+        return LA_BF16
+    raise TypeError(f"unsupported I/O dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(tensors, dtype=None, device=None):
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if dtype is not None and t.dtype != dtype:
+            raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+        if device is not None and t.device != device:
+            raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _host_cu(cu_seqlens_host):
+    if cu_seqlens_host is None:
+        return None, None
+    import torch
+    h = torch.as_tensor(cu_seqlens_host, dtype=torch.int32).contiguous()
+    return h, ctypes.c_void_p(h.data_ptr())
+
+
+def la_prefill_linear(q, k, v, o, cu_seqlens, init_S=None, init_z=None, final_S=None,
+                      final_z=None, cu_seqlens_host=None, stream=None):
+    """ELU+1 linear attention prefill.  q,k [ntok,H,dk]; v,o [ntok,H,dv]."""
+    import torch
+    _check(dict(q=q, k=k, v=v, o=o), dtype=q.dtype, device=q.device)
+    _check(dict(cu_seqlens=cu_seqlens), dtype=torch.int32, device=q.device)
+    _check(dict(init_S=init_S, init_z=init_z, final_S=final_S, final_z=final_z),
+           dtype=torch.float32, device=q.device)
+    ntok, H, dk = q.shape
+    dv = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    hold, hptr = _host_cu(cu_seqlens_host)
+    rc = library().la_prefill_linear(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _io(q), _ptr(cu_seqlens),
+                                     hptr, N, H, dk, dv, _ptr(init_S), _ptr(init_z),
+                                     _ptr(final_S), _ptr(final_z), _stream(stream))
+    if rc != LA_OK:
+        raise LinAttnError(rc, "la_prefill_linear")
+    return o
+
+
+def la_prefill_delta_workspace_size(N, ntok, H, dk, dv, chunk=64, io=LA_BF16) -> int:
+    return int(library().la_prefill_delta_workspace_size(N, ntok, H, dk, dv, chunk, io))
+
+
+def la_prefill_delta(q, k, v, beta_logits, gate_logits, o, cu_seqlens, chunk=64, scale=1.0,
+                     flags=LA_L2NORM_K, init_S=None, final_S=None, workspace=None,
+                     cu_seqlens_host=None, stream=None):
+    """(Gated) delta-rule prefill.  q,k [ntok,H,dk]; v,o [ntok,H,dv];
+    beta_logits [ntok,H]; gate_logits [ntok,H,dk] or None."""
+    import torch
+    _check(dict(q=q, k=k, v=v, o=o, beta_logits=beta_logits, gate_logits=gate_logits),
+           dtype=q.dtype, device=q.device)
+    _check(dict(cu_seqlens=cu_seqlens), dtype=torch.int32, device=q.device)
+    _check(dict(init_S=init_S, final_S=final_S), dtype=torch.float32, device=q.device)
+    ntok, H, dk = q.shape
+    dv = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    hold, hptr = _host_cu(cu_seqlens_host)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = library().la_prefill_delta(_ptr(q), _ptr(k), _ptr(v), _ptr(beta_logits),
+                                    _ptr(gate_logits), _ptr(o), _io(q), _ptr(cu_seqlens), hptr,
+                                    N, H, dk, dv, int(chunk), float(scale), int(flags),
+                                    _ptr(init_S), _ptr(final_S), _ptr(workspace), ws_bytes,
+                                    _stream(stream))
+    if rc != LA_OK:
+        raise LinAttnError(rc, "la_prefill_delta")
+    return o
+
+
+def la_decode_step(q, k, v, beta_logits, gate_logits, o, state, scale=1.0, flags=LA_L2NORM_K,
+                   stream=None):
+    """One decode step, state updated in place.  q,k [N,H,dk]; v,o [N,H,dv];
+    beta_logits [N,H]; gate_logits [N,H,dk] or None; state [N,H,dk,dv] fp32."""
+    import torch
+    _check(dict(q=q, k=k, v=v, o=o, beta_logits=beta_logits, gate_logits=gate_logits),
+           dtype=q.dtype, device=q.device)
+    _check(dict(state=state), dtype=torch.float32, device=q.device)
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    rc = library().la_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(beta_logits), _ptr(gate_logits),
+                                  _ptr(o), _io(q), N, H, dk, dv, float(scale), int(flags),
+                                  _ptr(state), _stream(stream))
+    if rc != LA_OK:
+        raise LinAttnError(rc, "la_decode_step")
+    return o
+
+
+def la_check_device(stream=None) -> int:
+    """Synchronise the stream and return (and clear) any device-side error."""
+    return int(library().la_check_device(_stream(stream)))

@@ -1,0 +1,103 @@
+// api.cu -- the C ABI (include/linattn.h): argument validation on the host,
+// then launches on the caller's stream.  Nothing here allocates, frees or
+// synchronises (la_check_device excepted), and no exception escapes.
+
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/linattn.h"
+#include "launch.h"
+
+namespace {
+
+bool head_size_ok(int d) { return d == 64 || d == 128; }
+
+bool dtype_ok(la_dtype io) { return io == LA_F32 || io == LA_BF16; }
+
+la_status check_cu_host(const int32_t *cu_host, int N) {
+    if (!cu_host) return LA_OK;
+    if (cu_host[0] < 0) return LA_ERR_INVALID_ARG;
+    for (int n = 0; n < N; ++n)
+        if (cu_host[n + 1] < cu_host[n]) return LA_ERR_INVALID_ARG;
+    return LA_OK;
+}
+
+la_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char *la_status_string(la_status s) {
+    switch (s) {
+        case LA_OK: return "LA_OK";
+        case LA_ERR_INVALID_ARG: return "LA_ERR_INVALID_ARG: invalid argument";
+        case LA_ERR_UNSUPPORTED: return "LA_ERR_UNSUPPORTED: no kernel for this configuration";
+        case LA_ERR_CUDA: return "LA_ERR_CUDA: CUDA runtime or launch error";
+        case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT: a bounded in-kernel wait expired";
+    }
+    return "LA_ERR_UNKNOWN";
+}
+
+la_status la_prefill_linear(const void *q, const void *k, const void *v, void *o, la_dtype io,
+                            const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int N,
+                            int H, int dk, int dv, const float *init_S, const float *init_z,
+                            float *final_S, float *final_z, void *stream) {
+    if (!q || !k || !v || !o || !cu_seqlens || N < 1 || H < 1 || !dtype_ok(io))
+        return LA_ERR_INVALID_ARG;
+    if (dk < 1 || dv < 1) return LA_ERR_INVALID_ARG;
+    if (!head_size_ok(dk) || !head_size_ok(dv) || N > 65535 || H > 65535) return LA_ERR_UNSUPPORTED;
+    if (la_status st = check_cu_host(cu_seqlens_host, N)) return st;
+    la::PrefillArgs a{q, k, v, nullptr, nullptr, o, cu_seqlens, N, H, dk, dv, 1.0f, 0u,
+                      init_S, init_z, final_S, final_z, io == LA_BF16};
+    return from_cuda(la::launch_linear_simt(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t la_prefill_delta_workspace_size(int N, int ntok, int H, int dk, int dv, int chunk,
+                                       la_dtype io) {
+    (void)N; (void)ntok; (void)H; (void)dk; (void)dv; (void)chunk; (void)io;
+    return 0;
+}
+
+la_status la_prefill_delta(const void *q, const void *k, const void *v, const void *beta_logits,
+                           const void *gate_logits, void *o, la_dtype io,
+                           const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int N,
+                           int H, int dk, int dv, int chunk, float scale, unsigned flags,
+                           const float *init_S, float *final_S, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+    (void)workspace;
+    if (!q || !k || !v || !beta_logits || !o || !cu_seqlens || N < 1 || H < 1 || !dtype_ok(io))
+        return LA_ERR_INVALID_ARG;
+    if (dk < 1 || dv < 1 || chunk < 1 || !std::isfinite(scale)) return LA_ERR_INVALID_ARG;
+    if (flags & ~(LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK)) return LA_ERR_INVALID_ARG;
+    if (!head_size_ok(dk) || !head_size_ok(dv) || chunk != 64) return LA_ERR_UNSUPPORTED;
+    if (N > 65535 || H > 65535) return LA_ERR_UNSUPPORTED;
+    if (workspace_bytes < la_prefill_delta_workspace_size(N, 0, H, dk, dv, chunk, io))
+        return LA_ERR_INVALID_ARG;
+    if (la_status st = check_cu_host(cu_seqlens_host, N)) return st;
+    la::PrefillArgs a{q, k, v, beta_logits, gate_logits, o, cu_seqlens, N, H, dk, dv, scale,
+                      flags, init_S, nullptr, final_S, nullptr, io == LA_BF16};
+    return from_cuda(la::launch_delta_simt(a, static_cast<cudaStream_t>(stream)));
+}
+
+la_status la_decode_step(const void *q, const void *k, const void *v, const void *beta_logits,
+                         const void *gate_logits, void *o, la_dtype io, int N, int H, int dk,
+                         int dv, float scale, unsigned flags, float *state, void *stream) {
+    if (!q || !k || !v || !beta_logits || !o || !state || N < 1 || H < 1 || !dtype_ok(io))
+        return LA_ERR_INVALID_ARG;
+    if (dk < 1 || dv < 1 || !std::isfinite(scale)) return LA_ERR_INVALID_ARG;
+    if (flags & ~(LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK)) return LA_ERR_INVALID_ARG;
+    if (!head_size_ok(dk) || !head_size_ok(dv)) return LA_ERR_UNSUPPORTED;
+    if ((int64_t)N * H > 0x7fffffffLL) return LA_ERR_UNSUPPORTED;
+    la::DecodeArgs a{q, k, v, beta_logits, gate_logits, o, N, H, dk, dv, scale, flags, state,
+                     io == LA_BF16};
+    return from_cuda(la::launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+la_status la_check_device(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LA_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
+    return LA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,47 @@
+// common.cuh -- device helpers shared by the linear-attention kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace la {
+
+// ---------------------------------------------------------------- I/O types
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// --------------------------------------------------------------- prologue
+// beta = sigmoid(x): the write strength of the delta rule.
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+// log alpha = -softplus(x) = -(max(x, 0) + log1p(exp(-|x|))): the per-key-
+// channel log decay, written so that it neither overflows nor loses digits.
+__device__ __forceinline__ float log_decay_f(float x) {
+    return -(fmaxf(x, 0.0f) + log1pf(expf(-fabsf(x))));
+}
+
+// alpha = exp(-softplus(x)) = 1 / (1 + e^x); e^x = inf gives alpha = 0.
+__device__ __forceinline__ float decay_f(float x) { return 1.0f / (1.0f + expf(x)); }
+
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
+
+// phi(x) = elu(x) + 1, the positive feature map of ELU+1 linear attention.
+__device__ __forceinline__ float elu1_f(float x) { return x > 0.0f ? x + 1.0f : expf(x); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Option bits (mirror the public header's LA_* values).
+constexpr unsigned kL2NormK = 1u, kL2NormQ = 2u, kSiluQK = 4u;
+
+}  // namespace la

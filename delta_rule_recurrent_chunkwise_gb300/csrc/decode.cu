@@ -1,0 +1,152 @@
+// decode.cu -- one recurrent decode step of the (gated) delta rule.
+//
+// Operation ("From GPT-2 to Kimi K3, explained", sections DeltaNet (Fast
+// Weight Programmers) and Gated DeltaNet, with the per-key-channel decay of
+// section KDA / Kimi Linear), per (sequence, head), state S in R^{dk x dv}:
+//   S' = Diag(alpha) S
+//   u  = beta (v - S'^T k)
+//   S  <- S' + k u^T                      (in place)
+//   o  = scale S^T q = scale (S'^T q + (q.k) u)
+// The last identity lets one pass over S produce both reductions S'^T k and
+// S'^T q, so the state is read once and written once: the step streams
+// 8 * dk * dv bytes of fp32 state per head and is bound by HBM bandwidth.
+//
+// Layout: one CTA of 256 threads per (sequence, head).  A thread owns a
+// float4 column group of `RPT` rows of S and keeps them in registers between
+// the read and the write.  All loads are issued before the prologue runs so
+// that every thread has its whole share of the state in flight at once.
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace la {
+namespace {
+
+struct DecodeParams {
+    const void *q, *k, *v, *beta_logits, *gate_logits;
+    void *o;
+    float *state;
+    int H;
+    float scale;
+    unsigned flags;
+};
+
+template <typename IO, int DK, int DV>
+__global__ void __launch_bounds__(256, 2) decode_step_kernel(DecodeParams p) {
+    constexpr int NT = 256;
+    constexpr int C4 = DV / 4;          // float4 column groups per state row
+    constexpr int RPP = NT / C4;        // rows covered by one pass of the block
+    constexpr int RPT = DK / RPP;       // rows held by each thread
+    static_assert(DK % RPP == 0, "shape");
+
+    __shared__ float sk[DK], sq[DK], sa[DK], sv[DV], su[DV];
+    __shared__ __align__(16) float red_k[RPP][DV];
+    __shared__ __align__(16) float red_q[RPP][DV];
+    __shared__ float s_beta, s_qk;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t nh = blockIdx.x;
+    const int col4 = tid % C4, row0 = tid / C4;
+    float4 *S4 = reinterpret_cast<float4 *>(p.state + nh * (int64_t)(DK * DV));
+
+    // 1. put this thread's share of the state in flight (streaming loads).
+    float4 s[RPT];
+#pragma unroll
+    for (int m = 0; m < RPT; ++m) s[m] = __ldcs(S4 + (row0 + m * RPP) * C4 + col4);
+
+    // 2. prologue: feature map / L2 norm of q and k, beta, per-channel decay.
+    const IO *q = static_cast<const IO *>(p.q) + nh * DK;
+    const IO *k = static_cast<const IO *>(p.k) + nh * DK;
+    const IO *v = static_cast<const IO *>(p.v) + nh * DV;
+    const bool silu = (p.flags & kSiluQK) != 0;
+    if (tid < DK) {
+        float kv = to_f32(k[tid]), qv = to_f32(q[tid]);
+        if (silu) { kv = silu_f(kv); qv = silu_f(qv); }
+        sk[tid] = kv;
+        sq[tid] = qv;
+        sa[tid] = p.gate_logits
+                      ? decay_f(to_f32(static_cast<const IO *>(p.gate_logits)[nh * DK + tid]))
+                      : 1.0f;
+    }
+    if (tid < DV) sv[tid] = to_f32(v[tid]);
+    __syncthreads();
+    if (warp < 2) {
+        float *x = warp == 0 ? sk : sq;
+        const bool norm = (p.flags & (warp == 0 ? kL2NormK : kL2NormQ)) != 0;
+        float ss = 0.0f;
+        for (int i = lane; i < DK; i += 32) ss += x[i] * x[i];
+        ss = warp_sum(ss);
+        const float inv = norm ? 1.0f / fmaxf(sqrtf(ss), 1e-12f) : 1.0f;
+        for (int i = lane; i < DK; i += 32) x[i] *= inv;
+    } else if (warp == 2 && lane == 0) {
+        s_beta = sigmoid_f(to_f32(static_cast<const IO *>(p.beta_logits)[nh]));
+    }
+    __syncthreads();
+    if (warp == 0) {
+        float d = 0.0f;
+        for (int i = lane; i < DK; i += 32) d += sq[i] * sk[i];
+        d = warp_sum(d);
+        if (lane == 0) s_qk = d;
+    }
+
+    // 3. decay the rows, partial reductions S'^T k and S'^T q over own rows.
+    float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
+#pragma unroll
+    for (int m = 0; m < RPT; ++m) {
+        const int r = row0 + m * RPP;
+        const float a = sa[r], kr = sk[r], qr = sq[r];
+        s[m].x *= a; s[m].y *= a; s[m].z *= a; s[m].w *= a;
+        pk.x += kr * s[m].x; pk.y += kr * s[m].y; pk.z += kr * s[m].z; pk.w += kr * s[m].w;
+        pq.x += qr * s[m].x; pq.y += qr * s[m].y; pq.z += qr * s[m].z; pq.w += qr * s[m].w;
+    }
+    reinterpret_cast<float4 *>(&red_k[row0][0])[col4] = pk;
+    reinterpret_cast<float4 *>(&red_q[row0][0])[col4] = pq;
+    __syncthreads();
+
+    // 4. column totals, the delta u and the output.
+    if (tid < DV) {
+        float rk = 0.0f, rq = 0.0f;
+#pragma unroll
+        for (int i = 0; i < RPP; ++i) { rk += red_k[i][tid]; rq += red_q[i][tid]; }
+        const float u = s_beta * (sv[tid] - rk);
+        su[tid] = u;
+        static_cast<IO *>(p.o)[nh * DV + tid] = from_f32<IO>(p.scale * (rq + s_qk * u));
+    }
+    __syncthreads();
+
+    // 5. write S' + k u^T back in place.
+    const float4 u4 = reinterpret_cast<const float4 *>(su)[col4];
+#pragma unroll
+    for (int m = 0; m < RPT; ++m) {
+        const int r = row0 + m * RPP;
+        const float kr = sk[r];
+        float4 w = s[m];
+        w.x += kr * u4.x; w.y += kr * u4.y; w.z += kr * u4.z; w.w += kr * u4.w;
+        __stcs(S4 + r * C4 + col4, w);
+    }
+}
+
+template <typename IO, int DK, int DV>
+cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
+    DecodeParams p{a.q, a.k, a.v, a.beta_logits, a.gate_logits, a.o, a.state,
+                   a.H, a.scale, a.flags};
+    const unsigned grid = (unsigned)((int64_t)a.N * a.H);
+    decode_step_kernel<IO, DK, DV><<<grid, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename IO>
+cudaError_t dispatch(const DecodeArgs &a, cudaStream_t s) {
+    if (a.dk == 128 && a.dv == 128) return launch_t<IO, 128, 128>(a, s);
+    if (a.dk == 128 && a.dv == 64) return launch_t<IO, 128, 64>(a, s);
+    if (a.dk == 64 && a.dv == 128) return launch_t<IO, 64, 128>(a, s);
+    return launch_t<IO, 64, 64>(a, s);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s) {
+    return a.bf16 ? dispatch<__nv_bfloat16>(a, s) : dispatch<float>(a, s);
+}
+
+}  // namespace la

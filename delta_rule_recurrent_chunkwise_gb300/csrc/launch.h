@@ -1,0 +1,39 @@
+// launch.h -- internal launchers behind the C ABI (host side, no validation:
+// api.cu checks every argument before calling these).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace la {
+
+struct PrefillArgs {
+    const void *q, *k, *v, *beta_logits, *gate_logits;
+    void *o;
+    const int32_t *cu_seqlens;
+    int N, H, dk, dv;
+    float scale;
+    unsigned flags;
+    const float *init_S, *init_z;
+    float *final_S, *final_z;
+    bool bf16;
+};
+
+struct DecodeArgs {
+    const void *q, *k, *v, *beta_logits, *gate_logits;
+    void *o;
+    int N, H, dk, dv;
+    float scale;
+    unsigned flags;
+    float *state;
+    bool bf16;
+};
+
+// fp32 SIMT chunk kernels (any I/O dtype).
+cudaError_t launch_linear_simt(const PrefillArgs &a, cudaStream_t s);
+cudaError_t launch_delta_simt(const PrefillArgs &a, cudaStream_t s);
+// HBM-streaming decode step.
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
+
+}  // namespace la

@@ -1,0 +1,362 @@
+// prefill_simt.cu -- fp32 CUDA-core chunkwise prefill kernels.
+//
+// These kernels compute every product in fp32 FMA (no tensor cores), which
+// is what fp32 I/O at a 1e-4 relative tolerance needs.  One CTA of 256
+// threads scans one (sequence, head, 32-wide dv slice) chunk by chunk; the
+// dv columns of the state are independent, so slicing dv multiplies the
+// number of concurrent scans without any exchange.
+//
+// Chunked forms ("From GPT-2 to Kimi K3, explained", section DeltaNet
+// (Parallelizing Linear Transformers with Delta Rule)): inside a chunk the
+// masked q k^T scores act on the chunk's own values, across chunks
+// everything is folded into the state and read back with one product.
+//
+// Delta rule (eq. 8-10 of that section, extended with the cumulative
+// per-key-channel decay of sections Gated DeltaNet and KDA / Kimi Linear):
+// with b = inclusive cumulative sum of log alpha inside the chunk,
+//   A[r][i]  = beta_r sum_c k_rc k_ic e^{b_rc - b_ic}      (i < r)
+//   Aq[r][i] =        sum_c q_rc k_ic e^{b_rc - b_ic}      (i <= r)
+//   T        = (I + A)^{-1}                               (forward substitution)
+//   u        = T (beta (V - (K e^{b}) S))                 (= U - W S of eq. 8-10)
+//   O        = scale ((Q e^{b}) S + Aq u)
+//   S       <- Diag(e^{b_end}) S + (K e^{b_end - b})^T u
+// Every exponent used is a difference b_r - b_i with i <= r, so it is <= 0:
+// nothing overflows however strong the decay.  The tail chunk of a sequence
+// is padded with k = q = v = 0, beta = 0, log alpha = 0, which leaves the
+// state and the valid rows unchanged.
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace la {
+namespace {
+
+constexpr int kC = 64;    // tokens per chunk
+constexpr int kDVS = 32;  // dv columns per CTA
+constexpr int kNT = 256;  // threads per CTA
+
+struct SimtParams {
+    const void *q, *k, *v, *beta_logits, *gate_logits;
+    void *o;
+    const int32_t *cu_seqlens;
+    int H, dv;
+    float scale;
+    unsigned flags;
+    const float *init_S, *init_z;
+    float *final_S, *final_z;
+};
+
+template <int DK>
+constexpr size_t delta_smem_floats() {
+    return 3 * (size_t)kC * (DK + 1) + 2 * (size_t)kC * (kDVS + 1) + 2 * (size_t)kC * (kC + 1) +
+           (size_t)DK * (kDVS + 1) + kC + DK;
+}
+
+template <typename IO, int DK>
+__global__ void __launch_bounds__(kNT) delta_chunk_simt_kernel(SimtParams p) {
+    constexpr int C = kC, DVS = kDVS, NT = kNT;
+    constexpr int LDK = DK + 1, LDV = DVS + 1, LDC = C + 1;
+    extern __shared__ float smem[];
+    float *sK = smem;              // [C][LDK]  k (prepared) -> K e^{b_end - b}
+    float *sQ = sK + C * LDK;      // [C][LDK]  q (prepared) -> Q e^{b}
+    float *sB = sQ + C * LDK;      // [C][LDK]  b = cumsum log alpha -> K e^{b}
+    float *sV = sB + C * LDK;      // [C][LDV]  v -> beta (v - K e^{b} S)
+    float *sU = sV + C * LDV;      // [C][LDV]  u
+    float *sA = sU + C * LDV;      // [C][LDC]  A -> T
+    float *sAq = sA + C * LDC;     // [C][LDC]  Aq
+    float *sS = sAq + C * LDC;     // [DK][LDV] state slice
+    float *sBeta = sS + DK * LDV;  // [C]
+    float *sGend = sBeta + C;      // [DK]      b_end, then e^{b_end}
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n = blockIdx.z, h = blockIdx.y, j0 = blockIdx.x * DVS;
+    const int H = p.H, dv = p.dv;
+    const bool gated = p.gate_logits != nullptr;
+    const bool silu = (p.flags & kSiluQK) != 0;
+    const IO *Q = static_cast<const IO *>(p.q), *K = static_cast<const IO *>(p.k);
+    const IO *V = static_cast<const IO *>(p.v);
+    const IO *BL = static_cast<const IO *>(p.beta_logits);
+    const IO *GL = static_cast<const IO *>(p.gate_logits);
+    IO *O = static_cast<IO *>(p.o);
+    const int t_begin = p.cu_seqlens[n], t_end = p.cu_seqlens[n + 1];
+    const int64_t sbase = ((int64_t)n * H + h) * DK * dv + j0;
+
+    for (int e = tid; e < DK * DVS; e += NT) {
+        const int c = e / DVS, j = e % DVS;
+        sS[c * LDV + j] = p.init_S ? p.init_S[sbase + (int64_t)c * dv + j] : 0.0f;
+    }
+
+    for (int cs = t_begin; cs < t_end; cs += C) {
+        const int len = min(C, t_end - cs);
+        __syncthreads();
+        // ---- load the chunk (padded rows are zero; log alpha = 0 there)
+        for (int e = tid; e < C * DK; e += NT) {
+            const int r = e / DK, c = e % DK;
+            const bool ok = r < len;
+            const int64_t g = ((int64_t)(cs + r) * H + h) * DK + c;
+            sK[r * LDK + c] = ok ? to_f32(K[g]) : 0.0f;
+            sQ[r * LDK + c] = ok ? to_f32(Q[g]) : 0.0f;
+            if (gated) sB[r * LDK + c] = ok ? log_decay_f(to_f32(GL[g])) : 0.0f;
+        }
+        for (int e = tid; e < C * DVS; e += NT) {
+            const int r = e / DVS, j = e % DVS;
+            sV[r * LDV + j] = r < len ? to_f32(V[((int64_t)(cs + r) * H + h) * dv + j0 + j]) : 0.0f;
+        }
+        if (tid < C) sBeta[tid] = tid < len ? sigmoid_f(to_f32(BL[(int64_t)(cs + tid) * H + h])) : 0.0f;
+        __syncthreads();
+        // ---- prologue: silu, L2 norms (one warp per row), decay cumsum
+        for (int r = warp; r < C; r += NT / 32) {
+            float sk = 0.0f, sq = 0.0f;
+            for (int c = lane; c < DK; c += 32) {
+                float kv = sK[r * LDK + c], qv = sQ[r * LDK + c];
+                if (silu) { kv = silu_f(kv); qv = silu_f(qv); sK[r * LDK + c] = kv; sQ[r * LDK + c] = qv; }
+                sk += kv * kv;
+                sq += qv * qv;
+            }
+            sk = warp_sum(sk);
+            sq = warp_sum(sq);
+            const float ik = (p.flags & kL2NormK) ? 1.0f / fmaxf(sqrtf(sk), 1e-12f) : 1.0f;
+            const float iq = (p.flags & kL2NormQ) ? 1.0f / fmaxf(sqrtf(sq), 1e-12f) : 1.0f;
+            for (int c = lane; c < DK; c += 32) { sK[r * LDK + c] *= ik; sQ[r * LDK + c] *= iq; }
+        }
+        if (gated) {
+            for (int c = tid; c < DK; c += NT) {
+                float acc = 0.0f;
+                for (int r = 0; r < C; ++r) { acc += sB[r * LDK + c]; sB[r * LDK + c] = acc; }
+                sGend[c] = acc;
+            }
+        }
+        __syncthreads();
+        // ---- A (strict, beta-scaled rows) and Aq (inclusive)
+        for (int e = tid; e < C * C; e += NT) {
+            const int r = e / C, i = e % C;
+            float akk = 0.0f, aqk = 0.0f;
+            if (i <= r) {
+                const float *kr = sK + r * LDK, *ki = sK + i * LDK, *qr = sQ + r * LDK;
+                if (gated) {
+                    const float *br = sB + r * LDK, *bi = sB + i * LDK;
+                    for (int c = 0; c < DK; ++c) {
+                        const float f = ki[c] * expf(br[c] - bi[c]);
+                        akk += kr[c] * f;
+                        aqk += qr[c] * f;
+                    }
+                } else {
+                    for (int c = 0; c < DK; ++c) { akk += kr[c] * ki[c]; aqk += qr[c] * ki[c]; }
+                }
+            }
+            sA[r * LDC + i] = i < r ? sBeta[r] * akk : 0.0f;
+            sAq[r * LDC + i] = aqk;
+        }
+        __syncthreads();
+        // ---- T = (I + A)^{-1}: T[i][j] = -(A[i][j] + sum_{j<m<i} A[i][m] T[m][j])
+        for (int i = 1; i < C; ++i) {
+            float tv = 0.0f;
+            if (tid < i) {
+                float acc = sA[i * LDC + tid];
+                for (int m = tid + 1; m < i; ++m) acc += sA[i * LDC + m] * sA[m * LDC + tid];
+                tv = -acc;
+            }
+            __syncthreads();
+            if (tid < i) sA[i * LDC + tid] = tv;
+            __syncthreads();
+        }
+        if (tid < C) sA[tid * LDC + tid] = 1.0f;
+        // ---- decay factors: Q e^{b}, K e^{b} (into sB), K e^{b_end - b}
+        if (gated) {
+            for (int e = tid; e < C * DK; e += NT) {
+                const int r = e / DK, c = e % DK;
+                const float b = sB[r * LDK + c], kk = sK[r * LDK + c];
+                sQ[r * LDK + c] *= expf(b);
+                sB[r * LDK + c] = kk * expf(b);
+                sK[r * LDK + c] = kk * expf(sGend[c] - b);
+            }
+        }
+        __syncthreads();
+        if (gated && tid < DK) sGend[tid] = expf(sGend[tid]);
+        const float *sKg = gated ? sB : sK;
+        // ---- R = beta (V - (K e^{b}) S)
+        for (int e = tid; e < C * DVS; e += NT) {
+            const int r = e / DVS, j = e % DVS;
+            float acc = 0.0f;
+            for (int c = 0; c < DK; ++c) acc += sKg[r * LDK + c] * sS[c * LDV + j];
+            sV[r * LDV + j] = sBeta[r] * (sV[r * LDV + j] - acc);
+        }
+        __syncthreads();
+        // ---- u = T R
+        for (int e = tid; e < C * DVS; e += NT) {
+            const int r = e / DVS, j = e % DVS;
+            float acc = 0.0f;
+            for (int i = 0; i <= r; ++i) acc += sA[r * LDC + i] * sV[i * LDV + j];
+            sU[r * LDV + j] = acc;
+        }
+        __syncthreads();
+        // ---- O = scale ((Q e^{b}) S + Aq u)
+        for (int e = tid; e < C * DVS; e += NT) {
+            const int r = e / DVS, j = e % DVS;
+            if (r < len) {
+                float acc = 0.0f;
+                for (int c = 0; c < DK; ++c) acc += sQ[r * LDK + c] * sS[c * LDV + j];
+                for (int i = 0; i <= r; ++i) acc += sAq[r * LDC + i] * sU[i * LDV + j];
+                O[((int64_t)(cs + r) * H + h) * dv + j0 + j] = from_f32<IO>(p.scale * acc);
+            }
+        }
+        __syncthreads();
+        // ---- S <- Diag(e^{b_end}) S + (K e^{b_end - b})^T u
+        for (int e = tid; e < DK * DVS; e += NT) {
+            const int c = e / DVS, j = e % DVS;
+            float acc = 0.0f;
+            for (int i = 0; i < C; ++i) acc += sK[i * LDK + c] * sU[i * LDV + j];
+            const float g = gated ? sGend[c] : 1.0f;
+            sS[c * LDV + j] = g * sS[c * LDV + j] + acc;
+        }
+    }
+    __syncthreads();
+    if (p.final_S) {
+        for (int e = tid; e < DK * DVS; e += NT) {
+            const int c = e / DVS, j = e % DVS;
+            p.final_S[sbase + (int64_t)c * dv + j] = sS[c * LDV + j];
+        }
+    }
+}
+
+template <int DK>
+constexpr size_t linear_smem_floats() {
+    return 2 * (size_t)kC * (DK + 1) + (size_t)kC * (kDVS + 1) + (size_t)kC * (kC + 1) +
+           (size_t)DK * (kDVS + 1) + DK + kC;
+}
+
+// ELU+1 linear attention ("From GPT-2 to Kimi K3, explained", section Linear
+// attention, chunked as in the next section):
+//   A = tril(phi(Q) phi(K)^T)                           (inclusive)
+//   O = (phi(Q) S + A V) / (phi(Q) z + A 1)
+//   S <- S + phi(K)^T V,   z <- z + sum_i phi(k_i)
+template <typename IO, int DK>
+__global__ void __launch_bounds__(kNT) linear_chunk_simt_kernel(SimtParams p) {
+    constexpr int C = kC, DVS = kDVS, NT = kNT;
+    constexpr int LDK = DK + 1, LDV = DVS + 1, LDC = C + 1;
+    extern __shared__ float smem[];
+    float *sK = smem;              // [C][LDK] phi(k)
+    float *sQ = sK + C * LDK;      // [C][LDK] phi(q)
+    float *sV = sQ + C * LDK;      // [C][LDV]
+    float *sA = sV + C * LDV;      // [C][LDC]
+    float *sS = sA + C * LDC;      // [DK][LDV]
+    float *sZ = sS + DK * LDV;     // [DK]
+    float *sDen = sZ + DK;         // [C]
+
+    const int tid = threadIdx.x;
+    const int n = blockIdx.z, h = blockIdx.y, j0 = blockIdx.x * DVS;
+    const int H = p.H, dv = p.dv;
+    const IO *Q = static_cast<const IO *>(p.q), *K = static_cast<const IO *>(p.k);
+    const IO *V = static_cast<const IO *>(p.v);
+    IO *O = static_cast<IO *>(p.o);
+    const int t_begin = p.cu_seqlens[n], t_end = p.cu_seqlens[n + 1];
+    const int64_t sbase = ((int64_t)n * H + h) * DK * dv + j0;
+    const int64_t zbase = ((int64_t)n * H + h) * DK;
+
+    for (int e = tid; e < DK * DVS; e += NT) {
+        const int c = e / DVS, j = e % DVS;
+        sS[c * LDV + j] = p.init_S ? p.init_S[sbase + (int64_t)c * dv + j] : 0.0f;
+    }
+    for (int c = tid; c < DK; c += NT) sZ[c] = p.init_z ? p.init_z[zbase + c] : 0.0f;
+
+    for (int cs = t_begin; cs < t_end; cs += C) {
+        const int len = min(C, t_end - cs);
+        __syncthreads();
+        for (int e = tid; e < C * DK; e += NT) {
+            const int r = e / DK, c = e % DK;
+            const bool ok = r < len;
+            const int64_t g = ((int64_t)(cs + r) * H + h) * DK + c;
+            sK[r * LDK + c] = ok ? elu1_f(to_f32(K[g])) : 0.0f;
+            sQ[r * LDK + c] = ok ? elu1_f(to_f32(Q[g])) : 0.0f;
+        }
+        for (int e = tid; e < C * DVS; e += NT) {
+            const int r = e / DVS, j = e % DVS;
+            sV[r * LDV + j] = r < len ? to_f32(V[((int64_t)(cs + r) * H + h) * dv + j0 + j]) : 0.0f;
+        }
+        __syncthreads();
+        for (int e = tid; e < C * C; e += NT) {
+            const int r = e / C, i = e % C;
+            float acc = 0.0f;
+            if (i <= r)
+                for (int c = 0; c < DK; ++c) acc += sQ[r * LDK + c] * sK[i * LDK + c];
+            sA[r * LDC + i] = acc;
+        }
+        __syncthreads();
+        if (tid < C) {
+            float d = 0.0f;
+            for (int c = 0; c < DK; ++c) d += sQ[tid * LDK + c] * sZ[c];
+            for (int i = 0; i <= tid; ++i) d += sA[tid * LDC + i];
+            sDen[tid] = d;
+        }
+        __syncthreads();
+        for (int e = tid; e < C * DVS; e += NT) {
+            const int r = e / DVS, j = e % DVS;
+            if (r < len) {
+                float acc = 0.0f;
+                for (int c = 0; c < DK; ++c) acc += sQ[r * LDK + c] * sS[c * LDV + j];
+                for (int i = 0; i <= r; ++i) acc += sA[r * LDC + i] * sV[i * LDV + j];
+                O[((int64_t)(cs + r) * H + h) * dv + j0 + j] = from_f32<IO>(acc / sDen[r]);
+            }
+        }
+        __syncthreads();
+        for (int e = tid; e < DK * DVS; e += NT) {
+            const int c = e / DVS, j = e % DVS;
+            float acc = 0.0f;
+            for (int i = 0; i < C; ++i) acc += sK[i * LDK + c] * sV[i * LDV + j];
+            sS[c * LDV + j] += acc;
+        }
+        for (int c = tid; c < DK; c += NT) {
+            float acc = 0.0f;
+            for (int i = 0; i < C; ++i) acc += sK[i * LDK + c];
+            sZ[c] += acc;
+        }
+    }
+    __syncthreads();
+    if (p.final_S)
+        for (int e = tid; e < DK * DVS; e += NT) {
+            const int c = e / DVS, j = e % DVS;
+            p.final_S[sbase + (int64_t)c * dv + j] = sS[c * LDV + j];
+        }
+    if (p.final_z && blockIdx.x == 0)
+        for (int c = tid; c < DK; c += NT) p.final_z[zbase + c] = sZ[c];
+}
+
+SimtParams to_params(const PrefillArgs &a) {
+    return SimtParams{a.q, a.k, a.v, a.beta_logits, a.gate_logits, a.o, a.cu_seqlens, a.H, a.dv,
+                      a.scale, a.flags, a.init_S, a.init_z, a.final_S, a.final_z};
+}
+
+template <typename Kern>
+cudaError_t launch_kernel(Kern kern, size_t smem, const PrefillArgs &a, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.dv / kDVS, a.H, a.N);
+    kern<<<grid, kNT, smem, s>>>(to_params(a));
+    return cudaGetLastError();
+}
+
+template <typename IO>
+cudaError_t delta_dispatch(const PrefillArgs &a, cudaStream_t s) {
+    if (a.dk == 128)
+        return launch_kernel(delta_chunk_simt_kernel<IO, 128>, delta_smem_floats<128>() * 4, a, s);
+    return launch_kernel(delta_chunk_simt_kernel<IO, 64>, delta_smem_floats<64>() * 4, a, s);
+}
+
+template <typename IO>
+cudaError_t linear_dispatch(const PrefillArgs &a, cudaStream_t s) {
+    if (a.dk == 128)
+        return launch_kernel(linear_chunk_simt_kernel<IO, 128>, linear_smem_floats<128>() * 4, a, s);
+    return launch_kernel(linear_chunk_simt_kernel<IO, 64>, linear_smem_floats<64>() * 4, a, s);
+}
+
+}  // namespace
+
+cudaError_t launch_delta_simt(const PrefillArgs &a, cudaStream_t s) {
+    return a.bf16 ? delta_dispatch<__nv_bfloat16>(a, s) : delta_dispatch<float>(a, s);
+}
+
+cudaError_t launch_linear_simt(const PrefillArgs &a, cudaStream_t s) {
+    return a.bf16 ? linear_dispatch<__nv_bfloat16>(a, s) : linear_dispatch<float>(a, s);
+}
+
+}  // namespace la

@@ -1,0 +1,135 @@
+/*
+ * linattn.h -- C ABI of the GB300 (sm_103a) causal linear-attention library.
+ *
+ * The operations follow the web page "From GPT-2 to Kimi K3, explained"
+ * (sections Linear attention; DeltaNet (Fast Weight Programmers);
+ * DeltaNet (Parallelizing Linear Transformers with Delta Rule); Gated
+ * DeltaNet; KDA / Kimi Linear).  Each head keeps a fixed dk x dv fp32 state
+ * S instead of a growing KV cache.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - State layout: row convention of the page's listings, S in R^{dk x dv},
+ *   read o = S^T q, write S += k u^T.  States are fp32, row-major,
+ *   [N][H][dk][dv] (the column form S_t q_t of the chunkwise section is its
+ *   transpose; outputs are identical).
+ * - Token tensors are packed, all sequences back to back:
+ *   q, k [ntok][H][dk]; v, o [ntok][H][dv]; beta_logits [ntok][H];
+ *   gate_logits [ntok][H][dk].  All are dense and contiguous, in the I/O
+ *   dtype `io` (LA_F32 or LA_BF16); states are always fp32.
+ * - cu_seqlens: int32 DEVICE array of N+1 non-decreasing offsets into the
+ *   token dimension; sequence n owns tokens [cu_seqlens[n], cu_seqlens[n+1]).
+ *   An equal-length batch of B sequences of T tokens is {0, T, 2T, ..., BT}.
+ *   cu_seqlens_host (nullable) is a HOST copy of the same array; when given,
+ *   it is validated before any launch.
+ * - Supported head sizes: dk, dv in {64, 128}.  N >= 1, H >= 1.
+ * - Every pointer is a device pointer unless stated otherwise.  The caller
+ *   owns every buffer; the library allocates, frees and synchronises nothing
+ *   (except la_check_device, which synchronises the given stream).  Outputs
+ *   must not alias inputs; final states may alias the matching initial state
+ *   only where stated.
+ * - stream: a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream).  All work is enqueued on it; calls return once enqueued.
+ * - Errors: every call returns an la_status.  Argument checks run on the
+ *   host before any launch, and a rejected call launches nothing.  A launch
+ *   failure returns LA_ERR_CUDA.  No C++ exception crosses this boundary.
+ */
+#ifndef LINATTN_H
+#define LINATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum la_status {
+    LA_OK = 0,
+    LA_ERR_INVALID_ARG = 1, /* null pointer, bad size, non-monotone cu_seqlens_host, bad flag */
+    LA_ERR_UNSUPPORTED = 2, /* valid request this build has no kernel for (e.g. dk = 96)     */
+    LA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed                            */
+    LA_ERR_TIMEOUT = 4      /* a bounded in-kernel wait expired (reported by la_check_device)  */
+} la_status;
+
+typedef enum la_dtype { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
+
+/* Prologue options (`flags`) for the delta-rule calls.
+ * LA_L2NORM_K: k <- k / max(||k||_2, 1e-12) per token and head.
+ * LA_L2NORM_Q: the same for q.
+ * LA_SILU_QK : q, k <- silu(q), silu(k), applied before the normalisation
+ *              (the page's DeltaNet layer uses normalize(silu(.))). */
+#define LA_L2NORM_K 1u
+#define LA_L2NORM_Q 2u
+#define LA_SILU_QK 4u
+
+/* Causal ELU+1 linear attention, chunkwise-parallel prefill.
+ * Defined in section Linear attention (the forward() that replaces the KV
+ * cache) and its chunked form in section DeltaNet (Parallelizing Linear
+ * Transformers with Delta Rule):
+ *   phi(x) = elu(x) + 1 on q and k separately;
+ *   S_t = S_{t-1} + phi(k_t) v_t^T,  z_t = z_{t-1} + phi(k_t),
+ *   o_t = S_t^T phi(q_t) / (z_t^T phi(q_t)).
+ * init_S [N][H][dk][dv], init_z [N][H][dk]: nullable (NULL = zero state).
+ * final_S, final_z: nullable outputs, same shapes; final_S may equal init_S
+ * and final_z may equal init_z (in-place continuation). */
+la_status la_prefill_linear(const void *q, const void *k, const void *v, void *o, la_dtype io,
+                            const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int N,
+                            int H, int dk, int dv, const float *init_S, const float *init_z,
+                            float *final_S, float *final_z, void *stream);
+
+/* (Gated) delta rule, chunkwise-parallel prefill.
+ * Defined in sections DeltaNet (Fast Weight Programmers) (the step), DeltaNet
+ * (Parallelizing Linear Transformers with Delta Rule) (the Householder
+ * reparametrisation and the chunkwise WY/UT algorithm, eq. 8-10), Gated
+ * DeltaNet (decay alpha, cumulative decay) and KDA / Kimi Linear (one decay
+ * per key channel).  Per sequence and head, with S' = Diag(alpha_t) S_{t-1}:
+ *   u_t = beta_t (v_t - S'^T k_t),  S_t = S' + k_t u_t^T,  o_t = scale S_t^T q_t
+ * where beta_t = sigmoid(beta_logits[t][h]) and
+ * alpha_t[c] = exp(-softplus(gate_logits[t][h][c])).
+ * gate_logits: nullable; NULL means alpha = 1 (plain DeltaNet).
+ * flags: LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK (see above).
+ * chunk: tokens per chunk; 64 is the supported value.
+ * scale: output scale (the page's delta-rule listings use 1.0).
+ * init_S: nullable [N][H][dk][dv]; final_S: nullable, may equal init_S.
+ * workspace / workspace_bytes: scratch of at least
+ * la_prefill_delta_workspace_size(...) bytes, 256-byte aligned; may be NULL
+ * when that size is 0. */
+la_status la_prefill_delta(const void *q, const void *k, const void *v, const void *beta_logits,
+                           const void *gate_logits, void *o, la_dtype io,
+                           const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int N,
+                           int H, int dk, int dv, int chunk, float scale, unsigned flags,
+                           const float *init_S, float *final_S, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/* Scratch bytes la_prefill_delta needs for these sizes (0 if none).
+ * ntok = total packed tokens. */
+size_t la_prefill_delta_workspace_size(int N, int ntok, int H, int dk, int dv, int chunk,
+                                       la_dtype io);
+
+/* One recurrent decode step: one new token for each of N sequences, state
+ * updated IN PLACE (sections DeltaNet (Fast Weight Programmers) and Gated
+ * DeltaNet: forward(x, cache) with t = 1; KDA / Kimi Linear for the
+ * per-channel decay).  Same arithmetic as la_prefill_delta with one token:
+ *   S' = Diag(alpha) S;  u = beta (v - S'^T k);  S <- S' + k u^T;
+ *   o = scale S^T q.
+ * q, k [N][H][dk]; v, o [N][H][dv]; beta_logits [N][H];
+ * gate_logits [N][H][dk] or NULL (alpha = 1); state [N][H][dk][dv] fp32,
+ * read and rewritten once per call.  state must not alias any other buffer. */
+la_status la_decode_step(const void *q, const void *k, const void *v, const void *beta_logits,
+                         const void *gate_logits, void *o, la_dtype io, int N, int H, int dk,
+                         int dv, float scale, unsigned flags, float *state, void *stream);
+
+/* Synchronises `stream`, then reports (and clears) any error raised on the
+ * current device since the previous check: LA_ERR_TIMEOUT if a bounded
+ * in-kernel wait gave up, LA_ERR_CUDA for a CUDA error, else LA_OK. */
+la_status la_check_device(void *stream);
+
+/* Static, human-readable name of a status code. */
+const char *la_status_string(la_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LINATTN_H */

@@ -1,0 +1,109 @@
+"""Host-only checks of the C ABI: the library builds for sm_103a, loads, exports
+every function that include/linattn.h declares, and rejects bad arguments on
+the host before any launch (these calls never reach the GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import delta_rule_recurrent_chunkwise_gb300 as la
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    la.build()
+    return la.library()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"^\w[\w\s\*]*?\b(la_\w+)\s*\(", text, flags=re.M))
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("la_prefill_linear", "la_prefill_delta", "la_decode_step"):
+        assert required in names
+    assert set(la.EXPORTED) <= names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert la.la_status_string(la.LA_OK) == "LA_OK"
+    for s in (1, 2, 3, 4):
+        assert la.la_status_string(s).startswith("LA_ERR_")
+    assert la.la_status_string(99) == "LA_ERR_UNKNOWN"
+
+
+FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: every call below is rejected first
+
+
+def prefill_delta(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, bl=FAKE, gl=None, o=FAKE, io=la.LA_BF16, cu=FAKE,
+             cuh=None, N=2, H=4, dk=64, dv=64, chunk=64, scale=1.0, flags=la.LA_L2NORM_K,
+             iS=None, fS=None, ws=None, wsb=0, stream=None)
+    a.update(kw)
+    return lib.la_prefill_delta(a["q"], a["k"], a["v"], a["bl"], a["gl"], a["o"], a["io"],
+                                a["cu"], a["cuh"], a["N"], a["H"], a["dk"], a["dv"], a["chunk"],
+                                a["scale"], a["flags"], a["iS"], a["fS"], a["ws"], a["wsb"],
+                                a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), la.LA_ERR_INVALID_ARG),
+    (dict(bl=None), la.LA_ERR_INVALID_ARG),
+    (dict(cu=None), la.LA_ERR_INVALID_ARG),
+    (dict(N=0), la.LA_ERR_INVALID_ARG),
+    (dict(H=-1), la.LA_ERR_INVALID_ARG),
+    (dict(io=7), la.LA_ERR_INVALID_ARG),
+    (dict(flags=64), la.LA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), la.LA_ERR_INVALID_ARG),
+    (dict(dk=96), la.LA_ERR_UNSUPPORTED),
+    (dict(dv=32), la.LA_ERR_UNSUPPORTED),
+    (dict(chunk=128), la.LA_ERR_UNSUPPORTED),
+    (dict(chunk=0), la.LA_ERR_INVALID_ARG),
+])
+def test_prefill_delta_rejects_bad_arguments(lib, kw, code):
+    assert prefill_delta(lib, **kw) == code
+
+
+def test_non_monotone_host_cu_seqlens_rejected(lib):
+    bad = (ctypes.c_int32 * 3)(0, 10, 5)
+    assert prefill_delta(lib, cuh=bad) == la.LA_ERR_INVALID_ARG
+    neg = (ctypes.c_int32 * 3)(-1, 10, 20)
+    assert prefill_delta(lib, cuh=neg) == la.LA_ERR_INVALID_ARG
+    assert lib.la_prefill_linear(FAKE, FAKE, FAKE, FAKE, la.LA_F32, FAKE, bad, 2, 1, 64, 64,
+                                 None, None, None, None, None) == la.LA_ERR_INVALID_ARG
+
+
+def test_decode_and_linear_reject_bad_arguments(lib):
+    d = lib.la_decode_step
+    assert d(FAKE, FAKE, FAKE, FAKE, None, FAKE, la.LA_BF16, 4, 2, 128, 128, 1.0, 1, None,
+             None) == la.LA_ERR_INVALID_ARG          # no state
+    assert d(FAKE, FAKE, FAKE, FAKE, None, FAKE, la.LA_BF16, 4, 2, 100, 128, 1.0, 1, FAKE,
+             None) == la.LA_ERR_UNSUPPORTED
+    assert d(FAKE, FAKE, FAKE, FAKE, None, FAKE, la.LA_BF16, 0, 2, 128, 128, 1.0, 1, FAKE,
+             None) == la.LA_ERR_INVALID_ARG
+    assert lib.la_prefill_linear(None, FAKE, FAKE, FAKE, la.LA_F32, FAKE, None, 1, 1, 64, 64,
+                                 None, None, None, None, None) == la.LA_ERR_INVALID_ARG
+    assert lib.la_prefill_linear(FAKE, FAKE, FAKE, FAKE, la.LA_F32, FAKE, None, 1, 1, 48, 64,
+                                 None, None, None, None, None) == la.LA_ERR_UNSUPPORTED
+
+
+def test_workspace_size_independent_of_sequence_length(lib):
+    """The recurrent state is fixed-size: no buffer the library asks for
+    grows with the number of tokens beyond per-chunk bookkeeping."""
+    a = la.la_prefill_delta_workspace_size(4, 1024, 32, 128, 128)
+    b = la.la_prefill_delta_workspace_size(4, 1024 * 64, 32, 128, 128)
+    assert a == b
