@@ -330,12 +330,48 @@ def cpu_oracle_throughput(w: wl.Workload, target_s: float, nseq=None):
         oracle.delta(*args, cu, nthreads=threads)
         passes += 1
         el = time.perf_counter() - t0
-        if el >= target_s or passes >= 50:
+        if el >= target_s or passes >= 2000:
             break
     tokens = sum(lens) * passes
     return {"value": tokens / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": f"{len(lens)} of {len(w.lengths)} sequences x {w.H} heads x "
                       f"{lens[0]} tokens, {passes} pass(es), {el:.1f} s, fp64"}
+
+
+# ------------------------------------------------------------ profile cases
+
+def profile_case(args):
+    """Runs `warmup + steps` launches of one workload and nothing else, so an
+    ncu capture sees a known launch sequence.  Small cases keep inputs above
+    L2 size but a few hundred MB on the device at most."""
+    import delta_rule_recurrent_chunkwise_gb300 as la
+    la.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    name = args.profile_case
+    if name in ("decode", "decode_small"):
+        w = wl.workload("decode")
+        n_seq = w.n_seq if name == "decode" else 128
+        d = wl.decode_inputs(n_seq, w.H, w.dk, w.dv, 1, w.dtype, seed=0)
+        t = {n: d[n][0].to(dev) for n in ("q", "k", "v", "beta_logits", "gate_logits")}
+        st = d["state"].to(dev)
+        o = torch.empty((n_seq, w.H, w.dv), dtype=w.dtype, device=dev)
+        fn = lambda: la.la_decode_step(t["q"], t["k"], t["v"], t["beta_logits"],
+                                       t["gate_logits"], o, st, stream=stream)
+    else:
+        if name == "gated_small":
+            w = wl.Workload("gated_small", "prefill_delta", 32, 128, 128, torch.bfloat16,
+                            gated=True, lengths=(4096,) * 2)
+        else:
+            w = wl.workload(name, seed=0)
+        p = Prefill(la, w, seed=0, dev=dev, final_states=(name == "varlen_prefill"))
+        fn = lambda: p.step(stream)
+    for _ in range(args.warmup + args.steps):
+        fn()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": name, "launches": args.warmup + args.steps,
+                      "status": la.la_check_device()}))
 
 
 # --------------------------------------------------------------------- main
@@ -348,7 +384,12 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile-case", default=None,
+                    help="run one workload only (for ncu): gpt2_prefill, gated_prefill, "
+                         "varlen_prefill, decode, decode_small, gated_small")
     args = ap.parse_args()
+    if args.profile_case:
+        return profile_case(args)
     args.warmup = max(3, args.warmup)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -44,10 +44,10 @@ def library():
         lib = ctypes.CDLL(LIB_PATH)
         vp, ip, fp = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         u, sz = ctypes.c_uint, ctypes.c_size_t
-        lib.la_prefill_linear.argtypes = [vp, vp, vp, vp, ip, vp, vp, ip, ip, ip, ip,
+        lib.la_prefill_linear.argtypes = [vp, vp, vp, vp, ip, vp, vp, ip, ip, ip, ip, ip,
                                           vp, vp, vp, vp, vp]
         lib.la_prefill_delta.argtypes = [vp, vp, vp, vp, vp, vp, ip, vp, vp, ip, ip, ip, ip, ip,
-                                         fp, u, vp, vp, vp, sz, vp]
+                                         ip, fp, u, vp, vp, vp, sz, vp]
         lib.la_prefill_delta_workspace_size.argtypes = [ip, ip, ip, ip, ip, ip, ip]
         lib.la_prefill_delta_workspace_size.restype = sz
         lib.la_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, ip, ip, ip, ip, ip, fp, u, vp, vp]
@@ -121,7 +121,7 @@ def la_prefill_linear(q, k, v, o, cu_seqlens, init_S=None, init_z=None, final_S=
     N = cu_seqlens.numel() - 1
     hold, hptr = _host_cu(cu_seqlens_host)
     rc = library().la_prefill_linear(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _io(q), _ptr(cu_seqlens),
-                                     hptr, N, H, dk, dv, _ptr(init_S), _ptr(init_z),
+                                     hptr, N, ntok, H, dk, dv, _ptr(init_S), _ptr(init_z),
                                      _ptr(final_S), _ptr(final_z), _stream(stream))
     if rc != LA_OK:
         raise LinAttnError(rc, "la_prefill_linear")
@@ -149,7 +149,7 @@ def la_prefill_delta(q, k, v, beta_logits, gate_logits, o, cu_seqlens, chunk=64,
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = library().la_prefill_delta(_ptr(q), _ptr(k), _ptr(v), _ptr(beta_logits),
                                     _ptr(gate_logits), _ptr(o), _io(q), _ptr(cu_seqlens), hptr,
-                                    N, H, dk, dv, int(chunk), float(scale), int(flags),
+                                    N, ntok, H, dk, dv, int(chunk), float(scale), int(flags),
                                     _ptr(init_S), _ptr(final_S), _ptr(workspace), ws_bytes,
                                     _stream(stream))
     if rc != LA_OK:

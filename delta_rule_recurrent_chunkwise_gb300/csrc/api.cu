@@ -14,9 +14,9 @@ bool head_size_ok(int d) { return d == 64 || d == 128; }
 
 bool dtype_ok(la_dtype io) { return io == LA_F32 || io == LA_BF16; }
 
-la_status check_cu_host(const int32_t *cu_host, int N) {
+la_status check_cu_host(const int32_t *cu_host, int N, int ntok) {
     if (!cu_host) return LA_OK;
-    if (cu_host[0] < 0) return LA_ERR_INVALID_ARG;
+    if (cu_host[0] < 0 || cu_host[N] > ntok) return LA_ERR_INVALID_ARG;
     for (int n = 0; n < N; ++n)
         if (cu_host[n + 1] < cu_host[n]) return LA_ERR_INVALID_ARG;
     return LA_OK;
@@ -41,14 +41,14 @@ const char *la_status_string(la_status s) {
 
 la_status la_prefill_linear(const void *q, const void *k, const void *v, void *o, la_dtype io,
                             const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int N,
-                            int H, int dk, int dv, const float *init_S, const float *init_z,
-                            float *final_S, float *final_z, void *stream) {
-    if (!q || !k || !v || !o || !cu_seqlens || N < 1 || H < 1 || !dtype_ok(io))
+                            int ntok, int H, int dk, int dv, const float *init_S,
+                            const float *init_z, float *final_S, float *final_z, void *stream) {
+    if (!q || !k || !v || !o || !cu_seqlens || N < 1 || ntok < 0 || H < 1 || !dtype_ok(io))
         return LA_ERR_INVALID_ARG;
     if (dk < 1 || dv < 1) return LA_ERR_INVALID_ARG;
     if (!head_size_ok(dk) || !head_size_ok(dv) || N > 65535 || H > 65535) return LA_ERR_UNSUPPORTED;
-    if (la_status st = check_cu_host(cu_seqlens_host, N)) return st;
-    la::PrefillArgs a{q, k, v, nullptr, nullptr, o, cu_seqlens, N, H, dk, dv, 1.0f, 0u,
+    if (la_status st = check_cu_host(cu_seqlens_host, N, ntok)) return st;
+    la::PrefillArgs a{q, k, v, nullptr, nullptr, o, cu_seqlens, N, ntok, H, dk, dv, 1.0f, 0u,
                       init_S, init_z, final_S, final_z, io == LA_BF16};
     return from_cuda(la::launch_linear_simt(a, static_cast<cudaStream_t>(stream)));
 }
@@ -62,11 +62,12 @@ size_t la_prefill_delta_workspace_size(int N, int ntok, int H, int dk, int dv, i
 la_status la_prefill_delta(const void *q, const void *k, const void *v, const void *beta_logits,
                            const void *gate_logits, void *o, la_dtype io,
                            const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int N,
-                           int H, int dk, int dv, int chunk, float scale, unsigned flags,
-                           const float *init_S, float *final_S, void *workspace,
+                           int ntok, int H, int dk, int dv, int chunk, float scale,
+                           unsigned flags, const float *init_S, float *final_S, void *workspace,
                            size_t workspace_bytes, void *stream) {
     (void)workspace;
-    if (!q || !k || !v || !beta_logits || !o || !cu_seqlens || N < 1 || H < 1 || !dtype_ok(io))
+    if (!q || !k || !v || !beta_logits || !o || !cu_seqlens || N < 1 || ntok < 0 || H < 1 ||
+        !dtype_ok(io))
         return LA_ERR_INVALID_ARG;
     if (dk < 1 || dv < 1 || chunk < 1 || !std::isfinite(scale)) return LA_ERR_INVALID_ARG;
     if (flags & ~(LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK)) return LA_ERR_INVALID_ARG;
@@ -74,10 +75,12 @@ la_status la_prefill_delta(const void *q, const void *k, const void *v, const vo
     if (N > 65535 || H > 65535) return LA_ERR_UNSUPPORTED;
     if (workspace_bytes < la_prefill_delta_workspace_size(N, 0, H, dk, dv, chunk, io))
         return LA_ERR_INVALID_ARG;
-    if (la_status st = check_cu_host(cu_seqlens_host, N)) return st;
-    la::PrefillArgs a{q, k, v, beta_logits, gate_logits, o, cu_seqlens, N, H, dk, dv, scale,
+    if (la_status st = check_cu_host(cu_seqlens_host, N, ntok)) return st;
+    la::PrefillArgs a{q, k, v, beta_logits, gate_logits, o, cu_seqlens, N, ntok, H, dk, dv, scale,
                       flags, init_S, nullptr, final_S, nullptr, io == LA_BF16};
-    return from_cuda(la::launch_delta_simt(a, static_cast<cudaStream_t>(stream)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (la::delta_tc_supported(a)) return from_cuda(la::launch_delta_tc(a, s));
+    return from_cuda(la::launch_delta_simt(a, s));
 }
 
 la_status la_decode_step(const void *q, const void *k, const void *v, const void *beta_logits,
@@ -95,8 +98,13 @@ la_status la_decode_step(const void *q, const void *k, const void *v, const void
 }
 
 la_status la_check_device(void *stream) {
-    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return LA_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
+    unsigned code = 0;
+    if (la::tc_take_error(s, &code) != cudaSuccess) return LA_ERR_CUDA;
+    if (code == 100u) return LA_ERR_INVALID_ARG;  // cu_seqlens outside [0, ntok]
+    if (code != 0u) return LA_ERR_TIMEOUT;
     return LA_OK;
 }
 

@@ -12,7 +12,7 @@ struct PrefillArgs {
     const void *q, *k, *v, *beta_logits, *gate_logits;
     void *o;
     const int32_t *cu_seqlens;
-    int N, H, dk, dv;
+    int N, ntok, H, dk, dv;
     float scale;
     unsigned flags;
     const float *init_S, *init_z;
@@ -33,6 +33,14 @@ struct DecodeArgs {
 // fp32 SIMT chunk kernels (any I/O dtype).
 cudaError_t launch_linear_simt(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_delta_simt(const PrefillArgs &a, cudaStream_t s);
+// tcgen05 tensor-core chunk kernel (bf16 I/O, dk == dv in {64, 128}).
+bool delta_tc_supported(const PrefillArgs &a);
+cudaError_t launch_delta_tc(const PrefillArgs &a, cudaStream_t s);
+// Device address of the library's error word on the current device (kernels
+// record the first failure there; la_check_device reads and clears it).
+unsigned *device_error_word();
+// Reads and clears the device error word (synchronises s).
+cudaError_t tc_take_error(cudaStream_t s, unsigned *code);
 // HBM-streaming decode step.
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
 

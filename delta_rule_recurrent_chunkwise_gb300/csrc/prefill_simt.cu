@@ -39,7 +39,8 @@ struct SimtParams {
     const void *q, *k, *v, *beta_logits, *gate_logits;
     void *o;
     const int32_t *cu_seqlens;
-    int H, dv;
+    unsigned *err;
+    int H, dv, ntok;
     float scale;
     unsigned flags;
     const float *init_S, *init_z;
@@ -78,7 +79,11 @@ __global__ void __launch_bounds__(kNT) delta_chunk_simt_kernel(SimtParams p) {
     const IO *BL = static_cast<const IO *>(p.beta_logits);
     const IO *GL = static_cast<const IO *>(p.gate_logits);
     IO *O = static_cast<IO *>(p.o);
-    const int t_begin = p.cu_seqlens[n], t_end = p.cu_seqlens[n + 1];
+    int t_begin = p.cu_seqlens[n], t_end = p.cu_seqlens[n + 1];
+    if (t_begin < 0 || t_end < t_begin || t_end > p.ntok) {
+        if (tid == 0 && p.err) atomicCAS(p.err, 0u, 100u);
+        t_begin = t_end = 0;
+    }
     const int64_t sbase = ((int64_t)n * H + h) * DK * dv + j0;
 
     for (int e = tid; e < DK * DVS; e += NT) {
@@ -249,7 +254,11 @@ __global__ void __launch_bounds__(kNT) linear_chunk_simt_kernel(SimtParams p) {
     const IO *Q = static_cast<const IO *>(p.q), *K = static_cast<const IO *>(p.k);
     const IO *V = static_cast<const IO *>(p.v);
     IO *O = static_cast<IO *>(p.o);
-    const int t_begin = p.cu_seqlens[n], t_end = p.cu_seqlens[n + 1];
+    int t_begin = p.cu_seqlens[n], t_end = p.cu_seqlens[n + 1];
+    if (t_begin < 0 || t_end < t_begin || t_end > p.ntok) {
+        if (tid == 0 && p.err) atomicCAS(p.err, 0u, 100u);
+        t_begin = t_end = 0;
+    }
     const int64_t sbase = ((int64_t)n * H + h) * DK * dv + j0;
     const int64_t zbase = ((int64_t)n * H + h) * DK;
 
@@ -322,8 +331,9 @@ __global__ void __launch_bounds__(kNT) linear_chunk_simt_kernel(SimtParams p) {
 }
 
 SimtParams to_params(const PrefillArgs &a) {
-    return SimtParams{a.q, a.k, a.v, a.beta_logits, a.gate_logits, a.o, a.cu_seqlens, a.H, a.dv,
-                      a.scale, a.flags, a.init_S, a.init_z, a.final_S, a.final_z};
+    return SimtParams{a.q, a.k, a.v, a.beta_logits, a.gate_logits, a.o, a.cu_seqlens,
+                      device_error_word(), a.H, a.dv, a.ntok, a.scale, a.flags, a.init_S,
+                      a.init_z, a.final_S, a.final_z};
 }
 
 template <typename Kern>

@@ -20,8 +20,12 @@
  * - cu_seqlens: int32 DEVICE array of N+1 non-decreasing offsets into the
  *   token dimension; sequence n owns tokens [cu_seqlens[n], cu_seqlens[n+1]).
  *   An equal-length batch of B sequences of T tokens is {0, T, 2T, ..., BT}.
+ *   ntok is the number of packed tokens the token tensors hold (their first
+ *   dimension); every cu_seqlens entry must lie in [0, ntok].
  *   cu_seqlens_host (nullable) is a HOST copy of the same array; when given,
- *   it is validated before any launch.
+ *   it is validated before any launch.  Without it, a device-side range
+ *   check skips offending sequences and la_check_device reports
+ *   LA_ERR_INVALID_ARG.
  * - Supported head sizes: dk, dv in {64, 128}.  N >= 1, H >= 1.
  * - Every pointer is a device pointer unless stated otherwise.  The caller
  *   owns every buffer; the library allocates, frees and synchronises nothing
@@ -75,8 +79,8 @@ typedef enum la_dtype { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
  * and final_z may equal init_z (in-place continuation). */
 la_status la_prefill_linear(const void *q, const void *k, const void *v, void *o, la_dtype io,
                             const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int N,
-                            int H, int dk, int dv, const float *init_S, const float *init_z,
-                            float *final_S, float *final_z, void *stream);
+                            int ntok, int H, int dk, int dv, const float *init_S,
+                            const float *init_z, float *final_S, float *final_z, void *stream);
 
 /* (Gated) delta rule, chunkwise-parallel prefill.
  * Defined in sections DeltaNet (Fast Weight Programmers) (the step), DeltaNet
@@ -98,8 +102,8 @@ la_status la_prefill_linear(const void *q, const void *k, const void *v, void *o
 la_status la_prefill_delta(const void *q, const void *k, const void *v, const void *beta_logits,
                            const void *gate_logits, void *o, la_dtype io,
                            const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int N,
-                           int H, int dk, int dv, int chunk, float scale, unsigned flags,
-                           const float *init_S, float *final_S, void *workspace,
+                           int ntok, int H, int dk, int dv, int chunk, float scale,
+                           unsigned flags, const float *init_S, float *final_S, void *workspace,
                            size_t workspace_bytes, void *stream);
 
 /* Scratch bytes la_prefill_delta needs for these sizes (0 if none).

@@ -51,11 +51,12 @@ FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: every call below is reject
 
 def prefill_delta(lib, **kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, bl=FAKE, gl=None, o=FAKE, io=la.LA_BF16, cu=FAKE,
-             cuh=None, N=2, H=4, dk=64, dv=64, chunk=64, scale=1.0, flags=la.LA_L2NORM_K,
-             iS=None, fS=None, ws=None, wsb=0, stream=None)
+             cuh=None, N=2, ntok=40, H=4, dk=64, dv=64, chunk=64, scale=1.0,
+             flags=la.LA_L2NORM_K, iS=None, fS=None, ws=None, wsb=0, stream=None)
     a.update(kw)
     return lib.la_prefill_delta(a["q"], a["k"], a["v"], a["bl"], a["gl"], a["o"], a["io"],
-                                a["cu"], a["cuh"], a["N"], a["H"], a["dk"], a["dv"], a["chunk"],
+                                a["cu"], a["cuh"], a["N"], a["ntok"], a["H"], a["dk"], a["dv"],
+                                a["chunk"],
                                 a["scale"], a["flags"], a["iS"], a["fS"], a["ws"], a["wsb"],
                                 a["stream"])
 
@@ -66,6 +67,7 @@ def prefill_delta(lib, **kw):
     (dict(cu=None), la.LA_ERR_INVALID_ARG),
     (dict(N=0), la.LA_ERR_INVALID_ARG),
     (dict(H=-1), la.LA_ERR_INVALID_ARG),
+    (dict(ntok=-5), la.LA_ERR_INVALID_ARG),
     (dict(io=7), la.LA_ERR_INVALID_ARG),
     (dict(flags=64), la.LA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), la.LA_ERR_INVALID_ARG),
@@ -83,7 +85,9 @@ def test_non_monotone_host_cu_seqlens_rejected(lib):
     assert prefill_delta(lib, cuh=bad) == la.LA_ERR_INVALID_ARG
     neg = (ctypes.c_int32 * 3)(-1, 10, 20)
     assert prefill_delta(lib, cuh=neg) == la.LA_ERR_INVALID_ARG
-    assert lib.la_prefill_linear(FAKE, FAKE, FAKE, FAKE, la.LA_F32, FAKE, bad, 2, 1, 64, 64,
+    past_end = (ctypes.c_int32 * 3)(0, 10, 41)   # beyond ntok = 40
+    assert prefill_delta(lib, cuh=past_end) == la.LA_ERR_INVALID_ARG
+    assert lib.la_prefill_linear(FAKE, FAKE, FAKE, FAKE, la.LA_F32, FAKE, bad, 2, 40, 1, 64, 64,
                                  None, None, None, None, None) == la.LA_ERR_INVALID_ARG
 
 
@@ -95,9 +99,9 @@ def test_decode_and_linear_reject_bad_arguments(lib):
              None) == la.LA_ERR_UNSUPPORTED
     assert d(FAKE, FAKE, FAKE, FAKE, None, FAKE, la.LA_BF16, 0, 2, 128, 128, 1.0, 1, FAKE,
              None) == la.LA_ERR_INVALID_ARG
-    assert lib.la_prefill_linear(None, FAKE, FAKE, FAKE, la.LA_F32, FAKE, None, 1, 1, 64, 64,
+    assert lib.la_prefill_linear(None, FAKE, FAKE, FAKE, la.LA_F32, FAKE, None, 1, 8, 1, 64, 64,
                                  None, None, None, None, None) == la.LA_ERR_INVALID_ARG
-    assert lib.la_prefill_linear(FAKE, FAKE, FAKE, FAKE, la.LA_F32, FAKE, None, 1, 1, 48, 64,
+    assert lib.la_prefill_linear(FAKE, FAKE, FAKE, FAKE, la.LA_F32, FAKE, None, 1, 8, 1, 48, 64,
                                  None, None, None, None, None) == la.LA_ERR_UNSUPPORTED
 
 
