@@ -163,6 +163,27 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+# ------------------------------------------------------------ multi-rank
+
+def max_over_ranks(x: float, dist, device) -> float:
+    """Max of a per-rank scalar over all ranks (the slowest rank's time)."""
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: int, world: int, slowest_ms: float) -> float:
+    """Whole-job units/s: every rank processes its own equal share (weak scaling)."""
+    return units_per_rank * world / (slowest_ms / 1e3)
+
+
+def rank_seed(rank: int) -> int:
+    """Each rank draws its own independent batch of the same shape."""
+    return rank
+
+
 # --------------------------------------------------------------- GPU timing
 
 class Prefill:
@@ -219,22 +240,16 @@ def run_ours(args, rank, world, dev, dist):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     barrier = (lambda: dist.barrier()) if dist is not None else None
 
-    def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    mor = lambda x: max_over_ranks(x, dist, dev)
 
     result = {}
     with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
         # ---- headline: GPT-2-shaped delta prefill
         w = wl.workload(HEADLINE)
-        pf = Prefill(la, w, seed=rank, dev=dev)
+        pf = Prefill(la, w, seed=rank_seed(rank), dev=dev)
         ms = time_steps(lambda: pf.step(stream), args.steps, args.warmup, flush, stream, barrier)
-        total_ms = max_over_ranks(sum(ms))
-        tokens = w.ntok * world * args.steps
-        value = tokens / (total_ms / 1e3)
+        total_ms = mor(sum(ms))
+        value = job_throughput(w.ntok * args.steps, world, total_ms)
         kern_ms = sum(ms) / len(ms)
         nbytes, flops = prefill_algo(w)
         achieved = nbytes / (kern_ms / 1e3) / 1e9
@@ -262,8 +277,8 @@ def run_ours(args, rank, world, dev, dist):
             o_host.copy_(pf.o, non_blocking=True)
 
         e2e_ms = time_steps(e2e_step, max(3, args.steps // 2), 2, None, stream, barrier)
-        e2e_total = max_over_ranks(sum(e2e_ms))
-        result["e2e"] = {"value": w.ntok * world * len(e2e_ms) / (e2e_total / 1e3),
+        e2e_total = mor(sum(e2e_ms))
+        result["e2e"] = {"value": job_throughput(w.ntok * len(e2e_ms), world, e2e_total),
                          "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
         del pf
 
@@ -271,7 +286,7 @@ def run_ours(args, rank, world, dev, dist):
             extra = {}
             # ---- decode: 64 consecutive steps on 256 x 32 states
             dw = wl.workload("decode")
-            d = wl.inputs_for(dw, seed=rank)
+            d = wl.inputs_for(dw, seed=rank_seed(rank))
             toks = {n: (None if d[n] is None else d[n].to(dev))
                     for n in ("q", "k", "v", "beta_logits", "gate_logits")}
             state = d["state"].to(dev)
@@ -284,7 +299,7 @@ def run_ours(args, rank, world, dev, dist):
                                       stream=stream)
 
             dms = time_steps(decode_64, max(2, args.steps // 4), 1, None, stream, barrier)
-            d_ms = max_over_ranks(sum(dms)) / len(dms)
+            d_ms = mor(sum(dms)) / len(dms)
             sb = decode_state_bytes(dw) * dw.steps
             gbs = sb / (d_ms / 1e3) / 1e9
             extra["decode"] = {"workload": "256 seq x 32 heads, dk=dv=128, fp32 state, 64 steps",
@@ -297,10 +312,10 @@ def run_ours(args, rank, world, dev, dist):
             for name in ("gated_prefill", "varlen_prefill"):
                 gw = wl.workload(name, seed=0)
                 fs = name == "varlen_prefill"
-                p = Prefill(la, gw, seed=rank, dev=dev, final_states=fs)
+                p = Prefill(la, gw, seed=rank_seed(rank), dev=dev, final_states=fs)
                 gms = time_steps(lambda: p.step(stream), max(3, args.steps // 4), 2, flush,
                                  stream, barrier)
-                g_ms = max_over_ranks(sum(gms)) / len(gms)
+                g_ms = mor(sum(gms)) / len(gms)
                 nb, fl = prefill_algo(gw, final_states=fs)
                 extra[name] = {"tokens_per_s": gw.ntok * world / (g_ms / 1e3), "ms": g_ms,
                                "hbm_frac": nb / (g_ms / 1e3) / 1e9 / pk["hbm_gbs"],

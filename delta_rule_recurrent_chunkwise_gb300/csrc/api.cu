@@ -91,7 +91,7 @@ la_status la_decode_step(const void *q, const void *k, const void *v, const void
     if (dk < 1 || dv < 1 || !std::isfinite(scale)) return LA_ERR_INVALID_ARG;
     if (flags & ~(LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK)) return LA_ERR_INVALID_ARG;
     if (!head_size_ok(dk) || !head_size_ok(dv)) return LA_ERR_UNSUPPORTED;
-    if ((int64_t)N * H > 0x7fffffffLL) return LA_ERR_UNSUPPORTED;
+    if ((int64_t)N * H * 2 > 0x7fffffffLL) return LA_ERR_UNSUPPORTED;
     la::DecodeArgs a{q, k, v, beta_logits, gate_logits, o, N, H, dk, dv, scale, flags, state,
                      io == LA_BF16};
     return from_cuda(la::launch_decode(a, static_cast<cudaStream_t>(stream)));

@@ -11,10 +11,13 @@
 // S'^T q, so the state is read once and written once: the step streams
 // 8 * dk * dv bytes of fp32 state per head and is bound by HBM bandwidth.
 //
-// Layout: one CTA of 256 threads per (sequence, head).  A thread owns a
-// float4 column group of `RPT` rows of S and keeps them in registers between
-// the read and the write.  All loads are issued before the prologue runs so
-// that every thread has its whole share of the state in flight at once.
+// Layout: the dv columns of S are independent, so each (sequence, head) is
+// split into SPLIT column slices, one CTA of 256 threads each.  A thread
+// owns a float4 column group of `RPT` rows of its slice and keeps them in
+// registers between the read and the write; all loads are issued before the
+// prologue runs so that each thread's whole share is in flight at once.
+// With 32 KB per CTA and ~60 registers per thread, four CTAs share an SM,
+// so one CTA's write phase overlaps the others' reads.
 
 #include "common.cuh"
 #include "launch.h"
@@ -31,28 +34,33 @@ struct DecodeParams {
     unsigned flags;
 };
 
+constexpr int kSplit = 2;  // column slices per (sequence, head)
+
 template <typename IO, int DK, int DV>
-__global__ void __launch_bounds__(256, 2) decode_step_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(256, 4) decode_step_kernel(DecodeParams p) {
     constexpr int NT = 256;
-    constexpr int C4 = DV / 4;          // float4 column groups per state row
+    constexpr int DVS = DV / kSplit;    // columns of this CTA's slice
+    constexpr int C4 = DVS / 4;         // float4 column groups per slice row
     constexpr int RPP = NT / C4;        // rows covered by one pass of the block
     constexpr int RPT = DK / RPP;       // rows held by each thread
+    constexpr int C4F = DV / 4;         // float4 groups per full state row
     static_assert(DK % RPP == 0, "shape");
 
-    __shared__ float sk[DK], sq[DK], sa[DK], sv[DV], su[DV];
-    __shared__ __align__(16) float red_k[RPP][DV];
-    __shared__ __align__(16) float red_q[RPP][DV];
+    __shared__ float sk[DK], sq[DK], sa[DK], sv[DVS], su[DVS];
+    __shared__ __align__(16) float red_k[RPP][DVS];
+    __shared__ __align__(16) float red_q[RPP][DVS];
     __shared__ float s_beta, s_qk;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t nh = blockIdx.x;
+    const int64_t nh = blockIdx.x / kSplit;
+    const int j0 = (blockIdx.x % kSplit) * DVS;   // first column of the slice
     const int col4 = tid % C4, row0 = tid / C4;
-    float4 *S4 = reinterpret_cast<float4 *>(p.state + nh * (int64_t)(DK * DV));
+    float4 *S4 = reinterpret_cast<float4 *>(p.state + nh * (int64_t)(DK * DV) + j0);
 
     // 1. put this thread's share of the state in flight (streaming loads).
     float4 s[RPT];
 #pragma unroll
-    for (int m = 0; m < RPT; ++m) s[m] = __ldcs(S4 + (row0 + m * RPP) * C4 + col4);
+    for (int m = 0; m < RPT; ++m) s[m] = __ldcs(S4 + (row0 + m * RPP) * C4F + col4);
 
     // 2. prologue: feature map / L2 norm of q and k, beta, per-channel decay.
     const IO *q = static_cast<const IO *>(p.q) + nh * DK;
@@ -68,7 +76,7 @@ __global__ void __launch_bounds__(256, 2) decode_step_kernel(DecodeParams p) {
                       ? decay_f(to_f32(static_cast<const IO *>(p.gate_logits)[nh * DK + tid]))
                       : 1.0f;
     }
-    if (tid < DV) sv[tid] = to_f32(v[tid]);
+    if (tid < DVS) sv[tid] = to_f32(v[j0 + tid]);
     __syncthreads();
     if (warp < 2) {
         float *x = warp == 0 ? sk : sq;
@@ -104,13 +112,13 @@ __global__ void __launch_bounds__(256, 2) decode_step_kernel(DecodeParams p) {
     __syncthreads();
 
     // 4. column totals, the delta u and the output.
-    if (tid < DV) {
+    if (tid < DVS) {
         float rk = 0.0f, rq = 0.0f;
 #pragma unroll
         for (int i = 0; i < RPP; ++i) { rk += red_k[i][tid]; rq += red_q[i][tid]; }
         const float u = s_beta * (sv[tid] - rk);
         su[tid] = u;
-        static_cast<IO *>(p.o)[nh * DV + tid] = from_f32<IO>(p.scale * (rq + s_qk * u));
+        static_cast<IO *>(p.o)[nh * DV + j0 + tid] = from_f32<IO>(p.scale * (rq + s_qk * u));
     }
     __syncthreads();
 
@@ -122,7 +130,7 @@ __global__ void __launch_bounds__(256, 2) decode_step_kernel(DecodeParams p) {
         const float kr = sk[r];
         float4 w = s[m];
         w.x += kr * u4.x; w.y += kr * u4.y; w.z += kr * u4.z; w.w += kr * u4.w;
-        __stcs(S4 + r * C4 + col4, w);
+        __stcs(S4 + r * C4F + col4, w);
     }
 }
 
@@ -130,7 +138,7 @@ template <typename IO, int DK, int DV>
 cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
     DecodeParams p{a.q, a.k, a.v, a.beta_logits, a.gate_logits, a.o, a.state,
                    a.H, a.scale, a.flags};
-    const unsigned grid = (unsigned)((int64_t)a.N * a.H);
+    const unsigned grid = (unsigned)((int64_t)a.N * a.H * kSplit);
     decode_step_kernel<IO, DK, DV><<<grid, 256, 0, s>>>(p);
     return cudaGetLastError();
 }

@@ -58,40 +58,44 @@ namespace {
 using namespace tc;
 
 constexpr int C = 64;     // tokens per chunk
-constexpr int NT = 256;   // threads per CTA
+constexpr int NT = 512;   // threads per CTA (16 warps)
 constexpr int TMEM_COLS = 512;
+constexpr int LDT = 68;   // fp32 row stride of the A and T scratch (16-byte rows)
 
 // ------------------------------------------------------------- smem layout
 // Every operand tile is a "row-swizzled" (RS) tile: `rows` rows of D bf16,
 // stored as D/64 column blocks of rows x 128 bytes, 128-byte swizzled with
 // 1024-byte atoms.  The same bytes serve as a K-major operand (rows = M or
 // N) or an MN-major operand (rows = K).
-template <int D>
+template <int D, bool GATED>
 struct Layout {
     static constexpr uint32_t tile64 = C * D * 2;               // [64][D]
     static constexpr uint32_t RAW_Q = 0;
     static constexpr uint32_t RAW_K = RAW_Q + tile64;
     static constexpr uint32_t RAW_V = RAW_K + tile64;
     static constexpr uint32_t RAW_G = RAW_V + tile64;
-    static constexpr uint32_t X = RAW_G + tile64;
-    // X during the block products: [Q^; K^] (128 rows) and packed K_R (160)
+    static constexpr uint32_t X = RAW_G + (GATED ? tile64 : 0);
+    // X, prologue (gated): fp32 prefix products P and 1/P ([64][D] each),
+    // then the block-product operands [Q^; K^] (128 rows) and packed K_R (160)
+    static constexpr uint32_t PP = X;
+    static constexpr uint32_t PPI = X + 64 * D * 4;
     static constexpr uint32_t QKH = X;
     static constexpr uint32_t KR = X + 128 * D * 2;
     // X during and after the solve
-    static constexpr uint32_t T16 = X;                 // T, bf16 [64][64]
-    static constexpr uint32_t AQK = X + 8192;          // Aq, bf16 [64][64]
-    static constexpr uint32_t SA = X + 16384;          // A, fp32 [64][65]
-    static constexpr uint32_t ST = SA + 64 * 65 * 4;   // T, fp32 [64][65]
-    static constexpr uint32_t SX = ST + 64 * 65 * 4;   // block temp, fp32 [3][16][17]
-    static constexpr uint32_t SB = X + 16384;          // S, bf16 [D][D] (after the solve)
-    static constexpr uint32_t X_END_A = KR + 160 * D * 2;
-    static constexpr uint32_t X_END_B = SX + 3 * 16 * 17 * 4;
+    static constexpr uint32_t T16 = X;                  // T, bf16 [64][64]
+    static constexpr uint32_t AQK = X + 8192;           // Aq, bf16 [64][64]
+    static constexpr uint32_t SA = X + 16384;           // A, fp32 [64][LDT]
+    static constexpr uint32_t ST = SA + 64 * LDT * 4;   // T, fp32 [64][LDT]
+    static constexpr uint32_t SX = ST + 64 * LDT * 4;   // merge temps, fp32 (6 KB)
+    static constexpr uint32_t SB = (SX + 6144 + 1023) & ~1023u;  // S, bf16 [D][D]
+    static constexpr uint32_t X_END_A = GATED ? KR + 160 * D * 2 : X;
+    static constexpr uint32_t X_END_P = GATED ? PPI + 64 * D * 4 : X;
     static constexpr uint32_t X_END_C = SB + D * D * 2;
-    static constexpr uint32_t X_END0 = X_END_A > X_END_B ? X_END_A : X_END_B;
+    static constexpr uint32_t X_END0 = X_END_A > X_END_P ? X_END_A : X_END_P;
     static constexpr uint32_t X_END1 = X_END0 > X_END_C ? X_END0 : X_END_C;
-    static constexpr uint32_t QG = (X_END1 + 1023) & ~1023u;   // Q e^{b}       [64][D]
-    static constexpr uint32_t KT = QG + tile64;                // K e^{b_end-b} [64][D]
-    static constexpr uint32_t BKG = KT + tile64;               // beta K e^{b}, later W
+    // [Q e^b ; K e^{b_end - b}] (gated) or [q^ ; k^] (ungated), 128 rows
+    static constexpr uint32_t PAIR = (X_END1 + 1023) & ~1023u;
+    static constexpr uint32_t BKG = PAIR + 2 * tile64;         // beta K e^b, later W
     static constexpr uint32_t BV = BKG + tile64;               // beta V, later u
     static constexpr uint32_t SMALL = BV + tile64;
     static constexpr uint32_t BETA = SMALL;                    // fp32 [64]
@@ -105,7 +109,8 @@ struct Layout {
 };
 
 // TMEM column map.  S: fp32 state (rows = key channels).  U: the delta u.
-// A: four 64-column block products (phase B only), later O and W.
+// A: block products (phase B only; four 64-column blocks when gated, one
+// otherwise), later O and W.
 template <int D>
 struct Cols {
     static constexpr uint32_t S = 0, U = D, A = 2 * D, O = 2 * D, W = 3 * D;
@@ -114,14 +119,6 @@ struct Cols {
 
 __device__ __forceinline__ uint32_t rs_off(int rows, int row, int col) {
     return (uint32_t)(col >> 6) * (uint32_t)rows * 128u + sw128_offset(row, col & 63);
-}
-
-__device__ __forceinline__ void st_bf16(uint8_t *tile, int rows, int row, int col, float v) {
-    *reinterpret_cast<__nv_bfloat16 *>(tile + rs_off(rows, row, col)) = __float2bfloat16_rn(v);
-}
-
-__device__ __forceinline__ float ld_bf16(const uint8_t *tile, int rows, int row, int col) {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + rs_off(rows, row, col)));
 }
 
 // 8 consecutive columns (col % 8 == 0) as one 16-byte store.
@@ -134,9 +131,7 @@ __device__ __forceinline__ void st_bf16x8(uint8_t *tile, int rows, int row, int 
     *reinterpret_cast<uint4 *>(tile + rs_off(rows, row, col)) = u;
 }
 
-__device__ __forceinline__ void ld_bf16x8(const uint8_t *tile, int rows, int row, int col,
-                                          float *v) {
-    uint4 u = *reinterpret_cast<const uint4 *>(tile + rs_off(rows, row, col));
+__device__ __forceinline__ void unpack8(uint4 u, float *v) {
     const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -146,16 +141,34 @@ __device__ __forceinline__ void ld_bf16x8(const uint8_t *tile, int rows, int row
     }
 }
 
-// K-major operand descriptor for K-step s (16 elements) of an RS tile.
+__device__ __forceinline__ uint4 pack8(const float *v) {
+    uint4 u;
+    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    return u;
+}
+
+__device__ __forceinline__ float bf(const uint8_t *p) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(p));
+}
+
+__device__ __forceinline__ void stbf(uint8_t *p, float v) {
+    *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(v);
+}
+
+// K-major operand descriptor for K-step s (16 elements) of an RS tile,
+// starting at row row0.
 __device__ __forceinline__ uint64_t kdesc(const uint8_t *tile, int rows, int row0, int s) {
     return smem_desc_sw128(smem_u32(tile) + (uint32_t)(s >> 2) * rows * 128u + row0 * 128u +
                                (uint32_t)(s & 3) * 32u,
                            16, 1024);
 }
 
-// MN-major operand descriptor for K-step s (rows 16s..16s+15) of an RS tile.
-__device__ __forceinline__ uint64_t mdesc(const uint8_t *tile, int rows, int s) {
-    return smem_desc_sw128(smem_u32(tile) + (uint32_t)s * 2048u, (uint32_t)rows * 128u, 1024);
+// MN-major operand descriptor for K-step s (rows row0+16s .. +15) of an RS tile.
+__device__ __forceinline__ uint64_t mdesc(const uint8_t *tile, int rows, int row0, int s) {
+    return smem_desc_sw128(smem_u32(tile) + (uint32_t)row0 * 128u + (uint32_t)s * 2048u,
+                           (uint32_t)rows * 128u, 1024);
 }
 
 // Row of a TMEM accumulator held by this thread (lane quarter q = warp % 4),
@@ -185,19 +198,21 @@ __global__ void __launch_bounds__(NT, 1)
                           const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v,
                           const __grid_constant__ CUtensorMap tm_g, TcParams p) {
-    using L = Layout<D>;
+    using L = Layout<D, GATED>;
     using TC = Cols<D>;
+    constexpr int DQ = D / 4;  // TMEM columns per warp in the readbacks
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *rawq = sm + L::RAW_Q, *rawk = sm + L::RAW_K, *rawv = sm + L::RAW_V,
             *rawg = sm + L::RAW_G;
     uint8_t *qkh = sm + L::QKH, *kr = sm + L::KR, *t16 = sm + L::T16, *aqk = sm + L::AQK;
+    float *sP = reinterpret_cast<float *>(sm + L::PP);
+    float *sPi = reinterpret_cast<float *>(sm + L::PPI);
     float *sA = reinterpret_cast<float *>(sm + L::SA);
     float *sT = reinterpret_cast<float *>(sm + L::ST);
     float *sX = reinterpret_cast<float *>(sm + L::SX);
-    uint8_t *sb = sm + L::SB, *qg = sm + L::QG, *kt = sm + L::KT, *bkg = sm + L::BKG,
-            *bv = sm + L::BV;
+    uint8_t *sb = sm + L::SB, *pair = sm + L::PAIR, *bkg = sm + L::BKG, *bv = sm + L::BV;
     uint8_t *wt = bkg, *ut = bv;  // W and u tiles reuse beta K e^b and beta V
     float *sbeta = reinterpret_cast<float *>(sm + L::BETA);
     float *skn = reinterpret_cast<float *>(sm + L::KN);
@@ -209,7 +224,7 @@ __global__ void __launch_bounds__(NT, 1)
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar_tma + 2);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int qd = warp & 3, hf = warp >> 2;
+    const int qd = warp & 3, cp = warp >> 2;  // TMEM lane quarter, column part
     const int h = blockIdx.x, n = blockIdx.y, H = p.H;
     int t_begin = p.cu_seqlens[n], t_end = p.cu_seqlens[n + 1];
     if (t_begin < 0 || t_end < t_begin || t_end > p.ntok) {
@@ -256,8 +271,8 @@ __global__ void __launch_bounds__(NT, 1)
     {
         const int row = acc_row(TC::MS, qd, lane);
 #pragma unroll
-        for (int cb = 0; cb < D / 2; cb += 16) {
-            const int col = hf * (D / 2) + cb;
+        for (int cb = 0; cb < DQ; cb += 16) {
+            const int col = cp * DQ + cb;
             float v[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
@@ -270,6 +285,10 @@ __global__ void __launch_bounds__(NT, 1)
     tma_pending = t_begin < t_end;
     uint32_t tma_par = 0, mma_par = 0;
     bool failed = false;
+    // beta logits of the next chunk, loaded one chunk ahead (threads 0..63)
+    float beta_next = 0.0f;
+    if (tid < C && t_begin + tid < t_end)
+        beta_next = __bfloat162float(p.beta_logits[(int64_t)(t_begin + tid) * H + h]);
 
     auto mma_wait = [&]() -> bool {
         const bool ok = mbar_wait(bar_mma, mma_par, &g_tc_error, 2);
@@ -296,17 +315,20 @@ __global__ void __launch_bounds__(NT, 1)
             tc_fence_after();
         }
         // ---------------------------------------------- A0: beta, row norms
-        if (tid < C)
-            sbeta[tid] = tid < len ? sigmoid_f(__bfloat162float(p.beta_logits[(int64_t)(cs + tid) * H + h]))
-                                   : 0.0f;
+        if (tid < C) {
+            sbeta[tid] = tid < len ? sigmoid_f(beta_next) : 0.0f;
+            const int tn = cs + C + tid;
+            beta_next = tn < t_end ? __bfloat162float(p.beta_logits[(int64_t)tn * H + h]) : 0.0f;
+        }
         {
-            const int r = tid >> 2, part = tid & 3;
+            // 8 threads per row, D/8 channels each, 16-byte loads
+            const int r = tid >> 3, part = tid & 7;
             float ssk = 0.0f, ssq = 0.0f;
 #pragma unroll
-            for (int c = part * (D / 4); c < (part + 1) * (D / 4); c += 8) {
+            for (int c = part * (D / 8); c < (part + 1) * (D / 8); c += 8) {
                 float kv[8], qv[8];
-                ld_bf16x8(rawk, C, r, c, kv);
-                ld_bf16x8(rawq, C, r, c, qv);
+                unpack8(*reinterpret_cast<const uint4 *>(rawk + rs_off(C, r, c)), kv);
+                unpack8(*reinterpret_cast<const uint4 *>(rawq + rs_off(C, r, c)), qv);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     if (silu) { kv[i] = silu_fast(kv[i]); qv[i] = silu_fast(qv[i]); }
@@ -314,10 +336,11 @@ __global__ void __launch_bounds__(NT, 1)
                     ssq += qv[i] * qv[i];
                 }
             }
-            ssk += __shfl_xor_sync(0xffffffffu, ssk, 1);
-            ssk += __shfl_xor_sync(0xffffffffu, ssk, 2);
-            ssq += __shfl_xor_sync(0xffffffffu, ssq, 1);
-            ssq += __shfl_xor_sync(0xffffffffu, ssq, 2);
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+                ssk += __shfl_xor_sync(0xffffffffu, ssk, o);
+                ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
+            }
             if (part == 0) {
                 const bool valid = r < len;
                 skn[r] = valid ? (l2k ? 1.0f / fmaxf(sqrtf(ssk), 1e-12f) : 1.0f) : 0.0f;
@@ -325,112 +348,152 @@ __global__ void __launch_bounds__(NT, 1)
             }
         }
         __syncthreads();
-        // ---------------------------------------------- A1: decay factors, operands
-        {
-            constexpr int CPT = D / 64;  // channels per thread
-            const int cg = tid & 63, R = tid >> 6, c0 = cg * CPT;
-            const int rb = 16 * R;
-            float al[16][CPT], ai[16][CPT];
-            if (GATED) {
-                float E[CPT];
+        // ---------------------------------------------- A1: operand tiles
+        if (!GATED) {
+            // [q^; k^] into PAIR, beta k^ into BKG, beta v into BV: 16-byte units
+            for (int u = tid; u < C * D / 8; u += NT) {
+                const uint32_t off = (uint32_t)u * 16u;                 // offset in a [64][D] tile
+                const uint32_t cb = off >> 13, in = off & 8191u;         // column block, offset in it
+                const int r = (int)(in >> 7);
+                const uint32_t po = cb * (128u * 128u) + in;            // same row in PAIR
+                float kv[8], qv[8], vv[8];
+                unpack8(*reinterpret_cast<const uint4 *>(rawk + off), kv);
+                unpack8(*reinterpret_cast<const uint4 *>(rawq + off), qv);
+                unpack8(*reinterpret_cast<const uint4 *>(rawv + off), vv);
+                const float kn = skn[r], qn = sqn[r], be = sbeta[r];
+                float bk[8];
 #pragma unroll
-                for (int j = 0; j < CPT; ++j) E[j] = 1.0f;
+                for (int i = 0; i < 8; ++i) {
+                    if (silu) { kv[i] = silu_fast(kv[i]); qv[i] = silu_fast(qv[i]); }
+                    kv[i] *= kn;
+                    qv[i] *= qn;
+                    bk[i] = be * kv[i];
+                    vv[i] *= be;
+                }
+                *reinterpret_cast<uint4 *>(pair + po) = pack8(qv);
+                *reinterpret_cast<uint4 *>(pair + po + 64u * 128u) = pack8(kv);
+                *reinterpret_cast<uint4 *>(bkg + off) = pack8(bk);
+                *reinterpret_cast<uint4 *>(bv + off) = pack8(vv);
+            }
+            if (tid < D) sgend[tid] = 1.0f;
+        } else {
+            // (a) one thread per (key channel c, 16-token block R): alpha = 1/(1+e^g),
+            // within-block prefix products P and 1/P (fp32 scratch), block totals E_R.
+            if (tid < 4 * D) {
+                const int c = tid % D, R = tid / D;
+                const uint8_t *pg = rawg + (c >> 6) * 8192 + (16 * R) * 128;
+                const uint32_t lo = (uint32_t)(c & 7) * 2u;
+                const int ch = (c >> 3) & 7;
+                float P = 1.0f, Pi = 1.0f;
 #pragma unroll
                 for (int rho = 0; rho < 16; ++rho) {
-                    const int r = rb + rho;
-#pragma unroll
-                    for (int j = 0; j < CPT; ++j) {
-                        const float g = fminf(ld_bf16(rawg, C, r, c0 + j), 80.0f);
-                        const float e = __expf(g);
-                        const bool valid = r < len;
-                        al[rho][j] = valid ? __fdividef(1.0f, 1.0f + e) : 1.0f;
-                        ai[rho][j] = valid ? 1.0f + e : 1.0f;
-                        E[j] *= al[rho][j];
+                    const int r = 16 * R + rho;
+                    const float g = fminf(bf(pg + rho * 128 + (((ch ^ (rho & 7)) << 4) + lo)), 80.0f);
+                    const float e = __expf(g);
+                    if (r < len) {
+                        P *= __fdividef(1.0f, 1.0f + e);
+                        Pi = fminf(Pi * (1.0f + e), 1e30f);
                     }
+                    sP[r * D + c] = P;
+                    sPi[r * D + c] = Pi;
                 }
-#pragma unroll
-                for (int j = 0; j < CPT; ++j) sE[R * D + c0 + j] = E[j];
-                __syncthreads();
+                sE[R * D + c] = P;
             }
-            float Gb[CPT], Ea[CPT];
+            __syncthreads();
+            // (b) one thread per (row r, 8 channels): every operand is (q or k) x
+            // (P or 1/P) x a per-(block, channel) constant, using the
+            // within-block suffix prod_{t>r} alpha_t = E_R / P_r.
+            constexpr int UNITS = C * D / 8, UPT = (UNITS + NT - 1) / NT;
+            float vq[UPT][8], vk[UPT][8], vp[UPT][8], vpi[UPT][8];
 #pragma unroll
-            for (int j = 0; j < CPT; ++j) {
-                Gb[j] = 1.0f;
-                Ea[j] = 1.0f;
-                if (GATED) {
+            for (int j = 0; j < UPT; ++j) {
+                const int u = tid + j * NT;
+                if (u < UNITS) {
+                    const int r = u / (D / 8), c8 = (u % (D / 8)) * 8;
+                    unpack8(*reinterpret_cast<const uint4 *>(rawq + rs_off(C, r, c8)), vq[j]);
+                    unpack8(*reinterpret_cast<const uint4 *>(rawk + rs_off(C, r, c8)), vk[j]);
+                    const float4 *pp = reinterpret_cast<const float4 *>(sP + r * D + c8);
+                    const float4 *pi = reinterpret_cast<const float4 *>(sPi + r * D + c8);
+                    const float4 a0 = pp[0], a1 = pp[1], b0 = pi[0], b1 = pi[1];
+                    vp[j][0] = a0.x; vp[j][1] = a0.y; vp[j][2] = a0.z; vp[j][3] = a0.w;
+                    vp[j][4] = a1.x; vp[j][5] = a1.y; vp[j][6] = a1.z; vp[j][7] = a1.w;
+                    vpi[j][0] = b0.x; vpi[j][1] = b0.y; vpi[j][2] = b0.z; vpi[j][3] = b0.w;
+                    vpi[j][4] = b1.x; vpi[j][5] = b1.y; vpi[j][6] = b1.z; vpi[j][7] = b1.w;
+                }
+            }
+            __syncthreads();  // P / 1/P scratch overlaps the outputs below
+#pragma unroll
+            for (int j = 0; j < UPT; ++j) {
+                const int u = tid + j * NT;
+                if (u < UNITS) {
+                    const int r = u / (D / 8), c8 = (u % (D / 8)) * 8, R = r >> 4;
+                    const float kn = skn[r], qn = sqn[r], be = sbeta[r];
+                    float o1[8], o2[8], o3[8], o4[8], o5[8], o6[8];
+                    float mk[3][8];
+                    float Ev[4][8];
+#pragma unroll
                     for (int R2 = 0; R2 < 4; ++R2) {
-                        const float e = sE[R2 * D + c0 + j];
-                        if (R2 < R) Gb[j] *= e;
-                        if (R2 > R) Ea[j] *= e;
+                        const float4 e0 = *reinterpret_cast<const float4 *>(sE + R2 * D + c8);
+                        const float4 e1 = *reinterpret_cast<const float4 *>(sE + R2 * D + c8 + 4);
+                        Ev[R2][0] = e0.x; Ev[R2][1] = e0.y; Ev[R2][2] = e0.z; Ev[R2][3] = e0.w;
+                        Ev[R2][4] = e1.x; Ev[R2][5] = e1.y; Ev[R2][6] = e1.z; Ev[R2][7] = e1.w;
                     }
-                    if (R == 0) sgend[c0 + j] = Gb[j] * sE[c0 + j] * Ea[j];
-                } else if (R == 0) {
-                    sgend[c0 + j] = 1.0f;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float E0 = Ev[0][i], E1 = Ev[1][i], E2 = Ev[2][i], E3 = Ev[3][i];
+                        const float Gb = R == 0 ? 1.0f : R == 1 ? E0 : R == 2 ? E0 * E1 : E0 * E1 * E2;
+                        const float EaK = R == 0 ? E0 * E1 * E2 * E3 : R == 1 ? E1 * E2 * E3 : R == 2 ? E2 * E3 : E3;
+                        float qv = vq[j][i], kv = vk[j][i];
+                        if (silu) { qv = silu_fast(qv); kv = silu_fast(kv); }
+                        qv *= qn;
+                        kv *= kn;
+                        const float P = vp[j][i], Pi = vpi[j][i];
+                        o1[i] = qv * P;                 // Q^
+                        o2[i] = kv * P;                 // K^
+                        o3[i] = o1[i] * Gb;             // Q e^b
+                        o4[i] = be * o2[i] * Gb;        // beta K e^b
+                        o5[i] = kv * Pi;                // K_R, own block
+                        o6[i] = o5[i] * EaK;            // K e^{b_end - b}
+                        // K_R' for R' = R+1+t: k / P_r * prod_{R <= R'' < R'} E_R''
+                        float f = o5[i];
+#pragma unroll
+                        for (int t = 0; t < 3; ++t) {
+                            const int Rt = R + t;
+                            f *= Rt == 0 ? E0 : Rt == 1 ? E1 : Rt == 2 ? E2 : E3;
+                            mk[t][i] = f;
+                        }
+                    }
+                    *reinterpret_cast<uint4 *>(qkh + rs_off(128, r, c8)) = pack8(o1);
+                    *reinterpret_cast<uint4 *>(qkh + rs_off(128, 64 + r, c8)) = pack8(o2);
+                    *reinterpret_cast<uint4 *>(pair + rs_off(128, r, c8)) = pack8(o3);
+                    *reinterpret_cast<uint4 *>(pair + rs_off(128, 64 + r, c8)) = pack8(o6);
+                    *reinterpret_cast<uint4 *>(bkg + rs_off(C, r, c8)) = pack8(o4);
+                    *reinterpret_cast<uint4 *>(kr + rs_off(160, 8 * R * (R + 1) + r, c8)) = pack8(o5);
+#pragma unroll
+                    for (int t = 0; t < 3; ++t) {
+                        const int R2 = R + 1 + t;
+                        if (R2 < 4)
+                            *reinterpret_cast<uint4 *>(kr + rs_off(160, 8 * R2 * (R2 + 1) + r, c8)) =
+                                pack8(mk[t]);
+                    }
+                    if (r == 0) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            sgend[c8 + i] = sE[c8 + i] * sE[D + c8 + i] * sE[2 * D + c8 + i] * sE[3 * D + c8 + i];
+                    }
                 }
             }
-            // forward over the block: prefix products
-            float P[CPT], Pi[CPT];
+            // beta V
+            for (int u = tid; u < C * D / 8; u += NT) {
+                const uint32_t off = (uint32_t)u * 16u;
+                const int r = (int)((off & 8191u) >> 7);
+                float vv[8];
+                unpack8(*reinterpret_cast<const uint4 *>(rawv + off), vv);
+                const float be = sbeta[r];
 #pragma unroll
-            for (int j = 0; j < CPT; ++j) { P[j] = 1.0f; Pi[j] = 1.0f; }
-#pragma unroll
-            for (int rho = 0; rho < 16; ++rho) {
-                const int r = rb + rho;
-                const float kn = skn[r], qn = sqn[r], be = sbeta[r];
-#pragma unroll
-                for (int j = 0; j < CPT; ++j) {
-                    const int c = c0 + j;
-                    float kv = ld_bf16(rawk, C, r, c), qv = ld_bf16(rawq, C, r, c);
-                    if (silu) { kv = silu_fast(kv); qv = silu_fast(qv); }
-                    kv *= kn;
-                    qv *= qn;
-                    if (GATED) {
-                        P[j] *= al[rho][j];
-                        Pi[j] = fminf(Pi[j] * ai[rho][j], 1e30f);
-                    }
-                    st_bf16(qkh, 128, r, c, qv * P[j]);
-                    st_bf16(qkh, 128, 64 + r, c, kv * P[j]);
-                    st_bf16(qg, C, r, c, qv * Gb[j] * P[j]);
-                    st_bf16(bkg, C, r, c, be * kv * Gb[j] * P[j]);
-                    st_bf16(kr, 160, 8 * R * (R + 1) + r, c, kv * Pi[j]);
-                }
+                for (int i = 0; i < 8; ++i) vv[i] *= be;
+                *reinterpret_cast<uint4 *>(bv + off) = pack8(vv);
             }
-            // backward over the block: suffix products
-            float Sb[CPT];
-#pragma unroll
-            for (int j = 0; j < CPT; ++j) Sb[j] = 1.0f;
-#pragma unroll
-            for (int rho = 15; rho >= 0; --rho) {
-                const int r = rb + rho;
-                const float kn = skn[r];
-#pragma unroll
-                for (int j = 0; j < CPT; ++j) {
-                    const int c = c0 + j;
-                    float kv = ld_bf16(rawk, C, r, c);
-                    if (silu) kv = silu_fast(kv);
-                    kv *= kn;
-                    st_bf16(kt, C, r, c, kv * Sb[j] * Ea[j]);
-                    float f = Sb[j];
-                    for (int R2 = R + 1; R2 < 4; ++R2) {
-                        st_bf16(kr, 160, 8 * R2 * (R2 + 1) + r, c, kv * f);
-                        if (GATED) f *= sE[R2 * D + c];
-                    }
-                    if (GATED) Sb[j] *= al[rho][j];
-                }
-            }
-        }
-        // ---------------------------------------------- A2: beta V
-        for (int e = tid; e < C * D / 8; e += NT) {
-            const uint32_t off = (uint32_t)e * 16u;
-            const int row = (int)((off % (uint32_t)(C * 128)) >> 7);
-            uint4 u = *reinterpret_cast<const uint4 *>(rawv + off);
-            __nv_bfloat162 *hv = reinterpret_cast<__nv_bfloat162 *>(&u);
-            const float be = sbeta[row];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float2 f = __bfloat1622float2(hv[i]);
-                hv[i] = __floats2bfloat162_rn(f.x * be, f.y * be);
-            }
-            *reinterpret_cast<uint4 *>(bv + off) = u;
         }
         phase_sync();
         // raw tiles consumed: fetch the next chunk while this one computes
@@ -441,131 +504,99 @@ __global__ void __launch_bounds__(NT, 1)
         // ---------------------------------------------- B: block products
         if (tid == 0) {
             constexpr uint32_t id = idesc_bf16(128, 64, false, false);
+            if (GATED) {
 #pragma unroll
-            for (int R = 0; R < 4; ++R)
+                for (int R = 0; R < 4; ++R)
+#pragma unroll
+                    for (int s = 0; s < D / 16; ++s)
+                        mma_bf16(tmem + TC::A + 64 * R, kdesc(qkh, 128, 0, s),
+                                 kdesc(kr, 160, 8 * R * (R + 1), s), id, s > 0);
+            } else {
 #pragma unroll
                 for (int s = 0; s < D / 16; ++s)
-                    mma_bf16(tmem + TC::A + 64 * R, kdesc(qkh, 128, 0, s),
-                             kdesc(kr, 160, 8 * R * (R + 1), s), id, s > 0);
+                    mma_bf16(tmem + TC::A, kdesc(pair, 128, 0, s), kdesc(pair, 128, 64, s), id,
+                             s > 0);
+            }
             mma_commit(bar_mma);
         }
         if (__syncthreads_or(!mma_wait())) { failed = true; break; }
-        // ---------------------------------------------- C1: Aq tile, A rows, diagonal inverses
+        // ---------------------------------------------- C1: Aq tile, A rows
         // TMEM lanes 0..63 hold rows of Aq, lanes 64..127 rows of A (before
-        // beta); row r belongs to block R = r / 16, whose product sits in
-        // columns [64 R, 64 R + 64).  A warp covers two blocks, so it reads
-        // both (addresses stay warp-uniform) and each lane keeps its own.
-        if (hf == 0) {
+        // beta).  Gated: row r of block R = r/16 sits in columns 64 R + i.
+        // Each warp reads 16 columns (part cp) of its quarter; a warp spans
+        // two blocks, so it reads both and each lane keeps its own (TMEM
+        // addresses stay warp-uniform).
+        {
             const bool is_q = qd < 2;
-            const int rb0 = 32 * (is_q ? qd : qd - 2);
-            const int r = rb0 + lane, R = r >> 4, rho = r & 15;
-            float row[64];
+            const int r = 32 * (is_q ? qd : qd - 2) + lane, R = r >> 4;
+            const int col = 16 * cp;
+            float v[16];
+            if (GATED) {
+                float w0[16], w1[16];
+                const int Rw = (32 * (is_q ? qd : qd - 2)) >> 4;
+                tmem_ld16(tq + TC::A + 64 * Rw + col, w0);
+                tmem_ld16(tq + TC::A + 64 * (Rw + 1) + col, w1);
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const int Rw = (rb0 >> 4) + half;
-#pragma unroll
-                for (int cb = 0; cb < 64; cb += 16) {
-                    float v[16];
-                    tmem_ld16(tq + TC::A + 64 * Rw + cb, v);
-                    if (R == Rw) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) row[cb + i] = v[i];
-                    }
-                }
+                for (int i = 0; i < 16; ++i) v[i] = (R == Rw) ? w0[i] : w1[i];
+            } else {
+                tmem_ld16(tq + TC::A + col, v);
             }
             if (is_q) {
 #pragma unroll
-                for (int i = 0; i < 64; ++i)
-                    if (i > r) row[i] = 0.0f;
-#pragma unroll
-                for (int cb = 0; cb < 64; cb += 8) st_bf16x8(aqk, 64, r, cb, row + cb);
+                for (int i = 0; i < 16; ++i)
+                    if (col + i > r) v[i] = 0.0f;
+                st_bf16x8(aqk, 64, r, col, v);
+                st_bf16x8(aqk, 64, r, col + 8, v + 8);
             } else {
                 const float be = sbeta[r];
+                float4 *dst = reinterpret_cast<float4 *>(sA + r * LDT + col);
 #pragma unroll
-                for (int i = 0; i < 64; ++i) sA[r * 65 + i] = (i < r) ? be * row[i] : 0.0f;
-                float dg[16];
-#pragma unroll
-                for (int m = 0; m < 16; ++m) dg[m] = sA[r * 65 + 16 * R + m];
-                // T_RR = (I + A_RR)^{-1}: lane rho of each 16-lane group owns row rho
-                float t[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) t[j] = (j == rho) ? 1.0f : 0.0f;
-                const int gbase = lane & 16;
-#pragma unroll
-                for (int m = 0; m < 15; ++m) {
-#pragma unroll
-                    for (int j = 0; j <= m; ++j) {
-                        const float tm = __shfl_sync(0xffffffffu, t[j], gbase + m);
-                        if (rho > m) t[j] -= dg[m] * tm;
-                    }
+                for (int i = 0; i < 4; ++i) {
+                    float4 f;
+                    f.x = (col + 4 * i + 0 < r) ? be * v[4 * i + 0] : 0.0f;
+                    f.y = (col + 4 * i + 1 < r) ? be * v[4 * i + 1] : 0.0f;
+                    f.z = (col + 4 * i + 2 < r) ? be * v[4 * i + 2] : 0.0f;
+                    f.w = (col + 4 * i + 3 < r) ? be * v[4 * i + 3] : 0.0f;
+                    dst[i] = f;
                 }
-#pragma unroll
-                for (int j = 0; j < 64; ++j) sT[r * 65 + j] = 0.0f;
-#pragma unroll
-                for (int j = 0; j < 16; ++j) sT[r * 65 + 16 * R + j] = t[j];
             }
         }
         __syncthreads();
-        // ---------------------------------------------- C2: off-diagonal blocks of T
-        // T_RJ = -T_RR sum_{M=J}^{R-1} A_RM T_MJ, by levels L = R - J.
-#pragma unroll 1
-        for (int Lv = 1; Lv < 4; ++Lv) {
-            const int nb = 4 - Lv;
-            for (int e = tid; e < nb * 256; e += NT) {
-                const int b = e >> 8, i = (e >> 4) & 15, j = e & 15;
-                const int R = Lv + b, J = b;
-                float acc = 0.0f;
-                for (int m = 16 * J; m < 16 * R; ++m) acc += sA[(16 * R + i) * 65 + m] * sT[m * 65 + 16 * J + j];
-                sX[(b * 16 + i) * 17 + j] = acc;
-            }
-            __syncthreads();
-            for (int e = tid; e < nb * 256; e += NT) {
-                const int b = e >> 8, i = (e >> 4) & 15, j = e & 15;
-                const int R = Lv + b, J = b;
-                float acc = 0.0f;
+        // ---------------------------------------------- C1b: diagonal inverses; S to bf16
+        // Warps 0,1: T_RR = (I + A_RR)^{-1}, lane rho of each 16-lane group owns
+        // row rho.  Warps 8..15 meanwhile copy S (TMEM, fp32) to its bf16
+        // operand tile and apply this chunk's decay e^{b_end} to S in place.
+        if (warp < 2) {
+            const int r = 32 * warp + lane, R = r >> 4, rho = r & 15;
+            float dg[16], t[16];
 #pragma unroll
-                for (int m = 0; m < 16; ++m) acc += sT[(16 * R + i) * 65 + 16 * R + m] * sX[(b * 16 + m) * 17 + j];
-                sT[(16 * R + i) * 65 + 16 * J + j] = -acc;
+            for (int m = 0; m < 16; m += 4) {
+                const float4 f = *reinterpret_cast<const float4 *>(sA + r * LDT + 16 * R + m);
+                dg[m] = f.x; dg[m + 1] = f.y; dg[m + 2] = f.z; dg[m + 3] = f.w;
             }
-            __syncthreads();
-        }
-        // ---------------------------------------------- C3: T to bf16 operand
-        {
-            const int r = tid >> 2, c = (tid & 3) * 16;
-            st_bf16x8(t16, 64, r, c, sT + r * 65 + c);
-            st_bf16x8(t16, 64, r, c + 8, sT + r * 65 + c + 8);
-        }
-        phase_sync();
-        // ---------------------------------------------- D: W = T (beta K e^b), u = T (beta V)
-        if (tid == 0) {
-            constexpr uint32_t id = idesc_bf16(64, D, false, true);
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t a = kdesc(t16, 64, 0, s);
-                mma_bf16(tmem + TC::W, a, mdesc(bkg, C, s), id, s > 0);
-                mma_bf16(tmem + TC::U, a, mdesc(bv, C, s), id, s > 0);
-            }
-            mma_commit(bar_mma);
-        }
-        if (__syncthreads_or(!mma_wait())) { failed = true; break; }
-        // ---------------------------------------------- E: W tile; S -> bf16, decay S
-        {
-            const int r = acc_row(64, qd, lane);
+            for (int j = 0; j < 16; ++j) t[j] = (j == rho) ? 1.0f : 0.0f;
+            const int gbase = lane & 16;
 #pragma unroll
-            for (int cb = 0; cb < D / 2; cb += 16) {
-                const int col = hf * (D / 2) + cb;
-                float v[16];
-                tmem_ld16(tq + TC::W + col, v);
-                if (r >= 0) {
-                    st_bf16x8(wt, C, r, col, v);
-                    st_bf16x8(wt, C, r, col + 8, v + 8);
+            for (int m = 0; m < 15; ++m) {
+#pragma unroll
+                for (int j = 0; j <= m; ++j) {
+                    const float tm = __shfl_sync(0xffffffffu, t[j], gbase + m);
+                    if (rho > m) t[j] -= dg[m] * tm;
                 }
             }
+            float4 *dst = reinterpret_cast<float4 *>(sT + r * LDT);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) dst[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) dst[(16 * R + j) >> 2] = make_float4(t[j], t[j + 1], t[j + 2], t[j + 3]);
+        } else if (warp >= 8) {
             const int c = acc_row(TC::MS, qd, lane);
             const float gd = c >= 0 ? sgend[c] : 1.0f;
+            const int half = (warp >> 2) & 1;
 #pragma unroll
             for (int cb = 0; cb < D / 2; cb += 16) {
-                const int col = hf * (D / 2) + cb;
+                const int col = half * (D / 2) + cb;
                 float v[16];
                 tmem_ld16(tq + TC::S + col, v);
                 if (c >= 0) {
@@ -579,6 +610,101 @@ __global__ void __launch_bounds__(NT, 1)
                 }
             }
         }
+        __syncthreads();
+        // ---------------------------------------------- C2: off-diagonal blocks of T
+        // Two merges.  (1) T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22.
+        // (2) with T_TT = T[0:32,0:32], T_BB = T[32:64,32:64]:
+        //     T[32:64, 0:32] = -T_BB (A[32:64, 0:32] T_TT).
+        // Each thread produces four adjacent outputs (float4) of one row.
+        {
+            float *sX1 = sX;          // [2][16][16]
+            float *sY = sX + 512;     // [32][32]
+            const int b = tid >> 6, i1 = (tid >> 2) & 15, jq1 = tid & 3;   // merge 1: 128 threads
+            const int R1 = 1 + 2 * b, J1 = 2 * b;
+            if (tid < 128) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                const float *arow = sA + (16 * R1 + i1) * LDT + 16 * J1;
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    const float a = arow[m];
+                    const float4 t4 = *reinterpret_cast<const float4 *>(sT + (16 * J1 + m) * LDT + 16 * J1 + 4 * jq1);
+                    acc.x += a * t4.x; acc.y += a * t4.y; acc.z += a * t4.z; acc.w += a * t4.w;
+                }
+                *reinterpret_cast<float4 *>(sX1 + (b * 16 + i1) * 16 + 4 * jq1) = acc;
+            }
+            __syncthreads();
+            if (tid < 128) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                const float *trow = sT + (16 * R1 + i1) * LDT + 16 * R1;
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    const float a = trow[m];
+                    const float4 x4 = *reinterpret_cast<const float4 *>(sX1 + (b * 16 + m) * 16 + 4 * jq1);
+                    acc.x += a * x4.x; acc.y += a * x4.y; acc.z += a * x4.z; acc.w += a * x4.w;
+                }
+                *reinterpret_cast<float4 *>(sT + (16 * R1 + i1) * LDT + 16 * J1 + 4 * jq1) =
+                    make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+            }
+            __syncthreads();
+            const int i2 = tid >> 3, jq2 = tid & 7;                         // merge 2: 256 threads
+            if (tid < 256) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                const float *arow = sA + (32 + i2) * LDT;
+#pragma unroll
+                for (int m = 0; m < 32; ++m) {
+                    const float a = arow[m];
+                    const float4 t4 = *reinterpret_cast<const float4 *>(sT + m * LDT + 4 * jq2);
+                    acc.x += a * t4.x; acc.y += a * t4.y; acc.z += a * t4.z; acc.w += a * t4.w;
+                }
+                *reinterpret_cast<float4 *>(sY + i2 * 32 + 4 * jq2) = acc;
+            }
+            __syncthreads();
+            if (tid < 256) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                const float *trow = sT + (32 + i2) * LDT + 32;
+#pragma unroll
+                for (int m = 0; m < 32; ++m) {
+                    const float a = trow[m];
+                    const float4 y4 = *reinterpret_cast<const float4 *>(sY + m * 32 + 4 * jq2);
+                    acc.x += a * y4.x; acc.y += a * y4.y; acc.z += a * y4.z; acc.w += a * y4.w;
+                }
+                *reinterpret_cast<float4 *>(sT + (32 + i2) * LDT + 4 * jq2) =
+                    make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+            }
+            __syncthreads();
+        }
+        // ---------------------------------------------- C3: T to bf16 operand
+        {
+            const int r = tid >> 3, c = (tid & 7) * 8;
+            st_bf16x8(t16, 64, r, c, sT + r * LDT + c);
+        }
+        phase_sync();
+        // ---------------------------------------------- D: W = T (beta K e^b), u = T (beta V)
+        if (tid == 0) {
+            constexpr uint32_t id = idesc_bf16(64, D, false, true);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint64_t a = kdesc(t16, 64, 0, s);
+                mma_bf16(tmem + TC::W, a, mdesc(bkg, C, 0, s), id, s > 0);
+                mma_bf16(tmem + TC::U, a, mdesc(bv, C, 0, s), id, s > 0);
+            }
+            mma_commit(bar_mma);
+        }
+        if (__syncthreads_or(!mma_wait())) { failed = true; break; }
+        // ---------------------------------------------- E: W tile
+        {
+            const int r = acc_row(64, qd, lane);
+#pragma unroll
+            for (int cb = 0; cb < DQ; cb += 16) {
+                const int col = cp * DQ + cb;
+                float v[16];
+                tmem_ld16(tq + TC::W + col, v);
+                if (r >= 0) {
+                    st_bf16x8(wt, C, r, col, v);
+                    st_bf16x8(wt, C, r, col + 8, v + 8);
+                }
+            }
+        }
         phase_sync();
         // ---------------------------------------------- F: u -= W S, O = (Q e^b) S
         if (tid == 0) {
@@ -586,9 +712,9 @@ __global__ void __launch_bounds__(NT, 1)
             constexpr uint32_t ido = idesc_bf16(64, D, false, true);
 #pragma unroll
             for (int s = 0; s < D / 16; ++s) {
-                const uint64_t bS = mdesc(sb, D, s);
+                const uint64_t bS = mdesc(sb, D, 0, s);
                 mma_bf16(tmem + TC::U, kdesc(wt, C, 0, s), bS, idw, 1);
-                mma_bf16(tmem + TC::O, kdesc(qg, C, 0, s), bS, ido, s > 0);
+                mma_bf16(tmem + TC::O, kdesc(pair, 128, 0, s), bS, ido, s > 0);
             }
             mma_commit(bar_mma);
         }
@@ -597,8 +723,8 @@ __global__ void __launch_bounds__(NT, 1)
         {
             const int r = acc_row(64, qd, lane);
 #pragma unroll
-            for (int cb = 0; cb < D / 2; cb += 16) {
-                const int col = hf * (D / 2) + cb;
+            for (int cb = 0; cb < DQ; cb += 16) {
+                const int col = cp * DQ + cb;
                 float v[16];
                 tmem_ld16(tq + TC::U + col, v);
                 if (r >= 0) {
@@ -614,9 +740,9 @@ __global__ void __launch_bounds__(NT, 1)
             constexpr uint32_t ids = idesc_bf16(D, D, true, true);
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
-                const uint64_t bU = mdesc(ut, C, s);
+                const uint64_t bU = mdesc(ut, C, 0, s);
                 mma_bf16(tmem + TC::O, kdesc(aqk, 64, 0, s), bU, ido, 1);
-                mma_bf16(tmem + TC::S, mdesc(kt, C, s), bU, ids, 1);
+                mma_bf16(tmem + TC::S, mdesc(pair, 128, 64, s), bU, ids, 1);
             }
             mma_commit(bar_mma);
         }
@@ -627,19 +753,16 @@ __global__ void __launch_bounds__(NT, 1)
             const bool valid = r >= 0 && r < len;
             __nv_bfloat16 *orow = p.o + ((int64_t)(cs + (r < 0 ? 0 : r)) * H + h) * D;
 #pragma unroll
-            for (int cb = 0; cb < D / 2; cb += 16) {
-                const int col = hf * (D / 2) + cb;
+            for (int cb = 0; cb < DQ; cb += 16) {
+                const int col = cp * DQ + cb;
                 float v[16];
                 tmem_ld16(tq + TC::O + col, v);
                 if (valid) {
-                    uint4 u[2];
-                    __nv_bfloat162 *hv = reinterpret_cast<__nv_bfloat162 *>(u);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        hv[i] = __floats2bfloat162_rn(v[2 * i] * p.scale, v[2 * i + 1] * p.scale);
+                    for (int i = 0; i < 16; ++i) v[i] *= p.scale;
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + col);
-                    dst[0] = u[0];
-                    dst[1] = u[1];
+                    dst[0] = pack8(v);
+                    dst[1] = pack8(v + 8);
                 }
             }
         }
@@ -653,8 +776,8 @@ __global__ void __launch_bounds__(NT, 1)
     if (p.final_S && !failed) {
         const int row = acc_row(TC::MS, qd, lane);
 #pragma unroll
-        for (int cb = 0; cb < D / 2; cb += 16) {
-            const int col = hf * (D / 2) + cb;
+        for (int cb = 0; cb < DQ; cb += 16) {
+            const int col = cp * DQ + cb;
             float v[16];
             tmem_ld16(tq + TC::S + col, v);
             if (row >= 0) {
@@ -713,7 +836,8 @@ cudaError_t launch_t(const PrefillArgs &a, cudaStream_t s) {
     TcParams p{static_cast<const __nv_bfloat16 *>(a.beta_logits), static_cast<__nv_bfloat16 *>(a.o),
                a.cu_seqlens, a.init_S, a.final_S, a.H, a.ntok, a.scale, a.flags};
     // At least 120 KB so that one CTA (and its 512 TMEM columns) owns an SM.
-    const size_t smem = Layout<D>::TOTAL + 1024 > 120 * 1024 ? Layout<D>::TOTAL + 1024 : 120 * 1024;
+    constexpr size_t need = Layout<D, GATED>::TOTAL + 1024;
+    const size_t smem = need > 120 * 1024 ? need : 120 * 1024;
     auto kern = delta_chunk_tc_kernel<D, GATED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

@@ -39,9 +39,6 @@ L2NORM_K = 1
 L2NORM_Q = 2
 SILU_QK = 4
 
-_lib = None
-
-
 def build(force: bool = False) -> str:
     """Compile the oracle shared library with gcc (no GPU needed)."""
     os.makedirs(_OUT_DIR, exist_ok=True)
@@ -54,10 +51,15 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
-def _load():
-    global _lib
-    if _lib is None:
-        lib = ctypes.CDLL(build())
+class OracleLib:
+    """The oracle functions bound to one compiled copy of linattn_oracle.c.
+
+    The default instance uses the committed source; tests may bind a
+    deliberately altered copy (compiled with ``build_variant``) to check that
+    the pins catch it."""
+
+    def __init__(self, lib_path):
+        lib = ctypes.CDLL(lib_path)
         dp = ctypes.POINTER(ctypes.c_double)
         ip = ctypes.POINTER(ctypes.c_int64)
         c_int, c_uint, c_double = ctypes.c_int, ctypes.c_uint, ctypes.c_double
@@ -69,8 +71,44 @@ def _load():
                                          c_double, c_uint, dp, c_int]
         for f in (lib.la_oracle_linear, lib.la_oracle_delta, lib.la_oracle_decode):
             f.restype = c_int
-        _lib = lib
-    return _lib
+        self.lib = lib
+        self.L2NORM_K, self.L2NORM_Q, self.SILU_QK = L2NORM_K, L2NORM_Q, SILU_QK
+
+    def linear(self, *a, **k):
+        return _linear(self.lib, *a, **k)
+
+    def delta(self, *a, **k):
+        return _delta(self.lib, *a, **k)
+
+    def decode(self, *a, **k):
+        return _decode(self.lib, *a, **k)
+
+
+def build_variant(source_text: str, out_dir: str) -> str:
+    """Compile an altered copy of the oracle source into out_dir (tests only)."""
+    os.makedirs(out_dir, exist_ok=True)
+    src = os.path.join(out_dir, "variant.c")
+    with open(src, "w") as f:
+        f.write(source_text)
+    lib = os.path.join(out_dir, "libvariant.so")
+    subprocess.run(["gcc", "-O1", "-ffp-contract=off", "-fPIC", "-shared", "-pthread", "-o", lib,
+                    src, "-lm"], check=True)
+    return lib
+
+
+def source_text() -> str:
+    with open(_SRC) as f:
+        return f.read()
+
+
+_default = None
+
+
+def _load():
+    global _default
+    if _default is None:
+        _default = OracleLib(build())
+    return _default.lib
 
 
 def _f64(x):
@@ -98,6 +136,23 @@ def default_threads() -> int:
 
 
 def linear(q, k, v, cu_seqlens, init_S=None, init_z=None, nthreads=None):
+    """ELU+1 causal linear attention (see _linear)."""
+    return _linear(_load(), q, k, v, cu_seqlens, init_S, init_z, nthreads)
+
+
+def delta(q, k, v, beta_logits, gate_logits, cu_seqlens, scale=1.0, flags=L2NORM_K,
+          init_S=None, nthreads=None):
+    """(Gated) delta rule (see _delta)."""
+    return _delta(_load(), q, k, v, beta_logits, gate_logits, cu_seqlens, scale, flags, init_S,
+                  nthreads)
+
+
+def decode(q, k, v, beta_logits, gate_logits, state, scale=1.0, flags=L2NORM_K, nthreads=None):
+    """One decode step (see _decode)."""
+    return _decode(_load(), q, k, v, beta_logits, gate_logits, state, scale, flags, nthreads)
+
+
+def _linear(lib, q, k, v, cu_seqlens, init_S=None, init_z=None, nthreads=None):
     """ELU+1 causal linear attention.  Shapes: q,k [ntok,H,dk], v [ntok,H,dv].
 
     Returns (o [ntok,H,dv], final_S [N,H,dk,dv], final_z [N,H,dk]) in fp64.
@@ -111,16 +166,16 @@ def linear(q, k, v, cu_seqlens, init_S=None, init_z=None, nthreads=None):
     fS = np.zeros((N, H, dk, dv))
     fz = np.zeros((N, H, dk))
     iS, iz = _f64(init_S), _f64(init_z)
-    rc = _load().la_oracle_linear(_ptr(q), _ptr(k), _ptr(v), _ptr(o), cup, N, H, dk, dv,
-                                  _ptr(iS), _ptr(iz), _ptr(fS), _ptr(fz),
-                                  nthreads or default_threads())
+    rc = lib.la_oracle_linear(_ptr(q), _ptr(k), _ptr(v), _ptr(o), cup, N, H, dk, dv,
+                              _ptr(iS), _ptr(iz), _ptr(fS), _ptr(fz),
+                              nthreads or default_threads())
     if rc != 0:
         raise ValueError("la_oracle_linear rejected its arguments")
     return o, fS, fz
 
 
-def delta(q, k, v, beta_logits, gate_logits, cu_seqlens, scale=1.0, flags=L2NORM_K,
-          init_S=None, nthreads=None):
+def _delta(lib, q, k, v, beta_logits, gate_logits, cu_seqlens, scale=1.0, flags=L2NORM_K,
+           init_S=None, nthreads=None):
     """(Gated) delta rule, token by token.  gate_logits None means alpha = 1.
 
     Shapes: q,k [ntok,H,dk]; v [ntok,H,dv]; beta_logits [ntok,H];
@@ -134,15 +189,16 @@ def delta(q, k, v, beta_logits, gate_logits, cu_seqlens, scale=1.0, flags=L2NORM
     o = np.zeros((ntok, H, dv))
     fS = np.zeros((N, H, dk, dv))
     iS = _f64(init_S)
-    rc = _load().la_oracle_delta(_ptr(q), _ptr(k), _ptr(v), _ptr(bl), _ptr(gl), _ptr(o), cup,
-                                 N, H, dk, dv, float(scale), int(flags), _ptr(iS), _ptr(fS),
-                                 nthreads or default_threads())
+    rc = lib.la_oracle_delta(_ptr(q), _ptr(k), _ptr(v), _ptr(bl), _ptr(gl), _ptr(o), cup,
+                             N, H, dk, dv, float(scale), int(flags), _ptr(iS), _ptr(fS),
+                             nthreads or default_threads())
     if rc != 0:
         raise ValueError("la_oracle_delta rejected its arguments")
     return o, fS
 
 
-def decode(q, k, v, beta_logits, gate_logits, state, scale=1.0, flags=L2NORM_K, nthreads=None):
+def _decode(lib, q, k, v, beta_logits, gate_logits, state, scale=1.0, flags=L2NORM_K,
+            nthreads=None):
     """One decode step for N sequences.  q,k [N,H,dk]; v [N,H,dv]; state [N,H,dk,dv].
 
     Returns (o [N,H,dv], new_state) in fp64; the input state is not modified.
@@ -152,7 +208,7 @@ def decode(q, k, v, beta_logits, gate_logits, state, scale=1.0, flags=L2NORM_K, 
     N, H, dk = q.shape
     dv = v.shape[2]
     o = np.zeros((N, H, dv))
-    rc = _load().la_oracle_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(bl), _ptr(gl), _ptr(o),
+    rc = lib.la_oracle_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(bl), _ptr(gl), _ptr(o),
                                   N, H, dk, dv, float(scale), int(flags), _ptr(st),
                                   nthreads or default_threads())
     if rc != 0:
