@@ -353,6 +353,37 @@ def cpu_oracle_throughput(w: wl.Workload, target_s: float, nseq=None):
                       f"{lens[0]} tokens, {passes} pass(es), {el:.1f} s, fp64"}
 
 
+# ------------------------------------------------------------ ncu traffic
+
+def record_traffic(args):
+    """Store per-launch DRAM bytes of the profiled kernel, keyed to the
+    current kernel sources, in profiles/traffic.json."""
+    import csv
+    import re
+    rows = list(csv.reader(open(args.record_traffic)))
+    hdr, units = rows[0], rows[1]
+    name_i = hdr.index("Kernel Name")
+    rd, wr = hdr.index("dram__bytes_read.sum"), hdr.index("dram__bytes_write.sum")
+    scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    found = None
+    for r in rows[2:]:
+        if re.search(args.kernel_regex, r[name_i]):
+            found = (float(r[rd].replace(",", "")) * scale[units[rd]] +
+                     float(r[wr].replace(",", "")) * scale[units[wr]])
+            break
+    if found is None:
+        raise SystemExit("kernel not found in the capture")
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    data = json.load(open(path)) if os.path.exists(path) else {}
+    data[args.traffic_key] = {"source_hash": kernel_source_hash(),
+                              "dram_bytes_per_launch": found * args.launch_scale,
+                              "captured_bytes": found, "launch_scale": args.launch_scale,
+                              "capture": os.path.basename(args.record_traffic)}
+    with open(path, "w") as f:
+        json.dump(data, f, indent=1, sort_keys=True)
+    print(json.dumps(data[args.traffic_key]))
+
+
 # ------------------------------------------------------------ profile cases
 
 def profile_case(args):
@@ -399,6 +430,13 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--record-traffic", default=None, metavar="NCU_RAW_CSV",
+                    help="read dram bytes of one kernel from `ncu -i X --page raw --csv` output "
+                         "and store them in profiles/traffic.json under --traffic-key")
+    ap.add_argument("--traffic-key", default="delta_prefill:" + HEADLINE)
+    ap.add_argument("--kernel-regex", default="delta_chunk_tc")
+    ap.add_argument("--launch-scale", type=float, default=1.0,
+                    help="units of a full launch / units of the captured launch")
     ap.add_argument("--profile-case", default=None,
                     help="run one workload only (for ncu): gpt2_prefill, gated_prefill, "
                          "varlen_prefill, decode, decode_small, gated_small")
@@ -406,6 +444,8 @@ def main():
     if args.profile_case:
         return profile_case(args)
     args.warmup = max(3, args.warmup)
+    if args.record_traffic:
+        return record_traffic(args)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

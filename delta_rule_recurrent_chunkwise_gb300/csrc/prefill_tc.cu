@@ -86,8 +86,8 @@ struct Layout {
     static constexpr uint32_t AQK = X + 8192;           // Aq, bf16 [64][64]
     static constexpr uint32_t SA = X + 16384;           // A, fp32 [64][LDT]
     static constexpr uint32_t ST = SA + 64 * LDT * 4;   // T, fp32 [64][LDT]
-    static constexpr uint32_t SX = ST + 64 * LDT * 4;   // merge temps, fp32 (6 KB)
-    static constexpr uint32_t SB = (SX + 6144 + 1023) & ~1023u;  // S, bf16 [D][D]
+    static constexpr uint32_t SX = ST + 64 * LDT * 4;   // merge temps, fp32 (8 KB)
+    static constexpr uint32_t SB = (SX + 8192 + 1023) & ~1023u;  // S, bf16 [D][D]
     static constexpr uint32_t X_END_A = GATED ? KR + 160 * D * 2 : X;
     static constexpr uint32_t X_END_P = GATED ? PPI + 64 * D * 4 : X;
     static constexpr uint32_t X_END_C = SB + D * D * 2;
@@ -103,17 +103,21 @@ struct Layout {
     static constexpr uint32_t QN = KN + 256;                   // fp32 [64]
     static constexpr uint32_t EB = QN + 256;                   // fp32 [4][D] block decay
     static constexpr uint32_t GEND = EB + 16 * D;              // fp32 [D] chunk decay
+    // fp32 [5][4][D] block constants: live only between the decay scan and
+    // the operand stage, when the raw gate tile has been consumed
+    static constexpr uint32_t KC = RAW_G;
+    static_assert(80 * D <= tile64, "block constants fit in the gate tile");
     static constexpr uint32_t BARS = GEND + 4 * D;             // 2 mbarriers + tmem slot
     static constexpr uint32_t TOTAL = BARS + 64;
     static_assert(TOTAL + 1024 <= 227 * 1024, "shared memory budget");
 };
 
-// TMEM column map.  S: fp32 state (rows = key channels).  U: the delta u.
-// A: block products (phase B only; four 64-column blocks when gated, one
-// otherwise), later O and W.
+// TMEM column map.  S: fp32 state (rows = key channels).  W and U adjacent
+// (one N = 2D product writes both), O after them.  A: the block products
+// (phase B and C1 only, up to 160 columns), reusing W/U/O's columns.
 template <int D>
 struct Cols {
-    static constexpr uint32_t S = 0, U = D, A = 2 * D, O = 2 * D, W = 3 * D;
+    static constexpr uint32_t S = 0, W = D, U = 2 * D, O = 3 * D, A = D;
     static constexpr int MS = D;  // M of the state accumulator
 };
 
@@ -192,6 +196,37 @@ struct TcParams {
 
 __device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
+// ---- warp-level TF32 products for the small blocks of the triangular solve
+// (m16n8k8: A 16x8 row-major, B 8x8 as [k][n], C 16x8; fp32 accumulate).
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const float *A, int lda, const float *B,
+                                         int ldb, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    const uint32_t a0 = to_tf32(A[g * lda + t]), a1 = to_tf32(A[(g + 8) * lda + t]);
+    const uint32_t a2 = to_tf32(A[g * lda + t + 4]), a3 = to_tf32(A[(g + 8) * lda + t + 4]);
+    const uint32_t b0 = to_tf32(B[t * ldb + g]), b1 = to_tf32(B[(t + 4) * ldb + g]);
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// C (16x8 tile at Cp, row stride ldc) = sign * d
+__device__ __forceinline__ void store_c(float *Cp, int ldc, const float (&d)[4], float sign,
+                                        int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    Cp[g * ldc + 2 * t] = sign * d[0];
+    Cp[g * ldc + 2 * t + 1] = sign * d[1];
+    Cp[(g + 8) * ldc + 2 * t] = sign * d[2];
+    Cp[(g + 8) * ldc + 2 * t + 1] = sign * d[3];
+}
+
 template <int D, bool GATED>
 __global__ void __launch_bounds__(NT, 1)
     delta_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -219,6 +254,7 @@ __global__ void __launch_bounds__(NT, 1)
     float *sqn = reinterpret_cast<float *>(sm + L::QN);
     float *sE = reinterpret_cast<float *>(sm + L::EB);
     float *sgend = reinterpret_cast<float *>(sm + L::GEND);
+    float *sKC = reinterpret_cast<float *>(sm + L::KC);
     uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + L::BARS);
     uint64_t *bar_mma = bar_tma + 1;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar_tma + 2);
@@ -316,7 +352,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
         // ---------------------------------------------- A0: beta, row norms
         if (tid < C) {
-            sbeta[tid] = tid < len ? sigmoid_f(beta_next) : 0.0f;
+            sbeta[tid] = tid < len ? __fdividef(1.0f, 1.0f + __expf(-beta_next)) : 0.0f;
             const int tn = cs + C + tid;
             beta_next = tn < t_end ? __bfloat162float(p.beta_logits[(int64_t)tn * H + h]) : 0.0f;
         }
@@ -343,8 +379,8 @@ __global__ void __launch_bounds__(NT, 1)
             }
             if (part == 0) {
                 const bool valid = r < len;
-                skn[r] = valid ? (l2k ? 1.0f / fmaxf(sqrtf(ssk), 1e-12f) : 1.0f) : 0.0f;
-                sqn[r] = valid ? (l2q ? 1.0f / fmaxf(sqrtf(ssq), 1e-12f) : 1.0f) : 0.0f;
+                skn[r] = valid ? (l2k ? rsqrtf(fmaxf(ssk, 1e-24f)) : 1.0f) : 0.0f;
+                sqn[r] = valid ? (l2q ? rsqrtf(fmaxf(ssq, 1e-24f)) : 1.0f) : 0.0f;
             }
         }
         __syncthreads();
@@ -377,109 +413,114 @@ __global__ void __launch_bounds__(NT, 1)
             }
             if (tid < D) sgend[tid] = 1.0f;
         } else {
-            // (a) one thread per (key channel c, 16-token block R): alpha = 1/(1+e^g),
-            // within-block prefix products P and 1/P (fp32 scratch), block totals E_R.
-            if (tid < 4 * D) {
-                const int c = tid % D, R = tid / D;
-                const uint8_t *pg = rawg + (c >> 6) * 8192 + (16 * R) * 128;
-                const uint32_t lo = (uint32_t)(c & 7) * 2u;
-                const int ch = (c >> 3) & 7;
-                float P = 1.0f, Pi = 1.0f;
+            // One thread per (2 key channels, 8 rows of a 16-token block R); the
+            // two 8-row halves of a block sit in lanes l and l^16 of one warp.
+            // alpha = 1/(1+e^g), 1/alpha = 1+e^g; P = prefix product of alpha
+            // inside the block, Pi = 1/P.  Every operand is (q or k) x (P or Pi)
+            // x a per-(block, channel) constant; the within-block suffix is
+            // prod_{t>r} alpha_t = E_R / P_r with E_R the block total.
+            const bool act = warp < D / 8;
+            const int R = (warp * 32 / D) & 3, grp = warp % (D / 32);
+            const int hf2 = lane >> 4, c0 = 32 * grp + 2 * (lane & 15);
+            const int r0 = 16 * R + 8 * hf2;
+            // Addressing: the channel pair is fixed per thread and r0 is a
+            // multiple of 8, so row r0 + rho has swizzle phase rho.
+            const uint32_t cb = (uint32_t)c0 >> 6, ch = ((uint32_t)c0 >> 3) & 7u;
+            const uint32_t cboff64 = cb * 64u * 128u, cboff128 = cb * 128u * 128u,
+                           cboff160 = cb * 160u * 128u;
+            uint32_t swz[8];
 #pragma unroll
-                for (int rho = 0; rho < 16; ++rho) {
-                    const int r = 16 * R + rho;
-                    const float g = fminf(bf(pg + rho * 128 + (((ch ^ (rho & 7)) << 4) + lo)), 80.0f);
-                    const float e = __expf(g);
+            for (int j = 0; j < 8; ++j) swz[j] = ((ch ^ (uint32_t)j) << 4) + ((uint32_t)c0 & 7u) * 2u;
+            float P[8][2], Pi[8][2];
+#pragma unroll
+            for (int rho = 0; rho < 8; ++rho) { P[rho][0] = P[rho][1] = 1.0f; Pi[rho][0] = Pi[rho][1] = 1.0f; }
+            if (act) {
+                float p0 = 1.0f, p1 = 1.0f, q0 = 1.0f, q1 = 1.0f;
+#pragma unroll
+                for (int rho = 0; rho < 8; ++rho) {
+                    const int r = r0 + rho;
+                    const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162 *>(rawg + cboff64 + r * 128 + swz[rho]);
+                    const float2 g = __bfloat1622float2(g2);
+                    const float e0 = __expf(fminf(g.x, 80.0f)), e1 = __expf(fminf(g.y, 80.0f));
                     if (r < len) {
-                        P *= __fdividef(1.0f, 1.0f + e);
-                        Pi = fminf(Pi * (1.0f + e), 1e30f);
+                        p0 *= __fdividef(1.0f, 1.0f + e0);
+                        p1 *= __fdividef(1.0f, 1.0f + e1);
+                        q0 = fminf(q0 * (1.0f + e0), 1e30f);
+                        q1 = fminf(q1 * (1.0f + e1), 1e30f);
                     }
-                    sP[r * D + c] = P;
-                    sPi[r * D + c] = Pi;
+                    P[rho][0] = p0; P[rho][1] = p1; Pi[rho][0] = q0; Pi[rho][1] = q1;
                 }
-                sE[R * D + c] = P;
+            }
+            // carry the first half's totals into the second half
+            {
+                const float t0 = __shfl_sync(0xffffffffu, P[7][0], lane ^ 16);
+                const float t1 = __shfl_sync(0xffffffffu, P[7][1], lane ^ 16);
+                const float u0 = __shfl_sync(0xffffffffu, Pi[7][0], lane ^ 16);
+                const float u1 = __shfl_sync(0xffffffffu, Pi[7][1], lane ^ 16);
+                if (hf2) {
+#pragma unroll
+                    for (int rho = 0; rho < 8; ++rho) {
+                        P[rho][0] *= t0; P[rho][1] *= t1;
+                        Pi[rho][0] = fminf(Pi[rho][0] * u0, 1e30f);
+                        Pi[rho][1] = fminf(Pi[rho][1] * u1, 1e30f);
+                    }
+                }
+            }
+            if (act && hf2) {
+                sE[R * D + c0] = P[7][0];
+                sE[R * D + c0 + 1] = P[7][1];
             }
             __syncthreads();
-            // (b) one thread per (row r, 8 channels): every operand is (q or k) x
-            // (P or 1/P) x a per-(block, channel) constant, using the
-            // within-block suffix prod_{t>r} alpha_t = E_R / P_r.
-            constexpr int UNITS = C * D / 8, UPT = (UNITS + NT - 1) / NT;
-            float vq[UPT][8], vk[UPT][8], vp[UPT][8], vpi[UPT][8];
+            if (act) {
+                float Gb[2], EaK[2], mt[3][2];
 #pragma unroll
-            for (int j = 0; j < UPT; ++j) {
-                const int u = tid + j * NT;
-                if (u < UNITS) {
-                    const int r = u / (D / 8), c8 = (u % (D / 8)) * 8;
-                    unpack8(*reinterpret_cast<const uint4 *>(rawq + rs_off(C, r, c8)), vq[j]);
-                    unpack8(*reinterpret_cast<const uint4 *>(rawk + rs_off(C, r, c8)), vk[j]);
-                    const float4 *pp = reinterpret_cast<const float4 *>(sP + r * D + c8);
-                    const float4 *pi = reinterpret_cast<const float4 *>(sPi + r * D + c8);
-                    const float4 a0 = pp[0], a1 = pp[1], b0 = pi[0], b1 = pi[1];
-                    vp[j][0] = a0.x; vp[j][1] = a0.y; vp[j][2] = a0.z; vp[j][3] = a0.w;
-                    vp[j][4] = a1.x; vp[j][5] = a1.y; vp[j][6] = a1.z; vp[j][7] = a1.w;
-                    vpi[j][0] = b0.x; vpi[j][1] = b0.y; vpi[j][2] = b0.z; vpi[j][3] = b0.w;
-                    vpi[j][4] = b1.x; vpi[j][5] = b1.y; vpi[j][6] = b1.z; vpi[j][7] = b1.w;
+                for (int j = 0; j < 2; ++j) {
+                    const int c = c0 + j;
+                    const float E0 = sE[c], E1 = sE[D + c], E2 = sE[2 * D + c], E3 = sE[3 * D + c];
+                    Gb[j] = R == 0 ? 1.0f : R == 1 ? E0 : R == 2 ? E0 * E1 : E0 * E1 * E2;
+                    EaK[j] = R == 0 ? E0 * E1 * E2 * E3 : R == 1 ? E1 * E2 * E3 : R == 2 ? E2 * E3 : E3;
+                    float m = 1.0f;
+#pragma unroll
+                    for (int t = 0; t < 3; ++t) {
+                        const int Rt = R + t;
+                        m *= Rt == 0 ? E0 : Rt == 1 ? E1 : Rt == 2 ? E2 : E3;
+                        mt[t][j] = m;
+                    }
+                    if (R == 0 && hf2 == 0) sgend[c] = E0 * E1 * E2 * E3;
                 }
-            }
-            __syncthreads();  // P / 1/P scratch overlaps the outputs below
+                auto st2 = [](uint8_t *p, float a, float b) {
+                    *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(a, b);
+                };
+                uint8_t *const pq_raw = rawq + cboff64, *const pk_raw = rawk + cboff64;
+                uint8_t *const p_qh = qkh + cboff128, *const p_kh = qkh + cboff128 + 64 * 128;
+                uint8_t *const p_qg = pair + cboff128, *const p_kt = pair + cboff128 + 64 * 128;
+                uint8_t *const p_bk = bkg + cboff64, *const p_kr = kr + cboff160;
 #pragma unroll
-            for (int j = 0; j < UPT; ++j) {
-                const int u = tid + j * NT;
-                if (u < UNITS) {
-                    const int r = u / (D / 8), c8 = (u % (D / 8)) * 8, R = r >> 4;
-                    const float kn = skn[r], qn = sqn[r], be = sbeta[r];
-                    float o1[8], o2[8], o3[8], o4[8], o5[8], o6[8];
-                    float mk[3][8];
-                    float Ev[4][8];
-#pragma unroll
-                    for (int R2 = 0; R2 < 4; ++R2) {
-                        const float4 e0 = *reinterpret_cast<const float4 *>(sE + R2 * D + c8);
-                        const float4 e1 = *reinterpret_cast<const float4 *>(sE + R2 * D + c8 + 4);
-                        Ev[R2][0] = e0.x; Ev[R2][1] = e0.y; Ev[R2][2] = e0.z; Ev[R2][3] = e0.w;
-                        Ev[R2][4] = e1.x; Ev[R2][5] = e1.y; Ev[R2][6] = e1.z; Ev[R2][7] = e1.w;
+                for (int rho = 0; rho < 8; ++rho) {
+                    const int r = r0 + rho;
+                    const uint32_t o = (uint32_t)r * 128u + swz[rho];
+                    float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(pq_raw + o));
+                    float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(pk_raw + o));
+                    if (silu) {
+                        qv.x = silu_fast(qv.x); qv.y = silu_fast(qv.y);
+                        kv.x = silu_fast(kv.x); kv.y = silu_fast(kv.y);
                     }
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float E0 = Ev[0][i], E1 = Ev[1][i], E2 = Ev[2][i], E3 = Ev[3][i];
-                        const float Gb = R == 0 ? 1.0f : R == 1 ? E0 : R == 2 ? E0 * E1 : E0 * E1 * E2;
-                        const float EaK = R == 0 ? E0 * E1 * E2 * E3 : R == 1 ? E1 * E2 * E3 : R == 2 ? E2 * E3 : E3;
-                        float qv = vq[j][i], kv = vk[j][i];
-                        if (silu) { qv = silu_fast(qv); kv = silu_fast(kv); }
-                        qv *= qn;
-                        kv *= kn;
-                        const float P = vp[j][i], Pi = vpi[j][i];
-                        o1[i] = qv * P;                 // Q^
-                        o2[i] = kv * P;                 // K^
-                        o3[i] = o1[i] * Gb;             // Q e^b
-                        o4[i] = be * o2[i] * Gb;        // beta K e^b
-                        o5[i] = kv * Pi;                // K_R, own block
-                        o6[i] = o5[i] * EaK;            // K e^{b_end - b}
-                        // K_R' for R' = R+1+t: k / P_r * prod_{R <= R'' < R'} E_R''
-                        float f = o5[i];
-#pragma unroll
-                        for (int t = 0; t < 3; ++t) {
-                            const int Rt = R + t;
-                            f *= Rt == 0 ? E0 : Rt == 1 ? E1 : Rt == 2 ? E2 : E3;
-                            mk[t][i] = f;
-                        }
-                    }
-                    *reinterpret_cast<uint4 *>(qkh + rs_off(128, r, c8)) = pack8(o1);
-                    *reinterpret_cast<uint4 *>(qkh + rs_off(128, 64 + r, c8)) = pack8(o2);
-                    *reinterpret_cast<uint4 *>(pair + rs_off(128, r, c8)) = pack8(o3);
-                    *reinterpret_cast<uint4 *>(pair + rs_off(128, 64 + r, c8)) = pack8(o6);
-                    *reinterpret_cast<uint4 *>(bkg + rs_off(C, r, c8)) = pack8(o4);
-                    *reinterpret_cast<uint4 *>(kr + rs_off(160, 8 * R * (R + 1) + r, c8)) = pack8(o5);
+                    const float qn = sqn[r], kn = skn[r], be = sbeta[r];
+                    qv.x *= qn; qv.y *= qn; kv.x *= kn; kv.y *= kn;
+                    const float a0 = qv.x * P[rho][0], a1 = qv.y * P[rho][1];     // Q^
+                    const float b0 = kv.x * P[rho][0], b1 = kv.y * P[rho][1];     // K^
+                    const float k0 = kv.x * Pi[rho][0], k1 = kv.y * Pi[rho][1];   // K_R own block
+                    st2(p_qh + o, a0, a1);
+                    st2(p_kh + o, b0, b1);
+                    st2(p_qg + o, a0 * Gb[0], a1 * Gb[1]);                  // Q e^b
+                    st2(p_kt + o, k0 * EaK[0], k1 * EaK[1]);                // K e^{b_end-b}
+                    st2(p_bk + o, be * b0 * Gb[0], be * b1 * Gb[1]);        // beta K e^b
+                    st2(p_kr + (uint32_t)(8 * R * (R + 1)) * 128u + o, k0, k1);
 #pragma unroll
                     for (int t = 0; t < 3; ++t) {
                         const int R2 = R + 1 + t;
                         if (R2 < 4)
-                            *reinterpret_cast<uint4 *>(kr + rs_off(160, 8 * R2 * (R2 + 1) + r, c8)) =
-                                pack8(mk[t]);
-                    }
-                    if (r == 0) {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            sgend[c8 + i] = sE[c8 + i] * sE[D + c8 + i] * sE[2 * D + c8 + i] * sE[3 * D + c8 + i];
+                            st2(p_kr + (uint32_t)(8 * R2 * (R2 + 1)) * 128u + o, k0 * mt[t][0], k1 * mt[t][1]);
                     }
                 }
             }
@@ -505,12 +546,12 @@ __global__ void __launch_bounds__(NT, 1)
         if (tid == 0) {
             constexpr uint32_t id = idesc_bf16(128, 64, false, false);
             if (GATED) {
+                // the packed K_R tile is one 160-row operand: all four block
+                // products in one N = 160 product (block R at column 8R(R+1))
+                constexpr uint32_t id160 = idesc_bf16(128, 160, false, false);
 #pragma unroll
-                for (int R = 0; R < 4; ++R)
-#pragma unroll
-                    for (int s = 0; s < D / 16; ++s)
-                        mma_bf16(tmem + TC::A + 64 * R, kdesc(qkh, 128, 0, s),
-                                 kdesc(kr, 160, 8 * R * (R + 1), s), id, s > 0);
+                for (int s = 0; s < D / 16; ++s)
+                    mma_bf16(tmem + TC::A, kdesc(qkh, 128, 0, s), kdesc(kr, 160, 0, s), id160, s > 0);
             } else {
 #pragma unroll
                 for (int s = 0; s < D / 16; ++s)
@@ -520,156 +561,153 @@ __global__ void __launch_bounds__(NT, 1)
             mma_commit(bar_mma);
         }
         if (__syncthreads_or(!mma_wait())) { failed = true; break; }
-        // ---------------------------------------------- C1: Aq tile, A rows
+        // ---------------------------------------------- C1: Aq tile, A rows, T_RR, S to bf16
         // TMEM lanes 0..63 hold rows of Aq, lanes 64..127 rows of A (before
-        // beta).  Gated: row r of block R = r/16 sits in columns 64 R + i.
-        // Each warp reads 16 columns (part cp) of its quarter; a warp spans
-        // two blocks, so it reads both and each lane keeps its own (TMEM
-        // addresses stay warp-uniform).
+        // beta).  Gated: block R's product sits at column 8R(R+1).  A warp
+        // spans two blocks, so it reads both (TMEM addresses stay
+        // warp-uniform) and each lane keeps its own.
+        //  - every warp: 16 columns (part cp) of its quarter -> Aq tile / A rows
+        //  - warps 2, 3 then invert the diagonal 16x16 blocks, read straight
+        //    from TMEM: T_RR = (I + A_RR)^{-1}, lane rho of each 16-lane group
+        //    owning row rho (forward substitution with shuffles)
+        //  - warps 8..15 then copy S to its bf16 operand tile and apply this
+        //    chunk's decay e^{b_end} to S in place
         {
             const bool is_q = qd < 2;
-            const int r = 32 * (is_q ? qd : qd - 2) + lane, R = r >> 4;
-            const int col = 16 * cp;
-            float v[16];
-            if (GATED) {
-                float w0[16], w1[16];
-                const int Rw = (32 * (is_q ? qd : qd - 2)) >> 4;
-                tmem_ld16(tq + TC::A + 64 * Rw + col, w0);
-                tmem_ld16(tq + TC::A + 64 * (Rw + 1) + col, w1);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = (R == Rw) ? w0[i] : w1[i];
-            } else {
-                tmem_ld16(tq + TC::A + col, v);
-            }
-            if (is_q) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    if (col + i > r) v[i] = 0.0f;
-                st_bf16x8(aqk, 64, r, col, v);
-                st_bf16x8(aqk, 64, r, col + 8, v + 8);
-            } else {
-                const float be = sbeta[r];
-                float4 *dst = reinterpret_cast<float4 *>(sA + r * LDT + col);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    float4 f;
-                    f.x = (col + 4 * i + 0 < r) ? be * v[4 * i + 0] : 0.0f;
-                    f.y = (col + 4 * i + 1 < r) ? be * v[4 * i + 1] : 0.0f;
-                    f.z = (col + 4 * i + 2 < r) ? be * v[4 * i + 2] : 0.0f;
-                    f.w = (col + 4 * i + 3 < r) ? be * v[4 * i + 3] : 0.0f;
-                    dst[i] = f;
-                }
-            }
-        }
-        __syncthreads();
-        // ---------------------------------------------- C1b: diagonal inverses; S to bf16
-        // Warps 0,1: T_RR = (I + A_RR)^{-1}, lane rho of each 16-lane group owns
-        // row rho.  Warps 8..15 meanwhile copy S (TMEM, fp32) to its bf16
-        // operand tile and apply this chunk's decay e^{b_end} to S in place.
-        if (warp < 2) {
-            const int r = 32 * warp + lane, R = r >> 4, rho = r & 15;
-            float dg[16], t[16];
-#pragma unroll
-            for (int m = 0; m < 16; m += 4) {
-                const float4 f = *reinterpret_cast<const float4 *>(sA + r * LDT + 16 * R + m);
-                dg[m] = f.x; dg[m + 1] = f.y; dg[m + 2] = f.z; dg[m + 3] = f.w;
-            }
-#pragma unroll
-            for (int j = 0; j < 16; ++j) t[j] = (j == rho) ? 1.0f : 0.0f;
-            const int gbase = lane & 16;
-#pragma unroll
-            for (int m = 0; m < 15; ++m) {
-#pragma unroll
-                for (int j = 0; j <= m; ++j) {
-                    const float tm = __shfl_sync(0xffffffffu, t[j], gbase + m);
-                    if (rho > m) t[j] -= dg[m] * tm;
-                }
-            }
-            float4 *dst = reinterpret_cast<float4 *>(sT + r * LDT);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) dst[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int j = 0; j < 16; j += 4) dst[(16 * R + j) >> 2] = make_float4(t[j], t[j + 1], t[j + 2], t[j + 3]);
-        } else if (warp >= 8) {
-            const int c = acc_row(TC::MS, qd, lane);
-            const float gd = c >= 0 ? sgend[c] : 1.0f;
-            const int half = (warp >> 2) & 1;
-#pragma unroll
-            for (int cb = 0; cb < D / 2; cb += 16) {
-                const int col = half * (D / 2) + cb;
+            const int rb0 = 32 * (is_q ? qd : qd - 2);
+            const int r = rb0 + lane, R = r >> 4, rho = r & 15;
+            const int Rw = rb0 >> 4;
+            auto colof = [](int Rb) { return GATED ? 8 * Rb * (Rb + 1) : 0; };
+            {
+                const int col = 16 * cp;
                 float v[16];
-                tmem_ld16(tq + TC::S + col, v);
-                if (c >= 0) {
-                    st_bf16x8(sb, D, c, col, v);
-                    st_bf16x8(sb, D, c, col + 8, v + 8);
-                }
                 if (GATED) {
+                    float w0[16], w1[16];
+                    // parts beyond a block's product are masked below (col + i > r)
+                    tmem_ld16(tq + TC::A + colof(Rw) + col, w0);
+                    tmem_ld16(tq + TC::A + colof(Rw + 1) + col, w1);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] *= gd;
-                    tmem_st16(tq + TC::S + col, v);
+                    for (int i = 0; i < 16; ++i) v[i] = (R == Rw) ? w0[i] : w1[i];
+                } else {
+                    tmem_ld16(tq + TC::A + col, v);
+                }
+                if (is_q) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (col + i > r) v[i] = 0.0f;
+                    st_bf16x8(aqk, 64, r, col, v);
+                    st_bf16x8(aqk, 64, r, col + 8, v + 8);
+                } else {
+                    const float be = sbeta[r];
+                    float4 *dst = reinterpret_cast<float4 *>(sA + r * LDT + col);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        float4 f;
+                        f.x = (col + 4 * i + 0 < r) ? be * v[4 * i + 0] : 0.0f;
+                        f.y = (col + 4 * i + 1 < r) ? be * v[4 * i + 1] : 0.0f;
+                        f.z = (col + 4 * i + 2 < r) ? be * v[4 * i + 2] : 0.0f;
+                        f.w = (col + 4 * i + 3 < r) ? be * v[4 * i + 3] : 0.0f;
+                        dst[i] = f;
+                    }
+                }
+            }
+            if (warp == 2 || warp == 3) {
+                float w0[16], w1[16], dg[16], t[16];
+                tmem_ld16(tq + TC::A + colof(Rw) + 16 * Rw, w0);
+                tmem_ld16(tq + TC::A + colof(Rw + 1) + 16 * (Rw + 1), w1);
+                const float be = sbeta[r];
+#pragma unroll
+                for (int m = 0; m < 16; ++m) dg[m] = (m < rho) ? be * ((R == Rw) ? w0[m] : w1[m]) : 0.0f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) t[j] = (j == rho) ? 1.0f : 0.0f;
+                const int gbase = lane & 16;
+#pragma unroll
+                for (int m = 0; m < 15; ++m) {
+#pragma unroll
+                    for (int j = 0; j <= m; ++j) {
+                        const float tm = __shfl_sync(0xffffffffu, t[j], gbase + m);
+                        if (rho > m) t[j] -= dg[m] * tm;
+                    }
+                }
+                float4 *dst = reinterpret_cast<float4 *>(sT + r * LDT);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) dst[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < 16; j += 4) dst[(16 * R + j) >> 2] = make_float4(t[j], t[j + 1], t[j + 2], t[j + 3]);
+            } else if (warp >= 8) {
+                const int c = acc_row(TC::MS, qd, lane);
+                const float gd = c >= 0 ? sgend[c] : 1.0f;
+                const int half = (warp >> 2) & 1;
+#pragma unroll
+                for (int cb = 0; cb < D / 2; cb += 16) {
+                    const int col = half * (D / 2) + cb;
+                    float v[16];
+                    tmem_ld16(tq + TC::S + col, v);
+                    if (c >= 0) {
+                        st_bf16x8(sb, D, c, col, v);
+                        st_bf16x8(sb, D, c, col + 8, v + 8);
+                    }
+                    if (GATED) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] *= gd;
+                        tmem_st16(tq + TC::S + col, v);
+                    }
                 }
             }
         }
         __syncthreads();
         // ---------------------------------------------- C2: off-diagonal blocks of T
-        // Two merges.  (1) T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22.
+        // Two merges, as warp-level TF32 products (the blocks are 16 and 32
+        // wide; T is rounded to bf16 afterwards, coarser than TF32).
+        // (1) T_10 = -T_11 (A_10 T_00), T_32 = -T_33 (A_32 T_22)   (warps 0, 1)
         // (2) with T_TT = T[0:32,0:32], T_BB = T[32:64,32:64]:
-        //     T[32:64, 0:32] = -T_BB (A[32:64, 0:32] T_TT).
-        // Each thread produces four adjacent outputs (float4) of one row.
+        //     T[32:64, 0:32] = -T_BB (A[32:64, 0:32] T_TT)           (warps 0..7)
         {
-            float *sX1 = sX;          // [2][16][16]
-            float *sY = sX + 512;     // [32][32]
-            const int b = tid >> 6, i1 = (tid >> 2) & 15, jq1 = tid & 3;   // merge 1: 128 threads
-            const int R1 = 1 + 2 * b, J1 = 2 * b;
-            if (tid < 128) {
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                const float *arow = sA + (16 * R1 + i1) * LDT + 16 * J1;
+            constexpr int LX = 24, LY = 40;
+            float *sX1 = sX;                 // [2][16][LX]
+            float *sY = sX + 2 * 16 * LX;    // [32][LY]
+            if (warp < 2) {
+                const int b = warp, R = 1 + 2 * b, J = 2 * b;
+                float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    const float a = arow[m];
-                    const float4 t4 = *reinterpret_cast<const float4 *>(sT + (16 * J1 + m) * LDT + 16 * J1 + 4 * jq1);
-                    acc.x += a * t4.x; acc.y += a * t4.y; acc.z += a * t4.z; acc.w += a * t4.w;
+                for (int ks = 0; ks < 2; ++ks) {
+                    const float *Ab = sA + (16 * R) * LDT + 16 * J + 8 * ks;
+                    const float *Bb = sT + (16 * J + 8 * ks) * LDT + 16 * J;
+                    mma_tf32(d0, Ab, LDT, Bb, LDT, lane);
+                    mma_tf32(d1, Ab, LDT, Bb + 8, LDT, lane);
                 }
-                *reinterpret_cast<float4 *>(sX1 + (b * 16 + i1) * 16 + 4 * jq1) = acc;
+                store_c(sX1 + b * 16 * LX, LX, d0, 1.0f, lane);
+                store_c(sX1 + b * 16 * LX + 8, LX, d1, 1.0f, lane);
+                __syncwarp();
+                float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    const float *Ab = sT + (16 * R) * LDT + 16 * R + 8 * ks;
+                    const float *Bb = sX1 + b * 16 * LX + (8 * ks) * LX;
+                    mma_tf32(e0, Ab, LDT, Bb, LX, lane);
+                    mma_tf32(e1, Ab, LDT, Bb + 8, LX, lane);
+                }
+                store_c(sT + (16 * R) * LDT + 16 * J, LDT, e0, -1.0f, lane);
+                store_c(sT + (16 * R) * LDT + 16 * J + 8, LDT, e1, -1.0f, lane);
             }
             __syncthreads();
-            if (tid < 128) {
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                const float *trow = sT + (16 * R1 + i1) * LDT + 16 * R1;
+            const int mt = (warp >> 2) & 1, nt = warp & 3;
+            if (warp < 8) {
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    const float a = trow[m];
-                    const float4 x4 = *reinterpret_cast<const float4 *>(sX1 + (b * 16 + m) * 16 + 4 * jq1);
-                    acc.x += a * x4.x; acc.y += a * x4.y; acc.z += a * x4.z; acc.w += a * x4.w;
-                }
-                *reinterpret_cast<float4 *>(sT + (16 * R1 + i1) * LDT + 16 * J1 + 4 * jq1) =
-                    make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_tf32(d, sA + (32 + 16 * mt) * LDT + 8 * ks, LDT,
+                             sT + (8 * ks) * LDT + 8 * nt, LDT, lane);
+                store_c(sY + (16 * mt) * LY + 8 * nt, LY, d, 1.0f, lane);
             }
             __syncthreads();
-            const int i2 = tid >> 3, jq2 = tid & 7;                         // merge 2: 256 threads
-            if (tid < 256) {
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                const float *arow = sA + (32 + i2) * LDT;
+            if (warp < 8) {
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int m = 0; m < 32; ++m) {
-                    const float a = arow[m];
-                    const float4 t4 = *reinterpret_cast<const float4 *>(sT + m * LDT + 4 * jq2);
-                    acc.x += a * t4.x; acc.y += a * t4.y; acc.z += a * t4.z; acc.w += a * t4.w;
-                }
-                *reinterpret_cast<float4 *>(sY + i2 * 32 + 4 * jq2) = acc;
-            }
-            __syncthreads();
-            if (tid < 256) {
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                const float *trow = sT + (32 + i2) * LDT + 32;
-#pragma unroll
-                for (int m = 0; m < 32; ++m) {
-                    const float a = trow[m];
-                    const float4 y4 = *reinterpret_cast<const float4 *>(sY + m * 32 + 4 * jq2);
-                    acc.x += a * y4.x; acc.y += a * y4.y; acc.z += a * y4.z; acc.w += a * y4.w;
-                }
-                *reinterpret_cast<float4 *>(sT + (32 + i2) * LDT + 4 * jq2) =
-                    make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_tf32(d, sT + (32 + 16 * mt) * LDT + 32 + 8 * ks, LDT,
+                             sY + (8 * ks) * LY + 8 * nt, LY, lane);
+                store_c(sT + (32 + 16 * mt) * LDT + 8 * nt, LDT, d, -1.0f, lane);
             }
             __syncthreads();
         }
@@ -681,13 +719,12 @@ __global__ void __launch_bounds__(NT, 1)
         phase_sync();
         // ---------------------------------------------- D: W = T (beta K e^b), u = T (beta V)
         if (tid == 0) {
-            constexpr uint32_t id = idesc_bf16(64, D, false, true);
+            // beta K e^b and beta V are adjacent column blocks: one N = 2D
+            // product writes W (columns W) and U (columns U = W + D)
+            constexpr uint32_t id = idesc_bf16(64, 2 * D, false, true);
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t a = kdesc(t16, 64, 0, s);
-                mma_bf16(tmem + TC::W, a, mdesc(bkg, C, 0, s), id, s > 0);
-                mma_bf16(tmem + TC::U, a, mdesc(bv, C, 0, s), id, s > 0);
-            }
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tmem + TC::W, kdesc(t16, 64, 0, s), mdesc(bkg, C, 0, s), id, s > 0);
             mma_commit(bar_mma);
         }
         if (__syncthreads_or(!mma_wait())) { failed = true; break; }
