@@ -77,10 +77,18 @@ def decode_state_bytes(w: wl.Workload):
     return 8 * w.n_seq * w.H * w.dk * w.dv   # fp32 state read + written once per step
 
 
-def kernel_source_hash():
+KERNEL_SOURCES = {
+    "delta_prefill": ("prefill_tc.cu", "tc.cuh", "common.cuh", "launch.h"),
+    "decode": ("decode.cu", "common.cuh", "launch.h"),
+}
+
+
+def kernel_source_hash(key: str) -> str:
+    """Hash of the source files a kernel is built from (its ncu figures go
+    stale when any of them changes)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "delta_rule_recurrent_chunkwise_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in KERNEL_SOURCES[key.split(":")[0]]:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
@@ -94,7 +102,7 @@ def ncu_traffic(kernel_key: str):
         with open(path) as f:
             t = json.load(f)
         e = t[kernel_key]
-        if e.get("source_hash") != kernel_source_hash():
+        if e.get("source_hash") != kernel_source_hash(kernel_key):
             return None
         return float(e["dram_bytes_per_launch"])
     except Exception:
@@ -375,7 +383,7 @@ def record_traffic(args):
         raise SystemExit("kernel not found in the capture")
     path = os.path.join(ROOT, "profiles", "traffic.json")
     data = json.load(open(path)) if os.path.exists(path) else {}
-    data[args.traffic_key] = {"source_hash": kernel_source_hash(),
+    data[args.traffic_key] = {"source_hash": kernel_source_hash(args.traffic_key),
                               "dram_bytes_per_launch": found * args.launch_scale,
                               "captured_bytes": found, "launch_scale": args.launch_scale,
                               "capture": os.path.basename(args.record_traffic)}

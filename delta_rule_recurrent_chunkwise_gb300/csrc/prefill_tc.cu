@@ -183,6 +183,13 @@ __device__ __forceinline__ int acc_row(int M, int q, int lane) {
     return lane < 16 ? 16 * q + lane : -1;
 }
 
+// NC (16 or 32) consecutive TMEM columns of this thread's lane, one wait.
+template <int NC>
+__device__ __forceinline__ void tmem_cols(uint32_t taddr, float (&v)[NC]) {
+    if constexpr (NC == 32) tmem_ld32(taddr, v);
+    else tmem_ld16(taddr, v);
+}
+
 struct TcParams {
     const __nv_bfloat16 *beta_logits;
     __nv_bfloat16 *o;
@@ -423,6 +430,10 @@ __global__ void __launch_bounds__(NT, 1)
             const int R = (warp * 32 / D) & 3, grp = warp % (D / 32);
             const int hf2 = lane >> 4, c0 = 32 * grp + 2 * (lane & 15);
             const int r0 = 16 * R + 8 * hf2;
+            // Rows r0 and r0 + 8 share a swizzle phase, so at step rho the
+            // second-half lanes work on row r0 + (rho ^ 4): the two halves of
+            // the warp then hit disjoint banks.
+            const int pr = 4 * hf2;
             // Addressing: the channel pair is fixed per thread and r0 is a
             // multiple of 8, so row r0 + rho has swizzle phase rho.
             const uint32_t cb = (uint32_t)c0 >> 6, ch = ((uint32_t)c0 >> 3) & 7u;
@@ -438,6 +449,8 @@ __global__ void __launch_bounds__(NT, 1)
                 float p0 = 1.0f, p1 = 1.0f, q0 = 1.0f, q1 = 1.0f;
 #pragma unroll
                 for (int rho = 0; rho < 8; ++rho) {
+                    // the scan runs in natural row order (a prefix product);
+                    // only the store pass below uses the permuted order
                     const int r = r0 + rho;
                     const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162 *>(rawg + cboff64 + r * 128 + swz[rho]);
                     const float2 g = __bfloat1622float2(g2);
@@ -495,10 +508,22 @@ __global__ void __launch_bounds__(NT, 1)
                 uint8_t *const p_qh = qkh + cboff128, *const p_kh = qkh + cboff128 + 64 * 128;
                 uint8_t *const p_qg = pair + cboff128, *const p_kt = pair + cboff128 + 64 * 128;
                 uint8_t *const p_bk = bkg + cboff64, *const p_kr = kr + cboff160;
+                // second-half lanes: swap register rows rho <-> rho ^ 4 so the
+                // store pass can index P[rho] with a compile-time rho
+                if (pr) {
+#pragma unroll
+                    for (int rho = 0; rho < 4; ++rho) {
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            float t = P[rho][j]; P[rho][j] = P[rho + 4][j]; P[rho + 4][j] = t;
+                            t = Pi[rho][j]; Pi[rho][j] = Pi[rho + 4][j]; Pi[rho + 4][j] = t;
+                        }
+                    }
+                }
 #pragma unroll
                 for (int rho = 0; rho < 8; ++rho) {
-                    const int r = r0 + rho;
-                    const uint32_t o = (uint32_t)r * 128u + swz[rho];
+                    const int r = r0 + (rho ^ pr);
+                    const uint32_t o = (uint32_t)r * 128u + (((ch ^ (uint32_t)(rho ^ pr)) << 4) + ((uint32_t)c0 & 7u) * 2u);
                     float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(pq_raw + o));
                     float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(pk_raw + o));
                     if (silu) {
@@ -639,18 +664,19 @@ __global__ void __launch_bounds__(NT, 1)
                 const float gd = c >= 0 ? sgend[c] : 1.0f;
                 const int half = (warp >> 2) & 1;
 #pragma unroll
-                for (int cb = 0; cb < D / 2; cb += 16) {
+                for (int cb = 0; cb < D / 2; cb += 32) {
                     const int col = half * (D / 2) + cb;
-                    float v[16];
-                    tmem_ld16(tq + TC::S + col, v);
+                    float v[32];
+                    tmem_ld32(tq + TC::S + col, v);
                     if (c >= 0) {
-                        st_bf16x8(sb, D, c, col, v);
-                        st_bf16x8(sb, D, c, col + 8, v + 8);
+#pragma unroll
+                        for (int i = 0; i < 32; i += 8) st_bf16x8(sb, D, c, col + i, v + i);
                     }
                     if (GATED) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] *= gd;
-                        tmem_st16(tq + TC::S + col, v);
+                        for (int i = 0; i < 32; ++i) v[i] *= gd;
+                        tmem_st16(tq + TC::S + col, *reinterpret_cast<float(*)[16]>(v));
+                        tmem_st16(tq + TC::S + col + 16, *reinterpret_cast<float(*)[16]>(v + 16));
                     }
                 }
             }
@@ -731,14 +757,15 @@ __global__ void __launch_bounds__(NT, 1)
         // ---------------------------------------------- E: W tile
         {
             const int r = acc_row(64, qd, lane);
+            constexpr int NC = DQ >= 32 ? 32 : 16;
 #pragma unroll
-            for (int cb = 0; cb < DQ; cb += 16) {
+            for (int cb = 0; cb < DQ; cb += NC) {
                 const int col = cp * DQ + cb;
-                float v[16];
-                tmem_ld16(tq + TC::W + col, v);
+                float v[NC];
+                tmem_cols<NC>(tq + TC::W + col, v);
                 if (r >= 0) {
-                    st_bf16x8(wt, C, r, col, v);
-                    st_bf16x8(wt, C, r, col + 8, v + 8);
+#pragma unroll
+                    for (int i = 0; i < NC; i += 8) st_bf16x8(wt, C, r, col + i, v + i);
                 }
             }
         }
@@ -759,14 +786,15 @@ __global__ void __launch_bounds__(NT, 1)
         // ---------------------------------------------- G: u tile
         {
             const int r = acc_row(64, qd, lane);
+            constexpr int NC = DQ >= 32 ? 32 : 16;
 #pragma unroll
-            for (int cb = 0; cb < DQ; cb += 16) {
+            for (int cb = 0; cb < DQ; cb += NC) {
                 const int col = cp * DQ + cb;
-                float v[16];
-                tmem_ld16(tq + TC::U + col, v);
+                float v[NC];
+                tmem_cols<NC>(tq + TC::U + col, v);
                 if (r >= 0) {
-                    st_bf16x8(ut, C, r, col, v);
-                    st_bf16x8(ut, C, r, col + 8, v + 8);
+#pragma unroll
+                    for (int i = 0; i < NC; i += 8) st_bf16x8(ut, C, r, col + i, v + i);
                 }
             }
         }
@@ -789,17 +817,18 @@ __global__ void __launch_bounds__(NT, 1)
             const int r = acc_row(64, qd, lane);
             const bool valid = r >= 0 && r < len;
             __nv_bfloat16 *orow = p.o + ((int64_t)(cs + (r < 0 ? 0 : r)) * H + h) * D;
+            constexpr int NC = DQ >= 32 ? 32 : 16;
 #pragma unroll
-            for (int cb = 0; cb < DQ; cb += 16) {
+            for (int cb = 0; cb < DQ; cb += NC) {
                 const int col = cp * DQ + cb;
-                float v[16];
-                tmem_ld16(tq + TC::O + col, v);
+                float v[NC];
+                tmem_cols<NC>(tq + TC::O + col, v);
                 if (valid) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] *= p.scale;
+                    for (int i = 0; i < NC; ++i) v[i] *= p.scale;
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + col);
-                    dst[0] = pack8(v);
-                    dst[1] = pack8(v + 8);
+#pragma unroll
+                    for (int i = 0; i < NC / 8; ++i) dst[i] = pack8(v + 8 * i);
                 }
             }
         }
