@@ -175,6 +175,11 @@ __device__ __forceinline__ uint64_t mdesc(const uint8_t *tile, int rows, int row
                            (uint32_t)rows * 128u, 1024);
 }
 
+// Descriptor of the same operand `units` x 16 bytes further on: the start
+// address occupies the low 14 bits and never carries out of them here
+// (shared-memory addresses are below 256 KB).
+__device__ __forceinline__ uint64_t dstep(uint64_t d, uint32_t units) { return d + units; }
+
 // Row of a TMEM accumulator held by this thread (lane quarter q = warp % 4),
 // or -1.  M = 128: row = lane; M = 64: rows 16q..16q+15 sit in lanes 0..15
 // of quarter q.
@@ -333,10 +338,13 @@ __global__ void __launch_bounds__(NT, 1)
     if (tid < C && t_begin + tid < t_end)
         beta_next = __bfloat162float(p.beta_logits[(int64_t)(t_begin + tid) * H + h]);
 
+    // One thread waits on an mbarrier; the CTA barrier that follows every
+    // wait (a __syncthreads_or carrying the outcome) releases the others,
+    // who then order their tensor-memory accesses after it.
     auto mma_wait = [&]() -> bool {
-        const bool ok = mbar_wait(bar_mma, mma_par, &g_tc_error, 2);
+        bool ok = true;
+        if (tid == 0) ok = mbar_wait(bar_mma, mma_par, &g_tc_error, 2);
         mma_par ^= 1;
-        tc_fence_after();
         return ok;
     };
     auto phase_sync = [&]() {
@@ -350,7 +358,7 @@ __global__ void __launch_bounds__(NT, 1)
         const int len = min(C, t_end - cs);
         // ---------------------------------------------- raw tiles of this chunk
         {
-            const bool ok = mbar_wait(bar_tma, tma_par, &g_tc_error, 1);
+            const bool ok = tid == 0 ? mbar_wait(bar_tma, tma_par, &g_tc_error, 1) : true;
             tma_par ^= 1;
             tma_pending = false;
             tc_fence_before();
@@ -568,24 +576,27 @@ __global__ void __launch_bounds__(NT, 1)
             tma_pending = true;
         }
         // ---------------------------------------------- B: block products
+        // Issue loops are kept rolled and short: this code runs on one thread,
+        // so every instruction of it is fetched without help from other warps.
         if (tid == 0) {
-            constexpr uint32_t id = idesc_bf16(128, 64, false, false);
-            if (GATED) {
-                // the packed K_R tile is one 160-row operand: all four block
-                // products in one N = 160 product (block R at column 8R(R+1))
-                constexpr uint32_t id160 = idesc_bf16(128, 160, false, false);
+            // gated: the packed K_R tile is one 160-row operand, so all four block
+            // products form one N = 160 product (block R at column 8R(R+1));
+            // ungated: one product [q^; k^] x k^T (N = 64)
+            const uint32_t id = GATED ? idesc_bf16(128, 160, false, false) : idesc_bf16(128, 64, false, false);
+            const uint32_t bRows = GATED ? 160u : 128u;
+            const uint64_t a0 = GATED ? kdesc(qkh, 128, 0, 0) : kdesc(pair, 128, 0, 0);
+            const uint64_t b0 = GATED ? kdesc(kr, 160, 0, 0) : kdesc(pair, 128, 64, 0);
+#pragma unroll 1
+            for (int kb = 0; kb < D / 64; ++kb) {
 #pragma unroll
-                for (int s = 0; s < D / 16; ++s)
-                    mma_bf16(tmem + TC::A, kdesc(qkh, 128, 0, s), kdesc(kr, 160, 0, s), id160, s > 0);
-            } else {
-#pragma unroll
-                for (int s = 0; s < D / 16; ++s)
-                    mma_bf16(tmem + TC::A, kdesc(pair, 128, 0, s), kdesc(pair, 128, 64, s), id,
-                             s > 0);
+                for (int s4 = 0; s4 < 4; ++s4)
+                    mma_bf16(tmem + TC::A, dstep(a0, kb * 128 * 8 + s4 * 2),
+                             dstep(b0, kb * bRows * 8 + s4 * 2), id, (kb | s4) != 0);
             }
             mma_commit(bar_mma);
         }
         if (__syncthreads_or(!mma_wait())) { failed = true; break; }
+        tc_fence_after();
         // ---------------------------------------------- C1: Aq tile, A rows, T_RR, S to bf16
         // TMEM lanes 0..63 hold rows of Aq, lanes 64..127 rows of A (before
         // beta).  Gated: block R's product sits at column 8R(R+1).  A warp
@@ -637,21 +648,28 @@ __global__ void __launch_bounds__(NT, 1)
                 }
             }
             if (warp == 2 || warp == 3) {
-                float w0[16], w1[16], dg[16], t[16];
-                tmem_ld16(tq + TC::A + colof(Rw) + 16 * Rw, w0);
-                tmem_ld16(tq + TC::A + colof(Rw + 1) + 16 * (Rw + 1), w1);
-                const float be = sbeta[r];
+                // diagonal block values, beta-scaled and strict, staged per lane
+                // in shared memory so the substitution loop can stay rolled
+                float *dgs = sX + (warp - 2) * 32 * 17 + lane * 17;
+                {
+                    float w0[16], w1[16];
+                    tmem_ld16(tq + TC::A + colof(Rw) + 16 * Rw, w0);
+                    tmem_ld16(tq + TC::A + colof(Rw + 1) + 16 * (Rw + 1), w1);
+                    const float be = sbeta[r];
 #pragma unroll
-                for (int m = 0; m < 16; ++m) dg[m] = (m < rho) ? be * ((R == Rw) ? w0[m] : w1[m]) : 0.0f;
+                    for (int m = 0; m < 16; ++m) dgs[m] = (m < rho) ? be * ((R == Rw) ? w0[m] : w1[m]) : 0.0f;
+                }
+                float t[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) t[j] = (j == rho) ? 1.0f : 0.0f;
                 const int gbase = lane & 16;
-#pragma unroll
+#pragma unroll 1
                 for (int m = 0; m < 15; ++m) {
+                    const float a = dgs[m];
 #pragma unroll
-                    for (int j = 0; j <= m; ++j) {
+                    for (int j = 0; j < 16; ++j) {
                         const float tm = __shfl_sync(0xffffffffu, t[j], gbase + m);
-                        if (rho > m) t[j] -= dg[m] * tm;
+                        if (j <= m) t[j] -= a * tm;
                     }
                 }
                 float4 *dst = reinterpret_cast<float4 *>(sT + r * LDT);
@@ -748,12 +766,14 @@ __global__ void __launch_bounds__(NT, 1)
             // beta K e^b and beta V are adjacent column blocks: one N = 2D
             // product writes W (columns W) and U (columns U = W + D)
             constexpr uint32_t id = idesc_bf16(64, 2 * D, false, true);
+            const uint64_t a0 = kdesc(t16, 64, 0, 0), b0 = mdesc(bkg, C, 0, 0);
 #pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_bf16(tmem + TC::W, kdesc(t16, 64, 0, s), mdesc(bkg, C, 0, s), id, s > 0);
+            for (int s4 = 0; s4 < 4; ++s4)
+                mma_bf16(tmem + TC::W, dstep(a0, s4 * 2), dstep(b0, s4 * 128), id, s4 > 0);
             mma_commit(bar_mma);
         }
         if (__syncthreads_or(!mma_wait())) { failed = true; break; }
+        tc_fence_after();
         // ---------------------------------------------- E: W tile
         {
             const int r = acc_row(64, qd, lane);
@@ -774,15 +794,20 @@ __global__ void __launch_bounds__(NT, 1)
         if (tid == 0) {
             constexpr uint32_t idw = idesc_bf16(64, D, false, true, true);
             constexpr uint32_t ido = idesc_bf16(64, D, false, true);
+            const uint64_t bS = mdesc(sb, D, 0, 0), aW = kdesc(wt, C, 0, 0), aQ = kdesc(pair, 128, 0, 0);
+#pragma unroll 1
+            for (int kb = 0; kb < D / 64; ++kb) {
 #pragma unroll
-            for (int s = 0; s < D / 16; ++s) {
-                const uint64_t bS = mdesc(sb, D, 0, s);
-                mma_bf16(tmem + TC::U, kdesc(wt, C, 0, s), bS, idw, 1);
-                mma_bf16(tmem + TC::O, kdesc(pair, 128, 0, s), bS, ido, s > 0);
+                for (int s4 = 0; s4 < 4; ++s4) {
+                    const uint64_t b = dstep(bS, (kb * 4 + s4) * 128);
+                    mma_bf16(tmem + TC::U, dstep(aW, kb * 64 * 8 + s4 * 2), b, idw, 1);
+                    mma_bf16(tmem + TC::O, dstep(aQ, kb * 128 * 8 + s4 * 2), b, ido, (kb | s4) != 0);
+                }
             }
             mma_commit(bar_mma);
         }
         if (__syncthreads_or(!mma_wait())) { failed = true; break; }
+        tc_fence_after();
         // ---------------------------------------------- G: u tile
         {
             const int r = acc_row(64, qd, lane);
@@ -803,15 +828,17 @@ __global__ void __launch_bounds__(NT, 1)
         if (tid == 0) {
             constexpr uint32_t ido = idesc_bf16(64, D, false, true);
             constexpr uint32_t ids = idesc_bf16(D, D, true, true);
+            const uint64_t bU = mdesc(ut, C, 0, 0), aA = kdesc(aqk, 64, 0, 0), aK = mdesc(pair, 128, 64, 0);
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t bU = mdesc(ut, C, 0, s);
-                mma_bf16(tmem + TC::O, kdesc(aqk, 64, 0, s), bU, ido, 1);
-                mma_bf16(tmem + TC::S, mdesc(pair, 128, 64, s), bU, ids, 1);
+            for (int s4 = 0; s4 < 4; ++s4) {
+                const uint64_t b = dstep(bU, s4 * 128);
+                mma_bf16(tmem + TC::O, dstep(aA, s4 * 2), b, ido, 1);
+                mma_bf16(tmem + TC::S, dstep(aK, s4 * 128), b, ids, 1);
             }
             mma_commit(bar_mma);
         }
         if (__syncthreads_or(!mma_wait())) { failed = true; break; }
+        tc_fence_after();
         // ---------------------------------------------- I: O -> global
         {
             const int r = acc_row(64, qd, lane);
@@ -837,7 +864,7 @@ __global__ void __launch_bounds__(NT, 1)
         tc_fence_after();
     }
 
-    if (failed && tma_pending) mbar_wait(bar_tma, tma_par, &g_tc_error, 3);
+    if (failed && tma_pending && tid == 0) mbar_wait(bar_tma, tma_par, &g_tc_error, 3);
     // ---- final state
     if (p.final_S && !failed) {
         const int row = acc_row(TC::MS, qd, lane);
