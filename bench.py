@@ -78,7 +78,8 @@ def decode_state_bytes(w: wl.Workload):
 
 
 KERNEL_SOURCES = {
-    "delta_prefill": ("prefill_tc.cu", "tc.cuh", "common.cuh", "launch.h"),
+    "delta_prefill": ("prefill_tc.cu", "delta_intra_tc.cu", "delta_inter_tc.cu", "delta_tc.h",
+                      "tc_tile.cuh", "tc.cuh", "common.cuh", "launch.h"),
     "decode": ("decode.cu", "common.cuh", "launch.h"),
 }
 

@@ -136,7 +136,9 @@ def la_prefill_delta(q, k, v, beta_logits, gate_logits, o, cu_seqlens, chunk=64,
                      flags=LA_L2NORM_K, init_S=None, final_S=None, workspace=None,
                      cu_seqlens_host=None, stream=None):
     """(Gated) delta-rule prefill.  q,k [ntok,H,dk]; v,o [ntok,H,dv];
-    beta_logits [ntok,H]; gate_logits [ntok,H,dk] or None."""
+    beta_logits [ntok,H]; gate_logits [ntok,H,dk] or None.  workspace: a
+    device buffer of at least la_prefill_delta_workspace_size(...) bytes;
+    allocated here (on q's device) when not given."""
     import torch
     _check(dict(q=q, k=k, v=v, o=o, beta_logits=beta_logits, gate_logits=gate_logits),
            dtype=q.dtype, device=q.device)
@@ -146,6 +148,10 @@ def la_prefill_delta(q, k, v, beta_logits, gate_logits, o, cu_seqlens, chunk=64,
     dv = v.shape[2]
     N = cu_seqlens.numel() - 1
     hold, hptr = _host_cu(cu_seqlens_host)
+    if workspace is None:
+        need = la_prefill_delta_workspace_size(N, ntok, H, dk, dv, chunk, _io(q))
+        if need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = library().la_prefill_delta(_ptr(q), _ptr(k), _ptr(v), _ptr(beta_logits),
                                     _ptr(gate_logits), _ptr(o), _io(q), _ptr(cu_seqlens), hptr,

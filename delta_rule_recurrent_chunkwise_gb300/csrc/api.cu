@@ -55,8 +55,8 @@ la_status la_prefill_linear(const void *q, const void *k, const void *v, void *o
 
 size_t la_prefill_delta_workspace_size(int N, int ntok, int H, int dk, int dv, int chunk,
                                        la_dtype io) {
-    (void)N; (void)ntok; (void)H; (void)dk; (void)dv; (void)chunk; (void)io;
-    return 0;
+    if (!dtype_ok(io)) return 0;
+    return la::delta_tc_workspace_bytes(N, ntok, H, dk, dv, chunk, io == LA_BF16);
 }
 
 la_status la_prefill_delta(const void *q, const void *k, const void *v, const void *beta_logits,
@@ -65,7 +65,6 @@ la_status la_prefill_delta(const void *q, const void *k, const void *v, const vo
                            int ntok, int H, int dk, int dv, int chunk, float scale,
                            unsigned flags, const float *init_S, float *final_S, void *workspace,
                            size_t workspace_bytes, void *stream) {
-    (void)workspace;
     if (!q || !k || !v || !beta_logits || !o || !cu_seqlens || N < 1 || ntok < 0 || H < 1 ||
         !dtype_ok(io))
         return LA_ERR_INVALID_ARG;
@@ -73,11 +72,14 @@ la_status la_prefill_delta(const void *q, const void *k, const void *v, const vo
     if (flags & ~(LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK)) return LA_ERR_INVALID_ARG;
     if (!head_size_ok(dk) || !head_size_ok(dv) || chunk != 64) return LA_ERR_UNSUPPORTED;
     if (N > 65535 || H > 65535) return LA_ERR_UNSUPPORTED;
-    if (workspace_bytes < la_prefill_delta_workspace_size(N, 0, H, dk, dv, chunk, io))
+    const size_t ws_need = la_prefill_delta_workspace_size(N, ntok, H, dk, dv, chunk, io);
+    if (ws_need > 0 && (!workspace || workspace_bytes < ws_need ||
+                        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
         return LA_ERR_INVALID_ARG;
     if (la_status st = check_cu_host(cu_seqlens_host, N, ntok)) return st;
     la::PrefillArgs a{q, k, v, beta_logits, gate_logits, o, cu_seqlens, N, ntok, H, dk, dv, scale,
-                      flags, init_S, nullptr, final_S, nullptr, io == LA_BF16};
+                      flags, init_S, nullptr, final_S, nullptr, io == LA_BF16, workspace,
+                      workspace_bytes};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (la::delta_tc_supported(a)) return from_cuda(la::launch_delta_tc(a, s));
     return from_cuda(la::launch_delta_simt(a, s));

@@ -1,0 +1,401 @@
+// delta_inter_tc.cu -- inter-chunk half of the tensor-core (gated) delta-rule
+// prefill: the state recurrence across chunks, one CTA per (head, sequence).
+//
+// ("From GPT-2 to Kimi K3, explained", section DeltaNet (Parallelizing
+// Linear Transformers with Delta Rule), eq. 8-10, with the cumulative decay of
+// sections Gated DeltaNet and KDA / Kimi Linear.)  Per chunk, reading the
+// record the intra-chunk kernel wrote (W, U, Aq, Q e^b, K~ = K e^{b_end - b},
+// e^{b_end}):
+//   u = U - W S                     (S = state at the end of the previous chunk)
+//   O = scale ((Q e^b) S + Aq u)
+//   S <- Diag(e^{b_end}) S + K~^T u
+//
+// Only S -> u -> S is sequential; everything else is arranged around that
+// chain.  Three warp roles, synchronised by mbarriers only:
+//   issuer (one thread)  tensor-core products and record loads:
+//       u  = I_64 U            issued one chunk early (U enters TMEM through an
+//                              identity product, so u accumulates in place)
+//       u -= W S               -> commit "u"
+//       O  = (Q e^b) S
+//       S += K~^T u            -> commit "s"          (after "u tile ready")
+//       O += Aq u              -> commit "o"
+//   converters   u (TMEM fp32) -> bf16 operand tile          -> "u tile ready"
+//                S (TMEM fp32) -> bf16 operand tile          -> "S tile ready"
+//                gated: S *= e^{b_end} of the next chunk, in TMEM (off the
+//                chain: the next S += K~^T u waits for "u tile ready")
+//   output warps O (TMEM fp32, two buffers) -> scale -> bf16 -> global
+// The chain per chunk is then: W S product, u readback, K~^T u product,
+// S readback.  The fp32 state lives in tensor memory for the whole sequence;
+// the next chunk's record streams in by one bulk copy while this one runs.
+
+#include "common.cuh"
+#include "delta_tc.h"
+#include "tc_tile.cuh"
+
+namespace la {
+namespace {
+
+using namespace tc;
+using namespace tile;
+
+template <int D>
+struct Roles {
+    static constexpr int CW = D == 64 ? 4 : 8;   // converter warps (2 per lane quarter at D = 128)
+    static constexpr int OW = 4;                 // output warps (one per lane quarter)
+    static constexpr int ISSUER = CW + OW;       // warp of the issuing thread
+    static constexpr int NT = 32 * (CW + OW + 1);
+    static constexpr int CPT = D / (CW / 4);     // state / u columns per converter thread
+};
+
+template <int D>
+struct Layout {
+    using Rec = Record<D>;
+    // record buffers: loads run NB - 1 chunks ahead of the recurrence
+    static constexpr int NB = D == 64 ? 4 : 2;
+    static constexpr uint32_t REC0 = 0;
+    static constexpr uint32_t SB = NB * Rec::BYTES;      // S, bf16 [D][D] RS tile
+    static constexpr uint32_t UT = SB + D * D * 2;        // u, bf16 [64][D] RS tile
+    static constexpr uint32_t IDENT = UT + C * D * 2;     // I_64, bf16 RS tile
+    static constexpr uint32_t BARS = IDENT + 8192;        // mbarriers + tmem slot
+    static constexpr uint32_t TOTAL = BARS + 128;
+    static_assert(TOTAL + 1024 <= 227 * 1024, "shared memory budget");
+};
+
+// mbarrier slots (B_REC0 .. B_REC0 + NB - 1: record buffers)
+enum : int { B_U = 0, B_S, B_O, B_SREADY, B_UREADY, B_OFREE0, B_OFREE1, B_REC0, B_COUNT = B_REC0 + 4 };
+
+// TMEM columns: S (M = D rows = key channels), u, two O buffers.
+template <int D>
+struct Cols {
+    static constexpr uint32_t S = 0, U = D, O = 2 * D, TOTAL = 4 * D;
+};
+
+struct InterParams {
+    const uint8_t *records;   // [slots][H] records
+    __nv_bfloat16 *o;
+    const int32_t *cu_seqlens;
+    const float *init_S;
+    float *final_S;
+    unsigned *err;
+    int H, ntok;
+    float scale;
+};
+
+template <int D, bool GATED>
+__global__ void __launch_bounds__(Roles<D>::NT, 1) delta_inter_kernel(InterParams p) {
+    using L = Layout<D>;
+    using Rec = Record<D>;
+    using TC = Cols<D>;
+    using RL = Roles<D>;
+    constexpr int CPT = RL::CPT;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sb = sm + L::SB, *ut = sm + L::UT, *ident = sm + L::IDENT;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::BARS);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + B_COUNT);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.x, n = blockIdx.y, H = p.H;
+    int t_begin = p.cu_seqlens[n], t_end = p.cu_seqlens[n + 1];
+    if (t_begin < 0 || t_end < t_begin || t_end > p.ntok) {
+        if (tid == 0) atomicCAS(p.err, 0u, 100u);
+        t_begin = t_end = 0;
+    }
+    const int nc = (t_end - t_begin + C - 1) / C;
+    const int64_t slot0 = (int64_t)(t_begin / C) + n;
+    auto rec_src = [&](int c) { return p.records + ((slot0 + c) * H + h) * (int64_t)Rec::BYTES; };
+    constexpr int NB = L::NB;
+    auto buf = [&](int c) { return sm + L::REC0 + (uint32_t)(c % NB) * Rec::BYTES; };
+    auto rec_bar = [&](int c) { return &bars[B_REC0 + c % NB]; };
+    auto rec_par = [](int c) { return (uint32_t)(c / NB) & 1u; };
+    // Record loads (one bulk copy each).  The issuer starts records 0 .. NB-1;
+    // output warp 0 loads record c + NB into chunk c's buffer once every
+    // product reading it is done.  So the records loaded are always 0 .. K-1;
+    // both threads count theirs (s_loads) so the CTA can wait the last ones
+    // out before it exits.
+    int *s_loads = reinterpret_cast<int *>(tslot + 1);
+    auto issue_rec = [&](int c) {
+        fence_proxy_async();
+        mbar_arrive_expect_tx(rec_bar(c), Rec::BYTES);
+        bulk_load(buf(c), rec_src(c), Rec::BYTES, rec_bar(c));
+    };
+
+    if (tid == 0) {
+        for (int b = 0; b < NB; ++b) mbar_init(&bars[B_REC0 + b], 1);
+        mbar_init(&bars[B_U], 1);
+        mbar_init(&bars[B_S], 1);
+        mbar_init(&bars[B_O], 1);
+        mbar_init(&bars[B_SREADY], RL::CW);
+        mbar_init(&bars[B_UREADY], RL::CW);
+        mbar_init(&bars[B_OFREE0], RL::OW);
+        mbar_init(&bars[B_OFREE1], RL::OW);
+        fence_mbar_init();
+        s_loads[0] = s_loads[1] = 0;
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, TC::TOTAL);
+        tmem_relinquish();
+    }
+    // the identity operand: 64 rows x 8 sixteen-byte units
+    for (int u = tid; u < C * 8; u += RL::NT) {
+        const int r = u >> 3, c8 = (u & 7) * 8;
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = (c8 + i == r) ? 1.0f : 0.0f;
+        st_bf16x8(ident, C, r, c8, v);
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t tq = tmem + ((uint32_t)(32 * (warp & 3)) << 16);  // this warp's lane quarter
+    const int64_t sbase = ((int64_t)n * H + h) * D * D;
+
+    if (warp == RL::ISSUER) {
+        // ================================================= issuer
+        if (lane == 0 && nc > 0) {
+            constexpr uint32_t idp = idesc_bf16(64, D, false, true);
+            constexpr uint32_t idn = idesc_bf16(64, D, false, true, true);
+            constexpr uint32_t ids = idesc_bf16(D, D, true, true);
+            const uint64_t aI = kdesc(ident, C, 0, 0), bS = mdesc(sb, D, 0, 0), bU = mdesc(ut, C, 0, 0);
+            auto issue_iu = [&](int c) {  // u = I_64 U
+                const uint64_t b = mdesc(buf(c) + Rec::U, C, 0, 0);
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4)
+                    mma_bf16(tmem + TC::U, dstep(aI, s4 * 2), dstep(b, s4 * 128), idp, s4 > 0);
+            };
+            for (int c = 0; c < NB && c < nc; ++c) issue_rec(c);
+            s_loads[0] = NB < nc ? NB : nc;
+            bool ok = true, iu_ready = false;  // iu_ready: u = I U of chunk c issued
+            for (int c = 0; c < nc && ok; ++c) {
+                uint8_t *rb = buf(c);
+                const uint32_t tO = tmem + TC::O + (uint32_t)(c & 1) * D;
+                if (!iu_ready) {
+                    if (!(ok = mbar_wait(rec_bar(c), rec_par(c), p.err, 4))) break;
+                    issue_iu(c);
+                }
+                // S tile of this chunk ready (converters)
+                if (!(ok = mbar_wait(&bars[B_SREADY], (uint32_t)c & 1u, p.err, 5))) break;
+                tc_fence_after();
+                const uint64_t aW = kdesc(rb + Rec::W, C, 0, 0), aQ = kdesc(rb + Rec::PAIR, 128, 0, 0);
+#pragma unroll 1
+                for (int kb = 0; kb < D / 64; ++kb) {
+#pragma unroll
+                    for (int s4 = 0; s4 < 4; ++s4) {
+                        const int s = 4 * kb + s4;
+                        mma_bf16(tmem + TC::U, dstep(aW, kstep_units(C, s)), dstep(bS, s * 128), idn, 1);
+                    }
+                }
+                mma_commit(&bars[B_U]);
+                // O buffer c & 1 was drained (chunk c - 2) before the previous
+                // chunk's "o" commit
+#pragma unroll 1
+                for (int kb = 0; kb < D / 64; ++kb) {
+#pragma unroll
+                    for (int s4 = 0; s4 < 4; ++s4) {
+                        const int s = 4 * kb + s4;
+                        mma_bf16(tO, dstep(aQ, kstep_units(128, s)), dstep(bS, s * 128), idp, s > 0);
+                    }
+                }
+                // u tile ready (converters), state decayed for this chunk
+                if (!(ok = mbar_wait(&bars[B_UREADY], (uint32_t)c & 1u, p.err, 7))) break;
+                tc_fence_after();
+                const uint64_t aK = mdesc(rb + Rec::PAIR, 128, 64, 0), aA = kdesc(rb + Rec::AQ, 64, 0, 0);
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4)
+                    mma_bf16(tmem + TC::S, dstep(aK, s4 * 128), dstep(bU, s4 * 128), ids, 1);
+                mma_commit(&bars[B_S]);
+                // the next chunk's u = I U, if its record is already here (the
+                // converters have read this chunk's u out of TMEM)
+                iu_ready = c + 1 < nc && mbar_test_wait(rec_bar(c + 1), rec_par(c + 1));
+                if (iu_ready) issue_iu(c + 1);
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4)
+                    mma_bf16(tO, dstep(aA, s4 * 2), dstep(bU, s4 * 128), idp, 1);
+                // The output warps must have taken chunk c - 1 (and so seen its
+                // "o" phase) before this chunk's "o" phase completes; that also
+                // frees O buffer (c + 1) & 1 for the next chunk.
+                if (c >= 1 && !(ok = mbar_wait(&bars[B_OFREE0 + ((c - 1) & 1)], (uint32_t)((c - 1) >> 1) & 1u, p.err, 6)))
+                    break;
+                mma_commit(&bars[B_O]);
+            }
+        }
+    } else if (warp < RL::CW) {
+        // ================================================= converters
+        const int srow = acc_row(D, warp & 3, lane);   // state row (key channel)
+        const int urow = acc_row(64, warp & 3, lane);  // u row (token)
+        const int c0 = (warp >> 2) * CPT;              // first column of this thread
+        bool ok = true;
+        // initial state: bf16 operand copy; TMEM state decayed by chunk 0's e^{b_end}
+        if (GATED && nc > 0) ok = mbar_wait(rec_bar(0), 0, p.err, 10);
+        if (ok) {
+            const float gd = (GATED && nc > 0 && srow >= 0)
+                                 ? reinterpret_cast<const float *>(buf(0) + Rec::GEND)[srow]
+                                 : 1.0f;
+#pragma unroll
+            for (int cb = 0; cb < CPT; cb += 16) {
+                const int col = c0 + cb;
+                float v[16];
+                if (srow >= 0 && p.init_S) {
+                    const float4 *src = reinterpret_cast<const float4 *>(p.init_S + sbase + (int64_t)srow * D + col);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float4 f = src[i];
+                        v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+                }
+                if (srow >= 0) {
+                    st_bf16x8(sb, D, srow, col, v);
+                    st_bf16x8(sb, D, srow, col + 8, v + 8);
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] *= gd;
+                tmem_st16(tq + TC::S + col, v);
+            }
+            fence_proxy_async();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_SREADY]);
+        }
+        for (int c = 0; c < nc && ok; ++c) {
+            // ---- u -> bf16 operand tile
+            if (!(ok = mbar_wait(&bars[B_U], (uint32_t)c & 1u, p.err, 11))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int cb = 0; cb < CPT; cb += 32) {
+                float v[32];
+                tmem_ld32(tq + TC::U + c0 + cb, v);
+                if (urow >= 0) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) st_bf16x8(ut, C, urow, c0 + cb + i, v + i);
+                }
+            }
+            fence_proxy_async();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_UREADY]);
+            // ---- S after this chunk
+            if (!(ok = mbar_wait(&bars[B_S], (uint32_t)c & 1u, p.err, 12))) break;
+            tc_fence_after();
+            if (c + 1 < nc) {
+#pragma unroll
+                for (int cb = 0; cb < CPT; cb += 32) {
+                    float v[32];
+                    tmem_ld32(tq + TC::S + c0 + cb, v);
+                    if (srow >= 0) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 8) st_bf16x8(sb, D, srow, c0 + cb + i, v + i);
+                    }
+                }
+                fence_proxy_async();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[B_SREADY]);
+                if (GATED) {
+                    // decay for the next chunk (needs its record's e^{b_end});
+                    // the state is read again rather than held in registers
+                    if (!(ok = mbar_wait(rec_bar(c + 1), rec_par(c + 1), p.err, 13))) break;
+                    const float gd = srow >= 0
+                                         ? reinterpret_cast<const float *>(buf(c + 1) + Rec::GEND)[srow]
+                                         : 1.0f;
+#pragma unroll
+                    for (int cb = 0; cb < CPT; cb += 32) {
+                        float v[32];
+                        tmem_ld32(tq + TC::S + c0 + cb, v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] *= gd;
+                        tmem_st16(tq + TC::S + c0 + cb, *reinterpret_cast<float(*)[16]>(v));
+                        tmem_st16(tq + TC::S + c0 + cb + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+                    }
+                    tc_fence_before();
+                }
+            }
+        }
+        // ---- final state
+        if (ok && p.final_S) {
+#pragma unroll
+            for (int cb = 0; cb < CPT; cb += 16) {
+                float v[16];
+                tmem_ld16(tq + TC::S + c0 + cb, v);
+                if (srow >= 0) {
+                    float4 *dst = reinterpret_cast<float4 *>(p.final_S + sbase + (int64_t)srow * D + c0 + cb);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                }
+            }
+        }
+    } else {
+        // ================================================= output warps
+        const int r = acc_row(64, warp & 3, lane);
+        int refills = 0;
+        for (int c = 0; c < nc; ++c) {
+            if (!mbar_wait(&bars[B_O], (uint32_t)c & 1u, p.err, 14)) break;
+            tc_fence_after();
+            const int tok0 = t_begin + c * C;
+            const bool valid = r >= 0 && r < t_end - tok0;
+            const uint32_t tO = tq + TC::O + (uint32_t)(c & 1) * D;
+#pragma unroll
+            for (int cb = 0; cb < D; cb += 32) {
+                float v[32];
+                tmem_ld32(tO + cb, v);
+                if (valid) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= p.scale;
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + ((int64_t)(tok0 + r) * H + h) * D + cb);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dst[i] = pack8(v + 8 * i);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&bars[B_OFREE0 + (c & 1)]);
+                // every product that reads record c has completed ("o" is the
+                // last commit of chunk c): its buffer takes record c + NB
+                if (warp == RL::CW && c + NB < nc) {
+                    issue_rec(c + NB);
+                    ++refills;
+                }
+            }
+        }
+        if (warp == RL::CW && lane == 0) s_loads[1] = refills;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+        // the last load into each buffer (earlier ones completed before it was issued)
+        const int K = s_loads[0] + s_loads[1];
+        for (int j = K - NB > 0 ? K - NB : 0; j < K; ++j) mbar_wait(rec_bar(j), rec_par(j), p.err, 9);
+    }
+    if (warp == 0) tmem_dealloc(tmem, TC::TOTAL);
+}
+
+template <int D, bool GATED>
+cudaError_t launch_t(const TcLaunch &x, cudaStream_t s) {
+    const PrefillArgs &a = *x.a;
+    InterParams p{x.records, static_cast<__nv_bfloat16 *>(a.o), a.cu_seqlens, a.init_S,
+                  a.final_S, x.err, a.H, a.ntok, a.scale};
+    constexpr size_t smem = Layout<D>::TOTAL + 1024;
+    auto kern = delta_inter_kernel<D, GATED>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.H, a.N);
+    kern<<<grid, Roles<D>::NT, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_delta_inter(const TcLaunch &x, cudaStream_t s) {
+    const bool g = x.a->gate_logits != nullptr;
+    if (x.a->dk == 128) return g ? launch_t<128, true>(x, s) : launch_t<128, false>(x, s);
+    return g ? launch_t<64, true>(x, s) : launch_t<64, false>(x, s);
+}
+
+}  // namespace la

@@ -1,0 +1,770 @@
+// delta_intra_tc.cu -- intra-chunk half of the tensor-core (gated) delta-rule
+// prefill: everything that depends on one chunk alone, for all chunks of all
+// sequences and heads at once.  bf16 I/O, fp32 accumulators, dk = dv = D in
+// {64, 128}, chunk C = 64.
+//
+// Algorithm ("From GPT-2 to Kimi K3, explained", section DeltaNet
+// (Parallelizing Linear Transformers with Delta Rule), eq. 8-10, with the
+// cumulative per-key-channel decay of sections Gated DeltaNet and
+// KDA / Kimi Linear).  Per chunk, with b = cumulative log decay inside the
+// chunk (per key channel):
+//   A[r][i]  = beta_r sum_c k_rc k_ic e^{b_rc - b_ic}   (i < r)     UT matrix
+//   Aq[r][i] =        sum_c q_rc k_ic e^{b_rc - b_ic}   (i <= r)    scores
+//   T  = (I + A)^{-1}                                   blocked forward substitution
+//   W  = T (beta K e^{b}),  U = T (beta V)              (eq. 10)
+// plus the operands the state recurrence needs: Q e^{b}, K e^{b_end - b} and
+// e^{b_end}.  None of it depends on the state, so every (chunk, head) is an
+// independent task; the inter-chunk kernel then carries the state through
+// the chunks with u = U - W S, O = (Q e^b) S + Aq u, S <- e^{b_end} S + K~^T u.
+//
+// Decay factors.  Only products of alpha are formed, never exponentials of
+// cumulative sums: alpha = 1 / (1 + e^g) and 1/alpha = 1 + e^g cost one
+// exponential and one reciprocal per element, and every other factor is a
+// running product.  Aq and A need e^{b_r - b_i} for i <= r, which does not
+// factor into a row term times a column term over a whole chunk without
+// overflow.  The chunk is cut into four 16-token blocks; for rows r of block
+// R the reference point is the token just before R:
+//   row factor  P_r = prod_{t=start(R)}^{r} alpha_t               (<= 1)
+//   col factor  prod_{t=i+1}^{start(R)-1} alpha_t   for i < start(R)   (<= 1)
+//               1 / prod_{t=start(R)}^{i} alpha_t   for i in R         (>= 1)
+// so one tensor-core product per block R (the columns of K scaled for R)
+// gives the rows of A and Aq that belong to R.  The reciprocal column factor
+// spans at most 16 tokens; it is exact while that 16-token decay of a
+// channel stays above ~1e-30 (mean alpha above ~0.013), and is clamped
+// (never inf/NaN) beyond.
+//
+// Mapping: a persistent grid (one CTA of 512 threads per SM) walks the
+// (chunk slot, head) tasks; the next task's raw q, k, v, gate tiles arrive
+// by TMA while the current one computes.  Products on tcgen05 (bf16 x bf16
+// -> fp32 in TMEM): [Q;K]-hat x K_R^T (one N = 160 product when gated) and
+// T x [beta K e^b | beta V] (one N = 2D product).  The triangular solve runs
+// in fp32 on CUDA cores: the four diagonal 16x16 blocks by warp-shuffle
+// forward substitution, the off-diagonal blocks by warp-level TF32 products.
+// The finished operands leave as one record per task by bulk copies.
+
+#include <cuda.h>
+
+#include "common.cuh"
+#include "delta_tc.h"
+#include "tc_tile.cuh"
+
+namespace la {
+namespace {
+
+using namespace tc;
+using namespace tile;
+
+constexpr int NT = 512;          // threads per CTA (16 warps)
+constexpr int TMEM_COLS = 256;   // block products (<= 160 columns), then W | U
+constexpr int LDT = 68;          // fp32 row stride of the A and T scratch (16-byte rows)
+constexpr uint32_t TC_A = 0, TC_W = 0;  // TMEM columns; U follows W
+
+// ------------------------------------------------------------- smem layout
+template <int D, bool GATED>
+struct Layout {
+    static constexpr uint32_t tile64 = C * D * 2;               // [64][D]
+    static constexpr uint32_t RAW_Q = 0;
+    static constexpr uint32_t RAW_K = RAW_Q + tile64;
+    static constexpr uint32_t RAW_V = RAW_K + tile64;
+    static constexpr uint32_t RAW_G = RAW_V + tile64;
+    static constexpr uint32_t X = RAW_G + (GATED ? tile64 : 0);
+    // X, prologue (gated): the block-product operands [Q^; K^] (128 rows)
+    // and the packed K_R tile (160 rows)
+    static constexpr uint32_t QKH = X;
+    static constexpr uint32_t KR = X + 128 * D * 2;
+    // X during and after the solve
+    static constexpr uint32_t T16 = X;                  // T, bf16 [64][64]
+    static constexpr uint32_t AQK = X + 8192;           // Aq, bf16 [64][64]
+    static constexpr uint32_t SA = X + 16384;           // A, fp32 [64][LDT]
+    static constexpr uint32_t ST = SA + 64 * LDT * 4;   // T, fp32 [64][LDT]
+    static constexpr uint32_t SX = ST + 64 * LDT * 4;   // merge temps, fp32 (8 KB)
+    static constexpr uint32_t X_END_A = GATED ? KR + 160 * D * 2 : X;
+    static constexpr uint32_t X_END_C = SX + 8192;
+    static constexpr uint32_t X_END = X_END_A > X_END_C ? X_END_A : X_END_C;
+    // [Q e^b ; K e^{b_end - b}] (gated) or [q^ ; k^] (ungated), 128 rows, then
+    // beta K e^b (later W) and beta V (later U): the record's first four
+    // tiles, contiguous as in the record
+    static constexpr uint32_t PAIR = (X_END + 1023) & ~1023u;
+    static constexpr uint32_t BKG = PAIR + 2 * tile64;
+    static constexpr uint32_t BV = BKG + tile64;
+    static constexpr uint32_t SMALL = BV + tile64;
+    static constexpr uint32_t BETA = SMALL;                    // fp32 [64]
+    static constexpr uint32_t KN = BETA + 256;                 // fp32 [64]
+    static constexpr uint32_t QN = KN + 256;                   // fp32 [64]
+    static constexpr uint32_t EB = QN + 256;                   // fp32 [4][D] block decay
+    static constexpr uint32_t GEND = EB + 16 * D;              // fp32 [D] chunk decay
+    static constexpr uint32_t INFO = GEND + 4 * D;             // int4: next task
+    static constexpr uint32_t BARS = INFO + 16;                // 2 mbarriers + tmem slot
+    static constexpr uint32_t TOTAL = BARS + 64;
+    static_assert(BKG - PAIR == Record<D>::W && BV - PAIR == Record<D>::U, "record image");
+    static_assert(TOTAL + 1024 <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+
+// ---- warp-level TF32 products for the small blocks of the triangular solve
+// (m16n8k8: A 16x8 row-major, B 8x8 as [k][n], C 16x8; fp32 accumulate).
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const float *A, int lda, const float *B,
+                                         int ldb, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    const uint32_t a0 = to_tf32(A[g * lda + t]), a1 = to_tf32(A[(g + 8) * lda + t]);
+    const uint32_t a2 = to_tf32(A[g * lda + t + 4]), a3 = to_tf32(A[(g + 8) * lda + t + 4]);
+    const uint32_t b0 = to_tf32(B[t * ldb + g]), b1 = to_tf32(B[(t + 4) * ldb + g]);
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// C (16x8 tile at Cp, row stride ldc) = sign * d
+__device__ __forceinline__ void store_c(float *Cp, int ldc, const float (&d)[4], float sign,
+                                        int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    Cp[g * ldc + 2 * t] = sign * d[0];
+    Cp[g * ldc + 2 * t + 1] = sign * d[1];
+    Cp[(g + 8) * ldc + 2 * t] = sign * d[2];
+    Cp[(g + 8) * ldc + 2 * t + 1] = sign * d[3];
+}
+
+struct IntraParams {
+    const __nv_bfloat16 *beta_logits;
+    const int2 *table;      // [slots] {first token, length}
+    uint8_t *records;       // [slots][H] records
+    unsigned *err;
+    int64_t n_tasks;        // slots * H
+    int H, ntok;
+    unsigned flags;
+};
+
+
+template <int D, bool GATED>
+__global__ void __launch_bounds__(NT, 1)
+    delta_intra_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_g, IntraParams p) {
+    using L = Layout<D, GATED>;
+    using Rec = Record<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *rawq = sm + L::RAW_Q, *rawk = sm + L::RAW_K, *rawv = sm + L::RAW_V,
+            *rawg = sm + L::RAW_G;
+    uint8_t *qkh = sm + L::QKH, *kr = sm + L::KR, *t16 = sm + L::T16, *aqk = sm + L::AQK;
+    float *sA = reinterpret_cast<float *>(sm + L::SA);
+    float *sT = reinterpret_cast<float *>(sm + L::ST);
+    float *sX = reinterpret_cast<float *>(sm + L::SX);
+    uint8_t *pair = sm + L::PAIR, *bkg = sm + L::BKG, *bv = sm + L::BV;
+    uint8_t *wt = bkg, *ut = bv;  // W and U tiles reuse beta K e^b and beta V
+    float *sbeta = reinterpret_cast<float *>(sm + L::BETA);
+    float *skn = reinterpret_cast<float *>(sm + L::KN);
+    float *sqn = reinterpret_cast<float *>(sm + L::QN);
+    float *sE = reinterpret_cast<float *>(sm + L::EB);
+    float *sgend = reinterpret_cast<float *>(sm + L::GEND);
+    int4 *sinfo = reinterpret_cast<int4 *>(sm + L::INFO);
+    uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + L::BARS);
+    uint64_t *bar_mma = bar_tma + 1;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar_tma + 2);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qd = warp & 3, cp = warp >> 2;  // TMEM lane quarter, column part
+    const int H = p.H;
+    const bool silu = (p.flags & kSiluQK) != 0;
+    const bool l2k = (p.flags & kL2NormK) != 0, l2q = (p.flags & kL2NormQ) != 0;
+    constexpr uint32_t tx_bytes = (GATED ? 4u : 3u) * L::tile64;
+
+    if (tid == 0) {
+        mbar_init(bar_tma, 1);
+        mbar_init(bar_mma, 1);
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        if (GATED) tma_prefetch_desc(&tm_g);
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);  // this warp's lane quarter
+
+    // Task t = slot * H + head.  {first token, length, head, slot}; length 0
+    // marks a slot no chunk occupies (or a table entry out of range).
+    auto task_info = [&](int64_t t) -> int4 {
+        int4 r = make_int4(0, 0, 0, 0);
+        if (t < p.n_tasks) {
+            const int64_t s = t / H;
+            const int2 e = p.table[s];
+            if (e.x >= 0 && e.y > 0 && e.y <= C && e.x <= p.ntok - e.y)
+                r = make_int4(e.x, e.y, (int)(t - s * H), (int)s);
+        }
+        return r;
+    };
+    auto issue_tma = [&](int t0, int hh) {
+        fence_proxy_async();
+        mbar_arrive_expect_tx(bar_tma, tx_bytes);
+#pragma unroll
+        for (int cb = 0; cb < D / 64; ++cb) {
+            tma_load_3d(rawq + cb * 8192, &tm_q, bar_tma, cb * 64, hh, t0);
+            tma_load_3d(rawk + cb * 8192, &tm_k, bar_tma, cb * 64, hh, t0);
+            tma_load_3d(rawv + cb * 8192, &tm_v, bar_tma, cb * 64, hh, t0);
+            if (GATED) tma_load_3d(rawg + cb * 8192, &tm_g, bar_tma, cb * 64, hh, t0);
+        }
+    };
+    auto load_beta = [&](const int4 &ti) -> float {
+        return (tid < C && tid < ti.y)
+                   ? __bfloat162float(p.beta_logits[(int64_t)(ti.x + tid) * H + ti.z])
+                   : 0.0f;
+    };
+
+    int64_t t = blockIdx.x;
+    int4 cur = task_info(t);
+    bool tma_pending = false;  // meaningful in thread 0, which issues and waits
+    if (tid == 0 && cur.y > 0) {
+        issue_tma(cur.x, cur.z);
+        tma_pending = true;
+    }
+    float beta_cur = load_beta(cur);  // threads 0..63
+    uint32_t tma_par = 0, mma_par = 0;
+    bool failed = false;
+
+    // One thread waits on an mbarrier; the CTA barrier that follows every
+    // wait (a __syncthreads_or carrying the outcome) releases the others,
+    // who then order their tensor-memory accesses after it.
+    auto mma_wait = [&]() -> bool {
+        bool ok = true;
+        if (tid == 0) ok = mbar_wait(bar_mma, mma_par, p.err, 2);
+        mma_par ^= 1;
+        return ok;
+    };
+    auto phase_sync = [&]() {
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    };
+
+    while (t < p.n_tasks) {
+        const int64_t t_next = t + gridDim.x;
+        int4 nxt = make_int4(0, 0, 0, 0);
+        if (tid == 0) nxt = task_info(t_next);  // consumed after the operand stage
+        if (cur.y == 0) {
+            // empty slot: nothing to compute, start the next task's loads
+            if (tid == 0) {
+                *sinfo = nxt;
+                if (nxt.y > 0) {
+                    issue_tma(nxt.x, nxt.z);
+                    tma_pending = true;
+                }
+            }
+            __syncthreads();
+            cur = *sinfo;
+            beta_cur = load_beta(cur);
+            t = t_next;
+            __syncthreads();
+            continue;
+        }
+        const int len = cur.y, h = cur.z;
+        // ---------------------------------------------- raw tiles of this chunk
+        {
+            const bool ok = tid == 0 ? mbar_wait(bar_tma, tma_par, p.err, 1) : true;
+            tma_par ^= 1;
+            tma_pending = false;
+            tc_fence_before();
+            if (__syncthreads_or(!ok)) { failed = true; break; }
+            tc_fence_after();
+        }
+        // ---------------------------------------------- A0: beta, row norms
+        if (tid < C) sbeta[tid] = tid < len ? __fdividef(1.0f, 1.0f + __expf(-beta_cur)) : 0.0f;
+        {
+            // 8 threads per row, D/8 channels each, 16-byte loads
+            const int r = tid >> 3, part = tid & 7;
+            float ssk = 0.0f, ssq = 0.0f;
+#pragma unroll
+            for (int c = part * (D / 8); c < (part + 1) * (D / 8); c += 8) {
+                float kv[8], qv[8];
+                unpack8(*reinterpret_cast<const uint4 *>(rawk + rs_off(C, r, c)), kv);
+                unpack8(*reinterpret_cast<const uint4 *>(rawq + rs_off(C, r, c)), qv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (silu) { kv[i] = silu_fast(kv[i]); qv[i] = silu_fast(qv[i]); }
+                    ssk += kv[i] * kv[i];
+                    ssq += qv[i] * qv[i];
+                }
+            }
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+                ssk += __shfl_xor_sync(0xffffffffu, ssk, o);
+                ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
+            }
+            if (part == 0) {
+                const bool valid = r < len;
+                skn[r] = valid ? (l2k ? rsqrtf(fmaxf(ssk, 1e-24f)) : 1.0f) : 0.0f;
+                sqn[r] = valid ? (l2q ? rsqrtf(fmaxf(ssq, 1e-24f)) : 1.0f) : 0.0f;
+            }
+        }
+        if (tid == 0) bulk_wait_read();  // previous record's sources are rewritten below
+        __syncthreads();
+        // ---------------------------------------------- A1: operand tiles
+        if (!GATED) {
+            // [q^; k^] into PAIR, beta k^ into BKG, beta v into BV: 16-byte units
+            for (int u = tid; u < C * D / 8; u += NT) {
+                const uint32_t off = (uint32_t)u * 16u;                 // offset in a [64][D] tile
+                const uint32_t cb = off >> 13, in = off & 8191u;         // column block, offset in it
+                const int r = (int)(in >> 7);
+                const uint32_t po = cb * (128u * 128u) + in;            // same row in PAIR
+                float kv[8], qv[8], vv[8];
+                unpack8(*reinterpret_cast<const uint4 *>(rawk + off), kv);
+                unpack8(*reinterpret_cast<const uint4 *>(rawq + off), qv);
+                unpack8(*reinterpret_cast<const uint4 *>(rawv + off), vv);
+                const float kn = skn[r], qn = sqn[r], be = sbeta[r];
+                float bk[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (silu) { kv[i] = silu_fast(kv[i]); qv[i] = silu_fast(qv[i]); }
+                    kv[i] *= kn;
+                    qv[i] *= qn;
+                    bk[i] = be * kv[i];
+                    vv[i] *= be;
+                }
+                *reinterpret_cast<uint4 *>(pair + po) = pack8(qv);
+                *reinterpret_cast<uint4 *>(pair + po + 64u * 128u) = pack8(kv);
+                *reinterpret_cast<uint4 *>(bkg + off) = pack8(bk);
+                *reinterpret_cast<uint4 *>(bv + off) = pack8(vv);
+            }
+            if (tid < D) sgend[tid] = 1.0f;
+        } else {
+            // One thread per (2 key channels, 8 rows of a 16-token block R); the
+            // two 8-row halves of a block sit in lanes l and l^16 of one warp.
+            // alpha = 1/(1+e^g), 1/alpha = 1+e^g; P = prefix product of alpha
+            // inside the block, Pi = 1/P.  Every operand is (q or k) x (P or Pi)
+            // x a per-(block, channel) constant; the within-block suffix is
+            // prod_{t>r} alpha_t = E_R / P_r with E_R the block total.
+            const bool act = warp < D / 8;
+            const int R = (warp * 32 / D) & 3, grp = warp % (D / 32);
+            const int hf2 = lane >> 4, c0 = 32 * grp + 2 * (lane & 15);
+            const int r0 = 16 * R + 8 * hf2;
+            // Rows r0 and r0 + 8 share a swizzle phase, so at step rho the
+            // second-half lanes work on row r0 + (rho ^ 4): the two halves of
+            // the warp then hit disjoint banks.
+            const int pr = 4 * hf2;
+            // Addressing: the channel pair is fixed per thread and r0 is a
+            // multiple of 8, so row r0 + rho has swizzle phase rho.
+            const uint32_t cb = (uint32_t)c0 >> 6, ch = ((uint32_t)c0 >> 3) & 7u;
+            const uint32_t cboff64 = cb * 64u * 128u, cboff128 = cb * 128u * 128u,
+                           cboff160 = cb * 160u * 128u;
+            uint32_t swz[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) swz[j] = ((ch ^ (uint32_t)j) << 4) + ((uint32_t)c0 & 7u) * 2u;
+            float P[8][2], Pi[8][2];
+#pragma unroll
+            for (int rho = 0; rho < 8; ++rho) { P[rho][0] = P[rho][1] = 1.0f; Pi[rho][0] = Pi[rho][1] = 1.0f; }
+            if (act) {
+                float p0 = 1.0f, p1 = 1.0f, q0 = 1.0f, q1 = 1.0f;
+#pragma unroll
+                for (int rho = 0; rho < 8; ++rho) {
+                    // the scan runs in natural row order (a prefix product);
+                    // only the store pass below uses the permuted order
+                    const int r = r0 + rho;
+                    const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162 *>(rawg + cboff64 + r * 128 + swz[rho]);
+                    const float2 g = __bfloat1622float2(g2);
+                    const float e0 = __expf(fminf(g.x, 80.0f)), e1 = __expf(fminf(g.y, 80.0f));
+                    if (r < len) {
+                        p0 *= __fdividef(1.0f, 1.0f + e0);
+                        p1 *= __fdividef(1.0f, 1.0f + e1);
+                        q0 = fminf(q0 * (1.0f + e0), 1e30f);
+                        q1 = fminf(q1 * (1.0f + e1), 1e30f);
+                    }
+                    P[rho][0] = p0; P[rho][1] = p1; Pi[rho][0] = q0; Pi[rho][1] = q1;
+                }
+            }
+            // carry the first half's totals into the second half
+            {
+                const float t0 = __shfl_sync(0xffffffffu, P[7][0], lane ^ 16);
+                const float t1 = __shfl_sync(0xffffffffu, P[7][1], lane ^ 16);
+                const float u0 = __shfl_sync(0xffffffffu, Pi[7][0], lane ^ 16);
+                const float u1 = __shfl_sync(0xffffffffu, Pi[7][1], lane ^ 16);
+                if (hf2) {
+#pragma unroll
+                    for (int rho = 0; rho < 8; ++rho) {
+                        P[rho][0] *= t0; P[rho][1] *= t1;
+                        Pi[rho][0] = fminf(Pi[rho][0] * u0, 1e30f);
+                        Pi[rho][1] = fminf(Pi[rho][1] * u1, 1e30f);
+                    }
+                }
+            }
+            if (act && hf2) {
+                sE[R * D + c0] = P[7][0];
+                sE[R * D + c0 + 1] = P[7][1];
+            }
+            __syncthreads();
+            if (act) {
+                float Gb[2], EaK[2], mt[3][2];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int c = c0 + j;
+                    const float E0 = sE[c], E1 = sE[D + c], E2 = sE[2 * D + c], E3 = sE[3 * D + c];
+                    Gb[j] = R == 0 ? 1.0f : R == 1 ? E0 : R == 2 ? E0 * E1 : E0 * E1 * E2;
+                    EaK[j] = R == 0 ? E0 * E1 * E2 * E3 : R == 1 ? E1 * E2 * E3 : R == 2 ? E2 * E3 : E3;
+                    float m = 1.0f;
+#pragma unroll
+                    for (int t = 0; t < 3; ++t) {
+                        const int Rt = R + t;
+                        m *= Rt == 0 ? E0 : Rt == 1 ? E1 : Rt == 2 ? E2 : E3;
+                        mt[t][j] = m;
+                    }
+                    if (R == 0 && hf2 == 0) sgend[c] = E0 * E1 * E2 * E3;
+                }
+                auto st2 = [](uint8_t *p, float a, float b) {
+                    *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(a, b);
+                };
+                uint8_t *const pq_raw = rawq + cboff64, *const pk_raw = rawk + cboff64;
+                uint8_t *const p_qh = qkh + cboff128, *const p_kh = qkh + cboff128 + 64 * 128;
+                uint8_t *const p_qg = pair + cboff128, *const p_kt = pair + cboff128 + 64 * 128;
+                uint8_t *const p_bk = bkg + cboff64, *const p_kr = kr + cboff160;
+                // second-half lanes: swap register rows rho <-> rho ^ 4 so the
+                // store pass can index P[rho] with a compile-time rho
+                if (pr) {
+#pragma unroll
+                    for (int rho = 0; rho < 4; ++rho) {
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            float t = P[rho][j]; P[rho][j] = P[rho + 4][j]; P[rho + 4][j] = t;
+                            t = Pi[rho][j]; Pi[rho][j] = Pi[rho + 4][j]; Pi[rho + 4][j] = t;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int rho = 0; rho < 8; ++rho) {
+                    const int r = r0 + (rho ^ pr);
+                    const uint32_t o = (uint32_t)r * 128u + (((ch ^ (uint32_t)(rho ^ pr)) << 4) + ((uint32_t)c0 & 7u) * 2u);
+                    float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(pq_raw + o));
+                    float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(pk_raw + o));
+                    if (silu) {
+                        qv.x = silu_fast(qv.x); qv.y = silu_fast(qv.y);
+                        kv.x = silu_fast(kv.x); kv.y = silu_fast(kv.y);
+                    }
+                    const float qn = sqn[r], kn = skn[r], be = sbeta[r];
+                    qv.x *= qn; qv.y *= qn; kv.x *= kn; kv.y *= kn;
+                    const float a0 = qv.x * P[rho][0], a1 = qv.y * P[rho][1];     // Q^
+                    const float b0 = kv.x * P[rho][0], b1 = kv.y * P[rho][1];     // K^
+                    const float k0 = kv.x * Pi[rho][0], k1 = kv.y * Pi[rho][1];   // K_R own block
+                    st2(p_qh + o, a0, a1);
+                    st2(p_kh + o, b0, b1);
+                    st2(p_qg + o, a0 * Gb[0], a1 * Gb[1]);                  // Q e^b
+                    st2(p_kt + o, k0 * EaK[0], k1 * EaK[1]);                // K e^{b_end-b}
+                    st2(p_bk + o, be * b0 * Gb[0], be * b1 * Gb[1]);        // beta K e^b
+                    st2(p_kr + (uint32_t)(8 * R * (R + 1)) * 128u + o, k0, k1);
+#pragma unroll
+                    for (int t = 0; t < 3; ++t) {
+                        const int R2 = R + 1 + t;
+                        if (R2 < 4)
+                            st2(p_kr + (uint32_t)(8 * R2 * (R2 + 1)) * 128u + o, k0 * mt[t][0], k1 * mt[t][1]);
+                    }
+                }
+            }
+            // beta V
+            for (int u = tid; u < C * D / 8; u += NT) {
+                const uint32_t off = (uint32_t)u * 16u;
+                const int r = (int)((off & 8191u) >> 7);
+                float vv[8];
+                unpack8(*reinterpret_cast<const uint4 *>(rawv + off), vv);
+                const float be = sbeta[r];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) vv[i] *= be;
+                *reinterpret_cast<uint4 *>(bv + off) = pack8(vv);
+            }
+        }
+        phase_sync();
+        // raw tiles consumed: fetch the next task's while this one computes
+        if (tid == 0) {
+            *sinfo = nxt;
+            if (nxt.y > 0) {
+                issue_tma(nxt.x, nxt.z);
+                tma_pending = true;
+            }
+        }
+        // ---------------------------------------------- B: block products
+        // Issue loops are kept rolled and short: this code runs on one thread,
+        // so every instruction of it is fetched without help from other warps.
+        if (tid == 0) {
+            // gated: the packed K_R tile is one 160-row operand, so all four block
+            // products form one N = 160 product (block R at column 8R(R+1));
+            // ungated: one product [q^; k^] x k^T (N = 64)
+            const uint32_t id = GATED ? idesc_bf16(128, 160, false, false) : idesc_bf16(128, 64, false, false);
+            const int bRows = GATED ? 160 : 128;
+            const uint64_t a0 = GATED ? kdesc(qkh, 128, 0, 0) : kdesc(pair, 128, 0, 0);
+            const uint64_t b0 = GATED ? kdesc(kr, 160, 0, 0) : kdesc(pair, 128, 64, 0);
+#pragma unroll 1
+            for (int kb = 0; kb < D / 64; ++kb) {
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4)
+                    mma_bf16(tmem + TC_A, dstep(a0, kstep_units(128, 4 * kb + s4)),
+                             dstep(b0, kstep_units(bRows, 4 * kb + s4)), id, (kb | s4) != 0);
+            }
+            mma_commit(bar_mma);
+        }
+        if (__syncthreads_or(!mma_wait())) { failed = true; break; }
+        tc_fence_after();
+        // the next task is known to every thread now: prefetch its beta
+        const int4 nx = *sinfo;
+        const float beta_nx = load_beta(nx);
+        // ---------------------------------------------- C1: Aq tile, A rows, T_RR
+        // TMEM lanes 0..63 hold rows of Aq, lanes 64..127 rows of A (before
+        // beta).  Gated: block R's product sits at column 8R(R+1).  A warp
+        // spans two blocks, so it reads both (TMEM addresses stay
+        // warp-uniform) and each lane keeps its own.
+        //  - every warp: 16 columns (part cp) of its quarter -> Aq tile / A rows
+        //  - warps 2, 3 then invert the diagonal 16x16 blocks, read straight
+        //    from TMEM: T_RR = (I + A_RR)^{-1}, lane rho of each 16-lane group
+        //    owning row rho (forward substitution with shuffles)
+        {
+            const bool is_q = qd < 2;
+            const int rb0 = 32 * (is_q ? qd : qd - 2);
+            const int r = rb0 + lane, R = r >> 4, rho = r & 15;
+            const int Rw = rb0 >> 4;
+            auto colof = [](int Rb) { return GATED ? 8 * Rb * (Rb + 1) : 0; };
+            {
+                const int col = 16 * cp;
+                float v[16];
+                if (GATED) {
+                    float w0[16], w1[16];
+                    // parts beyond a block's product are masked below (col + i > r)
+                    tmem_ld16(tq + TC_A + colof(Rw) + col, w0);
+                    tmem_ld16(tq + TC_A + colof(Rw + 1) + col, w1);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = (R == Rw) ? w0[i] : w1[i];
+                } else {
+                    tmem_ld16(tq + TC_A + col, v);
+                }
+                if (is_q) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (col + i > r) v[i] = 0.0f;
+                    st_bf16x8(aqk, 64, r, col, v);
+                    st_bf16x8(aqk, 64, r, col + 8, v + 8);
+                } else {
+                    const float be = sbeta[r];
+                    float4 *dst = reinterpret_cast<float4 *>(sA + r * LDT + col);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        float4 f;
+                        f.x = (col + 4 * i + 0 < r) ? be * v[4 * i + 0] : 0.0f;
+                        f.y = (col + 4 * i + 1 < r) ? be * v[4 * i + 1] : 0.0f;
+                        f.z = (col + 4 * i + 2 < r) ? be * v[4 * i + 2] : 0.0f;
+                        f.w = (col + 4 * i + 3 < r) ? be * v[4 * i + 3] : 0.0f;
+                        dst[i] = f;
+                    }
+                }
+            }
+            if (warp == 2 || warp == 3) {
+                // diagonal block values, beta-scaled and strict, staged per lane
+                // in shared memory so the substitution loop can stay rolled
+                float *dgs = sX + (warp - 2) * 32 * 17 + lane * 17;
+                {
+                    float w0[16], w1[16];
+                    tmem_ld16(tq + TC_A + colof(Rw) + 16 * Rw, w0);
+                    tmem_ld16(tq + TC_A + colof(Rw + 1) + 16 * (Rw + 1), w1);
+                    const float be = sbeta[r];
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) dgs[m] = (m < rho) ? be * ((R == Rw) ? w0[m] : w1[m]) : 0.0f;
+                }
+                float t[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) t[j] = (j == rho) ? 1.0f : 0.0f;
+                const int gbase = lane & 16;
+#pragma unroll 1
+                for (int m = 0; m < 15; ++m) {
+                    const float a = dgs[m];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float tm = __shfl_sync(0xffffffffu, t[j], gbase + m);
+                        if (j <= m) t[j] -= a * tm;
+                    }
+                }
+                float4 *dst = reinterpret_cast<float4 *>(sT + r * LDT);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) dst[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < 16; j += 4) dst[(16 * R + j) >> 2] = make_float4(t[j], t[j + 1], t[j + 2], t[j + 3]);
+            }
+        }
+        __syncthreads();
+        // ---------------------------------------------- C2: off-diagonal blocks of T
+        // Two merges, as warp-level TF32 products (the blocks are 16 and 32
+        // wide; T is rounded to bf16 afterwards, coarser than TF32).
+        // (1) T_10 = -T_11 (A_10 T_00), T_32 = -T_33 (A_32 T_22)   (warps 0, 1)
+        // (2) with T_TT = T[0:32,0:32], T_BB = T[32:64,32:64]:
+        //     T[32:64, 0:32] = -T_BB (A[32:64, 0:32] T_TT)           (warps 0..7)
+        {
+            constexpr int LX = 24, LY = 40;
+            float *sX1 = sX;                 // [2][16][LX]
+            float *sY = sX + 2 * 16 * LX;    // [32][LY]
+            if (warp < 2) {
+                const int b = warp, R = 1 + 2 * b, J = 2 * b;
+                float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    const float *Ab = sA + (16 * R) * LDT + 16 * J + 8 * ks;
+                    const float *Bb = sT + (16 * J + 8 * ks) * LDT + 16 * J;
+                    mma_tf32(d0, Ab, LDT, Bb, LDT, lane);
+                    mma_tf32(d1, Ab, LDT, Bb + 8, LDT, lane);
+                }
+                store_c(sX1 + b * 16 * LX, LX, d0, 1.0f, lane);
+                store_c(sX1 + b * 16 * LX + 8, LX, d1, 1.0f, lane);
+                __syncwarp();
+                float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    const float *Ab = sT + (16 * R) * LDT + 16 * R + 8 * ks;
+                    const float *Bb = sX1 + b * 16 * LX + (8 * ks) * LX;
+                    mma_tf32(e0, Ab, LDT, Bb, LX, lane);
+                    mma_tf32(e1, Ab, LDT, Bb + 8, LX, lane);
+                }
+                store_c(sT + (16 * R) * LDT + 16 * J, LDT, e0, -1.0f, lane);
+                store_c(sT + (16 * R) * LDT + 16 * J + 8, LDT, e1, -1.0f, lane);
+            }
+            __syncthreads();
+            const int mt = (warp >> 2) & 1, nt = warp & 3;
+            if (warp < 8) {
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_tf32(d, sA + (32 + 16 * mt) * LDT + 8 * ks, LDT,
+                             sT + (8 * ks) * LDT + 8 * nt, LDT, lane);
+                store_c(sY + (16 * mt) * LY + 8 * nt, LY, d, 1.0f, lane);
+            }
+            __syncthreads();
+            if (warp < 8) {
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_tf32(d, sT + (32 + 16 * mt) * LDT + 32 + 8 * ks, LDT,
+                             sY + (8 * ks) * LY + 8 * nt, LY, lane);
+                store_c(sT + (32 + 16 * mt) * LDT + 8 * nt, LDT, d, -1.0f, lane);
+            }
+            __syncthreads();
+        }
+        // ---------------------------------------------- C3: T to bf16 operand
+        {
+            const int r = tid >> 3, c = (tid & 7) * 8;
+            st_bf16x8(t16, 64, r, c, sT + r * LDT + c);
+        }
+        phase_sync();
+        // ---------------------------------------------- D: W = T (beta K e^b), U = T (beta V)
+        if (tid == 0) {
+            // beta K e^b and beta V are adjacent column blocks: one N = 2D
+            // product writes W (columns TC_W) and U (columns TC_W + D)
+            constexpr uint32_t id = idesc_bf16(64, 2 * D, false, true);
+            const uint64_t a0 = kdesc(t16, 64, 0, 0), b0 = mdesc(bkg, C, 0, 0);
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4)
+                mma_bf16(tmem + TC_W, dstep(a0, s4 * 2), dstep(b0, s4 * 128), id, s4 > 0);
+            mma_commit(bar_mma);
+        }
+        if (__syncthreads_or(!mma_wait())) { failed = true; break; }
+        tc_fence_after();
+        // ---------------------------------------------- E: W and U tiles
+        {
+            // column parts 0, 1: W; 2, 3: U (D/2 columns each)
+            const int r = acc_row(64, qd, lane);
+            uint8_t *dst = cp < 2 ? wt : ut;
+            const int c0 = (cp & 1) * (D / 2);
+#pragma unroll
+            for (int cb = 0; cb < D / 2; cb += 32) {
+                float v[32];
+                tmem_ld32(tq + TC_W + (cp >> 1) * D + c0 + cb, v);
+                if (r >= 0) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) st_bf16x8(dst, C, r, c0 + cb + i, v + i);
+                }
+            }
+        }
+        phase_sync();
+        // ---------------------------------------------- F: record out
+        if (tid == 0) {
+            uint8_t *rec = p.records + ((int64_t)cur.w * H + h) * Rec::BYTES;
+            bulk_store(rec + Rec::PAIR, pair, 4 * L::tile64);
+            bulk_store(rec + Rec::AQ, aqk, 8192);
+            if (GATED) bulk_store(rec + Rec::GEND, sgend, 4 * D);
+            bulk_commit();
+        }
+        cur = nx;
+        beta_cur = beta_nx;
+        t = t_next;
+    }
+
+    if (tid == 0) {
+        if (failed && tma_pending) mbar_wait(bar_tma, tma_par, p.err, 3);
+        bulk_wait_all();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// One warp per sequence: the table entries of its chunk slots, then zeros
+// for the (at most two) unused slots before the next sequence's first one.
+__global__ void chunk_table_kernel(const int32_t *cu, int N, int ntok, int64_t slots,
+                                   int2 *table) {
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (gw >= N) return;
+    const int n = (int)gw;
+    const int a = cu[n], e = cu[n + 1];
+    if (n == 0 && a >= 0 && a <= ntok)
+        for (int64_t s = lane; s < a / C; s += 32) table[s] = make_int2(0, 0);
+    if (a < 0 || e < a || e > ntok) return;  // reported by the inter-chunk kernel
+    const int64_t b = (int64_t)(a / C) + n;
+    const int nc = (e - a + C - 1) / C;
+    for (int j = lane; j < nc; j += 32) table[b + j] = make_int2(a + C * j, min(C, e - a - C * j));
+    const int64_t gap_end = n + 1 < N ? (int64_t)(e / C) + n + 1 : slots;
+    for (int64_t s = b + nc + lane; s < gap_end; s += 32) table[s] = make_int2(0, 0);
+}
+
+template <int D, bool GATED>
+cudaError_t launch_t(const TcLaunch &x, cudaStream_t s) {
+    IntraParams p{static_cast<const __nv_bfloat16 *>(x.a->beta_logits), x.table, x.records,
+                  x.err, x.slots * x.a->H, x.a->H, x.a->ntok, x.a->flags};
+    // At least 120 KB so that one CTA (and its TMEM) owns an SM.
+    constexpr size_t need = Layout<D, GATED>::TOTAL + 1024;
+    const size_t smem = need > 120 * 1024 ? need : 120 * 1024;
+    auto kern = delta_intra_kernel<D, GATED>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int64_t tasks = p.n_tasks;
+    const unsigned grid = (unsigned)(tasks < x.sms ? tasks : x.sms);
+    if (grid == 0) return cudaSuccess;
+    kern<<<grid, NT, smem, s>>>(x.mq, x.mk, x.mv, x.mg, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_table(const TcLaunch &x, cudaStream_t s) {
+    const int64_t threads = (int64_t)x.a->N * 32;
+    const unsigned blocks = (unsigned)((threads + 255) / 256);
+    chunk_table_kernel<<<blocks, 256, 0, s>>>(x.a->cu_seqlens, x.a->N, x.a->ntok, x.slots,
+                                              x.table);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_delta_intra(const TcLaunch &x, cudaStream_t s) {
+    const bool g = x.a->gate_logits != nullptr;
+    if (x.a->dk == 128) return g ? launch_t<128, true>(x, s) : launch_t<128, false>(x, s);
+    return g ? launch_t<64, true>(x, s) : launch_t<64, false>(x, s);
+}
+
+}  // namespace la

@@ -18,6 +18,8 @@ struct PrefillArgs {
     const float *init_S, *init_z;
     float *final_S, *final_z;
     bool bf16;
+    void *workspace;          // device scratch (tensor-core delta path)
+    size_t workspace_bytes;
 };
 
 struct DecodeArgs {
@@ -33,7 +35,10 @@ struct DecodeArgs {
 // fp32 SIMT chunk kernels (any I/O dtype).
 cudaError_t launch_linear_simt(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_delta_simt(const PrefillArgs &a, cudaStream_t s);
-// tcgen05 tensor-core chunk kernel (bf16 I/O, dk == dv in {64, 128}).
+// tcgen05 tensor-core chunk kernels (bf16 I/O, dk == dv in {64, 128}): a
+// chunk table, the intra-chunk kernel and the inter-chunk kernel, with the
+// per-chunk records in the caller's workspace.
+size_t delta_tc_workspace_bytes(int N, int ntok, int H, int dk, int dv, int chunk, bool bf16);
 bool delta_tc_supported(const PrefillArgs &a);
 cudaError_t launch_delta_tc(const PrefillArgs &a, cudaStream_t s);
 // Device address of the library's error word on the current device (kernels

@@ -96,9 +96,11 @@ la_status la_prefill_linear(const void *q, const void *k, const void *v, void *o
  * chunk: tokens per chunk; 64 is the supported value.
  * scale: output scale (the page's delta-rule listings use 1.0).
  * init_S: nullable [N][H][dk][dv]; final_S: nullable, may equal init_S.
- * workspace / workspace_bytes: scratch of at least
+ * workspace / workspace_bytes: device scratch of at least
  * la_prefill_delta_workspace_size(...) bytes, 256-byte aligned; may be NULL
- * when that size is 0. */
+ * only when that size is 0 (else LA_ERR_INVALID_ARG, nothing launched).  It
+ * needs no initialisation and holds nothing useful afterwards; calls that
+ * may run at the same time (other streams) need separate workspaces. */
 la_status la_prefill_delta(const void *q, const void *k, const void *v, const void *beta_logits,
                            const void *gate_logits, void *o, la_dtype io,
                            const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int N,
@@ -106,8 +108,14 @@ la_status la_prefill_delta(const void *q, const void *k, const void *v, const vo
                            unsigned flags, const float *init_S, float *final_S, void *workspace,
                            size_t workspace_bytes, void *stream);
 
-/* Scratch bytes la_prefill_delta needs for these sizes (0 if none).
- * ntok = total packed tokens. */
+/* Scratch bytes la_prefill_delta needs for these sizes; ntok = total packed
+ * tokens.  Nonzero exactly for the tensor-core configuration (io = LA_BF16,
+ * dk = dv in {64, 128}, chunk = 64), whose first pass computes everything
+ * that depends on one chunk alone (the WY/UT operands of eq. 10 and the
+ * decayed q, k of the chunk) for all chunks in parallel and hands it to the
+ * sequential state pass through this buffer: a table of 8 bytes per chunk
+ * slot, then one record per (chunk slot, head) of 41 KB (d = 64) or 73 KB
+ * (d = 128), with at most ntok/64 + N + 1 slots.  0 otherwise. */
 size_t la_prefill_delta_workspace_size(int N, int ntok, int H, int dk, int dv, int chunk,
                                        la_dtype io);
 

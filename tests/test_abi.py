@@ -105,9 +105,29 @@ def test_decode_and_linear_reject_bad_arguments(lib):
                                  None, None, None, None, None) == la.LA_ERR_UNSUPPORTED
 
 
-def test_workspace_size_independent_of_sequence_length(lib):
-    """The recurrent state is fixed-size: no buffer the library asks for
-    grows with the number of tokens beyond per-chunk bookkeeping."""
-    a = la.la_prefill_delta_workspace_size(4, 1024, 32, 128, 128)
-    b = la.la_prefill_delta_workspace_size(4, 1024 * 64, 32, 128, 128)
-    assert a == b
+def test_workspace_size_covers_the_chunk_records(lib):
+    """The tensor-core path (bf16 I/O, dk == dv in {64, 128}) keeps one record
+    per (64-token chunk slot, head); every other configuration needs none."""
+    ws = la.la_prefill_delta_workspace_size
+    assert ws(4, 1024, 32, 128, 128, 64, la.LA_F32) == 0
+    assert ws(4, 1024, 32, 64, 128, 64, la.LA_BF16) == 0
+    rec = {64: 4 * 64 * 64 * 2 + 8192 + 4 * 64, 128: 4 * 64 * 128 * 2 + 8192 + 4 * 128}
+    for D in (64, 128):
+        rec_bytes = (rec[D] + 1023) // 1024 * 1024
+        for N, ntok, H in ((1, 64, 1), (4, 1024, 32), (5, 65536, 16), (3, 100, 2)):
+            slots = ntok // 64 + N + 1
+            table = (slots * 8 + 1023) // 1024 * 1024
+            assert ws(N, ntok, H, D, D, 64, la.LA_BF16) == table + slots * H * rec_bytes
+
+
+def test_prefill_rejects_missing_workspace(lib):
+    """A call that needs a workspace and gets none (or too little, or a
+    misaligned one) is refused on the host before any launch."""
+    need = la.la_prefill_delta_workspace_size(2, 256, 4, 64, 64, 64, la.LA_BF16)
+    assert need > 0
+    d = lib.la_prefill_delta
+    args = (FAKE, FAKE, FAKE, FAKE, None, FAKE, la.LA_BF16, FAKE, None, 2, 256, 4, 64, 64, 64,
+            1.0, 1, None, None)
+    assert d(*args, None, 0, None) == la.LA_ERR_INVALID_ARG
+    assert d(*args, FAKE, need - 1, None) == la.LA_ERR_INVALID_ARG
+    assert d(*args, ctypes.c_void_p(0x1010), need, None) == la.LA_ERR_INVALID_ARG
