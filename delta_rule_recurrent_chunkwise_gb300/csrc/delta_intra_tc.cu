@@ -33,9 +33,13 @@
 // channel stays above ~1e-30 (mean alpha above ~0.013), and is clamped
 // (never inf/NaN) beyond.
 //
-// Mapping: a persistent grid (one CTA of 512 threads per SM) walks the
-// (chunk slot, head) tasks; the next task's raw q, k, v, gate tiles arrive
-// by TMA while the current one computes.  Products on tcgen05 (bf16 x bf16
+// Mapping: a persistent grid walks the (chunk slot, head) tasks; the next
+// task's raw q, k, v, gate tiles arrive by TMA while the current one
+// computes.  Every phase is short and bound by latency and by its CTA
+// barriers (several phases keep only a few warps busy), so where shared
+// memory and tensor memory allow (d = 64 without gate) the CTA is 256
+// threads and two of them share an SM, each filling the other's idle
+// phases; otherwise one CTA of 512 threads per SM.  Products on tcgen05 (bf16 x bf16
 // -> fp32 in TMEM): [Q;K]-hat x K_R^T (one N = 160 product when gated) and
 // T x [beta K e^b | beta V] (one N = 2D product).  The triangular solve runs
 // in fp32 on CUDA cores: the four diagonal 16x16 blocks by warp-shuffle
@@ -54,8 +58,6 @@ namespace {
 using namespace tc;
 using namespace tile;
 
-constexpr int NT = 512;          // threads per CTA (16 warps)
-constexpr int TMEM_COLS = 256;   // block products (<= 160 columns), then W | U
 constexpr int LDT = 68;          // fp32 row stride of the A and T scratch (16-byte rows)
 constexpr uint32_t TC_A = 0, TC_W = 0;  // TMEM columns; U follows W
 
@@ -77,9 +79,9 @@ struct Layout {
     static constexpr uint32_t AQK = X + 8192;           // Aq, bf16 [64][64]
     static constexpr uint32_t SA = X + 16384;           // A, fp32 [64][LDT]
     static constexpr uint32_t ST = SA + 64 * LDT * 4;   // T, fp32 [64][LDT]
-    static constexpr uint32_t SX = ST + 64 * LDT * 4;   // merge temps, fp32 (8 KB)
+    static constexpr uint32_t SX = T16;                 // solve temps, fp32 (8 KB; dead before T16)
     static constexpr uint32_t X_END_A = GATED ? KR + 160 * D * 2 : X;
-    static constexpr uint32_t X_END_C = SX + 8192;
+    static constexpr uint32_t X_END_C = ST + 64 * LDT * 4;
     static constexpr uint32_t X_END = X_END_A > X_END_C ? X_END_A : X_END_C;
     // [Q e^b ; K e^{b_end - b}] (gated) or [q^ ; k^] (ungated), 128 rows, then
     // beta K e^b (later W) and beta V (later U): the record's first four
@@ -94,10 +96,23 @@ struct Layout {
     static constexpr uint32_t EB = QN + 256;                   // fp32 [4][D] block decay
     static constexpr uint32_t GEND = EB + 16 * D;              // fp32 [D] chunk decay
     static constexpr uint32_t INFO = GEND + 4 * D;             // int4: next task
-    static constexpr uint32_t BARS = INFO + 16;                // 2 mbarriers + tmem slot
-    static constexpr uint32_t TOTAL = BARS + 64;
+    static constexpr uint32_t BAR_TMA = INFO + 16;             // mbarrier: raw tiles
+    static constexpr uint32_t TASK_BYTES = (BAR_TMA + 8 + 1023) & ~1023u;
     static_assert(BKG - PAIR == Record<D>::W && BV - PAIR == Record<D>::U, "record image");
+    // threads per CTA, CTAs per SM, TMEM columns (block products, then W | U)
+    static constexpr bool SMALL_CTA = D == 64 && !GATED;
+    static constexpr int NT = SMALL_CTA ? 256 : 512;
+    static constexpr int CTAS_PER_SM = SMALL_CTA ? 2 : 1;
+    static constexpr uint32_t TMEM_COLS = SMALL_CTA ? 128 : 256;
+    // tasks side by side in one CTA (lockstep) and threads / warps per task
+    static constexpr int P = 1;
+    static constexpr int NTC = NT / P, NW = NTC / 32;
+    static constexpr uint32_t TCOLS = TMEM_COLS / P;
+    static constexpr uint32_t COMMON = P * TASK_BYTES;         // mbarrier (products) + tmem slot
+    static constexpr uint32_t TOTAL = COMMON + 64;
     static_assert(TOTAL + 1024 <= 227 * 1024, "shared memory budget");
+    static_assert(CTAS_PER_SM * (TOTAL + 2048) <= 228 * 1024, "CTAs per SM");
+    static_assert(TCOLS >= (GATED ? 160u : 64u) && TCOLS >= 2u * D, "TMEM columns per task");
 };
 
 __device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
@@ -145,16 +160,23 @@ struct IntraParams {
 
 
 template <int D, bool GATED>
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_PER_SM)
     delta_intra_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_g, IntraParams p) {
     using L = Layout<D, GATED>;
     using Rec = Record<D>;
+    constexpr int P = L::P, NTC = L::NTC, NW = L::NW;
+    constexpr uint32_t TMEM_COLS = L::TMEM_COLS;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>(
+    uint8_t *const sbase = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // this thread's task slot in the CTA, its warp and thread index within it
+    const int kslot = warp / NW, lw = warp % NW, ltid = tid % NTC;
+    const bool leader = ltid == 0;
+    uint8_t *sm = sbase + kslot * L::TASK_BYTES;
     uint8_t *rawq = sm + L::RAW_Q, *rawk = sm + L::RAW_K, *rawv = sm + L::RAW_V,
             *rawg = sm + L::RAW_G;
     uint8_t *qkh = sm + L::QKH, *kr = sm + L::KR, *t16 = sm + L::T16, *aqk = sm + L::AQK;
@@ -169,26 +191,25 @@ __global__ void __launch_bounds__(NT, 1)
     float *sE = reinterpret_cast<float *>(sm + L::EB);
     float *sgend = reinterpret_cast<float *>(sm + L::GEND);
     int4 *sinfo = reinterpret_cast<int4 *>(sm + L::INFO);
-    uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + L::BARS);
-    uint64_t *bar_mma = bar_tma + 1;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar_tma + 2);
+    uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + L::BAR_TMA);
+    uint64_t *bar_mma = reinterpret_cast<uint64_t *>(sbase + L::COMMON);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar_mma + 1);
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int qd = warp & 3, cp = warp >> 2;  // TMEM lane quarter, column part
+    const int qd = lw & 3, cp = lw >> 2;  // TMEM lane quarter, column part
     const int H = p.H;
     const bool silu = (p.flags & kSiluQK) != 0;
     const bool l2k = (p.flags & kL2NormK) != 0, l2q = (p.flags & kL2NormQ) != 0;
     constexpr uint32_t tx_bytes = (GATED ? 4u : 3u) * L::tile64;
 
+    if (leader) mbar_init(bar_tma, 1);
     if (tid == 0) {
-        mbar_init(bar_tma, 1);
         mbar_init(bar_mma, 1);
-        fence_mbar_init();
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         if (GATED) tma_prefetch_desc(&tm_g);
     }
+    if (leader) fence_mbar_init();
     if (warp == 0) {
         tmem_alloc(tslot, TMEM_COLS);
         tmem_relinquish();
@@ -197,7 +218,11 @@ __global__ void __launch_bounds__(NT, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);  // this warp's lane quarter
+    // this task's TMEM columns, and this warp's lane quarter of them
+    const uint32_t tq = tmem + kslot * L::TCOLS + ((uint32_t)(32 * qd) << 16);
+    // shared-memory region and TMEM columns of task slot kk (for the issuing thread)
+    auto task_sm = [&](int kk) { return sbase + kk * L::TASK_BYTES; };
+    auto task_tmem = [&](int kk) { return tmem + kk * L::TCOLS; };
 
     // Task t = slot * H + head.  {first token, length, head, slot}; length 0
     // marks a slot no chunk occupies (or a table entry out of range).
@@ -223,19 +248,23 @@ __global__ void __launch_bounds__(NT, 1)
         }
     };
     auto load_beta = [&](const int4 &ti) -> float {
-        return (tid < C && tid < ti.y)
-                   ? __bfloat162float(p.beta_logits[(int64_t)(ti.x + tid) * H + ti.z])
+        return (ltid < C && ltid < ti.y)
+                   ? __bfloat162float(p.beta_logits[(int64_t)(ti.x + ltid) * H + ti.z])
                    : 0.0f;
     };
 
-    int64_t t = blockIdx.x;
-    int4 cur = task_info(t);
-    bool tma_pending = false;  // meaningful in thread 0, which issues and waits
-    if (tid == 0 && cur.y > 0) {
+    // The CTA takes task groups g = blockIdx.x, + gridDim.x, ...; task slot
+    // kslot of group g is task g * P + kslot.  Each task's leader thread
+    // issues and waits for its raw tiles and stores its record.
+    const int64_t n_groups = (p.n_tasks + P - 1) / P;
+    int64_t g = blockIdx.x;
+    int4 cur = task_info(g * P + kslot);
+    bool tma_pending = false;  // meaningful in the leader
+    if (leader && cur.y > 0) {
         issue_tma(cur.x, cur.z);
         tma_pending = true;
     }
-    float beta_cur = load_beta(cur);  // threads 0..63
+    float beta_cur = load_beta(cur);  // threads 0..63 of the task
     uint32_t tma_par = 0, mma_par = 0;
     bool failed = false;
 
@@ -255,13 +284,13 @@ __global__ void __launch_bounds__(NT, 1)
         tc_fence_after();
     };
 
-    while (t < p.n_tasks) {
-        const int64_t t_next = t + gridDim.x;
+    while (g < n_groups) {
+        const int64_t g_next = g + gridDim.x;
         int4 nxt = make_int4(0, 0, 0, 0);
-        if (tid == 0) nxt = task_info(t_next);  // consumed after the operand stage
-        if (cur.y == 0) {
-            // empty slot: nothing to compute, start the next task's loads
-            if (tid == 0) {
+        if (leader) nxt = task_info(g_next * P + kslot);  // consumed after the operand stage
+        if (!__syncthreads_or(cur.y > 0)) {
+            // empty slots only: nothing to compute, start the next tasks' loads
+            if (leader) {
                 *sinfo = nxt;
                 if (nxt.y > 0) {
                     issue_tma(nxt.x, nxt.z);
@@ -271,28 +300,34 @@ __global__ void __launch_bounds__(NT, 1)
             __syncthreads();
             cur = *sinfo;
             beta_cur = load_beta(cur);
-            t = t_next;
+            g = g_next;
             __syncthreads();
             continue;
         }
+        // A slot with no task (len 0) runs along on whatever its buffers
+        // hold; nothing of it is stored.
         const int len = cur.y, h = cur.z;
         // ---------------------------------------------- raw tiles of this chunk
         {
-            const bool ok = tid == 0 ? mbar_wait(bar_tma, tma_par, p.err, 1) : true;
-            tma_par ^= 1;
-            tma_pending = false;
+            bool ok = true;
+            if (leader && len > 0) {
+                ok = mbar_wait(bar_tma, tma_par, p.err, 1);
+                tma_par ^= 1;
+                tma_pending = false;
+            }
             tc_fence_before();
             if (__syncthreads_or(!ok)) { failed = true; break; }
             tc_fence_after();
         }
         // ---------------------------------------------- A0: beta, row norms
-        if (tid < C) sbeta[tid] = tid < len ? __fdividef(1.0f, 1.0f + __expf(-beta_cur)) : 0.0f;
+        if (ltid < C) sbeta[ltid] = ltid < len ? __fdividef(1.0f, 1.0f + __expf(-beta_cur)) : 0.0f;
         {
-            // 8 threads per row, D/8 channels each, 16-byte loads
-            const int r = tid >> 3, part = tid & 7;
+            // TPR threads per row, D/TPR channels each, 16-byte loads
+            constexpr int TPR = NTC / C;
+            const int r = ltid / TPR, part = ltid % TPR;
             float ssk = 0.0f, ssq = 0.0f;
 #pragma unroll
-            for (int c = part * (D / 8); c < (part + 1) * (D / 8); c += 8) {
+            for (int c = part * (D / TPR); c < (part + 1) * (D / TPR); c += 8) {
                 float kv[8], qv[8];
                 unpack8(*reinterpret_cast<const uint4 *>(rawk + rs_off(C, r, c)), kv);
                 unpack8(*reinterpret_cast<const uint4 *>(rawq + rs_off(C, r, c)), qv);
@@ -304,7 +339,7 @@ __global__ void __launch_bounds__(NT, 1)
                 }
             }
 #pragma unroll
-            for (int o = 1; o < 8; o <<= 1) {
+            for (int o = 1; o < TPR; o <<= 1) {
                 ssk += __shfl_xor_sync(0xffffffffu, ssk, o);
                 ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
             }
@@ -314,12 +349,12 @@ __global__ void __launch_bounds__(NT, 1)
                 sqn[r] = valid ? (l2q ? rsqrtf(fmaxf(ssq, 1e-24f)) : 1.0f) : 0.0f;
             }
         }
-        if (tid == 0) bulk_wait_read();  // previous record's sources are rewritten below
+        if (leader) bulk_wait_read();  // previous record's sources are rewritten below
         __syncthreads();
         // ---------------------------------------------- A1: operand tiles
         if (!GATED) {
             // [q^; k^] into PAIR, beta k^ into BKG, beta v into BV: 16-byte units
-            for (int u = tid; u < C * D / 8; u += NT) {
+            for (int u = ltid; u < C * D / 8; u += NTC) {
                 const uint32_t off = (uint32_t)u * 16u;                 // offset in a [64][D] tile
                 const uint32_t cb = off >> 13, in = off & 8191u;         // column block, offset in it
                 const int r = (int)(in >> 7);
@@ -343,7 +378,7 @@ __global__ void __launch_bounds__(NT, 1)
                 *reinterpret_cast<uint4 *>(bkg + off) = pack8(bk);
                 *reinterpret_cast<uint4 *>(bv + off) = pack8(vv);
             }
-            if (tid < D) sgend[tid] = 1.0f;
+            if (ltid < D) sgend[ltid] = 1.0f;
         } else {
             // One thread per (2 key channels, 8 rows of a 16-token block R); the
             // two 8-row halves of a block sit in lanes l and l^16 of one warp.
@@ -351,8 +386,9 @@ __global__ void __launch_bounds__(NT, 1)
             // inside the block, Pi = 1/P.  Every operand is (q or k) x (P or Pi)
             // x a per-(block, channel) constant; the within-block suffix is
             // prod_{t>r} alpha_t = E_R / P_r with E_R the block total.
-            const bool act = warp < D / 8;
-            const int R = (warp * 32 / D) & 3, grp = warp % (D / 32);
+            static_assert(NW * 8 >= D, "one thread per (channel pair, 8 rows)");
+            const bool act = lw < D / 8;
+            const int R = (lw * 32 / D) & 3, grp = lw % (D / 32);
             const int hf2 = lane >> 4, c0 = 32 * grp + 2 * (lane & 15);
             const int r0 = 16 * R + 8 * hf2;
             // Rows r0 and r0 + 8 share a swizzle phase, so at step rho the
@@ -475,7 +511,7 @@ __global__ void __launch_bounds__(NT, 1)
                 }
             }
             // beta V
-            for (int u = tid; u < C * D / 8; u += NT) {
+            for (int u = ltid; u < C * D / 8; u += NTC) {
                 const uint32_t off = (uint32_t)u * 16u;
                 const int r = (int)((off & 8191u) >> 7);
                 float vv[8];
@@ -488,7 +524,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
         phase_sync();
         // raw tiles consumed: fetch the next task's while this one computes
-        if (tid == 0) {
+        if (leader) {
             *sinfo = nxt;
             if (nxt.y > 0) {
                 issue_tma(nxt.x, nxt.z);
@@ -504,14 +540,18 @@ __global__ void __launch_bounds__(NT, 1)
             // ungated: one product [q^; k^] x k^T (N = 64)
             const uint32_t id = GATED ? idesc_bf16(128, 160, false, false) : idesc_bf16(128, 64, false, false);
             const int bRows = GATED ? 160 : 128;
-            const uint64_t a0 = GATED ? kdesc(qkh, 128, 0, 0) : kdesc(pair, 128, 0, 0);
-            const uint64_t b0 = GATED ? kdesc(kr, 160, 0, 0) : kdesc(pair, 128, 64, 0);
 #pragma unroll 1
-            for (int kb = 0; kb < D / 64; ++kb) {
+            for (int kk = 0; kk < P; ++kk) {
+                uint8_t *tsm = task_sm(kk);
+                const uint64_t a0 = GATED ? kdesc(tsm + L::QKH, 128, 0, 0) : kdesc(tsm + L::PAIR, 128, 0, 0);
+                const uint64_t b0 = GATED ? kdesc(tsm + L::KR, 160, 0, 0) : kdesc(tsm + L::PAIR, 128, 64, 0);
+#pragma unroll 1
+                for (int kb = 0; kb < D / 64; ++kb) {
 #pragma unroll
-                for (int s4 = 0; s4 < 4; ++s4)
-                    mma_bf16(tmem + TC_A, dstep(a0, kstep_units(128, 4 * kb + s4)),
-                             dstep(b0, kstep_units(bRows, 4 * kb + s4)), id, (kb | s4) != 0);
+                    for (int s4 = 0; s4 < 4; ++s4)
+                        mma_bf16(task_tmem(kk) + TC_A, dstep(a0, kstep_units(128, 4 * kb + s4)),
+                                 dstep(b0, kstep_units(bRows, 4 * kb + s4)), id, (kb | s4) != 0);
+                }
             }
             mma_commit(bar_mma);
         }
@@ -525,7 +565,8 @@ __global__ void __launch_bounds__(NT, 1)
         // beta).  Gated: block R's product sits at column 8R(R+1).  A warp
         // spans two blocks, so it reads both (TMEM addresses stay
         // warp-uniform) and each lane keeps its own.
-        //  - every warp: 16 columns (part cp) of its quarter -> Aq tile / A rows
+        //  - every warp: 64 / (NW / 4) columns (part cp) of its quarter -> Aq
+        //    tile / A rows
         //  - warps 2, 3 then invert the diagonal 16x16 blocks, read straight
         //    from TMEM: T_RR = (I + A_RR)^{-1}, lane rho of each 16-lane group
         //    owning row rho (forward substitution with shuffles)
@@ -535,8 +576,9 @@ __global__ void __launch_bounds__(NT, 1)
             const int r = rb0 + lane, R = r >> 4, rho = r & 15;
             const int Rw = rb0 >> 4;
             auto colof = [](int Rb) { return GATED ? 8 * Rb * (Rb + 1) : 0; };
-            {
-                const int col = 16 * cp;
+#pragma unroll
+            for (int sub = 0; sub < 16 / NW; ++sub) {
+                const int col = 16 * (cp + sub * (NW / 4));
                 float v[16];
                 if (GATED) {
                     float w0[16], w1[16];
@@ -568,10 +610,10 @@ __global__ void __launch_bounds__(NT, 1)
                     }
                 }
             }
-            if (warp == 2 || warp == 3) {
+            if (lw == 2 || lw == 3) {
                 // diagonal block values, beta-scaled and strict, staged per lane
                 // in shared memory so the substitution loop can stay rolled
-                float *dgs = sX + (warp - 2) * 32 * 17 + lane * 17;
+                float *dgs = sX + (lw - 2) * 32 * 17 + lane * 17;
                 {
                     float w0[16], w1[16];
                     tmem_ld16(tq + TC_A + colof(Rw) + 16 * Rw, w0);
@@ -611,8 +653,8 @@ __global__ void __launch_bounds__(NT, 1)
             constexpr int LX = 24, LY = 40;
             float *sX1 = sX;                 // [2][16][LX]
             float *sY = sX + 2 * 16 * LX;    // [32][LY]
-            if (warp < 2) {
-                const int b = warp, R = 1 + 2 * b, J = 2 * b;
+            if (lw < 2) {
+                const int b = lw, R = 1 + 2 * b, J = 2 * b;
                 float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks) {
@@ -636,8 +678,8 @@ __global__ void __launch_bounds__(NT, 1)
                 store_c(sT + (16 * R) * LDT + 16 * J + 8, LDT, e1, -1.0f, lane);
             }
             __syncthreads();
-            const int mt = (warp >> 2) & 1, nt = warp & 3;
-            if (warp < 8) {
+            const int mt = (lw >> 2) & 1, nt = lw & 3;
+            if (lw < 8) {
                 float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
@@ -646,7 +688,7 @@ __global__ void __launch_bounds__(NT, 1)
                 store_c(sY + (16 * mt) * LY + 8 * nt, LY, d, 1.0f, lane);
             }
             __syncthreads();
-            if (warp < 8) {
+            if (lw < 8) {
                 float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
@@ -657,8 +699,8 @@ __global__ void __launch_bounds__(NT, 1)
             __syncthreads();
         }
         // ---------------------------------------------- C3: T to bf16 operand
-        {
-            const int r = tid >> 3, c = (tid & 7) * 8;
+        for (int u = ltid; u < 64 * 8; u += NTC) {
+            const int r = u >> 3, c = (u & 7) * 8;
             st_bf16x8(t16, 64, r, c, sT + r * LDT + c);
         }
         phase_sync();
@@ -667,24 +709,30 @@ __global__ void __launch_bounds__(NT, 1)
             // beta K e^b and beta V are adjacent column blocks: one N = 2D
             // product writes W (columns TC_W) and U (columns TC_W + D)
             constexpr uint32_t id = idesc_bf16(64, 2 * D, false, true);
-            const uint64_t a0 = kdesc(t16, 64, 0, 0), b0 = mdesc(bkg, C, 0, 0);
+#pragma unroll 1
+            for (int kk = 0; kk < P; ++kk) {
+                const uint64_t a0 = kdesc(task_sm(kk) + L::T16, 64, 0, 0);
+                const uint64_t b0 = mdesc(task_sm(kk) + L::BKG, C, 0, 0);
 #pragma unroll
-            for (int s4 = 0; s4 < 4; ++s4)
-                mma_bf16(tmem + TC_W, dstep(a0, s4 * 2), dstep(b0, s4 * 128), id, s4 > 0);
+                for (int s4 = 0; s4 < 4; ++s4)
+                    mma_bf16(task_tmem(kk) + TC_W, dstep(a0, s4 * 2), dstep(b0, s4 * 128), id, s4 > 0);
+            }
             mma_commit(bar_mma);
         }
         if (__syncthreads_or(!mma_wait())) { failed = true; break; }
         tc_fence_after();
         // ---------------------------------------------- E: W and U tiles
         {
-            // column parts 0, 1: W; 2, 3: U (D/2 columns each)
+            // the 2D columns W | U split into NW / 4 parts of CPP columns
+            constexpr int CPP = 2 * D / (NW / 4);
             const int r = acc_row(64, qd, lane);
-            uint8_t *dst = cp < 2 ? wt : ut;
-            const int c0 = (cp & 1) * (D / 2);
+            const int w0 = cp * CPP;                   // first column of the part in W | U
+            uint8_t *dst = w0 < D ? wt : ut;
+            const int c0 = w0 % D;
 #pragma unroll
-            for (int cb = 0; cb < D / 2; cb += 32) {
+            for (int cb = 0; cb < CPP; cb += 32) {
                 float v[32];
-                tmem_ld32(tq + TC_W + (cp >> 1) * D + c0 + cb, v);
+                tmem_ld32(tq + TC_W + w0 + cb, v);
                 if (r >= 0) {
 #pragma unroll
                     for (int i = 0; i < 32; i += 8) st_bf16x8(dst, C, r, c0 + cb + i, v + i);
@@ -693,7 +741,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
         phase_sync();
         // ---------------------------------------------- F: record out
-        if (tid == 0) {
+        if (leader && len > 0) {
             uint8_t *rec = p.records + ((int64_t)cur.w * H + h) * Rec::BYTES;
             bulk_store(rec + Rec::PAIR, pair, 4 * L::tile64);
             bulk_store(rec + Rec::AQ, aqk, 8192);
@@ -702,10 +750,10 @@ __global__ void __launch_bounds__(NT, 1)
         }
         cur = nx;
         beta_cur = beta_nx;
-        t = t_next;
+        g = g_next;
     }
 
-    if (tid == 0) {
+    if (leader) {
         if (failed && tma_pending) mbar_wait(bar_tma, tma_par, p.err, 3);
         bulk_wait_all();
     }
@@ -738,16 +786,20 @@ template <int D, bool GATED>
 cudaError_t launch_t(const TcLaunch &x, cudaStream_t s) {
     IntraParams p{static_cast<const __nv_bfloat16 *>(x.a->beta_logits), x.table, x.records,
                   x.err, x.slots * x.a->H, x.a->H, x.a->ntok, x.a->flags};
-    // At least 120 KB so that one CTA (and its TMEM) owns an SM.
-    constexpr size_t need = Layout<D, GATED>::TOTAL + 1024;
-    const size_t smem = need > 120 * 1024 ? need : 120 * 1024;
+    using L = Layout<D, GATED>;
+    // Shared memory caps the CTAs per SM at CTAS_PER_SM, which keeps their
+    // TMEM allocations within the SM's 512 columns.
+    constexpr size_t need = L::TOTAL + 1024;
+    constexpr size_t floor_ = L::CTAS_PER_SM == 1 ? 120 * 1024 : 77 * 1024;
+    const size_t smem = need > floor_ ? need : floor_;
     auto kern = delta_intra_kernel<D, GATED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int64_t tasks = p.n_tasks;
-    const unsigned grid = (unsigned)(tasks < x.sms ? tasks : x.sms);
+    const int64_t groups = (p.n_tasks + L::P - 1) / L::P;
+    const int64_t slots = (int64_t)x.sms * L::CTAS_PER_SM;
+    const unsigned grid = (unsigned)(groups < slots ? groups : slots);
     if (grid == 0) return cudaSuccess;
-    kern<<<grid, NT, smem, s>>>(x.mq, x.mk, x.mv, x.mg, p);
+    kern<<<grid, L::NT, smem, s>>>(x.mq, x.mk, x.mv, x.mg, p);
     return cudaGetLastError();
 }
 
