@@ -8,7 +8,7 @@ the library is not built, the first call raises.
 
 Functions (same names as the C ABI):
   la_prefill_linear, la_prefill_delta, la_prefill_delta_workspace_size,
-  la_decode_step, la_check_device, la_status_string.
+  la_prefill_delta_static, la_decode_step, la_check_device, la_status_string.
 """
 from __future__ import annotations
 
@@ -18,11 +18,14 @@ import os
 from ._build import LIB_PATH, build  # noqa: F401  (build needs no GPU)
 
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT = 0, 1, 2, 3, 4
+LA_ERR_TOO_LARGE = 5
+LA_STATIC_SCRATCH_BYTES = 256 << 20
 LA_F32, LA_BF16 = 0, 1
 LA_L2NORM_K, LA_L2NORM_Q, LA_SILU_QK = 1, 2, 4
 
 EXPORTED = ("la_prefill_linear", "la_prefill_delta", "la_prefill_delta_workspace_size",
-            "la_decode_step", "la_check_device", "la_status_string")
+            "la_prefill_delta_static", "la_decode_step", "la_check_device",
+            "la_status_string")
 
 
 class LinAttnError(RuntimeError):
@@ -48,13 +51,16 @@ def library():
                                           vp, vp, vp, vp, vp]
         lib.la_prefill_delta.argtypes = [vp, vp, vp, vp, vp, vp, ip, vp, vp, ip, ip, ip, ip, ip,
                                          ip, fp, u, vp, vp, vp, sz, vp]
+        lib.la_prefill_delta_static.argtypes = [vp, vp, vp, vp, vp, vp, ip, vp, vp, ip, ip, ip,
+                                                ip, ip, ip, fp, u, vp, vp, vp]
         lib.la_prefill_delta_workspace_size.argtypes = [ip, ip, ip, ip, ip, ip, ip]
         lib.la_prefill_delta_workspace_size.restype = sz
         lib.la_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, ip, ip, ip, ip, ip, fp, u, vp, vp]
         lib.la_check_device.argtypes = [vp]
         lib.la_status_string.argtypes = [ip]
         lib.la_status_string.restype = ctypes.c_char_p
-        for f in ("la_prefill_linear", "la_prefill_delta", "la_decode_step", "la_check_device"):
+        for f in ("la_prefill_linear", "la_prefill_delta", "la_prefill_delta_static",
+                  "la_decode_step", "la_check_device"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -160,6 +166,30 @@ def la_prefill_delta(q, k, v, beta_logits, gate_logits, o, cu_seqlens, chunk=64,
                                     _stream(stream))
     if rc != LA_OK:
         raise LinAttnError(rc, "la_prefill_delta")
+    return o
+
+
+def la_prefill_delta_static(q, k, v, beta_logits, gate_logits, o, cu_seqlens, chunk=64,
+                            scale=1.0, flags=LA_L2NORM_K, init_S=None, final_S=None,
+                            cu_seqlens_host=None, stream=None):
+    """la_prefill_delta on the library's static scratch: allocates nothing.
+    Calls on one device must not overlap in time (they share the scratch)."""
+    import torch
+    _check(dict(q=q, k=k, v=v, o=o, beta_logits=beta_logits, gate_logits=gate_logits),
+           dtype=q.dtype, device=q.device)
+    _check(dict(cu_seqlens=cu_seqlens), dtype=torch.int32, device=q.device)
+    _check(dict(init_S=init_S, final_S=final_S), dtype=torch.float32, device=q.device)
+    ntok, H, dk = q.shape
+    dv = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    hold, hptr = _host_cu(cu_seqlens_host)
+    rc = library().la_prefill_delta_static(_ptr(q), _ptr(k), _ptr(v), _ptr(beta_logits),
+                                           _ptr(gate_logits), _ptr(o), _io(q), _ptr(cu_seqlens),
+                                           hptr, N, ntok, H, dk, dv, int(chunk), float(scale),
+                                           int(flags), _ptr(init_S), _ptr(final_S),
+                                           _stream(stream))
+    if rc != LA_OK:
+        raise LinAttnError(rc, "la_prefill_delta_static")
     return o
 
 

@@ -24,6 +24,21 @@ la_status check_cu_host(const int32_t *cu_host, int N, int ntok) {
 
 la_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
 
+// Host checks shared by the delta-rule prefill entry points (workspace aside).
+la_status check_delta_args(const void *q, const void *k, const void *v, const void *beta_logits,
+                           const void *o, la_dtype io, const int32_t *cu_seqlens,
+                           const int32_t *cu_seqlens_host, int N, int ntok, int H, int dk,
+                           int dv, int chunk, float scale, unsigned flags) {
+    if (!q || !k || !v || !beta_logits || !o || !cu_seqlens || N < 1 || ntok < 0 || H < 1 ||
+        !dtype_ok(io))
+        return LA_ERR_INVALID_ARG;
+    if (dk < 1 || dv < 1 || chunk < 1 || !std::isfinite(scale)) return LA_ERR_INVALID_ARG;
+    if (flags & ~(LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK)) return LA_ERR_INVALID_ARG;
+    if (!head_size_ok(dk) || !head_size_ok(dv) || chunk != 64) return LA_ERR_UNSUPPORTED;
+    if (N > 65535 || H > 65535) return LA_ERR_UNSUPPORTED;
+    return check_cu_host(cu_seqlens_host, N, ntok);
+}
+
 }  // namespace
 
 extern "C" {
@@ -35,6 +50,8 @@ const char *la_status_string(la_status s) {
         case LA_ERR_UNSUPPORTED: return "LA_ERR_UNSUPPORTED: no kernel for this configuration";
         case LA_ERR_CUDA: return "LA_ERR_CUDA: CUDA runtime or launch error";
         case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT: a bounded in-kernel wait expired";
+        case LA_ERR_TOO_LARGE:
+            return "LA_ERR_TOO_LARGE: scratch needed exceeds the library's static buffer";
     }
     return "LA_ERR_UNKNOWN";
 }
@@ -65,24 +82,38 @@ la_status la_prefill_delta(const void *q, const void *k, const void *v, const vo
                            int ntok, int H, int dk, int dv, int chunk, float scale,
                            unsigned flags, const float *init_S, float *final_S, void *workspace,
                            size_t workspace_bytes, void *stream) {
-    if (!q || !k || !v || !beta_logits || !o || !cu_seqlens || N < 1 || ntok < 0 || H < 1 ||
-        !dtype_ok(io))
-        return LA_ERR_INVALID_ARG;
-    if (dk < 1 || dv < 1 || chunk < 1 || !std::isfinite(scale)) return LA_ERR_INVALID_ARG;
-    if (flags & ~(LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK)) return LA_ERR_INVALID_ARG;
-    if (!head_size_ok(dk) || !head_size_ok(dv) || chunk != 64) return LA_ERR_UNSUPPORTED;
-    if (N > 65535 || H > 65535) return LA_ERR_UNSUPPORTED;
+    if (la_status st = check_delta_args(q, k, v, beta_logits, o, io, cu_seqlens, cu_seqlens_host,
+                                        N, ntok, H, dk, dv, chunk, scale, flags))
+        return st;
     const size_t ws_need = la_prefill_delta_workspace_size(N, ntok, H, dk, dv, chunk, io);
     if (ws_need > 0 && (!workspace || workspace_bytes < ws_need ||
                         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
         return LA_ERR_INVALID_ARG;
-    if (la_status st = check_cu_host(cu_seqlens_host, N, ntok)) return st;
     la::PrefillArgs a{q, k, v, beta_logits, gate_logits, o, cu_seqlens, N, ntok, H, dk, dv, scale,
                       flags, init_S, nullptr, final_S, nullptr, io == LA_BF16, workspace,
                       workspace_bytes};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (la::delta_tc_supported(a)) return from_cuda(la::launch_delta_tc(a, s));
     return from_cuda(la::launch_delta_simt(a, s));
+}
+
+la_status la_prefill_delta_static(const void *q, const void *k, const void *v,
+                                  const void *beta_logits, const void *gate_logits, void *o,
+                                  la_dtype io, const int32_t *cu_seqlens,
+                                  const int32_t *cu_seqlens_host, int N, int ntok, int H, int dk,
+                                  int dv, int chunk, float scale, unsigned flags,
+                                  const float *init_S, float *final_S, void *stream) {
+    static_assert(la::kStaticScratchBytes == LA_STATIC_SCRATCH_BYTES, "static scratch size");
+    if (la_status st = check_delta_args(q, k, v, beta_logits, o, io, cu_seqlens, cu_seqlens_host,
+                                        N, ntok, H, dk, dv, chunk, scale, flags))
+        return st;
+    const size_t need = la_prefill_delta_workspace_size(N, ntok, H, dk, dv, chunk, io);
+    if (need > la::kStaticScratchBytes) return LA_ERR_TOO_LARGE;
+    void *ws = nullptr;
+    if (need > 0 && !(ws = la::static_scratch())) return LA_ERR_CUDA;
+    return la_prefill_delta(q, k, v, beta_logits, gate_logits, o, io, cu_seqlens, cu_seqlens_host,
+                            N, ntok, H, dk, dv, chunk, scale, flags, init_S, final_S, ws,
+                            ws ? la::kStaticScratchBytes : 0, stream);
 }
 
 la_status la_decode_step(const void *q, const void *k, const void *v, const void *beta_logits,

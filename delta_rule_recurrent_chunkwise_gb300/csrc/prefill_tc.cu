@@ -16,6 +16,9 @@ namespace la {
 
 __device__ unsigned g_tc_error;  // first error code raised in a kernel
 
+// Library-owned scratch for the allocation-free prefill entry point.
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
 namespace {
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -103,6 +106,18 @@ cudaError_t launch_delta_tc(const PrefillArgs &a, cudaStream_t s) {
     if (e == cudaSuccess) e = launch_delta_intra(x, s);
     if (e == cudaSuccess) e = launch_delta_inter(x, s);
     return e;
+}
+
+void *static_scratch() {
+    static void *ptr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!ptr[dev]) {
+        void *a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_static_scratch) != cudaSuccess) return nullptr;
+        ptr[dev] = a;
+    }
+    return ptr[dev];
 }
 
 unsigned *device_error_word() {

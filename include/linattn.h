@@ -53,7 +53,8 @@ typedef enum la_status {
     LA_ERR_INVALID_ARG = 1, /* null pointer, bad size, non-monotone cu_seqlens_host, bad flag */
     LA_ERR_UNSUPPORTED = 2, /* valid request this build has no kernel for (e.g. dk = 96)     */
     LA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed                            */
-    LA_ERR_TIMEOUT = 4      /* a bounded in-kernel wait expired (reported by la_check_device)  */
+    LA_ERR_TIMEOUT = 4,     /* a bounded in-kernel wait expired (reported by la_check_device)  */
+    LA_ERR_TOO_LARGE = 5    /* la_prefill_delta_static: scratch need above its static buffer   */
 } la_status;
 
 typedef enum la_dtype { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
@@ -118,6 +119,29 @@ la_status la_prefill_delta(const void *q, const void *k, const void *v, const vo
  * (d = 128), with at most ntok/64 + N + 1 slots.  0 otherwise. */
 size_t la_prefill_delta_workspace_size(int N, int ntok, int H, int dk, int dv, int chunk,
                                        la_dtype io);
+
+/* la_prefill_delta without a caller workspace, allocating nothing: the
+ * per-chunk scratch comes from one library-owned static device buffer of
+ * LA_STATIC_SCRATCH_BYTES (256 MiB) per device.  The page has no counterpart:
+ * it is a deployment convenience (CUDA-graph capture, or callers without an
+ * allocator), not part of the method.
+ * Arguments, results and errors are those of la_prefill_delta, plus
+ * LA_ERR_TOO_LARGE (nothing launched) when la_prefill_delta_workspace_size
+ * for these sizes exceeds LA_STATIC_SCRATCH_BYTES (e.g. the d = 64 layout
+ * fits about 6000 chunk-heads: ntok/64 + N + 1 slots times H).
+ * The buffer's address is looked up (cudaGetSymbolAddress) on the first call
+ * on each device; make that first call outside CUDA stream capture.  The
+ * buffer needs no initialisation (every call rewrites what it reads).  All
+ * calls on a device share it, so calls whose executions may overlap in time
+ * (different streams, or host threads without ordering) race on it and give
+ * undefined results: serialise them. */
+#define LA_STATIC_SCRATCH_BYTES (256u << 20)
+la_status la_prefill_delta_static(const void *q, const void *k, const void *v,
+                                  const void *beta_logits, const void *gate_logits, void *o,
+                                  la_dtype io, const int32_t *cu_seqlens,
+                                  const int32_t *cu_seqlens_host, int N, int ntok, int H, int dk,
+                                  int dv, int chunk, float scale, unsigned flags,
+                                  const float *init_S, float *final_S, void *stream);
 
 /* One recurrent decode step: one new token for each of N sequences, state
  * updated IN PLACE (sections DeltaNet (Fast Weight Programmers) and Gated

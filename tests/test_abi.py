@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_status_strings(lib):
     assert la.la_status_string(la.LA_OK) == "LA_OK"
-    for s in (1, 2, 3, 4):
+    for s in (1, 2, 3, 4, 5):
         assert la.la_status_string(s).startswith("LA_ERR_")
     assert la.la_status_string(99) == "LA_ERR_UNKNOWN"
 
@@ -52,7 +52,7 @@ FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: every call below is reject
 def prefill_delta(lib, **kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, bl=FAKE, gl=None, o=FAKE, io=la.LA_BF16, cu=FAKE,
              cuh=None, N=2, ntok=40, H=4, dk=64, dv=64, chunk=64, scale=1.0,
-             flags=la.LA_L2NORM_K, iS=None, fS=None, ws=None, wsb=0, stream=None)
+             flags=la.LA_L2NORM_K, iS=None, fS=None, ws=FAKE, wsb=1 << 40, stream=None)
     a.update(kw)
     return lib.la_prefill_delta(a["q"], a["k"], a["v"], a["bl"], a["gl"], a["o"], a["io"],
                                 a["cu"], a["cuh"], a["N"], a["ntok"], a["H"], a["dk"], a["dv"],
@@ -131,3 +131,20 @@ def test_prefill_rejects_missing_workspace(lib):
     assert d(*args, None, 0, None) == la.LA_ERR_INVALID_ARG
     assert d(*args, FAKE, need - 1, None) == la.LA_ERR_INVALID_ARG
     assert d(*args, ctypes.c_void_p(0x1010), need, None) == la.LA_ERR_INVALID_ARG
+
+
+def test_static_entry_point_refuses_requests_beyond_its_scratch(lib):
+    """la_prefill_delta_static answers LA_ERR_TOO_LARGE, on the host and
+    before any launch, when the sizes need more scratch than its static
+    buffer; a request that fits is not refused for size."""
+    d = lib.la_prefill_delta_static
+    ws = la.la_prefill_delta_workspace_size
+    big = (4, 8192 * 4, 32, 128, 128)
+    assert ws(*big, 64, la.LA_BF16) > la.LA_STATIC_SCRATCH_BYTES
+    assert d(FAKE, FAKE, FAKE, FAKE, None, FAKE, la.LA_BF16, FAKE, None, *big, 64, 1.0, 1,
+             None, None, None) == la.LA_ERR_TOO_LARGE
+    small = (2, 256, 4, 64, 64)
+    assert ws(*small, 64, la.LA_BF16) <= la.LA_STATIC_SCRATCH_BYTES
+    bad = (ctypes.c_int32 * 3)(0, 10, 5)   # rejected later, for its cu_seqlens_host
+    assert d(FAKE, FAKE, FAKE, FAKE, None, FAKE, la.LA_BF16, FAKE, bad, *small, 64, 1.0, 1,
+             None, None, None) == la.LA_ERR_INVALID_ARG
