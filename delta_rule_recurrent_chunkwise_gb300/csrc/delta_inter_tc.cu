@@ -4,29 +4,31 @@
 // ("From GPT-2 to Kimi K3, explained", section DeltaNet (Parallelizing
 // Linear Transformers with Delta Rule), eq. 8-10, with the cumulative decay of
 // sections Gated DeltaNet and KDA / Kimi Linear.)  Per chunk, reading the
-// record the intra-chunk kernel wrote (W, U, Aq, Q e^b, K~ = K e^{b_end - b},
+// record the intra-chunk kernel wrote (-W, U, Aq, Q e^b, K~ = K e^{b_end - b},
 // e^{b_end}):
 //   u = U - W S                     (S = state at the end of the previous chunk)
 //   O = scale ((Q e^b) S + Aq u)
 //   S <- Diag(e^{b_end}) S + K~^T u
 //
-// Only S -> u -> S is sequential; everything else is arranged around that
-// chain.  Three warp roles, synchronised by mbarriers only:
-//   issuer (one thread)  tensor-core products and record loads:
-//       u  = I_64 U            issued one chunk early (U enters TMEM through an
-//                              identity product, so u accumulates in place)
-//       u -= W S               -> commit "u"
-//       O  = (Q e^b) S
-//       S += K~^T u            -> commit "s"          (after "u tile ready")
-//       O += Aq u              -> commit "o"
-//   converters   u (TMEM fp32) -> bf16 operand tile          -> "u tile ready"
-//                S (TMEM fp32) -> bf16 operand tile          -> "S tile ready"
-//                gated: S *= e^{b_end} of the next chunk, in TMEM (off the
-//                chain: the next S += K~^T u waits for "u tile ready")
-//   output warps O (TMEM fp32, two buffers) -> scale -> bf16 -> global
-// The chain per chunk is then: W S product, u readback, K~^T u product,
-// S readback.  The fp32 state lives in tensor memory for the whole sequence;
-// the next chunk's record streams in by one bulk copy while this one runs.
+// Three tensor-core products per chunk, all M = 128 where the rows allow,
+// into one TMEM accumulator per chunk (two, alternating) whose lanes 0..63
+// hold u and lanes 64..127 hold O:
+//   [-W ; Q e^b] S         on top of [U ; 0]  ->  [u ; (Q e^b) S]   commit "u"
+//   S += K~^T u                                                     commit "s"
+//   [anything ; Aq] u      ->  lanes 64..127 += Aq u (lanes 0..63, already
+//                              read out, take a harmless sum)       commit "o"
+// Only S -> u -> S is sequential.  Warp roles, synchronised by mbarriers:
+//   warps 0..7     state: S (TMEM fp32) -> bf16 operand tile for the next
+//                  chunk, then (gated) S *= e^{b_end} of the next chunk in
+//                  TMEM; the four on lanes 0..63 first turn u into its bf16
+//                  operand tile
+//   warps 8, 9     put U of the chunk into accumulator lanes 0..63
+//   warps 10, 11   O (lanes 64..127) -> scale -> bf16 -> global, then zero
+//                  those lanes for the chunk after next
+//   warp 12        one thread issues the products
+// (13 warps: a 16th would cost the register budget of 20.)
+// The fp32 state lives in tensor memory for the whole sequence; records
+// stream in by bulk copies up to NB - 1 chunks ahead.
 
 #include "common.cuh"
 #include "delta_tc.h"
@@ -38,36 +40,33 @@ namespace {
 using namespace tc;
 using namespace tile;
 
-template <int D>
-struct Roles {
-    static constexpr int CW = D == 64 ? 4 : 8;   // converter warps (2 per lane quarter at D = 128)
-    static constexpr int OW = 4;                 // output warps (one per lane quarter)
-    static constexpr int ISSUER = CW + OW;       // warp of the issuing thread
-    static constexpr int NT = 32 * (CW + OW + 1);
-    static constexpr int CPT = D / (CW / 4);     // state / u columns per converter thread
-};
+constexpr int NT = 13 * 32;
+constexpr int W_ISSUER = 12;
 
 template <int D>
 struct Layout {
     using Rec = Record<D>;
-    // record buffers: loads run NB - 1 chunks ahead of the recurrence
+    // record buffers: loads run up to NB - 1 chunks ahead of the recurrence
     static constexpr int NB = D == 64 ? 4 : 2;
     static constexpr uint32_t REC0 = 0;
     static constexpr uint32_t SB = NB * Rec::BYTES;      // S, bf16 [D][D] RS tile
     static constexpr uint32_t UT = SB + D * D * 2;        // u, bf16 [64][D] RS tile
-    static constexpr uint32_t IDENT = UT + C * D * 2;     // I_64, bf16 RS tile
-    static constexpr uint32_t BARS = IDENT + 8192;        // mbarriers + tmem slot
+    static constexpr uint32_t BARS = UT + C * D * 2;      // mbarriers, tmem slot, load counts
     static constexpr uint32_t TOTAL = BARS + 128;
     static_assert(TOTAL + 1024 <= 227 * 1024, "shared memory budget");
 };
 
 // mbarrier slots (B_REC0 .. B_REC0 + NB - 1: record buffers)
-enum : int { B_U = 0, B_S, B_O, B_SREADY, B_UREADY, B_OFREE0, B_OFREE1, B_REC0, B_COUNT = B_REC0 + 4 };
+enum : int {
+    B_U = 0, B_S, B_O, B_SREADY, B_UREADY, B_UPRE, B_OFREE0, B_OFREE1, B_REC0,
+    B_COUNT = B_REC0 + 4
+};
+constexpr uint32_t N_STATE = 8, N_UPRE = 2, N_OUT = 2;  // arrivals per phase
 
-// TMEM columns: S (M = D rows = key channels), u, two O buffers.
+// TMEM columns: S (M = D rows = key channels), then two [u ; O] accumulators.
 template <int D>
 struct Cols {
-    static constexpr uint32_t S = 0, U = D, O = 2 * D, TOTAL = 4 * D;
+    static constexpr uint32_t S = 0, ACC = D, TOTAL = D == 64 ? 256 : 512;
 };
 
 struct InterParams {
@@ -82,20 +81,23 @@ struct InterParams {
 };
 
 template <int D, bool GATED>
-__global__ void __launch_bounds__(Roles<D>::NT, 1) delta_inter_kernel(InterParams p) {
+__global__ void __launch_bounds__(NT, 1) delta_inter_kernel(InterParams p) {
     using L = Layout<D>;
     using Rec = Record<D>;
     using TC = Cols<D>;
-    using RL = Roles<D>;
-    constexpr int CPT = RL::CPT;
+    constexpr int NB = L::NB;
+    constexpr int HALF = D / 2;  // columns per thread in every readback (two column halves)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t *sb = sm + L::SB, *ut = sm + L::UT, *ident = sm + L::IDENT;
+    uint8_t *sb = sm + L::SB, *ut = sm + L::UT;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::BARS);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + B_COUNT);
+    int *s_loads = reinterpret_cast<int *>(tslot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qd = warp & 3;                  // TMEM lane quarter
+    const int c0 = ((warp >> 2) & 1) * HALF;  // state warps: this warp's column half
     const int h = blockIdx.x, n = blockIdx.y, H = p.H;
     int t_begin = p.cu_seqlens[n], t_end = p.cu_seqlens[n + 1];
     if (t_begin < 0 || t_end < t_begin || t_end > p.ntok) {
@@ -105,16 +107,13 @@ __global__ void __launch_bounds__(Roles<D>::NT, 1) delta_inter_kernel(InterParam
     const int nc = (t_end - t_begin + C - 1) / C;
     const int64_t slot0 = (int64_t)(t_begin / C) + n;
     auto rec_src = [&](int c) { return p.records + ((slot0 + c) * H + h) * (int64_t)Rec::BYTES; };
-    constexpr int NB = L::NB;
     auto buf = [&](int c) { return sm + L::REC0 + (uint32_t)(c % NB) * Rec::BYTES; };
     auto rec_bar = [&](int c) { return &bars[B_REC0 + c % NB]; };
     auto rec_par = [](int c) { return (uint32_t)(c / NB) & 1u; };
-    // Record loads (one bulk copy each).  The issuer starts records 0 .. NB-1;
-    // output warp 0 loads record c + NB into chunk c's buffer once every
-    // product reading it is done.  So the records loaded are always 0 .. K-1;
-    // both threads count theirs (s_loads) so the CTA can wait the last ones
-    // out before it exits.
-    int *s_loads = reinterpret_cast<int *>(tslot + 1);
+    // Record loads (one bulk copy each): the issuer starts records 0 .. NB-1,
+    // output warp 10 loads record c + NB into chunk c's buffer once chunk c
+    // is finished with it, so the records loaded are always 0 .. K-1; both
+    // count theirs (s_loads) for the final wait.
     auto issue_rec = [&](int c) {
         fence_proxy_async();
         mbar_arrive_expect_tx(rec_bar(c), Rec::BYTES);
@@ -126,10 +125,11 @@ __global__ void __launch_bounds__(Roles<D>::NT, 1) delta_inter_kernel(InterParam
         mbar_init(&bars[B_U], 1);
         mbar_init(&bars[B_S], 1);
         mbar_init(&bars[B_O], 1);
-        mbar_init(&bars[B_SREADY], RL::CW);
-        mbar_init(&bars[B_UREADY], RL::CW);
-        mbar_init(&bars[B_OFREE0], RL::OW);
-        mbar_init(&bars[B_OFREE1], RL::OW);
+        mbar_init(&bars[B_SREADY], N_STATE);
+        mbar_init(&bars[B_UREADY], N_STATE);
+        mbar_init(&bars[B_UPRE], N_UPRE);
+        mbar_init(&bars[B_OFREE0], N_OUT);
+        mbar_init(&bars[B_OFREE1], N_OUT);
         fence_mbar_init();
         s_loads[0] = s_loads[1] = 0;
     }
@@ -137,96 +137,71 @@ __global__ void __launch_bounds__(Roles<D>::NT, 1) delta_inter_kernel(InterParam
         tmem_alloc(tslot, TC::TOTAL);
         tmem_relinquish();
     }
-    // the identity operand: 64 rows x 8 sixteen-byte units
-    for (int u = tid; u < C * 8; u += RL::NT) {
-        const int r = u >> 3, c8 = (u & 7) * 8;
-        float v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = (c8 + i == r) ? 1.0f : 0.0f;
-        st_bf16x8(ident, C, r, c8, v);
-    }
-    fence_proxy_async();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t tq = tmem + ((uint32_t)(32 * (warp & 3)) << 16);  // this warp's lane quarter
+    const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);  // this warp's lane quarter
+    auto acc = [&](int c) { return (uint32_t)(TC::ACC + (c & 1) * D); };
     const int64_t sbase = ((int64_t)n * H + h) * D * D;
+    // one lane of each warp arrives once the warp's work is ordered before it
+    auto warp_arrive = [&](uint64_t *bar) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar);
+    };
 
-    if (warp == RL::ISSUER) {
+    if (warp == W_ISSUER) {
         // ================================================= issuer
         if (lane == 0 && nc > 0) {
-            constexpr uint32_t idp = idesc_bf16(64, D, false, true);
-            constexpr uint32_t idn = idesc_bf16(64, D, false, true, true);
+            constexpr uint32_t id128 = idesc_bf16(128, D, false, true);
             constexpr uint32_t ids = idesc_bf16(D, D, true, true);
-            const uint64_t aI = kdesc(ident, C, 0, 0), bS = mdesc(sb, D, 0, 0), bU = mdesc(ut, C, 0, 0);
-            auto issue_iu = [&](int c) {  // u = I_64 U
-                const uint64_t b = mdesc(buf(c) + Rec::U, C, 0, 0);
-#pragma unroll
-                for (int s4 = 0; s4 < 4; ++s4)
-                    mma_bf16(tmem + TC::U, dstep(aI, s4 * 2), dstep(b, s4 * 128), idp, s4 > 0);
-            };
+            const uint64_t bS = mdesc(sb, D, 0, 0), bU = mdesc(ut, C, 0, 0);
             for (int c = 0; c < NB && c < nc; ++c) issue_rec(c);
             s_loads[0] = NB < nc ? NB : nc;
-            bool ok = true, iu_ready = false;  // iu_ready: u = I U of chunk c issued
-            for (int c = 0; c < nc && ok; ++c) {
+            for (int c = 0; c < nc; ++c) {
                 uint8_t *rb = buf(c);
-                const uint32_t tO = tmem + TC::O + (uint32_t)(c & 1) * D;
-                if (!iu_ready) {
-                    if (!(ok = mbar_wait(rec_bar(c), rec_par(c), p.err, 4))) break;
-                    issue_iu(c);
-                }
-                // S tile of this chunk ready (converters)
-                if (!(ok = mbar_wait(&bars[B_SREADY], (uint32_t)c & 1u, p.err, 5))) break;
+                const uint32_t ta = tmem + acc(c);
+                // the state tile, U in lanes 0..63 (and zeros below it), the record
+                if (!mbar_wait(&bars[B_SREADY], (uint32_t)c & 1u, p.err, 5)) break;
+                if (!mbar_wait(&bars[B_UPRE], (uint32_t)c & 1u, p.err, 6)) break;
+                if (!mbar_wait(rec_bar(c), rec_par(c), p.err, 4)) break;
                 tc_fence_after();
-                const uint64_t aW = kdesc(rb + Rec::W, C, 0, 0), aQ = kdesc(rb + Rec::PAIR, 128, 0, 0);
+                const uint64_t aWQ = kdesc(rb + Rec::WQ, 128, 0, 0);
 #pragma unroll 1
                 for (int kb = 0; kb < D / 64; ++kb) {
 #pragma unroll
                     for (int s4 = 0; s4 < 4; ++s4) {
                         const int s = 4 * kb + s4;
-                        mma_bf16(tmem + TC::U, dstep(aW, kstep_units(C, s)), dstep(bS, s * 128), idn, 1);
+                        mma_bf16(ta, dstep(aWQ, kstep_units(128, s)), dstep(bS, s * 128), id128, 1);
                     }
                 }
                 mma_commit(&bars[B_U]);
-                // O buffer c & 1 was drained (chunk c - 2) before the previous
-                // chunk's "o" commit
-#pragma unroll 1
-                for (int kb = 0; kb < D / 64; ++kb) {
-#pragma unroll
-                    for (int s4 = 0; s4 < 4; ++s4) {
-                        const int s = 4 * kb + s4;
-                        mma_bf16(tO, dstep(aQ, kstep_units(128, s)), dstep(bS, s * 128), idp, s > 0);
-                    }
-                }
-                // u tile ready (converters), state decayed for this chunk
-                if (!(ok = mbar_wait(&bars[B_UREADY], (uint32_t)c & 1u, p.err, 7))) break;
+                // u tile ready, state decayed for this chunk
+                if (!mbar_wait(&bars[B_UREADY], (uint32_t)c & 1u, p.err, 7)) break;
                 tc_fence_after();
-                const uint64_t aK = mdesc(rb + Rec::PAIR, 128, 64, 0), aA = kdesc(rb + Rec::AQ, 64, 0, 0);
+                const uint64_t aK = mdesc(rb + Rec::UK, 128, 64, 0);
+                const uint64_t aA = kdesc(rb + Rec::AQ - 8192, 128, 0, 0);
 #pragma unroll
                 for (int s4 = 0; s4 < 4; ++s4)
                     mma_bf16(tmem + TC::S, dstep(aK, s4 * 128), dstep(bU, s4 * 128), ids, 1);
                 mma_commit(&bars[B_S]);
-                // the next chunk's u = I U, if its record is already here (the
-                // converters have read this chunk's u out of TMEM)
-                iu_ready = c + 1 < nc && mbar_test_wait(rec_bar(c + 1), rec_par(c + 1));
-                if (iu_ready) issue_iu(c + 1);
 #pragma unroll
                 for (int s4 = 0; s4 < 4; ++s4)
-                    mma_bf16(tO, dstep(aA, s4 * 2), dstep(bU, s4 * 128), idp, 1);
-                // The output warps must have taken chunk c - 1 (and so seen its
-                // "o" phase) before this chunk's "o" phase completes; that also
-                // frees O buffer (c + 1) & 1 for the next chunk.
-                if (c >= 1 && !(ok = mbar_wait(&bars[B_OFREE0 + ((c - 1) & 1)], (uint32_t)((c - 1) >> 1) & 1u, p.err, 6)))
+                    mma_bf16(ta, dstep(aA, s4 * 2), dstep(bU, s4 * 128), id128, 1);
+                // The output warps must have taken chunk c - 1 (so seen its "o"
+                // phase) before this chunk's "o" phase can complete.
+                if (c >= 1 &&
+                    !mbar_wait(&bars[B_OFREE0 + ((c - 1) & 1)], (uint32_t)(((c - 1) >> 1) + 1) & 1u, p.err, 8))
                     break;
                 mma_commit(&bars[B_O]);
             }
         }
-    } else if (warp < RL::CW) {
-        // ================================================= converters
-        const int srow = acc_row(D, warp & 3, lane);   // state row (key channel)
-        const int urow = acc_row(64, warp & 3, lane);  // u row (token)
-        const int c0 = (warp >> 2) * CPT;              // first column of this thread
+    } else if (warp < 8) {
+        // ================================================= state (and u) warps
+        const int srow = acc_row(D, qd, lane);     // state row (key channel), or -1
+        const bool u_warp = qd < 2;
+        const int urow = 32 * qd + lane;           // u row (token) for u_warp
         bool ok = true;
         // initial state: bf16 operand copy; TMEM state decayed by chunk 0's e^{b_end}
         if (GATED && nc > 0) ok = mbar_wait(rec_bar(0), 0, p.err, 10);
@@ -235,7 +210,7 @@ __global__ void __launch_bounds__(Roles<D>::NT, 1) delta_inter_kernel(InterParam
                                  ? reinterpret_cast<const float *>(buf(0) + Rec::GEND)[srow]
                                  : 1.0f;
 #pragma unroll
-            for (int cb = 0; cb < CPT; cb += 16) {
+            for (int cb = 0; cb < HALF; cb += 16) {
                 const int col = c0 + cb;
                 float v[16];
                 if (srow >= 0 && p.init_S) {
@@ -258,33 +233,29 @@ __global__ void __launch_bounds__(Roles<D>::NT, 1) delta_inter_kernel(InterParam
                 tmem_st16(tq + TC::S + col, v);
             }
             fence_proxy_async();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_SREADY]);
+            warp_arrive(&bars[B_SREADY]);
         }
         for (int c = 0; c < nc && ok; ++c) {
-            // ---- u -> bf16 operand tile
-            if (!(ok = mbar_wait(&bars[B_U], (uint32_t)c & 1u, p.err, 11))) break;
-            tc_fence_after();
+            // ---- u -> bf16 operand tile (lanes 0..63 of the accumulator)
+            if (u_warp) {
+                if (!(ok = mbar_wait(&bars[B_U], (uint32_t)c & 1u, p.err, 11))) break;
+                tc_fence_after();
 #pragma unroll
-            for (int cb = 0; cb < CPT; cb += 32) {
-                float v[32];
-                tmem_ld32(tq + TC::U + c0 + cb, v);
-                if (urow >= 0) {
+                for (int cb = 0; cb < HALF; cb += 32) {
+                    float v[32];
+                    tmem_ld32(tq + acc(c) + c0 + cb, v);
 #pragma unroll
                     for (int i = 0; i < 32; i += 8) st_bf16x8(ut, C, urow, c0 + cb + i, v + i);
                 }
+                fence_proxy_async();
             }
-            fence_proxy_async();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_UREADY]);
+            warp_arrive(&bars[B_UREADY]);
             // ---- S after this chunk
             if (!(ok = mbar_wait(&bars[B_S], (uint32_t)c & 1u, p.err, 12))) break;
             tc_fence_after();
             if (c + 1 < nc) {
 #pragma unroll
-                for (int cb = 0; cb < CPT; cb += 32) {
+                for (int cb = 0; cb < HALF; cb += 32) {
                     float v[32];
                     tmem_ld32(tq + TC::S + c0 + cb, v);
                     if (srow >= 0) {
@@ -293,9 +264,7 @@ __global__ void __launch_bounds__(Roles<D>::NT, 1) delta_inter_kernel(InterParam
                     }
                 }
                 fence_proxy_async();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[B_SREADY]);
+                warp_arrive(&bars[B_SREADY]);
                 if (GATED) {
                     // decay for the next chunk (needs its record's e^{b_end});
                     // the state is read again rather than held in registers
@@ -304,7 +273,7 @@ __global__ void __launch_bounds__(Roles<D>::NT, 1) delta_inter_kernel(InterParam
                                          ? reinterpret_cast<const float *>(buf(c + 1) + Rec::GEND)[srow]
                                          : 1.0f;
 #pragma unroll
-                    for (int cb = 0; cb < CPT; cb += 32) {
+                    for (int cb = 0; cb < HALF; cb += 32) {
                         float v[32];
                         tmem_ld32(tq + TC::S + c0 + cb, v);
 #pragma unroll
@@ -312,14 +281,13 @@ __global__ void __launch_bounds__(Roles<D>::NT, 1) delta_inter_kernel(InterParam
                         tmem_st16(tq + TC::S + c0 + cb, *reinterpret_cast<float(*)[16]>(v));
                         tmem_st16(tq + TC::S + c0 + cb + 16, *reinterpret_cast<float(*)[16]>(v + 16));
                     }
-                    tc_fence_before();
                 }
             }
         }
         // ---- final state
         if (ok && p.final_S) {
 #pragma unroll
-            for (int cb = 0; cb < CPT; cb += 16) {
+            for (int cb = 0; cb < HALF; cb += 16) {
                 float v[16];
                 tmem_ld16(tq + TC::S + c0 + cb, v);
                 if (srow >= 0) {
@@ -329,41 +297,72 @@ __global__ void __launch_bounds__(Roles<D>::NT, 1) delta_inter_kernel(InterParam
                 }
             }
         }
+    } else if (qd < 2) {
+        // ================================================= U pre-load (warps 8, 9)
+        const int urow = 32 * qd + lane;
+        for (int c = 0; c < nc; ++c) {
+            // the issuer has taken the previous chunk's U (so phases cannot run
+            // ahead of it); this accumulator drained and zeroed (chunk c - 2)
+            if (c >= 1 && !mbar_wait(&bars[B_U], (uint32_t)(c - 1) & 1u, p.err, 15)) break;
+            if (!mbar_wait(&bars[B_OFREE0 + (c & 1)], (uint32_t)(c >> 1) & 1u, p.err, 16)) break;
+            if (!mbar_wait(rec_bar(c), rec_par(c), p.err, 17)) break;
+            tc_fence_after();
+            const uint8_t *uk = buf(c) + Rec::UK;
+#pragma unroll
+            for (int cb = 0; cb < D; cb += 16) {
+                float v[16];
+                unpack8(*reinterpret_cast<const uint4 *>(uk + rs_off(128, urow, cb)), v);
+                unpack8(*reinterpret_cast<const uint4 *>(uk + rs_off(128, urow, cb + 8)), v + 8);
+                tmem_st16(tq + acc(c) + cb, v);
+            }
+            warp_arrive(&bars[B_UPRE]);
+        }
     } else {
-        // ================================================= output warps
-        const int r = acc_row(64, warp & 3, lane);
+        // ================================================= output warps (10, 11)
+        const int orow = 32 * (qd - 2) + lane;  // row of O in the chunk
         int refills = 0;
+        // both accumulators' O lanes start at zero
+        {
+            float z[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) z[i] = 0.0f;
+#pragma unroll
+            for (int b = 0; b < 2; ++b)
+#pragma unroll
+                for (int cb = 0; cb < D; cb += 16) tmem_st16(tq + acc(b) + cb, z);
+            warp_arrive(&bars[B_OFREE0]);
+            warp_arrive(&bars[B_OFREE1]);
+        }
         for (int c = 0; c < nc; ++c) {
             if (!mbar_wait(&bars[B_O], (uint32_t)c & 1u, p.err, 14)) break;
             tc_fence_after();
             const int tok0 = t_begin + c * C;
-            const bool valid = r >= 0 && r < t_end - tok0;
-            const uint32_t tO = tq + TC::O + (uint32_t)(c & 1) * D;
+            const bool valid = orow < t_end - tok0;
 #pragma unroll
             for (int cb = 0; cb < D; cb += 32) {
                 float v[32];
-                tmem_ld32(tO + cb, v);
+                tmem_ld32(tq + acc(c) + cb, v);
                 if (valid) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] *= p.scale;
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + ((int64_t)(tok0 + r) * H + h) * D + cb);
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + ((int64_t)(tok0 + orow) * H + h) * D + cb);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) dst[i] = pack8(v + 8 * i);
                 }
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+                tmem_st16(tq + acc(c) + cb, *reinterpret_cast<float(*)[16]>(v));
+                tmem_st16(tq + acc(c) + cb + 16, *reinterpret_cast<float(*)[16]>(v + 16));
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&bars[B_OFREE0 + (c & 1)]);
-                // every product that reads record c has completed ("o" is the
-                // last commit of chunk c): its buffer takes record c + NB
-                if (warp == RL::CW && c + NB < nc) {
-                    issue_rec(c + NB);
-                    ++refills;
-                }
+            warp_arrive(&bars[B_OFREE0 + (c & 1)]);
+            // every product that reads record c has completed ("o" is the last
+            // commit of chunk c): its buffer takes record c + NB
+            if (warp == 10 && lane == 0 && c + NB < nc) {
+                issue_rec(c + NB);
+                ++refills;
             }
         }
-        if (warp == RL::CW && lane == 0) s_loads[1] = refills;
+        if (warp == 10 && lane == 0) s_loads[1] = refills;
     }
     tc_fence_before();
     __syncthreads();
@@ -386,7 +385,7 @@ cudaError_t launch_t(const TcLaunch &x, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(a.H, a.N);
-    kern<<<grid, Roles<D>::NT, smem, s>>>(p);
+    kern<<<grid, NT, smem, s>>>(p);
     return cudaGetLastError();
 }
 

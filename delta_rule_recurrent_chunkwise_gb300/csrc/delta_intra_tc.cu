@@ -70,8 +70,8 @@ struct Layout {
     static constexpr uint32_t RAW_V = RAW_K + tile64;
     static constexpr uint32_t RAW_G = RAW_V + tile64;
     static constexpr uint32_t X = RAW_G + (GATED ? tile64 : 0);
-    // X, prologue (gated): the block-product operands [Q^; K^] (128 rows)
-    // and the packed K_R tile (160 rows)
+    // X, prologue: the block-product operand [Q^; K^] (128 rows) and, gated,
+    // the packed K_R tile (160 rows)
     static constexpr uint32_t QKH = X;
     static constexpr uint32_t KR = X + 128 * D * 2;
     // X during and after the solve
@@ -80,16 +80,17 @@ struct Layout {
     static constexpr uint32_t SA = X + 16384;           // A, fp32 [64][LDT]
     static constexpr uint32_t ST = SA + 64 * LDT * 4;   // T, fp32 [64][LDT]
     static constexpr uint32_t SX = T16;                 // solve temps, fp32 (8 KB; dead before T16)
-    static constexpr uint32_t X_END_A = GATED ? KR + 160 * D * 2 : X;
+    static constexpr uint32_t X_END_A = GATED ? KR + 160 * D * 2 : KR;
     static constexpr uint32_t X_END_C = ST + 64 * LDT * 4;
     static constexpr uint32_t X_END = X_END_A > X_END_C ? X_END_A : X_END_C;
-    // [Q e^b ; K e^{b_end - b}] (gated) or [q^ ; k^] (ungated), 128 rows, then
-    // beta K e^b (later W) and beta V (later U): the record's first four
-    // tiles, contiguous as in the record
-    static constexpr uint32_t PAIR = (X_END + 1023) & ~1023u;
-    static constexpr uint32_t BKG = PAIR + 2 * tile64;
-    static constexpr uint32_t BV = BKG + tile64;
-    static constexpr uint32_t SMALL = BV + tile64;
+    // The record's first four tiles, contiguous as in the record:
+    //   WQ = [beta K e^b, later -W (rows 0..63) ; Q e^b (rows 64..127)]
+    //   UK = [beta V, later U      (rows 0..63) ; K e^{b_end - b} (rows 64..127)]
+    // (ungated: e^b = 1).  Rows 0..63 of WQ and UK, 16 KB apart per
+    // 64-column block, are also the B operand [beta K e^b | beta V].
+    static constexpr uint32_t WQ = (X_END + 1023) & ~1023u;
+    static constexpr uint32_t UK = WQ + 2 * tile64;
+    static constexpr uint32_t SMALL = UK + 2 * tile64;
     static constexpr uint32_t BETA = SMALL;                    // fp32 [64]
     static constexpr uint32_t KN = BETA + 256;                 // fp32 [64]
     static constexpr uint32_t QN = KN + 256;                   // fp32 [64]
@@ -98,7 +99,7 @@ struct Layout {
     static constexpr uint32_t INFO = GEND + 4 * D;             // int4: next task
     static constexpr uint32_t BAR_TMA = INFO + 16;             // mbarrier: raw tiles
     static constexpr uint32_t TASK_BYTES = (BAR_TMA + 8 + 1023) & ~1023u;
-    static_assert(BKG - PAIR == Record<D>::W && BV - PAIR == Record<D>::U, "record image");
+    static_assert(UK - WQ == Record<D>::UK, "record image");
     // threads per CTA, CTAs per SM, TMEM columns (block products, then W | U)
     static constexpr bool SMALL_CTA = D == 64 && !GATED;
     static constexpr int NT = SMALL_CTA ? 256 : 512;
@@ -183,8 +184,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
     float *sA = reinterpret_cast<float *>(sm + L::SA);
     float *sT = reinterpret_cast<float *>(sm + L::ST);
     float *sX = reinterpret_cast<float *>(sm + L::SX);
-    uint8_t *pair = sm + L::PAIR, *bkg = sm + L::BKG, *bv = sm + L::BV;
-    uint8_t *wt = bkg, *ut = bv;  // W and U tiles reuse beta K e^b and beta V
+    uint8_t *wq = sm + L::WQ, *uk = sm + L::UK;
     float *sbeta = reinterpret_cast<float *>(sm + L::BETA);
     float *skn = reinterpret_cast<float *>(sm + L::KN);
     float *sqn = reinterpret_cast<float *>(sm + L::QN);
@@ -353,12 +353,12 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
         __syncthreads();
         // ---------------------------------------------- A1: operand tiles
         if (!GATED) {
-            // [q^; k^] into PAIR, beta k^ into BKG, beta v into BV: 16-byte units
+            // [q^; k^] into QKH; beta k^, q^ into WQ; beta v, k^ into UK: 16-byte units
             for (int u = ltid; u < C * D / 8; u += NTC) {
                 const uint32_t off = (uint32_t)u * 16u;                 // offset in a [64][D] tile
                 const uint32_t cb = off >> 13, in = off & 8191u;         // column block, offset in it
                 const int r = (int)(in >> 7);
-                const uint32_t po = cb * (128u * 128u) + in;            // same row in PAIR
+                const uint32_t po = cb * (128u * 128u) + in;            // same row, 128-row tile
                 float kv[8], qv[8], vv[8];
                 unpack8(*reinterpret_cast<const uint4 *>(rawk + off), kv);
                 unpack8(*reinterpret_cast<const uint4 *>(rawq + off), qv);
@@ -373,10 +373,13 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
                     bk[i] = be * kv[i];
                     vv[i] *= be;
                 }
-                *reinterpret_cast<uint4 *>(pair + po) = pack8(qv);
-                *reinterpret_cast<uint4 *>(pair + po + 64u * 128u) = pack8(kv);
-                *reinterpret_cast<uint4 *>(bkg + off) = pack8(bk);
-                *reinterpret_cast<uint4 *>(bv + off) = pack8(vv);
+                const uint4 qh = pack8(qv), kh = pack8(kv);
+                *reinterpret_cast<uint4 *>(qkh + po) = qh;
+                *reinterpret_cast<uint4 *>(qkh + po + 64u * 128u) = kh;
+                *reinterpret_cast<uint4 *>(wq + po) = pack8(bk);
+                *reinterpret_cast<uint4 *>(wq + po + 64u * 128u) = qh;
+                *reinterpret_cast<uint4 *>(uk + po) = pack8(vv);
+                *reinterpret_cast<uint4 *>(uk + po + 64u * 128u) = kh;
             }
             if (ltid < D) sgend[ltid] = 1.0f;
         } else {
@@ -467,8 +470,8 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
                 };
                 uint8_t *const pq_raw = rawq + cboff64, *const pk_raw = rawk + cboff64;
                 uint8_t *const p_qh = qkh + cboff128, *const p_kh = qkh + cboff128 + 64 * 128;
-                uint8_t *const p_qg = pair + cboff128, *const p_kt = pair + cboff128 + 64 * 128;
-                uint8_t *const p_bk = bkg + cboff64, *const p_kr = kr + cboff160;
+                uint8_t *const p_qg = wq + cboff128 + 64 * 128, *const p_kt = uk + cboff128 + 64 * 128;
+                uint8_t *const p_bk = wq + cboff128, *const p_kr = kr + cboff160;
                 // second-half lanes: swap register rows rho <-> rho ^ 4 so the
                 // store pass can index P[rho] with a compile-time rho
                 if (pr) {
@@ -519,7 +522,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
                 const float be = sbeta[r];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) vv[i] *= be;
-                *reinterpret_cast<uint4 *>(bv + off) = pack8(vv);
+                *reinterpret_cast<uint4 *>(uk + (off >> 13) * (128u * 128u) + (off & 8191u)) = pack8(vv);
             }
         }
         phase_sync();
@@ -543,8 +546,8 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
 #pragma unroll 1
             for (int kk = 0; kk < P; ++kk) {
                 uint8_t *tsm = task_sm(kk);
-                const uint64_t a0 = GATED ? kdesc(tsm + L::QKH, 128, 0, 0) : kdesc(tsm + L::PAIR, 128, 0, 0);
-                const uint64_t b0 = GATED ? kdesc(tsm + L::KR, 160, 0, 0) : kdesc(tsm + L::PAIR, 128, 64, 0);
+                const uint64_t a0 = kdesc(tsm + L::QKH, 128, 0, 0);
+                const uint64_t b0 = GATED ? kdesc(tsm + L::KR, 160, 0, 0) : kdesc(tsm + L::UK, 128, 64, 0);
 #pragma unroll 1
                 for (int kb = 0; kb < D / 64; ++kb) {
 #pragma unroll
@@ -712,7 +715,8 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
 #pragma unroll 1
             for (int kk = 0; kk < P; ++kk) {
                 const uint64_t a0 = kdesc(task_sm(kk) + L::T16, 64, 0, 0);
-                const uint64_t b0 = mdesc(task_sm(kk) + L::BKG, C, 0, 0);
+                // [beta K e^b | beta V]: rows 0..63 of WQ then UK, 16 KB per column block
+                const uint64_t b0 = mdesc(task_sm(kk) + L::WQ, 128, 0, 0);
 #pragma unroll
                 for (int s4 = 0; s4 < 4; ++s4)
                     mma_bf16(task_tmem(kk) + TC_W, dstep(a0, s4 * 2), dstep(b0, s4 * 128), id, s4 > 0);
@@ -723,11 +727,14 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
         tc_fence_after();
         // ---------------------------------------------- E: W and U tiles
         {
-            // the 2D columns W | U split into NW / 4 parts of CPP columns
+            // the 2D columns W | U split into NW / 4 parts of CPP columns;
+            // -W into rows 0..63 of WQ, U into rows 0..63 of UK
             constexpr int CPP = 2 * D / (NW / 4);
             const int r = acc_row(64, qd, lane);
             const int w0 = cp * CPP;                   // first column of the part in W | U
-            uint8_t *dst = w0 < D ? wt : ut;
+            const bool is_w = w0 < D;
+            uint8_t *dst = is_w ? wq : uk;
+            const float sgn = is_w ? -1.0f : 1.0f;
             const int c0 = w0 % D;
 #pragma unroll
             for (int cb = 0; cb < CPP; cb += 32) {
@@ -735,7 +742,9 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
                 tmem_ld32(tq + TC_W + w0 + cb, v);
                 if (r >= 0) {
 #pragma unroll
-                    for (int i = 0; i < 32; i += 8) st_bf16x8(dst, C, r, c0 + cb + i, v + i);
+                    for (int i = 0; i < 32; ++i) v[i] *= sgn;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) st_bf16x8(dst, 128, r, c0 + cb + i, v + i);
                 }
             }
         }
@@ -743,7 +752,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
         // ---------------------------------------------- F: record out
         if (leader && len > 0) {
             uint8_t *rec = p.records + ((int64_t)cur.w * H + h) * Rec::BYTES;
-            bulk_store(rec + Rec::PAIR, pair, 4 * L::tile64);
+            bulk_store(rec + Rec::WQ, wq, 4 * L::tile64);
             bulk_store(rec + Rec::AQ, aqk, 8192);
             if (GATED) bulk_store(rec + Rec::GEND, sgend, 4 * D);
             bulk_commit();

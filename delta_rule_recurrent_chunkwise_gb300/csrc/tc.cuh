@@ -73,6 +73,7 @@ constexpr uint32_t kSpinLimit = 1u << 22;
 // (after recording `code` in *err) if it does not complete in time.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *err,
                                           unsigned code) {
+    if (mbar_test_wait(bar, parity)) return true;  // already complete: no suspend
     for (uint32_t i = 0; i < kSpinLimit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     if (err) atomicCAS(err, 0u, code);

@@ -90,19 +90,22 @@ __device__ __forceinline__ void tmem_cols(uint32_t taddr, float (&v)[NC]) {
 
 // Per-(chunk, head) record written by the intra-chunk kernel and read by the
 // inter-chunk kernel, byte-for-byte the shared-memory image of its operands:
-//   PAIR  [Q e^{b} ; K e^{b_end - b}]  128-row RS tile (A operand of O = Q S;
-//                                      MN-major A operand of S += K~^T u)
-//   W     T (beta K e^{b})              64-row RS tile
-//   U     T (beta V)                    64-row RS tile
-//   AQ    Aq (masked, decayed scores)   64 x 64 RS tile
-//   GEND  e^{b_end} per key channel     fp32 [D]
+//   WQ    [-W ; Q e^{b}]                 128-row RS tile (W = T (beta K e^{b}));
+//                                        A operand of the stacked product
+//                                        [-W ; Q e^b] S  (M = 128)
+//   UK    [U ; K e^{b_end - b}]          128-row RS tile (U = T (beta V));
+//                                        rows 64..127 are the MN-major A
+//                                        operand of S += K~^T u
+//   AQ    Aq (masked, decayed scores)    64 x 64 RS tile, right after UK so
+//                                        that [UK's last 64 rows ; Aq] is a
+//                                        128-row operand
+//   GEND  e^{b_end} per key channel      fp32 [D]
 // Rows past the end of a ragged chunk are zero in every tile.
 template <int D>
 struct Record {
     static constexpr uint32_t tile64 = C * D * 2;
-    static constexpr uint32_t PAIR = 0;
-    static constexpr uint32_t W = 2 * tile64;
-    static constexpr uint32_t U = 3 * tile64;
+    static constexpr uint32_t WQ = 0;
+    static constexpr uint32_t UK = 2 * tile64;
     static constexpr uint32_t AQ = 4 * tile64;
     static constexpr uint32_t GEND = AQ + 8192;
     static constexpr uint32_t BYTES = (GEND + 4 * D + 1023) & ~1023u;
