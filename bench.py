@@ -263,11 +263,15 @@ def run_ours(args, rank, world, dev, dist):
         nbytes, flops = prefill_algo(w)
         achieved = nbytes / (kern_ms / 1e3) / 1e9
         traffic = ncu_traffic("delta_prefill:" + HEADLINE)
+        # the tensor-core path (it takes a workspace) launches the chunk table,
+        # the intra-chunk and the inter-chunk kernels; the fp32 path one kernel
+        per_call = 3 if pf.ws is not None else 1
         result.update(
-            value=value, ms_per_step=total_ms / args.steps, gpu_launches=args.steps,
+            value=value, ms_per_step=total_ms / args.steps, gpu_launches=per_call * args.steps,
             roofline={"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                       "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
-                      "kernel": "la_prefill_delta (chunkwise delta rule)",
+                      "kernel": "one la_prefill_delta call: chunk table + intra-chunk + "
+                                "inter-chunk kernels, timed together",
                       "algorithmic_bytes_per_launch": nbytes,
                       "tensor_tflops": flops / (kern_ms / 1e3) / 1e12,
                       "tensor_frac": flops / (kern_ms / 1e3) / 1e12 / pk["bf16_tflops"],
@@ -374,20 +378,23 @@ def record_traffic(args):
     name_i = hdr.index("Kernel Name")
     rd, wr = hdr.index("dram__bytes_read.sum"), hdr.index("dram__bytes_write.sum")
     scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
-    found = None
+    # one call of the path: the first launch of each distinct kernel matching the regex
+    found, seen = 0.0, set()
     for r in rows[2:]:
-        if re.search(args.kernel_regex, r[name_i]):
-            found = (float(r[rd].replace(",", "")) * scale[units[rd]] +
-                     float(r[wr].replace(",", "")) * scale[units[wr]])
-            break
-    if found is None:
+        name = r[name_i]
+        if re.search(args.kernel_regex, name) and name not in seen:
+            seen.add(name)
+            found += (float(r[rd].replace(",", "")) * scale[units[rd]] +
+                      float(r[wr].replace(",", "")) * scale[units[wr]])
+    if not seen:
         raise SystemExit("kernel not found in the capture")
     path = os.path.join(ROOT, "profiles", "traffic.json")
     data = json.load(open(path)) if os.path.exists(path) else {}
     data[args.traffic_key] = {"source_hash": kernel_source_hash(args.traffic_key),
                               "dram_bytes_per_launch": found * args.launch_scale,
                               "captured_bytes": found, "launch_scale": args.launch_scale,
-                              "capture": os.path.basename(args.record_traffic)}
+                              "capture": os.path.basename(args.record_traffic),
+                              "kernels": sorted(seen)}
     with open(path, "w") as f:
         json.dump(data, f, indent=1, sort_keys=True)
     print(json.dumps(data[args.traffic_key]))
@@ -443,7 +450,7 @@ def main():
                     help="read dram bytes of one kernel from `ncu -i X --page raw --csv` output "
                          "and store them in profiles/traffic.json under --traffic-key")
     ap.add_argument("--traffic-key", default="delta_prefill:" + HEADLINE)
-    ap.add_argument("--kernel-regex", default="delta_chunk_tc")
+    ap.add_argument("--kernel-regex", default="chunk_table|delta_intra|delta_inter")
     ap.add_argument("--launch-scale", type=float, default=1.0,
                     help="units of a full launch / units of the captured launch")
     ap.add_argument("--profile-case", default=None,
