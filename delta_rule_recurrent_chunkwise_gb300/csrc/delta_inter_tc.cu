@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(NT, 1) delta_inter_kernel(InterParams p) {
     auto issue_rec = [&](int c) {
         fence_proxy_async();
         mbar_arrive_expect_tx(rec_bar(c), Rec::BYTES);
-        bulk_load(buf(c), rec_src(c), Rec::BYTES, rec_bar(c));
+        bulk_load_hint(buf(c), rec_src(c), Rec::BYTES, rec_bar(c), l2_evict_first());
     };
 
     if (tid == 0) {

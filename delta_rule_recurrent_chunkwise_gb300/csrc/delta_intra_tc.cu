@@ -563,20 +563,17 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
         // the next task is known to every thread now: prefetch its beta
         const int4 nx = *sinfo;
         const float beta_nx = load_beta(nx);
-        // ---------------------------------------------- C1: Aq tile, A rows, T_RR
+        // ---------------------------------------------- C1: Aq tile, A rows
         // TMEM lanes 0..63 hold rows of Aq, lanes 64..127 rows of A (before
         // beta).  Gated: block R's product sits at column 8R(R+1).  A warp
         // spans two blocks, so it reads both (TMEM addresses stay
         // warp-uniform) and each lane keeps its own.
-        //  - every warp: 64 / (NW / 4) columns (part cp) of its quarter -> Aq
-        //    tile / A rows
-        //  - warps 2, 3 then invert the diagonal 16x16 blocks, read straight
-        //    from TMEM: T_RR = (I + A_RR)^{-1}, lane rho of each 16-lane group
-        //    owning row rho (forward substitution with shuffles)
+        // Every warp: 64 / (NW / 4) columns (part cp) of its quarter -> Aq
+        // tile / A rows (beta-scaled, strictly lower, fp32).
         {
             const bool is_q = qd < 2;
             const int rb0 = 32 * (is_q ? qd : qd - 2);
-            const int r = rb0 + lane, R = r >> 4, rho = r & 15;
+            const int r = rb0 + lane, R = r >> 4;
             const int Rw = rb0 >> 4;
             auto colof = [](int Rb) { return GATED ? 8 * Rb * (Rb + 1) : 0; };
 #pragma unroll
@@ -613,37 +610,34 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
                     }
                 }
             }
-            if (lw == 2 || lw == 3) {
-                // diagonal block values, beta-scaled and strict, staged per lane
-                // in shared memory so the substitution loop can stay rolled
-                float *dgs = sX + (lw - 2) * 32 * 17 + lane * 17;
-                {
-                    float w0[16], w1[16];
-                    tmem_ld16(tq + TC_A + colof(Rw) + 16 * Rw, w0);
-                    tmem_ld16(tq + TC_A + colof(Rw + 1) + 16 * (Rw + 1), w1);
-                    const float be = sbeta[r];
+        }
+        // T starts at zero; the solve below fills its diagonal blocks, the
+        // merges its lower blocks
+        for (int u = ltid; u < 64 * 16; u += NTC)
+            reinterpret_cast<float4 *>(sT + (u >> 4) * LDT)[u & 15] = make_float4(0.f, 0.f, 0.f, 0.f);
+        __syncthreads();
+        // ---------------------------------------------- C1b: T_RR = (I + A_RR)^{-1}
+        // Column-oriented forward substitution: lane (R, j) of warps 2, 3
+        // owns column j of block R and needs only its own earlier entries
+        // (A broadcast from shared memory), so there is no cross-lane
+        // exchange on the chain:  T[r][j] = [r == j] - sum_{k<r} A[r][k] T[k][j].
+        if (lw == 2 || lw == 3) {
+            const int R = 2 * (lw - 2) + (lane >> 4), j = lane & 15;
+            const float *Ab = sA + (16 * R) * LDT + 16 * R;
+            float t[16];
 #pragma unroll
-                    for (int m = 0; m < 16; ++m) dgs[m] = (m < rho) ? be * ((R == Rw) ? w0[m] : w1[m]) : 0.0f;
+            for (int r = 0; r < 16; ++r) {
+                float a0 = (r == j) ? 1.0f : 0.0f, a1 = 0.0f;
+#pragma unroll
+                for (int k = 0; k < r; ++k) {
+                    if (k & 1) a1 = fmaf(-Ab[r * LDT + k], t[k], a1);
+                    else a0 = fmaf(-Ab[r * LDT + k], t[k], a0);
                 }
-                float t[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) t[j] = (j == rho) ? 1.0f : 0.0f;
-                const int gbase = lane & 16;
-#pragma unroll 1
-                for (int m = 0; m < 15; ++m) {
-                    const float a = dgs[m];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float tm = __shfl_sync(0xffffffffu, t[j], gbase + m);
-                        if (j <= m) t[j] -= a * tm;
-                    }
-                }
-                float4 *dst = reinterpret_cast<float4 *>(sT + r * LDT);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) dst[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int j = 0; j < 16; j += 4) dst[(16 * R + j) >> 2] = make_float4(t[j], t[j + 1], t[j + 2], t[j + 3]);
+                t[r] = a0 + a1;
             }
+            float *Tb = sT + (16 * R) * LDT + 16 * R + j;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) Tb[r * LDT] = t[r];
         }
         __syncthreads();
         // ---------------------------------------------- C2: off-diagonal blocks of T
