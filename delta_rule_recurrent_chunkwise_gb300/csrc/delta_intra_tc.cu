@@ -225,14 +225,17 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
     auto task_tmem = [&](int kk) { return tmem + kk * L::TCOLS; };
 
     // Task t = slot * H + head.  {first token, length, head, slot}; length 0
-    // marks a slot no chunk occupies (or a table entry out of range).
-    auto task_info = [&](int64_t t) -> int4 {
+    // marks a slot no chunk occupies (or a table entry out of range).  The
+    // table entry is fetched (table_entry) well before it is decoded
+    // (task_info), so the load's latency stays off the critical path.
+    auto table_entry = [&](int64_t t) -> int2 {
+        return t < p.n_tasks ? p.table[t / H] : make_int2(0, 0);
+    };
+    auto task_info = [&](int64_t t, int2 e) -> int4 {
         int4 r = make_int4(0, 0, 0, 0);
-        if (t < p.n_tasks) {
+        if (t < p.n_tasks && e.x >= 0 && e.y > 0 && e.y <= C && e.x <= p.ntok - e.y) {
             const int64_t s = t / H;
-            const int2 e = p.table[s];
-            if (e.x >= 0 && e.y > 0 && e.y <= C && e.x <= p.ntok - e.y)
-                r = make_int4(e.x, e.y, (int)(t - s * H), (int)s);
+            r = make_int4(e.x, e.y, (int)(t - s * H), (int)s);
         }
         return r;
     };
@@ -258,7 +261,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
     // issues and waits for its raw tiles and stores its record.
     const int64_t n_groups = (p.n_tasks + P - 1) / P;
     int64_t g = blockIdx.x;
-    int4 cur = task_info(g * P + kslot);
+    int4 cur = task_info(g * P + kslot, table_entry(g * P + kslot));
     bool tma_pending = false;  // meaningful in the leader
     if (leader && cur.y > 0) {
         issue_tma(cur.x, cur.z);
@@ -286,9 +289,12 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
 
     while (g < n_groups) {
         const int64_t g_next = g + gridDim.x;
-        int4 nxt = make_int4(0, 0, 0, 0);
-        if (leader) nxt = task_info(g_next * P + kslot);  // consumed after the operand stage
-        if (!__syncthreads_or(cur.y > 0)) {
+        int2 nxt_e = make_int2(0, 0);
+        if (leader) nxt_e = table_entry(g_next * P + kslot);  // decoded after the operand stage
+        // one task per CTA: cur is the same in every thread
+        const bool any_task = P == 1 ? cur.y > 0 : __syncthreads_or(cur.y > 0);
+        if (!any_task) {
+            const int4 nxt = leader ? task_info(g_next * P + kslot, nxt_e) : make_int4(0, 0, 0, 0);
             // empty slots only: nothing to compute, start the next tasks' loads
             if (leader) {
                 *sinfo = nxt;
@@ -528,6 +534,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
         phase_sync();
         // raw tiles consumed: fetch the next task's while this one computes
         if (leader) {
+            const int4 nxt = task_info(g_next * P + kslot, nxt_e);
             *sinfo = nxt;
             if (nxt.y > 0) {
                 issue_tma(nxt.x, nxt.z);
