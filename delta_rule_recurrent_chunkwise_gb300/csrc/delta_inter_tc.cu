@@ -140,6 +140,8 @@ __global__ void __launch_bounds__(NT, 1) delta_inter_kernel(InterParams p) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the records come from the intra-chunk kernel (launched just before)
+    grid_wait_prerequisites();
     const uint32_t tmem = *tslot;
     const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);  // this warp's lane quarter
     auto acc = [&](int c) { return (uint32_t)(TC::ACC + (c & 1) * D); };
@@ -385,8 +387,7 @@ cudaError_t launch_t(const TcLaunch &x, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(a.H, a.N);
-    kern<<<grid, NT, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_programmatic(kern, grid, dim3(NT), smem, s, p);
 }
 
 }  // namespace

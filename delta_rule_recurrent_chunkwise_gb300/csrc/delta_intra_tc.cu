@@ -261,6 +261,10 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
     // issues and waits for its raw tiles and stores its record.
     const int64_t n_groups = (p.n_tasks + P - 1) / P;
     int64_t g = blockIdx.x;
+    // the chunk table comes from the previous launch; the inter-chunk kernel
+    // may be scheduled as SMs free up (it waits for this grid to finish)
+    grid_wait_prerequisites();
+    grid_launch_dependents();
     int4 cur = task_info(g * P + kslot, table_entry(g * P + kslot));
     bool tma_pending = false;  // meaningful in the leader
     if (leader && cur.y > 0) {
@@ -777,6 +781,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
 // for the (at most two) unused slots before the next sequence's first one.
 __global__ void chunk_table_kernel(const int32_t *cu, int N, int ntok, int64_t slots,
                                    int2 *table) {
+    grid_launch_dependents();  // the intra-chunk kernel may start its prologue
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (gw >= N) return;
@@ -809,8 +814,7 @@ cudaError_t launch_t(const TcLaunch &x, cudaStream_t s) {
     const int64_t slots = (int64_t)x.sms * L::CTAS_PER_SM;
     const unsigned grid = (unsigned)(groups < slots ? groups : slots);
     if (grid == 0) return cudaSuccess;
-    kern<<<grid, L::NT, smem, s>>>(x.mq, x.mk, x.mv, x.mg, p);
-    return cudaGetLastError();
+    return launch_programmatic(kern, dim3(grid), dim3(L::NT), smem, s, x.mq, x.mk, x.mv, x.mg, p);
 }
 
 }  // namespace

@@ -20,6 +20,25 @@ struct TcLaunch {
     int sms;                     // multiprocessors of the current device
 };
 
+// Launch with the programmatic-stream-serialisation attribute: the kernel
+// may start while the previous kernel on the stream finishes, and must wait
+// (griddepcontrol.wait) before reading that kernel's output.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_programmatic(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 cudaError_t launch_chunk_table(const TcLaunch &x, cudaStream_t s);
 cudaError_t launch_delta_intra(const TcLaunch &x, cudaStream_t s);
 cudaError_t launch_delta_inter(const TcLaunch &x, cudaStream_t s);

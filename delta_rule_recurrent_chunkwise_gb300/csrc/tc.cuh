@@ -80,6 +80,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
     return false;
 }
 
+// ------------------------------------------------ programmatic dependent launch
+// The three prefill kernels run back to back on one stream; each lets the
+// next one be scheduled early (launch_dependents) and the next one waits,
+// before its first read of the previous kernel's output, until that kernel
+// has completed and its writes are visible (wait).  A kernel launched
+// without the programmatic attribute passes through wait at once.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_wait_prerequisites() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- proxies
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy reads (tcgen05.mma operands, TMA stores).
