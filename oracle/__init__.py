@@ -38,6 +38,7 @@ _LIB_PATH = os.path.join(_OUT_DIR, "liblinattn_oracle.so")
 L2NORM_K = 1
 L2NORM_Q = 2
 SILU_QK = 4
+SCALAR_GATE = 8   # gate_logits [ntok][H]: one decay per token and head
 
 def build(force: bool = False) -> str:
     """Compile the oracle shared library with gcc (no GPU needed)."""
@@ -73,6 +74,7 @@ class OracleLib:
             f.restype = c_int
         self.lib = lib
         self.L2NORM_K, self.L2NORM_Q, self.SILU_QK = L2NORM_K, L2NORM_Q, SILU_QK
+        self.SCALAR_GATE = SCALAR_GATE
 
     def linear(self, *a, **k):
         return _linear(self.lib, *a, **k)
@@ -179,7 +181,8 @@ def _delta(lib, q, k, v, beta_logits, gate_logits, cu_seqlens, scale=1.0, flags=
     """(Gated) delta rule, token by token.  gate_logits None means alpha = 1.
 
     Shapes: q,k [ntok,H,dk]; v [ntok,H,dv]; beta_logits [ntok,H];
-    gate_logits [ntok,H,dk]; init_S [N,H,dk,dv].  Returns (o, final_S) in fp64.
+    gate_logits [ntok,H,dk] (or [ntok,H] with flags & SCALAR_GATE);
+    init_S [N,H,dk,dv].  Returns (o, final_S) in fp64.
     """
     q, k, v, bl, gl = _f64(q), _f64(k), _f64(v), _f64(beta_logits), _f64(gate_logits)
     cu, cup = _cu(cu_seqlens)

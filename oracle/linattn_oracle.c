@@ -23,6 +23,8 @@
  *   v, o         [ntok][H][dv]
  *   beta_logits  [ntok][H]
  *   gate_logits  [ntok][H][dk]      (NULL: no decay, alpha = 1)
+ *                [ntok][H]          with ORACLE_SCALAR_GATE (one decay per
+ *                                   token and head, all key channels)
  *   S, init/final[N][H][dk][dv]
  *   z            [N][H][dk]          (ELU+1 normaliser)
  */
@@ -37,6 +39,7 @@
 #define ORACLE_L2NORM_K 1u
 #define ORACLE_L2NORM_Q 2u
 #define ORACLE_SILU_QK 4u
+#define ORACLE_SCALAR_GATE 8u
 
 /* ---------------------------------------------------------------- prologue */
 
@@ -226,8 +229,13 @@ static void delta_pair(void *vctx, int64_t pair) {
         const double *vt = c->v + (t * H + h) * dv;
         double *ot = c->o + (t * H + h) * dv;
         const double beta = sigmoid(c->beta_logits[t * H + h]);
+        /* one decay per key channel (section KDA / Kimi Linear), or one per
+         * token and head for every channel (section Gated DeltaNet) */
+        const int scalar_gate = (c->flags & ORACLE_SCALAR_GATE) != 0;
         for (int i = 0; i < dk; ++i)
-            alpha[i] = c->gate_logits ? exp(-softplus(c->gate_logits[(t * H + h) * dk + i])) : 1.0;
+            alpha[i] = !c->gate_logits ? 1.0
+                       : exp(-softplus(scalar_gate ? c->gate_logits[t * H + h]
+                                                   : c->gate_logits[(t * H + h) * dk + i]));
         /* S' = Diag(alpha) S */
         for (int i = 0; i < dk; ++i)
             for (int j = 0; j < dv; ++j) S[i * dv + j] *= alpha[i];

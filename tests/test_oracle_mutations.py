@@ -25,7 +25,7 @@ MUTATIONS = [
     ("scale dropped", "ot[j] = c->scale * acc;", "ot[j] = acc;", 1),
     ("sigmoid sign", "if (x >= 0.0) return 1.0 / (1.0 + exp(-x));",
      "if (x >= 0.0) return 1.0 / (1.0 + exp(x));", 1),
-    ("softplus sign", "? exp(-softplus(c->gate_logits", "? exp(softplus(c->gate_logits", 1),
+    ("softplus sign", ": exp(-softplus(scalar_gate", ": exp(softplus(scalar_gate", 1),
     ("norm without sqrt", "double nrm = sqrt(s);", "double nrm = s;", 1),
     ("feature map without +1", "return x > 0.0 ? x + 1.0 : exp(x);",
      "return x > 0.0 ? x : exp(x);", 1),
@@ -37,6 +37,10 @@ MUTATIONS = [
      "if (0) memcpy(S, c->init_S + sbase", 2),
     ("first token of each sequence skipped", "for (int64_t t = c->cu[n]; t < c->cu[n + 1]; ++t)",
      "for (int64_t t = c->cu[n] + 1; t < c->cu[n + 1]; ++t)", 2),
+    ("scalar gate of head 0 for every head", "scalar_gate ? c->gate_logits[t * H + h]",
+     "scalar_gate ? c->gate_logits[t * H]", 1),
+    ("scalar gate taken as no decay", "alpha[i] = !c->gate_logits ? 1.0",
+     "alpha[i] = (!c->gate_logits || scalar_gate) ? 1.0", 1),
 ]
 
 

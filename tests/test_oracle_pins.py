@@ -296,6 +296,56 @@ def test_gate_one_equals_pure_delta_and_gate_zero_restarts():
     np.testing.assert_allclose(S_all, S_tail, rtol=1e-12, atol=1e-14)
 
 
+def test_scalar_gate_decays_orthonormal_memories_exactly():
+    """One decay per token and head (section Gated DeltaNet): with
+    orthonormal keys and beta = 1 nothing interferes, so after T steps the
+    memory written at step j reads back as prod_{t>j} alpha_t times v_j."""
+    r = rng(30)
+    dk, dv, H = 12, 5, 2
+    T = dk
+    Qm, _ = np.linalg.qr(r.normal(size=(dk, dk)))
+    k = np.stack([Qm.T for _ in range(H)], axis=1)
+    v = r.normal(size=(T, H, dv))
+    q = r.normal(size=(T, H, dk))
+    bl = np.full((T, H), BIG)
+    gl = r.normal(size=(T, H)) + 1.0
+    _, S = oracle.delta(q, k, v, bl, gl, [0, T], flags=oracle.L2NORM_K | oracle.SCALAR_GATE)
+    la = log_alpha_from_logits(gl)                       # [T][H]
+    for h in range(H):
+        tail = np.exp(np.cumsum(la[::-1, h])[::-1])      # prod_{t>=j} alpha_t
+        decay_after = np.append(tail[1:], 1.0)           # prod_{t>j} alpha_t
+        np.testing.assert_allclose(k[:, h] @ S[0, h], decay_after[:, None] * v[:, h],
+                                   rtol=1e-12, atol=1e-14)
+
+
+def test_scalar_gate_is_the_per_channel_gate_held_constant_across_channels():
+    r = rng(31)
+    lens = [23, 1, 40]
+    H, dk, dv = 3, 6, 4
+    ntok = sum(lens)
+    q, k, v = r.normal(size=(ntok, H, dk)), r.normal(size=(ntok, H, dk)), r.normal(size=(ntok, H, dv))
+    bl = r.normal(size=(ntok, H))
+    gl = r.normal(size=(ntok, H)) + 2.0
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    S0 = r.normal(size=(len(lens), H, dk, dv))
+    o_s, S_s = oracle.delta(q, k, v, bl, gl, cu, flags=oracle.L2NORM_K | oracle.SCALAR_GATE,
+                            init_S=S0)
+    o_c, S_c = oracle.delta(q, k, v, bl, np.repeat(gl[:, :, None], dk, axis=2), cu,
+                            flags=oracle.L2NORM_K, init_S=S0)
+    np.testing.assert_array_equal(o_s, o_c)
+    np.testing.assert_array_equal(S_s, S_c)
+    # a zero decay at one token restarts the memory from there (per head)
+    t0 = 9
+    gl2 = gl[:40].copy()
+    gl2[t0] = BIG
+    o_all, S_all = oracle.delta(q[:40], k[:40], v[:40], bl[:40], gl2, [0, 40],
+                                flags=oracle.L2NORM_K | oracle.SCALAR_GATE, init_S=S0[:1])
+    o_tail, S_tail = oracle.delta(q[t0:40], k[t0:40], v[t0:40], bl[t0:40], gl2[t0:], [0, 40 - t0],
+                                  flags=oracle.L2NORM_K | oracle.SCALAR_GATE)
+    np.testing.assert_allclose(o_all[t0:], o_tail, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(S_all, S_tail, rtol=1e-12, atol=1e-14)
+
+
 def test_one_token_closed_form_and_scale():
     r = rng(11)
     H, dk, dv = 3, 8, 5
