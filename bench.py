@@ -60,13 +60,15 @@ def prefill_algo(w: wl.Workload, chunk=64, final_states=False):
     """Algorithmic bytes and contraction FLOPs of one delta-rule prefill.
 
     Bytes: q, k, v read and o written once in the I/O dtype, beta logits
-    (one per token and head), gate logits (dk per token and head) when gated,
+    (one per token and head), gate logits (dk per token and head, or one with
+    a scalar gate) when gated,
     final states (fp32) when returned.  FLOPs per token and head:
     10 C d + 6 d^2 (dense C x C tiles: K K^T, T K, T V, Q K^T, A u; and
     W S, Q S, K^T u), with d = dk = dv."""
     esz = torch.tensor([], dtype=w.dtype).element_size()
     th = w.ntok * w.H
-    per = esz * (2 * w.dk + 2 * w.dv) + esz + (esz * w.dk if w.gated else 0)
+    gate = (1 if w.extra.get("scalar_gate") else w.dk) if w.gated else 0
+    per = esz * (2 * w.dk + 2 * w.dv) + esz + esz * gate
     nbytes = th * per + (len(w.lengths) * w.H * w.dk * w.dv * 4 if final_states else 0)
     d = w.dk
     flops = th * (10 * chunk * d + 6 * d * d)
@@ -210,12 +212,13 @@ class Prefill:
         nbytes = la.la_prefill_delta_workspace_size(len(w.lengths), w.ntok, w.H, w.dk, w.dv)
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
         self.cu_host = inp["cu_seqlens"]
+        self.flags = la.LA_L2NORM_K | (la.LA_GATE_SCALAR if w.extra.get("scalar_gate") else 0)
 
     def step(self, stream):
         t = self.t
         self.la.la_prefill_delta(t["q"], t["k"], t["v"], t["beta_logits"], t["gate_logits"],
-                                 self.o, t["cu_seqlens"], final_S=self.fS, workspace=self.ws,
-                                 cu_seqlens_host=self.cu_host, stream=stream)
+                                 self.o, t["cu_seqlens"], flags=self.flags, final_S=self.fS,
+                                 workspace=self.ws, cu_seqlens_host=self.cu_host, stream=stream)
 
 
 def time_steps(step_fn, steps, warmup, flush, stream, barrier=None):
@@ -322,7 +325,7 @@ def run_ours(args, rank, world, dev, dist):
                                "state_bytes_per_step": decode_state_bytes(dw)}
             del toks, state, d
             # ---- gated and varlen prefills
-            for name in ("gated_prefill", "varlen_prefill"):
+            for name in ("gated_prefill", "varlen_prefill", "gpt2_scalar_gate"):
                 gw = wl.workload(name, seed=0)
                 fs = name == "varlen_prefill"
                 p = Prefill(la, gw, seed=rank_seed(rank), dev=dev, final_states=fs)

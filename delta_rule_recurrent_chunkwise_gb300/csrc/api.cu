@@ -26,14 +26,16 @@ la_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CU
 
 // Host checks shared by the delta-rule prefill entry points (workspace aside).
 la_status check_delta_args(const void *q, const void *k, const void *v, const void *beta_logits,
-                           const void *o, la_dtype io, const int32_t *cu_seqlens,
+                           const void *gate_logits, const void *o, la_dtype io,
+                           const int32_t *cu_seqlens,
                            const int32_t *cu_seqlens_host, int N, int ntok, int H, int dk,
                            int dv, int chunk, float scale, unsigned flags) {
     if (!q || !k || !v || !beta_logits || !o || !cu_seqlens || N < 1 || ntok < 0 || H < 1 ||
         !dtype_ok(io))
         return LA_ERR_INVALID_ARG;
     if (dk < 1 || dv < 1 || chunk < 1 || !std::isfinite(scale)) return LA_ERR_INVALID_ARG;
-    if (flags & ~(LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK)) return LA_ERR_INVALID_ARG;
+    if (flags & ~(LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK | LA_GATE_SCALAR)) return LA_ERR_INVALID_ARG;
+    if ((flags & LA_GATE_SCALAR) && !gate_logits) return LA_ERR_INVALID_ARG;
     if (!head_size_ok(dk) || !head_size_ok(dv) || chunk != 64) return LA_ERR_UNSUPPORTED;
     if (N > 65535 || H > 65535) return LA_ERR_UNSUPPORTED;
     return check_cu_host(cu_seqlens_host, N, ntok);
@@ -82,7 +84,7 @@ la_status la_prefill_delta(const void *q, const void *k, const void *v, const vo
                            int ntok, int H, int dk, int dv, int chunk, float scale,
                            unsigned flags, const float *init_S, float *final_S, void *workspace,
                            size_t workspace_bytes, void *stream) {
-    if (la_status st = check_delta_args(q, k, v, beta_logits, o, io, cu_seqlens, cu_seqlens_host,
+    if (la_status st = check_delta_args(q, k, v, beta_logits, gate_logits, o, io, cu_seqlens, cu_seqlens_host,
                                         N, ntok, H, dk, dv, chunk, scale, flags))
         return st;
     const size_t ws_need = la_prefill_delta_workspace_size(N, ntok, H, dk, dv, chunk, io);
@@ -104,7 +106,7 @@ la_status la_prefill_delta_static(const void *q, const void *k, const void *v,
                                   int dv, int chunk, float scale, unsigned flags,
                                   const float *init_S, float *final_S, void *stream) {
     static_assert(la::kStaticScratchBytes == LA_STATIC_SCRATCH_BYTES, "static scratch size");
-    if (la_status st = check_delta_args(q, k, v, beta_logits, o, io, cu_seqlens, cu_seqlens_host,
+    if (la_status st = check_delta_args(q, k, v, beta_logits, gate_logits, o, io, cu_seqlens, cu_seqlens_host,
                                         N, ntok, H, dk, dv, chunk, scale, flags))
         return st;
     const size_t need = la_prefill_delta_workspace_size(N, ntok, H, dk, dv, chunk, io);
@@ -122,7 +124,8 @@ la_status la_decode_step(const void *q, const void *k, const void *v, const void
     if (!q || !k || !v || !beta_logits || !o || !state || N < 1 || H < 1 || !dtype_ok(io))
         return LA_ERR_INVALID_ARG;
     if (dk < 1 || dv < 1 || !std::isfinite(scale)) return LA_ERR_INVALID_ARG;
-    if (flags & ~(LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK)) return LA_ERR_INVALID_ARG;
+    if (flags & ~(LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK | LA_GATE_SCALAR)) return LA_ERR_INVALID_ARG;
+    if ((flags & LA_GATE_SCALAR) && !gate_logits) return LA_ERR_INVALID_ARG;
     if (!head_size_ok(dk) || !head_size_ok(dv)) return LA_ERR_UNSUPPORTED;
     if ((int64_t)N * H * 2 > 0x7fffffffLL) return LA_ERR_UNSUPPORTED;
     la::DecodeArgs a{q, k, v, beta_logits, gate_logits, o, N, H, dk, dv, scale, flags, state,

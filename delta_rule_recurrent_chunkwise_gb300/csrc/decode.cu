@@ -72,9 +72,8 @@ __global__ void __launch_bounds__(256, 4) decode_step_kernel(DecodeParams p) {
         if (silu) { kv = silu_f(kv); qv = silu_f(qv); }
         sk[tid] = kv;
         sq[tid] = qv;
-        sa[tid] = p.gate_logits
-                      ? decay_f(to_f32(static_cast<const IO *>(p.gate_logits)[nh * DK + tid]))
-                      : 1.0f;
+        const int64_t gi = (p.flags & kGateScalar) ? nh : nh * DK + tid;  // scalar: one per head
+        sa[tid] = p.gate_logits ? decay_f(to_f32(static_cast<const IO *>(p.gate_logits)[gi])) : 1.0f;
     }
     if (tid < DVS) sv[tid] = to_f32(v[j0 + tid]);
     __syncthreads();

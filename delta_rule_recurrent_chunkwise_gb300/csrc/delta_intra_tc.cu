@@ -96,7 +96,12 @@ struct Layout {
     static constexpr uint32_t QN = KN + 256;                   // fp32 [64]
     static constexpr uint32_t EB = QN + 256;                   // fp32 [4][D] block decay
     static constexpr uint32_t GEND = EB + 16 * D;              // fp32 [D] chunk decay
-    static constexpr uint32_t INFO = GEND + 4 * D;             // int4: next task
+    // scalar gate (one decay per token): log alpha, then cumulative b, and
+    // the row factors e^b, e^{b_end - b}
+    static constexpr uint32_t SLB = GEND + 4 * D;              // fp32 [64]
+    static constexpr uint32_t SEB = SLB + 256;                 // fp32 [64]
+    static constexpr uint32_t SEK = SEB + 256;                 // fp32 [64]
+    static constexpr uint32_t INFO = SEK + 256;                // int4: next task
     static constexpr uint32_t BAR_TMA = INFO + 16;             // mbarrier: raw tiles
     static constexpr uint32_t TASK_BYTES = (BAR_TMA + 8 + 1023) & ~1023u;
     static_assert(UK - WQ == Record<D>::UK, "record image");
@@ -151,6 +156,7 @@ __device__ __forceinline__ void store_c(float *Cp, int ldc, const float (&d)[4],
 
 struct IntraParams {
     const __nv_bfloat16 *beta_logits;
+    const __nv_bfloat16 *gate_scalar;  // [ntok][H] with a scalar gate (ungated kernel), else null
     const int2 *table;      // [slots] {first token, length}
     uint8_t *records;       // [slots][H] records
     unsigned *err;
@@ -160,7 +166,8 @@ struct IntraParams {
 };
 
 
-template <int D, bool GATED>
+// SCALAR: one decay per token and head (ungated layout plus per-row factors)
+template <int D, bool GATED, bool SCALAR>
 __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_PER_SM)
     delta_intra_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -191,6 +198,11 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
     float *sE = reinterpret_cast<float *>(sm + L::EB);
     float *sgend = reinterpret_cast<float *>(sm + L::GEND);
     int4 *sinfo = reinterpret_cast<int4 *>(sm + L::INFO);
+    float *sLb = reinterpret_cast<float *>(sm + L::SLB);
+    float *sEb = reinterpret_cast<float *>(sm + L::SEB);
+    float *sEk = reinterpret_cast<float *>(sm + L::SEK);
+    static_assert(!(GATED && SCALAR), "a scalar gate uses the ungated layout");
+    constexpr bool scalar = SCALAR;
     uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + L::BAR_TMA);
     uint64_t *bar_mma = reinterpret_cast<uint64_t *>(sbase + L::COMMON);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar_mma + 1);
@@ -239,20 +251,26 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
         }
         return r;
     };
+    const uint64_t pol = l2_evict_first();  // inputs and records pass through L2 once
     auto issue_tma = [&](int t0, int hh) {
         fence_proxy_async();
         mbar_arrive_expect_tx(bar_tma, tx_bytes);
 #pragma unroll
         for (int cb = 0; cb < D / 64; ++cb) {
-            tma_load_3d(rawq + cb * 8192, &tm_q, bar_tma, cb * 64, hh, t0);
-            tma_load_3d(rawk + cb * 8192, &tm_k, bar_tma, cb * 64, hh, t0);
-            tma_load_3d(rawv + cb * 8192, &tm_v, bar_tma, cb * 64, hh, t0);
-            if (GATED) tma_load_3d(rawg + cb * 8192, &tm_g, bar_tma, cb * 64, hh, t0);
+            tma_load_3d_hint(rawq + cb * 8192, &tm_q, bar_tma, cb * 64, hh, t0, pol);
+            tma_load_3d_hint(rawk + cb * 8192, &tm_k, bar_tma, cb * 64, hh, t0, pol);
+            tma_load_3d_hint(rawv + cb * 8192, &tm_v, bar_tma, cb * 64, hh, t0, pol);
+            if (GATED) tma_load_3d_hint(rawg + cb * 8192, &tm_g, bar_tma, cb * 64, hh, t0, pol);
         }
     };
     auto load_beta = [&](const int4 &ti) -> float {
         return (ltid < C && ltid < ti.y)
                    ? __bfloat162float(p.beta_logits[(int64_t)(ti.x + ltid) * H + ti.z])
+                   : 0.0f;
+    };
+    auto load_gate = [&](const int4 &ti) -> float {  // scalar gate logit of row ltid
+        return (scalar && ltid < C && ltid < ti.y)
+                   ? __bfloat162float(p.gate_scalar[(int64_t)(ti.x + ltid) * H + ti.z])
                    : 0.0f;
     };
 
@@ -272,6 +290,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
         tma_pending = true;
     }
     float beta_cur = load_beta(cur);  // threads 0..63 of the task
+    float gate_cur = load_gate(cur);
     uint32_t tma_par = 0, mma_par = 0;
     bool failed = false;
 
@@ -310,6 +329,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
             __syncthreads();
             cur = *sinfo;
             beta_cur = load_beta(cur);
+            gate_cur = load_gate(cur);
             g = g_next;
             __syncthreads();
             continue;
@@ -331,6 +351,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
         }
         // ---------------------------------------------- A0: beta, row norms
         if (ltid < C) sbeta[ltid] = ltid < len ? __fdividef(1.0f, 1.0f + __expf(-beta_cur)) : 0.0f;
+        if (scalar && ltid < C) sLb[ltid] = ltid < len ? log_decay_f(gate_cur) : 0.0f;  // log alpha
         {
             // TPR threads per row, D/TPR channels each, 16-byte loads
             constexpr int TPR = NTC / C;
@@ -363,6 +384,29 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
         __syncthreads();
         // ---------------------------------------------- A1: operand tiles
         if (!GATED) {
+            if (scalar) {
+                // b_r = sum_{t<=r} log alpha_t inside the chunk (warp 0, two rows
+                // per lane); row factors e^{b_r} and e^{b_end - b_r} (both <= 1)
+                if (warp == 0) {
+                    const float l0 = sLb[2 * lane], l1 = sLb[2 * lane + 1];
+                    float x = l0 + l1;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float y = __shfl_up_sync(0xffffffffu, x, o);
+                        if (lane >= o) x += y;
+                    }
+                    const float b1 = x, b0 = x - l1;
+                    const float bend = __shfl_sync(0xffffffffu, x, 31);  // b of row 63 = b_end
+                    sLb[2 * lane] = b0;
+                    sLb[2 * lane + 1] = b1;
+                    sEb[2 * lane] = __expf(b0);
+                    sEb[2 * lane + 1] = __expf(b1);
+                    sEk[2 * lane] = __expf(bend - b0);
+                    sEk[2 * lane + 1] = __expf(bend - b1);
+                }
+                __syncthreads();
+                if (ltid < D) sgend[ltid] = sEb[63];  // e^{b_end}, the same for every channel
+            }
             // [q^; k^] into QKH; beta k^, q^ into WQ; beta v, k^ into UK: 16-byte units
             for (int u = ltid; u < C * D / 8; u += NTC) {
                 const uint32_t off = (uint32_t)u * 16u;                 // offset in a [64][D] tile
@@ -386,12 +430,22 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
                 const uint4 qh = pack8(qv), kh = pack8(kv);
                 *reinterpret_cast<uint4 *>(qkh + po) = qh;
                 *reinterpret_cast<uint4 *>(qkh + po + 64u * 128u) = kh;
-                *reinterpret_cast<uint4 *>(wq + po) = pack8(bk);
-                *reinterpret_cast<uint4 *>(wq + po + 64u * 128u) = qh;
                 *reinterpret_cast<uint4 *>(uk + po) = pack8(vv);
-                *reinterpret_cast<uint4 *>(uk + po + 64u * 128u) = kh;
+                if (scalar) {
+                    // Q e^b, beta K e^b, K e^{b_end - b}: one factor per row
+                    const float eb = sEb[r], ek = sEk[r];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) { bk[i] *= eb; qv[i] *= eb; kv[i] *= ek; }
+                    *reinterpret_cast<uint4 *>(wq + po) = pack8(bk);
+                    *reinterpret_cast<uint4 *>(wq + po + 64u * 128u) = pack8(qv);
+                    *reinterpret_cast<uint4 *>(uk + po + 64u * 128u) = pack8(kv);
+                } else {
+                    *reinterpret_cast<uint4 *>(wq + po) = pack8(bk);
+                    *reinterpret_cast<uint4 *>(wq + po + 64u * 128u) = qh;
+                    *reinterpret_cast<uint4 *>(uk + po + 64u * 128u) = kh;
+                }
             }
-            if (ltid < D) sgend[ltid] = 1.0f;
+            if (!scalar && ltid < D) sgend[ltid] = 1.0f;
         } else {
             // One thread per (2 key channels, 8 rows of a 16-token block R); the
             // two 8-row halves of a block sit in lanes l and l^16 of one warp.
@@ -558,7 +612,9 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
             for (int kk = 0; kk < P; ++kk) {
                 uint8_t *tsm = task_sm(kk);
                 const uint64_t a0 = kdesc(tsm + L::QKH, 128, 0, 0);
-                const uint64_t b0 = GATED ? kdesc(tsm + L::KR, 160, 0, 0) : kdesc(tsm + L::UK, 128, 64, 0);
+                // ungated: B = k^, the lower half of [q^; k^] (UK's lower half holds
+                // K e^{b_end - b} under a scalar gate)
+                const uint64_t b0 = GATED ? kdesc(tsm + L::KR, 160, 0, 0) : kdesc(tsm + L::QKH, 128, 64, 0);
 #pragma unroll 1
                 for (int kb = 0; kb < D / 64; ++kb) {
 #pragma unroll
@@ -574,6 +630,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
         // the next task is known to every thread now: prefetch its beta
         const int4 nx = *sinfo;
         const float beta_nx = load_beta(nx);
+        const float gate_nx = load_gate(nx);
         // ---------------------------------------------- C1: Aq tile, A rows
         // TMEM lanes 0..63 hold rows of Aq, lanes 64..127 rows of A (before
         // beta).  Gated: block R's product sits at column 8R(R+1).  A warp
@@ -600,6 +657,13 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
                     for (int i = 0; i < 16; ++i) v[i] = (R == Rw) ? w0[i] : w1[i];
                 } else {
                     tmem_ld16(tq + TC_A + col, v);
+                    if (scalar) {
+                        // e^{b_r - b_i} for i <= r (exponent <= 0); later columns are masked
+                        const float br = sLb[r];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            v[i] *= (col + i <= r) ? __expf(br - sLb[col + i]) : 0.0f;
+                    }
                 }
                 if (is_q) {
 #pragma unroll
@@ -757,13 +821,14 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
         // ---------------------------------------------- F: record out
         if (leader && len > 0) {
             uint8_t *rec = p.records + ((int64_t)cur.w * H + h) * Rec::BYTES;
-            bulk_store(rec + Rec::WQ, wq, 4 * L::tile64);
-            bulk_store(rec + Rec::AQ, aqk, 8192);
-            if (GATED) bulk_store(rec + Rec::GEND, sgend, 4 * D);
+            bulk_store_hint(rec + Rec::WQ, wq, 4 * L::tile64, pol);
+            bulk_store_hint(rec + Rec::AQ, aqk, 8192, pol);
+            if (GATED || scalar) bulk_store_hint(rec + Rec::GEND, sgend, 4 * D, pol);
             bulk_commit();
         }
         cur = nx;
         beta_cur = beta_nx;
+        gate_cur = gate_nx;
         g = g_next;
     }
 
@@ -797,9 +862,11 @@ __global__ void chunk_table_kernel(const int32_t *cu, int N, int ntok, int64_t s
     for (int64_t s = b + nc + lane; s < gap_end; s += 32) table[s] = make_int2(0, 0);
 }
 
-template <int D, bool GATED>
+template <int D, bool GATED, bool SCALAR>
 cudaError_t launch_t(const TcLaunch &x, cudaStream_t s) {
-    IntraParams p{static_cast<const __nv_bfloat16 *>(x.a->beta_logits), x.table, x.records,
+    IntraParams p{static_cast<const __nv_bfloat16 *>(x.a->beta_logits),
+                  SCALAR ? static_cast<const __nv_bfloat16 *>(x.a->gate_logits) : nullptr,
+                  x.table, x.records,
                   x.err, x.slots * x.a->H, x.a->H, x.a->ntok, x.a->flags};
     using L = Layout<D, GATED>;
     // Shared memory caps the CTAs per SM at CTAS_PER_SM, which keeps their
@@ -807,7 +874,7 @@ cudaError_t launch_t(const TcLaunch &x, cudaStream_t s) {
     constexpr size_t need = L::TOTAL + 1024;
     constexpr size_t floor_ = L::CTAS_PER_SM == 1 ? 120 * 1024 : 77 * 1024;
     const size_t smem = need > floor_ ? need : floor_;
-    auto kern = delta_intra_kernel<D, GATED>;
+    auto kern = delta_intra_kernel<D, GATED, SCALAR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t groups = (p.n_tasks + L::P - 1) / L::P;
@@ -828,9 +895,15 @@ cudaError_t launch_chunk_table(const TcLaunch &x, cudaStream_t s) {
 }
 
 cudaError_t launch_delta_intra(const TcLaunch &x, cudaStream_t s) {
-    const bool g = x.a->gate_logits != nullptr;
-    if (x.a->dk == 128) return g ? launch_t<128, true>(x, s) : launch_t<128, false>(x, s);
-    return g ? launch_t<64, true>(x, s) : launch_t<64, false>(x, s);
+    // per-channel gate: the gated kernel; scalar gate: the ungated one, which
+    // applies the per-row decay itself
+    const bool sc = x.a->gate_logits != nullptr && (x.a->flags & kGateScalar);
+    const bool g = x.a->gate_logits != nullptr && !sc;
+    if (x.a->dk == 128)
+        return g ? launch_t<128, true, false>(x, s)
+                 : sc ? launch_t<128, false, true>(x, s) : launch_t<128, false, false>(x, s);
+    return g ? launch_t<64, true, false>(x, s)
+             : sc ? launch_t<64, false, true>(x, s) : launch_t<64, false, false>(x, s);
 }
 
 }  // namespace la

@@ -73,6 +73,7 @@ __global__ void __launch_bounds__(kNT) delta_chunk_simt_kernel(SimtParams p) {
     const int n = blockIdx.z, h = blockIdx.y, j0 = blockIdx.x * DVS;
     const int H = p.H, dv = p.dv;
     const bool gated = p.gate_logits != nullptr;
+    const bool gate_scalar = (p.flags & kGateScalar) != 0;  // gate [ntok][H]
     const bool silu = (p.flags & kSiluQK) != 0;
     const IO *Q = static_cast<const IO *>(p.q), *K = static_cast<const IO *>(p.k);
     const IO *V = static_cast<const IO *>(p.v);
@@ -101,7 +102,9 @@ __global__ void __launch_bounds__(kNT) delta_chunk_simt_kernel(SimtParams p) {
             const int64_t g = ((int64_t)(cs + r) * H + h) * DK + c;
             sK[r * LDK + c] = ok ? to_f32(K[g]) : 0.0f;
             sQ[r * LDK + c] = ok ? to_f32(Q[g]) : 0.0f;
-            if (gated) sB[r * LDK + c] = ok ? log_decay_f(to_f32(GL[g])) : 0.0f;
+            if (gated)
+                sB[r * LDK + c] = ok ? log_decay_f(to_f32(GL[gate_scalar ? (int64_t)(cs + r) * H + h : g]))
+                                     : 0.0f;
         }
         for (int e = tid; e < C * DVS; e += NT) {
             const int r = e / DVS, j = e % DVS;

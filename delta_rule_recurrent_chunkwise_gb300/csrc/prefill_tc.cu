@@ -8,6 +8,7 @@
 
 #include <mutex>
 
+#include "common.cuh"
 #include "delta_tc.h"
 #include "launch.h"
 #include "tc_tile.cuh"
@@ -90,7 +91,7 @@ cudaError_t launch_delta_tc(const PrefillArgs &a, cudaStream_t s) {
     if (!make_map(&x.mq, a.q, D, a.H, a.ntok) || !make_map(&x.mk, a.k, D, a.H, a.ntok) ||
         !make_map(&x.mv, a.v, D, a.H, a.ntok))
         return cudaErrorInvalidValue;
-    if (a.gate_logits) {
+    if (a.gate_logits && !(a.flags & kGateScalar)) {  // a scalar gate is read without TMA
         if (!make_map(&x.mg, a.gate_logits, D, a.H, a.ntok)) return cudaErrorInvalidValue;
     } else {
         x.mg = x.mq;

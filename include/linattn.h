@@ -67,6 +67,12 @@ typedef enum la_dtype { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
 #define LA_L2NORM_K 1u
 #define LA_L2NORM_Q 2u
 #define LA_SILU_QK 4u
+/* LA_GATE_SCALAR: gate_logits holds one value per token and head
+ * ([ntok][H] in prefill, [N][H] in decode) and alpha applies to every key
+ * channel alike -- the scalar decay of section Gated DeltaNet (Mamba-2's
+ * cache = alpha * S_old + S_new) instead of the per-key-channel decay of
+ * section KDA / Kimi Linear.  Requires gate_logits. */
+#define LA_GATE_SCALAR 8u
 
 /* Causal ELU+1 linear attention, chunkwise-parallel prefill.
  * Defined in section Linear attention (the forward() that replaces the KV
@@ -92,8 +98,9 @@ la_status la_prefill_linear(const void *q, const void *k, const void *v, void *o
  *   u_t = beta_t (v_t - S'^T k_t),  S_t = S' + k_t u_t^T,  o_t = scale S_t^T q_t
  * where beta_t = sigmoid(beta_logits[t][h]) and
  * alpha_t[c] = exp(-softplus(gate_logits[t][h][c])).
- * gate_logits: nullable; NULL means alpha = 1 (plain DeltaNet).
- * flags: LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK (see above).
+ * gate_logits: nullable; NULL means alpha = 1 (plain DeltaNet).  With
+ * LA_GATE_SCALAR it is [ntok][H] and alpha_t applies to all channels.
+ * flags: LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK | LA_GATE_SCALAR (above).
  * chunk: tokens per chunk; 64 is the supported value.
  * scale: output scale (the page's delta-rule listings use 1.0).
  * init_S: nullable [N][H][dk][dv]; final_S: nullable, may equal init_S.
@@ -150,7 +157,8 @@ la_status la_prefill_delta_static(const void *q, const void *k, const void *v,
  *   S' = Diag(alpha) S;  u = beta (v - S'^T k);  S <- S' + k u^T;
  *   o = scale S^T q.
  * q, k [N][H][dk]; v, o [N][H][dv]; beta_logits [N][H];
- * gate_logits [N][H][dk] or NULL (alpha = 1); state [N][H][dk][dv] fp32,
+ * gate_logits [N][H][dk] ([N][H] with LA_GATE_SCALAR) or NULL (alpha = 1);
+ * state [N][H][dk][dv] fp32,
  * read and rewritten once per call.  state must not alias any other buffer. */
 la_status la_decode_step(const void *q, const void *k, const void *v, const void *beta_logits,
                          const void *gate_logits, void *o, la_dtype io, int N, int H, int dk,

@@ -148,3 +148,14 @@ def test_static_entry_point_refuses_requests_beyond_its_scratch(lib):
     bad = (ctypes.c_int32 * 3)(0, 10, 5)   # rejected later, for its cu_seqlens_host
     assert d(FAKE, FAKE, FAKE, FAKE, None, FAKE, la.LA_BF16, FAKE, bad, *small, 64, 1.0, 1,
              None, None, None) == la.LA_ERR_INVALID_ARG
+
+
+def test_scalar_gate_flag_needs_gate_logits(lib):
+    """LA_GATE_SCALAR says how to read gate_logits; without them it is an
+    argument error (prefill, allocation-free prefill and decode)."""
+    args = (FAKE, FAKE, FAKE, FAKE, None, FAKE, la.LA_BF16, FAKE, None, 2, 40, 4, 64, 64, 64,
+            1.0, la.LA_L2NORM_K | la.LA_GATE_SCALAR, None, None)
+    assert lib.la_prefill_delta(*args, FAKE, 1 << 40, None) == la.LA_ERR_INVALID_ARG
+    assert lib.la_prefill_delta_static(*args, None) == la.LA_ERR_INVALID_ARG
+    assert lib.la_decode_step(FAKE, FAKE, FAKE, FAKE, None, FAKE, la.LA_BF16, 4, 2, 128, 128, 1.0,
+                              la.LA_L2NORM_K | la.LA_GATE_SCALAR, FAKE, None) == la.LA_ERR_INVALID_ARG

@@ -200,3 +200,39 @@ def test_decode_full_sampled(cuda_lib):
     got_st = st[pairs[0], pairs[1]][:, None].numpy()
     assert rel_err(got_o, ro) <= TOL[torch.bfloat16]
     assert rel_err(got_st, rst) <= TOL[torch.bfloat16]
+
+
+# ------------------------------------------------- scalar gate (one decay per token and head)
+
+@pytest.mark.parametrize("dtype,dk,dv", [(torch.float32, 64, 64), (torch.float32, 64, 128),
+                                         (torch.float32, 128, 128), (torch.bfloat16, 64, 64),
+                                         (torch.bfloat16, 128, 128)])
+def test_delta_scalar_gate_ragged(cuda_lib, dtype, dk, dv):
+    """LA_GATE_SCALAR: fp32 I/O on the CUDA-core kernel, bf16 (dk == dv) on the
+    tensor-core kernels; ragged lengths, empty sequence, initial states."""
+    inp = wl.prefill_inputs(RAGGED, 2, dk, dv, dtype, True, seed=40 + dk + dv, init_state=True,
+                            scalar_gate=True)
+    o, fS = gpu_prefill_delta(cuda_lib, inp, flags=cuda_lib.LA_L2NORM_K | cuda_lib.LA_GATE_SCALAR)
+    ref_o, ref_S = oracle_prefill_delta(inp, flags=oracle.L2NORM_K | oracle.SCALAR_GATE)
+    assert rel_err(o.numpy(), ref_o) <= TOL[dtype]
+    assert rel_err(fS.numpy(), ref_S) <= TOL[dtype]
+
+
+def test_gpt2_shape_scalar_gate_full(cuda_lib):
+    """The GPT-2-shaped workload (8 x 2048 tokens, 12 heads of 64) with a
+    scalar gate per token and head, every head against the oracle."""
+    w = wl.workload("gpt2_prefill")
+    inp = wl.prefill_inputs(w.lengths, w.H, w.dk, w.dv, w.dtype, True, seed=1, scalar_gate=True)
+    o, fS = gpu_prefill_delta(cuda_lib, inp, flags=cuda_lib.LA_L2NORM_K | cuda_lib.LA_GATE_SCALAR)
+    ref_o, ref_S = oracle_prefill_delta(inp, flags=oracle.L2NORM_K | oracle.SCALAR_GATE)
+    assert rel_err(o.numpy(), ref_o) <= TOL[torch.bfloat16]
+    assert rel_err(fS.numpy(), ref_S) <= TOL[torch.bfloat16]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_decode_scalar_gate(cuda_lib, dtype):
+    inp = wl.decode_inputs(5, 3, 128, 128, 4, dtype, seed=41, scalar_gate=True)
+    o, st = run_decode(cuda_lib, inp, 4, flags=cuda_lib.LA_L2NORM_K | cuda_lib.LA_GATE_SCALAR)
+    ro, rst = oracle_decode(inp, 4, flags=oracle.L2NORM_K | oracle.SCALAR_GATE)
+    assert rel_err(o.numpy(), ro) <= TOL[dtype]
+    assert rel_err(st.numpy(), rst) <= TOL[dtype]

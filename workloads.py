@@ -66,6 +66,9 @@ def workload(name: str, seed: int = 0) -> Workload:
         return Workload(name, "prefill_delta", 1, 64, 64, torch.float32, lengths=(256,))
     if name == "gpt2_prefill":     # GPT-2-small-shaped: 12 heads of 64, 8 x 2048 tokens
         return Workload(name, "prefill_delta", 12, 64, 64, torch.bfloat16, lengths=(2048,) * 8)
+    if name == "gpt2_scalar_gate":  # the GPT-2 shape with one decay per token and head
+        return Workload(name, "prefill_delta", 12, 64, 64, torch.bfloat16, gated=True,
+                        lengths=(2048,) * 8, extra={"scalar_gate": True})
     if name == "gated_prefill":    # per-channel decay, 32 heads of 128, 4 x 8192 tokens
         return Workload(name, "prefill_delta", 32, 128, 128, torch.bfloat16, gated=True,
                         lengths=(8192,) * 4)
@@ -80,7 +83,7 @@ def workload(name: str, seed: int = 0) -> Workload:
 
 
 ALL_WORKLOADS = ("tiny_linear", "tiny_delta", "gpt2_prefill", "gated_prefill", "decode",
-                 "varlen_prefill")
+                 "varlen_prefill", "gpt2_scalar_gate")
 
 
 def cu_seqlens(lengths) -> torch.Tensor:
@@ -100,8 +103,10 @@ def _randn(g, shape, dtype, mean=0.0, std=1.0):
 
 
 def prefill_inputs(lengths, H, dk, dv, dtype, gated, seed=0, init_state=False,
-                   gate_mean=2.0):
-    """Raw prefill inputs on the CPU: q, k, v, beta/gate logits, optional state."""
+                   gate_mean=2.0, scalar_gate=False):
+    """Raw prefill inputs on the CPU: q, k, v, beta/gate logits, optional state.
+    scalar_gate: one gate logit per token and head ([ntok][H]) instead of one
+    per key channel."""
     g = torch.Generator().manual_seed(seed)
     ntok = int(sum(lengths))
     out = {
@@ -109,7 +114,8 @@ def prefill_inputs(lengths, H, dk, dv, dtype, gated, seed=0, init_state=False,
         "k": _randn(g, (ntok, H, dk), dtype),
         "v": _randn(g, (ntok, H, dv), dtype),
         "beta_logits": _randn(g, (ntok, H), dtype),
-        "gate_logits": _randn(g, (ntok, H, dk), dtype, mean=gate_mean) if gated else None,
+        "gate_logits": (_randn(g, (ntok, H) if scalar_gate else (ntok, H, dk), dtype,
+                               mean=gate_mean) if gated else None),
         "cu_seqlens": cu_seqlens(lengths),
     }
     out["init_S"] = (_randn(g, (len(lengths), H, dk, dv), torch.float32, std=0.02)
@@ -117,15 +123,18 @@ def prefill_inputs(lengths, H, dk, dv, dtype, gated, seed=0, init_state=False,
     return out
 
 
-def decode_inputs(n_seq, H, dk, dv, steps, dtype, seed=0, gated=True, gate_mean=2.0):
-    """Raw decode inputs: ``steps`` tokens per sequence and the pre-filled state."""
+def decode_inputs(n_seq, H, dk, dv, steps, dtype, seed=0, gated=True, gate_mean=2.0,
+                  scalar_gate=False):
+    """Raw decode inputs: ``steps`` tokens per sequence and the pre-filled state
+    (scalar_gate: gate logits [steps][n_seq][H])."""
     g = torch.Generator().manual_seed(seed)
     return {
         "q": _randn(g, (steps, n_seq, H, dk), dtype),
         "k": _randn(g, (steps, n_seq, H, dk), dtype),
         "v": _randn(g, (steps, n_seq, H, dv), dtype),
         "beta_logits": _randn(g, (steps, n_seq, H), dtype),
-        "gate_logits": _randn(g, (steps, n_seq, H, dk), dtype, mean=gate_mean) if gated else None,
+        "gate_logits": (_randn(g, (steps, n_seq, H) if scalar_gate else (steps, n_seq, H, dk),
+                               dtype, mean=gate_mean) if gated else None),
         "state": _randn(g, (n_seq, H, dk, dv), torch.float32, std=0.02),
     }
 
@@ -134,4 +143,4 @@ def inputs_for(w: Workload, seed=0, init_state=False):
     if w.kind == "decode":
         return decode_inputs(w.n_seq, w.H, w.dk, w.dv, w.steps, w.dtype, seed, gated=w.gated)
     return prefill_inputs(w.lengths, w.H, w.dk, w.dv, w.dtype, w.gated, seed,
-                          init_state=init_state)
+                          init_state=init_state, scalar_gate=w.extra.get("scalar_gate", False))
