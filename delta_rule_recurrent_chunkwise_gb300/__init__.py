@@ -24,8 +24,8 @@ LA_F32, LA_BF16 = 0, 1
 LA_L2NORM_K, LA_L2NORM_Q, LA_SILU_QK, LA_GATE_SCALAR = 1, 2, 4, 8
 
 EXPORTED = ("la_prefill_linear", "la_prefill_delta", "la_prefill_delta_workspace_size",
-            "la_prefill_delta_static", "la_decode_step", "la_check_device",
-            "la_status_string")
+            "la_prefill_delta_static", "la_decode_step", "la_decode_step_slots",
+            "la_check_device", "la_status_string")
 
 
 class LinAttnError(RuntimeError):
@@ -56,11 +56,13 @@ def library():
         lib.la_prefill_delta_workspace_size.argtypes = [ip, ip, ip, ip, ip, ip, ip]
         lib.la_prefill_delta_workspace_size.restype = sz
         lib.la_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, ip, ip, ip, ip, ip, fp, u, vp, vp]
+        lib.la_decode_step_slots.argtypes = [vp, vp, vp, vp, vp, vp, ip, ip, ip, ip, ip, fp, u,
+                                             vp, ip, vp, vp]
         lib.la_check_device.argtypes = [vp]
         lib.la_status_string.argtypes = [ip]
         lib.la_status_string.restype = ctypes.c_char_p
         for f in ("la_prefill_linear", "la_prefill_delta", "la_prefill_delta_static",
-                  "la_decode_step", "la_check_device"):
+                  "la_decode_step", "la_decode_step_slots", "la_check_device"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -208,6 +210,31 @@ def la_decode_step(q, k, v, beta_logits, gate_logits, o, state, scale=1.0, flags
                                   _ptr(state), _stream(stream))
     if rc != LA_OK:
         raise LinAttnError(rc, "la_decode_step")
+    return o
+
+
+def la_decode_step_slots(q, k, v, beta_logits, gate_logits, o, state_pool, state_indices,
+                         scale=1.0, flags=LA_L2NORM_K, stream=None):
+    """One decode step over a state pool: sequence n updates
+    state_pool[state_indices[n]] in place (a negative index skips sequence
+    n).  q,k [N,H,dk]; v,o [N,H,dv]; beta_logits [N,H]; gate_logits
+    [N,H,dk] or None; state_pool [P,H,dk,dv] fp32; state_indices [N] int32."""
+    import torch
+    _check(dict(q=q, k=k, v=v, o=o, beta_logits=beta_logits, gate_logits=gate_logits),
+           dtype=q.dtype, device=q.device)
+    _check(dict(state_pool=state_pool), dtype=torch.float32, device=q.device)
+    _check(dict(state_indices=state_indices), dtype=torch.int32, device=q.device)
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    if state_indices.shape != (N,) or state_pool.shape[1:] != (H, dk, dv):
+        raise ValueError("state_indices must be [N] and state_pool [P, H, dk, dv]")
+    rc = library().la_decode_step_slots(_ptr(q), _ptr(k), _ptr(v), _ptr(beta_logits),
+                                        _ptr(gate_logits), _ptr(o), _io(q), N, H, dk, dv,
+                                        float(scale), int(flags), _ptr(state_pool),
+                                        int(state_pool.shape[0]), _ptr(state_indices),
+                                        _stream(stream))
+    if rc != LA_OK:
+        raise LinAttnError(rc, "la_decode_step_slots")
     return o
 
 

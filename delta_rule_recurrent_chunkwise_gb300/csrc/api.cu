@@ -41,6 +41,19 @@ la_status check_delta_args(const void *q, const void *k, const void *v, const vo
     return check_cu_host(cu_seqlens_host, N, ntok);
 }
 
+la_status check_decode_args(const void *q, const void *k, const void *v, const void *beta_logits,
+                            const void *gate_logits, const void *o, la_dtype io, int N, int H,
+                            int dk, int dv, float scale, unsigned flags, const float *state) {
+    if (!q || !k || !v || !beta_logits || !o || !state || N < 1 || H < 1 || !dtype_ok(io))
+        return LA_ERR_INVALID_ARG;
+    if (dk < 1 || dv < 1 || !std::isfinite(scale)) return LA_ERR_INVALID_ARG;
+    if (flags & ~(LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK | LA_GATE_SCALAR)) return LA_ERR_INVALID_ARG;
+    if ((flags & LA_GATE_SCALAR) && !gate_logits) return LA_ERR_INVALID_ARG;
+    if (!head_size_ok(dk) || !head_size_ok(dv)) return LA_ERR_UNSUPPORTED;
+    if ((int64_t)N * H * 2 > 0x7fffffffLL) return LA_ERR_UNSUPPORTED;
+    return LA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -121,15 +134,26 @@ la_status la_prefill_delta_static(const void *q, const void *k, const void *v,
 la_status la_decode_step(const void *q, const void *k, const void *v, const void *beta_logits,
                          const void *gate_logits, void *o, la_dtype io, int N, int H, int dk,
                          int dv, float scale, unsigned flags, float *state, void *stream) {
-    if (!q || !k || !v || !beta_logits || !o || !state || N < 1 || H < 1 || !dtype_ok(io))
-        return LA_ERR_INVALID_ARG;
-    if (dk < 1 || dv < 1 || !std::isfinite(scale)) return LA_ERR_INVALID_ARG;
-    if (flags & ~(LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK | LA_GATE_SCALAR)) return LA_ERR_INVALID_ARG;
-    if ((flags & LA_GATE_SCALAR) && !gate_logits) return LA_ERR_INVALID_ARG;
-    if (!head_size_ok(dk) || !head_size_ok(dv)) return LA_ERR_UNSUPPORTED;
-    if ((int64_t)N * H * 2 > 0x7fffffffLL) return LA_ERR_UNSUPPORTED;
+    if (la_status st = check_decode_args(q, k, v, beta_logits, gate_logits, o, io, N, H, dk, dv,
+                                         scale, flags, state))
+        return st;
     la::DecodeArgs a{q, k, v, beta_logits, gate_logits, o, N, H, dk, dv, scale, flags, state,
                      io == LA_BF16};
+    return from_cuda(la::launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+la_status la_decode_step_slots(const void *q, const void *k, const void *v,
+                               const void *beta_logits, const void *gate_logits, void *o,
+                               la_dtype io, int N, int H, int dk, int dv, float scale,
+                               unsigned flags, float *state_pool, int n_slots,
+                               const int32_t *state_indices, void *stream) {
+    if (la_status st = check_decode_args(q, k, v, beta_logits, gate_logits, o, io, N, H, dk, dv,
+                                         scale, flags, state_pool))
+        return st;
+    if (!state_indices || n_slots < 1) return LA_ERR_INVALID_ARG;
+    la::DecodeArgs a{q, k, v, beta_logits, gate_logits, o, N, H, dk, dv, scale, flags,
+                     state_pool, io == LA_BF16, state_indices, n_slots, la::device_error_word()};
+    if (!a.err) return LA_ERR_CUDA;
     return from_cuda(la::launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -139,7 +163,7 @@ la_status la_check_device(void *stream) {
     if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
     unsigned code = 0;
     if (la::tc_take_error(s, &code) != cudaSuccess) return LA_ERR_CUDA;
-    if (code == 100u) return LA_ERR_INVALID_ARG;  // cu_seqlens outside [0, ntok]
+    if (code == 100u) return LA_ERR_INVALID_ARG;  // cu_seqlens or a state slot out of range
     if (code != 0u) return LA_ERR_TIMEOUT;
     return LA_OK;
 }

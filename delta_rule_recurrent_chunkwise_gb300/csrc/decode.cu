@@ -18,6 +18,11 @@
 // prologue runs so that each thread's whole share is in flight at once.
 // With 32 KB per CTA and ~60 registers per thread, four CTAs share an SM,
 // so one CTA's write phase overlaps the others' reads.
+//
+// Slot map (optional): with `slots` set, sequence n's state is entry
+// slots[n] of a pool of n_slots states [n_slots][H][dk][dv]; a negative
+// entry marks a padding sequence (no state or output is touched), an entry
+// >= n_slots records code 100 in the error word and touches nothing.
 
 #include "common.cuh"
 #include "launch.h"
@@ -29,6 +34,9 @@ struct DecodeParams {
     const void *q, *k, *v, *beta_logits, *gate_logits;
     void *o;
     float *state;
+    const int32_t *slots;  // nullable: state of sequence n is slot n
+    int64_t n_slots;
+    unsigned *err;
     int H;
     float scale;
     unsigned flags;
@@ -55,7 +63,17 @@ __global__ void __launch_bounds__(256, 4) decode_step_kernel(DecodeParams p) {
     const int64_t nh = blockIdx.x / kSplit;
     const int j0 = (blockIdx.x % kSplit) * DVS;   // first column of the slice
     const int col4 = tid % C4, row0 = tid / C4;
-    float4 *S4 = reinterpret_cast<float4 *>(p.state + nh * (int64_t)(DK * DV) + j0);
+    int64_t sh = nh;                               // (state slot, head) of this CTA
+    if (p.slots) {
+        const int64_t n = nh / p.H, slot = p.slots[n];
+        if (slot < 0) return;                      // padding sequence
+        if (slot >= p.n_slots) {
+            if (tid == 0) atomicCAS(p.err, 0u, 100u);
+            return;
+        }
+        sh = slot * p.H + (nh - n * p.H);
+    }
+    float4 *S4 = reinterpret_cast<float4 *>(p.state + sh * (int64_t)(DK * DV) + j0);
 
     // 1. put this thread's share of the state in flight (streaming loads).
     float4 s[RPT];
@@ -136,7 +154,7 @@ __global__ void __launch_bounds__(256, 4) decode_step_kernel(DecodeParams p) {
 template <typename IO, int DK, int DV>
 cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
     DecodeParams p{a.q, a.k, a.v, a.beta_logits, a.gate_logits, a.o, a.state,
-                   a.H, a.scale, a.flags};
+                   a.slots, a.n_slots, a.err, a.H, a.scale, a.flags};
     const unsigned grid = (unsigned)((int64_t)a.N * a.H * kSplit);
     decode_step_kernel<IO, DK, DV><<<grid, 256, 0, s>>>(p);
     return cudaGetLastError();

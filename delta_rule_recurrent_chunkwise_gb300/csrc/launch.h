@@ -30,6 +30,9 @@ struct DecodeArgs {
     unsigned flags;
     float *state;
     bool bf16;
+    const int32_t *slots = nullptr;  // optional slot map into a state pool
+    int64_t n_slots = 0;
+    unsigned *err = nullptr;         // device error word (slot map only)
 };
 
 // fp32 SIMT chunk kernels (any I/O dtype).

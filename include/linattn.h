@@ -164,9 +164,29 @@ la_status la_decode_step(const void *q, const void *k, const void *v, const void
                          const void *gate_logits, void *o, la_dtype io, int N, int H, int dk,
                          int dv, float scale, unsigned flags, float *state, void *stream);
 
+/* la_decode_step over a pool of states addressed through a slot map, for
+ * servers that keep the recurrent states of many requests in one
+ * persistent buffer and step an arbitrary subset of them.  The page has no
+ * counterpart (its forward(x, cache) takes each sequence's cache on its
+ * own); the arithmetic per sequence is exactly that of la_decode_step.
+ * state_pool [n_slots][H][dk][dv] fp32; state_indices: device int32 [N],
+ * sequence n reads and rewrites state_pool[state_indices[n]] in place.
+ * A negative index marks a padding sequence: its state and its output rows
+ * are left untouched.  Non-negative indices must be distinct (two
+ * sequences on one slot race; not checked).  An index >= n_slots touches
+ * nothing for that sequence and makes the next la_check_device return
+ * LA_ERR_INVALID_ARG.  Other arguments and errors as la_decode_step, plus
+ * LA_ERR_INVALID_ARG for a NULL state_indices or n_slots < 1. */
+la_status la_decode_step_slots(const void *q, const void *k, const void *v,
+                               const void *beta_logits, const void *gate_logits, void *o,
+                               la_dtype io, int N, int H, int dk, int dv, float scale,
+                               unsigned flags, float *state_pool, int n_slots,
+                               const int32_t *state_indices, void *stream);
+
 /* Synchronises `stream`, then reports (and clears) any error raised on the
  * current device since the previous check: LA_ERR_TIMEOUT if a bounded
- * in-kernel wait gave up, LA_ERR_CUDA for a CUDA error, else LA_OK. */
+ * in-kernel wait gave up, LA_ERR_INVALID_ARG if a kernel found cu_seqlens
+ * or a state slot out of range, LA_ERR_CUDA for a CUDA error, else LA_OK. */
 la_status la_check_device(void *stream);
 
 /* Static, human-readable name of a status code. */

@@ -159,3 +159,17 @@ def test_scalar_gate_flag_needs_gate_logits(lib):
     assert lib.la_prefill_delta_static(*args, None) == la.LA_ERR_INVALID_ARG
     assert lib.la_decode_step(FAKE, FAKE, FAKE, FAKE, None, FAKE, la.LA_BF16, 4, 2, 128, 128, 1.0,
                               la.LA_L2NORM_K | la.LA_GATE_SCALAR, FAKE, None) == la.LA_ERR_INVALID_ARG
+
+
+def test_decode_slots_rejects_bad_arguments(lib):
+    """The slot-map decode checks its own arguments (and la_decode_step's) on
+    the host before touching the GPU."""
+    d = lib.la_decode_step_slots
+    base = (FAKE, FAKE, FAKE, FAKE, None, FAKE, la.LA_BF16, 4, 2, 128, 128, 1.0, 1)
+    assert d(*base, FAKE, 8, None, None) == la.LA_ERR_INVALID_ARG       # no slot map
+    assert d(*base, FAKE, 0, FAKE, None) == la.LA_ERR_INVALID_ARG       # empty pool
+    assert d(*base, None, 8, FAKE, None) == la.LA_ERR_INVALID_ARG       # no pool
+    assert d(FAKE, FAKE, FAKE, FAKE, None, FAKE, la.LA_BF16, 4, 2, 96, 128, 1.0, 1, FAKE, 8,
+             FAKE, None) == la.LA_ERR_UNSUPPORTED
+    assert d(FAKE, FAKE, FAKE, FAKE, None, FAKE, la.LA_BF16, 4, 2, 128, 128, 1.0,
+             la.LA_GATE_SCALAR, FAKE, 8, FAKE, None) == la.LA_ERR_INVALID_ARG
