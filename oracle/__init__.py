@@ -20,6 +20,12 @@ Parity status of each function (what pins it, see ``tests/test_oracle_pins.py``)
   decay; closed forms for one token and for beta = 0; alpha = 0 restarts.
 * ``decode``  -- pinned: equals ``delta`` one token at a time, and a single
   step equals its closed form.
+* ``delta_backward`` -- pinned: central finite differences of ``delta``'s
+  outputs (element by element on tiny inputs, along random directions on
+  larger ones, with and without gate, scalar gate, silu / q-norm flags and
+  an initial state); beta = 0 leaves v without gradient; with alpha = 1 and
+  orthonormal keys written once, d v_i of a read-back is exactly the output
+  gradient.
 """
 from __future__ import annotations
 
@@ -70,7 +76,11 @@ class OracleLib:
                                         c_double, c_uint, dp, dp, c_int]
         lib.la_oracle_decode.argtypes = [dp, dp, dp, dp, dp, dp, c_int, c_int, c_int, c_int,
                                          c_double, c_uint, dp, c_int]
-        for f in (lib.la_oracle_linear, lib.la_oracle_delta, lib.la_oracle_decode):
+        lib.la_oracle_delta_backward.argtypes = [dp, dp, dp, dp, dp, ip, c_int, c_int, c_int,
+                                                 c_int, c_double, c_uint, dp, dp, dp, dp, dp,
+                                                 dp, dp, dp, dp, c_int]
+        for f in (lib.la_oracle_linear, lib.la_oracle_delta, lib.la_oracle_decode,
+                  lib.la_oracle_delta_backward):
             f.restype = c_int
         self.lib = lib
         self.L2NORM_K, self.L2NORM_Q, self.SILU_QK = L2NORM_K, L2NORM_Q, SILU_QK
@@ -81,6 +91,9 @@ class OracleLib:
 
     def delta(self, *a, **k):
         return _delta(self.lib, *a, **k)
+
+    def delta_backward(self, *a, **k):
+        return _delta_backward(self.lib, *a, **k)
 
     def decode(self, *a, **k):
         return _decode(self.lib, *a, **k)
@@ -147,6 +160,13 @@ def delta(q, k, v, beta_logits, gate_logits, cu_seqlens, scale=1.0, flags=L2NORM
     """(Gated) delta rule (see _delta)."""
     return _delta(_load(), q, k, v, beta_logits, gate_logits, cu_seqlens, scale, flags, init_S,
                   nthreads)
+
+
+def delta_backward(q, k, v, beta_logits, gate_logits, cu_seqlens, d_o, d_final_S=None,
+                   scale=1.0, flags=L2NORM_K, init_S=None, nthreads=None):
+    """Gradients of the (gated) delta rule (see _delta_backward)."""
+    return _delta_backward(_load(), q, k, v, beta_logits, gate_logits, cu_seqlens, d_o,
+                           d_final_S, scale, flags, init_S, nthreads)
 
 
 def decode(q, k, v, beta_logits, gate_logits, state, scale=1.0, flags=L2NORM_K, nthreads=None):
@@ -217,3 +237,30 @@ def _decode(lib, q, k, v, beta_logits, gate_logits, state, scale=1.0, flags=L2NO
     if rc != 0:
         raise ValueError("la_oracle_decode rejected its arguments")
     return o, st
+
+
+def _delta_backward(lib, q, k, v, beta_logits, gate_logits, cu_seqlens, d_o, d_final_S=None,
+                    scale=1.0, flags=L2NORM_K, init_S=None, nthreads=None):
+    """Gradients of ``_delta``'s outputs with respect to all its inputs,
+    given the output gradient d_o [ntok,H,dv] and optionally the final-state
+    gradient d_final_S [N,H,dk,dv].  Returns a dict of fp64 arrays: dq, dk,
+    dv, d_beta_logits, d_gate_logits (None without gate), d_init_S.
+    Rows of tokens outside every sequence stay zero."""
+    q, k, v, bl, gl = _f64(q), _f64(k), _f64(v), _f64(beta_logits), _f64(gate_logits)
+    do, dfS, iS = _f64(d_o), _f64(d_final_S), _f64(init_S)
+    cu, cup = _cu(cu_seqlens)
+    ntok, H, dk = q.shape
+    dv = v.shape[2]
+    N = len(cu) - 1
+    out = {"dq": np.zeros_like(q), "dk": np.zeros_like(k), "dv": np.zeros_like(v),
+           "d_beta_logits": np.zeros_like(bl),
+           "d_gate_logits": None if gl is None else np.zeros_like(gl),
+           "d_init_S": np.zeros((N, H, dk, dv))}
+    rc = lib.la_oracle_delta_backward(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(bl), _ptr(gl), cup, N, H, dk, dv, float(scale),
+        int(flags), _ptr(iS), _ptr(do), _ptr(dfS), _ptr(out["dq"]), _ptr(out["dk"]),
+        _ptr(out["dv"]), _ptr(out["d_beta_logits"]), _ptr(out["d_gate_logits"]),
+        _ptr(out["d_init_S"]), nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("la_oracle_delta_backward rejected its arguments")
+    return out

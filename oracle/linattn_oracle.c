@@ -290,3 +290,216 @@ int la_oracle_decode(const double *q, const double *k, const double *v,
     free(cu);
     return rc;
 }
+
+/* ------------------------------------------- delta rule: reverse mode */
+
+/* Derivative of prep_qk: given x (raw), y = prep(x) and dy, writes dx.
+ * L2 step y = s / max(||s||, 1e-12): ds = (dy - y (y.dy)) / ||s|| while the
+ * norm is above the floor, dy / 1e-12 below it (the floor is a constant).
+ * silu step s = x sigmoid(x): ds/dx = sigmoid(x) (1 + x (1 - sigmoid(x))). */
+static void prep_qk_backward(const double *x, const double *y, const double *dy, double *dx,
+                             int n, int do_silu, int do_norm) {
+    double *ds = (double *)malloc(sizeof(double) * (size_t)n);
+    if (do_norm) {
+        double ss = 0.0, ydy = 0.0;
+        for (int i = 0; i < n; ++i) {
+            const double s = do_silu ? x[i] * sigmoid(x[i]) : x[i];
+            ss += s * s;
+            ydy += y[i] * dy[i];
+        }
+        const double nrm = sqrt(ss);
+        for (int i = 0; i < n; ++i)
+            ds[i] = nrm > 1e-12 ? (dy[i] - y[i] * ydy) / nrm : dy[i] / 1e-12;
+    } else {
+        for (int i = 0; i < n; ++i) ds[i] = dy[i];
+    }
+    for (int i = 0; i < n; ++i) {
+        if (do_silu) {
+            const double sg = sigmoid(x[i]);
+            dx[i] = ds[i] * sg * (1.0 + x[i] * (1.0 - sg));
+        } else {
+            dx[i] = ds[i];
+        }
+    }
+    free(ds);
+}
+
+typedef struct {
+    const double *q, *k, *v, *beta_logits, *gate_logits;
+    const int64_t *cu;
+    int H, dk, dv;
+    double scale;
+    unsigned flags;
+    const double *init_S, *d_o, *d_final_S;
+    double *dq, *dk_out, *dv_out, *d_beta_logits, *d_gate_logits, *d_init_S;
+} delta_bwd_ctx;
+
+/* Gradients of the gated delta rule of delta_pair, one (sequence, head), by
+ * reverse-mode differentiation of its token loop.  The page gives only the
+ * forward pass (section DeltaNet (Parallelizing Linear Transformers with
+ * Delta Rule) motivates the chunked form by training); the backward pass
+ * here is the chain rule applied to each statement of delta_pair in reverse
+ * order, with every intermediate state kept from a first forward sweep:
+ *   o_t = scale S_t^T q_t      -> dq_t = scale S_t do_t,  dS_t += scale q_t do_t^T
+ *   S_t = S' + k_t u_t^T       -> dk_t += dS_t u_t,  du_t = dS_t^T k_t,  dS' = dS_t
+ *   u_t = beta (v_t - S'^T k)  -> dbeta = du.(v_t - S'^T k),  dv_t = beta du,
+ *                                 dS' -= beta k du^T,  dk_t -= beta S' du
+ *   S' = Diag(alpha) S_{t-1}   -> dalpha_i = sum_j dS'_ij S_{t-1,ij},
+ *                                 dS_{t-1} = Diag(alpha) dS'
+ * then through the prologue: beta = sigmoid(b) gives db = dbeta beta (1-beta);
+ * log alpha = -softplus(g) gives dg = -dalpha alpha sigmoid(g) (summed over
+ * the key channels for a scalar gate); q, k through prep_qk_backward.
+ * d_o is the gradient of the outputs, d_final_S (optional) that of the
+ * final state; d_init_S receives the gradient of the initial state. */
+static void delta_backward_pair(void *vctx, int64_t pair) {
+    const delta_bwd_ctx *c = (const delta_bwd_ctx *)vctx;
+    const int H = c->H, dk = c->dk, dv = c->dv;
+    const int64_t n = pair / H, h = pair % H;
+    const int64_t t0 = c->cu[n], L = c->cu[n + 1] - c->cu[n];
+    const size_t DD = (size_t)dk * dv;
+    const int silu = (c->flags & ORACLE_SILU_QK) != 0;
+    const int norm_q = (c->flags & ORACLE_L2NORM_Q) != 0, norm_k = (c->flags & ORACLE_L2NORM_K) != 0;
+    const int scalar_gate = (c->flags & ORACLE_SCALAR_GATE) != 0;
+    const int64_t sbase = (n * H + h) * (int64_t)DD;
+
+    /* forward sweep, keeping the state before each token (index t) and after
+     * the last one (index L) */
+    double *Sh = (double *)calloc((size_t)(L + 1) * DD, sizeof(double));
+    double *qh = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * dk);
+    double *kh = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * dk);
+    double *ah = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * dk);
+    double *uh = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * dv);
+    double *bh = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+    if (c->init_S) memcpy(Sh, c->init_S + sbase, sizeof(double) * DD);
+    for (int64_t s = 0; s < L; ++s) {
+        const int64_t t = t0 + s;
+        double *qq = qh + s * dk, *kk = kh + s * dk, *al = ah + s * dk, *u = uh + s * dv;
+        prep_qk(c->q + (t * H + h) * dk, qq, dk, silu, norm_q);
+        prep_qk(c->k + (t * H + h) * dk, kk, dk, silu, norm_k);
+        bh[s] = sigmoid(c->beta_logits[t * H + h]);
+        for (int i = 0; i < dk; ++i)
+            al[i] = !c->gate_logits ? 1.0
+                    : exp(-softplus(scalar_gate ? c->gate_logits[t * H + h]
+                                                : c->gate_logits[(t * H + h) * dk + i]));
+        const double *Sp = Sh + s * DD;
+        double *Sn = Sh + (s + 1) * DD;
+        for (int i = 0; i < dk; ++i)
+            for (int j = 0; j < dv; ++j) Sn[i * dv + j] = al[i] * Sp[i * dv + j];
+        const double *vt = c->v + (t * H + h) * dv;
+        for (int j = 0; j < dv; ++j) {
+            double old = 0.0;
+            for (int i = 0; i < dk; ++i) old += kk[i] * Sn[i * dv + j];
+            u[j] = bh[s] * (vt[j] - old);
+        }
+        for (int i = 0; i < dk; ++i)
+            for (int j = 0; j < dv; ++j) Sn[i * dv + j] += kk[i] * u[j];
+    }
+
+    /* reverse sweep */
+    double *dS = (double *)calloc(DD, sizeof(double));
+    double *Sd = (double *)malloc(sizeof(double) * DD);   /* S' of the token */
+    double *dqh = (double *)malloc(sizeof(double) * (size_t)dk);
+    double *dkh = (double *)malloc(sizeof(double) * (size_t)dk);
+    double *da = (double *)malloc(sizeof(double) * (size_t)dk);
+    double *du = (double *)malloc(sizeof(double) * (size_t)dv);
+    if (c->d_final_S) memcpy(dS, c->d_final_S + sbase, sizeof(double) * DD);
+    for (int64_t s = L - 1; s >= 0; --s) {
+        const int64_t t = t0 + s;
+        const double *qq = qh + s * dk, *kk = kh + s * dk, *al = ah + s * dk, *u = uh + s * dv;
+        const double beta = bh[s];
+        const double *Sp = Sh + s * DD, *St = Sh + (s + 1) * DD;
+        const double *dot = c->d_o + (t * H + h) * dv;
+        const double *vt = c->v + (t * H + h) * dv;
+        for (int i = 0; i < dk; ++i)
+            for (int j = 0; j < dv; ++j) Sd[i * dv + j] = al[i] * Sp[i * dv + j];
+        /* o_t = scale S_t^T q_t */
+        for (int i = 0; i < dk; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < dv; ++j) acc += St[i * dv + j] * dot[j];
+            dqh[i] = c->scale * acc;
+        }
+        for (int i = 0; i < dk; ++i)
+            for (int j = 0; j < dv; ++j) dS[i * dv + j] += c->scale * qq[i] * dot[j];
+        /* S_t = S' + k u^T */
+        for (int i = 0; i < dk; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < dv; ++j) acc += dS[i * dv + j] * u[j];
+            dkh[i] = acc;
+        }
+        for (int j = 0; j < dv; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < dk; ++i) acc += dS[i * dv + j] * kk[i];
+            du[j] = acc;
+        }
+        /* u = beta (v - S'^T k); dS currently holds dS' */
+        double dbeta = 0.0;
+        for (int j = 0; j < dv; ++j) {
+            double old = 0.0;
+            for (int i = 0; i < dk; ++i) old += kk[i] * Sd[i * dv + j];
+            dbeta += du[j] * (vt[j] - old);
+            c->dv_out[(t * H + h) * dv + j] = beta * du[j];
+        }
+        for (int i = 0; i < dk; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < dv; ++j) acc += Sd[i * dv + j] * du[j];
+            dkh[i] -= beta * acc;
+        }
+        for (int i = 0; i < dk; ++i)
+            for (int j = 0; j < dv; ++j) dS[i * dv + j] -= beta * kk[i] * du[j];
+        /* S' = Diag(alpha) S_{t-1} */
+        for (int i = 0; i < dk; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < dv; ++j) acc += dS[i * dv + j] * Sp[i * dv + j];
+            da[i] = acc;
+            for (int j = 0; j < dv; ++j) dS[i * dv + j] *= al[i];
+        }
+        /* prologue */
+        c->d_beta_logits[t * H + h] = dbeta * beta * (1.0 - beta);
+        if (c->gate_logits) {
+            if (scalar_gate) {
+                const double g = c->gate_logits[t * H + h];
+                double acc = 0.0;
+                for (int i = 0; i < dk; ++i) acc += da[i];
+                c->d_gate_logits[t * H + h] = -acc * al[0] * sigmoid(g);
+            } else {
+                for (int i = 0; i < dk; ++i) {
+                    const double g = c->gate_logits[(t * H + h) * dk + i];
+                    c->d_gate_logits[(t * H + h) * dk + i] = -da[i] * al[i] * sigmoid(g);
+                }
+            }
+        }
+        prep_qk_backward(c->q + (t * H + h) * dk, qq, dqh, c->dq + (t * H + h) * dk, dk, silu,
+                         norm_q);
+        prep_qk_backward(c->k + (t * H + h) * dk, kk, dkh, c->dk_out + (t * H + h) * dk, dk, silu,
+                         norm_k);
+    }
+    if (c->d_init_S) memcpy(c->d_init_S + sbase, dS, sizeof(double) * DD);
+    free(Sh); free(qh); free(kh); free(ah); free(uh); free(bh);
+    free(dS); free(Sd); free(dqh); free(dkh); free(da); free(du);
+}
+
+/* Gradients of la_oracle_delta's outputs (o, and final_S when d_final_S is
+ * given) with respect to every input: see delta_backward_pair.  Layouts as
+ * la_oracle_delta; dq, dk like q, k; dv like v; d_beta_logits like
+ * beta_logits; d_gate_logits like gate_logits (ignored when there is no
+ * gate); d_init_S [N][H][dk][dv] (optional).  Rows of tokens outside every
+ * sequence are not written. */
+int la_oracle_delta_backward(const double *q, const double *k, const double *v,
+                             const double *beta_logits, const double *gate_logits,
+                             const int64_t *cu_seqlens, int N, int H, int dk, int dv,
+                             double scale, unsigned flags, const double *init_S,
+                             const double *d_o, const double *d_final_S, double *dq,
+                             double *dk_out, double *dv_out, double *d_beta_logits,
+                             double *d_gate_logits, double *d_init_S, int nthreads) {
+    if (!q || !k || !v || !beta_logits || !cu_seqlens || !d_o || !dq || !dk_out || !dv_out ||
+        !d_beta_logits || N < 1 || H < 1 || dk < 1 || dv < 1)
+        return 1;
+    if (gate_logits && !d_gate_logits) return 1;
+    for (int n = 0; n < N; ++n)
+        if (cu_seqlens[n + 1] < cu_seqlens[n]) return 1;
+    delta_bwd_ctx c = {q, k, v, beta_logits, gate_logits, cu_seqlens, H, dk, dv, scale, flags,
+                       init_S, d_o, d_final_S, dq, dk_out, dv_out, d_beta_logits, d_gate_logits,
+                       d_init_S};
+    for_each_pair((int64_t)N * H, nthreads, delta_backward_pair, &c);
+    return 0;
+}
