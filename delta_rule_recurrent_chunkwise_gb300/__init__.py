@@ -25,7 +25,8 @@ LA_L2NORM_K, LA_L2NORM_Q, LA_SILU_QK, LA_GATE_SCALAR = 1, 2, 4, 8
 
 EXPORTED = ("la_prefill_linear", "la_prefill_delta", "la_prefill_delta_workspace_size",
             "la_prefill_delta_static", "la_decode_step", "la_decode_step_slots",
-            "la_check_device", "la_status_string")
+            "la_backward_delta", "la_backward_delta_workspace_size", "la_check_device",
+            "la_status_string")
 
 
 class LinAttnError(RuntimeError):
@@ -58,11 +59,16 @@ def library():
         lib.la_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, ip, ip, ip, ip, ip, fp, u, vp, vp]
         lib.la_decode_step_slots.argtypes = [vp, vp, vp, vp, vp, vp, ip, ip, ip, ip, ip, fp, u,
                                              vp, ip, vp, vp]
+        lib.la_backward_delta.argtypes = [vp, vp, vp, vp, vp, vp, vp, ip, vp, vp, ip, ip, ip, ip,
+                                          ip, fp, u, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        lib.la_backward_delta_workspace_size.argtypes = [ip, ip, ip, ip, ip]
+        lib.la_backward_delta_workspace_size.restype = sz
         lib.la_check_device.argtypes = [vp]
         lib.la_status_string.argtypes = [ip]
         lib.la_status_string.restype = ctypes.c_char_p
         for f in ("la_prefill_linear", "la_prefill_delta", "la_prefill_delta_static",
-                  "la_decode_step", "la_decode_step_slots", "la_check_device"):
+                  "la_decode_step", "la_decode_step_slots", "la_backward_delta",
+                  "la_check_device"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -193,6 +199,48 @@ def la_prefill_delta_static(q, k, v, beta_logits, gate_logits, o, cu_seqlens, ch
     if rc != LA_OK:
         raise LinAttnError(rc, "la_prefill_delta_static")
     return o
+
+
+def la_backward_delta_workspace_size(N, ntok, H, dk, dv) -> int:
+    return int(library().la_backward_delta_workspace_size(N, ntok, H, dk, dv))
+
+
+def la_backward_delta(q, k, v, beta_logits, gate_logits, d_o, cu_seqlens, d_final_S=None,
+                      scale=1.0, flags=LA_L2NORM_K, init_S=None, want_d_init_S=True,
+                      workspace=None, cu_seqlens_host=None, stream=None):
+    """Gradients of la_prefill_delta given d_o [ntok,H,dv] (q's dtype) and
+    optionally d_final_S [N,H,dk,dv] fp32.  Returns a dict of fp32 tensors
+    dq, dk, dv, d_beta_logits, d_gate_logits (None without gate), d_init_S
+    (None unless want_d_init_S).  Rows of tokens outside every sequence are
+    zero here (the library leaves them untouched; they are allocated zeroed)."""
+    import torch
+    _check(dict(q=q, k=k, v=v, d_o=d_o, beta_logits=beta_logits, gate_logits=gate_logits),
+           dtype=q.dtype, device=q.device)
+    _check(dict(cu_seqlens=cu_seqlens), dtype=torch.int32, device=q.device)
+    _check(dict(init_S=init_S, d_final_S=d_final_S), dtype=torch.float32, device=q.device)
+    ntok, H, dk = q.shape
+    dv = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    hold, hptr = _host_cu(cu_seqlens_host)
+    f32 = dict(dtype=torch.float32, device=q.device)
+    out = {"dq": torch.zeros((ntok, H, dk), **f32), "dk": torch.zeros((ntok, H, dk), **f32),
+           "dv": torch.zeros((ntok, H, dv), **f32),
+           "d_beta_logits": torch.zeros((ntok, H), **f32),
+           "d_gate_logits": None if gate_logits is None else torch.zeros(gate_logits.shape, **f32),
+           "d_init_S": torch.empty((N, H, dk, dv), **f32) if want_d_init_S else None}
+    if workspace is None:
+        workspace = torch.empty(la_backward_delta_workspace_size(N, ntok, H, dk, dv),
+                                dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = library().la_backward_delta(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(beta_logits), _ptr(gate_logits), _ptr(d_o),
+        _ptr(d_final_S), _io(q), _ptr(cu_seqlens), hptr, N, ntok, H, dk, dv, float(scale),
+        int(flags), _ptr(init_S), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
+        _ptr(out["d_beta_logits"]), _ptr(out["d_gate_logits"]), _ptr(out["d_init_S"]),
+        _ptr(workspace), ws_bytes, _stream(stream))
+    if rc != LA_OK:
+        raise LinAttnError(rc, "la_backward_delta")
+    return out
 
 
 def la_decode_step(q, k, v, beta_logits, gate_logits, o, state, scale=1.0, flags=LA_L2NORM_K,

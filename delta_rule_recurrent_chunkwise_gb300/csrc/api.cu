@@ -157,6 +157,33 @@ la_status la_decode_step_slots(const void *q, const void *k, const void *v,
     return from_cuda(la::launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
 
+size_t la_backward_delta_workspace_size(int N, int ntok, int H, int dk, int dv) {
+    if (N < 1 || ntok < 0 || H < 1 || !head_size_ok(dk) || !head_size_ok(dv)) return 0;
+    return la::delta_bwd_workspace_bytes(N, ntok, H, dk, dv);
+}
+
+la_status la_backward_delta(const void *q, const void *k, const void *v, const void *beta_logits,
+                            const void *gate_logits, const void *d_o, const float *d_final_S,
+                            la_dtype io, const int32_t *cu_seqlens,
+                            const int32_t *cu_seqlens_host, int N, int ntok, int H, int dk,
+                            int dv, float scale, unsigned flags, const float *init_S, float *dq,
+                            float *dk_out, float *dv_out, float *d_beta_logits,
+                            float *d_gate_logits, float *d_init_S, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+    if (la_status st = check_delta_args(q, k, v, beta_logits, gate_logits, d_o, io, cu_seqlens,
+                                        cu_seqlens_host, N, ntok, H, dk, dv, 64, scale, flags))
+        return st;
+    if (!dq || !dk_out || !dv_out || !d_beta_logits || (gate_logits && !d_gate_logits))
+        return LA_ERR_INVALID_ARG;
+    const size_t need = la::delta_bwd_workspace_bytes(N, ntok, H, dk, dv);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return LA_ERR_INVALID_ARG;
+    la::BwdArgs a{q, k, v, beta_logits, gate_logits, d_o, d_final_S, init_S, cu_seqlens, N, ntok,
+                  H, dk, dv, scale, flags, dq, dk_out, dv_out, d_beta_logits, d_gate_logits,
+                  d_init_S, workspace, io == LA_BF16};
+    return from_cuda(la::launch_delta_backward(a, static_cast<cudaStream_t>(stream)));
+}
+
 la_status la_check_device(void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaStreamSynchronize(s) != cudaSuccess) return LA_ERR_CUDA;

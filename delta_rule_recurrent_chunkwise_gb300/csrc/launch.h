@@ -35,6 +35,21 @@ struct DecodeArgs {
     unsigned *err = nullptr;         // device error word (slot map only)
 };
 
+// Gradients of the delta rule (token-serial, column per warp, clusters).
+struct BwdArgs {
+    const void *q, *k, *v, *beta_logits, *gate_logits, *d_o;
+    const float *d_final_S, *init_S;
+    const int32_t *cu_seqlens;
+    int N, ntok, H, dk, dv;
+    float scale;
+    unsigned flags;
+    float *dq, *dk_out, *dv_out, *d_beta_logits, *d_gate_logits, *d_init_S;
+    void *workspace;
+    bool bf16;
+};
+size_t delta_bwd_workspace_bytes(int N, int ntok, int H, int dk, int dv);
+cudaError_t launch_delta_backward(const BwdArgs &a, cudaStream_t s);
+
 // fp32 SIMT chunk kernels (any I/O dtype).
 cudaError_t launch_linear_simt(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_delta_simt(const PrefillArgs &a, cudaStream_t s);

@@ -183,6 +183,35 @@ la_status la_decode_step_slots(const void *q, const void *k, const void *v,
                                unsigned flags, float *state_pool, int n_slots,
                                const int32_t *state_indices, void *stream);
 
+/* Gradients of la_prefill_delta (the page gives the forward pass only; its
+ * section DeltaNet (Parallelizing Linear Transformers with Delta Rule)
+ * motivates the chunked form by training).  Given the gradient d_o of the
+ * outputs o (and optionally d_final_S of the final states), returns the
+ * gradients of the loss with respect to every input of the forward call
+ * with the same q, k, v, beta_logits, gate_logits, cu_seqlens, scale, flags
+ * and init_S: the chain rule through each step of the token recurrence in
+ * reverse and through the prologue (sigmoid, -softplus, silu, L2 norm).
+ * Inputs as la_prefill_delta; d_o [ntok][H][dv] in the I/O dtype;
+ * d_final_S [N][H][dk][dv] fp32 or NULL (zero).  Outputs, all fp32, shaped
+ * like their inputs: dq, dk [ntok][H][dk]; dv [ntok][H][dv];
+ * d_beta_logits [ntok][H]; d_gate_logits like gate_logits (required iff
+ * gate_logits is given); d_init_S [N][H][dk][dv] or NULL.  Rows of tokens
+ * outside every sequence are not written.
+ * Workspace: la_backward_delta_workspace_size bytes, 256-byte aligned
+ * (chunk-start states, per-token column sums); LA_ERR_INVALID_ARG if
+ * smaller or missing.  dk, dv in {64, 128}.  The sums over value columns
+ * inside a thread block use shared-memory atomics, so the last bits of
+ * dq, dk, d_beta_logits and d_gate_logits may differ between runs. */
+size_t la_backward_delta_workspace_size(int N, int ntok, int H, int dk, int dv);
+la_status la_backward_delta(const void *q, const void *k, const void *v, const void *beta_logits,
+                            const void *gate_logits, const void *d_o, const float *d_final_S,
+                            la_dtype io, const int32_t *cu_seqlens,
+                            const int32_t *cu_seqlens_host, int N, int ntok, int H, int dk,
+                            int dv, float scale, unsigned flags, const float *init_S, float *dq,
+                            float *dk_out, float *dv_out, float *d_beta_logits,
+                            float *d_gate_logits, float *d_init_S, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
 /* Synchronises `stream`, then reports (and clears) any error raised on the
  * current device since the previous check: LA_ERR_TIMEOUT if a bounded
  * in-kernel wait gave up, LA_ERR_INVALID_ARG if a kernel found cu_seqlens

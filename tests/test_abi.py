@@ -173,3 +173,26 @@ def test_decode_slots_rejects_bad_arguments(lib):
              FAKE, None) == la.LA_ERR_UNSUPPORTED
     assert d(FAKE, FAKE, FAKE, FAKE, None, FAKE, la.LA_BF16, 4, 2, 128, 128, 1.0,
              la.LA_GATE_SCALAR, FAKE, 8, FAKE, None) == la.LA_ERR_INVALID_ARG
+
+
+def test_backward_checks_arguments_and_workspace(lib):
+    """la_backward_delta: the forward call's checks, its own outputs, and a
+    workspace of la_backward_delta_workspace_size bytes (chunk-start states
+    plus per-token sums), all before any launch."""
+    N, ntok, H, d = 2, 40, 4, 64
+    need = la.la_backward_delta_workspace_size(N, ntok, H, d, d)
+    slots = ntok // 64 + N + 1
+    assert need >= slots * H * d * d * 4 + ntok * H * 3 * d * 4 + ntok * H * 4
+    assert la.la_backward_delta_workspace_size(N, ntok, H, 96, d) == 0
+    b = lib.la_backward_delta
+    head = (FAKE, FAKE, FAKE, FAKE, None, FAKE, None, la.LA_BF16, FAKE, None, N, ntok, H, d, d,
+            1.0, la.LA_L2NORM_K, None)
+    outs = (FAKE, FAKE, FAKE, FAKE, None, None)
+    assert b(*head, *outs, None, need, None) == la.LA_ERR_INVALID_ARG          # no workspace
+    assert b(*head, *outs, FAKE, need - 1, None) == la.LA_ERR_INVALID_ARG      # too small
+    assert b(*head, None, *outs[1:], FAKE, need, None) == la.LA_ERR_INVALID_ARG  # no dq
+    gated = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, la.LA_BF16, FAKE, None, N, ntok, H, d, d,
+             1.0, la.LA_L2NORM_K, None)
+    assert b(*gated, *outs, FAKE, need, None) == la.LA_ERR_INVALID_ARG         # no d_gate_logits
+    odd = head[:13] + (96,) + head[14:]
+    assert b(*odd, *outs, FAKE, need, None) == la.LA_ERR_UNSUPPORTED
