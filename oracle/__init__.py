@@ -20,6 +20,10 @@ Parity status of each function (what pins it, see ``tests/test_oracle_pins.py``)
   decay; closed forms for one token and for beta = 0; alpha = 0 restarts.
 * ``decode``  -- pinned: equals ``delta`` one token at a time, and a single
   step equals its closed form.
+* ``delta`` with ``ADDITIVE`` (u = v, the decayed additive state) -- pinned:
+  brute-force decayed causal attention written from the products of the
+  decays, with an initial state and per-channel or scalar gates; no gate
+  gives tril(QK^T) V.
 * ``delta_backward`` -- pinned: central finite differences of ``delta``'s
   outputs (element by element on tiny inputs, along random directions on
   larger ones, with and without gate, scalar gate, silu / q-norm flags and
@@ -45,6 +49,7 @@ L2NORM_K = 1
 L2NORM_Q = 2
 SILU_QK = 4
 SCALAR_GATE = 8   # gate_logits [ntok][H]: one decay per token and head
+ADDITIVE = 16     # u = v: decayed additive state, no delta term and no beta
 
 def build(force: bool = False) -> str:
     """Compile the oracle shared library with gcc (no GPU needed)."""
@@ -253,7 +258,7 @@ def _delta_backward(lib, q, k, v, beta_logits, gate_logits, cu_seqlens, d_o, d_f
     dv = v.shape[2]
     N = len(cu) - 1
     out = {"dq": np.zeros_like(q), "dk": np.zeros_like(k), "dv": np.zeros_like(v),
-           "d_beta_logits": np.zeros_like(bl),
+           "d_beta_logits": np.zeros(q.shape[:2]),
            "d_gate_logits": None if gl is None else np.zeros_like(gl),
            "d_init_S": np.zeros((N, H, dk, dv))}
     rc = lib.la_oracle_delta_backward(

@@ -21,7 +21,7 @@
  * Packed layouts (tokens of all sequences back to back, as cu_seqlens says):
  *   q, k         [ntok][H][dk]
  *   v, o         [ntok][H][dv]
- *   beta_logits  [ntok][H]
+ *   beta_logits  [ntok][H]          (unused, may be NULL, with ORACLE_ADDITIVE)
  *   gate_logits  [ntok][H][dk]      (NULL: no decay, alpha = 1)
  *                [ntok][H]          with ORACLE_SCALAR_GATE (one decay per
  *                                   token and head, all key channels)
@@ -40,6 +40,7 @@
 #define ORACLE_L2NORM_Q 2u
 #define ORACLE_SILU_QK 4u
 #define ORACLE_SCALAR_GATE 8u
+#define ORACLE_ADDITIVE 16u
 
 /* ---------------------------------------------------------------- prologue */
 
@@ -210,7 +211,11 @@ typedef struct {
  * token and head; alpha_t = exp(-softplus(gate_logit)) per key channel.
  * With the decay first, the step equals the Householder form of the
  * chunkwise section, S_t = S_{t-1} Diag(alpha)(I - beta k k^T) + beta v k^T
- * in the column convention. */
+ * in the column convention.
+ * ORACLE_ADDITIVE turns the delta off: u_t = v_t (no read of the old value,
+ * no beta), the decayed additive state of section Gated DeltaNet
+ * (Mamba-2: cache = alpha * S_old + S_new, S_new = k @ v added at full
+ * strength). */
 static void delta_pair(void *vctx, int64_t pair) {
     const delta_ctx *c = (const delta_ctx *)vctx;
     const int H = c->H, dk = c->dk, dv = c->dv;
@@ -228,7 +233,8 @@ static void delta_pair(void *vctx, int64_t pair) {
         prep_qk(c->k + (t * H + h) * dk, kk, dk, silu, (c->flags & ORACLE_L2NORM_K) != 0);
         const double *vt = c->v + (t * H + h) * dv;
         double *ot = c->o + (t * H + h) * dv;
-        const double beta = sigmoid(c->beta_logits[t * H + h]);
+        const int additive = (c->flags & ORACLE_ADDITIVE) != 0;
+        const double beta = additive ? 1.0 : sigmoid(c->beta_logits[t * H + h]);
         /* one decay per key channel (section KDA / Kimi Linear), or one per
          * token and head for every channel (section Gated DeltaNet) */
         const int scalar_gate = (c->flags & ORACLE_SCALAR_GATE) != 0;
@@ -239,11 +245,13 @@ static void delta_pair(void *vctx, int64_t pair) {
         /* S' = Diag(alpha) S */
         for (int i = 0; i < dk; ++i)
             for (int j = 0; j < dv; ++j) S[i * dv + j] *= alpha[i];
-        /* u = beta (v - S'^T k) */
+        /* u = beta (v - S'^T k); the additive rule writes v at full strength
+         * with no read (section Gated DeltaNet: Mamba-2's
+         * cache = alpha * S_old + k @ v) */
         for (int j = 0; j < dv; ++j) {
             double old = 0.0;
             for (int i = 0; i < dk; ++i) old += kk[i] * S[i * dv + j];
-            u[j] = beta * (vt[j] - old);
+            u[j] = additive ? vt[j] : beta * (vt[j] - old);
         }
         /* S = S' + k u^T */
         for (int i = 0; i < dk; ++i)
@@ -263,8 +271,8 @@ int la_oracle_delta(const double *q, const double *k, const double *v,
                     const double *beta_logits, const double *gate_logits, double *o,
                     const int64_t *cu_seqlens, int N, int H, int dk, int dv, double scale,
                     unsigned flags, const double *init_S, double *final_S, int nthreads) {
-    if (!q || !k || !v || !beta_logits || !o || !cu_seqlens || N < 1 || H < 1 || dk < 1 || dv < 1)
-        return 1;
+    if (!q || !k || !v || !o || !cu_seqlens || N < 1 || H < 1 || dk < 1 || dv < 1) return 1;
+    if (!beta_logits && !(flags & ORACLE_ADDITIVE)) return 1;
     for (int n = 0; n < N; ++n)
         if (cu_seqlens[n + 1] < cu_seqlens[n]) return 1;
     delta_ctx c = {q, k, v, beta_logits, gate_logits, o, cu_seqlens, H, dk, dv,
@@ -360,6 +368,7 @@ static void delta_backward_pair(void *vctx, int64_t pair) {
     const int silu = (c->flags & ORACLE_SILU_QK) != 0;
     const int norm_q = (c->flags & ORACLE_L2NORM_Q) != 0, norm_k = (c->flags & ORACLE_L2NORM_K) != 0;
     const int scalar_gate = (c->flags & ORACLE_SCALAR_GATE) != 0;
+    const int additive = (c->flags & ORACLE_ADDITIVE) != 0;
     const int64_t sbase = (n * H + h) * (int64_t)DD;
 
     /* forward sweep, keeping the state before each token (index t) and after
@@ -376,7 +385,7 @@ static void delta_backward_pair(void *vctx, int64_t pair) {
         double *qq = qh + s * dk, *kk = kh + s * dk, *al = ah + s * dk, *u = uh + s * dv;
         prep_qk(c->q + (t * H + h) * dk, qq, dk, silu, norm_q);
         prep_qk(c->k + (t * H + h) * dk, kk, dk, silu, norm_k);
-        bh[s] = sigmoid(c->beta_logits[t * H + h]);
+        bh[s] = additive ? 1.0 : sigmoid(c->beta_logits[t * H + h]);
         for (int i = 0; i < dk; ++i)
             al[i] = !c->gate_logits ? 1.0
                     : exp(-softplus(scalar_gate ? c->gate_logits[t * H + h]
@@ -389,7 +398,7 @@ static void delta_backward_pair(void *vctx, int64_t pair) {
         for (int j = 0; j < dv; ++j) {
             double old = 0.0;
             for (int i = 0; i < dk; ++i) old += kk[i] * Sn[i * dv + j];
-            u[j] = bh[s] * (vt[j] - old);
+            u[j] = additive ? vt[j] : bh[s] * (vt[j] - old);
         }
         for (int i = 0; i < dk; ++i)
             for (int j = 0; j < dv; ++j) Sn[i * dv + j] += kk[i] * u[j];
@@ -431,7 +440,8 @@ static void delta_backward_pair(void *vctx, int64_t pair) {
             for (int i = 0; i < dk; ++i) acc += dS[i * dv + j] * kk[i];
             du[j] = acc;
         }
-        /* u = beta (v - S'^T k); dS currently holds dS' */
+        /* u = beta (v - S'^T k), or u = v for the additive rule; dS
+         * currently holds dS' */
         double dbeta = 0.0;
         for (int j = 0; j < dv; ++j) {
             double old = 0.0;
@@ -439,13 +449,15 @@ static void delta_backward_pair(void *vctx, int64_t pair) {
             dbeta += du[j] * (vt[j] - old);
             c->dv_out[(t * H + h) * dv + j] = beta * du[j];
         }
-        for (int i = 0; i < dk; ++i) {
-            double acc = 0.0;
-            for (int j = 0; j < dv; ++j) acc += Sd[i * dv + j] * du[j];
-            dkh[i] -= beta * acc;
+        if (!additive) {
+            for (int i = 0; i < dk; ++i) {
+                double acc = 0.0;
+                for (int j = 0; j < dv; ++j) acc += Sd[i * dv + j] * du[j];
+                dkh[i] -= beta * acc;
+            }
+            for (int i = 0; i < dk; ++i)
+                for (int j = 0; j < dv; ++j) dS[i * dv + j] -= beta * kk[i] * du[j];
         }
-        for (int i = 0; i < dk; ++i)
-            for (int j = 0; j < dv; ++j) dS[i * dv + j] -= beta * kk[i] * du[j];
         /* S' = Diag(alpha) S_{t-1} */
         for (int i = 0; i < dk; ++i) {
             double acc = 0.0;
@@ -453,8 +465,8 @@ static void delta_backward_pair(void *vctx, int64_t pair) {
             da[i] = acc;
             for (int j = 0; j < dv; ++j) dS[i * dv + j] *= al[i];
         }
-        /* prologue */
-        c->d_beta_logits[t * H + h] = dbeta * beta * (1.0 - beta);
+        /* prologue (the additive rule has no beta: its gradient is 0) */
+        c->d_beta_logits[t * H + h] = additive ? 0.0 : dbeta * beta * (1.0 - beta);
         if (c->gate_logits) {
             if (scalar_gate) {
                 const double g = c->gate_logits[t * H + h];
@@ -491,9 +503,10 @@ int la_oracle_delta_backward(const double *q, const double *k, const double *v,
                              const double *d_o, const double *d_final_S, double *dq,
                              double *dk_out, double *dv_out, double *d_beta_logits,
                              double *d_gate_logits, double *d_init_S, int nthreads) {
-    if (!q || !k || !v || !beta_logits || !cu_seqlens || !d_o || !dq || !dk_out || !dv_out ||
-        !d_beta_logits || N < 1 || H < 1 || dk < 1 || dv < 1)
+    if (!q || !k || !v || !cu_seqlens || !d_o || !dq || !dk_out || !dv_out || !d_beta_logits ||
+        N < 1 || H < 1 || dk < 1 || dv < 1)
         return 1;
+    if (!beta_logits && !(flags & ORACLE_ADDITIVE)) return 1;
     if (gate_logits && !d_gate_logits) return 1;
     for (int n = 0; n < N; ++n)
         if (cu_seqlens[n + 1] < cu_seqlens[n]) return 1;

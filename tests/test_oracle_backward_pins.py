@@ -62,9 +62,12 @@ def _fd_element(inp, cu, grads, flags, scale, name, idx):
     return (lp - lm) / (2 * H_FD)
 
 
-@pytest.mark.parametrize("gate,extra,scale", [("channel", 0, 1.0), ("none", 0, 0.7),
-                                              ("scalar", 0, 1.0),
-                                              ("channel", oracle.SILU_QK | oracle.L2NORM_Q, 1.3)])
+FD_CASES = [("channel", 0, 1.0), ("none", 0, 0.7), ("scalar", 0, 1.0),
+            ("channel", oracle.SILU_QK | oracle.L2NORM_Q, 1.3),
+            ("scalar", oracle.ADDITIVE, 1.0), ("channel", oracle.ADDITIVE, 0.8)]
+
+
+@pytest.mark.parametrize("gate,extra,scale", FD_CASES)
 def test_backward_equals_finite_differences_elementwise(gate, extra, scale):
     """Every element of every input of a tiny ragged batch (an empty sequence
     included): the gradient equals the central difference of the loss."""
@@ -158,13 +161,14 @@ BACKWARD_MUTATIONS = [
     ("beta gradient without the read", "dbeta += du[j] * (vt[j] - old);",
      "dbeta += du[j] * vt[j];"),
     ("final-state gradient ignored", "if (c->d_final_S) memcpy(dS", "if (0) memcpy(dS"),
+    ("additive rule keeps the read-path terms", "        if (!additive) {\n            for (int i = 0; i < dk; ++i) {\n                double acc = 0.0;",
+     "        if (1) {\n            for (int i = 0; i < dk; ++i) {\n                double acc = 0.0;"),
 ]
 
 
 def _backward_pins():
     calls = []
-    for gate, extra, scale in [("channel", 0, 1.0), ("none", 0, 0.7), ("scalar", 0, 1.0),
-                               ("channel", oracle.SILU_QK | oracle.L2NORM_Q, 1.3)]:
+    for gate, extra, scale in FD_CASES:
         calls.append(lambda a=(gate, extra, scale):
                      test_backward_equals_finite_differences_elementwise(*a))
     calls += [test_zero_beta_gives_no_value_gradient,

@@ -18,8 +18,8 @@ MUTATIONS = [
     ("decay after the write",
      "S[i * dv + j] *= alpha[i];", "S[i * dv + j] *= 1.0;", 1,
      "S[i * dv + j] += kk[i] * u[j];", "S[i * dv + j] = (S[i * dv + j] + kk[i] * u[j]) * alpha[i];"),
-    ("delta sign", "u[j] = beta * (vt[j] - old);", "u[j] = beta * (vt[j] + old);", 1),
-    ("beta dropped", "u[j] = beta * (vt[j] - old);", "u[j] = (vt[j] - old);", 1),
+    ("delta sign", ": beta * (vt[j] - old);", ": beta * (vt[j] + old);", 1),
+    ("beta dropped", ": beta * (vt[j] - old);", ": (vt[j] - old);", 1),
     ("read before the write", "acc += qq[i] * S[i * dv + j];",
      "acc += qq[i] * (S[i * dv + j] - kk[i] * u[j]);", 1),
     ("scale dropped", "ot[j] = c->scale * acc;", "ot[j] = acc;", 1),
@@ -41,6 +41,8 @@ MUTATIONS = [
      "scalar_gate ? c->gate_logits[t * H]", 1),
     ("scalar gate taken as no decay", "alpha[i] = !c->gate_logits ? 1.0",
      "alpha[i] = (!c->gate_logits || scalar_gate) ? 1.0", 1),
+    ("additive rule keeps the delta", "u[j] = additive ? vt[j] : beta * (vt[j] - old);",
+     "u[j] = beta * (vt[j] - old);", 1),
 ]
 
 
@@ -56,6 +58,8 @@ def pin_calls():
             calls += [(name, lambda f=fn, C=C: f(C)) for C in (16, 64)]
         elif name == "test_gated_oracle_matches_gated_chunk_form":
             calls += [(name, lambda f=fn, C=C: f(C)) for C in (8, 64)]
+        elif name == "test_additive_rule_equals_bruteforce_decayed_attention":
+            calls += [(name, lambda f=fn, g=g: f(g)) for g in ("channel", "scalar")]
         else:
             calls.append((name, fn))
     return calls

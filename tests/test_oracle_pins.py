@@ -435,3 +435,58 @@ def test_thread_count_does_not_change_results():
     o8, S8 = oracle.delta(*args, nthreads=8)
     np.testing.assert_array_equal(o1, o8)
     np.testing.assert_array_equal(S1, S8)
+
+
+# ------------------------------------- additive decayed state (Mamba-2 form)
+
+def _decayed_attention(q, k, v, log_a, S0):
+    """Brute force from the products of the decays, one (sequence, head):
+    o_t = sum_{i<=t} sum_c q_t[c] k_i[c] prod_{i<s<=t} alpha_s[c] v_i
+          + sum_c q_t[c] prod_{s<=t} alpha_s[c] S0[c, :]."""
+    T, dk = q.shape
+    o = np.zeros((T, v.shape[1]))
+    for t in range(T):
+        for i in range(t + 1):
+            dec = np.exp(log_a[i + 1:t + 1].sum(0))   # prod over s in (i, t]
+            o[t] += (q[t] * k[i] * dec).sum() * v[i]
+        o[t] += (q[t] * np.exp(log_a[:t + 1].sum(0))) @ S0
+    fS = np.exp(log_a.sum(0))[:, None] * S0
+    for i in range(T):
+        fS += np.outer(k[i] * np.exp(log_a[i + 1:].sum(0)), v[i])
+    return o, fS
+
+
+@pytest.mark.parametrize("gate", ["channel", "scalar"])
+def test_additive_rule_equals_bruteforce_decayed_attention(gate):
+    """ADDITIVE: the page's Mamba-2 update cache = alpha * S_old + k @ v
+    (section Gated DeltaNet): every value is written at full strength and
+    only decays afterwards."""
+    r = rng(31)
+    lengths, H, dk, dv = [9, 4], 2, 5, 3
+    ntok = sum(lengths)
+    q, k, v = r.standard_normal((ntok, H, dk)), r.standard_normal((ntok, H, dk)), \
+        r.standard_normal((ntok, H, dv))
+    g = r.standard_normal((ntok, H) if gate == "scalar" else (ntok, H, dk)) + 0.5
+    S0 = r.standard_normal((2, H, dk, dv))
+    flags = oracle.ADDITIVE | (oracle.SCALAR_GATE if gate == "scalar" else 0)
+    o, fS = oracle.delta(q, k, v, None, g, [0, 9, 13], scale=0.5, flags=flags, init_S=S0)
+    la = log_alpha_from_logits(g)
+    if gate == "scalar":
+        la = np.repeat(la[:, :, None], dk, axis=2)
+    for n, (a, b) in enumerate([(0, 9), (9, 13)]):
+        for h in range(H):
+            ro, rS = _decayed_attention(q[a:b, h], k[a:b, h], v[a:b, h], la[a:b, h], S0[n, h])
+            assert np.abs(o[a:b, h] - 0.5 * ro).max() < 1e-12
+            assert np.abs(fS[n, h] - rS).max() < 1e-12
+
+
+def test_additive_rule_without_gate_is_unnormalised_linear_attention():
+    """No decay: o = tril(Q K^T) V, the additive form the delta rule replaces."""
+    r = rng(32)
+    T, dk, dv = 11, 4, 6
+    q, k, v = r.standard_normal((T, 1, dk)), r.standard_normal((T, 1, dk)), \
+        r.standard_normal((T, 1, dv))
+    o, fS = oracle.delta(q, k, v, r.standard_normal((T, 1)), None, [0, T], flags=oracle.ADDITIVE)
+    want = np.tril(q[:, 0] @ k[:, 0].T) @ v[:, 0]
+    assert np.abs(o[:, 0] - want).max() < 1e-12
+    assert np.abs(fS[0, 0] - k[:, 0].T @ v[:, 0]).max() < 1e-12
