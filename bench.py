@@ -75,6 +75,16 @@ def prefill_algo(w: wl.Workload, chunk=64, final_states=False):
     return nbytes, flops
 
 
+def backward_algo_bytes(w: wl.Workload) -> int:
+    """Bytes a backward call must move: q, k, v, beta logits and the output
+    gradient read (I/O dtype), the fp32 gradients dq, dk, dv, d_beta written."""
+    e = 2 if w.dtype == torch.bfloat16 else 4
+    per = (e * (2 * w.dk + 2 * w.dv + 1) + 4 * (2 * w.dk + w.dv + 1))
+    if w.gated:
+        per += e * w.dk + 4 * w.dk
+    return w.ntok * w.H * per
+
+
 def decode_state_bytes(w: wl.Workload):
     return 8 * w.n_seq * w.H * w.dk * w.dv   # fp32 state read + written once per step
 
@@ -339,6 +349,32 @@ def run_ours(args, rank, world, dev, dist):
                 if name == "varlen_prefill":
                     extra[name]["lengths"] = list(gw.lengths)
                 del p
+            # ---- backward pass on the GPT-2 shape (gradients of every input)
+            bw = wl.workload(HEADLINE)
+            b_in = wl.inputs_for(bw, seed=rank_seed(rank))
+            bt = {n: (None if b_in[n] is None else b_in[n].to(dev))
+                  for n in ("q", "k", "v", "beta_logits", "gate_logits", "cu_seqlens")}
+            g = torch.Generator().manual_seed(1000 + rank)
+            d_o = torch.randn((bw.ntok, bw.H, bw.dv), generator=g).to(bw.dtype).to(dev)
+            bws = torch.empty(la.la_backward_delta_workspace_size(len(bw.lengths), bw.ntok, bw.H,
+                                                                  bw.dk, bw.dv),
+                              dtype=torch.uint8, device=dev)
+
+            def backward_step():
+                la.la_backward_delta(bt["q"], bt["k"], bt["v"], bt["beta_logits"],
+                                     bt["gate_logits"], d_o, bt["cu_seqlens"],
+                                     want_d_init_S=False, workspace=bws,
+                                     cu_seqlens_host=b_in["cu_seqlens"], stream=stream)
+
+            bms = time_steps(backward_step, 3, 2, flush, stream, barrier)
+            b_ms = mor(sum(bms)) / len(bms)
+            nb = backward_algo_bytes(bw)
+            extra["gpt2_backward"] = {
+                "tokens_per_s": bw.ntok * world / (b_ms / 1e3), "ms": b_ms,
+                "hbm_frac": nb / (b_ms / 1e3) / 1e9 / pk["hbm_gbs"],
+                "algorithmic_bytes": nb,
+                "kernel": "token-serial reverse sweep (checkpoint, cluster sweep, prologue)"}
+            del bt, d_o, bws
             result["secondary"] = extra
     result["clocks"] = clocks.summary()
     return result

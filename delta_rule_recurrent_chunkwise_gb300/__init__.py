@@ -21,7 +21,7 @@ LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT = 0, 
 LA_ERR_TOO_LARGE = 5
 LA_STATIC_SCRATCH_BYTES = 256 << 20
 LA_F32, LA_BF16 = 0, 1
-LA_L2NORM_K, LA_L2NORM_Q, LA_SILU_QK, LA_GATE_SCALAR = 1, 2, 4, 8
+LA_L2NORM_K, LA_L2NORM_Q, LA_SILU_QK, LA_GATE_SCALAR, LA_ADDITIVE = 1, 2, 4, 8, 16
 
 EXPORTED = ("la_prefill_linear", "la_prefill_delta", "la_prefill_delta_workspace_size",
             "la_prefill_delta_static", "la_decode_step", "la_decode_step_slots",

@@ -30,11 +30,12 @@ la_status check_delta_args(const void *q, const void *k, const void *v, const vo
                            const int32_t *cu_seqlens,
                            const int32_t *cu_seqlens_host, int N, int ntok, int H, int dk,
                            int dv, int chunk, float scale, unsigned flags) {
-    if (!q || !k || !v || !beta_logits || !o || !cu_seqlens || N < 1 || ntok < 0 || H < 1 ||
-        !dtype_ok(io))
+    if (!q || !k || !v || !o || !cu_seqlens || N < 1 || ntok < 0 || H < 1 || !dtype_ok(io))
         return LA_ERR_INVALID_ARG;
+    if (!beta_logits && !(flags & LA_ADDITIVE)) return LA_ERR_INVALID_ARG;
     if (dk < 1 || dv < 1 || chunk < 1 || !std::isfinite(scale)) return LA_ERR_INVALID_ARG;
-    if (flags & ~(LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK | LA_GATE_SCALAR)) return LA_ERR_INVALID_ARG;
+    if (flags & ~(LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK | LA_GATE_SCALAR | LA_ADDITIVE))
+        return LA_ERR_INVALID_ARG;
     if ((flags & LA_GATE_SCALAR) && !gate_logits) return LA_ERR_INVALID_ARG;
     if (!head_size_ok(dk) || !head_size_ok(dv) || chunk != 64) return LA_ERR_UNSUPPORTED;
     if (N > 65535 || H > 65535) return LA_ERR_UNSUPPORTED;
@@ -44,10 +45,12 @@ la_status check_delta_args(const void *q, const void *k, const void *v, const vo
 la_status check_decode_args(const void *q, const void *k, const void *v, const void *beta_logits,
                             const void *gate_logits, const void *o, la_dtype io, int N, int H,
                             int dk, int dv, float scale, unsigned flags, const float *state) {
-    if (!q || !k || !v || !beta_logits || !o || !state || N < 1 || H < 1 || !dtype_ok(io))
+    if (!q || !k || !v || !o || !state || N < 1 || H < 1 || !dtype_ok(io))
         return LA_ERR_INVALID_ARG;
+    if (!beta_logits && !(flags & LA_ADDITIVE)) return LA_ERR_INVALID_ARG;
     if (dk < 1 || dv < 1 || !std::isfinite(scale)) return LA_ERR_INVALID_ARG;
-    if (flags & ~(LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK | LA_GATE_SCALAR)) return LA_ERR_INVALID_ARG;
+    if (flags & ~(LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK | LA_GATE_SCALAR | LA_ADDITIVE))
+        return LA_ERR_INVALID_ARG;
     if ((flags & LA_GATE_SCALAR) && !gate_logits) return LA_ERR_INVALID_ARG;
     if (!head_size_ok(dk) || !head_size_ok(dv)) return LA_ERR_UNSUPPORTED;
     if ((int64_t)N * H * 2 > 0x7fffffffLL) return LA_ERR_UNSUPPORTED;

@@ -42,6 +42,6 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // Option bits (mirror the public header's LA_* values).
-constexpr unsigned kL2NormK = 1u, kL2NormQ = 2u, kSiluQK = 4u, kGateScalar = 8u;
+constexpr unsigned kL2NormK = 1u, kL2NormQ = 2u, kSiluQK = 4u, kGateScalar = 8u, kAdditive = 16u;
 
 }  // namespace la

@@ -7,6 +7,7 @@
 //   u  = beta (v - S'^T k)
 //   S  <- S' + k u^T                      (in place)
 //   o  = scale S^T q = scale (S'^T q + (q.k) u)
+// (the additive rule of section Gated DeltaNet takes u = v instead)
 // The last identity lets one pass over S produce both reductions S'^T k and
 // S'^T q, so the state is read once and written once: the step streams
 // 8 * dk * dv bytes of fp32 state per head and is bound by HBM bandwidth.
@@ -104,7 +105,8 @@ __global__ void __launch_bounds__(256, 4) decode_step_kernel(DecodeParams p) {
         const float inv = norm ? 1.0f / fmaxf(sqrtf(ss), 1e-12f) : 1.0f;
         for (int i = lane; i < DK; i += 32) x[i] *= inv;
     } else if (warp == 2 && lane == 0) {
-        s_beta = sigmoid_f(to_f32(static_cast<const IO *>(p.beta_logits)[nh]));
+        s_beta = (p.flags & kAdditive) ? 1.0f
+                                       : sigmoid_f(to_f32(static_cast<const IO *>(p.beta_logits)[nh]));
     }
     __syncthreads();
     if (warp == 0) {
@@ -133,7 +135,7 @@ __global__ void __launch_bounds__(256, 4) decode_step_kernel(DecodeParams p) {
         float rk = 0.0f, rq = 0.0f;
 #pragma unroll
         for (int i = 0; i < RPP; ++i) { rk += red_k[i][tid]; rq += red_q[i][tid]; }
-        const float u = s_beta * (sv[tid] - rk);
+        const float u = s_beta * (sv[tid] - ((p.flags & kAdditive) ? 0.0f : rk));
         su[tid] = u;
         static_cast<IO *>(p.o)[nh * DV + j0 + tid] = from_f32<IO>(p.scale * (rq + s_qk * u));
     }

@@ -11,7 +11,9 @@
 //                                dk_t -= beta S' du;  dS' = dS - beta k_t du^T
 //   S' = Diag(alpha_t) S_{t-1}   dalpha = rowsum(dS' o S_{t-1});  dS <- Diag(alpha) dS'
 // then through the prologue (sigmoid beta, -softplus log-decay, silu and
-// L2 normalisation of q and k).
+// L2 normalisation of q and k).  The additive rule (u_t = v_t, section Gated
+// DeltaNet) drops the read path: beta = 1 and the terms weighted by beta S'
+// and beta k vanish; it has no beta gradient.
 //
 // Every column j of S evolves on its own: u_t[j], the j-th column of S and of
 // dS depend on column j and on the shared per-token q, k, alpha, beta only.
@@ -105,7 +107,10 @@ __device__ void stage_chunk(const BwdParams &p, int64_t t0, int Lc, int h, int j
         for (int r = 0; r < R; ++r)
             sA[s * DK + lane + 32 * r] =
                 !g ? 1.0f : decay_f(to_f32(scalar ? g[th] : g[th * DK + lane + 32 * r]));
-        if (lane == 0) sB[s] = sigmoid_f(to_f32(static_cast<const IO *>(p.beta_logits)[th]));
+        if (lane == 0)
+            sB[s] = (p.flags & kAdditive)
+                        ? 1.0f
+                        : sigmoid_f(to_f32(static_cast<const IO *>(p.beta_logits)[th]));
     }
     for (int idx = threadIdx.x; idx < Lc * kNW; idx += kNT) {
         const int s = idx / kNW, c = idx % kNW;
@@ -116,10 +121,12 @@ __device__ void stage_chunk(const BwdParams &p, int64_t t0, int Lc, int h, int j
 }
 
 // One forward token step of column j (rows lane + 32 r): S <- Diag(a) S,
-// r = S^T k (all lanes), u = beta (v - r), S += k u.
+// r = S^T k (all lanes), u = beta (v - r) (u = v for the additive rule),
+// S += k u.
 template <int DK>
 __device__ __forceinline__ void fwd_step(float (&S)[DK / 32], const float *a, const float *kk,
-                                         float beta, float v, float &rr, float &uu) {
+                                         float beta, float v, bool additive, float &rr,
+                                         float &uu) {
     constexpr int R = DK / 32;
     const int lane = threadIdx.x & 31;
     float acc = 0.0f;
@@ -129,7 +136,7 @@ __device__ __forceinline__ void fwd_step(float (&S)[DK / 32], const float *a, co
         acc = fmaf(kk[lane + 32 * r], S[r], acc);
     }
     rr = warp_sum(acc);
-    uu = beta * (v - rr);
+    uu = additive ? v : beta * (v - rr);
 #pragma unroll
     for (int r = 0; r < R; ++r) S[r] = fmaf(kk[lane + 32 * r], uu, S[r]);
 }
@@ -150,6 +157,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_ckpt_kernel(BwdParams p) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int h = blockIdx.y, n = blockIdx.z;
     const int j0 = blockIdx.x * kNW, j = j0 + w;
+    const bool additive = (p.flags & kAdditive) != 0;
     int64_t c0, len;
     if (!seq_bounds(p, n, c0, len)) {
         if (threadIdx.x == 0 && blockIdx.x == 0) atomicCAS(p.err, 0u, 100u);
@@ -173,7 +181,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_ckpt_kernel(BwdParams p) {
         for (int s = 0; s < Lc; ++s) {
             float rr, uu;
             fwd_step<DK>(S, smem + L::A + s * DK, smem + L::K + s * DK, smem[L::B + s],
-                         smem[L::V + s * kNW + w], rr, uu);
+                         smem[L::V + s * kNW + w], additive, rr, uu);
         }
     }
 }
@@ -199,6 +207,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_kernel(BwdParams p) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int h = blockIdx.y, n = blockIdx.z;
     const int j0 = blockIdx.x * kNW, j = j0 + w;
+    const bool additive = (p.flags & kAdditive) != 0;
     int64_t c0, len;
     // The same sequence for every CTA of the cluster: all leave here together.
     if (!seq_bounds(p, n, c0, len)) return;
@@ -237,7 +246,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_kernel(BwdParams p) {
                 for (int r = 0; r < R; ++r) sub[(s / kE) * DK + lane + 32 * r] = S[r];
             }
             float rr, uu;
-            fwd_step<DK>(S, sA + s * DK, sK + s * DK, sB[s], sV[s * kNW + w], rr, uu);
+            fwd_step<DK>(S, sA + s * DK, sK + s * DK, sB[s], sV[s * kNW + w], additive, rr, uu);
         }
         __syncwarp();
 
@@ -253,7 +262,8 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_kernel(BwdParams p) {
                 if (s < Lc) {
 #pragma unroll
                     for (int r = 0; r < R; ++r) hist[e][r] = S[r];
-                    fwd_step<DK>(S, sA + s * DK, sK + s * DK, sB[s], sV[s * kNW + w], rr[e], uu[e]);
+                    fwd_step<DK>(S, sA + s * DK, sK + s * DK, sB[s], sV[s * kNW + w], additive,
+                                 rr[e], uu[e]);
                 }
             }
             // Sweep it backwards.
@@ -263,6 +273,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_kernel(BwdParams p) {
                 if (s >= Lc) continue;
                 const float *a = sA + s * DK, *kk = sK + s * DK, *qq = sQ + s * DK;
                 const float beta = sB[s], dov = sDO[s * kNW + w];
+                const float bread = additive ? 0.0f : beta;   // weight of the read path
                 float *ae = acc + e * 3 * DK;
                 float Sd[R], pdu = 0.0f;
 #pragma unroll
@@ -278,8 +289,8 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_kernel(BwdParams p) {
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     const int i = lane + 32 * r;
-                    atomicAdd(&ae[DK + i], fmaf(dS[r], uu[e], -beta * Sd[r] * du));  // dk^
-                    const float dSp = fmaf(-beta * kk[i], du, dS[r]);               // dS'
+                    atomicAdd(&ae[DK + i], fmaf(dS[r], uu[e], -bread * Sd[r] * du)); // dk^
+                    const float dSp = fmaf(-bread * kk[i], du, dS[r]);              // dS'
                     atomicAdd(&ae[2 * DK + i], dSp * hist[e][r]);                    // dalpha
                     dS[r] = a[i] * dSp;
                 }
@@ -369,8 +380,14 @@ __global__ void __launch_bounds__(256) delta_bwd_prologue_kernel(BwdParams p) {
     if (!(p.cu[lo] <= t && t < p.cu[lo + 1])) return;
 
     const float *sum = p.sums + th * 3 * DK;
-    const float beta = sigmoid_f(to_f32(static_cast<const IO *>(p.beta_logits)[th]));
-    if (lane == 0) p.d_beta_logits[th] = p.dbeta[th] * beta * (1.0f - beta);
+    if (lane == 0) {
+        if (p.flags & kAdditive) {
+            p.d_beta_logits[th] = 0.0f;   // the additive rule has no beta
+        } else {
+            const float beta = sigmoid_f(to_f32(static_cast<const IO *>(p.beta_logits)[th]));
+            p.d_beta_logits[th] = p.dbeta[th] * beta * (1.0f - beta);
+        }
+    }
     const IO *g = static_cast<const IO *>(p.gate_logits);
     if (g) {
         if (p.flags & kGateScalar) {

@@ -16,6 +16,9 @@
 // e^{b_end}.  None of it depends on the state, so every (chunk, head) is an
 // independent task; the inter-chunk kernel then carries the state through
 // the chunks with u = U - W S, O = (Q e^b) S + Aq u, S <- e^{b_end} S + K~^T u.
+// The additive rule (section Gated DeltaNet: the decayed state plus k v^T at
+// full strength, no delta) is the same pipeline with A = 0 (so T = I),
+// beta = 1 and W = 0: then U = V and u = V.
 //
 // Decay factors.  Only products of alpha are formed, never exponentials of
 // cumulative sums: alpha = 1 / (1 + e^g) and 1/alpha = 1 + e^g cost one
@@ -210,6 +213,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
     const int qd = lw & 3, cp = lw >> 2;  // TMEM lane quarter, column part
     const int H = p.H;
     const bool silu = (p.flags & kSiluQK) != 0;
+    const bool additive = (p.flags & kAdditive) != 0;  // A = 0, W = 0, beta = 1: u = V
     const bool l2k = (p.flags & kL2NormK) != 0, l2q = (p.flags & kL2NormQ) != 0;
     constexpr uint32_t tx_bytes = (GATED ? 4u : 3u) * L::tile64;
 
@@ -264,7 +268,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
         }
     };
     auto load_beta = [&](const int4 &ti) -> float {
-        return (ltid < C && ltid < ti.y)
+        return (!additive && ltid < C && ltid < ti.y)
                    ? __bfloat162float(p.beta_logits[(int64_t)(ti.x + ltid) * H + ti.z])
                    : 0.0f;
     };
@@ -350,7 +354,8 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
             tc_fence_after();
         }
         // ---------------------------------------------- A0: beta, row norms
-        if (ltid < C) sbeta[ltid] = ltid < len ? __fdividef(1.0f, 1.0f + __expf(-beta_cur)) : 0.0f;
+        if (ltid < C)
+            sbeta[ltid] = ltid >= len ? 0.0f : additive ? 1.0f : __fdividef(1.0f, 1.0f + __expf(-beta_cur));
         if (scalar && ltid < C) sLb[ltid] = ltid < len ? log_decay_f(gate_cur) : 0.0f;  // log alpha
         {
             // TPR threads per row, D/TPR channels each, 16-byte loads
@@ -672,7 +677,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
                     st_bf16x8(aqk, 64, r, col, v);
                     st_bf16x8(aqk, 64, r, col + 8, v + 8);
                 } else {
-                    const float be = sbeta[r];
+                    const float be = additive ? 0.0f : sbeta[r];
                     float4 *dst = reinterpret_cast<float4 *>(sA + r * LDT + col);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -803,7 +808,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
             const int w0 = cp * CPP;                   // first column of the part in W | U
             const bool is_w = w0 < D;
             uint8_t *dst = is_w ? wq : uk;
-            const float sgn = is_w ? -1.0f : 1.0f;
+            const float sgn = is_w ? (additive ? 0.0f : -1.0f) : 1.0f;
             const int c0 = w0 % D;
 #pragma unroll
             for (int cb = 0; cb < CPP; cb += 32) {

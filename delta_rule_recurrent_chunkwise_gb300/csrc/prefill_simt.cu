@@ -18,6 +18,7 @@
 //   Aq[r][i] =        sum_c q_rc k_ic e^{b_rc - b_ic}      (i <= r)
 //   T        = (I + A)^{-1}                               (forward substitution)
 //   u        = T (beta (V - (K e^{b}) S))                 (= U - W S of eq. 8-10)
+//   (additive rule: A = 0, beta = 1 and no read, so u = V)
 //   O        = scale ((Q e^{b}) S + Aq u)
 //   S       <- Diag(e^{b_end}) S + (K e^{b_end - b})^T u
 // Every exponent used is a difference b_r - b_i with i <= r, so it is <= 0:
@@ -75,6 +76,7 @@ __global__ void __launch_bounds__(kNT) delta_chunk_simt_kernel(SimtParams p) {
     const bool gated = p.gate_logits != nullptr;
     const bool gate_scalar = (p.flags & kGateScalar) != 0;  // gate [ntok][H]
     const bool silu = (p.flags & kSiluQK) != 0;
+    const bool additive = (p.flags & kAdditive) != 0;  // u = v: no delta term, no beta
     const IO *Q = static_cast<const IO *>(p.q), *K = static_cast<const IO *>(p.k);
     const IO *V = static_cast<const IO *>(p.v);
     const IO *BL = static_cast<const IO *>(p.beta_logits);
@@ -110,7 +112,10 @@ __global__ void __launch_bounds__(kNT) delta_chunk_simt_kernel(SimtParams p) {
             const int r = e / DVS, j = e % DVS;
             sV[r * LDV + j] = r < len ? to_f32(V[((int64_t)(cs + r) * H + h) * dv + j0 + j]) : 0.0f;
         }
-        if (tid < C) sBeta[tid] = tid < len ? sigmoid_f(to_f32(BL[(int64_t)(cs + tid) * H + h])) : 0.0f;
+        if (tid < C)
+            sBeta[tid] = tid >= len ? 0.0f
+                         : additive ? 1.0f
+                                    : sigmoid_f(to_f32(BL[(int64_t)(cs + tid) * H + h]));
         __syncthreads();
         // ---- prologue: silu, L2 norms (one warp per row), decay cumsum
         for (int r = warp; r < C; r += NT / 32) {
@@ -152,7 +157,7 @@ __global__ void __launch_bounds__(kNT) delta_chunk_simt_kernel(SimtParams p) {
                     for (int c = 0; c < DK; ++c) { akk += kr[c] * ki[c]; aqk += qr[c] * ki[c]; }
                 }
             }
-            sA[r * LDC + i] = i < r ? sBeta[r] * akk : 0.0f;
+            sA[r * LDC + i] = (i < r && !additive) ? sBeta[r] * akk : 0.0f;
             sAq[r * LDC + i] = aqk;
         }
         __syncthreads();
@@ -187,7 +192,7 @@ __global__ void __launch_bounds__(kNT) delta_chunk_simt_kernel(SimtParams p) {
             const int r = e / DVS, j = e % DVS;
             float acc = 0.0f;
             for (int c = 0; c < DK; ++c) acc += sKg[r * LDK + c] * sS[c * LDV + j];
-            sV[r * LDV + j] = sBeta[r] * (sV[r * LDV + j] - acc);
+            sV[r * LDV + j] = sBeta[r] * (sV[r * LDV + j] - (additive ? 0.0f : acc));
         }
         __syncthreads();
         // ---- u = T R

@@ -73,6 +73,14 @@ typedef enum la_dtype { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
  * cache = alpha * S_old + S_new) instead of the per-key-channel decay of
  * section KDA / Kimi Linear.  Requires gate_logits. */
 #define LA_GATE_SCALAR 8u
+/* LA_ADDITIVE: the decayed additive state of section Gated DeltaNet
+ * (Mamba-2: cache = alpha * S_old + k @ v, the new association added at
+ * full strength): u_t = v_t, no read of the old value and no beta, so
+ * S_t = Diag(alpha_t) S_{t-1} + k_t v_t^T.  Any gate form (none, per key
+ * channel, LA_GATE_SCALAR) applies; beta_logits is ignored and may be NULL.
+ * Accepted by la_prefill_delta(_static), la_decode_step(_slots) and
+ * la_backward_delta (which then writes d_beta_logits = 0). */
+#define LA_ADDITIVE 16u
 
 /* Causal ELU+1 linear attention, chunkwise-parallel prefill.
  * Defined in section Linear attention (the forward() that replaces the KV
@@ -100,7 +108,8 @@ la_status la_prefill_linear(const void *q, const void *k, const void *v, void *o
  * alpha_t[c] = exp(-softplus(gate_logits[t][h][c])).
  * gate_logits: nullable; NULL means alpha = 1 (plain DeltaNet).  With
  * LA_GATE_SCALAR it is [ntok][H] and alpha_t applies to all channels.
- * flags: LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK | LA_GATE_SCALAR (above).
+ * flags: LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK | LA_GATE_SCALAR | LA_ADDITIVE
+ * (above).
  * chunk: tokens per chunk; 64 is the supported value.
  * scale: output scale (the page's delta-rule listings use 1.0).
  * init_S: nullable [N][H][dk][dv]; final_S: nullable, may equal init_S.

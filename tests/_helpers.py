@@ -25,7 +25,7 @@ def f64(t):
 def gpu_prefill_delta(la, inp, flags=None, scale=1.0, final=True, init=True):
     dev = torch.device("cuda")
     q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
-    bl = inp["beta_logits"].to(dev)
+    bl = None if inp["beta_logits"] is None else inp["beta_logits"].to(dev)
     gl = None if inp["gate_logits"] is None else inp["gate_logits"].to(dev)
     cu = inp["cu_seqlens"].to(dev)
     N, H, dk, dv = cu.numel() - 1, q.shape[1], q.shape[2], v.shape[2]
@@ -41,7 +41,8 @@ def gpu_prefill_delta(la, inp, flags=None, scale=1.0, final=True, init=True):
 
 def oracle_prefill_delta(inp, heads=None, flags=oracle.L2NORM_K, scale=1.0, init=True):
     sel = (lambda t: t) if heads is None else (lambda t: t[:, heads])
-    q, k, v, bl = (sel(inp[n]) for n in ("q", "k", "v", "beta_logits"))
+    q, k, v = (sel(inp[n]) for n in ("q", "k", "v"))
+    bl = None if inp["beta_logits"] is None else sel(inp["beta_logits"])
     gl = None if inp["gate_logits"] is None else sel(inp["gate_logits"])
     iS = inp.get("init_S") if init else None
     if iS is not None and heads is not None:
