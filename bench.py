@@ -451,7 +451,19 @@ def profile_case(args):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     name = args.profile_case
-    if name in ("decode", "decode_small"):
+    if name == "gpt2_backward":
+        w = wl.workload(HEADLINE)
+        inp = wl.inputs_for(w, seed=0, init_state=True)
+        t = {n: (None if inp[n] is None else inp[n].to(dev))
+             for n in ("q", "k", "v", "beta_logits", "gate_logits", "cu_seqlens", "init_S")}
+        d_o = torch.randn((w.ntok, w.H, w.dv), generator=torch.Generator().manual_seed(1)).to(
+            w.dtype).to(dev)
+        ws = torch.empty(la.la_backward_delta_workspace_size(len(w.lengths), w.ntok, w.H, w.dk,
+                                                             w.dv), dtype=torch.uint8, device=dev)
+        fn = lambda: la.la_backward_delta(t["q"], t["k"], t["v"], t["beta_logits"], None, d_o,
+                                          t["cu_seqlens"], init_S=t["init_S"], workspace=ws,
+                                          cu_seqlens_host=inp["cu_seqlens"], stream=stream)
+    elif name in ("decode", "decode_small"):
         w = wl.workload("decode")
         n_seq = w.n_seq if name == "decode" else 128
         d = wl.decode_inputs(n_seq, w.H, w.dk, w.dv, 1, w.dtype, seed=0)
@@ -494,7 +506,8 @@ def main():
                     help="units of a full launch / units of the captured launch")
     ap.add_argument("--profile-case", default=None,
                     help="run one workload only (for ncu): gpt2_prefill, gated_prefill, "
-                         "varlen_prefill, decode, decode_small, gated_small")
+                         "varlen_prefill, gpt2_scalar_gate, gpt2_backward, decode, decode_small, "
+                         "gated_small")
     args = ap.parse_args()
     if args.profile_case:
         return profile_case(args)

@@ -41,6 +41,42 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// d/dx of prep(x) = normalize(silu(x)) (each step optional) for one row held
+// by a warp, R values per lane; dy is overwritten by dx.  The norm's floor
+// (1e-12) is a constant, so below it the derivative is dy / 1e-12.
+template <int R>
+__device__ __forceinline__ void prep_backward(const float (&x)[R], float (&dy)[R], bool silu,
+                                              bool norm) {
+    float s[R], sg[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        sg[r] = silu ? sigmoid_f(x[r]) : 1.0f;
+        s[r] = silu ? x[r] * sg[r] : x[r];
+    }
+    if (norm) {
+        float ss = 0.0f;
+#pragma unroll
+        for (int r = 0; r < R; ++r) ss += s[r] * s[r];
+        const float nrm = sqrtf(warp_sum(ss));
+        if (nrm > 1e-12f) {
+            const float inv = 1.0f / nrm;
+            float ydy = 0.0f;
+#pragma unroll
+            for (int r = 0; r < R; ++r) ydy += s[r] * inv * dy[r];
+            ydy = warp_sum(ydy);
+#pragma unroll
+            for (int r = 0; r < R; ++r) dy[r] = (dy[r] - s[r] * inv * ydy) * inv;
+        } else {
+#pragma unroll
+            for (int r = 0; r < R; ++r) dy[r] *= 1e12f;
+        }
+    }
+    if (silu) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) dy[r] *= sg[r] * (1.0f + x[r] * (1.0f - sg[r]));
+    }
+}
+
 // Option bits (mirror the public header's LA_* values).
 constexpr unsigned kL2NormK = 1u, kL2NormQ = 2u, kSiluQK = 4u, kGateScalar = 8u, kAdditive = 16u;
 

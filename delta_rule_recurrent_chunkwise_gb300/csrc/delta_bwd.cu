@@ -59,7 +59,7 @@ struct BwdParams {
     const int32_t *cu;
     float *dq, *dk, *dv, *d_beta_logits, *d_gate_logits, *d_init_S;
     float *ckpt;     // [slots][H][dv][dk]
-    float *sums;     // [ntok][H][3][dk] : dq^ (unscaled), dk^, dalpha
+    float *sums;     // [ntok][H][3][dk] : dq^, dk^, d log alpha (per key channel)
     float *dbeta;    // [ntok][H]
     unsigned *err;
     int N, H, ntok;
@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_kernel(BwdParams p) {
                     const int i = lane + 32 * r;
                     Sd[r] = a[i] * hist[e][r];
                     const float St = fmaf(kk[i], uu[e], Sd[r]);   // S_t, after the write
-                    atomicAdd(&ae[i], St * dov);                   // dq^ / scale
+                    atomicAdd(&ae[i], p.scale * St * dov);         // dq^
                     dS[r] = fmaf(p.scale * qq[i], dov, dS[r]);
                     pdu = fmaf(dS[r], kk[i], pdu);
                 }
@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_kernel(BwdParams p) {
                     const int i = lane + 32 * r;
                     atomicAdd(&ae[DK + i], fmaf(dS[r], uu[e], -bread * Sd[r] * du)); // dk^
                     const float dSp = fmaf(-bread * kk[i], du, dS[r]);              // dS'
-                    atomicAdd(&ae[2 * DK + i], dSp * hist[e][r]);                    // dalpha
+                    atomicAdd(&ae[2 * DK + i], dSp * Sd[r]);     // d log alpha = dalpha alpha
                     dS[r] = a[i] * dSp;
                 }
                 if (lane == 0) {
@@ -327,41 +327,6 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_kernel(BwdParams p) {
     cl.sync();  // no CTA leaves while another may still read its shared memory
 }
 
-// d/dx of prep(x) = normalize(silu(x)) (each step optional), for one row of
-// R values per lane; dy is overwritten by dx.
-template <int R>
-__device__ __forceinline__ void prep_backward(const float (&x)[R], float (&dy)[R], bool silu,
-                                              bool norm) {
-    float s[R], sg[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        sg[r] = silu ? sigmoid_f(x[r]) : 1.0f;
-        s[r] = silu ? x[r] * sg[r] : x[r];
-    }
-    if (norm) {
-        float ss = 0.0f;
-#pragma unroll
-        for (int r = 0; r < R; ++r) ss += s[r] * s[r];
-        const float nrm = sqrtf(warp_sum(ss));
-        if (nrm > 1e-12f) {
-            const float inv = 1.0f / nrm;
-            float ydy = 0.0f;
-#pragma unroll
-            for (int r = 0; r < R; ++r) ydy += s[r] * inv * dy[r];
-            ydy = warp_sum(ydy);
-#pragma unroll
-            for (int r = 0; r < R; ++r) dy[r] = (dy[r] - s[r] * inv * ydy) * inv;
-        } else {
-#pragma unroll
-            for (int r = 0; r < R; ++r) dy[r] *= 1e12f;
-        }
-    }
-    if (silu) {
-#pragma unroll
-        for (int r = 0; r < R; ++r) dy[r] *= sg[r] * (1.0f + x[r] * (1.0f - sg[r]));
-    }
-}
-
 // One warp per (token, head): the column sums through the prologue.  Tokens
 // outside every sequence are skipped (their rows stay as the caller left them).
 template <typename IO, int DK>
@@ -395,14 +360,13 @@ __global__ void __launch_bounds__(256) delta_bwd_prologue_kernel(BwdParams p) {
 #pragma unroll
             for (int r = 0; r < R; ++r) da += sum[2 * DK + lane + 32 * r];
             da = warp_sum(da);
-            const float x = to_f32(g[th]);
-            if (lane == 0) p.d_gate_logits[th] = -da * decay_f(x) * sigmoid_f(x);
+            if (lane == 0) p.d_gate_logits[th] = -da * sigmoid_f(to_f32(g[th]));
         } else {
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const int i = lane + 32 * r;
-                const float x = to_f32(g[th * DK + i]);
-                p.d_gate_logits[th * DK + i] = -sum[2 * DK + i] * decay_f(x) * sigmoid_f(x);
+                // log alpha = -softplus(x): d x = -d(log alpha) sigmoid(x)
+                p.d_gate_logits[th * DK + i] = -sum[2 * DK + i] * sigmoid_f(to_f32(g[th * DK + i]));
             }
         }
     }
@@ -413,7 +377,7 @@ __global__ void __launch_bounds__(256) delta_bwd_prologue_kernel(BwdParams p) {
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             x[r] = to_f32(src[lane + 32 * r]);
-            d[r] = which ? sum[DK + lane + 32 * r] : p.scale * sum[lane + 32 * r];
+            d[r] = sum[(which ? DK : 0) + lane + 32 * r];
         }
         prep_backward<R>(x, d, silu, (p.flags & (which ? kL2NormK : kL2NormQ)) != 0);
         float *dst = (which ? p.dk : p.dq) + th * DK;
@@ -491,10 +455,14 @@ cudaError_t dispatch(const BwdArgs &a, BwdParams p, cudaStream_t s) {
 }  // namespace
 
 size_t delta_bwd_workspace_bytes(int N, int ntok, int H, int dk, int dv) {
-    return ws_parts(N, ntok, H, dk, dv).total;
+    // enough for either form (the chunkwise one exists for dk = dv = 64)
+    const size_t serial = ws_parts(N, ntok, H, dk, dv).total;
+    const size_t chunked = (dk == 64 && dv == 64) ? delta_bwd_chunked_workspace_bytes(N, ntok, H) : 0;
+    return serial > chunked ? serial : chunked;
 }
 
 cudaError_t launch_delta_backward(const BwdArgs &a, cudaStream_t s) {
+    if (delta_bwd_chunked_supported(a)) return launch_delta_backward_chunked(a, s);
     const WsParts w = ws_parts(a.N, a.ntok, a.H, a.dk, a.dv);
     uint8_t *base = static_cast<uint8_t *>(a.workspace);
     BwdParams p{a.q, a.k, a.v, a.beta_logits, a.gate_logits, a.d_o, a.d_final_S, a.init_S,

@@ -71,7 +71,8 @@ struct Cols {
 
 struct InterParams {
     const uint8_t *records;   // [slots][H] records
-    __nv_bfloat16 *o;
+    __nv_bfloat16 *o;         // null: outputs not written
+    float *states;            // null, or the state at each chunk start [slot][H][D][D]
     const int32_t *cu_seqlens;
     const float *init_S;
     float *final_S;
@@ -146,6 +147,14 @@ __global__ void __launch_bounds__(NT, 1) delta_inter_kernel(InterParams p) {
     const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);  // this warp's lane quarter
     auto acc = [&](int c) { return (uint32_t)(TC::ACC + (c & 1) * D); };
     const int64_t sbase = ((int64_t)n * H + h) * D * D;
+    // 16 consecutive fp32 state entries (row srow, columns col..col+15) at the
+    // start of chunk c, for the backward pass
+    auto store_state = [&](int c, int srow, int col, const float *v) {
+        float4 *dst = reinterpret_cast<float4 *>(
+            p.states + (((slot0 + c) * H + h) * D + srow) * (int64_t)D + col);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    };
     // one lane of each warp arrives once the warp's work is ordered before it
     auto warp_arrive = [&](uint64_t *bar) {
         tc_fence_before();
@@ -229,6 +238,7 @@ __global__ void __launch_bounds__(NT, 1) delta_inter_kernel(InterParams p) {
                 if (srow >= 0) {
                     st_bf16x8(sb, D, srow, col, v);
                     st_bf16x8(sb, D, srow, col + 8, v + 8);
+                    if (p.states) store_state(0, srow, col, v);
                 }
 #pragma unroll
                 for (int i = 0; i < 16; ++i) v[i] *= gd;
@@ -263,6 +273,10 @@ __global__ void __launch_bounds__(NT, 1) delta_inter_kernel(InterParams p) {
                     if (srow >= 0) {
 #pragma unroll
                         for (int i = 0; i < 32; i += 8) st_bf16x8(sb, D, srow, c0 + cb + i, v + i);
+                        if (p.states) {
+                            store_state(c + 1, srow, c0 + cb, v);
+                            store_state(c + 1, srow, c0 + cb + 16, v + 16);
+                        }
                     }
                 }
                 fence_proxy_async();
@@ -344,7 +358,7 @@ __global__ void __launch_bounds__(NT, 1) delta_inter_kernel(InterParams p) {
             for (int cb = 0; cb < D; cb += 32) {
                 float v[32];
                 tmem_ld32(tq + acc(c) + cb, v);
-                if (valid) {
+                if (valid && p.o) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] *= p.scale;
                     uint4 *dst = reinterpret_cast<uint4 *>(p.o + ((int64_t)(tok0 + orow) * H + h) * D + cb);
@@ -380,8 +394,8 @@ __global__ void __launch_bounds__(NT, 1) delta_inter_kernel(InterParams p) {
 template <int D, bool GATED>
 cudaError_t launch_t(const TcLaunch &x, cudaStream_t s) {
     const PrefillArgs &a = *x.a;
-    InterParams p{x.records, static_cast<__nv_bfloat16 *>(a.o), a.cu_seqlens, a.init_S,
-                  a.final_S, x.err, a.H, a.ntok, a.scale};
+    InterParams p{x.records, static_cast<__nv_bfloat16 *>(a.o), a.chunk_states, a.cu_seqlens,
+                  a.init_S, a.final_S, x.err, a.H, a.ntok, a.scale};
     constexpr size_t smem = Layout<D>::TOTAL + 1024;
     auto kern = delta_inter_kernel<D, GATED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -20,6 +20,10 @@ struct PrefillArgs {
     bool bf16;
     void *workspace;          // device scratch (tensor-core delta path)
     size_t workspace_bytes;
+    // Tensor-core delta path only, for the backward pass: the state at the
+    // start of every chunk, fp32 [slot][H][dk][dv] (slot as in the chunk
+    // table), or null.  With it, o may be null (no output written).
+    float *chunk_states = nullptr;
 };
 
 struct DecodeArgs {
@@ -49,6 +53,13 @@ struct BwdArgs {
 };
 size_t delta_bwd_workspace_bytes(int N, int ntok, int H, int dk, int dv);
 cudaError_t launch_delta_backward(const BwdArgs &a, cudaStream_t s);
+// Chunkwise form (bf16, dk = dv = 64, no gate or a scalar gate, not additive):
+// the tensor-core forward with chunk states, a reverse dS chain and a
+// parallel per-chunk gradient kernel that also takes the prologue's
+// derivatives.
+bool delta_bwd_chunked_supported(const BwdArgs &a);
+size_t delta_bwd_chunked_workspace_bytes(int N, int ntok, int H);
+cudaError_t launch_delta_backward_chunked(const BwdArgs &a, cudaStream_t s);
 
 // fp32 SIMT chunk kernels (any I/O dtype).
 cudaError_t launch_linear_simt(const PrefillArgs &a, cudaStream_t s);
