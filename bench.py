@@ -373,7 +373,8 @@ def run_ours(args, rank, world, dev, dist):
                 "tokens_per_s": bw.ntok * world / (b_ms / 1e3), "ms": b_ms,
                 "hbm_frac": nb / (b_ms / 1e3) / 1e9 / pk["hbm_gbs"],
                 "algorithmic_bytes": nb,
-                "kernel": "token-serial reverse sweep (checkpoint, cluster sweep, prologue)"}
+                "kernel": "chunkwise: forward with chunk states, reverse dS chain, per-chunk "
+                          "gradient kernel (TF32 mma.sync)"}
             del bt, d_o, bws
             result["secondary"] = extra
     result["clocks"] = clocks.summary()
