@@ -70,11 +70,11 @@ typedef enum la_dtype { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
 /* LA_GATE_SCALAR: gate_logits holds one value per token and head
  * ([ntok][H] in prefill, [N][H] in decode) and alpha applies to every key
  * channel alike -- the scalar decay of section Gated DeltaNet (Mamba-2's
- * cache = alpha * S_old + S_new) instead of the per-key-channel decay of
+ * S_t = alpha_t S_{t-1} + k_t v_t^T) instead of the per-key-channel decay of
  * section KDA / Kimi Linear.  Requires gate_logits. */
 #define LA_GATE_SCALAR 8u
 /* LA_ADDITIVE: the decayed additive state of section Gated DeltaNet
- * (Mamba-2: cache = alpha * S_old + k @ v, the new association added at
+ * (Mamba-2: S_t = alpha_t S_{t-1} + k_t v_t^T, the new association added at
  * full strength): u_t = v_t, no read of the old value and no beta, so
  * S_t = Diag(alpha_t) S_{t-1} + k_t v_t^T.  Any gate form (none, per key
  * channel, LA_GATE_SCALAR) applies; beta_logits is ignored and may be NULL.

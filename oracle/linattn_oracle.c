@@ -203,7 +203,7 @@ typedef struct {
  *     DeltaNet (Fast Weight Programmers) and
  *     DeltaNet (Parallelizing Linear Transformers with Delta Rule);
  *   - the decay of the old state before the write: section Gated DeltaNet
- *     (Mamba-2's cache = alpha * S_old + S_new; alpha = 1 gives the pure
+ *     (Mamba-2's decayed state, S = alpha S + k v^T; alpha = 1 gives the pure
  *     delta rule, alpha = 0 clears the memory);
  *   - one decay per key channel: section KDA / Kimi Linear
  *     (alpha.reshape(nb, C, d)).
@@ -214,7 +214,7 @@ typedef struct {
  * in the column convention.
  * ORACLE_ADDITIVE turns the delta off: u_t = v_t (no read of the old value,
  * no beta), the decayed additive state of section Gated DeltaNet
- * (Mamba-2: cache = alpha * S_old + S_new, S_new = k @ v added at full
+ * (Mamba-2: S_t = alpha_t S_{t-1} + k_t v_t^T, the new association added at full
  * strength). */
 static void delta_pair(void *vctx, int64_t pair) {
     const delta_ctx *c = (const delta_ctx *)vctx;
@@ -247,7 +247,7 @@ static void delta_pair(void *vctx, int64_t pair) {
             for (int j = 0; j < dv; ++j) S[i * dv + j] *= alpha[i];
         /* u = beta (v - S'^T k); the additive rule writes v at full strength
          * with no read (section Gated DeltaNet: Mamba-2's
-         * cache = alpha * S_old + k @ v) */
+         * S_t = alpha_t S_{t-1} + k_t v_t^T) */
         for (int j = 0; j < dv; ++j) {
             double old = 0.0;
             for (int i = 0; i < dk; ++i) old += kk[i] * S[i * dv + j];

@@ -1,5 +1,5 @@
 """GPU parity of the additive decayed rule (LA_ADDITIVE: u = v, the page's
-Mamba-2 form cache = alpha * S_old + k @ v) against the oracle, on every
+Mamba-2 form S_t = alpha_t S_{t-1} + k_t v_t^T) against the oracle, on every
 path: the CUDA-core prefill (fp32), the tensor-core prefill (bf16, dk = dv),
 the decode step and the backward pass."""
 import pytest

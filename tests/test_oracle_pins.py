@@ -458,7 +458,7 @@ def _decayed_attention(q, k, v, log_a, S0):
 
 @pytest.mark.parametrize("gate", ["channel", "scalar"])
 def test_additive_rule_equals_bruteforce_decayed_attention(gate):
-    """ADDITIVE: the page's Mamba-2 update cache = alpha * S_old + k @ v
+    """ADDITIVE: the page's Mamba-2 update S_t = alpha_t S_{t-1} + k_t v_t^T
     (section Gated DeltaNet): every value is written at full strength and
     only decays afterwards."""
     r = rng(31)
