@@ -253,6 +253,52 @@ def time_steps(step_fn, steps, warmup, flush, stream, barrier=None):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
+def e2e_pipelined(la, pf, host, stream, steps, barrier=None):
+    """Milliseconds for `steps` end-to-end prefill calls: each step copies its
+    inputs from pinned host memory into one of two device buffer sets (copy
+    stream), runs la_prefill_delta on the compute stream, and copies its
+    output back to pinned host memory (read-back stream).  Events order each
+    buffer's reuse two steps later."""
+    sets = [pf.t, {n: (None if t is None else t.clone()) for n, t in pf.t.items()}]
+    outs = [pf.o, torch.empty_like(pf.o)]
+    o_host = [torch.empty(pf.o.shape, dtype=pf.o.dtype).pin_memory() for _ in range(2)]
+    cs, rs = torch.cuda.Stream(), torch.cuda.Stream()
+    h2d = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    d2h = [torch.cuda.Event() for _ in range(2)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w = pf.w
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    start.record(cs)
+    for i in range(steps):
+        b = i & 1
+        with torch.cuda.stream(cs):
+            if i >= 2:
+                cs.wait_event(done[b])          # step i-2 has finished reading set b
+            for n, t in host.items():
+                sets[b][n].copy_(t, non_blocking=True)
+            h2d[b].record(cs)
+        stream.wait_event(h2d[b])
+        if i >= 2:
+            stream.wait_event(d2h[b])           # step i-2's output has been read back
+        t = sets[b]
+        la.la_prefill_delta(t["q"], t["k"], t["v"], t["beta_logits"], t["gate_logits"], outs[b],
+                            t["cu_seqlens"], flags=pf.flags, workspace=pf.ws,
+                            cu_seqlens_host=pf.cu_host, stream=stream)
+        done[b].record(stream)
+        with torch.cuda.stream(rs):
+            rs.wait_event(done[b])
+            o_host[b].copy_(outs[b], non_blocking=True)
+            d2h[b].record(rs)
+    end.record(rs)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    return start.elapsed_time(end)
+
+
 def run_ours(args, rank, world, dev, dist):
     import delta_rule_recurrent_chunkwise_gb300 as la
     la.build()
@@ -303,9 +349,17 @@ def run_ours(args, rank, world, dev, dist):
             o_host.copy_(pf.o, non_blocking=True)
 
         e2e_ms = time_steps(e2e_step, max(3, args.steps // 2), 2, None, stream, barrier)
-        e2e_total = mor(sum(e2e_ms))
-        result["e2e"] = {"value": job_throughput(w.ntok * len(e2e_ms), world, e2e_total),
-                         "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        serial_total = mor(sum(e2e_ms))
+        n_e2e = max(4, args.steps)
+        pipe_ms = mor(e2e_pipelined(la, pf, host, stream, n_e2e, barrier))
+        result["e2e"] = {"value": job_throughput(w.ntok * n_e2e, world, pipe_ms),
+                         "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                         "steps": n_e2e,
+                         "schedule": "every step copies its inputs in from pinned host memory and "
+                                     "its output back; copy-in, compute and copy-out run on three "
+                                     "streams over two device buffer sets, so step i+1's copy-in "
+                                     "and step i-1's copy-out overlap step i",
+                         "serial_value": job_throughput(w.ntok * len(e2e_ms), world, serial_total)}
         del pf
 
         if not args.headline_only:
