@@ -31,10 +31,13 @@
 //   col factor  prod_{t=i+1}^{start(R)-1} alpha_t   for i < start(R)   (<= 1)
 //               1 / prod_{t=start(R)}^{i} alpha_t   for i in R         (>= 1)
 // so one tensor-core product per block R (the columns of K scaled for R)
-// gives the rows of A and Aq that belong to R.  The reciprocal column factor
-// spans at most 16 tokens; it is exact while that 16-token decay of a
-// channel stays above ~1e-30 (mean alpha above ~0.013), and is clamped
-// (never inf/NaN) beyond.
+// gives the rows of A and Aq that belong to R.  Keys of earlier blocks are
+// decayed to the end of their block by suffix products (<= 1), so only a
+// key's own block uses the reciprocal 1/P; that stays exact while the
+// channel's 16-token decay stays above 1e-36.  Channels below it ("strong",
+// fast forgetting) contribute zero to the tensor-core product and get their
+// own-block scores from an exact CUDA-core pass (running products of alpha,
+// taken only for tasks that have such a channel).
 //
 // Mapping: a persistent grid walks the (chunk slot, head) tasks; the next
 // task's raw q, k, v, gate tiles arrive by TMA while the current one
@@ -104,7 +107,11 @@ struct Layout {
     static constexpr uint32_t SLB = GEND + 4 * D;              // fp32 [64]
     static constexpr uint32_t SEB = SLB + 256;                 // fp32 [64]
     static constexpr uint32_t SEK = SEB + 256;                 // fp32 [64]
-    static constexpr uint32_t INFO = SEK + 256;                // int4: next task
+    // gated: exact own-block scores of fast-decaying channels (Aq part, then
+    // K K^T part, [4][16][16] each) and the flag that some channel needs them
+    static constexpr uint32_t DIAG = SEK + 256;
+    static constexpr uint32_t SFLAG = DIAG + (GATED ? 2u * 4u * 256u * 4u : 0u);
+    static constexpr uint32_t INFO = SFLAG + 16;               // int4: next task
     static constexpr uint32_t BAR_TMA = INFO + 16;             // mbarrier: raw tiles
     static constexpr uint32_t TASK_BYTES = (BAR_TMA + 8 + 1023) & ~1023u;
     static_assert(UK - WQ == Record<D>::UK, "record image");
@@ -157,6 +164,56 @@ __device__ __forceinline__ void store_c(float *Cp, int ldc, const float (&d)[4],
     Cp[(g + 8) * ldc + 2 * t + 1] = sign * d[3];
 }
 
+// Exact own-block scores for the fast-decaying ("strong") channels of a
+// gated chunk: warp w takes block R = w / (D/32) and channels
+// 32 (w % (D/32)) + lane; for i <= r in the block it adds
+//   sum_c q^_rc k^_ic prod_{t=i+1}^{r} alpha_tc   (Aq part, sDiag[0..1023])
+//   sum_c k^_rc k^_ic prod_{t=i+1}^{r} alpha_tc   (A part,  sDiag[1024..])
+// over the warp's strong channels, the decay as a running product down each
+// column (factors <= 1).  Out of line: it runs only for chunks that have such
+// a channel and must not raise the register count of the common path.
+template <int D>
+__device__ __noinline__ void exact_own_block(const uint8_t *rawq, const uint8_t *rawk,
+                                             const uint8_t *rawg, const float *sqn,
+                                             const float *skn, const float *sE, float *sDiag,
+                                             int lw, int lane, int len, bool silu) {
+    constexpr int CG = D / 32;
+    const int R = lw / CG, c = 32 * (lw % CG) + lane;
+    const bool st = sE[R * D + c] < 1e-36f;
+    if (!__any_sync(0xffffffffu, st)) return;
+    float al[16], kh[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        const int row = 16 * R + r;
+        const uint32_t o = tile::rs_off(tile::C, row, c);
+        const float g = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(rawg + o));
+        float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(rawk + o));
+        if (silu) kv = kv / (1.0f + expf(-kv));
+        al[r] = row < len ? decay_f(g) : 1.0f;
+        kh[r] = kv * skn[row];
+    }
+    float *dq = sDiag + R * 256, *dk = sDiag + 1024 + R * 256;
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i) {
+        float pr = st ? kh[i] : 0.0f;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            if (r < i) continue;
+            if (r > i) pr *= al[r];
+            const int row = 16 * R + r;
+            float qv = __bfloat162float(
+                *reinterpret_cast<const __nv_bfloat16 *>(rawq + tile::rs_off(tile::C, row, c)));
+            if (silu) qv = qv / (1.0f + expf(-qv));
+            const float sq = warp_sum(qv * sqn[row] * pr);
+            const float sk = warp_sum(kh[r] * pr);
+            if (lane == 0) {
+                atomicAdd(&dq[r * 16 + i], sq);
+                atomicAdd(&dk[r * 16 + i], sk);
+            }
+        }
+    }
+}
+
 struct IntraParams {
     const __nv_bfloat16 *beta_logits;
     const __nv_bfloat16 *gate_scalar;  // [ntok][H] with a scalar gate (ungated kernel), else null
@@ -204,6 +261,8 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
     float *sLb = reinterpret_cast<float *>(sm + L::SLB);
     float *sEb = reinterpret_cast<float *>(sm + L::SEB);
     float *sEk = reinterpret_cast<float *>(sm + L::SEK);
+    float *sDiag = reinterpret_cast<float *>(sm + L::DIAG);
+    int *sflag = reinterpret_cast<int *>(sm + L::SFLAG);
     static_assert(!(GATED && SCALAR), "a scalar gate uses the ungated layout");
     constexpr bool scalar = SCALAR;
     uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + L::BAR_TMA);
@@ -354,6 +413,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
             tc_fence_after();
         }
         // ---------------------------------------------- A0: beta, row norms
+        if (GATED && ltid == 0) *sflag = 0;
         if (ltid < C)
             sbeta[ltid] = ltid >= len ? 0.0f : additive ? 1.0f : __fdividef(1.0f, 1.0f + __expf(-beta_cur));
         if (scalar && ltid < C) sLb[ltid] = ltid < len ? log_decay_f(gate_cur) : 0.0f;  // log alpha
@@ -454,10 +514,10 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
         } else {
             // One thread per (2 key channels, 8 rows of a 16-token block R); the
             // two 8-row halves of a block sit in lanes l and l^16 of one warp.
-            // alpha = 1/(1+e^g), 1/alpha = 1+e^g; P = prefix product of alpha
-            // inside the block, Pi = 1/P.  Every operand is (q or k) x (P or Pi)
-            // x a per-(block, channel) constant; the within-block suffix is
-            // prod_{t>r} alpha_t = E_R / P_r with E_R the block total.
+            // alpha = 1/(1+e^g); P = prefix product of alpha inside the block,
+            // Sf = suffix product prod_{t>r} alpha_t inside the block.  Every
+            // operand is (q or k) x (P, Sf or, for a key's own block, 1/P) x a
+            // per-(block, channel) product of block totals.
             static_assert(NW * 8 >= D, "one thread per (channel pair, 8 rows)");
             const bool act = lw < D / 8;
             const int R = (lw * 32 / D) & 3, grp = lw % (D / 32);
@@ -475,11 +535,14 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
             uint32_t swz[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) swz[j] = ((ch ^ (uint32_t)j) << 4) + ((uint32_t)c0 & 7u) * 2u;
-            float P[8][2], Pi[8][2];
+            float P[8][2], Sf[8][2];
 #pragma unroll
-            for (int rho = 0; rho < 8; ++rho) { P[rho][0] = P[rho][1] = 1.0f; Pi[rho][0] = Pi[rho][1] = 1.0f; }
+            for (int rho = 0; rho < 8; ++rho) {
+                P[rho][0] = P[rho][1] = 1.0f;
+                Sf[rho][0] = Sf[rho][1] = 1.0f;
+            }
             if (act) {
-                float p0 = 1.0f, p1 = 1.0f, q0 = 1.0f, q1 = 1.0f;
+                float p0 = 1.0f, p1 = 1.0f, a[8][2];
 #pragma unroll
                 for (int rho = 0; rho < 8; ++rho) {
                     // the scan runs in natural row order (a prefix product);
@@ -488,28 +551,33 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
                     const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162 *>(rawg + cboff64 + r * 128 + swz[rho]);
                     const float2 g = __bfloat1622float2(g2);
                     const float e0 = __expf(fminf(g.x, 80.0f)), e1 = __expf(fminf(g.y, 80.0f));
+                    a[rho][0] = a[rho][1] = 1.0f;
                     if (r < len) {
-                        p0 *= __fdividef(1.0f, 1.0f + e0);
-                        p1 *= __fdividef(1.0f, 1.0f + e1);
-                        q0 = fminf(q0 * (1.0f + e0), 1e30f);
-                        q1 = fminf(q1 * (1.0f + e1), 1e30f);
+                        a[rho][0] = __fdividef(1.0f, 1.0f + e0);
+                        a[rho][1] = __fdividef(1.0f, 1.0f + e1);
+                        p0 *= a[rho][0];
+                        p1 *= a[rho][1];
                     }
-                    P[rho][0] = p0; P[rho][1] = p1; Pi[rho][0] = q0; Pi[rho][1] = q1;
+                    P[rho][0] = p0; P[rho][1] = p1;
+                }
+                // within-half suffix products prod_{t > r} alpha_t (<= 1)
+#pragma unroll
+                for (int rho = 6; rho >= 0; --rho) {
+                    Sf[rho][0] = Sf[rho + 1][0] * a[rho + 1][0];
+                    Sf[rho][1] = Sf[rho + 1][1] * a[rho + 1][1];
                 }
             }
             // carry the first half's totals into the second half
             {
                 const float t0 = __shfl_sync(0xffffffffu, P[7][0], lane ^ 16);
                 const float t1 = __shfl_sync(0xffffffffu, P[7][1], lane ^ 16);
-                const float u0 = __shfl_sync(0xffffffffu, Pi[7][0], lane ^ 16);
-                const float u1 = __shfl_sync(0xffffffffu, Pi[7][1], lane ^ 16);
                 if (hf2) {
 #pragma unroll
-                    for (int rho = 0; rho < 8; ++rho) {
-                        P[rho][0] *= t0; P[rho][1] *= t1;
-                        Pi[rho][0] = fminf(Pi[rho][0] * u0, 1e30f);
-                        Pi[rho][1] = fminf(Pi[rho][1] * u1, 1e30f);
-                    }
+                    for (int rho = 0; rho < 8; ++rho) { P[rho][0] *= t0; P[rho][1] *= t1; }
+                } else {
+                    // first half: the suffix runs on through the second half
+#pragma unroll
+                    for (int rho = 0; rho < 8; ++rho) { Sf[rho][0] *= t0; Sf[rho][1] *= t1; }
                 }
             }
             if (act && hf2) {
@@ -518,22 +586,32 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
             }
             __syncthreads();
             if (act) {
-                float Gb[2], EaK[2], mt[3][2];
+                // Gb: decay of the blocks before R; Ea: of the blocks after R;
+                // mt[t]: of blocks R+1 .. R+t (keys of R used by block R+1+t).
+                // A channel whose block total falls below 1e-36 ("strong")
+                // gets its own-block scores from the exact path instead.
+                float Gb[2], Ea[2], mt[3][2], invE[2];
+                bool strong[2];
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int c = c0 + j;
                     const float E0 = sE[c], E1 = sE[D + c], E2 = sE[2 * D + c], E3 = sE[3 * D + c];
                     Gb[j] = R == 0 ? 1.0f : R == 1 ? E0 : R == 2 ? E0 * E1 : E0 * E1 * E2;
-                    EaK[j] = R == 0 ? E0 * E1 * E2 * E3 : R == 1 ? E1 * E2 * E3 : R == 2 ? E2 * E3 : E3;
+                    Ea[j] = R == 0 ? E1 * E2 * E3 : R == 1 ? E2 * E3 : R == 2 ? E3 : 1.0f;
                     float m = 1.0f;
 #pragma unroll
                     for (int t = 0; t < 3; ++t) {
-                        const int Rt = R + t;
-                        m *= Rt == 0 ? E0 : Rt == 1 ? E1 : Rt == 2 ? E2 : E3;
                         mt[t][j] = m;
+                        const int Rt = R + 1 + t;
+                        m *= Rt == 1 ? E1 : Rt == 2 ? E2 : Rt == 3 ? E3 : 1.0f;
                     }
+                    const float ER = sE[R * D + c];
+                    strong[j] = ER < 1e-36f;
+                    // 1/P_r = Sf_r / E_R: one reciprocal per channel
+                    invE[j] = strong[j] ? 0.0f : __fdividef(1.0f, ER);
                     if (R == 0 && hf2 == 0) sgend[c] = E0 * E1 * E2 * E3;
                 }
+                if (strong[0] || strong[1]) atomicOr(sflag, 1);
                 auto st2 = [](uint8_t *p, float a, float b) {
                     *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(a, b);
                 };
@@ -549,7 +627,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
 #pragma unroll
                         for (int j = 0; j < 2; ++j) {
                             float t = P[rho][j]; P[rho][j] = P[rho + 4][j]; P[rho + 4][j] = t;
-                            t = Pi[rho][j]; Pi[rho][j] = Pi[rho + 4][j]; Pi[rho + 4][j] = t;
+                            t = Sf[rho][j]; Sf[rho][j] = Sf[rho + 4][j]; Sf[rho + 4][j] = t;
                         }
                     }
                 }
@@ -567,18 +645,22 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
                     qv.x *= qn; qv.y *= qn; kv.x *= kn; kv.y *= kn;
                     const float a0 = qv.x * P[rho][0], a1 = qv.y * P[rho][1];     // Q^
                     const float b0 = kv.x * P[rho][0], b1 = kv.y * P[rho][1];     // K^
-                    const float k0 = kv.x * Pi[rho][0], k1 = kv.y * Pi[rho][1];   // K_R own block
+                    // keys decayed to the end of their block (suffix, <= 1)
+                    const float s0 = kv.x * Sf[rho][0], s1 = kv.y * Sf[rho][1];
+                    // K_R own block: k / P = k Sf / E_R (E_R >= 1e-36 keeps it in
+                    // range); zero for strong channels
+                    const float k0 = s0 * invE[0], k1 = s1 * invE[1];
                     st2(p_qh + o, a0, a1);
                     st2(p_kh + o, b0, b1);
                     st2(p_qg + o, a0 * Gb[0], a1 * Gb[1]);                  // Q e^b
-                    st2(p_kt + o, k0 * EaK[0], k1 * EaK[1]);                // K e^{b_end-b}
+                    st2(p_kt + o, s0 * Ea[0], s1 * Ea[1]);                  // K e^{b_end-b}
                     st2(p_bk + o, be * b0 * Gb[0], be * b1 * Gb[1]);        // beta K e^b
                     st2(p_kr + (uint32_t)(8 * R * (R + 1)) * 128u + o, k0, k1);
 #pragma unroll
                     for (int t = 0; t < 3; ++t) {
                         const int R2 = R + 1 + t;
                         if (R2 < 4)
-                            st2(p_kr + (uint32_t)(8 * R2 * (R2 + 1)) * 128u + o, k0 * mt[t][0], k1 * mt[t][1]);
+                            st2(p_kr + (uint32_t)(8 * R2 * (R2 + 1)) * 128u + o, s0 * mt[t][0], s1 * mt[t][1]);
                     }
                 }
             }
@@ -595,6 +677,21 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
             }
         }
         phase_sync();
+        if constexpr (GATED) {
+            // Exact own-block scores of the channels whose 16-token block decay
+            // fell below 1e-36 (their 1/P factor would leave the fp32 range):
+            // sum_c q^_rc k^_ic prod_{t=i+1}^{r} alpha_tc for i <= r in one
+            // block, with the decay as a running product down each column
+            // (every factor <= 1).  One warp per (block, 32 channels); the
+            // tensor-core product holds zero for these channels.
+            if (*sflag) {
+                for (int u = ltid; u < 2048; u += NTC) sDiag[u] = 0.0f;
+                __syncthreads();
+                if (lw < 4 * (D / 32))
+                    exact_own_block<D>(rawq, rawk, rawg, sqn, skn, sE, sDiag, lw, lane, len, silu);
+                __syncthreads();
+            }
+        }
         // raw tiles consumed: fetch the next task's while this one computes
         if (leader) {
             const int4 nxt = task_info(g_next * P + kslot, nxt_e);
@@ -648,6 +745,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
             const int rb0 = 32 * (is_q ? qd : qd - 2);
             const int r = rb0 + lane, R = r >> 4;
             const int Rw = rb0 >> 4;
+            const bool diag_on = GATED && *sflag != 0;
             auto colof = [](int Rb) { return GATED ? 8 * Rb * (Rb + 1) : 0; };
 #pragma unroll
             for (int sub = 0; sub < 16 / NW; ++sub) {
@@ -660,6 +758,12 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
                     tmem_ld16(tq + TC_A + colof(Rw + 1) + col, w1);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) v[i] = (R == Rw) ? w0[i] : w1[i];
+                    if (diag_on && (col >> 4) == R) {
+                        // own block of row r: add the exact part of strong channels
+                        const float *dg = sDiag + (is_q ? 0 : 1024) + R * 256 + (r & 15) * 16;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] += dg[i];
+                    }
                 } else {
                     tmem_ld16(tq + TC_A + col, v);
                     if (scalar) {
