@@ -48,7 +48,7 @@
 // phases; otherwise one CTA of 512 threads per SM.  Products on tcgen05 (bf16 x bf16
 // -> fp32 in TMEM): [Q;K]-hat x K_R^T (one N = 160 product when gated) and
 // T x [beta K e^b | beta V] (one N = 2D product).  The triangular solve runs
-// in fp32 on CUDA cores: the four diagonal 16x16 blocks by warp-shuffle
+// in fp32 on CUDA cores: the four diagonal 16x16 blocks by column-wise
 // forward substitution, the off-diagonal blocks by warp-level TF32 products.
 // The finished operands leave as one record per task by bulk copies.
 
