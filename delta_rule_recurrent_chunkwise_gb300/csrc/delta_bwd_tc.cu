@@ -56,6 +56,17 @@ __device__ __forceinline__ void mma8(float (&d)[4], const uint32_t (&a)[4], uint
 
 __device__ __forceinline__ uint32_t bits(float x) { return __float_as_uint(x); }
 
+// Four 8 x 4 fp32 blocks of shared memory in one instruction: ldmatrix moves
+// 8 x 8 blocks of 16-bit pairs, i.e. 8 rows x 16 bytes, and gives lane
+// (g, t) = (lane / 4, lane % 4) the 32-bit word in row g, column t of each
+// block -- the TF32 fragment layout.  p: this lane's row address (16-byte
+// aligned); lanes 8j .. 8j + 7 address the rows of block j.
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const float *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+}
+
 // Zero structure a product can skip: op(A) lower (entries k > m are zero) or
 // upper (k < m), op(B) upper (k > n), and outputs wanted only on or below the
 // diagonal (blocks above it are left unwritten).
@@ -85,14 +96,28 @@ __device__ __forceinline__ void mm(float *Cm, const float *A, const float *B, fl
         if ((SHAPE & kBUpper) && n0 + 16 < khi) khi = n0 + 16;
         const float *Ap = A + (m0 + g) * AM + t * AK;
         const float *Bp = B + t * BK + (n0 + g) * BN;
+        // ldmatrix row addresses: A row-major (k contiguous), B stored as B^T
+        const float *Al = A + (m0 + (lane & 15)) * LDA + (lane >> 4) * 4;
+        const float *Bl = B + (n0 + (lane & 7) + ((lane >> 4) << 3)) * LDB + ((lane >> 3) & 1) * 4;
         float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int k0 = 0; k0 < K; k0 += 8) {
             if (k0 < klo || k0 >= khi) continue;
-            const uint32_t a[4] = {bits(Ap[k0 * AK]), bits(Ap[8 * AM + k0 * AK]),
-                                   bits(Ap[(k0 + 4) * AK]), bits(Ap[8 * AM + (k0 + 4) * AK])};
-            mma8(d0, a, bits(Bp[k0 * BK]), bits(Bp[(k0 + 4) * BK]));
-            mma8(d1, a, bits(Bp[k0 * BK + 8 * BN]), bits(Bp[(k0 + 4) * BK + 8 * BN]));
+            uint32_t a[4], b[4];
+            if constexpr (!TA) {
+                ldsm_x4(a, Al + k0);
+            } else {
+                a[0] = bits(Ap[k0 * AK]); a[1] = bits(Ap[8 * AM + k0 * AK]);
+                a[2] = bits(Ap[(k0 + 4) * AK]); a[3] = bits(Ap[8 * AM + (k0 + 4) * AK]);
+            }
+            if constexpr (TB) {
+                ldsm_x4(b, Bl + k0);
+            } else {
+                b[0] = bits(Bp[k0 * BK]); b[1] = bits(Bp[(k0 + 4) * BK]);
+                b[2] = bits(Bp[k0 * BK + 8 * BN]); b[3] = bits(Bp[(k0 + 4) * BK + 8 * BN]);
+            }
+            mma8(d0, a, b[0], b[1]);
+            mma8(d1, a, b[2], b[3]);
         }
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
