@@ -61,6 +61,10 @@ __device__ __forceinline__ uint32_t bits(float x) { return __float_as_uint(x); }
 // (g, t) = (lane / 4, lane % 4) the 32-bit word in row g, column t of each
 // block -- the TF32 fragment layout.  p: this lane's row address (16-byte
 // aligned); lanes 8j .. 8j + 7 address the rows of block j.
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
+}
+
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const float *p) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -325,6 +329,28 @@ __global__ void __launch_bounds__(kGradNT, 1) delta_bwd_chunk_kernel(ChunkParams
         }
     };
 
+    // The next task's inputs (q, k, v, dO rows and the two 16 KB states) are
+    // prefetched into L2 while this task computes, one 128-byte line per
+    // thread, so its staging phase reads L2 rather than DRAM.
+    auto prefetch_task = [&](int64_t nt) {
+        if (nt >= p.n_tasks) return;
+        const int64_t ns = nt / H;
+        const int nh = (int)(nt % H);
+        const int2 e = p.table[ns];
+        if (e.y <= 0 || e.y > 64) return;
+        if (tid < 256) {
+            const int r = tid & 63, which = tid >> 6;
+            if (r < e.y) {
+                const __nv_bfloat16 *base = which == 0 ? p.q : which == 1 ? p.k : which == 2 ? p.v : p.d_o;
+                prefetch_l2(base + ((int64_t)(e.x + r) * H + nh) * 64);
+            }
+        } else {
+            const int v = tid - 256;  // 128 lines of each state
+            prefetch_l2((v < 128 ? p.states : p.dstates) + (ns * H + nh) * 4096 + (v & 127) * 32);
+        }
+    };
+    static_assert(kGradNT == 512, "one prefetched line per thread");
+
     for (int64_t task = blockIdx.x; task < p.n_tasks; task += gridDim.x) {
         const int64_t slot = task / H;
         h = (int)(task % H);
@@ -387,6 +413,7 @@ __global__ void __launch_bounds__(kGradNT, 1) delta_bwd_chunk_kernel(ChunkParams
         if (tid < 64) sDEB[tid] = sDEBL[tid] = sDB[tid] = sDBeta[tid] = 0.0f;
         if (tid == 0) sDEBLs[0] = 0.0f;
         __syncthreads();
+        prefetch_task(task + gridDim.x);
         if (w == 0) {
             // b = inclusive cumulative log decay; e^b and e^{b_L - b} (exponents <= 0)
             float v0 = sB[lane], v1 = sB[lane + 32];
