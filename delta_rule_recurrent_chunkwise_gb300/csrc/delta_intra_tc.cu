@@ -532,9 +532,9 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
             const uint32_t cb = (uint32_t)c0 >> 6, ch = ((uint32_t)c0 >> 3) & 7u;
             const uint32_t cboff64 = cb * 64u * 128u, cboff128 = cb * 128u * 128u,
                            cboff160 = cb * 160u * 128u;
-            uint32_t swz[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) swz[j] = ((ch ^ (uint32_t)j) << 4) + ((uint32_t)c0 & 7u) * 2u;
+            // byte offset of the channel pair in row phase j (the 16-byte chunk
+            // index is XOR-ed with the row's swizzle phase)
+            auto swz = [&](int j) { return ((ch ^ (uint32_t)j) << 4) + ((uint32_t)c0 & 7u) * 2u; };
             float P[8][2], Sf[8][2];
 #pragma unroll
             for (int rho = 0; rho < 8; ++rho) {
@@ -548,7 +548,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
                     // the scan runs in natural row order (a prefix product);
                     // only the store pass below uses the permuted order
                     const int r = r0 + rho;
-                    const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162 *>(rawg + cboff64 + r * 128 + swz[rho]);
+                    const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162 *>(rawg + cboff64 + r * 128 + swz(rho));
                     const float2 g = __bfloat1622float2(g2);
                     const float e0 = __expf(fminf(g.x, 80.0f)), e1 = __expf(fminf(g.y, 80.0f));
                     a[rho][0] = a[rho][1] = 1.0f;
@@ -612,13 +612,17 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
                     if (R == 0 && hf2 == 0) sgend[c] = E0 * E1 * E2 * E3;
                 }
                 if (strong[0] || strong[1]) atomicOr(sflag, 1);
-                auto st2 = [](uint8_t *p, float a, float b) {
-                    *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(a, b);
+                // 32-bit shared-memory addresses keep the six destinations in
+                // six registers (generic pointers would take twelve)
+                auto st2 = [](uint32_t a, float x, float y) {
+                    const __nv_bfloat162 v = __floats2bfloat162_rn(x, y);
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(*reinterpret_cast<const uint32_t *>(&v))
+                                 : "memory");
                 };
                 uint8_t *const pq_raw = rawq + cboff64, *const pk_raw = rawk + cboff64;
-                uint8_t *const p_qh = qkh + cboff128, *const p_kh = qkh + cboff128 + 64 * 128;
-                uint8_t *const p_qg = wq + cboff128 + 64 * 128, *const p_kt = uk + cboff128 + 64 * 128;
-                uint8_t *const p_bk = wq + cboff128, *const p_kr = kr + cboff160;
+                const uint32_t p_qh = smem_u32(qkh) + cboff128, p_kh = smem_u32(qkh) + cboff128 + 64 * 128;
+                const uint32_t p_qg = smem_u32(wq) + cboff128 + 64 * 128, p_kt = smem_u32(uk) + cboff128 + 64 * 128;
+                const uint32_t p_bk = smem_u32(wq) + cboff128, p_kr = smem_u32(kr) + cboff160;
                 // second-half lanes: swap register rows rho <-> rho ^ 4 so the
                 // store pass can index P[rho] with a compile-time rho
                 if (pr) {
