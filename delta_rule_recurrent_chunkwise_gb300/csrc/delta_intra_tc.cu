@@ -244,6 +244,10 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
     // this thread's task slot in the CTA, its warp and thread index within it
     const int kslot = warp / NW, lw = warp % NW, ltid = tid % NTC;
     const bool leader = ltid == 0;
+    // issues the next task's raw-tile loads in the middle of a task (thread 0
+    // issues the first tensor-core product right then; the loads' proxy fence
+    // would hold it up)
+    const bool fetcher = ltid == 32;
     uint8_t *sm = sbase + kslot * L::TASK_BYTES;
     uint8_t *rawq = sm + L::RAW_Q, *rawk = sm + L::RAW_K, *rawv = sm + L::RAW_V,
             *rawg = sm + L::RAW_G;
@@ -347,7 +351,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
     grid_wait_prerequisites();
     grid_launch_dependents();
     int4 cur = task_info(g * P + kslot, table_entry(g * P + kslot));
-    bool tma_pending = false;  // meaningful in the leader
+    bool tma_pending = false;  // meaningful in the leader, who waits for the loads
     if (leader && cur.y > 0) {
         issue_tma(cur.x, cur.z);
         tma_pending = true;
@@ -376,7 +380,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
     while (g < n_groups) {
         const int64_t g_next = g + gridDim.x;
         int2 nxt_e = make_int2(0, 0);
-        if (leader) nxt_e = table_entry(g_next * P + kslot);  // decoded after the operand stage
+        if (leader || fetcher) nxt_e = table_entry(g_next * P + kslot);  // decoded after the operand stage
         // one task per CTA: cur is the same in every thread
         const bool any_task = P == 1 ? cur.y > 0 : __syncthreads_or(cur.y > 0);
         if (!any_task) {
@@ -697,13 +701,10 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
             }
         }
         // raw tiles consumed: fetch the next task's while this one computes
-        if (leader) {
+        if (fetcher) {
             const int4 nxt = task_info(g_next * P + kslot, nxt_e);
             *sinfo = nxt;
-            if (nxt.y > 0) {
-                issue_tma(nxt.x, nxt.z);
-                tma_pending = true;
-            }
+            if (nxt.y > 0) issue_tma(nxt.x, nxt.z);
         }
         // ---------------------------------------------- B: block products
         // Issue loops are kept rolled and short: this code runs on one thread,
@@ -731,7 +732,13 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
             }
             mma_commit(bar_mma);
         }
-        if (__syncthreads_or(!mma_wait())) { failed = true; break; }
+        {
+            const bool mma_failed = __syncthreads_or(!mma_wait());
+            // the fetcher's loads are visible to the leader now, who must wait
+            // for them before leaving, whatever happens next
+            tma_pending = sinfo->y > 0;
+            if (mma_failed) { failed = true; break; }
+        }
         tc_fence_after();
         // the next task is known to every thread now: prefetch its beta
         const int4 nx = *sinfo;
