@@ -343,7 +343,8 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
 
     // The CTA takes task groups g = blockIdx.x, + gridDim.x, ...; task slot
     // kslot of group g is task g * P + kslot.  Each task's leader thread
-    // issues and waits for its raw tiles and stores its record.
+    // waits for its raw tiles and issues its products; the fetcher issues the
+    // next task's raw-tile loads and stores the record.
     const int64_t n_groups = (p.n_tasks + P - 1) / P;
     int64_t g = blockIdx.x;
     // the chunk table comes from the previous launch; the inter-chunk kernel
@@ -449,7 +450,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
                 sqn[r] = valid ? (l2q ? rsqrtf(fmaxf(ssq, 1e-24f)) : 1.0f) : 0.0f;
             }
         }
-        if (leader) bulk_wait_read();  // previous record's sources are rewritten below
+        if (fetcher) bulk_wait_read();  // previous record's sources are rewritten below
         __syncthreads();
         // ---------------------------------------------- A1: operand tiles
         if (!GATED) {
@@ -939,7 +940,9 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
         }
         phase_sync();
         // ---------------------------------------------- F: record out
-        if (leader && len > 0) {
+        // (by the fetcher, so that the leader goes straight on to the next
+        // task's raw tiles)
+        if (fetcher && len > 0) {
             uint8_t *rec = p.records + ((int64_t)cur.w * H + h) * Rec::BYTES;
             bulk_store_hint(rec + Rec::WQ, wq, 4 * L::tile64, pol);
             bulk_store_hint(rec + Rec::AQ, aqk, 8192, pol);
@@ -952,10 +955,8 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
         g = g_next;
     }
 
-    if (leader) {
-        if (failed && tma_pending) mbar_wait(bar_tma, tma_par, p.err, 3);
-        bulk_wait_all();
-    }
+    if (leader && failed && tma_pending) mbar_wait(bar_tma, tma_par, p.err, 3);
+    if (fetcher) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
