@@ -8,7 +8,9 @@ the library is not built, the first call raises.
 
 Functions (same names as the C ABI):
   la_prefill_linear, la_prefill_delta, la_prefill_delta_workspace_size,
-  la_prefill_delta_static, la_decode_step, la_check_device, la_status_string.
+  la_prefill_delta_static, la_decode_step, la_decode_step_slots,
+  la_backward_delta, la_check_device, la_selftest_wait_timeout,
+  la_status_string.
 """
 from __future__ import annotations
 
@@ -26,7 +28,7 @@ LA_L2NORM_K, LA_L2NORM_Q, LA_SILU_QK, LA_GATE_SCALAR, LA_ADDITIVE = 1, 2, 4, 8, 
 EXPORTED = ("la_prefill_linear", "la_prefill_delta", "la_prefill_delta_workspace_size",
             "la_prefill_delta_static", "la_decode_step", "la_decode_step_slots",
             "la_backward_delta", "la_backward_delta_workspace_size", "la_check_device",
-            "la_status_string")
+            "la_selftest_wait_timeout", "la_status_string")
 
 
 class LinAttnError(RuntimeError):
@@ -64,11 +66,12 @@ def library():
         lib.la_backward_delta_workspace_size.argtypes = [ip, ip, ip, ip, ip]
         lib.la_backward_delta_workspace_size.restype = sz
         lib.la_check_device.argtypes = [vp]
+        lib.la_selftest_wait_timeout.argtypes = [vp]
         lib.la_status_string.argtypes = [ip]
         lib.la_status_string.restype = ctypes.c_char_p
         for f in ("la_prefill_linear", "la_prefill_delta", "la_prefill_delta_static",
                   "la_decode_step", "la_decode_step_slots", "la_backward_delta",
-                  "la_check_device"):
+                  "la_check_device", "la_selftest_wait_timeout"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -289,3 +292,11 @@ def la_decode_step_slots(q, k, v, beta_logits, gate_logits, o, state_pool, state
 def la_check_device(stream=None) -> int:
     """Synchronise the stream and return (and clear) any device-side error."""
     return int(library().la_check_device(_stream(stream)))
+
+
+def la_selftest_wait_timeout(stream=None) -> None:
+    """Launch the failure-path self-test (a bounded in-kernel wait that runs
+    out); the next la_check_device reports LA_ERR_TIMEOUT."""
+    rc = library().la_selftest_wait_timeout(_stream(stream))
+    if rc != LA_OK:
+        raise LinAttnError(rc, "la_selftest_wait_timeout")

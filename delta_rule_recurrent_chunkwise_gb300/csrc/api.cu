@@ -7,8 +7,22 @@
 
 #include "../../include/linattn.h"
 #include "launch.h"
+#include "tc.cuh"
 
 namespace {
+
+// Waits on an mbarrier that nothing arrives on: the bounded wait every
+// kernel of the library uses runs out, records its code in the device error
+// word and returns, and the kernel ends normally.
+__global__ void wait_selftest_kernel(unsigned *err) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        la::tc::mbar_init(&bar, 1);
+        la::tc::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) la::tc::mbar_wait(&bar, 0, err, 99u);
+}
 
 bool head_size_ok(int d) { return d == 64 || d == 128; }
 
@@ -185,6 +199,13 @@ la_status la_backward_delta(const void *q, const void *k, const void *v, const v
                   H, dk, dv, scale, flags, dq, dk_out, dv_out, d_beta_logits, d_gate_logits,
                   d_init_S, workspace, io == LA_BF16};
     return from_cuda(la::launch_delta_backward(a, static_cast<cudaStream_t>(stream)));
+}
+
+la_status la_selftest_wait_timeout(void *stream) {
+    unsigned *err = la::device_error_word();
+    if (!err) return LA_ERR_CUDA;
+    wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(err);
+    return from_cuda(cudaGetLastError());
 }
 
 la_status la_check_device(void *stream) {

@@ -65,9 +65,11 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Spin limit for every wait: each try_wait already blocks for a
-// hardware-chosen interval, so this bounds a wait to well under a second.
-constexpr uint32_t kSpinLimit = 1u << 22;
+// Spin limit for every wait.  A try_wait on a phase that does not complete
+// blocks for a hardware-chosen interval before giving up, ~4 us on GB300
+// (2^22 of them measured ~16 s), so 2^18 bounds a wait to about a second;
+// no wait of the library legitimately lasts more than milliseconds.
+constexpr uint32_t kSpinLimit = 1u << 18;
 
 // Waits for the phase with the given parity to complete.  Returns false
 // (after recording `code` in *err) if it does not complete in time.

@@ -227,6 +227,15 @@ la_status la_backward_delta(const void *q, const void *k, const void *v, const v
  * or a state slot out of range, LA_ERR_CUDA for a CUDA error, else LA_OK. */
 la_status la_check_device(void *stream);
 
+/* Self-test of the failure path (no computation): launches one kernel on
+ * `stream` that waits on an mbarrier nothing ever completes.  The wait is
+ * bounded like every in-kernel wait of the library; when it runs out (well
+ * under a second) the kernel records a timeout in the device error word and
+ * ends normally, so the next la_check_device returns LA_ERR_TIMEOUT and the
+ * context stays usable.  Returns LA_ERR_CUDA if the launch fails, else
+ * LA_OK (the timeout itself is reported by la_check_device). */
+la_status la_selftest_wait_timeout(void *stream);
+
 /* Static, human-readable name of a status code. */
 const char *la_status_string(la_status s);
 
