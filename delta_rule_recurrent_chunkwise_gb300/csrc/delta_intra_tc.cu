@@ -217,11 +217,11 @@ __device__ __noinline__ void exact_own_block(const uint8_t *rawq, const uint8_t 
 struct IntraParams {
     const __nv_bfloat16 *beta_logits;
     const __nv_bfloat16 *gate_scalar;  // [ntok][H] with a scalar gate (ungated kernel), else null
-    const int2 *table;      // [slots] {first token, length}
+    const int32_t *cu_seqlens;         // [N + 1]
     uint8_t *records;       // [slots][H] records
     unsigned *err;
     int64_t n_tasks;        // slots * H
-    int H, ntok;
+    int N, H, ntok;
     unsigned flags;
 };
 
@@ -304,11 +304,31 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
     auto task_tmem = [&](int kk) { return tmem + kk * L::TCOLS; };
 
     // Task t = slot * H + head.  {first token, length, head, slot}; length 0
-    // marks a slot no chunk occupies (or a table entry out of range).  The
-    // table entry is fetched (table_entry) well before it is decoded
-    // (task_info), so the load's latency stays off the critical path.
+    // marks a slot no chunk occupies (or an entry out of range).  Sequence n
+    // owns slots f(n) .. f(n) + nc(n) - 1, f(n) = cu[n] / 64 + n (f grows
+    // by at least nc(n) from one sequence to the next, so slots never
+    // collide): a slot's sequence is the last n with f(n) <= slot, found by
+    // binary search over cu_seqlens.  The entry is looked up (table_entry)
+    // a task ahead of its decoding (task_info), so the loads' latency stays
+    // off the critical path.
     auto table_entry = [&](int64_t t) -> int2 {
-        return t < p.n_tasks ? p.table[t / H] : make_int2(0, 0);
+        const int2 none = make_int2(0, 0);
+        if (t >= p.n_tasks || p.N < 1) return none;
+        const int64_t slot = t / H;
+        auto f = [&](int n) { return (int64_t)(p.cu_seqlens[n] / C) + n; };
+        if (f(0) > slot) return none;
+        int lo = 0, hi = p.N - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (f(mid) <= slot) lo = mid;
+            else hi = mid - 1;
+        }
+        const int a = p.cu_seqlens[lo], e = p.cu_seqlens[lo + 1];
+        if (a < 0 || e < a || e > p.ntok) return none;  // reported by the inter-chunk kernel
+        const int64_t j = slot - f(lo);
+        if (j >= (e - a + C - 1) / C) return none;      // a gap after the sequence
+        const int x = a + (int)j * C;
+        return make_int2(x, e - x < C ? e - x : C);
     };
     auto task_info = [&](int64_t t, int2 e) -> int4 {
         int4 r = make_int4(0, 0, 0, 0);
@@ -347,8 +367,9 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
     // next task's raw-tile loads and stores the record.
     const int64_t n_groups = (p.n_tasks + P - 1) / P;
     int64_t g = blockIdx.x;
-    // the chunk table comes from the previous launch; the inter-chunk kernel
-    // may be scheduled as SMs free up (it waits for this grid to finish)
+    // cu_seqlens and the inputs may come from the previous launch; the
+    // inter-chunk kernel may be scheduled as SMs free up (it waits for this
+    // grid to finish)
     grid_wait_prerequisites();
     grid_launch_dependents();
     int4 cur = task_info(g * P + kslot, table_entry(g * P + kslot));
@@ -380,12 +401,15 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
 
     while (g < n_groups) {
         const int64_t g_next = g + gridDim.x;
+        // the next task's entry, decoded after the operand stage by the
+        // fetcher (the leader goes straight on to this task's raw tiles)
         int2 nxt_e = make_int2(0, 0);
-        if (leader || fetcher) nxt_e = table_entry(g_next * P + kslot);  // decoded after the operand stage
+        if (fetcher) nxt_e = table_entry(g_next * P + kslot);
         // one task per CTA: cur is the same in every thread
         const bool any_task = P == 1 ? cur.y > 0 : __syncthreads_or(cur.y > 0);
         if (!any_task) {
-            const int4 nxt = leader ? task_info(g_next * P + kslot, nxt_e) : make_int4(0, 0, 0, 0);
+            const int4 nxt = leader ? task_info(g_next * P + kslot, table_entry(g_next * P + kslot))
+                                    : make_int4(0, 0, 0, 0);
             // empty slots only: nothing to compute, start the next tasks' loads
             if (leader) {
                 *sinfo = nxt;
@@ -987,8 +1011,8 @@ template <int D, bool GATED, bool SCALAR>
 cudaError_t launch_t(const TcLaunch &x, cudaStream_t s) {
     IntraParams p{static_cast<const __nv_bfloat16 *>(x.a->beta_logits),
                   SCALAR ? static_cast<const __nv_bfloat16 *>(x.a->gate_logits) : nullptr,
-                  x.table, x.records,
-                  x.err, x.slots * x.a->H, x.a->H, x.a->ntok, x.a->flags};
+                  x.a->cu_seqlens, x.records,
+                  x.err, x.slots * x.a->H, x.a->N, x.a->H, x.a->ntok, x.a->flags};
     using L = Layout<D, GATED>;
     // Shared memory caps the CTAs per SM at CTAS_PER_SM, which keeps their
     // TMEM allocations within the SM's 512 columns.

@@ -1,7 +1,7 @@
-// delta_tc.h -- host-side interface between the three launches of the
-// tensor-core delta-rule prefill: chunk table, intra-chunk kernel (every
-// (chunk, head) task in parallel) and inter-chunk kernel (the state
-// recurrence, one CTA per (head, sequence)).
+// delta_tc.h -- host-side interface between the launches of the
+// tensor-core delta-rule prefill: intra-chunk kernel (every (chunk, head)
+// task in parallel) and inter-chunk kernel (the state recurrence, one CTA
+// per (head, sequence)), plus the chunk table the backward pass reads.
 #pragma once
 
 #include <cuda.h>
@@ -13,7 +13,7 @@ namespace la {
 struct TcLaunch {
     CUtensorMap mq, mk, mv, mg;  // TMA maps over q, k, v, gate (intra-chunk kernel)
     const PrefillArgs *a;
-    int2 *table;                 // workspace: [slots] chunk table
+    int2 *table;                 // workspace: [slots] chunk table (backward pass)
     uint8_t *records;            // workspace: [slots][H] per-chunk records
     int64_t slots;
     unsigned *err;               // device error word

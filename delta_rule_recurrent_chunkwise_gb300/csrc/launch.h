@@ -64,9 +64,9 @@ cudaError_t launch_delta_backward_chunked(const BwdArgs &a, cudaStream_t s);
 // fp32 SIMT chunk kernels (any I/O dtype).
 cudaError_t launch_linear_simt(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_delta_simt(const PrefillArgs &a, cudaStream_t s);
-// tcgen05 tensor-core chunk kernels (bf16 I/O, dk == dv in {64, 128}): a
-// chunk table, the intra-chunk kernel and the inter-chunk kernel, with the
-// per-chunk records in the caller's workspace.
+// tcgen05 tensor-core chunk kernels (bf16 I/O, dk == dv in {64, 128}): the
+// intra-chunk kernel and the inter-chunk kernel, with the per-chunk records
+// in the caller's workspace (and a chunk table for the backward pass).
 size_t delta_tc_workspace_bytes(int N, int ntok, int H, int dk, int dv, int chunk, bool bf16);
 bool delta_tc_supported(const PrefillArgs &a);
 cudaError_t launch_delta_tc(const PrefillArgs &a, cudaStream_t s);

@@ -1,7 +1,8 @@
 // prefill_tc.cu -- host side of the tensor-core (gated) delta-rule prefill:
-// TMA maps, workspace layout and the three launches (chunk table,
-// intra-chunk kernel, inter-chunk kernel), plus the library's device error
-// word.  The kernels live in delta_intra_tc.cu and delta_inter_tc.cu.
+// TMA maps, workspace layout and the launches (intra-chunk kernel, then
+// inter-chunk kernel; a chunk table first when the backward pass asks for
+// per-chunk states), plus the library's device error word.  The kernels live
+// in delta_intra_tc.cu and delta_inter_tc.cu.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -103,7 +104,10 @@ cudaError_t launch_delta_tc(const PrefillArgs &a, cudaStream_t s) {
     x.err = device_error_word();
     x.sms = sm_count();
     if (!x.err) return cudaErrorInvalidValue;
-    cudaError_t e = launch_chunk_table(x, s);
+    // The chunk table is read only by the backward pass's kernels (which ask
+    // for per-chunk states); the intra-chunk kernel finds its chunks from
+    // cu_seqlens itself.
+    cudaError_t e = a.chunk_states ? launch_chunk_table(x, s) : cudaSuccess;
     if (e == cudaSuccess) e = launch_delta_intra(x, s);
     if (e == cudaSuccess) e = launch_delta_inter(x, s);
     return e;
