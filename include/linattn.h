@@ -63,7 +63,8 @@ typedef enum la_dtype { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
  * LA_L2NORM_K: k <- k / max(||k||_2, 1e-12) per token and head.
  * LA_L2NORM_Q: the same for q.
  * LA_SILU_QK : q, k <- silu(q), silu(k), applied before the normalisation
- *              (the page's DeltaNet layer uses normalize(silu(.))). */
+ *              (the page's DeltaNet layer applies silu, then the L2
+ *              normalisation). */
 #define LA_L2NORM_K 1u
 #define LA_L2NORM_Q 2u
 #define LA_SILU_QK 4u

@@ -15,8 +15,8 @@
  *
  * Conventions (row convention of the page's listings): the state of one
  * (sequence, head) is S in R^{dk x dv}, stored row-major, S[c*dv + j];
- * a read is o = S^T q (the page's "o = q @ S"), a write adds k u^T
- * (the page's "S = S + k.transpose(-1,-2) @ u").
+ * a read is o = S^T q (the listings' row vector q times S), a write adds
+ * k u^T (the listings add the outer product of k and u to S).
  *
  * Packed layouts (tokens of all sequences back to back, as cu_seqlens says):
  *   q, k         [ntok][H][dk]
@@ -50,7 +50,7 @@
 static double elu_plus_one(double x) { return x > 0.0 ? x + 1.0 : exp(x); }
 
 /* silu(x) = x * sigmoid(x) (section DeltaNet (Fast Weight Programmers):
- * q, k = F.normalize(F.silu(.))). */
+ * the layer applies silu, then L2 normalisation, to q and k). */
 static double sigmoid(double x) {
     if (x >= 0.0) return 1.0 / (1.0 + exp(-x));
     double e = exp(x);
@@ -62,7 +62,8 @@ static double softplus(double x) {
     return (x > 0.0 ? x : 0.0) + log1p(exp(-fabs(x)));
 }
 
-/* x / max(||x||_2, 1e-12), the F.normalize default used on the page. */
+/* x / max(||x||_2, 1e-12): PyTorch's default floor for the L2
+ * normalisation the page's layer applies. */
 static void l2_normalize(double *x, int n) {
     double s = 0.0;
     for (int i = 0; i < n; ++i) s += x[i] * x[i];
@@ -205,9 +206,9 @@ typedef struct {
  *   - the decay of the old state before the write: section Gated DeltaNet
  *     (Mamba-2's decayed state, S = alpha S + k v^T; alpha = 1 gives the pure
  *     delta rule, alpha = 0 clears the memory);
- *   - one decay per key channel: section KDA / Kimi Linear
- *     (alpha.reshape(nb, C, d)).
- * beta_t = sigmoid(beta_logit) (the page's sigmoid(w_beta x)), one value per
+ *   - one decay per key channel: section KDA / Kimi Linear (alpha laid out
+ *     as one d-vector per token of each chunk).
+ * beta_t = sigmoid(beta_logit) (the page: a sigmoid of a projection), one value per
  * token and head; alpha_t = exp(-softplus(gate_logit)) per key channel.
  * With the decay first, the step equals the Householder form of the
  * chunkwise section, S_t = S_{t-1} Diag(alpha)(I - beta k k^T) + beta v k^T
