@@ -987,7 +987,9 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
     if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-// One warp per sequence: the table entries of its chunk slots, then zeros
+// The chunk table the backward pass's kernels read (the forward kernels find
+// their chunks from cu_seqlens).  One warp per sequence: the table entries
+// of its chunk slots, then zeros
 // for the (at most two) unused slots before the next sequence's first one.
 __global__ void chunk_table_kernel(const int32_t *cu, int N, int ntok, int64_t slots,
                                    int2 *table) {

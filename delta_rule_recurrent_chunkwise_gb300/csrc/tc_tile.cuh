@@ -111,7 +111,8 @@ struct Record {
     static constexpr uint32_t BYTES = (GEND + 4 * D + 1023) & ~1023u;
 };
 
-// Workspace of the tensor-core path: the chunk table (one {first token,
+// Workspace of the tensor-core path: the chunk table (written only when the
+// backward pass asks for per-chunk states; one {first token,
 // length} pair per chunk slot) followed by the records, [slot][head].
 // Sequence n's chunk j occupies slot cu[n]/64 + n + j; slots never collide
 // and number at most ntok/64 + N + 1.
