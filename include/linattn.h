@@ -131,9 +131,10 @@ la_status la_prefill_delta(const void *q, const void *k, const void *v, const vo
  * dk = dv in {64, 128}, chunk = 64), whose first pass computes everything
  * that depends on one chunk alone (the WY/UT operands of eq. 10 and the
  * decayed q, k of the chunk) for all chunks in parallel and hands it to the
- * sequential state pass through this buffer: a table of 8 bytes per chunk
- * slot, then one record per (chunk slot, head) of 41 KB (d = 64) or 73 KB
- * (d = 128), with at most ntok/64 + N + 1 slots.  0 otherwise. */
+ * sequential state pass through this buffer: 8 bytes per chunk slot (a
+ * chunk table, filled only by la_backward_delta's forward pass), then one
+ * record per (chunk slot, head) of 41 KB (d = 64) or 73 KB (d = 128), with
+ * at most ntok/64 + N + 1 slots.  0 otherwise. */
 size_t la_prefill_delta_workspace_size(int N, int ntok, int H, int dk, int dv, int chunk,
                                        la_dtype io);
 
