@@ -124,27 +124,45 @@ def ncu_traffic(kernel_key: str):
 
 
 class ClockSampler:
-    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    """Samples SM clocks and throttle reasons with nvidia-smi while running.
+
+    Each sample is stamped with its arrival time on the host; ``load(...)``
+    marks the windows in which the GPU runs the measured work, and the
+    summary's clock median is taken over the samples inside them."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 100
 
     def __init__(self, gpu_index: int, log_dir: str | None = None):
         self.gpu = gpu_index
         self.proc = None
+        self.rows = []        # (host time, fields)
+        self.windows = []     # (start, end) host times of measured work
         # the raw samples (the JSON line carries their summary)
         log_dir = log_dir or os.environ.get("BENCH_CLOCKS_DIR") or tempfile.gettempdir()
         self.path = os.path.join(log_dir, f"clocks_bench_gpu{gpu_index}.csv")
 
+    def _reader(self):
+        with open(self.path, "w") as f:
+            for line in self.proc.stdout:
+                t = time.time()
+                f.write(f"{t:.3f},{line}")
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    self.rows.append((t, parts))
+
     def __enter__(self):
+        import threading
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=self.f, stderr=subprocess.DEVNULL)
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
+            self.thread = threading.Thread(target=self._reader, daemon=True)
+            self.thread.start()
         except Exception:
             self.proc = None
         return self
@@ -156,35 +174,44 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
-            self.f.close()
+            self.thread.join(timeout=5)
+
+    class _Window:
+        def __init__(self, owner):
+            self.owner = owner
+
+        def __enter__(self):
+            self.t0 = time.time()
+
+        def __exit__(self, *exc):
+            self.owner.windows.append((self.t0, time.time()))
+
+    def load(self):
+        """Context manager marking a window of measured GPU work."""
+        return ClockSampler._Window(self)
 
     def summary(self):
-        if self.proc is None:
+        if self.proc is None or not self.rows:
             return None
-        rows = []
-        try:
-            for line in open(self.path):
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
-        except Exception:
-            return None
-        if not rows:
-            return None
+
         def num(x):
             try:
                 return float(x)
             except ValueError:
                 return None
+        # a sample taken within 0.25 s after a window closed still reports it
+        inside = [r for t, r in self.rows
+                  if any(a <= t <= b + 0.25 for a, b in self.windows)]
+        rows = inside or [r for _, r in self.rows]
         sm = [num(r[1]) for r in rows if num(r[1]) is not None]
-        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        mx = [num(r[2]) for r in self.rows if num(r[2]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]
                           and "Not" not in r[5 + i]})
-        loaded = [s for s in sm if mx and s >= 0.5 * max(mx)] or sm
-        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+        return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(rows)}
+                "samples": len(self.rows), "samples_under_load": len(inside),
+                "period_ms": self.PERIOD_MS}
 
 
 # ------------------------------------------------------------ multi-rank
@@ -256,6 +283,22 @@ def time_steps(step_fn, steps, warmup, flush, stream, barrier=None):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
+def soak(step_fn, seconds):
+    """Runs step_fn back to back for about `seconds` (untimed)."""
+    if seconds <= 0:
+        return
+    step_fn()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    step_fn()
+    torch.cuda.synchronize()
+    one = max(time.perf_counter() - t0, 1e-5)
+    n = max(1, int(seconds / one))
+    for _ in range(n):
+        step_fn()
+    torch.cuda.synchronize()
+
+
 def e2e_pipelined(la, pf, host, stream, steps, barrier=None):
     """Milliseconds for `steps` end-to-end prefill calls: each step copies its
     inputs from pinned host memory into one of two device buffer sets (copy
@@ -318,10 +361,16 @@ def run_ours(args, rank, world, dev, dist):
         # ---- headline: GPT-2-shaped delta prefill
         w = wl.workload(HEADLINE)
         pf = Prefill(la, w, seed=rank_seed(rank), dev=dev)
-        ms = time_steps(lambda: pf.step(stream), args.steps, args.warmup, flush, stream, barrier)
-        total_ms = mor(sum(ms))
-        value = job_throughput(w.ntok * args.steps, world, total_ms)
-        kern_ms = sum(ms) / len(ms)
+        # untimed soak of the same call (about a second), so that the clock
+        # record holds samples of the GPU running this work, then the K
+        # timed steps
+        with clocks.load():
+            soak(lambda: pf.step(stream), args.soak_s)
+            ms = time_steps(lambda: pf.step(stream), args.steps, args.warmup, flush, stream,
+                            barrier)
+        kern_ms = statistics.median(ms)
+        step_ms = mor(kern_ms)             # the slowest rank's median step
+        value = job_throughput(w.ntok, world, step_ms)
         nbytes, flops = prefill_algo(w)
         achieved = nbytes / (kern_ms / 1e3) / 1e9
         traffic = ncu_traffic("delta_prefill:" + HEADLINE)
@@ -329,7 +378,8 @@ def run_ours(args, rank, world, dev, dist):
         # and the inter-chunk kernels; the fp32 path one kernel
         per_call = 2 if pf.ws is not None else 1
         result.update(
-            value=value, ms_per_step=total_ms / args.steps, gpu_launches=per_call * args.steps,
+            value=value, ms_per_step=step_ms, mean_ms_per_step=mor(statistics.mean(ms)),
+            gpu_launches=per_call * args.steps,
             roofline={"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                       "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
                       "kernel": "one la_prefill_delta call: intra-chunk + inter-chunk "
@@ -381,8 +431,9 @@ def run_ours(args, rank, world, dev, dist):
                                       toks["beta_logits"][s], toks["gate_logits"][s], od, state,
                                       stream=stream)
 
-            dms = time_steps(decode_64, max(2, args.steps // 4), 1, None, stream, barrier)
-            d_ms = mor(sum(dms)) / len(dms)
+            with clocks.load():
+                dms = time_steps(decode_64, max(3, args.steps // 4), 1, None, stream, barrier)
+            d_ms = mor(statistics.median(dms))
             sb = decode_state_bytes(dw) * dw.steps
             gbs = sb / (d_ms / 1e3) / 1e9
             extra["decode"] = {"workload": "256 seq x 32 heads, dk=dv=128, fp32 state, 64 steps",
@@ -396,9 +447,10 @@ def run_ours(args, rank, world, dev, dist):
                 gw = wl.workload(name, seed=0)
                 fs = name == "varlen_prefill"
                 p = Prefill(la, gw, seed=rank_seed(rank), dev=dev, final_states=fs)
-                gms = time_steps(lambda: p.step(stream), max(3, args.steps // 4), 2, flush,
-                                 stream, barrier)
-                g_ms = mor(sum(gms)) / len(gms)
+                with clocks.load():
+                    gms = time_steps(lambda: p.step(stream), max(3, args.steps // 4), 2, flush,
+                                     stream, barrier)
+                g_ms = mor(statistics.median(gms))
                 nb, fl = prefill_algo(gw, final_states=fs)
                 extra[name] = {"tokens_per_s": gw.ntok * world / (g_ms / 1e3), "ms": g_ms,
                                "hbm_frac": nb / (g_ms / 1e3) / 1e9 / pk["hbm_gbs"],
@@ -423,8 +475,9 @@ def run_ours(args, rank, world, dev, dist):
                                      want_d_init_S=False, workspace=bws,
                                      cu_seqlens_host=b_in["cu_seqlens"], stream=stream)
 
-            bms = time_steps(backward_step, 3, 2, flush, stream, barrier)
-            b_ms = mor(sum(bms)) / len(bms)
+            with clocks.load():
+                bms = time_steps(backward_step, 3, 2, flush, stream, barrier)
+            b_ms = mor(statistics.median(bms))
             nb = backward_algo_bytes(bw)
             extra["gpt2_backward"] = {
                 "tokens_per_s": bw.ntok * world / (b_ms / 1e3), "ms": b_ms,
@@ -440,27 +493,97 @@ def run_ours(args, rank, world, dev, dist):
 
 # --------------------------------------------------------------- CPU oracle
 
-def cpu_oracle_throughput(w: wl.Workload, target_s: float, nseq=None):
-    """Time the oracle as it stands on a bounded sample of the workload."""
+def host_cores():
+    """Host core counts: what std::thread::hardware_concurrency() reports
+    (the online logical CPUs, os.cpu_count()) and what `nproc` prints (the
+    CPUs this process may run on)."""
+    try:
+        nproc = int(subprocess.run(["nproc"], capture_output=True, text=True).stdout.strip())
+    except Exception:
+        nproc = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else None
+    return {"hardware_concurrency": os.cpu_count(), "nproc": nproc}
+
+
+def _loop(fn, target_s, max_passes=2000):
+    """Calls fn() until target_s seconds have passed; (passes, seconds)."""
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= target_s or passes >= max_passes:
+            return passes, el
+
+
+def cpu_oracle_throughput(w: wl.Workload, target_s: float, nseq=None, max_tokens=None,
+                          nthreads=None):
+    """Time the oracle as it stands on a bounded sample of a prefill workload:
+    the first `nseq` sequences, each cut to its first `max_tokens` tokens
+    (the per-token cost of the recurrence does not depend on the position)."""
     import oracle
     oracle.build()
     lens = list(w.lengths[:nseq] if nseq else w.lengths)
-    inp = wl.prefill_inputs(lens, w.H, w.dk, w.dv, w.dtype, w.gated, seed=0)
+    if max_tokens:
+        lens = [min(L, max_tokens) for L in lens]
+    scalar = bool(w.extra.get("scalar_gate"))
+    inp = wl.prefill_inputs(lens, w.H, w.dk, w.dv, w.dtype, w.gated, seed=0,
+                            scalar_gate=scalar)
     f = lambda t: None if t is None else t.double().numpy()
-    args = [f(inp[n]) for n in ("q", "k", "v", "beta_logits", "gate_logits")]
     cu = inp["cu_seqlens"].numpy()
-    threads = min(oracle.default_threads(), len(lens) * w.H)
-    passes, t0 = 0, time.perf_counter()
-    while True:
-        oracle.delta(*args, cu, nthreads=threads)
-        passes += 1
-        el = time.perf_counter() - t0
-        if el >= target_s or passes >= 2000:
-            break
+    threads = nthreads or min(oracle.default_threads(), len(lens) * w.H)
+    if w.kind == "prefill_linear":
+        args = [f(inp[n]) for n in ("q", "k", "v")]
+        fn = lambda: oracle.linear(*args, cu, nthreads=threads)
+    else:
+        args = [f(inp[n]) for n in ("q", "k", "v", "beta_logits", "gate_logits")]
+        flags = oracle.L2NORM_K | (oracle.SCALAR_GATE if scalar else 0)
+        fn = lambda: oracle.delta(*args, cu, flags=flags, nthreads=threads)
+    passes, el = _loop(fn, target_s)
     tokens = sum(lens) * passes
+    cut = f", first {max_tokens} tokens of each" if max_tokens else ""
     return {"value": tokens / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"{len(lens)} of {len(w.lengths)} sequences x {w.H} heads x "
-                      f"{lens[0]} tokens, {passes} pass(es), {el:.1f} s, fp64"}
+            "sample": f"{len(lens)} of {len(w.lengths)} sequences{cut} x {w.H} heads "
+                      f"({sum(lens)} tokens), {passes} pass(es), {el:.1f} s, fp64"}
+
+
+def cpu_oracle_decode(w: wl.Workload, target_s: float, nseq: int):
+    """The oracle's decode step on `nseq` of the workload's sequences (all
+    heads, one step per pass), as state bytes read and written per second."""
+    import oracle
+    oracle.build()
+    d = wl.decode_inputs(nseq, w.H, w.dk, w.dv, 1, w.dtype, seed=0, gated=w.gated)
+    f = lambda t: t.double().numpy()
+    args = [f(d[n][0]) for n in ("q", "k", "v", "beta_logits", "gate_logits")]
+    st = f(d["state"])
+    threads = min(oracle.default_threads(), nseq * w.H)
+    passes, el = _loop(lambda: oracle.decode(*args, st, nthreads=threads), target_s)
+    nbytes = 8 * nseq * w.H * w.dk * w.dv * passes
+    return {"value": nbytes / el / 1e9, "unit": "state GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{nseq} of {w.n_seq} sequences x {w.H} heads, one step per pass, "
+                      f"{passes} pass(es), {el:.1f} s, fp64 (state bytes counted as fp32, "
+                      "as on the GPU)"}
+
+
+def cpu_baselines(target_s: float):
+    """The oracle on a bounded sample of every workload, on the host cores,
+    plus the tiny workloads on one thread."""
+    legs = {}
+    legs["tiny_linear"] = cpu_oracle_throughput(wl.workload("tiny_linear"), min(1.0, target_s))
+    legs["tiny_delta"] = cpu_oracle_throughput(wl.workload("tiny_delta"), min(1.0, target_s))
+    legs["tiny_delta_1thread"] = cpu_oracle_throughput(wl.workload("tiny_delta"),
+                                                       min(1.0, target_s), nthreads=1)
+    legs["tiny_linear_1thread"] = cpu_oracle_throughput(wl.workload("tiny_linear"),
+                                                        min(1.0, target_s), nthreads=1)
+    legs[HEADLINE] = cpu_oracle_throughput(wl.workload(HEADLINE), target_s, nseq=2)
+    part = max(1.0, target_s / 3)
+    legs["gpt2_scalar_gate"] = cpu_oracle_throughput(wl.workload("gpt2_scalar_gate"), part,
+                                                     nseq=1)
+    legs["gated_prefill"] = cpu_oracle_throughput(wl.workload("gated_prefill"), part, nseq=1,
+                                                  max_tokens=2048)
+    legs["varlen_prefill"] = cpu_oracle_throughput(wl.workload("varlen_prefill", seed=0), part,
+                                                   nseq=1, max_tokens=4096)
+    legs["decode"] = cpu_oracle_decode(wl.workload("decode"), part, nseq=64)
+    return legs
 
 
 # ------------------------------------------------------------ ncu traffic
@@ -470,19 +593,21 @@ def record_traffic(args):
     current kernel sources, in profiles/traffic.json."""
     import csv
     import re
-    rows = list(csv.reader(open(args.record_traffic)))
-    hdr, units = rows[0], rows[1]
-    name_i = hdr.index("Kernel Name")
-    rd, wr = hdr.index("dram__bytes_read.sum"), hdr.index("dram__bytes_write.sum")
     scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
-    # one call of the path: the first launch of each distinct kernel matching the regex
+    # one call of the path: the first launch of each distinct kernel matching
+    # the regex, over one capture per kernel (comma-separated files)
     found, seen = 0.0, set()
-    for r in rows[2:]:
-        name = r[name_i]
-        if re.search(args.kernel_regex, name) and name not in seen:
-            seen.add(name)
-            found += (float(r[rd].replace(",", "")) * scale[units[rd]] +
-                      float(r[wr].replace(",", "")) * scale[units[wr]])
+    for path in args.record_traffic.split(","):
+        rows = list(csv.reader(open(path)))
+        hdr, units = rows[0], rows[1]
+        name_i = hdr.index("Kernel Name")
+        rd, wr = hdr.index("dram__bytes_read.sum"), hdr.index("dram__bytes_write.sum")
+        for r in rows[2:]:
+            name = r[name_i]
+            if re.search(args.kernel_regex, name) and name not in seen:
+                seen.add(name)
+                found += (float(r[rd].replace(",", "")) * scale[units[rd]] +
+                          float(r[wr].replace(",", "")) * scale[units[wr]])
     if not seen:
         raise SystemExit("kernel not found in the capture")
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -490,7 +615,7 @@ def record_traffic(args):
     data[args.traffic_key] = {"source_hash": kernel_source_hash(args.traffic_key),
                               "dram_bytes_per_launch": found * args.launch_scale,
                               "captured_bytes": found, "launch_scale": args.launch_scale,
-                              "capture": os.path.basename(args.record_traffic),
+                              "capture": ",".join(os.path.basename(x) for x in args.record_traffic.split(",")),
                               "kernels": sorted(seen)}
     with open(path, "w") as f:
         json.dump(data, f, indent=1, sort_keys=True)
@@ -554,10 +679,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--headline-only", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--record-traffic", default=None, metavar="NCU_RAW_CSV",
-                    help="read dram bytes of one kernel from `ncu -i X --page raw --csv` output "
-                         "and store them in profiles/traffic.json under --traffic-key")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="host seconds for the headline's oracle sample (the other "
+                         "workloads' samples take about a third of that each)")
+    ap.add_argument("--soak-s", type=float, default=1.5,
+                    help="untimed seconds of the headline call before its timed steps, "
+                         "under the clock sampler")
+    ap.add_argument("--record-traffic", default=None, metavar="NCU_RAW_CSV[,CSV...]",
+                    help="read dram bytes of the path's kernels from `ncu -i X --page raw --csv` "
+                         "outputs (one capture per kernel, comma-separated) and store their sum "
+                         "in profiles/traffic.json under --traffic-key")
     ap.add_argument("--traffic-key", default="delta_prefill:" + HEADLINE)
     ap.add_argument("--kernel-regex", default="chunk_table|delta_intra|delta_inter")
     ap.add_argument("--launch-scale", type=float, default=1.0,
@@ -586,7 +717,8 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        cb = cpu_oracle_throughput(w, target_s=min(20.0, 3.0 * args.cpu_seconds), nseq=2)
+        cb = dict(cpu_oracle_throughput(w, target_s=min(20.0, 3.0 * args.cpu_seconds), nseq=2),
+                  **host_cores())
         line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "tokens/s",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": w.ntok / cb["value"] * 1e3, "higher_is_better": True,
@@ -608,15 +740,20 @@ def main():
     if rank == 0:
         line = {"metric": METRIC, "value": r["value"], "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
+                "mean_ms_per_step": r["mean_ms_per_step"],
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "f32", "data": "synthetic (seeded; shapes of the page's "
+                "dtype": "bf16", "dtype_detail": "bf16 I/O and bf16 tensor-core operands; "
+                "fp32 accumulation, fp32 state, fp32 triangular solve",
+                "timing": "median of the timed steps (CUDA events on the launching stream)",
+                "data": "synthetic (seeded; shapes of the page's "
                 "GPT-2-small-shaped model)", "config": config,
                 "roofline": r["roofline"], "e2e": r["e2e"], "gpu_launches": r["gpu_launches"],
                 "clocks": r["clocks"]}
         if "secondary" in r:
             line["secondary"] = r["secondary"]
         if world == 1:
-            line["cpu_baseline"] = cpu_oracle_throughput(w, target_s=args.cpu_seconds, nseq=2)
+            legs = cpu_baselines(args.cpu_seconds)
+            line["cpu_baseline"] = dict(legs[HEADLINE], **host_cores(), per_workload=legs)
         print(json.dumps(line))
     if dist is not None:
         dist.barrier()

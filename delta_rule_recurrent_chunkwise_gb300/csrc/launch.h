@@ -70,8 +70,8 @@ cudaError_t launch_delta_simt(const PrefillArgs &a, cudaStream_t s);
 size_t delta_tc_workspace_bytes(int N, int ntok, int H, int dk, int dv, int chunk, bool bf16);
 bool delta_tc_supported(const PrefillArgs &a);
 cudaError_t launch_delta_tc(const PrefillArgs &a, cudaStream_t s);
-// Static device scratch behind la_prefill_delta_static (per device; the
-// address is looked up on first use).
+// Static device scratch behind la_prefill_delta_static (static_scratch.cu,
+// a module of its own; per device, the address is looked up on first use).
 constexpr size_t kStaticScratchBytes = size_t(256) << 20;
 void *static_scratch();
 // Device address of the library's error word on the current device (kernels

@@ -2,11 +2,13 @@
 // TMA maps, workspace layout and the launches (intra-chunk kernel, then
 // inter-chunk kernel; a chunk table first when the backward pass asks for
 // per-chunk states), plus the library's device error word.  The kernels live
-// in delta_intra_tc.cu and delta_inter_tc.cu.
+// in delta_intra_tc.cu and delta_inter_tc.cu; the static scratch buffer of
+// la_prefill_delta_static in static_scratch.cu.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -17,9 +19,6 @@
 namespace la {
 
 __device__ unsigned g_tc_error;  // first error code raised in a kernel
-
-// Library-owned scratch for the allocation-free prefill entry point.
-static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
 namespace {
 
@@ -50,16 +49,18 @@ bool make_map(CUtensorMap *m, const void *ptr, int D, int H, int ntok) {
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Per-device values cached on first use.  Host threads racing on a first
+// call store the same value; a failed query is retried on the next call.
 int sm_count() {
-    static int count[64] = {};
+    static std::atomic<int> count[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (!count[dev]) {
-        int c = 0;
+    int c = count[dev].load(std::memory_order_acquire);
+    if (!c) {
         if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        count[dev] = c;
+        count[dev].store(c, std::memory_order_release);
     }
-    return count[dev];
+    return c;
 }
 
 size_t record_bytes(int D) {
@@ -113,28 +114,16 @@ cudaError_t launch_delta_tc(const PrefillArgs &a, cudaStream_t s) {
     return e;
 }
 
-void *static_scratch() {
-    static void *ptr[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!ptr[dev]) {
-        void *a = nullptr;
-        if (cudaGetSymbolAddress(&a, g_static_scratch) != cudaSuccess) return nullptr;
-        ptr[dev] = a;
-    }
-    return ptr[dev];
-}
-
 unsigned *device_error_word() {
-    static unsigned *ptr[64] = {};
+    static std::atomic<void *> addr[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!ptr[dev]) {
-        void *a = nullptr;
-        if (cudaGetSymbolAddress(&a, g_tc_error) != cudaSuccess) return nullptr;
-        ptr[dev] = static_cast<unsigned *>(a);
+    void *p = addr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        if (cudaGetSymbolAddress(&p, g_tc_error) != cudaSuccess) return nullptr;
+        addr[dev].store(p, std::memory_order_release);
     }
-    return ptr[dev];
+    return static_cast<unsigned *>(p);
 }
 
 cudaError_t tc_take_error(cudaStream_t s, unsigned *code) {

@@ -29,7 +29,8 @@
  * - Supported head sizes: dk, dv in {64, 128}.  N >= 1, H >= 1.
  * - Every pointer is a device pointer unless stated otherwise.  The caller
  *   owns every buffer; the library allocates, frees and synchronises nothing
- *   (except la_check_device, which synchronises the given stream).  Outputs
+ *   (except la_check_device, which synchronises the given stream, and the
+ *   static buffer of la_prefill_delta_static described there).  Outputs
  *   must not alias inputs; final states may alias the matching initial state
  *   only where stated.
  * - stream: a cudaStream_t passed as void* (NULL = the legacy default
@@ -152,7 +153,13 @@ size_t la_prefill_delta_workspace_size(int N, int ntok, int H, int dk, int dv, i
  * buffer needs no initialisation (every call rewrites what it reads).  All
  * calls on a device share it, so calls whose executions may overlap in time
  * (different streams, or host threads without ordering) race on it and give
- * undefined results: serialise them. */
+ * undefined results: serialise them.
+ * Footprint: the buffer sits in a CUDA module of its own.  Under lazy module
+ * loading (the CUDA runtime's default) it is reserved on a device at the
+ * first la_prefill_delta_static call there and held until the process
+ * exits; processes that never call this entry point never reserve it.
+ * Under eager loading (CUDA_MODULE_LOADING=EAGER) every device the process
+ * initialises reserves it at context creation. */
 #define LA_STATIC_SCRATCH_BYTES (256u << 20)
 la_status la_prefill_delta_static(const void *q, const void *k, const void *v,
                                   const void *beta_logits, const void *gate_logits, void *o,
