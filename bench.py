@@ -204,7 +204,7 @@ class ClockSampler:
                   if any(a <= t <= b + 0.25 for a, b in self.windows)]
         rows = inside or [r for _, r in self.rows]
         sm = [num(r[1]) for r in rows if num(r[1]) is not None]
-        mx = [num(r[2]) for r in self.rows if num(r[2]) is not None]
+        mx = [num(r[2]) for _, r in self.rows if num(r[2]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]
                           and "Not" not in r[5 + i]})

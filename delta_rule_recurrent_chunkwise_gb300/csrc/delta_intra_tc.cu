@@ -71,23 +71,29 @@ constexpr uint32_t TC_A = 0, TC_W = 0;  // TMEM columns; U follows W
 template <int D, bool GATED>
 struct Layout {
     static constexpr uint32_t tile64 = C * D * 2;               // [64][D]
-    static constexpr uint32_t RAW_Q = 0;
-    static constexpr uint32_t RAW_K = RAW_Q + tile64;
-    static constexpr uint32_t RAW_V = RAW_K + tile64;
+    // Raw q and k, interleaved per 64-column block so that [q; k] is one
+    // 128-row RS tile: column block cb holds q rows 0..63, then k rows
+    // 0..63 (rows 64..127), 16 KB per block.  That tile is the A operand and
+    // its k half the B operand of the first product when it runs on the raw
+    // inputs.
+    static constexpr uint32_t RAW_QK = 0;
+    static constexpr uint32_t RAW_V = RAW_QK + 2 * tile64;
     static constexpr uint32_t RAW_G = RAW_V + tile64;
     static constexpr uint32_t X = RAW_G + (GATED ? tile64 : 0);
-    // X, prologue: the block-product operand [Q^; K^] (128 rows) and, gated,
-    // the packed K_R tile (160 rows)
+    // X, prologue: the block-product operand [Q^; K^] (128 rows; gated or
+    // silu only) and, gated, the packed K_R tile (160 rows)
     static constexpr uint32_t QKH = X;
     static constexpr uint32_t KR = X + 128 * D * 2;
     // X during and after the solve
-    static constexpr uint32_t T16 = X;                  // T, bf16 [64][64]
-    static constexpr uint32_t AQK = X + 8192;           // Aq, bf16 [64][64]
-    static constexpr uint32_t SA = X + 16384;           // A, fp32 [64][LDT]
+    static constexpr uint32_t SA = X;                   // A, fp32 [64][LDT]
+    static constexpr uint32_t T16 = X;                  // [T; T], bf16 [128][64] (A dead by then)
     static constexpr uint32_t ST = SA + 64 * LDT * 4;   // T, fp32 [64][LDT]
-    static constexpr uint32_t SX = T16;                 // solve temps, fp32 (8 KB; dead before T16)
+    static constexpr uint32_t AQK = ST + 64 * LDT * 4;  // Aq, bf16 [64][64]
+    static constexpr uint32_t SX = AQK + 8192;          // solve temps, fp32 (7 KB)
+    static constexpr uint32_t SX_BYTES = 7 * 1024;
+    static_assert(128 * 128 <= 64 * LDT * 4, "[T; T] fits in the dead A scratch");
     static constexpr uint32_t X_END_A = GATED ? KR + 160 * D * 2 : KR;
-    static constexpr uint32_t X_END_C = ST + 64 * LDT * 4;
+    static constexpr uint32_t X_END_C = SX + SX_BYTES;
     static constexpr uint32_t X_END = X_END_A > X_END_C ? X_END_A : X_END_C;
     // The record's first four tiles, contiguous as in the record:
     //   WQ = [beta K e^b, later -W (rows 0..63) ; Q e^b (rows 64..127)]
@@ -100,8 +106,8 @@ struct Layout {
     static constexpr uint32_t BETA = SMALL;                    // fp32 [64]
     static constexpr uint32_t KN = BETA + 256;                 // fp32 [64]
     static constexpr uint32_t QN = KN + 256;                   // fp32 [64]
-    static constexpr uint32_t EB = QN + 256;                   // fp32 [4][D] block decay
-    static constexpr uint32_t GEND = EB + 16 * D;              // fp32 [D] chunk decay
+    static constexpr uint32_t EB = QN + 256;                   // fp32 [4][D] block decay (gated)
+    static constexpr uint32_t GEND = EB + (GATED ? 16 * D : 0);  // fp32 [D] chunk decay
     // scalar gate (one decay per token): log alpha, then cumulative b, and
     // the row factors e^b, e^{b_end - b}
     static constexpr uint32_t SLB = GEND + 4 * D;              // fp32 [64]
@@ -130,6 +136,10 @@ struct Layout {
     static_assert(CTAS_PER_SM * (TOTAL + 2048) <= 228 * 1024, "CTAs per SM");
     static_assert(TCOLS >= (GATED ? 160u : 64u) && TCOLS >= 2u * D, "TMEM columns per task");
 };
+
+// Offsets of raw q and k elements inside the interleaved RAW_QK tile.
+__device__ __forceinline__ uint32_t qoff(int r, int c) { return rs_off(128, r, c); }
+__device__ __forceinline__ uint32_t koff(int r, int c) { return rs_off(128, r + 64, c); }
 
 __device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
@@ -173,8 +183,8 @@ __device__ __forceinline__ void store_c(float *Cp, int ldc, const float (&d)[4],
 // column (factors <= 1).  Out of line: it runs only for chunks that have such
 // a channel and must not raise the register count of the common path.
 template <int D>
-__device__ __noinline__ void exact_own_block(const uint8_t *rawq, const uint8_t *rawk,
-                                             const uint8_t *rawg, const float *sqn,
+__device__ __noinline__ void exact_own_block(const uint8_t *rawqk, const uint8_t *rawg,
+                                             const float *sqn,
                                              const float *skn, const float *sE, float *sDiag,
                                              int lw, int lane, int len, bool silu) {
     constexpr int CG = D / 32;
@@ -187,7 +197,7 @@ __device__ __noinline__ void exact_own_block(const uint8_t *rawq, const uint8_t 
         const int row = 16 * R + r;
         const uint32_t o = tile::rs_off(tile::C, row, c);
         const float g = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(rawg + o));
-        float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(rawk + o));
+        float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(rawqk + koff(row, c)));
         if (silu) kv = kv / (1.0f + expf(-kv));
         al[r] = row < len ? decay_f(g) : 1.0f;
         kh[r] = kv * skn[row];
@@ -202,7 +212,7 @@ __device__ __noinline__ void exact_own_block(const uint8_t *rawq, const uint8_t 
             if (r > i) pr *= al[r];
             const int row = 16 * R + r;
             float qv = __bfloat162float(
-                *reinterpret_cast<const __nv_bfloat16 *>(rawq + tile::rs_off(tile::C, row, c)));
+                *reinterpret_cast<const __nv_bfloat16 *>(rawqk + qoff(row, c)));
             if (silu) qv = qv / (1.0f + expf(-qv));
             const float sq = warp_sum(qv * sqn[row] * pr);
             const float sk = warp_sum(kh[r] * pr);
@@ -249,8 +259,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
     // would hold it up)
     const bool fetcher = ltid == 32;
     uint8_t *sm = sbase + kslot * L::TASK_BYTES;
-    uint8_t *rawq = sm + L::RAW_Q, *rawk = sm + L::RAW_K, *rawv = sm + L::RAW_V,
-            *rawg = sm + L::RAW_G;
+    uint8_t *rawqk = sm + L::RAW_QK, *rawv = sm + L::RAW_V, *rawg = sm + L::RAW_G;
     uint8_t *qkh = sm + L::QKH, *kr = sm + L::KR, *t16 = sm + L::T16, *aqk = sm + L::AQK;
     float *sA = reinterpret_cast<float *>(sm + L::SA);
     float *sT = reinterpret_cast<float *>(sm + L::ST);
@@ -276,6 +285,10 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
     const int qd = lw & 3, cp = lw >> 2;  // TMEM lane quarter, column part
     const int H = p.H;
     const bool silu = (p.flags & kSiluQK) != 0;
+    // The first product [q; k] k^T runs on the raw tiles as soon as they land
+    // (the norms, beta and scalar decays are applied as it is read out of
+    // TMEM) unless silu or a per-channel gate changes the operands themselves.
+    const bool raw_p1 = !GATED && !silu;
     const bool additive = (p.flags & kAdditive) != 0;  // A = 0, W = 0, beta = 1: u = V
     const bool l2k = (p.flags & kL2NormK) != 0, l2q = (p.flags & kL2NormQ) != 0;
     constexpr uint32_t tx_bytes = (GATED ? 4u : 3u) * L::tile64;
@@ -344,8 +357,8 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
         mbar_arrive_expect_tx(bar_tma, tx_bytes);
 #pragma unroll
         for (int cb = 0; cb < D / 64; ++cb) {
-            tma_load_3d_hint(rawq + cb * 8192, &tm_q, bar_tma, cb * 64, hh, t0, pol);
-            tma_load_3d_hint(rawk + cb * 8192, &tm_k, bar_tma, cb * 64, hh, t0, pol);
+            tma_load_3d_hint(rawqk + cb * 16384, &tm_q, bar_tma, cb * 64, hh, t0, pol);
+            tma_load_3d_hint(rawqk + cb * 16384 + 8192, &tm_k, bar_tma, cb * 64, hh, t0, pol);
             tma_load_3d_hint(rawv + cb * 8192, &tm_v, bar_tma, cb * 64, hh, t0, pol);
             if (GATED) tma_load_3d_hint(rawg + cb * 8192, &tm_g, bar_tma, cb * 64, hh, t0, pol);
         }
@@ -398,6 +411,31 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
         __syncthreads();
         tc_fence_after();
     };
+    // B: the block products, one thread.  Gated: the packed K_R tile is one
+    // 160-row operand, so all four block products form one N = 160 product
+    // (block R at column 8R(R+1)); ungated: one product [q; k] x k^T
+    // (N = 64) on the raw tiles, or on [q^; k^] (QKH) with silu.  Issue loops
+    // are kept rolled and short: this code runs on one thread, so every
+    // instruction of it is fetched without help from other warps.
+    auto issue_p1 = [&]() {
+        const uint32_t id = GATED ? idesc_bf16(128, 160, false, false) : idesc_bf16(128, 64, false, false);
+        const int bRows = GATED ? 160 : 128;
+#pragma unroll 1
+        for (int kk = 0; kk < P; ++kk) {
+            uint8_t *tsm = task_sm(kk);
+            const uint8_t *qk = raw_p1 ? tsm + L::RAW_QK : tsm + L::QKH;
+            const uint64_t a0 = kdesc(qk, 128, 0, 0);
+            const uint64_t b0 = GATED ? kdesc(tsm + L::KR, 160, 0, 0) : kdesc(qk, 128, 64, 0);
+#pragma unroll 1
+            for (int kb = 0; kb < D / 64; ++kb) {
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4)
+                    mma_bf16(task_tmem(kk) + TC_A, dstep(a0, kstep_units(128, 4 * kb + s4)),
+                             dstep(b0, kstep_units(bRows, 4 * kb + s4)), id, (kb | s4) != 0);
+            }
+        }
+        mma_commit(bar_mma);
+    };
 
     while (g < n_groups) {
         const int64_t g_next = g + gridDim.x;
@@ -436,6 +474,9 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
                 ok = mbar_wait(bar_tma, tma_par, p.err, 1);
                 tma_par ^= 1;
                 tma_pending = false;
+                // the first product needs nothing but the raw tiles: it runs
+                // while the CUDA cores work through the prologue below
+                if (ok && raw_p1) issue_p1();
             }
             tc_fence_before();
             if (__syncthreads_or(!ok)) { failed = true; break; }
@@ -454,8 +495,8 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
 #pragma unroll
             for (int c = part * (D / TPR); c < (part + 1) * (D / TPR); c += 8) {
                 float kv[8], qv[8];
-                unpack8(*reinterpret_cast<const uint4 *>(rawk + rs_off(C, r, c)), kv);
-                unpack8(*reinterpret_cast<const uint4 *>(rawq + rs_off(C, r, c)), qv);
+                unpack8(*reinterpret_cast<const uint4 *>(rawqk + koff(r, c)), kv);
+                unpack8(*reinterpret_cast<const uint4 *>(rawqk + qoff(r, c)), qv);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     if (silu) { kv[i] = silu_fast(kv[i]); qv[i] = silu_fast(qv[i]); }
@@ -501,15 +542,17 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
                 __syncthreads();
                 if (ltid < D) sgend[ltid] = sEb[63];  // e^{b_end}, the same for every channel
             }
-            // [q^; k^] into QKH; beta k^, q^ into WQ; beta v, k^ into UK: 16-byte units
+            // beta k^, q^ into WQ; beta v, k^ into UK; with silu also [q^; k^]
+            // into QKH (the first product's operand; without silu that
+            // product runs on the raw tiles): 16-byte units
             for (int u = ltid; u < C * D / 8; u += NTC) {
                 const uint32_t off = (uint32_t)u * 16u;                 // offset in a [64][D] tile
                 const uint32_t cb = off >> 13, in = off & 8191u;         // column block, offset in it
                 const int r = (int)(in >> 7);
                 const uint32_t po = cb * (128u * 128u) + in;            // same row, 128-row tile
                 float kv[8], qv[8], vv[8];
-                unpack8(*reinterpret_cast<const uint4 *>(rawk + off), kv);
-                unpack8(*reinterpret_cast<const uint4 *>(rawq + off), qv);
+                unpack8(*reinterpret_cast<const uint4 *>(rawqk + po + 64u * 128u), kv);
+                unpack8(*reinterpret_cast<const uint4 *>(rawqk + po), qv);
                 unpack8(*reinterpret_cast<const uint4 *>(rawv + off), vv);
                 const float kn = skn[r], qn = sqn[r], be = sbeta[r];
                 float bk[8];
@@ -522,8 +565,10 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
                     vv[i] *= be;
                 }
                 const uint4 qh = pack8(qv), kh = pack8(kv);
-                *reinterpret_cast<uint4 *>(qkh + po) = qh;
-                *reinterpret_cast<uint4 *>(qkh + po + 64u * 128u) = kh;
+                if (!raw_p1) {
+                    *reinterpret_cast<uint4 *>(qkh + po) = qh;
+                    *reinterpret_cast<uint4 *>(qkh + po + 64u * 128u) = kh;
+                }
                 *reinterpret_cast<uint4 *>(uk + po) = pack8(vv);
                 if (scalar) {
                     // Q e^b, beta K e^b, K e^{b_end - b}: one factor per row
@@ -648,7 +693,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
                     asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(*reinterpret_cast<const uint32_t *>(&v))
                                  : "memory");
                 };
-                uint8_t *const pq_raw = rawq + cboff64, *const pk_raw = rawk + cboff64;
+                uint8_t *const pq_raw = rawqk + cboff128, *const pk_raw = rawqk + cboff128 + 64 * 128;
                 const uint32_t p_qh = smem_u32(qkh) + cboff128, p_kh = smem_u32(qkh) + cboff128 + 64 * 128;
                 const uint32_t p_qg = smem_u32(wq) + cboff128 + 64 * 128, p_kt = smem_u32(uk) + cboff128 + 64 * 128;
                 const uint32_t p_bk = smem_u32(wq) + cboff128, p_kr = smem_u32(kr) + cboff160;
@@ -721,48 +766,30 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
                 for (int u = ltid; u < 2048; u += NTC) sDiag[u] = 0.0f;
                 __syncthreads();
                 if (lw < 4 * (D / 32))
-                    exact_own_block<D>(rawq, rawk, rawg, sqn, skn, sE, sDiag, lw, lane, len, silu);
+                    exact_own_block<D>(rawqk, rawg, sqn, skn, sE, sDiag, lw, lane, len, silu);
                 __syncthreads();
             }
         }
-        // raw tiles consumed: fetch the next task's while this one computes
+        // Raw tiles consumed by the CUDA cores: fetch the next task's while
+        // this one computes -- at once when the first product reads the
+        // operand tiles, after it has completed when it reads the raw tiles.
         if (fetcher) {
             const int4 nxt = task_info(g_next * P + kslot, nxt_e);
             *sinfo = nxt;
-            if (nxt.y > 0) issue_tma(nxt.x, nxt.z);
+            if (!raw_p1 && nxt.y > 0) issue_tma(nxt.x, nxt.z);
         }
         // ---------------------------------------------- B: block products
-        // Issue loops are kept rolled and short: this code runs on one thread,
-        // so every instruction of it is fetched without help from other warps.
-        if (tid == 0) {
-            // gated: the packed K_R tile is one 160-row operand, so all four block
-            // products form one N = 160 product (block R at column 8R(R+1));
-            // ungated: one product [q^; k^] x k^T (N = 64)
-            const uint32_t id = GATED ? idesc_bf16(128, 160, false, false) : idesc_bf16(128, 64, false, false);
-            const int bRows = GATED ? 160 : 128;
-#pragma unroll 1
-            for (int kk = 0; kk < P; ++kk) {
-                uint8_t *tsm = task_sm(kk);
-                const uint64_t a0 = kdesc(tsm + L::QKH, 128, 0, 0);
-                // ungated: B = k^, the lower half of [q^; k^] (UK's lower half holds
-                // K e^{b_end - b} under a scalar gate)
-                const uint64_t b0 = GATED ? kdesc(tsm + L::KR, 160, 0, 0) : kdesc(tsm + L::QKH, 128, 64, 0);
-#pragma unroll 1
-                for (int kb = 0; kb < D / 64; ++kb) {
-#pragma unroll
-                    for (int s4 = 0; s4 < 4; ++s4)
-                        mma_bf16(task_tmem(kk) + TC_A, dstep(a0, kstep_units(128, 4 * kb + s4)),
-                                 dstep(b0, kstep_units(bRows, 4 * kb + s4)), id, (kb | s4) != 0);
-                }
-            }
-            mma_commit(bar_mma);
-        }
+        if (!raw_p1 && tid == 0) issue_p1();
         {
             const bool mma_failed = __syncthreads_or(!mma_wait());
-            // the fetcher's loads are visible to the leader now, who must wait
-            // for them before leaving, whatever happens next
+            if (mma_failed) {
+                // the leader must wait for loads in flight before leaving
+                tma_pending = !raw_p1 && sinfo->y > 0;
+                failed = true;
+                break;
+            }
+            if (raw_p1 && fetcher && sinfo->y > 0) issue_tma(sinfo->x, sinfo->z);
             tma_pending = sinfo->y > 0;
-            if (mma_failed) { failed = true; break; }
         }
         tc_fence_after();
         // the next task is known to every thread now: prefetch its beta
@@ -802,6 +829,13 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
                     }
                 } else {
                     tmem_ld16(tq + TC_A + col, v);
+                    if (raw_p1) {
+                        // raw operands: the row's and the key's norm factors
+                        // (zero for rows past the end of the chunk)
+                        const float rf = is_q ? sqn[r] : skn[r];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] *= rf * skn[col + i];
+                    }
                     if (scalar) {
                         // e^{b_r - b_i} for i <= r (exponent <= 0); later columns are masked
                         const float br = sLb[r];
@@ -831,47 +865,49 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
                 }
             }
         }
-        // T starts at zero; the solve below fills its diagonal blocks, the
-        // merges its lower blocks
-        for (int u = ltid; u < 64 * 16; u += NTC)
-            reinterpret_cast<float4 *>(sT + (u >> 4) * LDT)[u & 15] = make_float4(0.f, 0.f, 0.f, 0.f);
         __syncthreads();
-        // ---------------------------------------------- C1b: T_RR = (I + A_RR)^{-1}
-        // Column-oriented forward substitution: lane (R, j) of warps 2, 3
-        // owns column j of block R and needs only its own earlier entries
-        // (A broadcast from shared memory), so there is no cross-lane
-        // exchange on the chain:  T[r][j] = [r == j] - sum_{k<r} A[r][k] T[k][j].
-        if (lw == 2 || lw == 3) {
-            const int R = 2 * (lw - 2) + (lane >> 4), j = lane & 15;
-            const float *Ab = sA + (16 * R) * LDT + 16 * R;
-            float t[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                float a0 = (r == j) ? 1.0f : 0.0f, a1 = 0.0f;
-#pragma unroll
-                for (int k = 0; k < r; ++k) {
-                    if (k & 1) a1 = fmaf(-Ab[r * LDT + k], t[k], a1);
-                    else a0 = fmaf(-Ab[r * LDT + k], t[k], a0);
-                }
-                t[r] = a0 + a1;
-            }
-            float *Tb = sT + (16 * R) * LDT + 16 * R + j;
-#pragma unroll
-            for (int r = 0; r < 16; ++r) Tb[r * LDT] = t[r];
-        }
-        __syncthreads();
-        // ---------------------------------------------- C2: off-diagonal blocks of T
-        // Two merges, as warp-level TF32 products (the blocks are 16 and 32
-        // wide; T is rounded to bf16 afterwards, coarser than TF32).
-        // (1) T_10 = -T_11 (A_10 T_00), T_32 = -T_33 (A_32 T_22)   (warps 0, 1)
-        // (2) with T_TT = T[0:32,0:32], T_BB = T[32:64,32:64]:
-        //     T[32:64, 0:32] = -T_BB (A[32:64, 0:32] T_TT)           (warps 0..7)
+        // ---------------------------------------------- C1b: diagonal blocks and T_10, T_32
+        // Warp b (0, 1) takes blocks J = 2b and R = 2b + 1.
+        // (a) T_JJ, T_RR = (I + A_XX)^{-1} by column-oriented forward
+        //     substitution: lane (block, j) owns column j of its block and
+        //     needs only its own earlier entries (A broadcast from shared
+        //     memory), so there is no cross-lane exchange on the chain:
+        //     T[r][j] = [r == j] - sum_{k<r} A[r][k] T[k][j].  The lanes of
+        //     block R also zero the block above it (rows of J, columns of R),
+        //     which the merges below read.
+        // (b) T_RJ = -T_RR (A_RJ T_JJ) in the same warp, as warp-level TF32
+        //     products (T is rounded to bf16 afterwards, coarser than TF32).
+        // No T entry right of these blocks is ever read; C3 writes zeros there.
         {
-            constexpr int LX = 24, LY = 40;
+            constexpr int LX = 24;
             float *sX1 = sX;                 // [2][16][LX]
-            float *sY = sX + 2 * 16 * LX;    // [32][LY]
             if (lw < 2) {
-                const int b = lw, R = 1 + 2 * b, J = 2 * b;
+                const int b = lw;
+                {
+                    const int Rb = 2 * b + (lane >> 4), j = lane & 15;
+                    const float *Ab = sA + (16 * Rb) * LDT + 16 * Rb;
+                    float t[16];
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) {
+                        float a0 = (r == j) ? 1.0f : 0.0f, a1 = 0.0f;
+#pragma unroll
+                        for (int k = 0; k < r; ++k) {
+                            if (k & 1) a1 = fmaf(-Ab[r * LDT + k], t[k], a1);
+                            else a0 = fmaf(-Ab[r * LDT + k], t[k], a0);
+                        }
+                        t[r] = a0 + a1;
+                    }
+                    float *Tb = sT + (16 * Rb) * LDT + 16 * Rb + j;
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) Tb[r * LDT] = t[r];
+                    if (lane >= 16) {
+                        float *Tz = sT + (16 * (Rb - 1)) * LDT + 16 * Rb + j;
+#pragma unroll
+                        for (int r = 0; r < 16; ++r) Tz[r * LDT] = 0.0f;
+                    }
+                }
+                __syncwarp();
+                const int R = 1 + 2 * b, J = 2 * b;
                 float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks) {
@@ -895,40 +931,61 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
                 store_c(sT + (16 * R) * LDT + 16 * J + 8, LDT, e1, -1.0f, lane);
             }
             __syncthreads();
-            const int mt = (lw >> 2) & 1, nt = lw & 3;
-            if (lw < 8) {
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
+            // ------------------------------------------ C2: lower-left 32 x 32 block of T
+            // With T_TT = T[0:32,0:32], T_BB = T[32:64,32:64]:
+            //   T[32:64, 0:32] = -T_BB (A[32:64, 0:32] T_TT).
+            // Warp nt (0..3) takes the 8 columns 8 nt .. 8 nt + 7: it forms
+            // those columns of Y = A[32:64, 0:32] T_TT itself (in its own
+            // shared-memory slice, so only the warp synchronises) and then
+            // T_BB Y for them.
+            constexpr int LYW = 8;
+            float *sYw = sX + 2 * 16 * LX + lw * 32 * LYW;  // [32][LYW] per warp
+            if (lw < 4) {
+                const int nt = lw;
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_tf32(d, sA + (32 + 16 * mt) * LDT + 8 * ks, LDT,
-                             sT + (8 * ks) * LDT + 8 * nt, LDT, lane);
-                store_c(sY + (16 * mt) * LY + 8 * nt, LY, d, 1.0f, lane);
-            }
-            __syncthreads();
-            if (lw < 8) {
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int mt = 0; mt < 2; ++mt) {
+                    float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_tf32(d, sT + (32 + 16 * mt) * LDT + 32 + 8 * ks, LDT,
-                             sY + (8 * ks) * LY + 8 * nt, LY, lane);
-                store_c(sT + (32 + 16 * mt) * LDT + 8 * nt, LDT, d, -1.0f, lane);
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_tf32(d, sA + (32 + 16 * mt) * LDT + 8 * ks, LDT,
+                                 sT + (8 * ks) * LDT + 8 * nt, LDT, lane);
+                    store_c(sYw + (16 * mt) * LYW, LYW, d, 1.0f, lane);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_tf32(d, sT + (32 + 16 * mt) * LDT + 32 + 8 * ks, LDT,
+                                 sYw + (8 * ks) * LYW, LYW, lane);
+                    store_c(sT + (32 + 16 * mt) * LDT + 8 * nt, LDT, d, -1.0f, lane);
+                }
             }
+            static_assert((2 * 16 * LX + 4 * 32 * LYW) * 4 <= L::SX_BYTES, "solve temps");
             __syncthreads();
         }
-        // ---------------------------------------------- C3: T to bf16 operand
+        // ---------------------------------------------- C3: [T; T] to the bf16 operand
+        // (A is dead: the tile takes its place.)  Blocks right of the
+        // diagonal are zero.  T twice makes the W | U product M = 128, so its
+        // readback below uses all 128 TMEM lanes.
         for (int u = ltid; u < 64 * 8; u += NTC) {
             const int r = u >> 3, c = (u & 7) * 8;
-            st_bf16x8(t16, 64, r, c, sT + r * LDT + c);
+            uint4 pk = make_uint4(0u, 0u, 0u, 0u);  // bf16 zeros
+            if ((c >> 4) <= (r >> 4)) pk = pack8(sT + r * LDT + c);
+            *reinterpret_cast<uint4 *>(t16 + rs_off(128, r, c)) = pk;
+            *reinterpret_cast<uint4 *>(t16 + rs_off(128, r + 64, c)) = pk;
         }
         phase_sync();
         // ---------------------------------------------- D: W = T (beta K e^b), U = T (beta V)
         if (tid == 0) {
             // beta K e^b and beta V are adjacent column blocks: one N = 2D
-            // product writes W (columns TC_W) and U (columns TC_W + D)
-            constexpr uint32_t id = idesc_bf16(64, 2 * D, false, true);
+            // product with A = [T; T] writes [W | U] into TMEM lanes 0..63
+            // and again into lanes 64..127
+            constexpr uint32_t id = idesc_bf16(128, 2 * D, false, true);
 #pragma unroll 1
             for (int kk = 0; kk < P; ++kk) {
-                const uint64_t a0 = kdesc(task_sm(kk) + L::T16, 64, 0, 0);
+                const uint64_t a0 = kdesc(task_sm(kk) + L::T16, 128, 0, 0);
                 // [beta K e^b | beta V]: rows 0..63 of WQ then UK, 16 KB per column block
                 const uint64_t b0 = mdesc(task_sm(kk) + L::WQ, 128, 0, 0);
 #pragma unroll
@@ -941,25 +998,25 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
         tc_fence_after();
         // ---------------------------------------------- E: W and U tiles
         {
-            // the 2D columns W | U split into NW / 4 parts of CPP columns;
-            // -W into rows 0..63 of WQ, U into rows 0..63 of UK
-            constexpr int CPP = 2 * D / (NW / 4);
-            const int r = acc_row(64, qd, lane);
-            const int w0 = cp * CPP;                   // first column of the part in W | U
-            const bool is_w = w0 < D;
+            // lanes 0..63 read W (columns 0..D-1), lanes 64..127 U (columns
+            // D..2D-1), each in NW / 4 parts of CPP columns; -W into rows
+            // 0..63 of WQ, U into rows 0..63 of UK
+            constexpr int CPP = D / (NW / 4);
+            constexpr int CB = CPP >= 32 ? 32 : 16;
+            const bool is_w = qd < 2;
+            const int r = 32 * (qd & 1) + lane;
+            const int c0 = cp * CPP;
             uint8_t *dst = is_w ? wq : uk;
             const float sgn = is_w ? (additive ? 0.0f : -1.0f) : 1.0f;
-            const int c0 = w0 % D;
+            const uint32_t tc0 = TC_W + (is_w ? 0u : (uint32_t)D) + (uint32_t)c0;
 #pragma unroll
-            for (int cb = 0; cb < CPP; cb += 32) {
-                float v[32];
-                tmem_ld32(tq + TC_W + w0 + cb, v);
-                if (r >= 0) {
+            for (int cb = 0; cb < CPP; cb += CB) {
+                float v[CB];
+                tmem_cols<CB>(tq + tc0 + cb, v);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] *= sgn;
+                for (int i = 0; i < CB; ++i) v[i] *= sgn;
 #pragma unroll
-                    for (int i = 0; i < 32; i += 8) st_bf16x8(dst, 128, r, c0 + cb + i, v + i);
-                }
+                for (int i = 0; i < CB; i += 8) st_bf16x8(dst, 128, r, c0 + cb + i, v + i);
             }
         }
         phase_sync();

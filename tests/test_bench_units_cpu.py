@@ -48,3 +48,19 @@ def test_decode_state_bytes():
     assert (w.n_seq, w.H, w.dk, w.dv) == (256, 32, 128, 128)
     # fp32 state read and written once: 8 bytes per element, 1 GiB per step
     assert bench.decode_state_bytes(w) == 256 * 32 * 128 * 128 * 8 == 1 << 30
+
+
+def test_clock_summary_over_load_windows():
+    """The clock median is taken over the samples inside the measured
+    windows; throttle reasons are reported from those samples."""
+    import bench
+    cs = bench.ClockSampler(0, log_dir="/tmp")
+    cs.proc = object()  # a sampler that ran
+    row = lambda mhz, pc="Not Active": ["0", str(mhz), "2070", "500", "0x0", "Not Active",
+                                        "Not Active", "Not Active", pc]
+    cs.rows = [(0.0, row(800)), (1.0, row(2070)), (1.1, row(2060, "Active")), (3.0, row(900))]
+    cs.windows = [(0.9, 1.2)]
+    s = cs.summary()
+    assert s["samples"] == 4 and s["samples_under_load"] == 2
+    assert s["sm_mhz"] == 2065.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"]
