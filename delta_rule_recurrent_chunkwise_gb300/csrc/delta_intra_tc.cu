@@ -117,7 +117,11 @@ struct Layout {
     // K K^T part, [4][16][16] each) and the flag that some channel needs them
     static constexpr uint32_t DIAG = SEK + 256;
     static constexpr uint32_t SFLAG = DIAG + (GATED ? 2u * 4u * 256u * 4u : 0u);
-    static constexpr uint32_t INFO = SFLAG + 16;               // int4: next task
+    // cu_seqlens copied once per CTA (batches of up to CU_MAX - 1 sequences),
+    // so that the binary search naming a slot's sequence reads shared memory
+    static constexpr int CU_MAX = 256;
+    static constexpr uint32_t CU = SFLAG + 16;                 // int32 [CU_MAX]
+    static constexpr uint32_t INFO = CU + 4 * CU_MAX;          // int4: next task
     static constexpr uint32_t BAR_TMA = INFO + 16;             // mbarrier: raw tiles
     static constexpr uint32_t TASK_BYTES = (BAR_TMA + 8 + 1023) & ~1023u;
     static_assert(UK - WQ == Record<D>::UK, "record image");
@@ -324,11 +328,14 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
     // binary search over cu_seqlens.  The entry is looked up (table_entry)
     // a task ahead of its decoding (task_info), so the loads' latency stays
     // off the critical path.
+    const int *scu = reinterpret_cast<const int *>(sbase + L::CU);
+    const bool cu_in_smem = p.N < L::CU_MAX;
+    auto cu_at = [&](int n) { return cu_in_smem ? scu[n] : p.cu_seqlens[n]; };
     auto table_entry = [&](int64_t t) -> int2 {
         const int2 none = make_int2(0, 0);
         if (t >= p.n_tasks || p.N < 1) return none;
         const int64_t slot = t / H;
-        auto f = [&](int n) { return (int64_t)(p.cu_seqlens[n] / C) + n; };
+        auto f = [&](int n) { return (int64_t)(cu_at(n) / C) + n; };
         if (f(0) > slot) return none;
         int lo = 0, hi = p.N - 1;
         while (lo < hi) {
@@ -336,7 +343,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
             if (f(mid) <= slot) lo = mid;
             else hi = mid - 1;
         }
-        const int a = p.cu_seqlens[lo], e = p.cu_seqlens[lo + 1];
+        const int a = cu_at(lo), e = cu_at(lo + 1);
         if (a < 0 || e < a || e > p.ntok) return none;  // reported by the inter-chunk kernel
         const int64_t j = slot - f(lo);
         if (j >= (e - a + C - 1) / C) return none;      // a gap after the sequence
@@ -385,6 +392,11 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
     // grid to finish)
     grid_wait_prerequisites();
     grid_launch_dependents();
+    if (cu_in_smem) {
+        int *cu_w = reinterpret_cast<int *>(sbase + L::CU);
+        for (int n = tid; n <= p.N; n += blockDim.x) cu_w[n] = p.cu_seqlens[n];
+        __syncthreads();
+    }
     int4 cur = task_info(g * P + kslot, table_entry(g * P + kslot));
     bool tma_pending = false;  // meaningful in the leader, who waits for the loads
     if (leader && cur.y > 0) {
