@@ -374,16 +374,23 @@ def run_ours(args, rank, world, dev, dist):
         nbytes, flops = prefill_algo(w)
         achieved = nbytes / (kern_ms / 1e3) / 1e9
         traffic = ncu_traffic("delta_prefill:" + HEADLINE)
-        # the tensor-core path (it takes a workspace) launches the intra-chunk
-        # and the inter-chunk kernels; the fp32 path one kernel
-        per_call = 2 if pf.ws is not None else 1
+        # the tensor-core path (it takes a workspace): at d = 64 without a
+        # per-channel gate, one cooperative kernel (intra-chunk tasks and the
+        # recurrence together) when the chains fit in half the grid, else the
+        # intra-chunk and the inter-chunk kernels; the fp32 path one kernel
+        per_call = la.la_prefill_delta_launches(
+            len(w.lengths), w.ntok, w.H, w.dk, w.dv, io=la.LA_BF16, flags=pf.flags,
+            has_gate=w.gated)
+        fused = pf.ws is not None and per_call == 1
         result.update(
             value=value, ms_per_step=step_ms, mean_ms_per_step=mor(statistics.mean(ms)),
             gpu_launches=per_call * args.steps,
             roofline={"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                       "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
-                      "kernel": "one la_prefill_delta call: intra-chunk + inter-chunk "
-                                "kernels, timed together",
+                      "kernel": ("one la_prefill_delta call: delta_fused_kernel (intra-chunk "
+                                 "tasks and the recurrence in one cooperative grid)" if fused else
+                                 "one la_prefill_delta call: intra-chunk + inter-chunk "
+                                 "kernels, timed together"),
                       "algorithmic_bytes_per_launch": nbytes,
                       "tensor_tflops": flops / (kern_ms / 1e3) / 1e12,
                       "tensor_frac": flops / (kern_ms / 1e3) / 1e12 / pk["bf16_tflops"],
@@ -458,6 +465,30 @@ def run_ours(args, rank, world, dev, dist):
                 if name == "varlen_prefill":
                     extra[name]["lengths"] = list(gw.lengths)
                 del p
+            # ---- ELU+1 linear attention: the tiny fp32 case and the GPT-2 shape in bf16
+            for name, wlin in (("tiny_linear", wl.workload("tiny_linear")),
+                               ("gpt2_linear_bf16",
+                                wl.Workload("gpt2_linear_bf16", "prefill_linear", 12, 64, 64,
+                                            torch.bfloat16, lengths=(2048,) * 8))):
+                li = wl.prefill_inputs(wlin.lengths, wlin.H, wlin.dk, wlin.dv, wlin.dtype, False,
+                                       seed=rank_seed(rank))
+                lt = {n: li[n].to(dev) for n in ("q", "k", "v", "cu_seqlens")}
+                lo = torch.empty((wlin.ntok, wlin.H, wlin.dv), dtype=wlin.dtype, device=dev)
+                lin_step = lambda: la.la_prefill_linear(lt["q"], lt["k"], lt["v"], lo,
+                                                        lt["cu_seqlens"],
+                                                        cu_seqlens_host=li["cu_seqlens"],
+                                                        stream=stream)
+                with clocks.load():
+                    lms = time_steps(lin_step, max(5, args.steps // 2), 3, flush, stream, barrier)
+                l_ms = mor(statistics.median(lms))
+                esz = torch.tensor([], dtype=wlin.dtype).element_size()
+                lbytes = wlin.ntok * wlin.H * esz * (2 * wlin.dk + 2 * wlin.dv)
+                extra[name] = {"tokens_per_s": wlin.ntok * world / (l_ms / 1e3), "us": l_ms * 1e3,
+                               "hbm_frac": lbytes / (l_ms / 1e3) / 1e9 / pk["hbm_gbs"],
+                               "workload": f"{len(wlin.lengths)} x {wlin.lengths[0]} tokens, "
+                                           f"H={wlin.H}, d={wlin.dk}, {str(wlin.dtype)[6:]}",
+                               "kernel": "linear_chunk_simt_kernel (fp32 CUDA cores)"}
+                del lt, lo
             # ---- backward pass on the GPT-2 shape (gradients of every input)
             bw = wl.workload(HEADLINE)
             b_in = wl.inputs_for(bw, seed=rank_seed(rank))
@@ -646,6 +677,14 @@ def profile_case(args):
         fn = lambda: la.la_backward_delta(t["q"], t["k"], t["v"], t["beta_logits"], None, d_o,
                                           t["cu_seqlens"], init_S=t["init_S"], workspace=ws,
                                           cu_seqlens_host=inp["cu_seqlens"], stream=stream)
+    elif name in ("tiny_linear", "gpt2_linear_bf16"):
+        w = (wl.workload("tiny_linear") if name == "tiny_linear" else
+             wl.Workload(name, "prefill_linear", 12, 64, 64, torch.bfloat16, lengths=(2048,) * 8))
+        li = wl.prefill_inputs(w.lengths, w.H, w.dk, w.dv, w.dtype, False, seed=0)
+        t = {n: li[n].to(dev) for n in ("q", "k", "v", "cu_seqlens")}
+        o = torch.empty((w.ntok, w.H, w.dv), dtype=w.dtype, device=dev)
+        fn = lambda: la.la_prefill_linear(t["q"], t["k"], t["v"], o, t["cu_seqlens"],
+                                          cu_seqlens_host=li["cu_seqlens"], stream=stream)
     elif name in ("decode", "decode_small"):
         w = wl.workload("decode")
         n_seq = w.n_seq if name == "decode" else 128
@@ -696,7 +735,7 @@ def main():
     ap.add_argument("--profile-case", default=None,
                     help="run one workload only (for ncu): gpt2_prefill, gated_prefill, "
                          "varlen_prefill, gpt2_scalar_gate, gpt2_backward, decode, decode_small, "
-                         "gated_small")
+                         "gated_small, tiny_linear, gpt2_linear_bf16")
     args = ap.parse_args()
     if args.profile_case:
         return profile_case(args)

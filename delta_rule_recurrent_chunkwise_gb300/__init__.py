@@ -8,6 +8,7 @@ the library is not built, the first call raises.
 
 Functions (same names as the C ABI):
   la_prefill_linear, la_prefill_delta, la_prefill_delta_workspace_size,
+  la_prefill_delta_launches,
   la_prefill_delta_static, la_decode_step, la_decode_step_slots,
   la_backward_delta, la_check_device, la_selftest_wait_timeout,
   la_status_string.
@@ -26,6 +27,7 @@ LA_F32, LA_BF16 = 0, 1
 LA_L2NORM_K, LA_L2NORM_Q, LA_SILU_QK, LA_GATE_SCALAR, LA_ADDITIVE = 1, 2, 4, 8, 16
 
 EXPORTED = ("la_prefill_linear", "la_prefill_delta", "la_prefill_delta_workspace_size",
+            "la_prefill_delta_launches",
             "la_prefill_delta_static", "la_decode_step", "la_decode_step_slots",
             "la_backward_delta", "la_backward_delta_workspace_size", "la_check_device",
             "la_selftest_wait_timeout", "la_status_string")
@@ -58,6 +60,8 @@ def library():
                                                 ip, ip, ip, fp, u, vp, vp, vp]
         lib.la_prefill_delta_workspace_size.argtypes = [ip, ip, ip, ip, ip, ip, ip]
         lib.la_prefill_delta_workspace_size.restype = sz
+        lib.la_prefill_delta_launches.argtypes = [ip, ip, ip, ip, ip, ip, ip, u, ip]
+        lib.la_prefill_delta_launches.restype = ip
         lib.la_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, ip, ip, ip, ip, ip, fp, u, vp, vp]
         lib.la_decode_step_slots.argtypes = [vp, vp, vp, vp, vp, vp, ip, ip, ip, ip, ip, fp, u,
                                              vp, ip, vp, vp]
@@ -147,6 +151,14 @@ def la_prefill_linear(q, k, v, o, cu_seqlens, init_S=None, init_z=None, final_S=
 
 def la_prefill_delta_workspace_size(N, ntok, H, dk, dv, chunk=64, io=LA_BF16) -> int:
     return int(library().la_prefill_delta_workspace_size(N, ntok, H, dk, dv, chunk, io))
+
+
+def la_prefill_delta_launches(N, ntok, H, dk, dv, chunk=64, io=LA_BF16, flags=LA_L2NORM_K,
+                              has_gate=False) -> int:
+    """Kernels one la_prefill_delta call with these sizes launches on the
+    current device (0: the call would be rejected)."""
+    return int(library().la_prefill_delta_launches(N, ntok, H, dk, dv, chunk, io, flags,
+                                                   1 if has_gate else 0))
 
 
 def la_prefill_delta(q, k, v, beta_logits, gate_logits, o, cu_seqlens, chunk=64, scale=1.0,

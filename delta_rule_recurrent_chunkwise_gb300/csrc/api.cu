@@ -129,6 +129,17 @@ la_status la_prefill_delta(const void *q, const void *k, const void *v, const vo
     return from_cuda(la::launch_delta_simt(a, s));
 }
 
+int la_prefill_delta_launches(int N, int ntok, int H, int dk, int dv, int chunk, la_dtype io,
+                              unsigned flags, int has_gate) {
+    const void *g = has_gate ? reinterpret_cast<const void *>(16) : nullptr;
+    const void *x = reinterpret_cast<const void *>(16);
+    if (check_delta_args(x, x, x, x, g, x, io, reinterpret_cast<const int32_t *>(x), nullptr, N,
+                         ntok, H, dk, dv, chunk, 1.0f, flags) != LA_OK)
+        return 0;
+    return la::delta_tc_launches(N, ntok, H, dk, dv, chunk, io == LA_BF16, has_gate != 0,
+                                 has_gate && (flags & LA_GATE_SCALAR));
+}
+
 la_status la_prefill_delta_static(const void *q, const void *k, const void *v,
                                   const void *beta_logits, const void *gate_logits, void *o,
                                   la_dtype io, const int32_t *cu_seqlens,

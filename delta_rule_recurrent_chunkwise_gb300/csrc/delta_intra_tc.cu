@@ -122,7 +122,9 @@ struct Layout {
     static constexpr int CU_MAX = 256;
     static constexpr uint32_t CU = SFLAG + 16;                 // int32 [CU_MAX]
     static constexpr uint32_t INFO = CU + 4 * CU_MAX;          // int4: next task
-    static constexpr uint32_t BAR_TMA = INFO + 16;             // mbarrier: raw tiles
+    static constexpr uint32_t NIDX = INFO + 16;                // int64: its index
+    static constexpr uint32_t FST = NIDX + 16;                 // int64 [4]: the fetcher's task state
+    static constexpr uint32_t BAR_TMA = FST + 32;              // mbarrier: raw tiles
     static constexpr uint32_t TASK_BYTES = (BAR_TMA + 8 + 1023) & ~1023u;
     static_assert(UK - WQ == Record<D>::UK, "record image");
     // threads per CTA, CTAs per SM, TMEM columns (block products, then W | U)
@@ -240,17 +242,34 @@ struct IntraParams {
 };
 
 
-// SCALAR: one decay per token and head (ungated layout plus per-row factors)
-template <int D, bool GATED, bool SCALAR>
-__global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_PER_SM)
-    delta_intra_kernel(const __grid_constant__ CUtensorMap tm_q,
-                       const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v,
-                       const __grid_constant__ CUtensorMap tm_g, IntraParams p) {
+// Task source of the fused launch (intra-chunk work and the recurrence in
+// one grid): tasks are taken from two global counters in chunk-major order,
+// [0, cutoff) by every CTA and [cutoff, n_tasks) by the CTAs that do not
+// turn to the recurrence afterwards, and every finished record is published
+// through a flag.
+struct FusedSched {
+    unsigned *flags = nullptr;     // [slots * H]: record written and visible
+    unsigned *counters = nullptr;  // [2] task counters (zeroed before the launch)
+    int share_1024 = 0;            // cutoff = n_tasks * share_1024 / 1024
+    int n_chain_ctas = 0;          // CTAs 0 .. n_chain_ctas - 1 run the recurrence afterwards
+};
+
+// Every (chunk slot, head) task this CTA is given.  FUSED selects the task
+// source of the fused launch; otherwise the CTA walks its fixed stride of
+// the task list.  SCALAR: one decay per token and head (ungated layout plus
+// per-row factors).  Allocates n_tmem_cols TMEM columns and returns their
+// base (the caller frees them); returns after a CTA barrier, with every
+// load and store of the task loop complete.
+template <int D, bool GATED, bool SCALAR, bool FUSED>
+__device__ __forceinline__ uint32_t intra_run(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                                              const CUtensorMap &tm_v, const CUtensorMap &tm_g,
+                                              const IntraParams &p, const FusedSched &fs,
+                                              uint32_t n_tmem_cols) {
     using L = Layout<D, GATED>;
     using Rec = Record<D>;
     constexpr int P = L::P, NTC = L::NTC, NW = L::NW;
-    constexpr uint32_t TMEM_COLS = L::TMEM_COLS;
+    static_assert(!FUSED || P == 1, "the fused task source hands out one task at a time");
+    const uint32_t TMEM_COLS = n_tmem_cols;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *const sbase = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -320,43 +339,55 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
     auto task_sm = [&](int kk) { return sbase + kk * L::TASK_BYTES; };
     auto task_tmem = [&](int kk) { return tmem + kk * L::TCOLS; };
 
-    // Task t = slot * H + head.  {first token, length, head, slot}; length 0
-    // marks a slot no chunk occupies (or an entry out of range).  Sequence n
-    // owns slots f(n) .. f(n) + nc(n) - 1, f(n) = cu[n] / 64 + n (f grows
-    // by at least nc(n) from one sequence to the next, so slots never
-    // collide): a slot's sequence is the last n with f(n) <= slot, found by
-    // binary search over cu_seqlens.  The entry is looked up (table_entry)
-    // a task ahead of its decoding (task_info), so the loads' latency stays
-    // off the critical path.
+    // Task -> {first token, length, head, slot}; length 0 marks a task with
+    // no chunk (or an entry out of range).  Sequence n's chunk j has slot
+    // f(n) + j, f(n) = cu[n] / 64 + n (f grows by at least nc(n) from one
+    // sequence to the next, so slots never collide).
+    // Order: with cu_seqlens in shared memory (up to CU_MAX - 1 sequences)
+    // the tasks run chunk-major, t = j' N H + n H + h with j' = j in the
+    // fused launch (its recurrence needs chunk 0 first) and j' = J - 1 - j
+    // otherwise (the first chunks' records, which the recurrence kernel reads
+    // first, are then the last written), J = the longest sequence's chunk
+    // count.  Otherwise
+    // t = slot * H + head, and a slot's sequence is the last n with
+    // f(n) <= slot, found by binary search over cu_seqlens.
     const int *scu = reinterpret_cast<const int *>(sbase + L::CU);
-    const bool cu_in_smem = p.N < L::CU_MAX;
+    const bool cu_in_smem = p.N < L::CU_MAX - 1;  // entry CU_MAX - 1 holds J
     auto cu_at = [&](int n) { return cu_in_smem ? scu[n] : p.cu_seqlens[n]; };
-    auto table_entry = [&](int64_t t) -> int2 {
-        const int2 none = make_int2(0, 0);
-        if (t >= p.n_tasks || p.N < 1) return none;
-        const int64_t slot = t / H;
-        auto f = [&](int n) { return (int64_t)(cu_at(n) / C) + n; };
-        if (f(0) > slot) return none;
-        int lo = 0, hi = p.N - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (f(mid) <= slot) lo = mid;
-            else hi = mid - 1;
+    int J = 0;  // chunks of the longest sequence (chunk-major order)
+    auto task_at = [&](int64_t t, int64_t n_tasks) -> int4 {
+        const int4 none = make_int4(0, 0, 0, 0);
+        if (t < 0 || t >= n_tasks || p.N < 1) return none;
+        int n, h, j;
+        if (cu_in_smem) {
+            const int64_t NH = (int64_t)p.N * H;
+            // fused: forward, the recurrence running alongside needs chunk 0 first
+            j = FUSED ? (int)(t / NH) : J - 1 - (int)(t / NH);
+            const int rem = (int)(t % NH);
+            n = rem / H;
+            h = rem - n * H;
+        } else {
+            const int64_t slot = t / H;
+            h = (int)(t - slot * H);
+            auto f = [&](int m) { return (int64_t)(cu_at(m) / C) + m; };
+            if (f(0) > slot) return none;
+            int lo = 0, hi = p.N - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (f(mid) <= slot) lo = mid;
+                else hi = mid - 1;
+            }
+            n = lo;
+            j = (int)(slot - f(lo));
         }
-        const int a = cu_at(lo), e = cu_at(lo + 1);
+        const int a = cu_at(n), e = cu_at(n + 1);
         if (a < 0 || e < a || e > p.ntok) return none;  // reported by the inter-chunk kernel
-        const int64_t j = slot - f(lo);
-        if (j >= (e - a + C - 1) / C) return none;      // a gap after the sequence
-        const int x = a + (int)j * C;
-        return make_int2(x, e - x < C ? e - x : C);
-    };
-    auto task_info = [&](int64_t t, int2 e) -> int4 {
-        int4 r = make_int4(0, 0, 0, 0);
-        if (t < p.n_tasks && e.x >= 0 && e.y > 0 && e.y <= C && e.x <= p.ntok - e.y) {
-            const int64_t s = t / H;
-            r = make_int4(e.x, e.y, (int)(t - s * H), (int)s);
-        }
-        return r;
+        if (j < 0 || j >= (e - a + C - 1) / C) return none;  // past the sequence's chunks
+        const int x = a + j * C;
+        const int len = e - x < C ? e - x : C;
+        const int64_t slot = (int64_t)(a / C) + n + j;
+        if (slot >= p.n_tasks / H) return none;
+        return make_int4(x, len, h, (int)slot);
     };
     const uint64_t pol = l2_evict_first();  // inputs and records pass through L2 once
     auto issue_tma = [&](int t0, int hh) {
@@ -381,23 +412,93 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
                    : 0.0f;
     };
 
-    // The CTA takes task groups g = blockIdx.x, + gridDim.x, ...; task slot
-    // kslot of group g is task g * P + kslot.  Each task's leader thread
-    // waits for its raw tiles and issues its products; the fetcher issues the
-    // next task's raw-tile loads and stores the record.
-    const int64_t n_groups = (p.n_tasks + P - 1) / P;
-    int64_t g = blockIdx.x;
+    // Each task's leader thread waits for its raw tiles and issues its
+    // products; the fetcher issues the next task's raw-tile loads, stores the
+    // record and hands out the task indices: the current one (g) and, held
+    // in its own shared-memory slots, the next two (the next one's tiles are
+    // loaded during the current task).  Without FUSED the
+    // CTA takes task groups g = blockIdx.x, + gridDim.x, ...; task slot kslot
+    // of group g is task g * P + kslot.
     // cu_seqlens and the inputs may come from the previous launch; the
     // inter-chunk kernel may be scheduled as SMs free up (it waits for this
     // grid to finish)
     grid_wait_prerequisites();
     grid_launch_dependents();
+    int64_t n_tasks = p.n_tasks;
     if (cu_in_smem) {
         int *cu_w = reinterpret_cast<int *>(sbase + L::CU);
         for (int n = tid; n <= p.N; n += blockDim.x) cu_w[n] = p.cu_seqlens[n];
+        if (tid == 0) cu_w[L::CU_MAX - 1] = 0;
         __syncthreads();
+        int jmax = 0;
+        for (int n = tid; n < p.N; n += blockDim.x) {
+            const int a = cu_w[n], e = cu_w[n + 1];
+            if (a >= 0 && e >= a) jmax = max(jmax, (e - a + C - 1) / C);
+        }
+        jmax = __reduce_max_sync(0xffffffffu, jmax);
+        if (lane == 0 && jmax > 0) atomicMax(cu_w + L::CU_MAX - 1, jmax);
+        __syncthreads();
+        J = cu_w[L::CU_MAX - 1];
+        n_tasks = (int64_t)J * p.N * H;
     }
-    int4 cur = task_info(g * P + kslot, table_entry(g * P + kslot));
+    const int64_t n_groups = (n_tasks + P - 1) / P;
+    const bool chain_cta = FUSED && (int)blockIdx.x < fs.n_chain_ctas;
+    const int64_t cutoff = FUSED ? n_tasks * fs.share_1024 / 1024 : 0;
+    // The fetcher's own state, kept in shared memory rather than in
+    // registers every thread would carry: the next two task indices, the
+    // next group of the static order (or, fused, -1 once the shared range is
+    // used up) and the record waiting to be published.
+    int64_t *fst = reinterpret_cast<int64_t *>(sm + L::FST);
+    enum { F_NXT = 0, F_AFT = 1, F_STATIC = 2, F_PUB = 3 };
+    auto next_group = [&]() -> int64_t {
+        if constexpr (FUSED) {
+            if (fst[F_STATIC] >= 0) {
+                const int64_t t = atomicAdd(fs.counters, 1u);
+                if (t < cutoff) return t;
+                fst[F_STATIC] = -1;
+            }
+            if (chain_cta) return -1;
+            const int64_t t = cutoff + atomicAdd(fs.counters + 1, 1u);
+            return t < n_tasks ? t : -1;
+        } else {
+            const int64_t gg = fst[F_STATIC];
+            fst[F_STATIC] = gg + gridDim.x;
+            return gg < n_groups ? gg : -1;
+        }
+    };
+    int64_t *snidx = reinterpret_cast<int64_t *>(sm + L::NIDX);
+    if (fetcher) {
+        fst[F_STATIC] = FUSED ? 0 : (int64_t)blockIdx.x;
+        fst[F_PUB] = -1;
+        const int64_t g0 = next_group();
+        fst[F_NXT] = g0 >= 0 ? next_group() : -1;
+        fst[F_AFT] = fst[F_NXT] >= 0 ? next_group() : -1;
+        *snidx = g0;
+    }
+    __syncthreads();
+    int64_t g = *snidx;                        // -1: no task left
+    int4 cur = task_at(g * P + kslot, n_tasks);
+    // fetcher: the next task becomes the one whose tiles load now (its info
+    // and index to shared memory)
+    auto advance = [&]() -> int4 {
+        const int64_t ni = fst[F_NXT];
+        const int4 nxt = task_at(ni * P + kslot, n_tasks);
+        *sinfo = nxt;
+        *snidx = ni;
+        const int64_t ai = fst[F_AFT];
+        fst[F_NXT] = ai;
+        fst[F_AFT] = ai >= 0 ? next_group() : -1;
+        return nxt;
+    };
+    // fetcher (fused): the record stored last is complete; publish it
+    auto publish = [&]() {
+        const int64_t pub = fst[F_PUB];
+        if (pub >= 0) {
+            fence_proxy_async_global();
+            st_release_gpu(fs.flags + pub, 1u);
+            fst[F_PUB] = -1;
+        }
+    };
     bool tma_pending = false;  // meaningful in the leader, who waits for the loads
     if (leader && cur.y > 0) {
         issue_tma(cur.x, cur.z);
@@ -449,30 +550,27 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
         mma_commit(bar_mma);
     };
 
-    while (g < n_groups) {
-        const int64_t g_next = g + gridDim.x;
-        // the next task's entry, decoded after the operand stage by the
-        // fetcher (the leader goes straight on to this task's raw tiles)
-        int2 nxt_e = make_int2(0, 0);
-        if (fetcher) nxt_e = table_entry(g_next * P + kslot);
+    while (g >= 0) {
         // one task per CTA: cur is the same in every thread
         const bool any_task = P == 1 ? cur.y > 0 : __syncthreads_or(cur.y > 0);
         if (!any_task) {
-            const int4 nxt = leader ? task_info(g_next * P + kslot, table_entry(g_next * P + kslot))
-                                    : make_int4(0, 0, 0, 0);
             // empty slots only: nothing to compute, start the next tasks' loads
-            if (leader) {
-                *sinfo = nxt;
-                if (nxt.y > 0) {
-                    issue_tma(nxt.x, nxt.z);
-                    tma_pending = true;
+            if (fetcher) {
+                if constexpr (FUSED) {
+                    bulk_wait_all();
+                    publish();
                 }
+                advance();
             }
             __syncthreads();
+            if (leader && sinfo->y > 0) {
+                issue_tma(sinfo->x, sinfo->z);
+                tma_pending = true;
+            }
             cur = *sinfo;
+            g = *snidx;
             beta_cur = load_beta(cur);
             gate_cur = load_gate(cur);
-            g = g_next;
             __syncthreads();
             continue;
         }
@@ -786,8 +884,7 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
         // this one computes -- at once when the first product reads the
         // operand tiles, after it has completed when it reads the raw tiles.
         if (fetcher) {
-            const int4 nxt = task_info(g_next * P + kslot, nxt_e);
-            *sinfo = nxt;
+            const int4 nxt = advance();
             if (!raw_p1 && nxt.y > 0) issue_tma(nxt.x, nxt.z);
         }
         // ---------------------------------------------- B: block products
@@ -802,10 +899,18 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
             }
             if (raw_p1 && fetcher && sinfo->y > 0) issue_tma(sinfo->x, sinfo->z);
             tma_pending = sinfo->y > 0;
+            // the previous task's record stores, issued a task phase ago
+            if constexpr (FUSED) {
+                if (fetcher) {
+                    bulk_wait_all();
+                    publish();
+                }
+            }
         }
         tc_fence_after();
         // the next task is known to every thread now: prefetch its beta
         const int4 nx = *sinfo;
+        const int64_t nx_g = *snidx;
         const float beta_nx = load_beta(nx);
         const float gate_nx = load_gate(nx);
         // ---------------------------------------------- C1: Aq tile, A rows
@@ -1041,19 +1146,379 @@ __global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_P
             bulk_store_hint(rec + Rec::AQ, aqk, 8192, pol);
             if (GATED || scalar) bulk_store_hint(rec + Rec::GEND, sgend, 4 * D, pol);
             bulk_commit();
+            if constexpr (FUSED) fst[F_PUB] = (int64_t)cur.w * H + h;
         }
         cur = nx;
         beta_cur = beta_nx;
         gate_cur = gate_nx;
-        g = g_next;
+        g = nx_g;
     }
 
     if (leader && failed && tma_pending) mbar_wait(bar_tma, tma_par, p.err, 3);
-    if (fetcher) bulk_wait_all();
+    if (fetcher) {
+        bulk_wait_all();
+        if constexpr (FUSED) publish();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+    return tmem;
+}
+
+template <int D, bool GATED, bool SCALAR>
+__global__ void __launch_bounds__(Layout<D, GATED>::NT, Layout<D, GATED>::CTAS_PER_SM)
+    delta_intra_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_g, IntraParams p) {
+    using L = Layout<D, GATED>;
+    const uint32_t tmem =
+        intra_run<D, GATED, SCALAR, false>(tm_q, tm_k, tm_v, tm_g, p, FusedSched{}, L::TMEM_COLS);
+    if ((threadIdx.x >> 5) == 0) tmem_dealloc(tmem, L::TMEM_COLS);
+}
+
+// ================================================================ fused launch
+// The recurrence of one (sequence, head) inside the fused launch, on the 8
+// warps of a d = 64 intra-chunk CTA once its share of intra-chunk tasks is
+// done.  It computes what delta_inter_kernel computes, with the same three
+// products per chunk into the same TMEM accumulators (lanes 0..63 u, lanes
+// 64..127 O), and takes each record as soon as the task that wrote it has
+// published it:
+//   u = U - W S;  O = scale ((Q e^b) S + Aq u);  S <- Diag(e^{b_end}) S + K~^T u
+// Roles, joined by mbarriers (every phase chained so that no waiter can
+// fall two phases behind, as in the inter-chunk kernel):
+//   warps 0..3  state, lane quarter w: S -> bf16 operand tile; with a gate,
+//               S *= e^{b_end} of the next chunk in TMEM.  Warps 0, 1 (lanes
+//               0..63) also turn u into its bf16 tile and put the next
+//               chunk's U into the accumulator.
+//   warp 4      one thread issues the products
+//   warp 5      one thread loads each record into one of two buffers once
+//               its flag is set
+//   warps 6, 7  O (lanes 64..127) -> scale -> bf16 -> global, then zero
+struct ChainParams {
+    const uint8_t *records;   // [slots][H] records
+    const unsigned *flags;    // [slots * H] set once a record is complete
+    __nv_bfloat16 *o;
+    const float *init_S;
+    float *final_S;
+    unsigned *err;
+    int H, ntok;
+    float scale;
+};
+
+struct ChainLayout {
+    using Rec = Record<64>;
+    static constexpr int NB = 2;
+    static constexpr uint32_t REC0 = 0;
+    static constexpr uint32_t SB = NB * Rec::BYTES;      // S, bf16 [64][64] RS tile
+    static constexpr uint32_t UT = SB + 64 * 64 * 2;      // u, bf16 [64][64] RS tile
+    static constexpr uint32_t BARS = UT + 64 * 64 * 2;    // mbarriers
+    static constexpr uint32_t END = BARS + 128;
+    // below the intra-chunk role's cu_seqlens copy, which the recurrence reads
+    static_assert(END <= Layout<64, false>::CU, "recurrence buffers overlap the cu_seqlens copy");
+    static_assert(SB % 1024 == 0 && UT % 1024 == 0, "swizzled tiles on 1024-byte boundaries");
+};
+
+enum : int {
+    FB_U = 0, FB_S, FB_O, FB_SREADY, FB_UREADY, FB_UPRE, FB_OFREE0, FB_OFREE1, FB_REC0, FB_REC1,
+    FB_COUNT
+};
+
+template <bool GATED>
+__device__ __forceinline__ void chain_run(uint8_t *sm, uint32_t tmem, const ChainParams &p,
+                                          const int *cu, int chain) {
+    using Lc = ChainLayout;
+    using Rec = Record<64>;
+    constexpr int D = 64;
+    constexpr uint32_t S_COL = 0, ACC = 64;
+    uint8_t *sb = sm + Lc::SB, *ut = sm + Lc::UT;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Lc::BARS);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qd = warp & 3;
+    const int H = p.H, n = chain / H, h = chain - n * H;
+    int t_begin = cu[n], t_end = cu[n + 1];
+    if (t_begin < 0 || t_end < t_begin || t_end > p.ntok) {
+        if (tid == 0) atomicCAS(p.err, 0u, 100u);
+        t_begin = t_end = 0;
+    }
+    const int nc = (t_end - t_begin + C - 1) / C;
+    const int64_t slot0 = (int64_t)(t_begin / C) + n;
+    auto rec_src = [&](int c) { return p.records + ((slot0 + c) * H + h) * (int64_t)Rec::BYTES; };
+    auto buf = [&](int c) { return sm + Lc::REC0 + (uint32_t)(c & 1) * Rec::BYTES; };
+    auto rec_bar = [&](int c) { return &bars[FB_REC0 + (c & 1)]; };
+    auto rec_par = [](int c) { return (uint32_t)(c >> 1) & 1u; };
+    auto ofree = [&](int c) { return &bars[FB_OFREE0 + (c & 1)]; };
+    auto acc = [&](int c) { return ACC + (uint32_t)(c & 1) * D; };
+    const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);
+    const int64_t sbase = ((int64_t)n * H + h) * D * D;
+
+    if (tid == 0) {
+        mbar_init(&bars[FB_U], 1);
+        mbar_init(&bars[FB_S], 1);
+        mbar_init(&bars[FB_O], 1);
+        mbar_init(&bars[FB_SREADY], 4);
+        mbar_init(&bars[FB_UREADY], 4);
+        mbar_init(&bars[FB_UPRE], 2);
+        mbar_init(&bars[FB_OFREE0], 2);
+        mbar_init(&bars[FB_OFREE1], 2);
+        mbar_init(&bars[FB_REC0], 1);
+        mbar_init(&bars[FB_REC1], 1);
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    auto warp_arrive = [&](uint64_t *bar) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar);
+    };
+    // U rows of chunk c into accumulator lanes 0..63 (warps 0, 1)
+    auto preload_u = [&](int c) {
+        const uint8_t *uk = buf(c) + Rec::UK;
+        const int urow = 32 * qd + lane;
+#pragma unroll
+        for (int cb = 0; cb < D; cb += 16) {
+            float v[16];
+            unpack8(*reinterpret_cast<const uint4 *>(uk + rs_off(128, urow, cb)), v);
+            unpack8(*reinterpret_cast<const uint4 *>(uk + rs_off(128, urow, cb + 8)), v + 8);
+            tmem_st16(tq + acc(c) + cb, v);
+        }
+    };
+
+    if (warp == 5) {
+        // ====================================================== loader
+        if (lane == 0) {
+            int issued[2] = {-1, -1};
+            bool ok = true;
+            for (int c = 0; c < nc && ok; ++c) {
+                // chunk c - 2 drained: its buffer is free
+                if (c >= 2 && !(ok = mbar_wait(ofree(c), (uint32_t)(c >> 1) & 1u, p.err, 40))) break;
+                if (!(ok = wait_flag(p.flags + (slot0 + c) * H + h, p.err, 41))) break;
+                fence_proxy_async_global();
+                fence_proxy_async();
+                mbar_arrive_expect_tx(rec_bar(c), Rec::BYTES);
+                bulk_load_hint(buf(c), rec_src(c), Rec::BYTES, rec_bar(c), l2_evict_first());
+                issued[c & 1] = c;
+            }
+            if (!ok) {
+                // whatever happened elsewhere, no load may still be writing
+                // into shared memory when the CTA leaves
+                for (int b = 0; b < 2; ++b)
+                    if (issued[b] >= 0) mbar_wait(rec_bar(issued[b]), rec_par(issued[b]), p.err, 43);
+            }
+        }
+    } else if (warp == 4) {
+        // ====================================================== issuer
+        if (lane == 0 && nc > 0) {
+            constexpr uint32_t id128 = idesc_bf16(128, D, false, true);
+            constexpr uint32_t ids = idesc_bf16(D, D, true, true);
+            const uint64_t bS = mdesc(sb, D, 0, 0), bU = mdesc(ut, C, 0, 0);
+            for (int c = 0; c < nc; ++c) {
+                uint8_t *rb = buf(c);
+                const uint32_t ta = tmem + acc(c);
+                if (!mbar_wait(&bars[FB_SREADY], (uint32_t)c & 1u, p.err, 44)) break;
+                if (!mbar_wait(&bars[FB_UPRE], (uint32_t)c & 1u, p.err, 45)) break;
+                if (!mbar_wait(rec_bar(c), rec_par(c), p.err, 46)) break;
+                tc_fence_after();
+                const uint64_t aWQ = kdesc(rb + Rec::WQ, 128, 0, 0);
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4)
+                    mma_bf16(ta, dstep(aWQ, kstep_units(128, s4)), dstep(bS, s4 * 128), id128, 1);
+                mma_commit(&bars[FB_U]);
+                if (!mbar_wait(&bars[FB_UREADY], (uint32_t)c & 1u, p.err, 47)) break;
+                tc_fence_after();
+                const uint64_t aK = mdesc(rb + Rec::UK, 128, 64, 0);
+                const uint64_t aA = kdesc(rb + Rec::AQ - 8192, 128, 0, 0);
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4)
+                    mma_bf16(tmem + S_COL, dstep(aK, s4 * 128), dstep(bU, s4 * 128), ids, 1);
+                mma_commit(&bars[FB_S]);
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4)
+                    mma_bf16(ta, dstep(aA, s4 * 2), dstep(bU, s4 * 128), id128, 1);
+                // the output warps have taken chunk c - 1 before chunk c's
+                // output phase can complete
+                if (c >= 1 &&
+                    !mbar_wait(ofree(c - 1), (uint32_t)(((c - 1) >> 1) + 1) & 1u, p.err, 48))
+                    break;
+                mma_commit(&bars[FB_O]);
+            }
+        }
+    } else if (warp < 4) {
+        // ====================================================== state (and u)
+        const int srow = acc_row(D, qd, lane);   // state row (key channel), or -1
+        const bool u_warp = qd < 2;
+        const int urow = 32 * qd + lane;
+        bool ok = true;
+        if (GATED && nc > 0) ok = mbar_wait(rec_bar(0), 0, p.err, 50);
+        if (ok) {
+            const float gd = (GATED && nc > 0 && srow >= 0)
+                                 ? reinterpret_cast<const float *>(buf(0) + Rec::GEND)[srow]
+                                 : 1.0f;
+#pragma unroll
+            for (int cb = 0; cb < D; cb += 16) {
+                float v[16];
+                if (srow >= 0 && p.init_S) {
+                    const float4 *src = reinterpret_cast<const float4 *>(p.init_S + sbase + (int64_t)srow * D + cb);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float4 f = src[i];
+                        v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+                }
+                if (srow >= 0) {
+                    st_bf16x8(sb, D, srow, cb, v);
+                    st_bf16x8(sb, D, srow, cb + 8, v + 8);
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] *= gd;
+                tmem_st16(tq + S_COL + cb, v);
+            }
+            fence_proxy_async();
+            warp_arrive(&bars[FB_SREADY]);
+            if (u_warp && nc > 0) {
+                ok = mbar_wait(ofree(0), 0, p.err, 51) && mbar_wait(rec_bar(0), 0, p.err, 52);
+                if (ok) {
+                    tc_fence_after();
+                    preload_u(0);
+                    warp_arrive(&bars[FB_UPRE]);
+                }
+            }
+        }
+        for (int c = 0; c < nc && ok; ++c) {
+            if (u_warp) {
+                if (!(ok = mbar_wait(&bars[FB_U], (uint32_t)c & 1u, p.err, 53))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int cb = 0; cb < D; cb += 32) {
+                    float v[32];
+                    tmem_ld32(tq + acc(c) + cb, v);
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) st_bf16x8(ut, C, urow, cb + i, v + i);
+                }
+                fence_proxy_async();
+            }
+            // every state warp: u tile written, and S decayed for this chunk
+            warp_arrive(&bars[FB_UREADY]);
+            if (u_warp && c + 1 < nc) {
+                if (!(ok = mbar_wait(ofree(c + 1), (uint32_t)((c + 1) >> 1) & 1u, p.err, 54))) break;
+                if (!(ok = mbar_wait(rec_bar(c + 1), rec_par(c + 1), p.err, 55))) break;
+                tc_fence_after();
+                preload_u(c + 1);
+                warp_arrive(&bars[FB_UPRE]);
+            }
+            if (!(ok = mbar_wait(&bars[FB_S], (uint32_t)c & 1u, p.err, 56))) break;
+            tc_fence_after();
+            if (c + 1 < nc) {
+                float v[32];
+#pragma unroll
+                for (int cb = 0; cb < D; cb += 32) {
+                    tmem_ld32(tq + S_COL + cb, v);
+                    if (srow >= 0) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 8) st_bf16x8(sb, D, srow, cb + i, v + i);
+                    }
+                }
+                fence_proxy_async();
+                warp_arrive(&bars[FB_SREADY]);
+                if (GATED) {
+                    if (!(ok = mbar_wait(rec_bar(c + 1), rec_par(c + 1), p.err, 57))) break;
+                    const float gd = srow >= 0
+                                         ? reinterpret_cast<const float *>(buf(c + 1) + Rec::GEND)[srow]
+                                         : 1.0f;
+#pragma unroll
+                    for (int cb = 0; cb < D; cb += 32) {
+                        tmem_ld32(tq + S_COL + cb, v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] *= gd;
+                        tmem_st16(tq + S_COL + cb, *reinterpret_cast<float(*)[16]>(v));
+                        tmem_st16(tq + S_COL + cb + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+                    }
+                }
+            }
+        }
+        if (ok && p.final_S) {
+#pragma unroll
+            for (int cb = 0; cb < D; cb += 16) {
+                float v[16];
+                tmem_ld16(tq + S_COL + cb, v);
+                if (srow >= 0) {
+                    float4 *dst = reinterpret_cast<float4 *>(p.final_S + sbase + (int64_t)srow * D + cb);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                }
+            }
+        }
+    } else {
+        // ====================================================== output (warps 6, 7)
+        const int orow = 32 * (qd - 2) + lane;
+        {
+            float z[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) z[i] = 0.0f;
+#pragma unroll
+            for (int b = 0; b < 2; ++b)
+#pragma unroll
+                for (int cb = 0; cb < D; cb += 16) tmem_st16(tq + acc(b) + cb, z);
+            warp_arrive(&bars[FB_OFREE0]);
+            warp_arrive(&bars[FB_OFREE1]);
+        }
+        for (int c = 0; c < nc; ++c) {
+            if (!mbar_wait(&bars[FB_O], (uint32_t)c & 1u, p.err, 58)) break;
+            tc_fence_after();
+            const int tok0 = t_begin + c * C;
+            const bool valid = orow < t_end - tok0;
+#pragma unroll
+            for (int cb = 0; cb < D; cb += 32) {
+                float v[32];
+                tmem_ld32(tq + acc(c) + cb, v);
+                if (valid) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= p.scale;
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + ((int64_t)(tok0 + orow) * H + h) * D + cb);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dst[i] = pack8(v + 8 * i);
+                }
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+                tmem_st16(tq + acc(c) + cb, *reinterpret_cast<float(*)[16]>(v));
+                tmem_st16(tq + acc(c) + cb + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+            }
+            warp_arrive(ofree(c));
+        }
+    }
+}
+
+// Intra-chunk tasks and the recurrence in one cooperative grid (d = 64, no
+// gate or a scalar gate): every CTA takes intra-chunk tasks in chunk-major
+// order from the shared counters; CTAs 0 .. n_chain_ctas - 1 stop after the
+// first share of them and each runs the recurrence of one (sequence, head),
+// consuming records as the other CTAs publish them.  The intra-chunk work
+// never waits for the recurrence and every CTA is resident (cooperative
+// launch), so every wait ends.
+template <bool SCALAR>
+__global__ void __launch_bounds__(Layout<64, false>::NT, Layout<64, false>::CTAS_PER_SM)
+    delta_fused_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_g, IntraParams p, FusedSched fs,
+                       ChainParams cp) {
+    static_assert(Layout<64, false>::NT == 256, "the recurrence role takes 8 warps");
+    const uint32_t tmem = intra_run<64, false, SCALAR, true>(tm_q, tm_k, tm_v, tm_g, p, fs, 256);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *const sbase = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int *scu = reinterpret_cast<const int *>(sbase + Layout<64, false>::CU);
+    if ((int)blockIdx.x < fs.n_chain_ctas && (int)blockIdx.x < p.N * p.H)
+        chain_run<SCALAR>(sbase, tmem, cp, scu, blockIdx.x);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if ((threadIdx.x >> 5) == 0) tmem_dealloc(tmem, 256);
 }
 
 // The chunk table the backward pass's kernels read (the forward kernels find
@@ -1092,6 +1557,9 @@ cudaError_t launch_t(const TcLaunch &x, cudaStream_t s) {
     const size_t smem = need > floor_ ? need : floor_;
     auto kern = delta_intra_kernel<D, GATED, SCALAR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     const int64_t groups = (p.n_tasks + L::P - 1) / L::P;
     const int64_t slots = (int64_t)x.sms * L::CTAS_PER_SM;
@@ -1100,7 +1568,92 @@ cudaError_t launch_t(const TcLaunch &x, cudaStream_t s) {
     return launch_programmatic(kern, dim3(grid), dim3(L::NT), smem, s, x.mq, x.mk, x.mv, x.mg, p);
 }
 
+// Share of the intra-chunk tasks (in 1/1024) that the recurrence CTAs also
+// take before they turn to their chains: about half lets the recurrence
+// start when it can keep pace with the remaining tasks.
+constexpr int kFusedShare1024 = 512;
+
+template <bool SCALAR>
+cudaError_t launch_fused_t(const TcLaunch &x, cudaStream_t s, int grid) {
+    const PrefillArgs &a = *x.a;
+    IntraParams p{static_cast<const __nv_bfloat16 *>(a.beta_logits),
+                  SCALAR ? static_cast<const __nv_bfloat16 *>(a.gate_logits) : nullptr,
+                  a.cu_seqlens, x.records, x.err, x.slots * a.H, a.N, a.H, a.ntok, a.flags};
+    FusedSched fs;
+    fs.flags = x.flags;
+    fs.counters = x.counters;
+    fs.share_1024 = kFusedShare1024;
+    fs.n_chain_ctas = a.N * a.H;
+    ChainParams cp{x.records, x.flags, static_cast<__nv_bfloat16 *>(a.o), a.init_S, a.final_S,
+                   x.err, a.H, a.ntok, a.scale};
+    using L = Layout<64, false>;
+    const size_t smem = L::TOTAL + 1024 > 77 * 1024 ? L::TOTAL + 1024 : 77 * 1024;
+    auto kern = delta_fused_kernel<SCALAR>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(L::NT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, x.mq, x.mk, x.mv, x.mg, p, fs, cp);
+}
+
+// CTAs of the fused kernel that are resident at once on this device (0 if
+// the device cannot hold two per SM).
+template <bool SCALAR>
+int fused_resident_ctas(int sms) {
+    using L = Layout<64, false>;
+    const size_t smem = L::TOTAL + 1024 > 77 * 1024 ? L::TOTAL + 1024 : 77 * 1024;
+    auto kern = delta_fused_kernel<SCALAR>;
+    // two CTAs per SM need the largest shared-memory carveout
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+        return 0;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, L::NT, smem) != cudaSuccess)
+        return 0;
+    return per_sm >= L::CTAS_PER_SM ? L::CTAS_PER_SM * sms : 0;
+}
+
 }  // namespace
+
+bool delta_fused_eligible(int N, int H, int dk, int dv, bool gate, bool scalar, bool chunk_states,
+                          int sms) {
+    if (dk != 64 || dv != 64 || (gate && !scalar) || chunk_states) return false;
+    if (N < 1 || N >= Layout<64, false>::CU_MAX - 1 || sms < 1) return false;
+    const int grid = scalar ? fused_resident_ctas<true>(sms) : fused_resident_ctas<false>(sms);
+    // the recurrence CTAs (one per chain) leave most of the grid to the
+    // intra-chunk tasks
+    return grid > 0 && (int64_t)N * H <= grid / 2;
+}
+
+bool delta_fused_supported(const TcLaunch &x) {
+    const PrefillArgs &a = *x.a;
+    const bool scalar = a.gate_logits != nullptr && (a.flags & kGateScalar);
+    return x.flags && x.counters &&
+           delta_fused_eligible(a.N, a.H, a.dk, a.dv, a.gate_logits != nullptr, scalar,
+                                a.chunk_states != nullptr, x.sms);
+}
+
+cudaError_t launch_delta_fused(const TcLaunch &x, cudaStream_t s) {
+    const PrefillArgs &a = *x.a;
+    const bool scalar = a.gate_logits != nullptr && (a.flags & kGateScalar);
+    const int grid = scalar ? fused_resident_ctas<true>(x.sms) : fused_resident_ctas<false>(x.sms);
+    if (grid <= 0) return cudaErrorNotSupported;
+    cudaError_t e = cudaMemsetAsync(x.flags, 0, x.flag_bytes, s);
+    if (e != cudaSuccess) return e;
+    return scalar ? launch_fused_t<true>(x, s, grid) : launch_fused_t<false>(x, s, grid);
+}
 
 cudaError_t launch_chunk_table(const TcLaunch &x, cudaStream_t s) {
     const int64_t threads = (int64_t)x.a->N * 32;

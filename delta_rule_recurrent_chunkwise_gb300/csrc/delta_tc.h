@@ -15,6 +15,9 @@ struct TcLaunch {
     const PrefillArgs *a;
     int2 *table;                 // workspace: [slots] chunk table (backward pass)
     uint8_t *records;            // workspace: [slots][H] per-chunk records
+    unsigned *flags;             // workspace: [slots * H] record-published flags (fused launch)
+    unsigned *counters;          // workspace: [2] task counters (fused launch), right after flags
+    size_t flag_bytes;           // bytes of flags and counters (zeroed before a fused launch)
     int64_t slots;
     unsigned *err;               // device error word
     int sms;                     // multiprocessors of the current device
@@ -40,6 +43,12 @@ cudaError_t launch_programmatic(void (*kern)(KArgs...), dim3 grid, dim3 block, s
 }
 
 cudaError_t launch_chunk_table(const TcLaunch &x, cudaStream_t s);
+// One cooperative launch running the intra-chunk tasks and the recurrence
+// together (d = 64, no gate or a scalar gate, when the grid holds the chains).
+bool delta_fused_supported(const TcLaunch &x);
+bool delta_fused_eligible(int N, int H, int dk, int dv, bool gate, bool scalar, bool chunk_states,
+                          int sms);
+cudaError_t launch_delta_fused(const TcLaunch &x, cudaStream_t s);
 cudaError_t launch_delta_intra(const TcLaunch &x, cudaStream_t s);
 cudaError_t launch_delta_inter(const TcLaunch &x, cudaStream_t s);
 

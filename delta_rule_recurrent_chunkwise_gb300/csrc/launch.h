@@ -69,6 +69,11 @@ cudaError_t launch_delta_simt(const PrefillArgs &a, cudaStream_t s);
 // in the caller's workspace (and a chunk table for the backward pass).
 size_t delta_tc_workspace_bytes(int N, int ntok, int H, int dk, int dv, int chunk, bool bf16);
 bool delta_tc_supported(const PrefillArgs &a);
+// Kernels one la_prefill_delta call launches for these sizes (aligned
+// tensors, a workspace of the queried size): 1 or 2 on the tensor-core path,
+// 1 on the CUDA-core path.
+int delta_tc_launches(int N, int ntok, int H, int dk, int dv, int chunk, bool bf16, bool gate,
+                      bool scalar);
 cudaError_t launch_delta_tc(const PrefillArgs &a, cudaStream_t s);
 // Static device scratch behind la_prefill_delta_static (static_scratch.cu,
 // a module of its own; per device, the address is looked up on first use).

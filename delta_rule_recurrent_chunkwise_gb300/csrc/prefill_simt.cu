@@ -232,32 +232,47 @@ __global__ void __launch_bounds__(kNT) delta_chunk_simt_kernel(SimtParams p) {
     }
 }
 
-template <int DK>
-constexpr size_t linear_smem_floats() {
-    return 2 * (size_t)kC * (DK + 1) + (size_t)kC * (kDVS + 1) + (size_t)kC * (kC + 1) +
-           (size_t)DK * (kDVS + 1) + DK + kC;
-}
-
 // ELU+1 linear attention ("From GPT-2 to Kimi K3, explained", section Linear
 // attention, chunked as in the next section):
 //   A = tril(phi(Q) phi(K)^T)                           (inclusive)
 //   O = (phi(Q) S + A V) / (phi(Q) z + A 1)
 //   S <- S + phi(K)^T V,   z <- z + sum_i phi(k_i)
+// One CTA of 256 threads per (sequence, head, 16 value columns), chunk after
+// chunk.  Narrow value slices give more CTAs to short batches; each CTA
+// forms the chunk's score matrix itself (4 x 4 register tiles of the lower
+// triangle, float4 operands), then every thread owns 4 output columns of one
+// row, and the denominator is summed over the row's 4 threads.
+constexpr int kLJ = 16;  // value columns per CTA
+
+template <int DK>
+struct LinLayout {
+    static constexpr int LDQ = DK + 4;   // phi(q), phi(k) rows: 16-byte aligned, float4 columns conflict-free
+    static constexpr int LDP = kC + 4;
+    static constexpr int Q = 0, K = Q + kC * LDQ, P = K + kC * LDQ, V = P + kC * LDP;
+    static constexpr int HS = V + kC * kLJ, Z = HS + DK * kLJ, FLOATS = Z + DK;
+};
+
+__device__ __forceinline__ float dot4(const float4 a, const float4 b) {
+    return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+}
+
+__device__ __forceinline__ void axpy4(float4 &acc, float s, const float4 v) {
+    acc.x = fmaf(s, v.x, acc.x);
+    acc.y = fmaf(s, v.y, acc.y);
+    acc.z = fmaf(s, v.z, acc.z);
+    acc.w = fmaf(s, v.w, acc.w);
+}
+
 template <typename IO, int DK>
 __global__ void __launch_bounds__(kNT) linear_chunk_simt_kernel(SimtParams p) {
-    constexpr int C = kC, DVS = kDVS, NT = kNT;
-    constexpr int LDK = DK + 1, LDV = DVS + 1, LDC = C + 1;
-    extern __shared__ float smem[];
-    float *sK = smem;              // [C][LDK] phi(k)
-    float *sQ = sK + C * LDK;      // [C][LDK] phi(q)
-    float *sV = sQ + C * LDK;      // [C][LDV]
-    float *sA = sV + C * LDV;      // [C][LDC]
-    float *sS = sA + C * LDC;      // [DK][LDV]
-    float *sZ = sS + DK * LDV;     // [DK]
-    float *sDen = sZ + DK;         // [C]
+    using L = LinLayout<DK>;
+    constexpr int C = kC, NT = kNT, LDQ = L::LDQ, LDP = L::LDP, LJ = kLJ;
+    extern __shared__ __align__(16) float smem[];
+    float *sQ = smem + L::Q, *sK = smem + L::K, *sP = smem + L::P, *sV = smem + L::V;
+    float *sH = smem + L::HS, *sZ = smem + L::Z;
 
     const int tid = threadIdx.x;
-    const int n = blockIdx.z, h = blockIdx.y, j0 = blockIdx.x * DVS;
+    const int n = blockIdx.z, h = blockIdx.y, j0 = blockIdx.x * LJ;
     const int H = p.H, dv = p.dv;
     const IO *Q = static_cast<const IO *>(p.q), *K = static_cast<const IO *>(p.k);
     const IO *V = static_cast<const IO *>(p.v);
@@ -270,69 +285,135 @@ __global__ void __launch_bounds__(kNT) linear_chunk_simt_kernel(SimtParams p) {
     const int64_t sbase = ((int64_t)n * H + h) * DK * dv + j0;
     const int64_t zbase = ((int64_t)n * H + h) * DK;
 
-    for (int e = tid; e < DK * DVS; e += NT) {
-        const int c = e / DVS, j = e % DVS;
-        sS[c * LDV + j] = p.init_S ? p.init_S[sbase + (int64_t)c * dv + j] : 0.0f;
+    for (int e = tid; e < DK * LJ; e += NT) {
+        const int c = e / LJ, j = e % LJ;
+        sH[e] = p.init_S ? p.init_S[sbase + (int64_t)c * dv + j] : 0.0f;
     }
     for (int c = tid; c < DK; c += NT) sZ[c] = p.init_z ? p.init_z[zbase + c] : 0.0f;
+
+    // The raw q, k and value-slice elements of a chunk, held in registers:
+    // the next chunk's are loaded (all at once) while this one computes.
+    constexpr int QU = C * DK / 4 / NT;   // 4-element units of q (and k) per thread
+    static_assert(QU * NT * 4 == C * DK && C * LJ / 4 == NT, "load mapping");
+    float rq[QU][4], rk[QU][4], rv[4];
+    auto load_raw = [&](int cs) {
+        const int len = min(C, t_end - cs);
+#pragma unroll
+        for (int u = 0; u < QU; ++u) {
+            const int e = tid + u * NT, r = e / (DK / 4), c = (e % (DK / 4)) * 4;
+            const int64_t g = ((int64_t)(cs + (r < len ? r : 0)) * H + h) * DK + c;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                rq[u][i] = r < len ? to_f32(Q[g + i]) : 0.0f;
+                rk[u][i] = r < len ? to_f32(K[g + i]) : 0.0f;
+            }
+        }
+        const int r = tid / (LJ / 4), j = (tid % (LJ / 4)) * 4;
+        const int64_t g = ((int64_t)(cs + (r < len ? r : 0)) * H + h) * dv + j0 + j;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rv[i] = r < len ? to_f32(V[g + i]) : 0.0f;
+    };
+    if (t_begin < t_end) load_raw(t_begin);
 
     for (int cs = t_begin; cs < t_end; cs += C) {
         const int len = min(C, t_end - cs);
         __syncthreads();
-        for (int e = tid; e < C * DK; e += NT) {
-            const int r = e / DK, c = e % DK;
+        // phi(q), phi(k) (zero rows past the chunk's end) and the value slice
+#pragma unroll
+        for (int u = 0; u < QU; ++u) {
+            const int e = tid + u * NT, r = e / (DK / 4), c = (e % (DK / 4)) * 4;
             const bool ok = r < len;
-            const int64_t g = ((int64_t)(cs + r) * H + h) * DK + c;
-            sK[r * LDK + c] = ok ? elu1_f(to_f32(K[g])) : 0.0f;
-            sQ[r * LDK + c] = ok ? elu1_f(to_f32(Q[g])) : 0.0f;
+            const float4 fq = make_float4(ok ? elu1_f(rq[u][0]) : 0.f, ok ? elu1_f(rq[u][1]) : 0.f,
+                                          ok ? elu1_f(rq[u][2]) : 0.f, ok ? elu1_f(rq[u][3]) : 0.f);
+            const float4 fk = make_float4(ok ? elu1_f(rk[u][0]) : 0.f, ok ? elu1_f(rk[u][1]) : 0.f,
+                                          ok ? elu1_f(rk[u][2]) : 0.f, ok ? elu1_f(rk[u][3]) : 0.f);
+            *reinterpret_cast<float4 *>(sQ + r * LDQ + c) = fq;
+            *reinterpret_cast<float4 *>(sK + r * LDQ + c) = fk;
         }
-        for (int e = tid; e < C * DVS; e += NT) {
-            const int r = e / DVS, j = e % DVS;
-            sV[r * LDV + j] = r < len ? to_f32(V[((int64_t)(cs + r) * H + h) * dv + j0 + j]) : 0.0f;
-        }
+        *reinterpret_cast<float4 *>(sV + (tid / (LJ / 4)) * LJ + (tid % (LJ / 4)) * 4) =
+            make_float4(rv[0], rv[1], rv[2], rv[3]);
         __syncthreads();
-        for (int e = tid; e < C * C; e += NT) {
-            const int r = e / C, i = e % C;
-            float acc = 0.0f;
-            if (i <= r)
-                for (int c = 0; c < DK; ++c) acc += sQ[r * LDK + c] * sK[i * LDK + c];
-            sA[r * LDC + i] = acc;
-        }
-        __syncthreads();
-        if (tid < C) {
-            float d = 0.0f;
-            for (int c = 0; c < DK; ++c) d += sQ[tid * LDK + c] * sZ[c];
-            for (int i = 0; i <= tid; ++i) d += sA[tid * LDC + i];
-            sDen[tid] = d;
-        }
-        __syncthreads();
-        for (int e = tid; e < C * DVS; e += NT) {
-            const int r = e / DVS, j = e % DVS;
-            if (r < len) {
-                float acc = 0.0f;
-                for (int c = 0; c < DK; ++c) acc += sQ[r * LDK + c] * sS[c * LDV + j];
-                for (int i = 0; i <= r; ++i) acc += sA[r * LDC + i] * sV[i * LDV + j];
-                O[((int64_t)(cs + r) * H + h) * dv + j0 + j] = from_f32<IO>(acc / sDen[r]);
+        if (cs + C < t_end) load_raw(cs + C);   // in flight during this chunk's products
+        // scores A[r][i] = phi(q_r) . phi(k_i), i <= r: thread (tr, tc) takes
+        // rows 4 tr .. 4 tr + 3 and columns 4 tc .. 4 tc + 3 (tiles above the
+        // diagonal are never read)
+        {
+            const int tr = tid >> 4, tc = tid & 15;
+            if (tc <= tr) {
+                float acc[4][4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+#pragma unroll 4
+                for (int c = 0; c < DK; c += 4) {
+                    float4 a[4], b[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        a[i] = *reinterpret_cast<const float4 *>(sQ + (4 * tr + i) * LDQ + c);
+                        b[i] = *reinterpret_cast<const float4 *>(sK + (4 * tc + i) * LDQ + c);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) acc[i][j] += dot4(a[i], b[j]);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = 4 * tr + i;
+                    float4 o4;
+                    o4.x = (4 * tc + 0 <= r) ? acc[i][0] : 0.0f;
+                    o4.y = (4 * tc + 1 <= r) ? acc[i][1] : 0.0f;
+                    o4.z = (4 * tc + 2 <= r) ? acc[i][2] : 0.0f;
+                    o4.w = (4 * tc + 3 <= r) ? acc[i][3] : 0.0f;
+                    *reinterpret_cast<float4 *>(sP + r * LDP + 4 * tc) = o4;
+                }
             }
         }
         __syncthreads();
-        for (int e = tid; e < DK * DVS; e += NT) {
-            const int c = e / DVS, j = e % DVS;
-            float acc = 0.0f;
-            for (int i = 0; i < C; ++i) acc += sK[i * LDK + c] * sV[i * LDV + j];
-            sS[c * LDV + j] += acc;
+        // outputs: thread (r, jq) owns columns jq .. jq + 3 of row r; the
+        // row's four threads split the denominator's sums and add them up
+        {
+            const int r = tid >> 2, part = tid & 3, jq = part * 4;
+            float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+            float den = 0.0f;
+            const float *qr = sQ + r * LDQ, *pr = sP + r * LDP;
+#pragma unroll 8
+            for (int c = 0; c < DK; ++c) axpy4(num, qr[c], *reinterpret_cast<const float4 *>(sH + c * LJ + jq));
+            for (int c = part; c < DK; c += 4) den = fmaf(qr[c], sZ[c], den);
+            for (int i = 0; i <= r; ++i) axpy4(num, pr[i], *reinterpret_cast<const float4 *>(sV + i * LJ + jq));
+            for (int i = part; i <= r; i += 4) den += pr[i];
+            den += __shfl_xor_sync(0xffffffffu, den, 1);
+            den += __shfl_xor_sync(0xffffffffu, den, 2);
+            if (r < len) {
+                const float inv = 1.0f / den;
+                IO *dst = O + ((int64_t)(cs + r) * H + h) * dv + j0 + jq;
+                dst[0] = from_f32<IO>(num.x * inv);
+                dst[1] = from_f32<IO>(num.y * inv);
+                dst[2] = from_f32<IO>(num.z * inv);
+                dst[3] = from_f32<IO>(num.w * inv);
+            }
+        }
+        __syncthreads();
+        // state slice and normaliser: S += phi(K)^T V, z += sum of phi(k)
+        for (int e = tid; e < DK * (LJ / 4); e += NT) {
+            const int c = e / (LJ / 4), jq = (e % (LJ / 4)) * 4;
+            float4 acc = *reinterpret_cast<const float4 *>(sH + c * LJ + jq);
+#pragma unroll 8
+            for (int i = 0; i < C; ++i) axpy4(acc, sK[i * LDQ + c], *reinterpret_cast<const float4 *>(sV + i * LJ + jq));
+            *reinterpret_cast<float4 *>(sH + c * LJ + jq) = acc;
         }
         for (int c = tid; c < DK; c += NT) {
-            float acc = 0.0f;
-            for (int i = 0; i < C; ++i) acc += sK[i * LDK + c];
-            sZ[c] += acc;
+            float acc = sZ[c];
+            for (int i = 0; i < C; ++i) acc += sK[i * LDQ + c];
+            sZ[c] = acc;
         }
     }
     __syncthreads();
     if (p.final_S)
-        for (int e = tid; e < DK * DVS; e += NT) {
-            const int c = e / DVS, j = e % DVS;
-            p.final_S[sbase + (int64_t)c * dv + j] = sS[c * LDV + j];
+        for (int e = tid; e < DK * LJ; e += NT) {
+            const int c = e / LJ, j = e % LJ;
+            p.final_S[sbase + (int64_t)c * dv + j] = sH[e];
         }
     if (p.final_z && blockIdx.x == 0)
         for (int c = tid; c < DK; c += NT) p.final_z[zbase + c] = sZ[c];
@@ -345,10 +426,11 @@ SimtParams to_params(const PrefillArgs &a) {
 }
 
 template <typename Kern>
-cudaError_t launch_kernel(Kern kern, size_t smem, const PrefillArgs &a, cudaStream_t s) {
+cudaError_t launch_kernel(Kern kern, size_t smem, const PrefillArgs &a, cudaStream_t s,
+                          int dvs = kDVS) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.dv / kDVS, a.H, a.N);
+    dim3 grid(a.dv / dvs, a.H, a.N);
     kern<<<grid, kNT, smem, s>>>(to_params(a));
     return cudaGetLastError();
 }
@@ -363,8 +445,8 @@ cudaError_t delta_dispatch(const PrefillArgs &a, cudaStream_t s) {
 template <typename IO>
 cudaError_t linear_dispatch(const PrefillArgs &a, cudaStream_t s) {
     if (a.dk == 128)
-        return launch_kernel(linear_chunk_simt_kernel<IO, 128>, linear_smem_floats<128>() * 4, a, s);
-    return launch_kernel(linear_chunk_simt_kernel<IO, 64>, linear_smem_floats<64>() * 4, a, s);
+        return launch_kernel(linear_chunk_simt_kernel<IO, 128>, LinLayout<128>::FLOATS * 4, a, s, kLJ);
+    return launch_kernel(linear_chunk_simt_kernel<IO, 64>, LinLayout<64>::FLOATS * 4, a, s, kLJ);
 }
 
 }  // namespace

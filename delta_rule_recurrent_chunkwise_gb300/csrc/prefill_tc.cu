@@ -74,7 +74,8 @@ size_t delta_tc_workspace_bytes(int N, int ntok, int H, int dk, int dv, int chun
         H < 1)
         return 0;
     const int64_t slots = tile::Workspace::slots(N, ntok);
-    return (size_t)tile::Workspace::table_bytes(N, ntok) + (size_t)slots * H * record_bytes(dk);
+    return (size_t)tile::Workspace::table_bytes(N, ntok) + (size_t)slots * H * record_bytes(dk) +
+           (size_t)tile::Workspace::flag_bytes(N, ntok, H);
 }
 
 bool delta_tc_supported(const PrefillArgs &a) {
@@ -102,9 +103,19 @@ cudaError_t launch_delta_tc(const PrefillArgs &a, cudaStream_t s) {
     x.slots = tile::Workspace::slots(a.N, a.ntok);
     x.table = static_cast<int2 *>(a.workspace);
     x.records = static_cast<uint8_t *>(a.workspace) + tile::Workspace::table_bytes(a.N, a.ntok);
+    x.flags = reinterpret_cast<unsigned *>(x.records + x.slots * a.H * (int64_t)record_bytes(D));
+    x.counters = x.flags + (((x.slots * a.H * 4 + 255) & ~int64_t(255)) / 4);
+    x.flag_bytes = (size_t)tile::Workspace::flag_bytes(a.N, a.ntok, a.H);
     x.err = device_error_word();
     x.sms = sm_count();
     if (!x.err) return cudaErrorInvalidValue;
+    // d = 64 without a per-channel gate: both halves in one cooperative
+    // launch when the device holds the whole grid (else the two launches)
+    if (delta_fused_supported(x)) {
+        const cudaError_t ef = launch_delta_fused(x, s);
+        if (ef == cudaSuccess) return ef;
+        cudaGetLastError();  // clear the refused launch; fall back below
+    }
     // The chunk table is read only by the backward pass's kernels (which ask
     // for per-chunk states); the intra-chunk kernel finds its chunks from
     // cu_seqlens itself.
@@ -112,6 +123,12 @@ cudaError_t launch_delta_tc(const PrefillArgs &a, cudaStream_t s) {
     if (e == cudaSuccess) e = launch_delta_intra(x, s);
     if (e == cudaSuccess) e = launch_delta_inter(x, s);
     return e;
+}
+
+int delta_tc_launches(int N, int ntok, int H, int dk, int dv, int chunk, bool bf16, bool gate,
+                      bool scalar) {
+    if (delta_tc_workspace_bytes(N, ntok, H, dk, dv, chunk, bf16) == 0) return 1;  // CUDA-core kernel
+    return delta_fused_eligible(N, H, dk, dv, gate, scalar, false, sm_count()) ? 1 : 2;
 }
 
 unsigned *device_error_word() {

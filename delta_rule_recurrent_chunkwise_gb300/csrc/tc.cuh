@@ -95,6 +95,38 @@ __device__ __forceinline__ void grid_wait_prerequisites() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// ------------------------------------------------- flags between CTAs
+// Orders this thread's completed async-proxy global accesses (finished bulk
+// stores) with its later generic accesses, and the other way round.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_release_gpu(unsigned *p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(v)
+                 : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];"
+                 : "=r"(v)
+                 : "l"(reinterpret_cast<uint64_t>(p))
+                 : "memory");
+    return v;
+}
+
+// Waits (bounded, about half a second) until *flag is nonzero; records `code`
+// in *err and returns false if it never is.
+__device__ __forceinline__ bool wait_flag(const unsigned *flag, unsigned *err, unsigned code) {
+    for (uint32_t i = 0; i < (1u << 22); ++i) {
+        if (ld_acquire_gpu(flag) != 0u) return true;
+        __nanosleep(100);
+    }
+    if (err) atomicCAS(err, 0u, code);
+    return false;
+}
+
 // ---------------------------------------------------------------- proxies
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy reads (tcgen05.mma operands, TMA stores).

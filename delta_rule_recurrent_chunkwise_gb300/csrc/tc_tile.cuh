@@ -113,13 +113,19 @@ struct Record {
 
 // Workspace of the tensor-core path: the chunk table (written only when the
 // backward pass asks for per-chunk states; one {first token,
-// length} pair per chunk slot) followed by the records, [slot][head].
+// length} pair per chunk slot) followed by the records, [slot][head], then
+// the flags and counters of the fused launch.
 // Sequence n's chunk j occupies slot cu[n]/64 + n + j; slots never collide
 // and number at most ntok/64 + N + 1.
 struct Workspace {
     static inline int64_t slots(int N, int ntok) { return (int64_t)ntok / C + N + 1; }
     static inline int64_t table_bytes(int N, int ntok) {
         return (slots(N, ntok) * 8 + 1023) & ~int64_t(1023);
+    }
+    // after the records: one flag per record and two task counters, for the
+    // launch that runs the intra-chunk tasks and the recurrence together
+    static inline int64_t flag_bytes(int N, int ntok, int H) {
+        return ((slots(N, ntok) * H * 4 + 255) & ~int64_t(255)) + 256;
     }
 };
 

@@ -135,9 +135,25 @@ la_status la_prefill_delta(const void *q, const void *k, const void *v, const vo
  * sequential state pass through this buffer: 8 bytes per chunk slot (a
  * chunk table, filled only by la_backward_delta's forward pass), then one
  * record per (chunk slot, head) of 41 KB (d = 64) or 73 KB (d = 128), with
- * at most ntok/64 + N + 1 slots.  0 otherwise. */
+ * at most ntok/64 + N + 1 slots, then a 4-byte flag per record and 256
+ * bytes of task counters (used when both passes run in one launch, d = 64).
+ * 0 otherwise. */
 size_t la_prefill_delta_workspace_size(int N, int ntok, int H, int dk, int dv, int chunk,
                                        la_dtype io);
+
+/* Number of kernels one la_prefill_delta call with these sizes and options
+ * launches on the current device, given 16-byte-aligned tensors and a
+ * workspace of la_prefill_delta_workspace_size bytes (has_gate: whether
+ * gate_logits is given): 1 when d = 64 without a per-channel gate and the
+ * N * H (sequence, head) chains fit in half of the device's resident grid
+ * (one cooperative kernel runs the chunk-parallel half and the state
+ * recurrence together; a memset of the workspace's flags precedes it), 2 on
+ * the other tensor-core configurations (chunk-parallel kernel, then the
+ * recurrence kernel), 1 on the CUDA-core path; 0 if la_prefill_delta would
+ * reject the arguments.  For planning (graph capture, launch accounting);
+ * the page has no counterpart. */
+int la_prefill_delta_launches(int N, int ntok, int H, int dk, int dv, int chunk, la_dtype io,
+                              unsigned flags, int has_gate);
 
 /* la_prefill_delta without a caller workspace, allocating nothing: the
  * per-chunk scratch comes from one library-owned static device buffer of

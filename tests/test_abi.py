@@ -107,7 +107,9 @@ def test_decode_and_linear_reject_bad_arguments(lib):
 
 def test_workspace_size_covers_the_chunk_records(lib):
     """The tensor-core path (bf16 I/O, dk == dv in {64, 128}) keeps one record
-    per (64-token chunk slot, head); every other configuration needs none."""
+    per (64-token chunk slot, head), then one 4-byte flag per record and two
+    task counters (256 bytes) for the launch that runs both halves together;
+    every other configuration needs none."""
     ws = la.la_prefill_delta_workspace_size
     assert ws(4, 1024, 32, 128, 128, 64, la.LA_F32) == 0
     assert ws(4, 1024, 32, 64, 128, 64, la.LA_BF16) == 0
@@ -117,7 +119,8 @@ def test_workspace_size_covers_the_chunk_records(lib):
         for N, ntok, H in ((1, 64, 1), (4, 1024, 32), (5, 65536, 16), (3, 100, 2)):
             slots = ntok // 64 + N + 1
             table = (slots * 8 + 1023) // 1024 * 1024
-            assert ws(N, ntok, H, D, D, 64, la.LA_BF16) == table + slots * H * rec_bytes
+            flags = (slots * H * 4 + 255) // 256 * 256 + 256
+            assert ws(N, ntok, H, D, D, 64, la.LA_BF16) == table + slots * H * rec_bytes + flags
 
 
 def test_prefill_rejects_missing_workspace(lib):
@@ -196,3 +199,19 @@ def test_backward_checks_arguments_and_workspace(lib):
     assert b(*gated, *outs, FAKE, need, None) == la.LA_ERR_INVALID_ARG         # no d_gate_logits
     odd = head[:13] + (96,) + head[14:]
     assert b(*odd, *outs, FAKE, need, None) == la.LA_ERR_UNSUPPORTED
+
+
+def test_launch_count_query(lib):
+    """la_prefill_delta_launches: 1 for the CUDA-core path, 1 or 2 for the
+    tensor-core path (2 wherever no device can hold the one-launch grid, as
+    on a machine without a GPU), 0 for arguments la_prefill_delta rejects."""
+    q = la.la_prefill_delta_launches
+    assert q(2, 256, 4, 64, 64, io=la.LA_F32) == 1
+    assert q(2, 256, 4, 128, 128, io=la.LA_BF16, has_gate=True) == 2
+    assert q(2, 256, 4, 64, 64, io=la.LA_BF16) in (1, 2)
+    import torch
+    if not torch.cuda.is_available():
+        assert q(2, 256, 4, 64, 64, io=la.LA_BF16) == 2
+    assert q(2, 256, 4, 96, 96, io=la.LA_BF16) == 0          # unsupported head size
+    assert q(0, 256, 4, 64, 64, io=la.LA_BF16) == 0           # no sequence
+    assert q(2, 256, 4, 64, 64, io=la.LA_BF16, flags=la.LA_GATE_SCALAR) == 0  # scalar gate, no gate

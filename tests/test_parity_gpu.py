@@ -60,6 +60,23 @@ def test_delta_ragged_bf16(cuda_lib, dk, dv):
     check_delta(cuda_lib, inp, torch.bfloat16)
 
 
+@pytest.mark.parametrize("flags", [oracle.L2NORM_K, oracle.L2NORM_K | oracle.ADDITIVE])
+def test_delta_ragged_bf16_d64_ungated(cuda_lib, flags):
+    """d = 64 without a per-channel gate: the one-launch path that runs the
+    intra-chunk tasks and the recurrence together (ragged lengths, an empty
+    sequence, initial states, with and without the delta term)."""
+    inp = wl.prefill_inputs(RAGGED, 3, 64, 64, torch.bfloat16, False, seed=12, init_state=True)
+    check_delta(cuda_lib, inp, torch.bfloat16, flags=flags)
+
+
+def test_delta_bf16_d64_many_chains(cuda_lib):
+    """160 (sequence, head) chains, more than half the resident grid: the
+    same configuration takes the two-launch path."""
+    lens = [70, 1, 129, 64] * 10
+    inp = wl.prefill_inputs(lens, 4, 64, 64, torch.bfloat16, False, seed=13, init_state=True)
+    check_delta(cuda_lib, inp, torch.bfloat16, heads=[0, 3])
+
+
 def test_delta_resume_matches_single_pass(cuda_lib):
     la = cuda_lib
     T, t1 = 300, 131
