@@ -249,7 +249,9 @@ class Prefill:
         self.o = torch.empty((w.ntok, w.H, w.dv), dtype=w.dtype, device=dev)
         self.fS = (torch.empty((len(w.lengths), w.H, w.dk, w.dv), device=dev)
                    if final_states else None)
-        nbytes = la.la_prefill_delta_workspace_size(len(w.lengths), w.ntok, w.H, w.dk, w.dv)
+        self.chunk = w.extra.get("chunk", 64)
+        nbytes = la.la_prefill_delta_workspace_size(len(w.lengths), w.ntok, w.H, w.dk, w.dv,
+                                                    self.chunk)
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
         self.cu_host = inp["cu_seqlens"]
         self.flags = la.LA_L2NORM_K | (la.LA_GATE_SCALAR if w.extra.get("scalar_gate") else 0)
@@ -257,7 +259,8 @@ class Prefill:
     def step(self, stream):
         t = self.t
         self.la.la_prefill_delta(t["q"], t["k"], t["v"], t["beta_logits"], t["gate_logits"],
-                                 self.o, t["cu_seqlens"], flags=self.flags, final_S=self.fS,
+                                 self.o, t["cu_seqlens"], chunk=self.chunk, flags=self.flags,
+                                 final_S=self.fS,
                                  workspace=self.ws, cu_seqlens_host=self.cu_host, stream=stream)
 
 
@@ -450,7 +453,7 @@ def run_ours(args, rank, world, dev, dist):
                                "state_bytes_per_step": decode_state_bytes(dw)}
             del toks, state, d
             # ---- gated and varlen prefills
-            for name in ("gated_prefill", "varlen_prefill", "gpt2_scalar_gate"):
+            for name in ("gated_prefill", "varlen_prefill", "gpt2_scalar_gate", "gpt2_chunk128"):
                 gw = wl.workload(name, seed=0)
                 fs = name == "varlen_prefill"
                 p = Prefill(la, gw, seed=rank_seed(rank), dev=dev, final_states=fs)
@@ -464,6 +467,9 @@ def run_ours(args, rank, world, dev, dist):
                                "tensor_frac": fl / (g_ms / 1e3) / 1e12 / pk["bf16_tflops"]}
                 if name == "varlen_prefill":
                     extra[name]["lengths"] = list(gw.lengths)
+                if name == "gpt2_chunk128":
+                    extra[name]["note"] = ("chunk 128: intra-chunk pass per 64 tokens, recurrence over "
+                                           "128-token chunks; tensor_frac counts the chunk-64 FLOPs")
                 del p
             # ---- ELU+1 linear attention: the tiny fp32 case and the GPT-2 shape in bf16
             for name, wlin in (("tiny_linear", wl.workload("tiny_linear")),
@@ -734,7 +740,7 @@ def main():
                     help="units of a full launch / units of the captured launch")
     ap.add_argument("--profile-case", default=None,
                     help="run one workload only (for ncu): gpt2_prefill, gated_prefill, "
-                         "varlen_prefill, gpt2_scalar_gate, gpt2_backward, decode, decode_small, "
+                         "varlen_prefill, gpt2_scalar_gate, gpt2_chunk128, gpt2_backward, decode, decode_small, "
                          "gated_small, tiny_linear, gpt2_linear_bf16")
     args = ap.parse_args()
     if args.profile_case:

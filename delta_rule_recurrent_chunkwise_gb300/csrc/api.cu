@@ -51,7 +51,10 @@ la_status check_delta_args(const void *q, const void *k, const void *v, const vo
     if (flags & ~(LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK | LA_GATE_SCALAR | LA_ADDITIVE))
         return LA_ERR_INVALID_ARG;
     if ((flags & LA_GATE_SCALAR) && !gate_logits) return LA_ERR_INVALID_ARG;
-    if (!head_size_ok(dk) || !head_size_ok(dv) || chunk != 64) return LA_ERR_UNSUPPORTED;
+    if (!head_size_ok(dk) || !head_size_ok(dv)) return LA_ERR_UNSUPPORTED;
+    // chunk 128: the tensor-core path (bf16 I/O) with dk = dv = 64
+    if (chunk != 64 && !(chunk == 128 && io == LA_BF16 && dk == 64 && dv == 64))
+        return LA_ERR_UNSUPPORTED;
     if (N > 65535 || H > 65535) return LA_ERR_UNSUPPORTED;
     return check_cu_host(cu_seqlens_host, N, ntok);
 }
@@ -124,8 +127,11 @@ la_status la_prefill_delta(const void *q, const void *k, const void *v, const vo
     la::PrefillArgs a{q, k, v, beta_logits, gate_logits, o, cu_seqlens, N, ntok, H, dk, dv, scale,
                       flags, init_S, nullptr, final_S, nullptr, io == LA_BF16, workspace,
                       workspace_bytes};
+    a.chunk = chunk;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (la::delta_tc_supported(a)) return from_cuda(la::launch_delta_tc(a, s));
+    // the CUDA-core kernels step over 64-token chunks only
+    if (chunk != 64) return LA_ERR_UNSUPPORTED;
     return from_cuda(la::launch_delta_simt(a, s));
 }
 

@@ -51,5 +51,7 @@ bool delta_fused_eligible(int N, int H, int dk, int dv, bool gate, bool scalar, 
 cudaError_t launch_delta_fused(const TcLaunch &x, cudaStream_t s);
 cudaError_t launch_delta_intra(const TcLaunch &x, cudaStream_t s);
 cudaError_t launch_delta_inter(const TcLaunch &x, cudaStream_t s);
+// The recurrence over 128-token chunks (pairs of 64-token records; d = 64).
+cudaError_t launch_delta_inter128(const TcLaunch &x, cudaStream_t s);
 
 }  // namespace la

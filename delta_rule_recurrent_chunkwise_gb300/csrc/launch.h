@@ -24,6 +24,10 @@ struct PrefillArgs {
     // start of every chunk, fp32 [slot][H][dk][dv] (slot as in the chunk
     // table), or null.  With it, o may be null (no output written).
     float *chunk_states = nullptr;
+    // Tokens per chunk of the recurrence: 64, or 128 on the tensor-core path
+    // with dk = dv = 64 (the records stay per 64 tokens; the recurrence pairs
+    // them).
+    int chunk = 64;
 };
 
 struct DecodeArgs {

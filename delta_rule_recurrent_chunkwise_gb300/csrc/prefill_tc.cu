@@ -70,8 +70,9 @@ size_t record_bytes(int D) {
 }  // namespace
 
 size_t delta_tc_workspace_bytes(int N, int ntok, int H, int dk, int dv, int chunk, bool bf16) {
-    if (!bf16 || dk != dv || (dk != 64 && dk != 128) || chunk != tile::C || N < 1 || ntok < 0 ||
-        H < 1)
+    // chunk 128 (d = 64 only) keeps the 64-token records: the same workspace
+    const bool chunk_ok = chunk == tile::C || (chunk == 2 * tile::C && dk == 64);
+    if (!bf16 || dk != dv || (dk != 64 && dk != 128) || !chunk_ok || N < 1 || ntok < 0 || H < 1)
         return 0;
     const int64_t slots = tile::Workspace::slots(N, ntok);
     return (size_t)tile::Workspace::table_bytes(N, ntok) + (size_t)slots * H * record_bytes(dk) +
@@ -80,7 +81,9 @@ size_t delta_tc_workspace_bytes(int N, int ntok, int H, int dk, int dv, int chun
 
 bool delta_tc_supported(const PrefillArgs &a) {
     auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-    const size_t ws = delta_tc_workspace_bytes(a.N, a.ntok, a.H, a.dk, a.dv, tile::C, a.bf16);
+    const size_t ws = delta_tc_workspace_bytes(a.N, a.ntok, a.H, a.dk, a.dv, a.chunk, a.bf16);
+    // per-chunk states (the backward pass) are kept at 64-token chunks only
+    if (a.chunk != tile::C && a.chunk_states) return false;
     return ws > 0 && a.workspace && a.workspace_bytes >= ws &&
            (reinterpret_cast<uintptr_t>(a.workspace) & 255u) == 0 && al16(a.q) && al16(a.k) &&
            al16(a.v) && al16(a.o) && (!a.gate_logits || al16(a.gate_logits)) &&
@@ -111,7 +114,7 @@ cudaError_t launch_delta_tc(const PrefillArgs &a, cudaStream_t s) {
     if (!x.err) return cudaErrorInvalidValue;
     // d = 64 without a per-channel gate: both halves in one cooperative
     // launch when the device holds the whole grid (else the two launches)
-    if (delta_fused_supported(x)) {
+    if (a.chunk == tile::C && delta_fused_supported(x)) {
         const cudaError_t ef = launch_delta_fused(x, s);
         if (ef == cudaSuccess) return ef;
         cudaGetLastError();  // clear the refused launch; fall back below
@@ -121,13 +124,15 @@ cudaError_t launch_delta_tc(const PrefillArgs &a, cudaStream_t s) {
     // cu_seqlens itself.
     cudaError_t e = a.chunk_states ? launch_chunk_table(x, s) : cudaSuccess;
     if (e == cudaSuccess) e = launch_delta_intra(x, s);
-    if (e == cudaSuccess) e = launch_delta_inter(x, s);
+    if (e == cudaSuccess)
+        e = a.chunk == 2 * tile::C ? launch_delta_inter128(x, s) : launch_delta_inter(x, s);
     return e;
 }
 
 int delta_tc_launches(int N, int ntok, int H, int dk, int dv, int chunk, bool bf16, bool gate,
                       bool scalar) {
     if (delta_tc_workspace_bytes(N, ntok, H, dk, dv, chunk, bf16) == 0) return 1;  // CUDA-core kernel
+    if (chunk != tile::C) return 2;
     return delta_fused_eligible(N, H, dk, dv, gate, scalar, false, sm_count()) ? 1 : 2;
 }
 

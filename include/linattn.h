@@ -112,7 +112,13 @@ la_status la_prefill_linear(const void *q, const void *k, const void *v, void *o
  * LA_GATE_SCALAR it is [ntok][H] and alpha_t applies to all channels.
  * flags: LA_L2NORM_K | LA_L2NORM_Q | LA_SILU_QK | LA_GATE_SCALAR | LA_ADDITIVE
  * (above).
- * chunk: tokens per chunk; 64 is the supported value.
+ * chunk: tokens per chunk of the state recurrence, 64 or 128 (the page
+ * names both as the usual sizes).  128 needs io = LA_BF16 and dk = dv = 64
+ * (else LA_ERR_UNSUPPORTED): the chunk-parallel pass still forms the UT/WY
+ * operands per 64 tokens, and the recurrence joins each pair of them into
+ * the 128-token chunk's operands (the off-diagonal block of a two-level
+ * blocked solve) before its step, so the sequential chain runs once per 128
+ * tokens.  The results agree with chunk 64 up to rounding.
  * scale: output scale (the page's delta-rule listings use 1.0).
  * init_S: nullable [N][H][dk][dv]; final_S: nullable, may equal init_S.
  * workspace / workspace_bytes: device scratch of at least
@@ -128,8 +134,9 @@ la_status la_prefill_delta(const void *q, const void *k, const void *v, const vo
                            size_t workspace_bytes, void *stream);
 
 /* Scratch bytes la_prefill_delta needs for these sizes; ntok = total packed
- * tokens.  Nonzero exactly for the tensor-core configuration (io = LA_BF16,
- * dk = dv in {64, 128}, chunk = 64), whose first pass computes everything
+ * tokens.  Nonzero exactly for the tensor-core configurations (io = LA_BF16,
+ * dk = dv in {64, 128}, chunk = 64; or dk = dv = 64, chunk = 128, which
+ * needs the same bytes), whose first pass computes everything
  * that depends on one chunk alone (the WY/UT operands of eq. 10 and the
  * decayed q, k of the chunk) for all chunks in parallel and hands it to the
  * sequential state pass through this buffer: 8 bytes per chunk slot (a
@@ -144,13 +151,12 @@ size_t la_prefill_delta_workspace_size(int N, int ntok, int H, int dk, int dv, i
 /* Number of kernels one la_prefill_delta call with these sizes and options
  * launches on the current device, given 16-byte-aligned tensors and a
  * workspace of la_prefill_delta_workspace_size bytes (has_gate: whether
- * gate_logits is given): 1 when d = 64 without a per-channel gate and the
- * N * H (sequence, head) chains fit in half of the device's resident grid
- * (one cooperative kernel runs the chunk-parallel half and the state
- * recurrence together; a memset of the workspace's flags precedes it), 2 on
- * the other tensor-core configurations (chunk-parallel kernel, then the
- * recurrence kernel), 1 on the CUDA-core path; 0 if la_prefill_delta would
- * reject the arguments.  For planning (graph capture, launch accounting);
+ * gate_logits is given): 2 on the tensor-core configurations
+ * (chunk-parallel kernel, then the recurrence kernel), 1 on the CUDA-core
+ * path; 0 if la_prefill_delta would reject the arguments.  (A one-launch
+ * form for d = 64 -- one cooperative kernel running both passes, after a
+ * memset of the workspace's flags -- is built but not dispatched; this
+ * query would report 1 for the calls it would take.)  For planning (graph capture, launch accounting);
  * the page has no counterpart. */
 int la_prefill_delta_launches(int N, int ntok, int H, int dk, int dv, int chunk, la_dtype io,
                               unsigned flags, int has_gate);

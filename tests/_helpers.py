@@ -22,7 +22,7 @@ def f64(t):
     return None if t is None else t.detach().to("cpu").double().numpy()
 
 
-def gpu_prefill_delta(la, inp, flags=None, scale=1.0, final=True, init=True):
+def gpu_prefill_delta(la, inp, flags=None, scale=1.0, final=True, init=True, chunk=64):
     dev = torch.device("cuda")
     q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
     bl = None if inp["beta_logits"] is None else inp["beta_logits"].to(dev)
@@ -32,7 +32,7 @@ def gpu_prefill_delta(la, inp, flags=None, scale=1.0, final=True, init=True):
     o = torch.full((q.shape[0], H, dv), float("nan"), dtype=q.dtype, device=dev)
     iS = inp["init_S"].to(dev) if (init and inp.get("init_S") is not None) else None
     fS = torch.full((N, H, dk, dv), float("nan"), device=dev) if final else None
-    la.la_prefill_delta(q, k, v, bl, gl, o, cu, scale=scale,
+    la.la_prefill_delta(q, k, v, bl, gl, o, cu, chunk=chunk, scale=scale,
                         flags=la.LA_L2NORM_K if flags is None else flags, init_S=iS, final_S=fS,
                         cu_seqlens_host=inp["cu_seqlens"])
     assert la.la_check_device() == la.LA_OK

@@ -73,7 +73,10 @@ def prefill_delta(lib, **kw):
     (dict(scale=float("nan")), la.LA_ERR_INVALID_ARG),
     (dict(dk=96), la.LA_ERR_UNSUPPORTED),
     (dict(dv=32), la.LA_ERR_UNSUPPORTED),
-    (dict(chunk=128), la.LA_ERR_UNSUPPORTED),
+    (dict(chunk=96), la.LA_ERR_UNSUPPORTED),
+    (dict(chunk=256), la.LA_ERR_UNSUPPORTED),
+    (dict(chunk=128, dk=128, dv=128), la.LA_ERR_UNSUPPORTED),   # chunk 128: d = 64 only
+    (dict(chunk=128, io=la.LA_F32), la.LA_ERR_UNSUPPORTED),     # and the tensor-core path only
     (dict(chunk=0), la.LA_ERR_INVALID_ARG),
 ])
 def test_prefill_delta_rejects_bad_arguments(lib, kw, code):
@@ -121,6 +124,12 @@ def test_workspace_size_covers_the_chunk_records(lib):
             table = (slots * 8 + 1023) // 1024 * 1024
             flags = (slots * H * 4 + 255) // 256 * 256 + 256
             assert ws(N, ntok, H, D, D, 64, la.LA_BF16) == table + slots * H * rec_bytes + flags
+    # chunk 128 (d = 64) keeps the 64-token records: the same bytes; no other
+    # configuration takes it
+    for N, ntok, H in ((1, 64, 1), (4, 1024, 32), (3, 100, 2)):
+        assert ws(N, ntok, H, 64, 64, 128, la.LA_BF16) == ws(N, ntok, H, 64, 64, 64, la.LA_BF16)
+    assert ws(4, 1024, 32, 128, 128, 128, la.LA_BF16) == 0
+    assert ws(4, 1024, 32, 64, 64, 96, la.LA_BF16) == 0
 
 
 def test_prefill_rejects_missing_workspace(lib):
@@ -215,3 +224,6 @@ def test_launch_count_query(lib):
     assert q(2, 256, 4, 96, 96, io=la.LA_BF16) == 0          # unsupported head size
     assert q(0, 256, 4, 64, 64, io=la.LA_BF16) == 0           # no sequence
     assert q(2, 256, 4, 64, 64, io=la.LA_BF16, flags=la.LA_GATE_SCALAR) == 0  # scalar gate, no gate
+    assert q(2, 256, 4, 64, 64, chunk=128, io=la.LA_BF16) == 2              # intra, then the 128-token recurrence
+    assert q(2, 256, 4, 128, 128, chunk=128, io=la.LA_BF16) == 0
+    assert q(2, 256, 4, 64, 64, chunk=128, io=la.LA_F32) == 0

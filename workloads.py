@@ -69,6 +69,9 @@ def workload(name: str, seed: int = 0) -> Workload:
     if name == "gpt2_scalar_gate":  # the GPT-2 shape with one decay per token and head
         return Workload(name, "prefill_delta", 12, 64, 64, torch.bfloat16, gated=True,
                         lengths=(2048,) * 8, extra={"scalar_gate": True})
+    if name == "gpt2_chunk128":    # the GPT-2 shape with the recurrence over 128-token chunks
+        return Workload(name, "prefill_delta", 12, 64, 64, torch.bfloat16, lengths=(2048,) * 8,
+                        extra={"chunk": 128})
     if name == "gated_prefill":    # per-channel decay, 32 heads of 128, 4 x 8192 tokens
         return Workload(name, "prefill_delta", 32, 128, 128, torch.bfloat16, gated=True,
                         lengths=(8192,) * 4)
@@ -83,7 +86,7 @@ def workload(name: str, seed: int = 0) -> Workload:
 
 
 ALL_WORKLOADS = ("tiny_linear", "tiny_delta", "gpt2_prefill", "gated_prefill", "decode",
-                 "varlen_prefill", "gpt2_scalar_gate")
+                 "varlen_prefill", "gpt2_scalar_gate", "gpt2_chunk128")
 
 
 def cu_seqlens(lengths) -> torch.Tensor:
