@@ -264,6 +264,13 @@ class Prefill:
                                  workspace=self.ws, cu_seqlens_host=self.cu_host, stream=stream)
 
 
+# Spin (torch's sleep kernel, ~0.5 ms) queued before each step's start event,
+# so that the host has enqueued the step by the time the device reaches that
+# event: the timed region then holds the step's device work and not the
+# Python launch latency (which is longer than a small step's kernels).
+HOLD_CYCLES = 1_000_000
+
+
 def time_steps(step_fn, steps, warmup, flush, stream, barrier=None):
     """Per-step CUDA-event durations (ms) on `stream`, L2 flushed between steps."""
     for _ in range(warmup):
@@ -277,6 +284,8 @@ def time_steps(step_fn, steps, warmup, flush, stream, barrier=None):
     for i in range(steps):
         if flush is not None:
             flush.fill_(i & 0xFF)
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(HOLD_CYCLES)
         starts[i].record(stream)
         step_fn()
         ends[i].record(stream)
@@ -493,7 +502,8 @@ def run_ours(args, rank, world, dev, dist):
                                "hbm_frac": lbytes / (l_ms / 1e3) / 1e9 / pk["hbm_gbs"],
                                "workload": f"{len(wlin.lengths)} x {wlin.lengths[0]} tokens, "
                                            f"H={wlin.H}, d={wlin.dk}, {str(wlin.dtype)[6:]}",
-                               "kernel": "linear_chunk_simt_kernel (fp32 CUDA cores)"}
+                               "kernel": ("linear_prefix_simt_kernel (chunk-parallel, fp32 CUDA cores)"
+                                          if wlin.ntok <= 512 else "linear_tc_kernel (tcgen05)")}
                 del lt, lo
             # ---- backward pass on the GPT-2 shape (gradients of every input)
             bw = wl.workload(HEADLINE)

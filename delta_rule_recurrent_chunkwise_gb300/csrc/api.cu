@@ -2,6 +2,7 @@
 // then launches on the caller's stream.  Nothing here allocates, frees or
 // synchronises (la_check_device excepted), and no exception escapes.
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -102,7 +103,22 @@ la_status la_prefill_linear(const void *q, const void *k, const void *v, void *o
     if (la_status st = check_cu_host(cu_seqlens_host, N, ntok)) return st;
     la::PrefillArgs a{q, k, v, nullptr, nullptr, o, cu_seqlens, N, ntok, H, dk, dv, 1.0f, 0u,
                       init_S, init_z, final_S, final_z, io == LA_BF16};
-    return from_cuda(la::launch_linear_simt(a, static_cast<cudaStream_t>(stream)));
+    // longest sequence in chunks: from the host copy of cu_seqlens, else
+    // bounded by the packed total
+    if (cu_seqlens_host) {
+        int longest = 0;
+        for (int n = 0; n < N; ++n)
+            longest = std::max(longest, cu_seqlens_host[n + 1] - cu_seqlens_host[n]);
+        a.max_chunks = (longest + 63) / 64;
+    } else if (ntok <= la::kLinearParallelMaxChunks * 64) {
+        a.max_chunks = (ntok + 63) / 64;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // short sequences: the chunk-parallel CUDA-core kernel (fp32 or bf16);
+    // longer bf16 ones at d = 64: the tensor cores; else the CUDA-core scan
+    const bool short_seqs = a.max_chunks >= 0 && a.max_chunks <= la::kLinearParallelMaxChunks;
+    if (!short_seqs && la::linear_tc_supported(a)) return from_cuda(la::launch_linear_tc(a, s));
+    return from_cuda(la::launch_linear_simt(a, s));
 }
 
 size_t la_prefill_delta_workspace_size(int N, int ntok, int H, int dk, int dv, int chunk,

@@ -42,6 +42,10 @@ cudaError_t launch_programmatic(void (*kern)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// TMA map over a packed [ntok][H][D] bf16 tensor (box 64 tokens x 1 head x
+// 64 channels, 128-byte swizzle); false if the driver refuses it.
+bool make_map(CUtensorMap *m, const void *ptr, int D, int H, int ntok);
+
 cudaError_t launch_chunk_table(const TcLaunch &x, cudaStream_t s);
 // One cooperative launch running the intra-chunk tasks and the recurrence
 // together (d = 64, no gate or a scalar gate, when the grid holds the chains).

@@ -28,6 +28,9 @@ struct PrefillArgs {
     // with dk = dv = 64 (the records stay per 64 tokens; the recurrence pairs
     // them).
     int chunk = 64;
+    // ELU+1 prefill: the most 64-token chunks any sequence spans, when known
+    // on the host (-1: unknown); up to 8 selects the chunk-parallel kernel.
+    int max_chunks = -1;
 };
 
 struct DecodeArgs {
@@ -67,6 +70,12 @@ cudaError_t launch_delta_backward_chunked(const BwdArgs &a, cudaStream_t s);
 
 // fp32 SIMT chunk kernels (any I/O dtype).
 cudaError_t launch_linear_simt(const PrefillArgs &a, cudaStream_t s);
+// ELU+1 prefill on the tensor cores (bf16 I/O, dk = dv = 64, 16-byte aligned
+// tensors): one CTA per (head, sequence), used for sequences longer than
+// the chunk-parallel CUDA-core kernel takes.
+bool linear_tc_supported(const PrefillArgs &a);
+cudaError_t launch_linear_tc(const PrefillArgs &a, cudaStream_t s);
+constexpr int kLinearParallelMaxChunks = 8;  // the chunk-parallel kernel's limit
 cudaError_t launch_delta_simt(const PrefillArgs &a, cudaStream_t s);
 // tcgen05 tensor-core chunk kernels (bf16 I/O, dk == dv in {64, 128}): the
 // intra-chunk kernel and the inter-chunk kernel, with the per-chunk records

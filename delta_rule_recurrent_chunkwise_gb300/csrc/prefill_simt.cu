@@ -419,6 +419,223 @@ __global__ void __launch_bounds__(kNT) linear_chunk_simt_kernel(SimtParams p) {
         for (int c = tid; c < DK; c += NT) p.final_z[zbase + c] = sZ[c];
 }
 
+// Short sequences (at most kPMax chunks each): one 512-thread CTA per
+// (sequence, head, chunk, 16 value columns), all chunks of a sequence side by
+// side.  A chunk's starting state is the initial state plus the earlier
+// chunks' phi(K)^T V (at most kPMax - 1 of them, recomputed by the CTA), so
+// no chunk waits for another; the CTA of a sequence's last chunk also writes
+// the final state.  Narrow value slices keep each CTA's serial work short
+// (the recomputed sums and the outputs scale with the slice; only the
+// chunk's 64 x 64 scores are repeated per slice).  fp32 throughout.
+constexpr int kPMax = 8;    // chunks per sequence for the chunk-parallel form
+constexpr int kPJ = 16;     // value columns per CTA
+constexpr int kPNT = 512;   // threads per CTA
+
+template <int DK>
+struct PLayout {
+    static constexpr int LDK = DK + 4, LDV = kPJ + 4, LDP = kC + 4;
+    static constexpr int K = 0, V = K + kC * LDK, Q = V + kC * LDV, P = Q + kC * LDK,
+                         S = P + kC * LDP, Z = S + DK * LDV, FLOATS = Z + DK;
+};
+
+template <typename IO, int DK>
+__global__ void __launch_bounds__(kPNT) linear_prefix_simt_kernel(SimtParams p, int cmax) {
+    using L = PLayout<DK>;
+    constexpr int C = kC, NT = kPNT, LDK = L::LDK, LDV = L::LDV, LDP = L::LDP, J = kPJ;
+    constexpr int CPT = J * DK / NT;     // state columns per thread (one state row each)
+    constexpr int UK = C * DK / NT;      // phi(k) (and phi(q)) elements per thread per chunk
+    constexpr int UV = C * J / NT;       // value elements per thread per chunk
+    static_assert(CPT == 2 || CPT == 4, "state mapping");
+    extern __shared__ __align__(16) float smem[];
+    float *sK = smem + L::K, *sV = smem + L::V, *sQ = smem + L::Q, *sP = smem + L::P;
+    float *sS = smem + L::S, *sZ = smem + L::Z;
+
+    const int tid = threadIdx.x;
+    const int c = blockIdx.x % cmax, j0 = (blockIdx.x / cmax) * J;
+    const int h = blockIdx.y, n = blockIdx.z, H = p.H, dv = p.dv;
+    const IO *Q = static_cast<const IO *>(p.q), *K = static_cast<const IO *>(p.k);
+    const IO *V = static_cast<const IO *>(p.v);
+    IO *O = static_cast<IO *>(p.o);
+    int t_begin = p.cu_seqlens[n], t_end = p.cu_seqlens[n + 1];
+    if (t_begin < 0 || t_end < t_begin || t_end > p.ntok || t_end - t_begin > kPMax * C) {
+        if (tid == 0 && p.err) atomicCAS(p.err, 0u, 100u);
+        t_begin = t_end = 0;
+    }
+    const int nc = (t_end - t_begin + C - 1) / C;
+    // chunk 0 of an empty sequence still writes the final state (= initial)
+    if (c >= (nc > 0 ? nc : 1)) return;
+    const int64_t sbase = ((int64_t)n * H + h) * DK * dv + j0;
+    const int64_t zbase = ((int64_t)n * H + h) * DK;
+
+    // raw chunk elements in registers, loaded one chunk ahead
+    float rk[UK], rv[UV], rq[UK];
+    auto load_kv = [&](int j) {
+        const int cs = t_begin + j * C, len = min(C, t_end - cs);
+#pragma unroll
+        for (int u = 0; u < UK; ++u) {
+            const int e = tid + u * NT, r = e / DK, col = e % DK;
+            rk[u] = r < len ? to_f32(K[((int64_t)(cs + r) * H + h) * DK + col]) : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < UV; ++u) {
+            const int e = tid + u * NT, r = e / J, col = e % J;
+            rv[u] = r < len ? to_f32(V[((int64_t)(cs + r) * H + h) * dv + j0 + col]) : 0.0f;
+        }
+    };
+    // phi(k) (0 past the chunk's end) and the value slice into shared memory
+    auto stage_kv = [&](int j) {
+        const int len = min(C, t_end - (t_begin + j * C));
+#pragma unroll
+        for (int u = 0; u < UK; ++u) {
+            const int e = tid + u * NT, r = e / DK, col = e % DK;
+            sK[r * LDK + col] = r < len ? elu1_f(rk[u]) : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < UV; ++u) {
+            const int e = tid + u * NT, r = e / J, col = e % J;
+            sV[r * LDV + col] = rv[u];
+        }
+    };
+    // state row srow, columns scol .. scol + CPT - 1 of the slice, in registers
+    const int srow = tid / (J / CPT), scol = (tid % (J / CPT)) * CPT;
+    float acc[CPT];
+    float zacc = 0.0f;  // thread tid < DK: z[tid]
+#pragma unroll
+    for (int i = 0; i < CPT; ++i)
+        acc[i] = p.init_S ? p.init_S[sbase + (int64_t)srow * dv + scol + i] : 0.0f;
+    if (tid < DK) zacc = p.init_z ? p.init_z[zbase + tid] : 0.0f;
+    // S += phi(K)^T V, z += column sums of phi(K), from the staged chunk
+    auto accumulate = [&]() {
+#pragma unroll 8
+        for (int i = 0; i < C; ++i) {
+            const float kk = sK[i * LDK + srow];
+            if constexpr (CPT == 4) {
+                const float4 v4 = *reinterpret_cast<const float4 *>(sV + i * LDV + scol);
+                acc[0] = fmaf(kk, v4.x, acc[0]);
+                acc[1] = fmaf(kk, v4.y, acc[1]);
+                acc[2] = fmaf(kk, v4.z, acc[2]);
+                acc[3] = fmaf(kk, v4.w, acc[3]);
+            } else {
+                const float2 v2 = *reinterpret_cast<const float2 *>(sV + i * LDV + scol);
+                acc[0] = fmaf(kk, v2.x, acc[0]);
+                acc[1] = fmaf(kk, v2.y, acc[1]);
+            }
+        }
+        if (tid < DK)
+            for (int i = 0; i < C; ++i) zacc += sK[i * LDK + tid];
+    };
+
+    // ---- the state at this chunk's start
+    if (nc > 0) load_kv(0);
+    for (int j = 0; j < c; ++j) {
+        __syncthreads();
+        stage_kv(j);
+        __syncthreads();
+        load_kv(j + 1);  // the next chunk (this CTA's own at j + 1 == c) in flight
+        accumulate();
+    }
+    if (nc == 0) {
+        // empty sequence: the final state is the initial one
+        if (p.final_S)
+#pragma unroll
+            for (int i = 0; i < CPT; ++i) p.final_S[sbase + (int64_t)srow * dv + scol + i] = acc[i];
+        if (p.final_z && j0 == 0 && tid < DK) p.final_z[zbase + tid] = zacc;
+        return;
+    }
+    // ---- this chunk: phi(q), phi(k), v, and the state into shared memory
+    const int cs = t_begin + c * C, len = min(C, t_end - cs);
+#pragma unroll
+    for (int u = 0; u < UK; ++u) {
+        const int e = tid + u * NT, r = e / DK, col = e % DK;
+        rq[u] = r < len ? to_f32(Q[((int64_t)(cs + r) * H + h) * DK + col]) : 0.0f;
+    }
+    __syncthreads();
+    stage_kv(c);
+#pragma unroll
+    for (int u = 0; u < UK; ++u) {
+        const int e = tid + u * NT, r = e / DK, col = e % DK;
+        sQ[r * LDK + col] = r < len ? elu1_f(rq[u]) : 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) sS[srow * LDV + scol + i] = acc[i];
+    if (tid < DK) sZ[tid] = zacc;
+    __syncthreads();
+    // scores P[r][i] = phi(q_r) . phi(k_i), i <= r (else 0): thread (tr, tc)
+    // takes rows 2 tr, 2 tr + 1 and columns tc, tc + 16, tc + 32, tc + 48;
+    // tiles wholly above the diagonal only write zeros
+    {
+        const int tr = tid >> 4, tc = tid & 15;
+        float pa[2][4];
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) pa[a][b] = 0.0f;
+        const int nb = min(4, (2 * tr + 1 - tc) / 16 + 1);  // column groups reaching the diagonal
+        if (tc <= 2 * tr + 1) {
+#pragma unroll 2
+            for (int k0 = 0; k0 < DK; k0 += 4) {
+                const float4 q0 = *reinterpret_cast<const float4 *>(sQ + (2 * tr) * LDK + k0);
+                const float4 q1 = *reinterpret_cast<const float4 *>(sQ + (2 * tr + 1) * LDK + k0);
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    if (b < nb) {
+                        const float4 kb = *reinterpret_cast<const float4 *>(sK + (tc + 16 * b) * LDK + k0);
+                        pa[0][b] += dot4(q0, kb);
+                        pa[1][b] += dot4(q1, kb);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int r = 2 * tr + a, i = tc + 16 * b;
+                sP[r * LDP + i] = i <= r ? pa[a][b] : 0.0f;
+            }
+    }
+    __syncthreads();
+    // outputs: thread (r, part) owns columns 2 part, 2 part + 1 of row r; the
+    // row's eight threads (consecutive lanes) split the denominator's sums
+    {
+        const int r = tid >> 3, part = tid & 7, jq = 2 * part;
+        float n0 = 0.0f, n1 = 0.0f, den = 0.0f;
+        const float *qr = sQ + r * LDK, *pr = sP + r * LDP;
+#pragma unroll 8
+        for (int k0 = 0; k0 < DK; ++k0) {
+            const float a = qr[k0];
+            const float2 s2 = *reinterpret_cast<const float2 *>(sS + k0 * LDV + jq);
+            n0 = fmaf(a, s2.x, n0);
+            n1 = fmaf(a, s2.y, n1);
+        }
+        for (int k0 = part; k0 < DK; k0 += 8) den = fmaf(qr[k0], sZ[k0], den);
+        for (int i = 0; i <= r; ++i) {
+            const float a = pr[i];
+            const float2 v2 = *reinterpret_cast<const float2 *>(sV + i * LDV + jq);
+            n0 = fmaf(a, v2.x, n0);
+            n1 = fmaf(a, v2.y, n1);
+        }
+        for (int i = part; i <= r; i += 8) den += pr[i];
+        den += __shfl_xor_sync(0xffffffffu, den, 1);
+        den += __shfl_xor_sync(0xffffffffu, den, 2);
+        den += __shfl_xor_sync(0xffffffffu, den, 4);
+        if (r < len) {
+            const float inv = 1.0f / den;
+            IO *dst = O + ((int64_t)(cs + r) * H + h) * dv + j0 + jq;
+            dst[0] = from_f32<IO>(n0 * inv);
+            dst[1] = from_f32<IO>(n1 * inv);
+        }
+    }
+    // ---- the last chunk's CTA: the final state
+    if (c == nc - 1 && (p.final_S || p.final_z)) {
+        accumulate();  // reads the staged phi(k), v of this chunk (unchanged since)
+        if (p.final_S)
+#pragma unroll
+            for (int i = 0; i < CPT; ++i) p.final_S[sbase + (int64_t)srow * dv + scol + i] = acc[i];
+        if (p.final_z && j0 == 0 && tid < DK) p.final_z[zbase + tid] = zacc;
+    }
+}
+
 SimtParams to_params(const PrefillArgs &a) {
     return SimtParams{a.q, a.k, a.v, a.beta_logits, a.gate_logits, a.o, a.cu_seqlens,
                       device_error_word(), a.H, a.dv, a.ntok, a.scale, a.flags, a.init_S,
@@ -442,8 +659,24 @@ cudaError_t delta_dispatch(const PrefillArgs &a, cudaStream_t s) {
     return launch_kernel(delta_chunk_simt_kernel<IO, 64>, delta_smem_floats<64>() * 4, a, s);
 }
 
+template <typename IO, int DK>
+cudaError_t launch_prefix(const PrefillArgs &a, cudaStream_t s) {
+    auto kern = linear_prefix_simt_kernel<IO, DK>;
+    constexpr size_t smem = PLayout<DK>::FLOATS * 4;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int cmax = a.max_chunks > 0 ? a.max_chunks : 1;
+    dim3 grid((a.dv / kPJ) * cmax, a.H, a.N);
+    kern<<<grid, kPNT, smem, s>>>(to_params(a), cmax);
+    return cudaGetLastError();
+}
+
 template <typename IO>
 cudaError_t linear_dispatch(const PrefillArgs &a, cudaStream_t s) {
+    // every sequence known to span at most kPMax chunks: the chunk-parallel form
+    static_assert(kPMax == kLinearParallelMaxChunks, "one limit for the dispatch");
+    if (a.max_chunks >= 0 && a.max_chunks <= kPMax)
+        return a.dk == 128 ? launch_prefix<IO, 128>(a, s) : launch_prefix<IO, 64>(a, s);
     if (a.dk == 128)
         return launch_kernel(linear_chunk_simt_kernel<IO, 128>, LinLayout<128>::FLOATS * 4, a, s, kLJ);
     return launch_kernel(linear_chunk_simt_kernel<IO, 64>, LinLayout<64>::FLOATS * 4, a, s, kLJ);

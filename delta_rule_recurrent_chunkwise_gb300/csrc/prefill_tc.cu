@@ -36,6 +36,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+}  // namespace
+
 // 3-D map over a packed [ntok][H][D] bf16 tensor; box = 64 tokens x 1 head x 64 channels.
 bool make_map(CUtensorMap *m, const void *ptr, int D, int H, int ntok) {
     auto fn = encode_fn();
@@ -48,6 +50,8 @@ bool make_map(CUtensorMap *m, const void *ptr, int D, int H, int ntok) {
               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
 
 // Per-device values cached on first use.  Host threads racing on a first
 // call store the same value; a failed query is retried on the next call.

@@ -116,7 +116,7 @@ def test_varlen_prefill_full_sampled_heads(cuda_lib):
 
 # ------------------------------------------------------------ ELU+1 linear
 
-def check_linear(la, inp, dtype, init=False):
+def check_linear(la, inp, dtype, init=False, host_cu=True):
     dev = torch.device("cuda")
     q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
     cu = inp["cu_seqlens"]
@@ -129,7 +129,7 @@ def check_linear(la, inp, dtype, init=False):
     fz = torch.full((N, H, dk), float("nan"), device=dev)
     la.la_prefill_linear(q, k, v, o, cu.to(dev), init_S=None if iS is None else iS.to(dev),
                          init_z=None if iz is None else iz.to(dev), final_S=fS, final_z=fz,
-                         cu_seqlens_host=cu)
+                         cu_seqlens_host=cu if host_cu else None)
     assert la.la_check_device() == la.LA_OK
     ro, rS, rz = oracle.linear(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), cu.numpy(),
                                init_S=f64(iS), init_z=f64(iz))
@@ -153,6 +153,47 @@ def test_linear_ragged_fp32(cuda_lib, dk, dv):
 def test_linear_bf16(cuda_lib):
     inp = wl.prefill_inputs([300, 64, 5], 4, 64, 64, torch.bfloat16, False, seed=22)
     check_linear(cuda_lib, inp, torch.bfloat16)
+
+
+# Sequences of at most 8 chunks (512 tokens) take the chunk-parallel kernel,
+# longer ones the chunk-by-chunk scan: both, and the boundary between them.
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128)])
+def test_linear_long_sequences_fp32(cuda_lib, dk, dv):
+    inp = wl.prefill_inputs([700, 513, 64, 0], 2, dk, dv, torch.float32, False, seed=23)
+    check_linear(cuda_lib, inp, torch.float32, init=True)
+
+
+def test_linear_long_sequences_bf16(cuda_lib):
+    inp = wl.prefill_inputs([600, 200], 3, 64, 128, torch.bfloat16, False, seed=24)
+    check_linear(cuda_lib, inp, torch.bfloat16, init=True)
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 64)])
+def test_linear_eight_chunk_boundary(cuda_lib, dk, dv):
+    inp = wl.prefill_inputs([512, 511, 1, 0, 448], 2, dk, dv, torch.float32, False, seed=25)
+    check_linear(cuda_lib, inp, torch.float32, init=True)
+
+
+def test_linear_tensor_core_ragged(cuda_lib):
+    """bf16, dk = dv = 64, sequences past 8 chunks: the tensor-core kernel
+    (ragged tails, a 1-token and an empty sequence, initial states)."""
+    inp = wl.prefill_inputs([700, 129, 64, 1, 0, 513], 3, 64, 64, torch.bfloat16, False, seed=27)
+    check_linear(cuda_lib, inp, torch.bfloat16, init=True)
+    check_linear(cuda_lib, inp, torch.bfloat16, init=False, host_cu=False)
+
+
+def test_linear_tensor_core_gpt2_shape(cuda_lib):
+    """The GPT-2 shape (8 x 2048 tokens, 12 heads of 64) in bf16, every head."""
+    inp = wl.prefill_inputs((2048,) * 8, 12, 64, 64, torch.bfloat16, False, seed=28)
+    check_linear(cuda_lib, inp, torch.bfloat16)
+
+
+@pytest.mark.parametrize("lengths", [[200, 0, 57], [400, 300]])
+def test_linear_without_host_cu_seqlens(cuda_lib, lengths):
+    """No host copy of cu_seqlens: a packed total of at most 512 tokens
+    still takes the chunk-parallel kernel, a larger one the scan."""
+    inp = wl.prefill_inputs(lengths, 2, 64, 64, torch.float32, False, seed=26)
+    check_linear(cuda_lib, inp, torch.float32, init=True, host_cu=False)
 
 
 # ------------------------------------------------------------------ decode
