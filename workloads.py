@@ -147,3 +147,43 @@ def inputs_for(w: Workload, seed=0, init_state=False):
         return decode_inputs(w.n_seq, w.H, w.dk, w.dv, w.steps, w.dtype, seed, gated=w.gated)
     return prefill_inputs(w.lengths, w.H, w.dk, w.dv, w.dtype, w.gated, seed,
                           init_state=init_state, scalar_gate=w.extra.get("scalar_gate", False))
+
+
+def shard_sequences(inp: dict, rank: int, world: int) -> tuple[dict, list[int]]:
+    """Rank `rank`'s share of one packed prefill batch across `world` ranks:
+    sequences rank, rank + world, ... with their tokens, states and a fresh
+    cu_seqlens (the delta rule and ELU+1 treat every sequence on its own, so
+    no rank needs another's data).  Also returns the global indices of the
+    sequences taken, for putting the outputs back with gather_sequences."""
+    cu = [int(x) for x in inp["cu_seqlens"]]
+    n_seq = len(cu) - 1
+    mine = list(range(rank, n_seq, world))
+    rows = [torch.arange(cu[n], cu[n + 1]) for n in mine]
+    idx = torch.cat(rows) if rows else torch.zeros(0, dtype=torch.long)
+    out = {}
+    for name, t in inp.items():
+        if name == "cu_seqlens":
+            out[name] = cu_seqlens([cu[n + 1] - cu[n] for n in mine])
+        elif t is None:
+            out[name] = None
+        elif name in ("init_S", "state"):
+            out[name] = t[mine]
+        else:
+            out[name] = t[idx]
+    return out, mine
+
+
+def gather_sequences(shards: list[tuple[torch.Tensor, list[int]]], cu_full) -> torch.Tensor:
+    """Per-token outputs of every rank's shard (tensor [tokens of its
+    sequences, ...], global sequence indices) back in the packed order of
+    the full batch."""
+    cu = [int(x) for x in cu_full]
+    first = shards[0][0]
+    full = torch.empty((cu[-1],) + tuple(first.shape[1:]), dtype=first.dtype)
+    for part, seqs in shards:
+        at = 0
+        for n in seqs:
+            L = cu[n + 1] - cu[n]
+            full[cu[n]:cu[n + 1]] = part[at:at + L]
+            at += L
+    return full
