@@ -165,9 +165,10 @@ def la_prefill_delta(q, k, v, beta_logits, gate_logits, o, cu_seqlens, chunk=64,
                      flags=LA_L2NORM_K, init_S=None, final_S=None, workspace=None,
                      cu_seqlens_host=None, stream=None):
     """(Gated) delta-rule prefill.  q,k [ntok,H,dk]; v,o [ntok,H,dv];
-    beta_logits [ntok,H]; gate_logits [ntok,H,dk] or None.  workspace: a
-    device buffer of at least la_prefill_delta_workspace_size(...) bytes;
-    allocated here (on q's device) when not given."""
+    beta_logits [ntok,H]; gate_logits [ntok,H,dk] or None.  chunk: tokens
+    per chunk of the state recurrence, 64, or 128 for bf16 with dk = dv = 64.
+    workspace: a device buffer of at least la_prefill_delta_workspace_size(...)
+    bytes; allocated here (on q's device) when not given."""
     import torch
     _check(dict(q=q, k=k, v=v, o=o, beta_logits=beta_logits, gate_logits=gate_logits),
            dtype=q.dtype, device=q.device)
