@@ -56,6 +56,19 @@ def test_static_scratch_matches_workspace_entry_point():
         assert torch.equal(fS, ref[i][1]), f"problem {i}: final states differ"
 
 
+def test_static_scratch_at_chunk_128():
+    """The same at chunk 128 (bf16, d = 64): the recurrence over 128-token
+    chunks reads the 64-token records from the static scratch."""
+    la.build()
+    t, cu = _device_inputs(((200, 64, 1, 130), 4, 64, False), seed=21)
+
+    def at128(entry):
+        return lambda *a, **k: entry(*a, chunk=128, **k)
+    ref = _run(at128(la.la_prefill_delta), t, cu)
+    o, fS = _run(at128(la.la_prefill_delta_static), t, cu)
+    assert torch.equal(o, ref[0]) and torch.equal(fS, ref[1])
+
+
 def test_static_scratch_refuses_oversize_request():
     la.build()
     dev = torch.device("cuda")
