@@ -505,34 +505,43 @@ def run_ours(args, rank, world, dev, dist):
                                "kernel": ("linear_prefix_simt_kernel (chunk-parallel, fp32 CUDA cores)"
                                           if wlin.ntok <= 512 else "linear_tc_kernel (tcgen05)")}
                 del lt, lo
-            # ---- backward pass on the GPT-2 shape (gradients of every input)
-            bw = wl.workload(HEADLINE)
-            b_in = wl.inputs_for(bw, seed=rank_seed(rank))
-            bt = {n: (None if b_in[n] is None else b_in[n].to(dev))
-                  for n in ("q", "k", "v", "beta_logits", "gate_logits", "cu_seqlens")}
-            g = torch.Generator().manual_seed(1000 + rank)
-            d_o = torch.randn((bw.ntok, bw.H, bw.dv), generator=g).to(bw.dtype).to(dev)
-            bws = torch.empty(la.la_backward_delta_workspace_size(len(bw.lengths), bw.ntok, bw.H,
-                                                                  bw.dk, bw.dv),
-                              dtype=torch.uint8, device=dev)
+            # ---- backward pass (gradients of every input) on the GPT-2 shape and
+            # on the gated shape (per-channel decay, d = 128)
+            for bname, wname, kern in (
+                    ("gpt2_backward", HEADLINE,
+                     "chunkwise: forward with chunk states, reverse dS chain, per-chunk "
+                     "gradient kernel (TF32 mma.sync)"),
+                    ("gated_backward", "gated_prefill",
+                     "chunkwise: forward with chunk states, reverse dS chain, per-chunk "
+                     "gradient kernel with per-channel decay (bf16 mma.sync)")):
+                bw = wl.workload(wname)
+                b_in = wl.inputs_for(bw, seed=rank_seed(rank))
+                bt = {n: (None if b_in[n] is None else b_in[n].to(dev))
+                      for n in ("q", "k", "v", "beta_logits", "gate_logits", "cu_seqlens")}
+                g = torch.Generator().manual_seed(1000 + rank)
+                d_o = torch.randn((bw.ntok, bw.H, bw.dv), generator=g).to(bw.dtype).to(dev)
+                bws = torch.empty(la.la_backward_delta_workspace_size(len(bw.lengths), bw.ntok,
+                                                                      bw.H, bw.dk, bw.dv),
+                                  dtype=torch.uint8, device=dev)
 
-            def backward_step():
-                la.la_backward_delta(bt["q"], bt["k"], bt["v"], bt["beta_logits"],
-                                     bt["gate_logits"], d_o, bt["cu_seqlens"],
-                                     want_d_init_S=False, workspace=bws,
-                                     cu_seqlens_host=b_in["cu_seqlens"], stream=stream)
+                def backward_step():
+                    la.la_backward_delta(bt["q"], bt["k"], bt["v"], bt["beta_logits"],
+                                         bt["gate_logits"], d_o, bt["cu_seqlens"],
+                                         want_d_init_S=False, workspace=bws,
+                                         cu_seqlens_host=b_in["cu_seqlens"], stream=stream)
 
-            with clocks.load():
-                bms = time_steps(backward_step, 3, 2, flush, stream, barrier)
-            b_ms = mor(statistics.median(bms))
-            nb = backward_algo_bytes(bw)
-            extra["gpt2_backward"] = {
-                "tokens_per_s": bw.ntok * world / (b_ms / 1e3), "ms": b_ms,
-                "hbm_frac": nb / (b_ms / 1e3) / 1e9 / pk["hbm_gbs"],
-                "algorithmic_bytes": nb,
-                "kernel": "chunkwise: forward with chunk states, reverse dS chain, per-chunk "
-                          "gradient kernel (TF32 mma.sync)"}
-            del bt, d_o, bws
+                with clocks.load():
+                    bms = time_steps(backward_step, 3, 2, flush, stream, barrier)
+                b_ms = mor(statistics.median(bms))
+                nb = backward_algo_bytes(bw)
+                extra[bname] = {
+                    "tokens_per_s": bw.ntok * world / (b_ms / 1e3), "ms": b_ms,
+                    "hbm_frac": nb / (b_ms / 1e3) / 1e9 / pk["hbm_gbs"],
+                    "algorithmic_bytes": nb,
+                    "workload": f"{len(bw.lengths)} x {bw.lengths[0]} tokens, H={bw.H}, "
+                                f"d={bw.dk}, {'per-channel gate' if bw.gated else 'no gate'}",
+                    "kernel": kern}
+                del bt, d_o, bws
             result["secondary"] = extra
     result["clocks"] = clocks.summary()
     return result
@@ -681,8 +690,11 @@ def profile_case(args):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     name = args.profile_case
-    if name == "gpt2_backward":
-        w = wl.workload(HEADLINE)
+    if name in ("gpt2_backward", "gated_backward", "gated_backward_small"):
+        w = (wl.workload(HEADLINE) if name == "gpt2_backward" else
+             wl.workload("gated_prefill") if name == "gated_backward" else
+             wl.Workload(name, "prefill_delta", 32, 128, 128, torch.bfloat16, lengths=(4096,) * 2,
+                         gated=True))
         inp = wl.inputs_for(w, seed=0, init_state=True)
         t = {n: (None if inp[n] is None else inp[n].to(dev))
              for n in ("q", "k", "v", "beta_logits", "gate_logits", "cu_seqlens", "init_S")}
@@ -690,7 +702,7 @@ def profile_case(args):
             w.dtype).to(dev)
         ws = torch.empty(la.la_backward_delta_workspace_size(len(w.lengths), w.ntok, w.H, w.dk,
                                                              w.dv), dtype=torch.uint8, device=dev)
-        fn = lambda: la.la_backward_delta(t["q"], t["k"], t["v"], t["beta_logits"], None, d_o,
+        fn = lambda: la.la_backward_delta(t["q"], t["k"], t["v"], t["beta_logits"], t["gate_logits"], d_o,
                                           t["cu_seqlens"], init_S=t["init_S"], workspace=ws,
                                           cu_seqlens_host=inp["cu_seqlens"], stream=stream)
     elif name in ("tiny_linear", "gpt2_linear_bf16"):
@@ -750,7 +762,8 @@ def main():
                     help="units of a full launch / units of the captured launch")
     ap.add_argument("--profile-case", default=None,
                     help="run one workload only (for ncu): gpt2_prefill, gated_prefill, "
-                         "varlen_prefill, gpt2_scalar_gate, gpt2_chunk128, gpt2_backward, decode, decode_small, "
+                         "varlen_prefill, gpt2_scalar_gate, gpt2_chunk128, gpt2_backward, gated_backward, "
+                         "gated_backward_small, decode, decode_small, "
                          "gated_small, tiny_linear, gpt2_linear_bf16")
     args = ap.parse_args()
     if args.profile_case:

@@ -228,7 +228,8 @@ def la_backward_delta(q, k, v, beta_logits, gate_logits, d_o, cu_seqlens, d_fina
     optionally d_final_S [N,H,dk,dv] fp32.  Returns a dict of fp32 tensors
     dq, dk, dv, d_beta_logits, d_gate_logits (None without gate), d_init_S
     (None unless want_d_init_S).  Rows of tokens outside every sequence are
-    zero here (the library leaves them untouched; they are allocated zeroed)."""
+    zero here (the library leaves them untouched; they are allocated zeroed
+    unless cu_seqlens_host shows the sequences cover every row)."""
     import torch
     _check(dict(q=q, k=k, v=v, d_o=d_o, beta_logits=beta_logits, gate_logits=gate_logits),
            dtype=q.dtype, device=q.device)
@@ -239,10 +240,12 @@ def la_backward_delta(q, k, v, beta_logits, gate_logits, d_o, cu_seqlens, d_fina
     N = cu_seqlens.numel() - 1
     hold, hptr = _host_cu(cu_seqlens_host)
     f32 = dict(dtype=torch.float32, device=q.device)
-    out = {"dq": torch.zeros((ntok, H, dk), **f32), "dk": torch.zeros((ntok, H, dk), **f32),
-           "dv": torch.zeros((ntok, H, dv), **f32),
-           "d_beta_logits": torch.zeros((ntok, H), **f32),
-           "d_gate_logits": None if gate_logits is None else torch.zeros(gate_logits.shape, **f32),
+    covered = hold is not None and int(hold[0]) == 0 and int(hold[-1]) == ntok
+    alloc = torch.empty if covered else torch.zeros
+    out = {"dq": alloc((ntok, H, dk), **f32), "dk": alloc((ntok, H, dk), **f32),
+           "dv": alloc((ntok, H, dv), **f32),
+           "d_beta_logits": alloc((ntok, H), **f32),
+           "d_gate_logits": None if gate_logits is None else alloc(gate_logits.shape, **f32),
            "d_init_S": torch.empty((N, H, dk, dv), **f32) if want_d_init_S else None}
     if workspace is None:
         workspace = torch.empty(la_backward_delta_workspace_size(N, ntok, H, dk, dv),

@@ -455,9 +455,9 @@ cudaError_t dispatch(const BwdArgs &a, BwdParams p, cudaStream_t s) {
 }  // namespace
 
 size_t delta_bwd_workspace_bytes(int N, int ntok, int H, int dk, int dv) {
-    // enough for either form (the chunkwise one exists for dk = dv = 64)
+    // enough for either form (the chunkwise one exists for dk = dv)
     const size_t serial = ws_parts(N, ntok, H, dk, dv).total;
-    const size_t chunked = (dk == 64 && dv == 64) ? delta_bwd_chunked_workspace_bytes(N, ntok, H) : 0;
+    const size_t chunked = dk == dv ? delta_bwd_chunked_workspace_bytes(N, ntok, H, dk) : 0;
     return serial > chunked ? serial : chunked;
 }
 

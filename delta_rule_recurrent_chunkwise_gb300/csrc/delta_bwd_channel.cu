@@ -1,0 +1,855 @@
+// delta_bwd_channel.cu -- per-chunk gradients of the chunkwise delta rule with
+// a decay per key channel (the KDA form of "From GPT-2 to Kimi K3, explained",
+// section KDA / Kimi Linear; a scalar gate or none are its special cases),
+// d = dk = dv in {64, 128}, bf16 I/O.
+//
+// Forward of one chunk (section DeltaNet (Parallelizing Linear Transformers
+// with Delta Rule), eq. 8-10, with the decay folded in), b_r in R^dk the
+// inclusive cumulative log decay inside the chunk, b_L its value at the end:
+//   (X * Y)_ri = sum_c x_rc y_ic e^{b_rc - b_ic}   (i <= r)   "decayed scores"
+//   A = strict_tril(diag(beta) (K * K)),  T = (I + A)^{-1}
+//   Bk = diag(beta) (K o e^b),  Bv = diag(beta) V,  u~ = Bv - Bk S,  u = T u~
+//   O = scale ((Q o e^b) S + (Q * K) u),  S' = Diag(e^{b_L}) S + (K o e^{b_L-b})^T u
+// Given dO' = scale dO, dS' (the next chunk state's gradient) and du =
+// (Q * K)^T dO' + (K o e^{b_L - b}) dS' (both from the reverse chain):
+//   du_T = T^T du,  dV = diag(beta) du_T,  dT = du u~^T,  dA = -T^T dT T^T
+//   dBk = -du_T S^T,  dP = tril(dO' u^T),  d(Q o e^b) = dO' S^T
+//   d(K o e^{b_L - b}) = u dS'^T,  d e^{b_L} = rowsum(dS' o S)
+// and through the decayed scores, with G the gradient of X * Y:
+//   dX_rc += sum_{i<=r} G_ri y_ic e^{b_rc - b_ic},   db_rc += x_rc dX_rc
+//   dY_ic += sum_{r>=i} G_ri x_rc e^{b_rc - b_ic},   db_ic -= y_ic dY_ic
+// (G = dP for Q * K; G = diag(beta) dA for K * K).  Every term that moves
+// b adds x o dx with the sign of its exponent, so with dK+ the key-gradient
+// terms whose factor grows with b and dK- the others:
+//   db = q o dQ + k o (dK+ - dK-),   dK = dK+ + dK-
+// plus d b_L at the chunk's last row; d log alpha_t = sum_{r>=t} db_r.
+//
+// Decayed products without overflow.  e^{b_rc - b_ic} (i <= r, exponent <= 0)
+// does not split into a row factor and a column factor over a whole chunk.
+// The chunk is cut into four 16-token blocks.  For rows r of block R and
+// columns i of an earlier block I:
+//   e^{b_r - b_i} = e^{b_r - b_s(R)} e^{b_s(R) - b_e(I)} e^{b_e(I) - b_i}
+// with s(R) = 16R - 1 (the token before R) and e(I) = 16I + 15 (the end of
+// I): three factors <= 1, the middle one per (R, I) and channel.  So each
+// (R, I) block of a decayed product is one 16-deep tensor-core step on
+// operands scaled once per row, then scaled per output column.  The 16 x 16
+// diagonal blocks (i, r in the same block) take e^{b_r - b_i} directly on
+// the CUDA cores (exponent <= 0 again), whatever the decay's strength.
+//
+// Mapping: a persistent grid over (chunk, head) tasks, 16 warps per CTA.
+// Products are warp-level bf16 mma.sync (m16n8k16) on bf16 shared-memory
+// operands with fp32 accumulation; the three gradient accumulators dQ, dK+
+// and dK- stay in registers from the first product that feeds them to the
+// end of the task (warp w owns rows 16 (w / 4) .. +15 and a quarter of the
+// columns).  The triangular solve runs in fp32.
+
+#include "common.cuh"
+#include "delta_tc.h"
+#include "launch.h"
+#include "tc_tile.cuh"
+
+namespace la {
+namespace {
+
+using tile::C;
+using bf16 = __nv_bfloat16;
+constexpr int kNT = 512;              // threads per CTA: 16 warps
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ------------------------------------------------------------ warp products
+
+__device__ __forceinline__ uint32_t saddr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void ldsm(uint32_t (&r)[4], const bf16 *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(saddr(p)));
+}
+
+__device__ __forceinline__ void ldsm_t(uint32_t (&r)[4], const bf16 *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(saddr(p)));
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// One 16-deep step of a warp's 16 x 16 output block (two n8 tiles):
+//   d += op(A)[m0 .. m0+15][k .. k+15] op(B)[k .. k+15][n0 .. n0+15]
+// op(A) = A (stored [m][k], TA = false) or A^T (stored [k][m]); op(B) = B
+// (stored [k][n], TB = false) or B^T (stored [n][k]).  Row strides in
+// elements, multiples of 8; m0, n0, k multiples of 8 (k of 16).  ldmatrix
+// hands every lane its fragment: lanes 8j .. 8j + 7 address the rows of
+// 8 x 8 block j, transposed on the way for the [k][m] and [k][n] forms.
+template <bool TA, bool TB>
+__device__ __forceinline__ void mma_step(float (&d)[2][4], const bf16 *A, int lda, const bf16 *B,
+                                         int ldb, int m0, int n0, int k) {
+    const int lane = threadIdx.x & 31, li = lane & 7, lj = lane >> 3;
+    uint32_t a[4], b[4];
+    if constexpr (!TA) ldsm(a, A + (m0 + (lane & 15)) * lda + k + (lane >> 4) * 8);
+    else ldsm_t(a, A + (k + li + 8 * (lj >> 1)) * lda + m0 + 8 * (lj & 1));
+    if constexpr (TB) ldsm(b, B + (n0 + li + 8 * (lj >> 1)) * ldb + k + 8 * (lj & 1));
+    else ldsm_t(b, B + (k + li + 8 * (lj & 1)) * ldb + n0 + 8 * (lj >> 1));
+    mma16816(d[0], a, b[0], b[1]);
+    mma16816(d[1], a, b[2], b[3]);
+}
+
+// d (NT n8 tiles from column n0) += op(A) op(B) over k in [k0, k1).
+template <int NT, bool TA, bool TB>
+__device__ __forceinline__ void mma_rows(float (&d)[NT][4], const bf16 *A, int lda, const bf16 *B,
+                                         int ldb, int m0, int n0, int k0, int k1) {
+    for (int k = k0; k < k1; k += 16) {
+#pragma unroll
+        for (int j = 0; j < NT; j += 2) {
+            float (&dp)[2][4] = *reinterpret_cast<float (*)[2][4]>(&d[j]);
+            mma_step<TA, TB>(dp, A, lda, B, ldb, m0, n0 + 8 * j, k);
+        }
+    }
+}
+
+template <int NT>
+__device__ __forceinline__ void zero(float (&d)[NT][4]) {
+#pragma unroll
+    for (int j = 0; j < NT; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.0f;
+}
+
+__device__ __forceinline__ void st2(bf16 *p, float a, float b) {
+    *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(a, b);
+}
+
+__device__ __forceinline__ float2 ld2(const bf16 *p) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
+}
+
+// ------------------------------------------------------------ layout
+
+// Shared memory (bytes).  Persistent through a task: q^, k^ (bf16), b in
+// log2 units (fp32), K * K and T (bf16), row and channel vectors.  One union
+// region holds each phase's working tiles (offsets in the kernel's comments).
+template <int D>
+struct Lay {
+    static constexpr int XS = D + 8;            // bf16 stride of a 64 x D tile
+    static constexpr int XB = 64 * XS * 2;
+    static constexpr int SB = D * XS * 2;       // D x D bf16 (S or dS')
+    static constexpr int LS = 72;               // bf16 stride of a 64 x 64 tile
+    static constexpr int LB = 64 * LS * 2;
+    static constexpr int TS = 68;               // fp32 stride of T during the solve
+    static constexpr int FS = D + 4;            // fp32 stride of a 64 x D gradient
+    static constexpr int Q = 0, K = Q + XB, B = K + XB, KK = B + 64 * D * 4, TB = KK + LB;
+    static constexpr int BETA = TB + LB;                 // fp32 [64]
+    static constexpr int DBETA = BETA + 256;             // fp32 [64]
+    static constexpr int DBL = DBETA + 256;              // fp32 [D]: d b_L
+    static constexpr int DGL = DBL + 4 * D;              // fp32 [D]: d e^{b_L}
+    static constexpr int MF = DGL + 4 * D;               // fp32 [6][D]: middle factors
+    static constexpr int SEG = MF + 24 * D;              // fp32 [kNT / D][D]: scan totals
+    static constexpr int U = SEG + 4 * kNT;
+    // union region, phases 2-3 (the largest)
+    static constexpr int O_DO = 0, O_DU = XB, O_DUT = 2 * XB, O_UT = 3 * XB, O_BK = 4 * XB;
+    static constexpr int O_S = 5 * XB, U_BYTES = 5 * XB + SB;
+    static constexpr int BYTES = U + U_BYTES;
+    // phase 1 (K_s, the per-block copies Y_R and T in fp32) and phase 6 (dQ,
+    // dK and db in fp32) fit inside the union region
+    static_assert(XB + 96 * XS * 2 + 64 * TS * 4 <= U_BYTES, "phase 1");
+    static_assert(2 * 64 * FS * 4 + 64 * D * 4 <= U_BYTES, "phase 6");
+    static_assert(LB <= XB, "dP and dT fit in a 64 x D slot");
+};
+static_assert(Lay<128>::BYTES <= 232448, "shared memory at d = 128");
+
+struct Params {
+    const bf16 *q, *k, *v, *beta_logits, *gate_logits, *d_o;
+    const int2 *table;        // [slots] {first token, length}
+    const float *states;      // [slots][H][D][D] S at each chunk start
+    const float *dstates;     // [slots][H][D][D] dS' of each chunk
+    const float *du;          // [slots][H][64][D] du of each chunk
+    float *dq, *dk, *dv, *d_beta_logits, *d_gate_logits;
+    int64_t n_tasks;
+    int H;
+    float scale;
+    unsigned flags;
+};
+
+// Inclusive prefix sums down the 64 rows of each of the D columns of
+// x (fp32 [64][D]), in place; reverse = suffix sums.  All threads of the CTA.
+template <int D>
+__device__ __forceinline__ void column_scan(float *x, float *seg, bool reverse) {
+    constexpr int NS = kNT / D, RS = 64 / NS;   // segments per column, rows per segment
+    const int c = threadIdx.x % D, s = threadIdx.x / D;
+    float run = 0.0f;
+#pragma unroll
+    for (int i = 0; i < RS; ++i) {
+        const int r = reverse ? 63 - (s * RS + i) : s * RS + i;
+        run += x[r * D + c];
+        x[r * D + c] = run;
+    }
+    seg[s * D + c] = run;
+    __syncthreads();
+    float off = 0.0f;
+    for (int t = 0; t < s; ++t) off += seg[t * D + c];
+#pragma unroll
+    for (int i = 0; i < RS; ++i) {
+        const int r = reverse ? 63 - (s * RS + i) : s * RS + i;
+        x[r * D + c] += off;
+    }
+    __syncthreads();
+}
+
+// T = (I + A)^{-1} in place (fp32, row stride TS, A strictly lower): the four
+// 16 x 16 diagonal blocks by column-wise forward substitution, then block
+// rows 1..3 as T_ij = -T_ii sum_{j <= l < i} A_il T_lj.  X: 768 floats.
+template <int TS>
+__device__ __forceinline__ void solve_unit_lower(float *sT, float *X) {
+    const int tid = threadIdx.x;
+    {
+        float t[16];
+        const int R = tid >> 4, j = tid & 15;
+        if (tid < 64) {
+            const float *Ab = sT + (16 * R) * TS + 16 * R;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                float a = (r == j) ? 1.0f : 0.0f;
+#pragma unroll
+                for (int k = 0; k < r; ++k) a = fmaf(-Ab[r * TS + k], t[k], a);
+                t[r] = a;
+            }
+        }
+        __syncthreads();
+        if (tid < 64) {
+#pragma unroll
+            for (int r = 0; r < 16; ++r) sT[(16 * R + r) * TS + 16 * R + j] = t[r];
+        }
+        __syncthreads();
+    }
+#pragma unroll 1
+    for (int bi = 1; bi < 4; ++bi) {
+        for (int e = tid; e < bi * 256; e += kNT) {
+            const int bj = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+            float acc = 0.0f;
+            for (int l = bj; l < bi; ++l)
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    acc = fmaf(sT[(16 * bi + rr) * TS + 16 * l + k], sT[(16 * l + k) * TS + 16 * bj + cc], acc);
+            X[e] = acc;
+        }
+        __syncthreads();
+        for (int e = tid; e < bi * 256; e += kNT) {
+            const int bj = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+            float acc = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                acc = fmaf(sT[(16 * bi + rr) * TS + 16 * bi + k], X[(bj << 8) + k * 16 + cc], acc);
+            sT[(16 * bi + rr) * TS + 16 * bj + cc] = -acc;
+        }
+        __syncthreads();
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
+    using L = Lay<D>;
+    constexpr int XS = L::XS, LS = L::LS, TS = L::TS, FS = L::FS;
+    constexpr int CPL = D / 32;          // channels per lane in row-wise passes
+    constexpr int NT = D / 32;           // n8 tiles of a warp's 16 x D/4 output block
+    extern __shared__ __align__(16) uint8_t smem[];
+    bf16 *sQ = reinterpret_cast<bf16 *>(smem + L::Q), *sK = reinterpret_cast<bf16 *>(smem + L::K);
+    float *sB = reinterpret_cast<float *>(smem + L::B);
+    bf16 *sKK = reinterpret_cast<bf16 *>(smem + L::KK), *sTb = reinterpret_cast<bf16 *>(smem + L::TB);
+    float *sBeta = reinterpret_cast<float *>(smem + L::BETA);
+    float *sDBeta = reinterpret_cast<float *>(smem + L::DBETA);
+    float *sDBL = reinterpret_cast<float *>(smem + L::DBL), *sDGL = reinterpret_cast<float *>(smem + L::DGL);
+    float *sMF = reinterpret_cast<float *>(smem + L::MF), *sSeg = reinterpret_cast<float *>(smem + L::SEG);
+    uint8_t *U = smem + L::U;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int H = p.H;
+    const bool scalar_gate = (p.flags & kGateScalar) != 0;
+    const bool silu = (p.flags & kSiluQK) != 0;
+    // this warp's output block of a 64 x D product: rows 16R .. 16R + 15,
+    // columns n0 .. n0 + D/4 - 1; of a 64 x 64 product: columns 16 cq ..
+    const int R = w >> 2, cq = w & 3, n0 = cq * (D / 4);
+    const int r0 = 16 * R + g, r1 = r0 + 8;   // this lane's two output rows
+
+    for (int64_t task = blockIdx.x; task < p.n_tasks; task += gridDim.x) {
+        const int64_t slot = task / H;
+        const int h = (int)(task % H);
+        const int2 te = p.table[slot];
+        const int t0 = te.x, len = te.y;
+        if (len <= 0) continue;
+        auto tok = [&](int r) { return ((int64_t)(t0 + r) * H + h); };
+
+        // ---- 0. q^, k^ (silu, L2 norm), beta, log2 alpha; b = prefix sums
+        for (int rr = 0; rr < 4; ++rr) {
+            const int r = w + 16 * rr;
+            const bool ok = r < len;
+            float xq[CPL], xk[CPL], lg[CPL];
+            const bf16 *pq = p.q + tok(ok ? r : 0) * D, *pk = p.k + tok(ok ? r : 0) * D;
+#pragma unroll
+            for (int m = 0; m < CPL; ++m) {
+                const int c = lane + 32 * m;
+                xq[m] = ok ? __bfloat162float(pq[c]) : 0.0f;
+                xk[m] = ok ? __bfloat162float(pk[c]) : 0.0f;
+                float gl = 0.0f;
+                if (ok && p.gate_logits)
+                    gl = log_decay_f(__bfloat162float(scalar_gate ? p.gate_logits[tok(r)]
+                                                                  : p.gate_logits[tok(r) * D + c]));
+                lg[m] = gl * kLog2e;
+            }
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                float *x = which ? xk : xq;
+                float ss = 0.0f;
+#pragma unroll
+                for (int m = 0; m < CPL; ++m) {
+                    if (silu) x[m] = silu_f(x[m]);
+                    ss += x[m] * x[m];
+                }
+                const bool norm = (p.flags & (which ? kL2NormK : kL2NormQ)) != 0;
+                const float inv = norm ? 1.0f / fmaxf(sqrtf(warp_sum(ss)), 1e-12f) : 1.0f;
+                bf16 *dst = (which ? sK : sQ) + r * XS;
+#pragma unroll
+                for (int m = 0; m < CPL; ++m) dst[lane + 32 * m] = __float2bfloat16_rn(x[m] * inv);
+            }
+#pragma unroll
+            for (int m = 0; m < CPL; ++m) sB[r * D + lane + 32 * m] = lg[m];
+            if (lane == 0)
+                sBeta[r] = ok ? sigmoid_f(__bfloat162float(p.beta_logits[tok(r)])) : 0.0f;
+        }
+        if (tid < 64) sDBeta[tid] = 0.0f;
+        if (tid < D) sDBL[tid] = sDGL[tid] = 0.0f;
+        __syncthreads();
+        column_scan<D>(sB, sSeg, false);
+        // sB[r][c] = b_rc / ln 2 from here on; b at the token before block R
+        auto bs = [&](int Rb, int c) { return Rb == 0 ? 0.0f : sB[(16 * Rb - 1) * D + c]; };
+
+        // ---- 1. decayed scores K * K, A = beta (K * K), T = (I + A)^{-1}
+        // union: K_s at 0 (rows scaled to their block's start), Y_R for
+        // R = 1..3 at XB (rows 0 .. 16R - 1 scaled from R's start back to
+        // them), T in fp32 after them
+        bf16 *sKs = reinterpret_cast<bf16 *>(U);
+        bf16 *sY = reinterpret_cast<bf16 *>(U + L::XB);
+        float *sT = reinterpret_cast<float *>(U + L::XB + 96 * XS * 2);
+        auto yrow = [](int Rb) { return 8 * Rb * (Rb - 1); };   // first row of Y_R in sY
+        for (int e = tid; e < 64 * D / 2; e += kNT) {
+            const int r = e / (D / 2), c = 2 * (e % (D / 2)), Rb = r >> 4;
+            const float2 kv = ld2(sK + r * XS + c);
+            st2(sKs + r * XS + c, kv.x * exp2f(sB[r * D + c] - bs(Rb, c)),
+                kv.y * exp2f(sB[r * D + c + 1] - bs(Rb, c + 1)));
+            // row r of Y_R for every later block R
+            for (int Rb2 = Rb + 1; Rb2 < 4; ++Rb2)
+                st2(sY + (yrow(Rb2) + r) * XS + c, kv.x * exp2f(bs(Rb2, c) - sB[r * D + c]),
+                    kv.y * exp2f(bs(Rb2, c + 1) - sB[r * D + c + 1]));
+        }
+        for (int e = tid; e < 64 * 64; e += kNT) sT[(e >> 6) * TS + (e & 63)] = 0.0f;
+        __syncthreads();
+        // blocks below the diagonal: one warp per (R, I < R), K = D deep
+        if (cq < R) {
+            float d[2][4] = {};
+            for (int k = 0; k < D; k += 16)
+                mma_step<false, true>(d, sKs, XS, sY + yrow(R) * XS, XS, 16 * R, 16 * cq, k);
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = r0 + 8 * (e >> 1), i = 16 * cq + 8 * j + 2 * t + (e & 1);
+                    sT[r * TS + i] = sBeta[r] * d[j][e];
+                    sKK[r * LS + i] = __float2bfloat16_rn(d[j][e]);
+                }
+        }
+        // diagonal blocks exactly: warp w takes rows 16R + {qq, 7-qq, 8+qq, 15-qq}
+        // (30 (r, i) pairs for every warp), lanes split the channels
+#pragma unroll 1
+        for (int x = 0; x < 4; ++x) {
+            const int o = x == 0 ? cq : x == 1 ? 7 - cq : x == 2 ? 8 + cq : 15 - cq;
+            const int r = 16 * R + o;
+            float kr[CPL], br[CPL];
+#pragma unroll
+            for (int m = 0; m < CPL; ++m) {
+                kr[m] = __bfloat162float(sK[r * XS + lane + 32 * m]);
+                br[m] = sB[r * D + lane + 32 * m];
+            }
+            for (int i = 16 * R; i < r; ++i) {
+                float a = 0.0f;
+#pragma unroll
+                for (int m = 0; m < CPL; ++m) {
+                    const int c = lane + 32 * m;
+                    a = fmaf(kr[m] * __bfloat162float(sK[i * XS + c]), exp2f(br[m] - sB[i * D + c]), a);
+                }
+                a = warp_sum(a);
+                if (lane == 0) {
+                    sT[r * TS + i] = sBeta[r] * a;
+                    sKK[r * LS + i] = __float2bfloat16_rn(a);
+                }
+            }
+        }
+        __syncthreads();
+        solve_unit_lower<TS>(sT, reinterpret_cast<float *>(sY));
+        for (int e = tid; e < 64 * 64; e += kNT) {
+            const int r = e >> 6, i = e & 63;
+            sTb[r * LS + i] = __float2bfloat16_rn(i <= r ? sT[r * TS + i] : 0.0f);
+        }
+        __syncthreads();
+
+        // ---- 2. dO, du, S and Bk in; du_T = T^T du; u~, d(Q e^b), dBk
+        bf16 *sDO = reinterpret_cast<bf16 *>(U + L::O_DO), *sDU = reinterpret_cast<bf16 *>(U + L::O_DU);
+        bf16 *sDUT = reinterpret_cast<bf16 *>(U + L::O_DUT), *sUT = reinterpret_cast<bf16 *>(U + L::O_UT);
+        bf16 *sBK = reinterpret_cast<bf16 *>(U + L::O_BK), *sS = reinterpret_cast<bf16 *>(U + L::O_S);
+        const float *gS = p.states + (slot * H + h) * (int64_t)(D * D);
+        const float *gDS = p.dstates + (slot * H + h) * (int64_t)(D * D);
+        {
+            const float *gdu = p.du + (slot * H + h) * (int64_t)(64 * D);
+            for (int e = tid; e < 64 * D / 4; e += kNT) {
+                const int r = e / (D / 4), c = 4 * (e % (D / 4));
+                const float4 a = *reinterpret_cast<const float4 *>(gdu + r * D + c);
+                st2(sDU + r * XS + c, a.x, a.y);
+                st2(sDU + r * XS + c + 2, a.z, a.w);
+                const float be = sBeta[r];
+                const float2 k0 = ld2(sK + r * XS + c), k1 = ld2(sK + r * XS + c + 2);
+                const float *b = sB + r * D + c;
+                st2(sBK + r * XS + c, be * k0.x * exp2f(b[0]), be * k0.y * exp2f(b[1]));
+                st2(sBK + r * XS + c + 2, be * k1.x * exp2f(b[2]), be * k1.y * exp2f(b[3]));
+            }
+            for (int e = tid; e < 64 * D / 8; e += kNT) {
+                const int r = e / (D / 8), c = 8 * (e % (D / 8));
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(sDO + r * XS + c) =
+                    r < len ? *reinterpret_cast<const uint4 *>(p.d_o + tok(r) * D + c) : z;
+            }
+            for (int e = tid; e < D * D / 4; e += kNT) {
+                const int r = e / (D / 4), c = 4 * (e % (D / 4));
+                const float4 a = *reinterpret_cast<const float4 *>(gS + r * D + c);
+                st2(sS + r * XS + c, a.x, a.y);
+                st2(sS + r * XS + c + 2, a.z, a.w);
+            }
+        }
+        __syncthreads();
+        float aQ[NT][4], aKp[NT][4], aKm[NT][4];   // dQ, dK+, dK- (see the file header)
+        zero(aQ);
+        zero(aKp);
+        zero(aKm);
+        // dbeta partial sums of this lane's two rows, reduced over the quad and
+        // the four column warps of the row block
+        auto add_dbeta = [&](float s0, float s1) {
+            s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+            s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+            s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+            s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+            if (t == 0) {
+                atomicAdd(&sDBeta[r0], s0);
+                atomicAdd(&sDBeta[r1], s1);
+            }
+        };
+        {
+            // du_T = T^T du (T lower: rows r >= 16R of T reach rows of block R)
+            float d[NT][4];
+            zero(d);
+            mma_rows<NT, true, false>(d, sTb, LS, sDU, XS, 16 * R, n0, 16 * R, 64);
+            float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const int c = n0 + 8 * j + 2 * t;
+                st2(sDUT + r0 * XS + c, d[j][0], d[j][1]);
+                st2(sDUT + r1 * XS + c, d[j][2], d[j][3]);
+                // dV = beta du_T; dbeta += du_T . v
+                if (r0 < len) {
+                    const float2 v = ld2(p.v + tok(r0) * D + c);
+                    s0 += d[j][0] * v.x + d[j][1] * v.y;
+                    *reinterpret_cast<float2 *>(p.dv + tok(r0) * D + c) =
+                        make_float2(sBeta[r0] * d[j][0], sBeta[r0] * d[j][1]);
+                }
+                if (r1 < len) {
+                    const float2 v = ld2(p.v + tok(r1) * D + c);
+                    s1 += d[j][2] * v.x + d[j][3] * v.y;
+                    *reinterpret_cast<float2 *>(p.dv + tok(r1) * D + c) =
+                        make_float2(sBeta[r1] * d[j][2], sBeta[r1] * d[j][3]);
+                }
+            }
+            add_dbeta(s0, s1);
+        }
+        __syncthreads();
+        {
+            // u~ = beta V - Bk S
+            float d[NT][4];
+            zero(d);
+            mma_rows<NT, false, false>(d, sBK, XS, sS, XS, 16 * R, n0, 0, D);
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const int c = n0 + 8 * j + 2 * t;
+                const float2 v0 = r0 < len ? ld2(p.v + tok(r0) * D + c) : make_float2(0.f, 0.f);
+                const float2 v1 = r1 < len ? ld2(p.v + tok(r1) * D + c) : make_float2(0.f, 0.f);
+                st2(sUT + r0 * XS + c, sBeta[r0] * v0.x - d[j][0], sBeta[r0] * v0.y - d[j][1]);
+                st2(sUT + r1 * XS + c, sBeta[r1] * v1.x - d[j][2], sBeta[r1] * v1.y - d[j][3]);
+            }
+            // d(Q e^b) = scale dO S^T: dQ gets e^b times it
+            zero(d);
+            mma_rows<NT, false, true>(d, sDO, XS, sS, XS, 16 * R, n0, 0, D);
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = r0 + 8 * (e >> 1), c = n0 + 8 * j + 2 * t + (e & 1);
+                    aQ[j][e] = p.scale * exp2f(sB[r * D + c]) * d[j][e];
+                }
+            // dBk = -du_T S^T: dK+ gets beta e^b dBk; dbeta += dBk . (K e^b)
+            zero(d);
+            mma_rows<NT, false, true>(d, sDUT, XS, sS, XS, 16 * R, n0, 0, D);
+            float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = r0 + 8 * (e >> 1), c = n0 + 8 * j + 2 * t + (e & 1);
+                    const float kp = __bfloat162float(sK[r * XS + c]) * exp2f(sB[r * D + c]);
+                    const float dbk = -d[j][e];
+                    aKp[j][e] = sBeta[r] * exp2f(sB[r * D + c]) * dbk;
+                    if (e >> 1) s1 += dbk * kp;
+                    else s0 += dbk * kp;
+                }
+            add_dbeta(s0, s1);
+        }
+        __syncthreads();
+
+        // ---- 3. u = T u~, dT = du u~^T (strictly lower), dP = scale tril(dO u^T),
+        // then dS' in: d(K e^{b_L - b}) = u dS'^T, d e^{b_L} = rowsum(dS' o S)
+        bf16 *sU = sBK;                                             // 64 x D
+        bf16 *sDT = sDUT;                                           // 64 x 64
+        bf16 *sGP = sDU;                                            // 64 x 64, written after dT
+        {
+            float d[NT][4];
+            zero(d);
+            mma_rows<NT, false, false>(d, sTb, LS, sUT, XS, 16 * R, n0, 0, 16 * R + 16);
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const int c = n0 + 8 * j + 2 * t;
+                st2(sU + r0 * XS + c, d[j][0], d[j][1]);
+                st2(sU + r1 * XS + c, d[j][2], d[j][3]);
+            }
+            float e2[2][4] = {};
+            if (cq <= R)
+                for (int k = 0; k < D; k += 16)
+                    mma_step<false, true>(e2, sDU, XS, sUT, XS, 16 * R, 16 * cq, k);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int i = 16 * cq + 8 * j + 2 * t;
+                st2(sDT + r0 * LS + i, i < r0 ? e2[j][0] : 0.0f, i + 1 < r0 ? e2[j][1] : 0.0f);
+                st2(sDT + r1 * LS + i, i < r1 ? e2[j][2] : 0.0f, i + 1 < r1 ? e2[j][3] : 0.0f);
+            }
+        }
+        __syncthreads();
+        {
+            float e2[2][4] = {};
+            if (cq <= R)
+                for (int k = 0; k < D; k += 16)
+                    mma_step<false, true>(e2, sDO, XS, sU, XS, 16 * R, 16 * cq, k);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int i = 16 * cq + 8 * j + 2 * t;
+                const float s = p.scale;
+                st2(sGP + r0 * LS + i, i <= r0 ? s * e2[j][0] : 0.0f, i + 1 <= r0 ? s * e2[j][1] : 0.0f);
+                st2(sGP + r1 * LS + i, i <= r1 ? s * e2[j][2] : 0.0f, i + 1 <= r1 ? s * e2[j][3] : 0.0f);
+            }
+            // dS' (one row per warp at a time) and d e^{b_L}_c = sum_j dS'_cj S_cj
+            for (int c = w; c < D; c += kNT / 32) {
+                float acc = 0.0f;
+#pragma unroll
+                for (int m = 0; m < CPL; ++m) {
+                    const int j = lane + 32 * m;
+                    const float ds = gDS[c * D + j];
+                    acc = fmaf(ds, gS[c * D + j], acc);
+                    sS[c * XS + j] = __float2bfloat16_rn(ds);
+                }
+                acc = warp_sum(acc);
+                if (lane == 0) sDGL[c] = acc;
+            }
+        }
+        __syncthreads();
+        {
+            // K~ = K e^{b_L - b}: dK- gets e^{b_L - b} u dS'^T; d b_L += sum_i k~ (u dS'^T)
+            float d[NT][4];
+            zero(d);
+            mma_rows<NT, false, true>(d, sU, XS, sS, XS, 16 * R, n0, 0, D);
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int e1 = 0; e1 < 2; ++e1) {
+                    const int c = n0 + 8 * j + 2 * t + e1;
+                    const float bl = sB[63 * D + c];
+                    const float el0 = exp2f(bl - sB[r0 * D + c]), el1 = exp2f(bl - sB[r1 * D + c]);
+                    aKm[j][e1] = el0 * d[j][e1];
+                    aKm[j][2 + e1] = el1 * d[j][2 + e1];
+                    float s = __bfloat162float(sK[r0 * XS + c]) * aKm[j][e1] +
+                              __bfloat162float(sK[r1 * XS + c]) * aKm[j][2 + e1];
+                    s += __shfl_xor_sync(0xffffffffu, s, 4);
+                    s += __shfl_xor_sync(0xffffffffu, s, 8);
+                    s += __shfl_xor_sync(0xffffffffu, s, 16);
+                    if (g == 0) atomicAdd(&sDBL[c], s);
+                }
+        }
+        __syncthreads();
+
+        // ---- 4. dA = -T^T dT T^T (strictly lower); G_A = diag(beta) dA;
+        // dbeta += sum_i dA_ri (K * K)_ri
+        bf16 *sX = sUT;                                             // 64 x 64
+        bf16 *sGA = sDO;                                            // 64 x 64
+        {
+            // X = T^T dT: op(A)[i][r] = T[r][i], nonzero for r >= i
+            float e2[2][4] = {};
+            for (int k = 16 * R; k < 64; k += 16)
+                mma_step<true, false>(e2, sTb, LS, sDT, LS, 16 * R, 16 * cq, k);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int i = 16 * cq + 8 * j + 2 * t;
+                st2(sX + r0 * LS + i, e2[j][0], e2[j][1]);
+                st2(sX + r1 * LS + i, e2[j][2], e2[j][3]);
+            }
+        }
+        __syncthreads();
+        {
+            // dA = -X T^T: op(B)[a][i] = T[i][a], nonzero for a <= i
+            float e2[2][4] = {};
+            if (cq <= R)
+                for (int k = 0; k < 16 * cq + 16; k += 16)
+                    mma_step<false, true>(e2, sX, LS, sTb, LS, 16 * R, 16 * cq, k);
+            float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int e1 = 0; e1 < 2; ++e1) {
+                    const int i = 16 * cq + 8 * j + 2 * t + e1;
+                    const float da0 = i < r0 ? -e2[j][e1] : 0.0f, da1 = i < r1 ? -e2[j][2 + e1] : 0.0f;
+                    if (i < r0) s0 += da0 * __bfloat162float(sKK[r0 * LS + i]);
+                    if (i < r1) s1 += da1 * __bfloat162float(sKK[r1 * LS + i]);
+                    sGA[r0 * LS + i] = __float2bfloat16_rn(sBeta[r0] * da0);
+                    sGA[r1 * LS + i] = __float2bfloat16_rn(sBeta[r1] * da1);
+                }
+            add_dbeta(s0, s1);
+        }
+        __syncthreads();
+
+        // ---- 5. through the decayed scores Q * K (gradient dP) and K * K
+        // (gradient G_A).  Operands scaled once per row: K_e = k e^{b_e(I) - b}
+        // (to the end of the row's block), Q_s, K_s = (q, k) e^{b - b_s(R)} (from
+        // the start of the row's block); middle factors m(R, I) = e^{b_s(R) - b_e(I)}.
+        bf16 *sKe = reinterpret_cast<bf16 *>(U + L::O_DUT);
+        bf16 *sQs = reinterpret_cast<bf16 *>(U + L::O_UT);
+        bf16 *sKs2 = reinterpret_cast<bf16 *>(U + L::O_BK);
+        for (int e = tid; e < 64 * D / 2; e += kNT) {
+            const int r = e / (D / 2), c = 2 * (e % (D / 2)), Rb = r >> 4;
+            const float2 kv = ld2(sK + r * XS + c), qv = ld2(sQ + r * XS + c);
+            const float b0 = sB[r * D + c], b1 = sB[r * D + c + 1];
+            const float e0 = sB[(16 * Rb + 15) * D + c], e1 = sB[(16 * Rb + 15) * D + c + 1];
+            const float f0 = exp2f(b0 - bs(Rb, c)), f1 = exp2f(b1 - bs(Rb, c + 1));
+            st2(sKe + r * XS + c, kv.x * exp2f(e0 - b0), kv.y * exp2f(e1 - b1));
+            st2(sQs + r * XS + c, qv.x * f0, qv.y * f1);
+            st2(sKs2 + r * XS + c, kv.x * f0, kv.y * f1);
+        }
+        for (int e = tid; e < 6 * D; e += kNT) {
+            const int pi = e / D, c = e % D;
+            const int Rb = pi < 1 ? 1 : pi < 3 ? 2 : 3, Ib = pi - Rb * (Rb - 1) / 2;
+            sMF[pi * D + c] = exp2f(bs(Rb, c) - sB[(16 * Ib + 15) * D + c]);
+        }
+        __syncthreads();
+        auto mf = [&](int Rb, int Ib, int c) { return sMF[(Rb * (Rb - 1) / 2 + Ib) * D + c]; };
+        {
+            // off-diagonal blocks, two n8 tiles at a time.  Rows of block R:
+            //   dQ  += e^{b_r - b_s(R)} sum_{I<R} m(R,I) (dP[R,I] K_e[I])
+            //   dK+ += e^{b_r - b_s(R)} sum_{I<R} m(R,I) (G_A[R,I] K_e[I])
+            // rows of block I = R of this warp:
+            //   dK- += e^{b_e(I) - b_i} sum_{R'>I} m(R',I) (dP[R',I]^T Q_s[R'] + G_A[R',I]^T K_s[R'])
+#pragma unroll
+            for (int j = 0; j < NT; j += 2) {
+                const int nb = n0 + 8 * j;
+                float sq[2][4] = {}, sa[2][4] = {}, sm2[2][4] = {};
+                for (int Ib = 0; Ib < R; ++Ib) {
+                    float tq[2][4] = {}, ta[2][4] = {};
+                    mma_step<false, false>(tq, sGP, LS, sKe, XS, 16 * R, nb, 16 * Ib);
+                    mma_step<false, false>(ta, sGA, LS, sKe, XS, 16 * R, nb, 16 * Ib);
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float m = mf(R, Ib, nb + 8 * jj + 2 * t + (e & 1));
+                            sq[jj][e] = fmaf(m, tq[jj][e], sq[jj][e]);
+                            sa[jj][e] = fmaf(m, ta[jj][e], sa[jj][e]);
+                        }
+                }
+                for (int Rb = R + 1; Rb < 4; ++Rb) {
+                    float tb[2][4] = {};
+                    mma_step<true, false>(tb, sGP, LS, sQs, XS, 16 * R, nb, 16 * Rb);
+                    mma_step<true, false>(tb, sGA, LS, sKs2, XS, 16 * R, nb, 16 * Rb);
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float m = mf(Rb, R, nb + 8 * jj + 2 * t + (e & 1));
+                            sm2[jj][e] = fmaf(m, tb[jj][e], sm2[jj][e]);
+                        }
+                }
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int r = r0 + 8 * (e >> 1), c = nb + 8 * jj + 2 * t + (e & 1);
+                        const float b = sB[r * D + c];
+                        const float fr = exp2f(b - bs(R, c));
+                        const float fc = exp2f(sB[(16 * R + 15) * D + c] - b);
+                        aQ[j + jj][e] = fmaf(fr, sq[jj][e], aQ[j + jj][e]);
+                        aKp[j + jj][e] = fmaf(fr, sa[jj][e], aKp[j + jj][e]);
+                        aKm[j + jj][e] = fmaf(fc, sm2[jj][e], aKm[j + jj][e]);
+                    }
+            }
+        }
+        {
+            // diagonal blocks exactly, e^{b_r - b_i} taken directly (exponent <= 0):
+            //   dQ_rc  += sum_{16R <= i <= r} dP_ri k_ic e^{b_rc - b_ic}
+            //   dK+_rc += sum_{16R <= i <  r} G_A,ri k_ic e^{b_rc - b_ic}
+            //   dK-_ic += sum_{i <= r < 16R+16} (dP_ri q_rc + G_A,ri k_rc) e^{b_rc - b_ic}
+            // (per lane 34 (row, partner) steps whatever g)
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                const int r = r0 + 8 * hr;
+                float br[2 * NT];
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    const float2 b2 = *reinterpret_cast<const float2 *>(sB + r * D + n0 + 8 * j + 2 * t);
+                    br[2 * j] = b2.x;
+                    br[2 * j + 1] = b2.y;
+                }
+                for (int i = 16 * R; i <= r; ++i) {
+                    const float gp = __bfloat162float(sGP[r * LS + i]);
+                    const float ga = __bfloat162float(sGA[r * LS + i]);
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+                        const int c = n0 + 8 * j + 2 * t;
+                        const float2 kv = ld2(sK + i * XS + c);
+                        const float2 bi = *reinterpret_cast<const float2 *>(sB + i * D + c);
+                        const float w0 = kv.x * exp2f(br[2 * j] - bi.x);
+                        const float w1 = kv.y * exp2f(br[2 * j + 1] - bi.y);
+                        aQ[j][2 * hr] = fmaf(gp, w0, aQ[j][2 * hr]);
+                        aQ[j][2 * hr + 1] = fmaf(gp, w1, aQ[j][2 * hr + 1]);
+                        aKp[j][2 * hr] = fmaf(ga, w0, aKp[j][2 * hr]);
+                        aKp[j][2 * hr + 1] = fmaf(ga, w1, aKp[j][2 * hr + 1]);
+                    }
+                }
+                for (int rr = r; rr < 16 * R + 16; ++rr) {
+                    const float gp = __bfloat162float(sGP[rr * LS + r]);
+                    const float ga = __bfloat162float(sGA[rr * LS + r]);
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+                        const int c = n0 + 8 * j + 2 * t;
+                        const float2 qv = ld2(sQ + rr * XS + c), kv = ld2(sK + rr * XS + c);
+                        const float2 b2 = *reinterpret_cast<const float2 *>(sB + rr * D + c);
+                        const float w0 = exp2f(b2.x - br[2 * j]), w1 = exp2f(b2.y - br[2 * j + 1]);
+                        aKm[j][2 * hr] = fmaf(fmaf(gp, qv.x, ga * kv.x), w0, aKm[j][2 * hr]);
+                        aKm[j][2 * hr + 1] = fmaf(fmaf(gp, qv.y, ga * kv.y), w1, aKm[j][2 * hr + 1]);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+
+        // ---- 6. dQ, dK = dK+ + dK- and db = q dQ + k (dK+ - dK-) to shared
+        // memory; outputs through the prologue; d log alpha by suffix sums
+        float *sFQ = reinterpret_cast<float *>(U), *sFK = sFQ + 64 * FS, *sDB = sFK + 64 * FS;
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = r0 + 8 * (e >> 1), c = n0 + 8 * j + 2 * t + (e & 1);
+                const float dq = aQ[j][e], dkp = aKp[j][e], dkm = aKm[j][e];
+                sFQ[r * FS + c] = dq;
+                sFK[r * FS + c] = dkp + dkm;
+                sDB[r * D + c] = __bfloat162float(sQ[r * XS + c]) * dq +
+                                 __bfloat162float(sK[r * XS + c]) * (dkp - dkm);
+            }
+        __syncthreads();
+        if (tid < D && p.gate_logits)
+            sDB[63 * D + tid] += sDBL[tid] + exp2f(sB[63 * D + tid]) * sDGL[tid];
+#pragma unroll 1
+        for (int rr = 0; rr < 4; ++rr) {
+            const int r = w + 16 * rr;
+            if (r >= len) continue;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const bf16 *raw = (which ? p.k : p.q) + tok(r) * D;
+                const float *src = (which ? sFK : sFQ) + r * FS;
+                float x[CPL], d[CPL];
+#pragma unroll
+                for (int m = 0; m < CPL; ++m) {
+                    x[m] = __bfloat162float(raw[lane + 32 * m]);
+                    d[m] = src[lane + 32 * m];
+                }
+                prep_backward<CPL>(x, d, silu, (p.flags & (which ? kL2NormK : kL2NormQ)) != 0);
+                float *out = (which ? p.dk : p.dq) + tok(r) * D;
+#pragma unroll
+                for (int m = 0; m < CPL; ++m) out[lane + 32 * m] = d[m];
+            }
+        }
+        if (tid < len) {
+            const float be = sBeta[tid];
+            p.d_beta_logits[tok(tid)] = sDBeta[tid] * be * (1.0f - be);
+        }
+        if (p.gate_logits) {
+            __syncthreads();
+            column_scan<D>(sDB, sSeg, true);   // d log alpha_t = sum_{r >= t} db_r
+            // log alpha = -softplus(x): dx = -d(log alpha) sigmoid(x)
+            if (!scalar_gate) {
+                for (int e = tid; e < len * D; e += kNT) {
+                    const int r = e / D, c = e % D;
+                    const int64_t o = tok(r) * D + c;
+                    p.d_gate_logits[o] = -sDB[r * D + c] * sigmoid_f(__bfloat162float(p.gate_logits[o]));
+                }
+            } else {
+                for (int r = w; r < len; r += kNT / 32) {
+                    float s = 0.0f;
+#pragma unroll
+                    for (int m = 0; m < CPL; ++m) s += sDB[r * D + lane + 32 * m];
+                    s = warp_sum(s);
+                    if (lane == 0)
+                        p.d_gate_logits[tok(r)] = -s * sigmoid_f(__bfloat162float(p.gate_logits[tok(r)]));
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <int D>
+cudaError_t launch_d(const Params &p, cudaStream_t s) {
+    int dev = 0, sms = 0;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    constexpr int bytes = Lay<D>::BYTES;
+    if ((e = cudaFuncSetAttribute(delta_bwd_channel_kernel<D>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
+        return e;
+    const int64_t grid = p.n_tasks < sms ? p.n_tasks : sms;
+    if (grid > 0) {
+        delta_bwd_channel_kernel<D><<<(unsigned)grid, kNT, bytes, s>>>(p);
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
+}  // namespace
+
+cudaError_t launch_delta_bwd_channel(const BwdChannelArgs &a, cudaStream_t s) {
+    Params p{static_cast<const bf16 *>(a.q), static_cast<const bf16 *>(a.k),
+             static_cast<const bf16 *>(a.v), static_cast<const bf16 *>(a.beta_logits),
+             static_cast<const bf16 *>(a.gate_logits), static_cast<const bf16 *>(a.d_o),
+             a.table, a.states, a.dstates, a.du, a.dq, a.dk, a.dv, a.d_beta_logits,
+             a.d_gate_logits, a.n_tasks, a.H, a.scale, a.flags};
+    if (a.D == 64) return launch_d<64>(p, s);
+    if (a.D == 128) return launch_d<128>(p, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace la

@@ -1,5 +1,8 @@
 // delta_bwd_tc.cu -- chunkwise backward pass of the delta rule (bf16 I/O,
-// dk = dv = 64, no gate or one decay per token and head).
+// dk = dv in {64, 128}, any gate): the forward pass with records, the
+// reverse chain over chunks, and the per-chunk gradients for d = 64 without
+// a per-channel decay (the other per-chunk kernel, delta_bwd_channel.cu,
+// takes d = 128 and the per-channel decay).
 //
 // The page ("From GPT-2 to Kimi K3, explained", section DeltaNet
 // (Parallelizing Linear Transformers with Delta Rule), eq. 8-10) gives the
@@ -18,12 +21,13 @@
 //   dT  = dW Bk^T + du Bv^T (dW = -du S^T, Bk = diag(beta e^b) K, Bv = diag(beta) V)
 //   dA  = strict_tril(-T^T dT T^T), and so on through A, Bk, Bv and the
 //         decay factors to dbeta and d log alpha.
-// Three launches after the tensor-core forward pass (run with its per-chunk
+// Two launches after the tensor-core forward pass (run with its per-chunk
 // records kept and the state at every chunk start written out):
-//   delta_bwd_chain_kernel   per (head, sequence, 32 value columns): dS from
-//                            the last chunk to the first, reading the
-//                            forward's records (-W, Q e^b, K e^{b_L-b}, P,
-//                            e^{b_L}); stores dS' of every chunk.
+//   delta_bwd_chain_kernel   per (head, sequence, 32 or 64 value columns):
+//                            dS from the last chunk to the first, reading
+//                            the forward's records (-W, Q e^b, K e^{b_L-b},
+//                            P, e^{b_L}); stores dS' (and, for the other
+//                            per-chunk kernel, du) of every chunk.
 //   delta_bwd_chunk_kernel   every (chunk, head) in parallel: recomputes the
 //                            chunk in fp32 from q, k, v and the stored state,
 //                            then all gradients above (warp-level TF32
@@ -146,6 +150,7 @@ struct ChainParams {
     const int32_t *cu;
     const float *d_final_S;
     float *dstates;           // [slots][H][D][D]: dS' of every chunk
+    float *du;                // null, or [slots][H][64][D]: du of every chunk
     float *d_init_S;
     unsigned *err;
     int H, ntok;
@@ -153,27 +158,40 @@ struct ChainParams {
     bool gend;                // records carry e^{b_L} (gated); else it is 1
 };
 
-constexpr int kChainNT = 256;   // 8 warps
-constexpr int kJ = 32;          // value columns per chain CTA
-constexpr int LDJ = kJ + 4;
-
-// Shared-memory layout of the chain kernel (floats).
-struct ChainLayout {
-    static constexpr int W = 0, Q = W + MAT, K = Q + MAT, P = K + MAT;
-    static constexpr int G = P + MAT, DO = G + 64, DS = DO + 64 * LDJ, DU = DS + 64 * LDJ;
+// Threads and value columns of dS per chain CTA: 8 warps and 32 columns at
+// d = 64; 16 warps and 64 columns at d = 128 (half as many CTAs, each one
+// chain of the sequence's chunks).
+template <int D> struct ChainCfg {
+    static constexpr int NT = D == 64 ? 256 : 512;
+    static constexpr int J = D == 64 ? 32 : 64;
+    static constexpr int LDJ = J + 4;
+    static constexpr int LD = D + 4;            // fp32 row stride of a 64 x D record tile
+    // shared-memory layout (floats)
+    static constexpr int W = 0, Q = W + 64 * LD, K = Q + 64 * LD, P = K + 64 * LD;
+    static constexpr int G = P + MAT, DO = G + D, DS = DO + 64 * LDJ, DU = DS + D * LDJ;
     static constexpr int FLOATS = DU + 64 * LDJ;
+    // 16-byte units of one chunk's record operands: -W and Q e^b (128 rows),
+    // K e^{b_L - b} (64 rows), Aq (64 x 64)
+    static constexpr int UNITS = 128 * D / 8 + 64 * D / 8 + 512;
+    static constexpr int PER_THREAD = UNITS / NT;
+    static_assert(UNITS % NT == 0, "whole units per thread");
+    static_assert(NT == 64 * (J / 8), "one 16-byte unit of dO per thread");
 };
 
-// Reverse pass over the chunks of one (head, sequence), 32 value columns of
+// Reverse pass over the chunks of one (head, sequence), J value columns of
 // dS per CTA (the columns of dS never mix).
-__global__ void __launch_bounds__(kChainNT) delta_bwd_chain_kernel(ChainParams p) {
-    using L = ChainLayout;
-    using Rec = tile::Record<64>;
+template <int D>
+__global__ void __launch_bounds__(ChainCfg<D>::NT) delta_bwd_chain_kernel(ChainParams p) {
+    using L = ChainCfg<D>;
+    using Rec = tile::Record<D>;
+    constexpr int NT = L::NT, J = L::J, LDJ = L::LDJ, LD = L::LD, NW = NT / 32;
+    constexpr int WQU = 128 * D / 8, KU = 64 * D / 8;   // unit boundaries
+    constexpr int CPR = D / 8;                           // units per record row
     extern __shared__ __align__(16) float sm[];
     float *sW = sm + L::W, *sQ = sm + L::Q, *sK = sm + L::K, *sP = sm + L::P, *sG = sm + L::G;
     float *sDO = sm + L::DO, *sDS = sm + L::DS, *sDU = sm + L::DU;
     const int tid = threadIdx.x;
-    const int h = blockIdx.x, n = blockIdx.y, j0 = blockIdx.z * kJ, H = p.H;
+    const int h = blockIdx.x, n = blockIdx.y, j0 = blockIdx.z * J, H = p.H;
     int t_begin = p.cu[n], t_end = p.cu[n + 1];
     if (t_begin < 0 || t_end < t_begin || t_end > p.ntok) {
         if (tid == 0) atomicCAS(p.err, 0u, 100u);
@@ -181,40 +199,41 @@ __global__ void __launch_bounds__(kChainNT) delta_bwd_chain_kernel(ChainParams p
     }
     const int nc = (t_end - t_begin + C - 1) / C;
     const int64_t slot0 = (int64_t)(t_begin / C) + n;
-    const int64_t sbase = ((int64_t)n * H + h) * 64 * 64;
-    for (int e = tid; e < 64 * kJ; e += kChainNT) {
-        const int i = e / kJ, j = e % kJ;
-        sDS[i * LDJ + j] = p.d_final_S ? p.d_final_S[sbase + i * 64 + j0 + j] : 0.0f;
+    const int64_t sbase = ((int64_t)n * H + h) * D * D;
+    for (int e = tid; e < D * J; e += NT) {
+        const int i = e / J, j = e % J;
+        sDS[i * LDJ + j] = p.d_final_S ? p.d_final_S[sbase + i * D + j0 + j] : 0.0f;
     }
-    // One chunk's operands: 8 + 1 16-byte loads per thread (record tiles
-    // -W, Q e^b, K~, P; this CTA's 32 columns of dO) and e^{b_L}, loaded into
-    // registers one chunk ahead, then converted into shared memory.
-    uint4 raw[8], rdo;
+    // One chunk's operands: PER_THREAD + 1 16-byte loads per thread (record
+    // tiles -W, Q e^b, K~, P; this CTA's J columns of dO) and e^{b_L},
+    // loaded into registers one chunk ahead, then converted into shared memory.
+    uint4 raw[L::PER_THREAD], rdo;
     float graw = 1.0f;
+    constexpr int DO_UNITS = J / 8;            // 16-byte units of one dO row segment
     auto load = [&](int c) {
         const int tok0 = t_begin + c * C, len = min(C, t_end - tok0);
         const uint8_t *rec = p.records + ((slot0 + c) * H + h) * (int64_t)Rec::BYTES;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int u = tid + kChainNT * k;   // 16-byte unit: WQ (1024), UK rows 64.. (512), AQ (512)
+        for (int k = 0; k < L::PER_THREAD; ++k) {
+            const int u = tid + NT * k;
             const uint8_t *src =
-                u < 1024 ? rec + Rec::WQ + tile::rs_off(128, u >> 3, (u & 7) * 8)
-                : u < 1536 ? rec + Rec::UK + tile::rs_off(128, 64 + ((u - 1024) >> 3), ((u - 1024) & 7) * 8)
-                           : rec + Rec::AQ + tile::rs_off(64, (u - 1536) >> 3, ((u - 1536) & 7) * 8);
+                u < WQU ? rec + Rec::WQ + tile::rs_off(128, u / CPR, (u % CPR) * 8)
+                : u < WQU + KU ? rec + Rec::UK + tile::rs_off(128, 64 + (u - WQU) / CPR, ((u - WQU) % CPR) * 8)
+                               : rec + Rec::AQ + tile::rs_off(64, (u - WQU - KU) >> 3, ((u - WQU - KU) & 7) * 8);
             raw[k] = *reinterpret_cast<const uint4 *>(src);
         }
-        const int r = tid >> 2, c8 = (tid & 3) * 8;
-        rdo = r < len ? *reinterpret_cast<const uint4 *>(p.d_o + ((int64_t)(tok0 + r) * H + h) * 64 + j0 + c8)
+        const int r = tid / DO_UNITS, c8 = (tid % DO_UNITS) * 8;
+        rdo = r < len ? *reinterpret_cast<const uint4 *>(p.d_o + ((int64_t)(tok0 + r) * H + h) * D + j0 + c8)
                       : make_uint4(0u, 0u, 0u, 0u);
-        if (tid < 64) graw = p.gend ? reinterpret_cast<const float *>(rec + Rec::GEND)[tid] : 1.0f;
+        if (tid < D) graw = p.gend ? reinterpret_cast<const float *>(rec + Rec::GEND)[tid] : 1.0f;
     };
     auto store = [&]() {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int u = tid + kChainNT * k;
-            float *to = u < 1024 ? ((u >> 3) < 64 ? sW + (u >> 3) * LDM : sQ + ((u >> 3) - 64) * LDM) + (u & 7) * 8
-                        : u < 1536 ? sK + ((u - 1024) >> 3) * LDM + ((u - 1024) & 7) * 8
-                                   : sP + ((u - 1536) >> 3) * LDM + ((u - 1536) & 7) * 8;
+        for (int k = 0; k < L::PER_THREAD; ++k) {
+            const int u = tid + NT * k;
+            float *to = u < WQU ? ((u / CPR) < 64 ? sW + (u / CPR) * LD : sQ + (u / CPR - 64) * LD) + (u % CPR) * 8
+                        : u < WQU + KU ? sK + ((u - WQU) / CPR) * LD + ((u - WQU) % CPR) * 8
+                                       : sP + ((u - WQU - KU) >> 3) * LDM + ((u - WQU - KU) & 7) * 8;
             float v[8];
             tile::unpack8(raw[k], v);
 #pragma unroll
@@ -222,35 +241,42 @@ __global__ void __launch_bounds__(kChainNT) delta_bwd_chain_kernel(ChainParams p
         }
         float v[8];
         tile::unpack8(rdo, v);
-        float *to = sDO + (tid >> 2) * LDJ + (tid & 3) * 8;
+        float *to = sDO + (tid / DO_UNITS) * LDJ + (tid % DO_UNITS) * 8;
 #pragma unroll
         for (int i = 0; i < 8; ++i) to[i] = p.scale * v[i];
-        if (tid < 64) sG[tid] = graw;
+        if (tid < D) sG[tid] = graw;
     };
     if (nc > 0) load(nc - 1);
     for (int c = nc - 1; c >= 0; --c) {
         // dS' of this chunk out; the chunk's operands in
-        float *dst = p.dstates + ((slot0 + c) * H + h) * (int64_t)(64 * 64);
-        for (int e = tid; e < 64 * kJ; e += kChainNT) {
-            const int i = e / kJ, j = e % kJ;
-            dst[i * 64 + j0 + j] = sDS[i * LDJ + j];
+        float *dst = p.dstates + ((slot0 + c) * H + h) * (int64_t)(D * D);
+        for (int e = tid; e < D * J; e += NT) {
+            const int i = e / J, j = e % J;
+            dst[i * D + j0 + j] = sDS[i * LDJ + j];
         }
         store();
         __syncthreads();
         if (c > 0) load(c - 1);   // in flight during this chunk's products
         // du = P^T dO' + K~ dS'
-        mm<64, kJ, 64, true, false, LDM, LDJ, LDJ, 8>(sDU, sP, sDO, 1.0f, false);
-        mm<64, kJ, 64, false, false, LDM, LDJ, LDJ, 8>(sDU, sK, sDS, 1.0f, true);
+        mm<64, J, 64, true, false, LDM, LDJ, LDJ, NW>(sDU, sP, sDO, 1.0f, false);
+        mm<64, J, D, false, false, LD, LDJ, LDJ, NW>(sDU, sK, sDS, 1.0f, true);
         __syncthreads();
+        if (p.du) {
+            float *du = p.du + ((slot0 + c) * H + h) * (int64_t)(64 * D);
+            for (int e = tid; e < 64 * J; e += NT) {
+                const int i = e / J, j = e % J;
+                du[i * D + j0 + j] = sDU[i * LDJ + j];
+            }
+        }
         // dS = e^{b_L} dS' + (Q e^b)^T dO' + (-W)^T du   (same tiles per warp)
-        mm<64, kJ, 64, true, false, LDM, LDJ, LDJ, 8>(sDS, sQ, sDO, 1.0f, true, sG);
-        mm<64, kJ, 64, true, false, LDM, LDJ, LDJ, 8>(sDS, sW, sDU, 1.0f, true);
+        mm<D, J, 64, true, false, LD, LDJ, LDJ, NW>(sDS, sQ, sDO, 1.0f, true, sG);
+        mm<D, J, 64, true, false, LD, LDJ, LDJ, NW>(sDS, sW, sDU, 1.0f, true);
         __syncthreads();
     }
     if (p.d_init_S) {
-        for (int e = tid; e < 64 * kJ; e += kChainNT) {
-            const int i = e / kJ, j = e % kJ;
-            p.d_init_S[sbase + i * 64 + j0 + j] = sDS[i * LDJ + j];
+        for (int e = tid; e < D * J; e += NT) {
+            const int i = e / J, j = e % J;
+            p.d_init_S[sbase + i * D + j0 + j] = sDS[i * LDJ + j];
         }
     }
 }
@@ -695,41 +721,57 @@ __global__ void __launch_bounds__(kGradNT, 1) delta_bwd_chunk_kernel(ChunkParams
 size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct ChunkWs {
-    size_t fwd, states, dstates, total;
+    size_t fwd, states, dstates, du, total;
 };
 
-ChunkWs chunk_ws(int N, int ntok, int H) {
+ChunkWs chunk_ws(int N, int ntok, int H, int D) {
     const size_t slots = (size_t)tile::Workspace::slots(N, ntok);
     ChunkWs w;
-    w.fwd = a256(delta_tc_workspace_bytes(N, ntok, H, 64, 64, 64, true));
-    w.states = a256(slots * H * 4096 * sizeof(float));
+    w.fwd = a256(delta_tc_workspace_bytes(N, ntok, H, D, D, 64, true));
+    w.states = a256(slots * H * D * D * sizeof(float));
     w.dstates = w.states;
-    w.total = w.fwd + w.states + w.dstates;
+    w.du = a256(slots * H * 64 * D * sizeof(float));
+    w.total = w.fwd + w.states + w.dstates + w.du;
     return w;
+}
+
+template <int D>
+cudaError_t launch_chain(const ChainParams &cp, int N, int H, cudaStream_t s) {
+    using L = ChainCfg<D>;
+    const size_t smem = (size_t)L::FLOATS * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(delta_bwd_chain_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    delta_bwd_chain_kernel<D><<<dim3(H, N, D / L::J), L::NT, smem, s>>>(cp);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
 bool delta_bwd_chunked_supported(const BwdArgs &a) {
-    return a.bf16 && a.dk == 64 && a.dv == 64 && !(a.flags & kAdditive) &&
-           (!a.gate_logits || (a.flags & kGateScalar));
+    return a.bf16 && a.dk == a.dv && (a.dk == 64 || a.dk == 128) && !(a.flags & kAdditive);
 }
 
-size_t delta_bwd_chunked_workspace_bytes(int N, int ntok, int H) {
-    return chunk_ws(N, ntok, H).total;
+size_t delta_bwd_chunked_workspace_bytes(int N, int ntok, int H, int D) {
+    return chunk_ws(N, ntok, H, D).total;
 }
 
 cudaError_t launch_delta_backward_chunked(const BwdArgs &a, cudaStream_t s) {
-    const ChunkWs w = chunk_ws(a.N, a.ntok, a.H);
+    const int D = a.dk;
+    const ChunkWs w = chunk_ws(a.N, a.ntok, a.H, D);
     uint8_t *base = static_cast<uint8_t *>(a.workspace);
     float *states = reinterpret_cast<float *>(base + w.fwd);
     float *dstates = reinterpret_cast<float *>(base + w.fwd + w.states);
+    float *du = reinterpret_cast<float *>(base + w.fwd + w.states + w.dstates);
     unsigned *err = device_error_word();
     if (!err) return cudaErrorInvalidValue;
+    // d = 64 without a per-channel decay: the fp32 per-chunk kernel of this
+    // file; otherwise the bf16 one with per-channel decay (it needs du)
+    const bool channel = D != 64 || (a.gate_logits && !(a.flags & kGateScalar));
 
     // 1. the forward pass, keeping its records and the state at every chunk start
     PrefillArgs pa{a.q, a.k, a.v, a.beta_logits, a.gate_logits, nullptr, a.cu_seqlens, a.N,
-                   a.ntok, a.H, 64, 64, a.scale, a.flags, a.init_S, nullptr, nullptr, nullptr,
+                   a.ntok, a.H, D, D, a.scale, a.flags, a.init_S, nullptr, nullptr, nullptr,
                    true, base, w.fwd};
     pa.chunk_states = states;
     if (!delta_tc_supported(pa)) return cudaErrorInvalidValue;
@@ -739,24 +781,29 @@ cudaError_t launch_delta_backward_chunked(const BwdArgs &a, cudaStream_t s) {
     // 2. dS from the last chunk to the first
     const uint8_t *records = base + tile::Workspace::table_bytes(a.N, a.ntok);
     ChainParams cp{records, static_cast<const __nv_bfloat16 *>(a.d_o), a.cu_seqlens, a.d_final_S,
-                   dstates, a.d_init_S, err, a.H, a.ntok, a.scale, a.gate_logits != nullptr};
-    const size_t chain_smem = (size_t)ChainLayout::FLOATS * sizeof(float);
-    if ((e = cudaFuncSetAttribute(delta_bwd_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)chain_smem)) != cudaSuccess)
-        return e;
-    delta_bwd_chain_kernel<<<dim3(a.H, a.N, 64 / kJ), kChainNT, chain_smem, s>>>(cp);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+                   dstates, channel ? du : nullptr, a.d_init_S, err, a.H, a.ntok, a.scale,
+                   a.gate_logits != nullptr};
+    e = D == 64 ? launch_chain<64>(cp, a.N, a.H, s) : launch_chain<128>(cp, a.N, a.H, s);
+    if (e != cudaSuccess) return e;
 
     // 3. every (chunk, head): the gradients, through the prologue
+    const int64_t n_tasks = tile::Workspace::slots(a.N, a.ntok) * a.H;
+    const int2 *table = reinterpret_cast<const int2 *>(base);
+    if (channel) {
+        BwdChannelArgs ca{a.q, a.k, a.v, a.beta_logits, a.gate_logits, a.d_o, table, states,
+                          dstates, du, a.dq, a.dk_out, a.dv_out, a.d_beta_logits,
+                          a.gate_logits ? a.d_gate_logits : nullptr, n_tasks, a.H, D, a.scale,
+                          a.flags};
+        return launch_delta_bwd_channel(ca, s);
+    }
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    const int64_t n_tasks = tile::Workspace::slots(a.N, a.ntok) * a.H;
     ChunkParams gp{static_cast<const __nv_bfloat16 *>(a.q), static_cast<const __nv_bfloat16 *>(a.k),
                    static_cast<const __nv_bfloat16 *>(a.v),
                    static_cast<const __nv_bfloat16 *>(a.beta_logits),
                    a.gate_logits ? static_cast<const __nv_bfloat16 *>(a.gate_logits) : nullptr,
-                   static_cast<const __nv_bfloat16 *>(a.d_o), reinterpret_cast<const int2 *>(base),
+                   static_cast<const __nv_bfloat16 *>(a.d_o), table,
                    states, dstates, a.dq, a.dk_out, a.dv_out, a.d_beta_logits,
                    a.gate_logits ? a.d_gate_logits : nullptr, n_tasks, a.H, a.scale, a.flags};
     const size_t grad_smem = (size_t)GradLayout::FLOATS * sizeof(float);

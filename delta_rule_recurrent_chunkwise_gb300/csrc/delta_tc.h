@@ -58,4 +58,21 @@ cudaError_t launch_delta_inter(const TcLaunch &x, cudaStream_t s);
 // The recurrence over 128-token chunks (pairs of 64-token records; d = 64).
 cudaError_t launch_delta_inter128(const TcLaunch &x, cudaStream_t s);
 
+// Per-chunk gradients of the chunkwise backward pass (bf16, d = dk = dv in
+// {64, 128}, a decay per key channel, per token or none): every (chunk,
+// head) from its inputs, its starting state, the reverse chain's dS' and du.
+struct BwdChannelArgs {
+    const void *q, *k, *v, *beta_logits, *gate_logits, *d_o;
+    const int2 *table;        // [slots] {first token, length}
+    const float *states;      // [slots][H][D][D] S at each chunk start
+    const float *dstates;     // [slots][H][D][D] dS' of each chunk
+    const float *du;          // [slots][H][64][D] du of each chunk
+    float *dq, *dk, *dv, *d_beta_logits, *d_gate_logits;
+    int64_t n_tasks;
+    int H, D;
+    float scale;
+    unsigned flags;
+};
+cudaError_t launch_delta_bwd_channel(const BwdChannelArgs &a, cudaStream_t s);
+
 }  // namespace la

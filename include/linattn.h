@@ -238,10 +238,16 @@ la_status la_decode_step_slots(const void *q, const void *k, const void *v,
  * gate_logits is given); d_init_S [N][H][dk][dv] or NULL.  Rows of tokens
  * outside every sequence are not written.
  * Workspace: la_backward_delta_workspace_size bytes, 256-byte aligned
- * (chunk-start states, per-token column sums); LA_ERR_INVALID_ARG if
- * smaller or missing.  dk, dv in {64, 128}.  The sums over value columns
- * inside a thread block use shared-memory atomics, so the last bits of
- * dq, dk, d_beta_logits and d_gate_logits may differ between runs. */
+ * (the forward pass's per-chunk records, the state and its gradient at
+ * every chunk start, du per chunk; or, token-serial, checkpoints and
+ * per-token column sums); LA_ERR_INVALID_ARG if smaller or missing.
+ * dk, dv in {64, 128}.  Two forms, chosen from the arguments: chunkwise
+ * (io = LA_BF16, dk = dv, without LA_ADDITIVE; any gate) -- the
+ * tensor-core forward pass, a reverse pass over the chunks for the state
+ * gradient, then every (chunk, head) in parallel; token-serial otherwise.
+ * Sums over value columns inside a thread block use shared-memory atomics,
+ * so the last bits of dq, dk, d_beta_logits and d_gate_logits may differ
+ * between runs. */
 size_t la_backward_delta_workspace_size(int N, int ntok, int H, int dk, int dv);
 la_status la_backward_delta(const void *q, const void *k, const void *v, const void *beta_logits,
                             const void *gate_logits, const void *d_o, const float *d_final_S,

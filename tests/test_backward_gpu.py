@@ -103,3 +103,45 @@ def test_backward_gpt2_shape_sampled_heads(cuda_lib):
     ref = _oracle(inp, d_o, d_fS, oracle.L2NORM_K, heads=heads)
     sub = {n: (None if v is None else v[:, heads]) for n, v in got.items()}
     _compare(sub, ref, TOL[w.dtype])
+
+
+def test_backward_gated_shape_sampled_heads(cuda_lib):
+    """The gated prefill shape (4 x 8192 tokens, 32 heads, d = 128, a decay per
+    key channel, bf16): the whole backward on the GPU (chunkwise, per-channel
+    decay kernel), the oracle on two heads of every sequence."""
+    la = cuda_lib
+    w = wl.workload("gated_prefill")
+    inp = wl.inputs_for(w, seed=0, init_state=True)
+    d_o, d_fS = _grad_inputs(inp, w.dtype, seed=75)
+    got = _run(la, inp, d_o, d_fS, la.LA_L2NORM_K)
+    heads = [5, 30]
+    ref = _oracle(inp, d_o, d_fS, oracle.L2NORM_K, heads=heads)
+    sub = {n: (None if v is None else v[:, heads]) for n, v in got.items()}
+    _compare(sub, ref, TOL[w.dtype])
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_strong_channel_decay(cuda_lib, d):
+    """Gate logits around 8 (alpha ~ e^-8 per token and channel): the decay
+    across a 16-token block underflows fp32, so only the exact in-block terms
+    and products of factors <= 1 may carry it."""
+    la = cuda_lib
+    inp = wl.prefill_inputs([190, 64, 33], 2, d, d, torch.bfloat16, True, seed=76,
+                            init_state=True, gate_mean=8.0)
+    d_o, d_fS = _grad_inputs(inp, torch.bfloat16, seed=77)
+    got = _run(la, inp, d_o, d_fS, la.LA_L2NORM_K)
+    ref = _oracle(inp, d_o, d_fS, oracle.L2NORM_K)
+    _compare(got, ref, TOL[torch.bfloat16])
+
+
+def test_backward_channel_flags_and_scale_d128(cuda_lib):
+    """silu and L2 norm on q and k, a scale, per-channel gate, bf16, d = 128."""
+    la = cuda_lib
+    inp = wl.prefill_inputs([150, 64, 1], 3, 128, 128, torch.bfloat16, True, seed=78,
+                            init_state=True)
+    d_o, d_fS = _grad_inputs(inp, torch.bfloat16, seed=79)
+    flags = la.LA_L2NORM_K | la.LA_L2NORM_Q | la.LA_SILU_QK
+    oflags = oracle.L2NORM_K | oracle.L2NORM_Q | oracle.SILU_QK
+    got = _run(la, inp, d_o, d_fS, flags, scale=0.6)
+    ref = _oracle(inp, d_o, d_fS, oflags, scale=0.6)
+    _compare(got, ref, TOL[torch.bfloat16])
