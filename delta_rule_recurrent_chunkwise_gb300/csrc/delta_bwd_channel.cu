@@ -37,7 +37,7 @@
 // the CUDA cores (exponent <= 0 again), whatever the decay's strength.
 //
 // Mapping: a persistent grid over (chunk, head) tasks, 16 warps per CTA.
-// Products are warp-level bf16 mma.sync (m16n8k16) on bf16 shared-memory
+// Products are warp-level bf16 mma.sync (m16n8k16, warp_mma.cuh) on bf16 shared-memory
 // operands with fp32 accumulation; the three gradient accumulators dQ, dK+
 // and dK- stay in registers from the first product that feeds them to the
 // end of the task (warp w owns rows 16 (w / 4) .. +15 and a quarter of the
@@ -47,6 +47,7 @@
 #include "delta_tc.h"
 #include "launch.h"
 #include "tc_tile.cuh"
+#include "warp_mma.cuh"
 
 namespace la {
 namespace {
@@ -58,76 +59,23 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // ------------------------------------------------------------ warp products
 
-__device__ __forceinline__ uint32_t saddr(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
+using wmma16::ld2;
+using wmma16::PadView;
+using wmma16::st2;
+using wmma16::zero;
 
-__device__ __forceinline__ void ldsm(uint32_t (&r)[4], const bf16 *p) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(saddr(p)));
-}
-
-__device__ __forceinline__ void ldsm_t(uint32_t (&r)[4], const bf16 *p) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(saddr(p)));
-}
-
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// One 16-deep step of a warp's 16 x 16 output block (two n8 tiles):
-//   d += op(A)[m0 .. m0+15][k .. k+15] op(B)[k .. k+15][n0 .. n0+15]
-// op(A) = A (stored [m][k], TA = false) or A^T (stored [k][m]); op(B) = B
-// (stored [k][n], TB = false) or B^T (stored [n][k]).  Row strides in
-// elements, multiples of 8; m0, n0, k multiples of 8 (k of 16).  ldmatrix
-// hands every lane its fragment: lanes 8j .. 8j + 7 address the rows of
-// 8 x 8 block j, transposed on the way for the [k][m] and [k][n] forms.
+// Products on padded row-major tiles (warp_mma.cuh): one 16-deep step of a
+// 16 x 16 output block, and NT n8 tiles over a k range.
 template <bool TA, bool TB>
 __device__ __forceinline__ void mma_step(float (&d)[2][4], const bf16 *A, int lda, const bf16 *B,
                                          int ldb, int m0, int n0, int k) {
-    const int lane = threadIdx.x & 31, li = lane & 7, lj = lane >> 3;
-    uint32_t a[4], b[4];
-    if constexpr (!TA) ldsm(a, A + (m0 + (lane & 15)) * lda + k + (lane >> 4) * 8);
-    else ldsm_t(a, A + (k + li + 8 * (lj >> 1)) * lda + m0 + 8 * (lj & 1));
-    if constexpr (TB) ldsm(b, B + (n0 + li + 8 * (lj >> 1)) * ldb + k + 8 * (lj & 1));
-    else ldsm_t(b, B + (k + li + 8 * (lj & 1)) * ldb + n0 + 8 * (lj >> 1));
-    mma16816(d[0], a, b[0], b[1]);
-    mma16816(d[1], a, b[2], b[3]);
+    wmma16::mma_step<TA, TB>(d, PadView{A, lda}, PadView{B, ldb}, m0, n0, k);
 }
 
-// d (NT n8 tiles from column n0) += op(A) op(B) over k in [k0, k1).
 template <int NT, bool TA, bool TB>
 __device__ __forceinline__ void mma_rows(float (&d)[NT][4], const bf16 *A, int lda, const bf16 *B,
                                          int ldb, int m0, int n0, int k0, int k1) {
-    for (int k = k0; k < k1; k += 16) {
-#pragma unroll
-        for (int j = 0; j < NT; j += 2) {
-            float (&dp)[2][4] = *reinterpret_cast<float (*)[2][4]>(&d[j]);
-            mma_step<TA, TB>(dp, A, lda, B, ldb, m0, n0 + 8 * j, k);
-        }
-    }
-}
-
-template <int NT>
-__device__ __forceinline__ void zero(float (&d)[NT][4]) {
-#pragma unroll
-    for (int j = 0; j < NT; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.0f;
-}
-
-__device__ __forceinline__ void st2(bf16 *p, float a, float b) {
-    *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(a, b);
-}
-
-__device__ __forceinline__ float2 ld2(const bf16 *p) {
-    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
+    wmma16::mma_rows<NT, TA, TB>(d, PadView{A, lda}, PadView{B, ldb}, m0, n0, k0, k1);
 }
 
 // ------------------------------------------------------------ layout

@@ -39,6 +39,7 @@
 #include "delta_tc.h"
 #include "launch.h"
 #include "tc_tile.cuh"
+#include "warp_mma.cuh"
 
 namespace la {
 namespace {
@@ -158,40 +159,48 @@ struct ChainParams {
     bool gend;                // records carry e^{b_L} (gated); else it is 1
 };
 
-// Threads and value columns of dS per chain CTA: 8 warps and 32 columns at
-// d = 64; 16 warps and 64 columns at d = 128 (half as many CTAs, each one
-// chain of the sequence's chunks).
+// One CTA of 16 warps per (head, sequence).  Shared memory (bytes): two
+// record buffers (the operands of one chunk copied from its record: [-W ;
+// Q e^b] as a 128-row swizzled tile, K e^{b_L - b} as a 64-row one, Aq, and
+// e^{b_L}), two buffers of scale dO, the bf16 copy of dS' and du, barriers.
 template <int D> struct ChainCfg {
-    static constexpr int NT = D == 64 ? 256 : 512;
-    static constexpr int J = D == 64 ? 32 : 64;
-    static constexpr int LDJ = J + 4;
-    static constexpr int LD = D + 4;            // fp32 row stride of a 64 x D record tile
-    // shared-memory layout (floats)
-    static constexpr int W = 0, Q = W + 64 * LD, K = Q + 64 * LD, P = K + 64 * LD;
-    static constexpr int G = P + MAT, DO = G + D, DS = DO + 64 * LDJ, DU = DS + D * LDJ;
-    static constexpr int FLOATS = DU + 64 * LDJ;
-    // 16-byte units of one chunk's record operands: -W and Q e^b (128 rows),
-    // K e^{b_L - b} (64 rows), Aq (64 x 64)
-    static constexpr int UNITS = 128 * D / 8 + 64 * D / 8 + 512;
-    static constexpr int PER_THREAD = UNITS / NT;
-    static_assert(UNITS % NT == 0, "whole units per thread");
-    static_assert(NT == 64 * (J / 8), "one 16-byte unit of dO per thread");
+    static constexpr int NT = 512;
+    static constexpr int XS = D + 8;                      // bf16 stride of dO, du, dS'
+    static constexpr int WQB = 128 * D * 2, KB = 64 * D * 2, AQB = 64 * 64 * 2, GB = 4 * D;
+    static constexpr int TX = WQB + KB + AQB + GB;        // bytes a record copy delivers
+    static constexpr int BUF = (TX + 1023) & ~1023;
+    static constexpr int DO = 2 * BUF, DOB = 64 * XS * 2;
+    static constexpr int DS = DO + 2 * DOB, DU = DS + D * XS * 2, BARS = DU + 64 * XS * 2;
+    static constexpr int BYTES = BARS + 64;
+    // warp tiles: du (64 x D) in 4 row blocks x 4 column groups; dS (D x D)
+    // in D/16 row blocks x 16/(D/16) column groups
+    static constexpr int NT_DU = D / 32;
+    static constexpr int CG = 16 / (D / 16), NT_DS = D / CG / 8;
+    static constexpr int DO_UNITS = 64 * D / 8 / NT;     // 16-byte units of dO per thread
 };
 
-// Reverse pass over the chunks of one (head, sequence), J value columns of
-// dS per CTA (the columns of dS never mix).
+// Reverse pass over the chunks of one (head, sequence).  dS (fp32) stays in
+// registers for the whole sequence; per chunk c, last to first:
+//   store dS' (= dS) of chunk c;  du = Aq^T dO' + K~ dS';
+//   dS = Diag(e^{b_L}) dS' + (Q e^b)^T dO' + (-W)^T du
+// with bf16 operands (dS' and du rounded for the products only) read by
+// ldmatrix straight from the record tiles.  Chunk c - 1's record arrives by
+// bulk copy into the other buffer while chunk c computes.
 template <int D>
-__global__ void __launch_bounds__(ChainCfg<D>::NT) delta_bwd_chain_kernel(ChainParams p) {
+__global__ void __launch_bounds__(ChainCfg<D>::NT, 1) delta_bwd_chain_kernel(ChainParams p) {
+    using namespace tc;
     using L = ChainCfg<D>;
     using Rec = tile::Record<D>;
-    constexpr int NT = L::NT, J = L::J, LDJ = L::LDJ, LD = L::LD, NW = NT / 32;
-    constexpr int WQU = 128 * D / 8, KU = 64 * D / 8;   // unit boundaries
-    constexpr int CPR = D / 8;                           // units per record row
-    extern __shared__ __align__(16) float sm[];
-    float *sW = sm + L::W, *sQ = sm + L::Q, *sK = sm + L::K, *sP = sm + L::P, *sG = sm + L::G;
-    float *sDO = sm + L::DO, *sDS = sm + L::DS, *sDU = sm + L::DU;
-    const int tid = threadIdx.x;
-    const int h = blockIdx.x, n = blockIdx.y, j0 = blockIdx.z * J, H = p.H;
+    using wmma16::PadView;
+    using wmma16::RsView;
+    using bf16 = __nv_bfloat16;
+    constexpr int XS = L::XS, NT_DU = L::NT_DU, NT_DS = L::NT_DS;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BARS);
+    bf16 *sDS = reinterpret_cast<bf16 *>(smem + L::DS), *sDU = reinterpret_cast<bf16 *>(smem + L::DU);
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int h = blockIdx.x, n = blockIdx.y, H = p.H;
     int t_begin = p.cu[n], t_end = p.cu[n + 1];
     if (t_begin < 0 || t_end < t_begin || t_end > p.ntok) {
         if (tid == 0) atomicCAS(p.err, 0u, 100u);
@@ -200,84 +209,140 @@ __global__ void __launch_bounds__(ChainCfg<D>::NT) delta_bwd_chain_kernel(ChainP
     const int nc = (t_end - t_begin + C - 1) / C;
     const int64_t slot0 = (int64_t)(t_begin / C) + n;
     const int64_t sbase = ((int64_t)n * H + h) * D * D;
-    for (int e = tid; e < D * J; e += NT) {
-        const int i = e / J, j = e % J;
-        sDS[i * LDJ + j] = p.d_final_S ? p.d_final_S[sbase + i * D + j0 + j] : 0.0f;
+    // this warp's blocks: du rows 16 Ru, columns nu ..; dS rows 16 Rs, columns ns ..
+    const int Ru = w >> 2, nu = (w & 3) * (D / 4);
+    const int Rs = w / L::CG, ns = (w % L::CG) * (D / L::CG);
+
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_mbar_init();
     }
-    // One chunk's operands: PER_THREAD + 1 16-byte loads per thread (record
-    // tiles -W, Q e^b, K~, P; this CTA's J columns of dO) and e^{b_L},
-    // loaded into registers one chunk ahead, then converted into shared memory.
-    uint4 raw[L::PER_THREAD], rdo;
-    float graw = 1.0f;
-    constexpr int DO_UNITS = J / 8;            // 16-byte units of one dO row segment
-    auto load = [&](int c) {
-        const int tok0 = t_begin + c * C, len = min(C, t_end - tok0);
+    __syncthreads();
+    auto issue = [&](int c) {   // thread 0: chunk c's record into buffer c & 1
+        uint8_t *buf = smem + (c & 1) * L::BUF;
         const uint8_t *rec = p.records + ((slot0 + c) * H + h) * (int64_t)Rec::BYTES;
+        fence_proxy_async();
+        mbar_arrive_expect_tx(&bars[c & 1], L::TX);
+        bulk_load(buf, rec + Rec::WQ, L::WQB, &bars[c & 1]);
 #pragma unroll
-        for (int k = 0; k < L::PER_THREAD; ++k) {
-            const int u = tid + NT * k;
-            const uint8_t *src =
-                u < WQU ? rec + Rec::WQ + tile::rs_off(128, u / CPR, (u % CPR) * 8)
-                : u < WQU + KU ? rec + Rec::UK + tile::rs_off(128, 64 + (u - WQU) / CPR, ((u - WQU) % CPR) * 8)
-                               : rec + Rec::AQ + tile::rs_off(64, (u - WQU - KU) >> 3, ((u - WQU - KU) & 7) * 8);
-            raw[k] = *reinterpret_cast<const uint4 *>(src);
-        }
-        const int r = tid / DO_UNITS, c8 = (tid % DO_UNITS) * 8;
-        rdo = r < len ? *reinterpret_cast<const uint4 *>(p.d_o + ((int64_t)(tok0 + r) * H + h) * D + j0 + c8)
-                      : make_uint4(0u, 0u, 0u, 0u);
-        if (tid < D) graw = p.gend ? reinterpret_cast<const float *>(rec + Rec::GEND)[tid] : 1.0f;
+        for (int cb = 0; cb < D / 64; ++cb)   // rows 64..127 of each 64-column block of [U ; K~]
+            bulk_load(buf + L::WQB + cb * 8192, rec + Rec::UK + cb * 16384 + 8192, 8192, &bars[c & 1]);
+        bulk_load(buf + L::WQB + L::KB, rec + Rec::AQ, L::AQB, &bars[c & 1]);
+        bulk_load(buf + L::WQB + L::KB + L::AQB, rec + Rec::GEND, L::GB, &bars[c & 1]);
     };
-    auto store = [&]() {
+    // this thread's 16-byte units of scale * dO (rows past the end are zero)
+    uint4 rdo[L::DO_UNITS];
+    auto load_do = [&](int c) {
+        const int tok0 = t_begin + c * C, len = min(C, t_end - tok0);
 #pragma unroll
-        for (int k = 0; k < L::PER_THREAD; ++k) {
-            const int u = tid + NT * k;
-            float *to = u < WQU ? ((u / CPR) < 64 ? sW + (u / CPR) * LD : sQ + (u / CPR - 64) * LD) + (u % CPR) * 8
-                        : u < WQU + KU ? sK + ((u - WQU) / CPR) * LD + ((u - WQU) % CPR) * 8
-                                       : sP + ((u - WQU - KU) >> 3) * LDM + ((u - WQU - KU) & 7) * 8;
+        for (int k = 0; k < L::DO_UNITS; ++k) {
+            const int u = tid + L::NT * k, r = u / (D / 8), c8 = (u % (D / 8)) * 8;
+            rdo[k] = r < len ? *reinterpret_cast<const uint4 *>(p.d_o + ((int64_t)(tok0 + r) * H + h) * D + c8)
+                             : make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+    auto store_do = [&](int c) {
+        bf16 *dst = reinterpret_cast<bf16 *>(smem + L::DO + (c & 1) * L::DOB);
+#pragma unroll
+        for (int k = 0; k < L::DO_UNITS; ++k) {
+            const int u = tid + L::NT * k, r = u / (D / 8), c8 = (u % (D / 8)) * 8;
             float v[8];
-            tile::unpack8(raw[k], v);
+            tile::unpack8(rdo[k], v);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) to[i] = v[i];
+            for (int i = 0; i < 8; ++i) v[i] *= p.scale;
+            *reinterpret_cast<uint4 *>(dst + r * XS + c8) = tile::pack8(v);
         }
-        float v[8];
-        tile::unpack8(rdo, v);
-        float *to = sDO + (tid / DO_UNITS) * LDJ + (tid % DO_UNITS) * 8;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) to[i] = p.scale * v[i];
-        if (tid < D) sG[tid] = graw;
     };
-    if (nc > 0) load(nc - 1);
-    for (int c = nc - 1; c >= 0; --c) {
-        // dS' of this chunk out; the chunk's operands in
-        float *dst = p.dstates + ((slot0 + c) * H + h) * (int64_t)(D * D);
-        for (int e = tid; e < D * J; e += NT) {
-            const int i = e / J, j = e % J;
-            dst[i * D + j0 + j] = sDS[i * LDJ + j];
+
+    // dS' of the last chunk: the final state's gradient
+    float ds[NT_DS][4];
+#pragma unroll
+    for (int j = 0; j < NT_DS; ++j)
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+            const int r = 16 * Rs + g + 8 * hr, col = ns + 8 * j + 2 * t;
+            const float2 v = p.d_final_S ? *reinterpret_cast<const float2 *>(p.d_final_S + sbase + r * D + col)
+                                         : make_float2(0.0f, 0.0f);
+            ds[j][2 * hr] = v.x;
+            ds[j][2 * hr + 1] = v.y;
         }
-        store();
-        __syncthreads();
-        if (c > 0) load(c - 1);   // in flight during this chunk's products
-        // du = P^T dO' + K~ dS'
-        mm<64, J, 64, true, false, LDM, LDJ, LDJ, NW>(sDU, sP, sDO, 1.0f, false);
-        mm<64, J, D, false, false, LD, LDJ, LDJ, NW>(sDU, sK, sDS, 1.0f, true);
-        __syncthreads();
-        if (p.du) {
-            float *du = p.du + ((slot0 + c) * H + h) * (int64_t)(64 * D);
-            for (int e = tid; e < 64 * J; e += NT) {
-                const int i = e / J, j = e % J;
-                du[i * D + j0 + j] = sDU[i * LDJ + j];
-            }
-        }
-        // dS = e^{b_L} dS' + (Q e^b)^T dO' + (-W)^T du   (same tiles per warp)
-        mm<D, J, 64, true, false, LD, LDJ, LDJ, NW>(sDS, sQ, sDO, 1.0f, true, sG);
-        mm<D, J, 64, true, false, LD, LDJ, LDJ, NW>(sDS, sW, sDU, 1.0f, true);
-        __syncthreads();
+    if (nc > 0) {
+        if (tid == 0) issue(nc - 1);
+        load_do(nc - 1);
     }
-    if (p.d_init_S) {
-        for (int e = tid; e < D * J; e += NT) {
-            const int i = e / J, j = e % J;
-            p.d_init_S[sbase + i * D + j0 + j] = sDS[i * LDJ + j];
+    // chunk c is use (nc - 1 - c) / 2 of buffer c & 1: its phase parity
+    auto parity = [&](int c) { return (uint32_t)(((nc - 1 - c) >> 1) & 1); };
+    int pending = nc > 0 ? nc - 1 : -1;   // a record copy issued and not yet waited for
+    for (int c = nc - 1; c >= 0; --c) {
+        const int b = c & 1;
+        const uint8_t *buf = smem + b * L::BUF;
+        const RsView wq{buf, 128, 0}, qe{buf, 128, 64}, kt{buf + L::WQB, 64, 0};
+        const RsView aq{buf + L::WQB + L::KB, 64, 0};
+        const float *gend = reinterpret_cast<const float *>(buf + L::WQB + L::KB + L::AQB);
+        const PadView dO{reinterpret_cast<const bf16 *>(smem + L::DO + b * L::DOB), XS};
+        const PadView dSp{sDS, XS}, dU{sDU, XS};
+        // 1. dS' of chunk c out (fp32) and in (bf16 operand); this chunk's dO in
+        float *dst = p.dstates + ((slot0 + c) * H + h) * (int64_t)(D * D);
+#pragma unroll
+        for (int j = 0; j < NT_DS; ++j)
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                const int r = 16 * Rs + g + 8 * hr, col = ns + 8 * j + 2 * t;
+                *reinterpret_cast<float2 *>(dst + r * D + col) = make_float2(ds[j][2 * hr], ds[j][2 * hr + 1]);
+                wmma16::st2(sDS + r * XS + col, ds[j][2 * hr], ds[j][2 * hr + 1]);
+            }
+        store_do(c);
+        const bool ok = mbar_wait(&bars[b], parity(c), p.err, 15u);
+        if (__syncthreads_or(!ok)) break;
+        pending = -1;
+        if (c > 0) {
+            if (tid == 0) issue(c - 1);
+            pending = c - 1;
+            load_do(c - 1);
         }
+        // 2. du = Aq^T dO' + K~ dS' (Aq lower: rows r >= i of Aq reach column i)
+        {
+            float du[NT_DU][4];
+            wmma16::zero(du);
+            wmma16::mma_rows<NT_DU, true, false>(du, aq, dO, 16 * Ru, nu, 16 * Ru, 64);
+            wmma16::mma_rows<NT_DU, false, false>(du, kt, dSp, 16 * Ru, nu, 0, D);
+            float *gdu = p.du ? p.du + ((slot0 + c) * H + h) * (int64_t)(64 * D) : nullptr;
+#pragma unroll
+            for (int j = 0; j < NT_DU; ++j)
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int r = 16 * Ru + g + 8 * hr, col = nu + 8 * j + 2 * t;
+                    wmma16::st2(sDU + r * XS + col, du[j][2 * hr], du[j][2 * hr + 1]);
+                    if (gdu)
+                        *reinterpret_cast<float2 *>(gdu + r * D + col) = make_float2(du[j][2 * hr], du[j][2 * hr + 1]);
+                }
+        }
+        __syncthreads();
+        // 3. dS = Diag(e^{b_L}) dS' + (Q e^b)^T dO' + (-W)^T du
+        {
+            const float g0 = p.gend ? gend[16 * Rs + g] : 1.0f;
+            const float g1 = p.gend ? gend[16 * Rs + g + 8] : 1.0f;
+#pragma unroll
+            for (int j = 0; j < NT_DS; ++j) {
+                ds[j][0] *= g0; ds[j][1] *= g0;
+                ds[j][2] *= g1; ds[j][3] *= g1;
+            }
+            wmma16::mma_rows<NT_DS, true, false>(ds, qe, dO, 16 * Rs, ns, 0, 64);
+            wmma16::mma_rows<NT_DS, true, false>(ds, wq, dU, 16 * Rs, ns, 0, 64);
+        }
+    }
+    // a copy still in flight (only after a failed wait): let it land first
+    if (pending >= 0) mbar_wait(&bars[pending & 1], parity(pending), nullptr, 0u);
+    if (p.d_init_S) {
+#pragma unroll
+        for (int j = 0; j < NT_DS; ++j)
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                const int r = 16 * Rs + g + 8 * hr, col = ns + 8 * j + 2 * t;
+                *reinterpret_cast<float2 *>(p.d_init_S + sbase + r * D + col) =
+                    make_float2(ds[j][2 * hr], ds[j][2 * hr + 1]);
+            }
     }
 }
 
@@ -738,11 +803,11 @@ ChunkWs chunk_ws(int N, int ntok, int H, int D) {
 template <int D>
 cudaError_t launch_chain(const ChainParams &cp, int N, int H, cudaStream_t s) {
     using L = ChainCfg<D>;
-    const size_t smem = (size_t)L::FLOATS * sizeof(float);
+    const size_t smem = (size_t)L::BYTES;
     cudaError_t e = cudaFuncSetAttribute(delta_bwd_chain_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    delta_bwd_chain_kernel<D><<<dim3(H, N, D / L::J), L::NT, smem, s>>>(cp);
+    delta_bwd_chain_kernel<D><<<dim3(H, N), L::NT, smem, s>>>(cp);
     return cudaGetLastError();
 }
 
