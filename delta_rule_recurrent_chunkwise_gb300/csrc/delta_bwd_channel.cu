@@ -78,6 +78,18 @@ __device__ __forceinline__ void mma_rows(float (&d)[NT][4], const bf16 *A, int l
     wmma16::mma_rows<NT, TA, TB>(d, PadView{A, lda}, PadView{B, ldb}, m0, n0, k0, k1);
 }
 
+// 2^x for x <= 0 (every decay factor here): the hardware approximation,
+// relative error ~2^-22, flushing results below the fp32 normal range to 0.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
+}
+
 // ------------------------------------------------------------ layout
 
 // Shared memory (bytes).  Persistent through a task: q^, k^ (bf16), b in
@@ -91,8 +103,10 @@ struct Lay {
     static constexpr int LS = 72;               // bf16 stride of a 64 x 64 tile
     static constexpr int LB = 64 * LS * 2;
     static constexpr int TS = 68;               // fp32 stride of T during the solve
-    static constexpr int FS = D + 4;            // fp32 stride of a 64 x D gradient
-    static constexpr int Q = 0, K = Q + XB, B = K + XB, KK = B + 64 * D * 4, TB = KK + LB;
+    // fp32 stride of the decay table b and of the 64 x D gradients: D + 8
+    // words puts the rows of a quad's float2 accesses on distinct banks
+    static constexpr int FS = D + 8;
+    static constexpr int Q = 0, K = Q + XB, B = K + XB, KK = B + 64 * FS * 4, TB = KK + LB;
     static constexpr int BETA = TB + LB;                 // fp32 [64]
     static constexpr int DBETA = BETA + 256;             // fp32 [64]
     static constexpr int DBL = DBETA + 256;              // fp32 [D]: d b_L
@@ -107,7 +121,7 @@ struct Lay {
     // phase 1 (K_s, the per-block copies Y_R and T in fp32) and phase 6 (dQ,
     // dK and db in fp32) fit inside the union region
     static_assert(XB + 96 * XS * 2 + 64 * TS * 4 <= U_BYTES, "phase 1");
-    static_assert(2 * 64 * FS * 4 + 64 * D * 4 <= U_BYTES, "phase 6");
+    static_assert(3 * 64 * FS * 4 <= U_BYTES, "phase 6");
     static_assert(LB <= XB, "dP and dT fit in a 64 x D slot");
 };
 static_assert(Lay<128>::BYTES <= 232448, "shared memory at d = 128");
@@ -126,8 +140,8 @@ struct Params {
 };
 
 // Inclusive prefix sums down the 64 rows of each of the D columns of
-// x (fp32 [64][D]), in place; reverse = suffix sums.  All threads of the CTA.
-template <int D>
+// x (fp32 [64][LDX]), in place; reverse = suffix sums.  All threads of the CTA.
+template <int D, int LDX>
 __device__ __forceinline__ void column_scan(float *x, float *seg, bool reverse) {
     constexpr int NS = kNT / D, RS = 64 / NS;   // segments per column, rows per segment
     const int c = threadIdx.x % D, s = threadIdx.x / D;
@@ -135,8 +149,8 @@ __device__ __forceinline__ void column_scan(float *x, float *seg, bool reverse) 
 #pragma unroll
     for (int i = 0; i < RS; ++i) {
         const int r = reverse ? 63 - (s * RS + i) : s * RS + i;
-        run += x[r * D + c];
-        x[r * D + c] = run;
+        run += x[r * LDX + c];
+        x[r * LDX + c] = run;
     }
     seg[s * D + c] = run;
     __syncthreads();
@@ -145,7 +159,7 @@ __device__ __forceinline__ void column_scan(float *x, float *seg, bool reverse) 
 #pragma unroll
     for (int i = 0; i < RS; ++i) {
         const int r = reverse ? 63 - (s * RS + i) : s * RS + i;
-        x[r * D + c] += off;
+        x[r * LDX + c] += off;
     }
     __syncthreads();
 }
@@ -205,6 +219,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
     using L = Lay<D>;
     constexpr int XS = L::XS, LS = L::LS, TS = L::TS, FS = L::FS;
     constexpr int CPL = D / 32;          // channels per lane in row-wise passes
+    constexpr int P2 = D / 64;           // ... as pairs 2 lane + 64 m
     constexpr int NT = D / 32;           // n8 tiles of a warp's 16 x D/4 output block
     extern __shared__ __align__(16) uint8_t smem[];
     bf16 *sQ = reinterpret_cast<bf16 *>(smem + L::Q), *sK = reinterpret_cast<bf16 *>(smem + L::K);
@@ -225,6 +240,33 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
     const int R = w >> 2, cq = w & 3, n0 = cq * (D / 4);
     const int r0 = 16 * R + g, r1 = r0 + 8;   // this lane's two output rows
 
+    // inputs of task nt into L2 (one 128-byte line per request): the token
+    // rows of q, k, v, dO and per-channel gate logits, then S, dS' and du
+    auto prefetch_task = [&](int64_t nt) {
+        if (nt >= p.n_tasks) return;
+        const int64_t ns = nt / H;
+        const int nh = (int)(nt % H);
+        const int2 e = p.table[ns];
+        if (e.y <= 0 || e.y > 64) return;
+        constexpr int LPR = D * 2 / 128;   // lines per bf16 row
+        const bool pg = p.gate_logits && !scalar_gate;
+        for (int u = tid; u < 64 * LPR * 5; u += kNT) {
+            const int which = u / (64 * LPR), r = (u / LPR) % 64, l = u % LPR;
+            if (r >= e.y || (which == 4 && !pg)) continue;
+            const bf16 *base = which == 0 ? p.q : which == 1 ? p.k : which == 2 ? p.v
+                             : which == 3 ? p.d_o : p.gate_logits;
+            prefetch_l2(base + ((int64_t)(e.x + r) * H + nh) * D + l * 64);
+        }
+        const int64_t so = (ns * H + nh) * (int64_t)(D * D), uo = (ns * H + nh) * (int64_t)(64 * D);
+        for (int u = tid; u < D * D / 32 * 2 + 64 * D / 32; u += kNT) {
+            const float *q = u < D * D / 32 ? p.states + so + u * 32
+                           : u < D * D / 16 ? p.dstates + so + (u - D * D / 32) * 32
+                                            : p.du + uo + (u - D * D / 16) * 32;
+            prefetch_l2(q);
+        }
+    };
+    prefetch_task(blockIdx.x);
+
     for (int64_t task = blockIdx.x; task < p.n_tasks; task += gridDim.x) {
         const int64_t slot = task / H;
         const int h = (int)(task % H);
@@ -233,22 +275,29 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         if (len <= 0) continue;
         auto tok = [&](int r) { return ((int64_t)(t0 + r) * H + h); };
 
-        // ---- 0. q^, k^ (silu, L2 norm), beta, log2 alpha; b = prefix sums
+        // ---- 0. q^, k^ (silu, L2 norm), beta, log2 alpha; b = prefix sums.
+        // Lanes take channel pairs 2 lane + 64 m.
         for (int rr = 0; rr < 4; ++rr) {
             const int r = w + 16 * rr;
             const bool ok = r < len;
             float xq[CPL], xk[CPL], lg[CPL];
             const bf16 *pq = p.q + tok(ok ? r : 0) * D, *pk = p.k + tok(ok ? r : 0) * D;
+            const float gs = (ok && p.gate_logits && scalar_gate)
+                                 ? log_decay_f(__bfloat162float(p.gate_logits[tok(r)])) : 0.0f;
 #pragma unroll
-            for (int m = 0; m < CPL; ++m) {
-                const int c = lane + 32 * m;
-                xq[m] = ok ? __bfloat162float(pq[c]) : 0.0f;
-                xk[m] = ok ? __bfloat162float(pk[c]) : 0.0f;
-                float gl = 0.0f;
-                if (ok && p.gate_logits)
-                    gl = log_decay_f(__bfloat162float(scalar_gate ? p.gate_logits[tok(r)]
-                                                                  : p.gate_logits[tok(r) * D + c]));
-                lg[m] = gl * kLog2e;
+            for (int m = 0; m < P2; ++m) {
+                const int c = 2 * lane + 64 * m;
+                const float2 a = ok ? ld2(pq + c) : make_float2(0.0f, 0.0f);
+                const float2 b = ok ? ld2(pk + c) : make_float2(0.0f, 0.0f);
+                xq[2 * m] = a.x; xq[2 * m + 1] = a.y;
+                xk[2 * m] = b.x; xk[2 * m + 1] = b.y;
+                float2 gl = make_float2(gs, gs);
+                if (ok && p.gate_logits && !scalar_gate) {
+                    const float2 gg = ld2(p.gate_logits + tok(r) * D + c);
+                    gl = make_float2(log_decay_f(gg.x), log_decay_f(gg.y));
+                }
+                lg[2 * m] = gl.x * kLog2e;
+                lg[2 * m + 1] = gl.y * kLog2e;
             }
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
@@ -263,19 +312,23 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                 const float inv = norm ? 1.0f / fmaxf(sqrtf(warp_sum(ss)), 1e-12f) : 1.0f;
                 bf16 *dst = (which ? sK : sQ) + r * XS;
 #pragma unroll
-                for (int m = 0; m < CPL; ++m) dst[lane + 32 * m] = __float2bfloat16_rn(x[m] * inv);
+                for (int m = 0; m < P2; ++m)
+                    st2(dst + 2 * lane + 64 * m, x[2 * m] * inv, x[2 * m + 1] * inv);
             }
 #pragma unroll
-            for (int m = 0; m < CPL; ++m) sB[r * D + lane + 32 * m] = lg[m];
+            for (int m = 0; m < P2; ++m)
+                *reinterpret_cast<float2 *>(sB + r * FS + 2 * lane + 64 * m) = make_float2(lg[2 * m], lg[2 * m + 1]);
             if (lane == 0)
                 sBeta[r] = ok ? sigmoid_f(__bfloat162float(p.beta_logits[tok(r)])) : 0.0f;
         }
         if (tid < 64) sDBeta[tid] = 0.0f;
         if (tid < D) sDBL[tid] = sDGL[tid] = 0.0f;
         __syncthreads();
-        column_scan<D>(sB, sSeg, false);
+        column_scan<D, FS>(sB, sSeg, false);
+        prefetch_task(task + gridDim.x);
         // sB[r][c] = b_rc / ln 2 from here on; b at the token before block R
-        auto bs = [&](int Rb, int c) { return Rb == 0 ? 0.0f : sB[(16 * Rb - 1) * D + c]; };
+        auto bs = [&](int Rb, int c) { return Rb == 0 ? 0.0f : sB[(16 * Rb - 1) * FS + c]; };
+        auto b2at = [&](int r, int c) { return *reinterpret_cast<const float2 *>(sB + r * FS + c); };
 
         // ---- 1. decayed scores K * K, A = beta (K * K), T = (I + A)^{-1}
         // union: K_s at 0 (rows scaled to their block's start), Y_R for
@@ -287,13 +340,12 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         auto yrow = [](int Rb) { return 8 * Rb * (Rb - 1); };   // first row of Y_R in sY
         for (int e = tid; e < 64 * D / 2; e += kNT) {
             const int r = e / (D / 2), c = 2 * (e % (D / 2)), Rb = r >> 4;
-            const float2 kv = ld2(sK + r * XS + c);
-            st2(sKs + r * XS + c, kv.x * exp2f(sB[r * D + c] - bs(Rb, c)),
-                kv.y * exp2f(sB[r * D + c + 1] - bs(Rb, c + 1)));
+            const float2 kv = ld2(sK + r * XS + c), b = b2at(r, c);
+            st2(sKs + r * XS + c, kv.x * ex2(b.x - bs(Rb, c)), kv.y * ex2(b.y - bs(Rb, c + 1)));
             // row r of Y_R for every later block R
             for (int Rb2 = Rb + 1; Rb2 < 4; ++Rb2)
-                st2(sY + (yrow(Rb2) + r) * XS + c, kv.x * exp2f(bs(Rb2, c) - sB[r * D + c]),
-                    kv.y * exp2f(bs(Rb2, c + 1) - sB[r * D + c + 1]));
+                st2(sY + (yrow(Rb2) + r) * XS + c, kv.x * ex2(bs(Rb2, c) - b.x),
+                    kv.y * ex2(bs(Rb2, c + 1) - b.y));
         }
         for (int e = tid; e < 64 * 64; e += kNT) sT[(e >> 6) * TS + (e & 63)] = 0.0f;
         __syncthreads();
@@ -317,18 +369,20 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         for (int x = 0; x < 4; ++x) {
             const int o = x == 0 ? cq : x == 1 ? 7 - cq : x == 2 ? 8 + cq : 15 - cq;
             const int r = 16 * R + o;
-            float kr[CPL], br[CPL];
+            float2 kr[P2], br[P2];
 #pragma unroll
-            for (int m = 0; m < CPL; ++m) {
-                kr[m] = __bfloat162float(sK[r * XS + lane + 32 * m]);
-                br[m] = sB[r * D + lane + 32 * m];
+            for (int m = 0; m < P2; ++m) {
+                kr[m] = ld2(sK + r * XS + 2 * lane + 64 * m);
+                br[m] = b2at(r, 2 * lane + 64 * m);
             }
             for (int i = 16 * R; i < r; ++i) {
                 float a = 0.0f;
 #pragma unroll
-                for (int m = 0; m < CPL; ++m) {
-                    const int c = lane + 32 * m;
-                    a = fmaf(kr[m] * __bfloat162float(sK[i * XS + c]), exp2f(br[m] - sB[i * D + c]), a);
+                for (int m = 0; m < P2; ++m) {
+                    const int c = 2 * lane + 64 * m;
+                    const float2 ki = ld2(sK + i * XS + c), bi = b2at(i, c);
+                    a = fmaf(kr[m].x * ki.x, ex2(br[m].x - bi.x), a);
+                    a = fmaf(kr[m].y * ki.y, ex2(br[m].y - bi.y), a);
                 }
                 a = warp_sum(a);
                 if (lane == 0) {
@@ -360,9 +414,9 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                 st2(sDU + r * XS + c + 2, a.z, a.w);
                 const float be = sBeta[r];
                 const float2 k0 = ld2(sK + r * XS + c), k1 = ld2(sK + r * XS + c + 2);
-                const float *b = sB + r * D + c;
-                st2(sBK + r * XS + c, be * k0.x * exp2f(b[0]), be * k0.y * exp2f(b[1]));
-                st2(sBK + r * XS + c + 2, be * k1.x * exp2f(b[2]), be * k1.y * exp2f(b[3]));
+                const float4 b = *reinterpret_cast<const float4 *>(sB + r * FS + c);
+                st2(sBK + r * XS + c, be * k0.x * ex2(b.x), be * k0.y * ex2(b.y));
+                st2(sBK + r * XS + c + 2, be * k1.x * ex2(b.z), be * k1.y * ex2(b.w));
             }
             for (int e = tid; e < 64 * D / 8; e += kNT) {
                 const int r = e / (D / 8), c = 8 * (e % (D / 8));
@@ -441,9 +495,10 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
 #pragma unroll
             for (int j = 0; j < NT; ++j)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int r = r0 + 8 * (e >> 1), c = n0 + 8 * j + 2 * t + (e & 1);
-                    aQ[j][e] = p.scale * exp2f(sB[r * D + c]) * d[j][e];
+                for (int hr = 0; hr < 2; ++hr) {
+                    const float2 b = b2at(r0 + 8 * hr, n0 + 8 * j + 2 * t);
+                    aQ[j][2 * hr] = p.scale * ex2(b.x) * d[j][2 * hr];
+                    aQ[j][2 * hr + 1] = p.scale * ex2(b.y) * d[j][2 * hr + 1];
                 }
             // dBk = -du_T S^T: dK+ gets beta e^b dBk; dbeta += dBk . (K e^b)
             zero(d);
@@ -452,13 +507,16 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
 #pragma unroll
             for (int j = 0; j < NT; ++j)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int r = r0 + 8 * (e >> 1), c = n0 + 8 * j + 2 * t + (e & 1);
-                    const float kp = __bfloat162float(sK[r * XS + c]) * exp2f(sB[r * D + c]);
-                    const float dbk = -d[j][e];
-                    aKp[j][e] = sBeta[r] * exp2f(sB[r * D + c]) * dbk;
-                    if (e >> 1) s1 += dbk * kp;
-                    else s0 += dbk * kp;
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int r = r0 + 8 * hr, c = n0 + 8 * j + 2 * t;
+                    const float2 b = b2at(r, c), kv = ld2(sK + r * XS + c);
+                    const float e0 = ex2(b.x), e1 = ex2(b.y);
+                    const float dbk0 = -d[j][2 * hr], dbk1 = -d[j][2 * hr + 1];
+                    aKp[j][2 * hr] = sBeta[r] * e0 * dbk0;
+                    aKp[j][2 * hr + 1] = sBeta[r] * e1 * dbk1;
+                    const float sum = dbk0 * kv.x * e0 + dbk1 * kv.y * e1;
+                    if (hr) s1 += sum;
+                    else s0 += sum;
                 }
             add_dbeta(s0, s1);
         }
@@ -503,18 +561,18 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                 st2(sGP + r0 * LS + i, i <= r0 ? s * e2[j][0] : 0.0f, i + 1 <= r0 ? s * e2[j][1] : 0.0f);
                 st2(sGP + r1 * LS + i, i <= r1 ? s * e2[j][2] : 0.0f, i + 1 <= r1 ? s * e2[j][3] : 0.0f);
             }
-            // dS' (one row per warp at a time) and d e^{b_L}_c = sum_j dS'_cj S_cj
-            for (int c = w; c < D; c += kNT / 32) {
-                float acc = 0.0f;
+            // dS' in, and d e^{b_L}_c = sum_j dS'_cj S_cj: row c is D/4 float4
+            // units on D/4 consecutive lanes
+            for (int u = tid; u < D * D / 4; u += kNT) {
+                const int c = u / (D / 4), j = 4 * (u % (D / 4));
+                const float4 ds = *reinterpret_cast<const float4 *>(gDS + c * D + j);
+                const float4 sv = *reinterpret_cast<const float4 *>(gS + c * D + j);
+                float acc = ds.x * sv.x + ds.y * sv.y + ds.z * sv.z + ds.w * sv.w;
 #pragma unroll
-                for (int m = 0; m < CPL; ++m) {
-                    const int j = lane + 32 * m;
-                    const float ds = gDS[c * D + j];
-                    acc = fmaf(ds, gS[c * D + j], acc);
-                    sS[c * XS + j] = __float2bfloat16_rn(ds);
-                }
-                acc = warp_sum(acc);
-                if (lane == 0) sDGL[c] = acc;
+                for (int o = D / 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                if (u % (D / 4) == 0) sDGL[c] = acc;
+                st2(sS + c * XS + j, ds.x, ds.y);
+                st2(sS + c * XS + j + 2, ds.z, ds.w);
             }
         }
         __syncthreads();
@@ -524,21 +582,26 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
             zero(d);
             mma_rows<NT, false, true>(d, sU, XS, sS, XS, 16 * R, n0, 0, D);
 #pragma unroll
-            for (int j = 0; j < NT; ++j)
+            for (int j = 0; j < NT; ++j) {
+                const int c = n0 + 8 * j + 2 * t;
+                const float2 bl = b2at(63, c), b0 = b2at(r0, c), b1 = b2at(r1, c);
+                const float2 k0 = ld2(sK + r0 * XS + c), k1 = ld2(sK + r1 * XS + c);
+                aKm[j][0] = ex2(bl.x - b0.x) * d[j][0];
+                aKm[j][1] = ex2(bl.y - b0.y) * d[j][1];
+                aKm[j][2] = ex2(bl.x - b1.x) * d[j][2];
+                aKm[j][3] = ex2(bl.y - b1.y) * d[j][3];
+                float sx = k0.x * aKm[j][0] + k1.x * aKm[j][2];
+                float sy = k0.y * aKm[j][1] + k1.y * aKm[j][3];
 #pragma unroll
-                for (int e1 = 0; e1 < 2; ++e1) {
-                    const int c = n0 + 8 * j + 2 * t + e1;
-                    const float bl = sB[63 * D + c];
-                    const float el0 = exp2f(bl - sB[r0 * D + c]), el1 = exp2f(bl - sB[r1 * D + c]);
-                    aKm[j][e1] = el0 * d[j][e1];
-                    aKm[j][2 + e1] = el1 * d[j][2 + e1];
-                    float s = __bfloat162float(sK[r0 * XS + c]) * aKm[j][e1] +
-                              __bfloat162float(sK[r1 * XS + c]) * aKm[j][2 + e1];
-                    s += __shfl_xor_sync(0xffffffffu, s, 4);
-                    s += __shfl_xor_sync(0xffffffffu, s, 8);
-                    s += __shfl_xor_sync(0xffffffffu, s, 16);
-                    if (g == 0) atomicAdd(&sDBL[c], s);
+                for (int o = 4; o < 32; o <<= 1) {
+                    sx += __shfl_xor_sync(0xffffffffu, sx, o);
+                    sy += __shfl_xor_sync(0xffffffffu, sy, o);
                 }
+                if (g == 0) {
+                    atomicAdd(&sDBL[c], sx);
+                    atomicAdd(&sDBL[c + 1], sy);
+                }
+            }
         }
         __syncthreads();
 
@@ -591,17 +654,16 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         for (int e = tid; e < 64 * D / 2; e += kNT) {
             const int r = e / (D / 2), c = 2 * (e % (D / 2)), Rb = r >> 4;
             const float2 kv = ld2(sK + r * XS + c), qv = ld2(sQ + r * XS + c);
-            const float b0 = sB[r * D + c], b1 = sB[r * D + c + 1];
-            const float e0 = sB[(16 * Rb + 15) * D + c], e1 = sB[(16 * Rb + 15) * D + c + 1];
-            const float f0 = exp2f(b0 - bs(Rb, c)), f1 = exp2f(b1 - bs(Rb, c + 1));
-            st2(sKe + r * XS + c, kv.x * exp2f(e0 - b0), kv.y * exp2f(e1 - b1));
+            const float2 b = b2at(r, c), be = b2at(16 * Rb + 15, c);
+            const float f0 = ex2(b.x - bs(Rb, c)), f1 = ex2(b.y - bs(Rb, c + 1));
+            st2(sKe + r * XS + c, kv.x * ex2(be.x - b.x), kv.y * ex2(be.y - b.y));
             st2(sQs + r * XS + c, qv.x * f0, qv.y * f1);
             st2(sKs2 + r * XS + c, kv.x * f0, kv.y * f1);
         }
         for (int e = tid; e < 6 * D; e += kNT) {
             const int pi = e / D, c = e % D;
             const int Rb = pi < 1 ? 1 : pi < 3 ? 2 : 3, Ib = pi - Rb * (Rb - 1) / 2;
-            sMF[pi * D + c] = exp2f(bs(Rb, c) - sB[(16 * Ib + 15) * D + c]);
+            sMF[pi * D + c] = ex2(bs(Rb, c) - sB[(16 * Ib + 15) * FS + c]);
         }
         __syncthreads();
         auto mf = [&](int Rb, int Ib, int c) { return sMF[(Rb * (Rb - 1) / 2 + Ib) * D + c]; };
@@ -641,17 +703,21 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                         }
                 }
 #pragma unroll
-                for (int jj = 0; jj < 2; ++jj)
+                for (int jj = 0; jj < 2; ++jj) {
+                    const int c = nb + 8 * jj + 2 * t;
+                    const float2 bsr = R == 0 ? make_float2(0.0f, 0.0f) : b2at(16 * R - 1, c);
+                    const float2 ber = b2at(16 * R + 15, c);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int r = r0 + 8 * (e >> 1), c = nb + 8 * jj + 2 * t + (e & 1);
-                        const float b = sB[r * D + c];
-                        const float fr = exp2f(b - bs(R, c));
-                        const float fc = exp2f(sB[(16 * R + 15) * D + c] - b);
+                        const float2 b = b2at(r0 + 8 * (e >> 1), c);
+                        const float bb = (e & 1) ? b.y : b.x;
+                        const float fr = ex2(bb - ((e & 1) ? bsr.y : bsr.x));
+                        const float fc = ex2(((e & 1) ? ber.y : ber.x) - bb);
                         aQ[j + jj][e] = fmaf(fr, sq[jj][e], aQ[j + jj][e]);
                         aKp[j + jj][e] = fmaf(fr, sa[jj][e], aKp[j + jj][e]);
                         aKm[j + jj][e] = fmaf(fc, sm2[jj][e], aKm[j + jj][e]);
                     }
+                }
             }
         }
         {
@@ -666,7 +732,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                 float br[2 * NT];
 #pragma unroll
                 for (int j = 0; j < NT; ++j) {
-                    const float2 b2 = *reinterpret_cast<const float2 *>(sB + r * D + n0 + 8 * j + 2 * t);
+                    const float2 b2 = b2at(r, n0 + 8 * j + 2 * t);
                     br[2 * j] = b2.x;
                     br[2 * j + 1] = b2.y;
                 }
@@ -677,9 +743,9 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                     for (int j = 0; j < NT; ++j) {
                         const int c = n0 + 8 * j + 2 * t;
                         const float2 kv = ld2(sK + i * XS + c);
-                        const float2 bi = *reinterpret_cast<const float2 *>(sB + i * D + c);
-                        const float w0 = kv.x * exp2f(br[2 * j] - bi.x);
-                        const float w1 = kv.y * exp2f(br[2 * j + 1] - bi.y);
+                        const float2 bi = b2at(i, c);
+                        const float w0 = kv.x * ex2(br[2 * j] - bi.x);
+                        const float w1 = kv.y * ex2(br[2 * j + 1] - bi.y);
                         aQ[j][2 * hr] = fmaf(gp, w0, aQ[j][2 * hr]);
                         aQ[j][2 * hr + 1] = fmaf(gp, w1, aQ[j][2 * hr + 1]);
                         aKp[j][2 * hr] = fmaf(ga, w0, aKp[j][2 * hr]);
@@ -693,8 +759,8 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                     for (int j = 0; j < NT; ++j) {
                         const int c = n0 + 8 * j + 2 * t;
                         const float2 qv = ld2(sQ + rr * XS + c), kv = ld2(sK + rr * XS + c);
-                        const float2 b2 = *reinterpret_cast<const float2 *>(sB + rr * D + c);
-                        const float w0 = exp2f(b2.x - br[2 * j]), w1 = exp2f(b2.y - br[2 * j + 1]);
+                        const float2 b2 = b2at(rr, c);
+                        const float w0 = ex2(b2.x - br[2 * j]), w1 = ex2(b2.y - br[2 * j + 1]);
                         aKm[j][2 * hr] = fmaf(fmaf(gp, qv.x, ga * kv.x), w0, aKm[j][2 * hr]);
                         aKm[j][2 * hr + 1] = fmaf(fmaf(gp, qv.y, ga * kv.y), w1, aKm[j][2 * hr + 1]);
                     }
@@ -709,17 +775,20 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
 #pragma unroll
         for (int j = 0; j < NT; ++j)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = r0 + 8 * (e >> 1), c = n0 + 8 * j + 2 * t + (e & 1);
-                const float dq = aQ[j][e], dkp = aKp[j][e], dkm = aKm[j][e];
-                sFQ[r * FS + c] = dq;
-                sFK[r * FS + c] = dkp + dkm;
-                sDB[r * D + c] = __bfloat162float(sQ[r * XS + c]) * dq +
-                                 __bfloat162float(sK[r * XS + c]) * (dkp - dkm);
+            for (int hr = 0; hr < 2; ++hr) {
+                const int r = r0 + 8 * hr, c = n0 + 8 * j + 2 * t;
+                const float2 qv = ld2(sQ + r * XS + c), kv = ld2(sK + r * XS + c);
+                const float dq0 = aQ[j][2 * hr], dq1 = aQ[j][2 * hr + 1];
+                const float p0 = aKp[j][2 * hr], p1 = aKp[j][2 * hr + 1];
+                const float m0 = aKm[j][2 * hr], m1 = aKm[j][2 * hr + 1];
+                *reinterpret_cast<float2 *>(sFQ + r * FS + c) = make_float2(dq0, dq1);
+                *reinterpret_cast<float2 *>(sFK + r * FS + c) = make_float2(p0 + m0, p1 + m1);
+                *reinterpret_cast<float2 *>(sDB + r * FS + c) =
+                    make_float2(qv.x * dq0 + kv.x * (p0 - m0), qv.y * dq1 + kv.y * (p1 - m1));
             }
         __syncthreads();
         if (tid < D && p.gate_logits)
-            sDB[63 * D + tid] += sDBL[tid] + exp2f(sB[63 * D + tid]) * sDGL[tid];
+            sDB[63 * FS + tid] += sDBL[tid] + ex2(sB[63 * FS + tid]) * sDGL[tid];
 #pragma unroll 1
         for (int rr = 0; rr < 4; ++rr) {
             const int r = w + 16 * rr;
@@ -730,14 +799,17 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                 const float *src = (which ? sFK : sFQ) + r * FS;
                 float x[CPL], d[CPL];
 #pragma unroll
-                for (int m = 0; m < CPL; ++m) {
-                    x[m] = __bfloat162float(raw[lane + 32 * m]);
-                    d[m] = src[lane + 32 * m];
+                for (int m = 0; m < P2; ++m) {
+                    const int c = 2 * lane + 64 * m;
+                    const float2 xv = ld2(raw + c), dv = *reinterpret_cast<const float2 *>(src + c);
+                    x[2 * m] = xv.x; x[2 * m + 1] = xv.y;
+                    d[2 * m] = dv.x; d[2 * m + 1] = dv.y;
                 }
                 prep_backward<CPL>(x, d, silu, (p.flags & (which ? kL2NormK : kL2NormQ)) != 0);
                 float *out = (which ? p.dk : p.dq) + tok(r) * D;
 #pragma unroll
-                for (int m = 0; m < CPL; ++m) out[lane + 32 * m] = d[m];
+                for (int m = 0; m < P2; ++m)
+                    *reinterpret_cast<float2 *>(out + 2 * lane + 64 * m) = make_float2(d[2 * m], d[2 * m + 1]);
             }
         }
         if (tid < len) {
@@ -746,19 +818,25 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         }
         if (p.gate_logits) {
             __syncthreads();
-            column_scan<D>(sDB, sSeg, true);   // d log alpha_t = sum_{r >= t} db_r
+            column_scan<D, FS>(sDB, sSeg, true);   // d log alpha_t = sum_{r >= t} db_r
             // log alpha = -softplus(x): dx = -d(log alpha) sigmoid(x)
             if (!scalar_gate) {
-                for (int e = tid; e < len * D; e += kNT) {
-                    const int r = e / D, c = e % D;
+                for (int e = tid; e < len * D / 2; e += kNT) {
+                    const int r = e / (D / 2), c = 2 * (e % (D / 2));
                     const int64_t o = tok(r) * D + c;
-                    p.d_gate_logits[o] = -sDB[r * D + c] * sigmoid_f(__bfloat162float(p.gate_logits[o]));
+                    const float2 gg = ld2(p.gate_logits + o);
+                    const float2 dl = *reinterpret_cast<const float2 *>(sDB + r * FS + c);
+                    *reinterpret_cast<float2 *>(p.d_gate_logits + o) =
+                        make_float2(-dl.x * sigmoid_f(gg.x), -dl.y * sigmoid_f(gg.y));
                 }
             } else {
                 for (int r = w; r < len; r += kNT / 32) {
                     float s = 0.0f;
 #pragma unroll
-                    for (int m = 0; m < CPL; ++m) s += sDB[r * D + lane + 32 * m];
+                    for (int m = 0; m < P2; ++m) {
+                        const float2 dl = *reinterpret_cast<const float2 *>(sDB + r * FS + 2 * lane + 64 * m);
+                        s += dl.x + dl.y;
+                    }
                     s = warp_sum(s);
                     if (lane == 0)
                         p.d_gate_logits[tok(r)] = -s * sigmoid_f(__bfloat162float(p.gate_logits[tok(r)]));
