@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(ChainCfg<D>::NT, 1) delta_bwd_chain_kernel(Cha
             float du[NT_DU][4];
             wmma16::zero(du);
             wmma16::mma_rows<NT_DU, true, false>(du, aq, dO, 16 * Ru, nu, 16 * Ru, 64);
-            wmma16::mma_rows<NT_DU, false, false>(du, kt, dSp, 16 * Ru, nu, 0, D);
+            wmma16::mma_rows_c<0, D, NT_DU, false, false>(du, kt, dSp, 16 * Ru, nu);
             float *gdu = p.du ? p.du + ((slot0 + c) * H + h) * (int64_t)(64 * D) : nullptr;
 #pragma unroll
             for (int j = 0; j < NT_DU; ++j)
@@ -328,8 +328,8 @@ __global__ void __launch_bounds__(ChainCfg<D>::NT, 1) delta_bwd_chain_kernel(Cha
                 ds[j][0] *= g0; ds[j][1] *= g0;
                 ds[j][2] *= g1; ds[j][3] *= g1;
             }
-            wmma16::mma_rows<NT_DS, true, false>(ds, qe, dO, 16 * Rs, ns, 0, 64);
-            wmma16::mma_rows<NT_DS, true, false>(ds, wq, dU, 16 * Rs, ns, 0, 64);
+            wmma16::mma_rows_c<0, 64, NT_DS, true, false>(ds, qe, dO, 16 * Rs, ns);
+            wmma16::mma_rows_c<0, 64, NT_DS, true, false>(ds, wq, dU, 16 * Rs, ns);
         }
     }
     // a copy still in flight (only after a failed wait): let it land first

@@ -35,9 +35,11 @@ __device__ __forceinline__ void ldsm_t(uint32_t (&r)[4], const bf16 *p) {
                  : "r"(saddr(p)));
 }
 
+// A pure function of its registers (not volatile), so the compiler may issue
+// the next step's fragment loads ahead of it.
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
         "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -60,36 +62,68 @@ struct RsView {
     }
 };
 
+// Fragments of one 16-deep step (m16n8k16): A for rows m0 .. m0+15, B for
+// columns n0 .. n0+15 (two n8 tiles).  op(A) = A (stored [m][k], TA = false)
+// or A^T (stored [k][m]); op(B) = B (stored [k][n], TB = false) or B^T
+// (stored [n][k]).  m0, n0 multiples of 8, k of 16.
+template <bool TA, class VA>
+__device__ __forceinline__ void frag_a(uint32_t (&a)[4], const VA &A, int m0, int k) {
+    const int lane = threadIdx.x & 31, li = lane & 7, lj = lane >> 3;
+    if constexpr (!TA) ldsm(a, A.at(m0 + (lane & 15), k + (lane >> 4) * 8));
+    else ldsm_t(a, A.at(k + li + 8 * (lj >> 1), m0 + 8 * (lj & 1)));
+}
+
+template <bool TB, class VB>
+__device__ __forceinline__ void frag_b(uint32_t (&b)[4], const VB &B, int n0, int k) {
+    const int lane = threadIdx.x & 31, li = lane & 7, lj = lane >> 3;
+    if constexpr (TB) ldsm(b, B.at(n0 + li + 8 * (lj >> 1), k + 8 * (lj & 1)));
+    else ldsm_t(b, B.at(k + li + 8 * (lj & 1), n0 + 8 * (lj >> 1)));
+}
+
 // One 16-deep step of a warp's 16 x 16 output block (two n8 tiles):
 //   d += op(A)[m0 .. m0+15][k .. k+15] op(B)[k .. k+15][n0 .. n0+15]
-// op(A) = A (stored [m][k], TA = false) or A^T (stored [k][m]); op(B) = B
-// (stored [k][n], TB = false) or B^T (stored [n][k]).  m0, n0 multiples of
-// 8, k of 16.  Accumulator element e of tile j sits at row m0 + g + 8 (e/2),
-// column n0 + 8j + 2t + e%2 (g = lane / 4, t = lane % 4).
+// Accumulator element e of tile j sits at row m0 + g + 8 (e/2), column
+// n0 + 8j + 2t + e%2 (g = lane / 4, t = lane % 4).
 template <bool TA, bool TB, class VA, class VB>
 __device__ __forceinline__ void mma_step(float (&d)[2][4], const VA &A, const VB &B, int m0,
                                          int n0, int k) {
-    const int lane = threadIdx.x & 31, li = lane & 7, lj = lane >> 3;
     uint32_t a[4], b[4];
-    if constexpr (!TA) ldsm(a, A.at(m0 + (lane & 15), k + (lane >> 4) * 8));
-    else ldsm_t(a, A.at(k + li + 8 * (lj >> 1), m0 + 8 * (lj & 1)));
-    if constexpr (TB) ldsm(b, B.at(n0 + li + 8 * (lj >> 1), k + 8 * (lj & 1)));
-    else ldsm_t(b, B.at(k + li + 8 * (lj & 1), n0 + 8 * (lj >> 1)));
+    frag_a<TA>(a, A, m0, k);
+    frag_b<TB>(b, B, n0, k);
     mma16816(d[0], a, b[0], b[1]);
     mma16816(d[1], a, b[2], b[3]);
+}
+
+// One 16-deep step of NT n8 tiles from column n0 (NT even): the A fragment
+// is loaded once for all of them.
+template <int NT, bool TA, bool TB, class VA, class VB>
+__device__ __forceinline__ void mma_kstep(float (&d)[NT][4], const VA &A, const VB &B, int m0,
+                                          int n0, int k) {
+    uint32_t a[4];
+    frag_a<TA>(a, A, m0, k);
+#pragma unroll
+    for (int j = 0; j < NT; j += 2) {
+        uint32_t b[4];
+        frag_b<TB>(b, B, n0 + 8 * j, k);
+        mma16816(d[j], a, b[0], b[1]);
+        mma16816(d[j + 1], a, b[2], b[3]);
+    }
 }
 
 // d (NT n8 tiles from column n0, NT even) += op(A) op(B) over k in [k0, k1).
 template <int NT, bool TA, bool TB, class VA, class VB>
 __device__ __forceinline__ void mma_rows(float (&d)[NT][4], const VA &A, const VB &B, int m0,
                                          int n0, int k0, int k1) {
-    for (int k = k0; k < k1; k += 16) {
+#pragma unroll 2
+    for (int k = k0; k < k1; k += 16) mma_kstep<NT, TA, TB>(d, A, B, m0, n0, k);
+}
+
+// The same over a compile-time range [K0, K1), fully unrolled.
+template <int K0, int K1, int NT, bool TA, bool TB, class VA, class VB>
+__device__ __forceinline__ void mma_rows_c(float (&d)[NT][4], const VA &A, const VB &B, int m0,
+                                           int n0) {
 #pragma unroll
-        for (int j = 0; j < NT; j += 2) {
-            float(&dp)[2][4] = *reinterpret_cast<float(*)[2][4]>(&d[j]);
-            mma_step<TA, TB>(dp, A, B, m0, n0 + 8 * j, k);
-        }
-    }
+    for (int k = K0; k < K1; k += 16) mma_kstep<NT, TA, TB>(d, A, B, m0, n0, k);
 }
 
 template <int NT>
