@@ -1,7 +1,7 @@
-// delta_bwd_channel.cu -- per-chunk gradients of the chunkwise delta rule with
-// a decay per key channel (the KDA form of "From GPT-2 to Kimi K3, explained",
-// section KDA / Kimi Linear; a scalar gate or none are its special cases),
-// d = dk = dv in {64, 128}, bf16 I/O.
+// delta_bwd_channel.cu -- per-chunk gradients of the chunkwise delta rule,
+// d = dk = dv in {64, 128}, bf16 I/O, with a decay per key channel (the KDA
+// form of "From GPT-2 to Kimi K3, explained", section KDA / Kimi Linear), one
+// per token, or none.
 //
 // Forward of one chunk (section DeltaNet (Parallelizing Linear Transformers
 // with Delta Rule), eq. 8-10, with the decay folded in), b_r in R^dk the
@@ -11,11 +11,15 @@
 //   Bk = diag(beta) (K o e^b),  Bv = diag(beta) V,  u~ = Bv - Bk S,  u = T u~
 //   O = scale ((Q o e^b) S + (Q * K) u),  S' = Diag(e^{b_L}) S + (K o e^{b_L-b})^T u
 // Given dO' = scale dO, dS' (the next chunk state's gradient) and du =
-// (Q * K)^T dO' + (K o e^{b_L - b}) dS' (both from the reverse chain):
-//   du_T = T^T du,  dV = diag(beta) du_T,  dT = du u~^T,  dA = -T^T dT T^T
-//   dBk = -du_T S^T,  dP = tril(dO' u^T),  d(Q o e^b) = dO' S^T
-//   d(K o e^{b_L - b}) = u dS'^T,  d e^{b_L} = rowsum(dS' o S)
-// and through the decayed scores, with G the gradient of X * Y:
+// (Q * K)^T dO' + (K o e^{b_L - b}) dS' (both from the reverse chain), and T
+// from the forward pass:
+//   du_T = T^T du,  dV = diag(beta) du_T,  dBk = -du_T S^T,  d(Q o e^b) = dO' S^T
+//   dA = -T^T dT T^T with dT = du u~^T, i.e. dA = -strict_tril(du_T u^T)
+//   dP = tril(dO' u^T),  d(K o e^{b_L - b}) = u dS'^T,  d e^{b_L} = rowsum(dS' o S)
+//   dbeta_r = du_T,r . v_r + dBk_r . (K e^b)_r + sum_i dA_ri (K * K)_ri, whose
+//   last term is -(1/beta_r) du_T,r . (A u)_r with A u = u~ - u
+//   (since (I + A) u = u~): K * K itself is never formed.
+// Through the decayed scores, with G the gradient of X * Y:
 //   dX_rc += sum_{i<=r} G_ri y_ic e^{b_rc - b_ic},   db_rc += x_rc dX_rc
 //   dY_ic += sum_{r>=i} G_ri x_rc e^{b_rc - b_ic},   db_ic -= y_ic dY_ic
 // (G = dP for Q * K; G = diag(beta) dA for K * K).  Every term that moves
@@ -41,7 +45,8 @@
 // operands with fp32 accumulation; the three gradient accumulators dQ, dK+
 // and dK- stay in registers from the first product that feeds them to the
 // end of the task (warp w owns rows 16 (w / 4) .. +15 and a quarter of the
-// columns).  The triangular solve runs in fp32.
+// columns).  The quantities that cancel in the beta gradient (du_T . u~ and
+// du_T . u) are summed in fp32 from fp32 accumulators.
 
 #include "common.cuh"
 #include "delta_tc.h"
@@ -93,8 +98,8 @@ __device__ __forceinline__ void prefetch_l2(const void *p) {
 // ------------------------------------------------------------ layout
 
 // Shared memory (bytes).  Persistent through a task: q^, k^ (bf16), b in
-// log2 units (fp32), K * K and T (bf16), row and channel vectors.  One union
-// region holds each phase's working tiles (offsets in the kernel's comments).
+// log2 units (fp32), T (bf16, the forward pass's swizzled tile), row and
+// channel vectors.  One union region holds each phase's working tiles.
 template <int D>
 struct Lay {
     static constexpr int XS = D + 8;            // bf16 stride of a 64 x D tile
@@ -102,27 +107,25 @@ struct Lay {
     static constexpr int SB = D * XS * 2;       // D x D bf16 (S or dS')
     static constexpr int LS = 72;               // bf16 stride of a 64 x 64 tile
     static constexpr int LB = 64 * LS * 2;
-    static constexpr int TS = 68;               // fp32 stride of T during the solve
     // fp32 stride of the decay table b and of the 64 x D gradients: D + 8
     // words puts the rows of a quad's float2 accesses on distinct banks
     static constexpr int FS = D + 8;
-    static constexpr int Q = 0, K = Q + XB, B = K + XB, KK = B + 64 * FS * 4, TB = KK + LB;
-    static constexpr int BETA = TB + LB;                 // fp32 [64]
+    static constexpr int TR = 0, Q = TR + 8192, K = Q + XB, B = K + XB;
+    static constexpr int BETA = B + 64 * FS * 4;         // fp32 [64]
     static constexpr int DBETA = BETA + 256;             // fp32 [64]
     static constexpr int DBL = DBETA + 256;              // fp32 [D]: d b_L
     static constexpr int DGL = DBL + 4 * D;              // fp32 [D]: d e^{b_L}
     static constexpr int MF = DGL + 4 * D;               // fp32 [6][D]: middle factors
     static constexpr int SEG = MF + 24 * D;              // fp32 [kNT / D][D]: scan totals
-    static constexpr int U = SEG + 4 * kNT;
+    static constexpr int ROW = SEG + 4 * kNT;            // fp32 [2][64]: du_T . u~, du_T . u
+    static constexpr int U = ROW + 512;
     // union region, phases 2-3 (the largest)
     static constexpr int O_DO = 0, O_DU = XB, O_DUT = 2 * XB, O_UT = 3 * XB, O_BK = 4 * XB;
     static constexpr int O_S = 5 * XB, U_BYTES = 5 * XB + SB;
     static constexpr int BYTES = U + U_BYTES;
-    // phase 1 (K_s, the per-block copies Y_R and T in fp32) and phase 6 (dQ,
-    // dK and db in fp32) fit inside the union region
-    static_assert(XB + 96 * XS * 2 + 64 * TS * 4 <= U_BYTES, "phase 1");
+    // phase 6 (dQ, dK and db in fp32) fits inside the union region
     static_assert(3 * 64 * FS * 4 <= U_BYTES, "phase 6");
-    static_assert(LB <= XB, "dP and dT fit in a 64 x D slot");
+    static_assert(LB <= XB, "dP and G_A fit in a 64 x D slot");
 };
 static_assert(Lay<128>::BYTES <= 232448, "shared memory at d = 128");
 
@@ -132,6 +135,7 @@ struct Params {
     const float *states;      // [slots][H][D][D] S at each chunk start
     const float *dstates;     // [slots][H][D][D] dS' of each chunk
     const float *du;          // [slots][H][64][D] du of each chunk
+    const uint8_t *tiles;     // [slots][H] T of each chunk (8 KB bf16 swizzled tiles)
     float *dq, *dk, *dv, *d_beta_logits, *d_gate_logits;
     int64_t n_tasks;
     int H;
@@ -164,71 +168,21 @@ __device__ __forceinline__ void column_scan(float *x, float *seg, bool reverse) 
     __syncthreads();
 }
 
-// T = (I + A)^{-1} in place (fp32, row stride TS, A strictly lower): the four
-// 16 x 16 diagonal blocks by column-wise forward substitution, then block
-// rows 1..3 as T_ij = -T_ii sum_{j <= l < i} A_il T_lj.  X: 768 floats.
-template <int TS>
-__device__ __forceinline__ void solve_unit_lower(float *sT, float *X) {
-    const int tid = threadIdx.x;
-    {
-        float t[16];
-        const int R = tid >> 4, j = tid & 15;
-        if (tid < 64) {
-            const float *Ab = sT + (16 * R) * TS + 16 * R;
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                float a = (r == j) ? 1.0f : 0.0f;
-#pragma unroll
-                for (int k = 0; k < r; ++k) a = fmaf(-Ab[r * TS + k], t[k], a);
-                t[r] = a;
-            }
-        }
-        __syncthreads();
-        if (tid < 64) {
-#pragma unroll
-            for (int r = 0; r < 16; ++r) sT[(16 * R + r) * TS + 16 * R + j] = t[r];
-        }
-        __syncthreads();
-    }
-#pragma unroll 1
-    for (int bi = 1; bi < 4; ++bi) {
-        for (int e = tid; e < bi * 256; e += kNT) {
-            const int bj = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-            float acc = 0.0f;
-            for (int l = bj; l < bi; ++l)
-#pragma unroll
-                for (int k = 0; k < 16; ++k)
-                    acc = fmaf(sT[(16 * bi + rr) * TS + 16 * l + k], sT[(16 * l + k) * TS + 16 * bj + cc], acc);
-            X[e] = acc;
-        }
-        __syncthreads();
-        for (int e = tid; e < bi * 256; e += kNT) {
-            const int bj = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-            float acc = 0.0f;
-#pragma unroll
-            for (int k = 0; k < 16; ++k)
-                acc = fmaf(sT[(16 * bi + rr) * TS + 16 * bi + k], X[(bj << 8) + k * 16 + cc], acc);
-            sT[(16 * bi + rr) * TS + 16 * bj + cc] = -acc;
-        }
-        __syncthreads();
-    }
-}
-
 template <int D>
 __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
     using L = Lay<D>;
-    constexpr int XS = L::XS, LS = L::LS, TS = L::TS, FS = L::FS;
+    constexpr int XS = L::XS, LS = L::LS, FS = L::FS;
     constexpr int CPL = D / 32;          // channels per lane in row-wise passes
     constexpr int P2 = D / 64;           // ... as pairs 2 lane + 64 m
     constexpr int NT = D / 32;           // n8 tiles of a warp's 16 x D/4 output block
-    extern __shared__ __align__(16) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem[];
     bf16 *sQ = reinterpret_cast<bf16 *>(smem + L::Q), *sK = reinterpret_cast<bf16 *>(smem + L::K);
     float *sB = reinterpret_cast<float *>(smem + L::B);
-    bf16 *sKK = reinterpret_cast<bf16 *>(smem + L::KK), *sTb = reinterpret_cast<bf16 *>(smem + L::TB);
     float *sBeta = reinterpret_cast<float *>(smem + L::BETA);
     float *sDBeta = reinterpret_cast<float *>(smem + L::DBETA);
     float *sDBL = reinterpret_cast<float *>(smem + L::DBL), *sDGL = reinterpret_cast<float *>(smem + L::DGL);
     float *sMF = reinterpret_cast<float *>(smem + L::MF), *sSeg = reinterpret_cast<float *>(smem + L::SEG);
+    float *sRow = reinterpret_cast<float *>(smem + L::ROW);
     uint8_t *U = smem + L::U;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
@@ -330,74 +284,12 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         auto bs = [&](int Rb, int c) { return Rb == 0 ? 0.0f : sB[(16 * Rb - 1) * FS + c]; };
         auto b2at = [&](int r, int c) { return *reinterpret_cast<const float2 *>(sB + r * FS + c); };
 
-        // ---- 1. decayed scores K * K, A = beta (K * K), T = (I + A)^{-1}
-        // union: K_s at 0 (rows scaled to their block's start), Y_R for
-        // R = 1..3 at XB (rows 0 .. 16R - 1 scaled from R's start back to
-        // them), T in fp32 after them
-        bf16 *sKs = reinterpret_cast<bf16 *>(U);
-        bf16 *sY = reinterpret_cast<bf16 *>(U + L::XB);
-        float *sT = reinterpret_cast<float *>(U + L::XB + 96 * XS * 2);
-        auto yrow = [](int Rb) { return 8 * Rb * (Rb - 1); };   // first row of Y_R in sY
-        for (int e = tid; e < 64 * D / 2; e += kNT) {
-            const int r = e / (D / 2), c = 2 * (e % (D / 2)), Rb = r >> 4;
-            const float2 kv = ld2(sK + r * XS + c), b = b2at(r, c);
-            st2(sKs + r * XS + c, kv.x * ex2(b.x - bs(Rb, c)), kv.y * ex2(b.y - bs(Rb, c + 1)));
-            // row r of Y_R for every later block R
-            for (int Rb2 = Rb + 1; Rb2 < 4; ++Rb2)
-                st2(sY + (yrow(Rb2) + r) * XS + c, kv.x * ex2(bs(Rb2, c) - b.x),
-                    kv.y * ex2(bs(Rb2, c + 1) - b.y));
-        }
-        for (int e = tid; e < 64 * 64; e += kNT) sT[(e >> 6) * TS + (e & 63)] = 0.0f;
-        __syncthreads();
-        // blocks below the diagonal: one warp per (R, I < R), K = D deep
-        if (cq < R) {
-            float d[2][4] = {};
-            for (int k = 0; k < D; k += 16)
-                mma_step<false, true>(d, sKs, XS, sY + yrow(R) * XS, XS, 16 * R, 16 * cq, k);
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int r = r0 + 8 * (e >> 1), i = 16 * cq + 8 * j + 2 * t + (e & 1);
-                    sT[r * TS + i] = sBeta[r] * d[j][e];
-                    sKK[r * LS + i] = __float2bfloat16_rn(d[j][e]);
-                }
-        }
-        // diagonal blocks exactly: warp w takes rows 16R + {qq, 7-qq, 8+qq, 15-qq}
-        // (30 (r, i) pairs for every warp), lanes split the channels
-#pragma unroll 1
-        for (int x = 0; x < 4; ++x) {
-            const int o = x == 0 ? cq : x == 1 ? 7 - cq : x == 2 ? 8 + cq : 15 - cq;
-            const int r = 16 * R + o;
-            float2 kr[P2], br[P2];
-#pragma unroll
-            for (int m = 0; m < P2; ++m) {
-                kr[m] = ld2(sK + r * XS + 2 * lane + 64 * m);
-                br[m] = b2at(r, 2 * lane + 64 * m);
-            }
-            for (int i = 16 * R; i < r; ++i) {
-                float a = 0.0f;
-#pragma unroll
-                for (int m = 0; m < P2; ++m) {
-                    const int c = 2 * lane + 64 * m;
-                    const float2 ki = ld2(sK + i * XS + c), bi = b2at(i, c);
-                    a = fmaf(kr[m].x * ki.x, ex2(br[m].x - bi.x), a);
-                    a = fmaf(kr[m].y * ki.y, ex2(br[m].y - bi.y), a);
-                }
-                a = warp_sum(a);
-                if (lane == 0) {
-                    sT[r * TS + i] = sBeta[r] * a;
-                    sKK[r * LS + i] = __float2bfloat16_rn(a);
-                }
-            }
-        }
-        __syncthreads();
-        solve_unit_lower<TS>(sT, reinterpret_cast<float *>(sY));
-        for (int e = tid; e < 64 * 64; e += kNT) {
-            const int r = e >> 6, i = e & 63;
-            sTb[r * LS + i] = __float2bfloat16_rn(i <= r ? sT[r * TS + i] : 0.0f);
-        }
-        __syncthreads();
+        // ---- 1. T = (I + A)^{-1} from the forward pass (bf16, one 64-row
+        // swizzled tile of 8 KB: one 16-byte unit per thread)
+        static_assert(kNT * 16 == 8192, "one unit of T per thread");
+        *reinterpret_cast<uint4 *>(smem + L::TR + tid * 16) =
+            *reinterpret_cast<const uint4 *>(p.tiles + (slot * H + h) * (int64_t)8192 + tid * 16);
+        const wmma16::RsView tv{smem + L::TR, 64, 0};
 
         // ---- 2. dO, du, S and Bk in; du_T = T^T du; u~, d(Q e^b), dBk
         bf16 *sDO = reinterpret_cast<bf16 *>(U + L::O_DO), *sDU = reinterpret_cast<bf16 *>(U + L::O_DU);
@@ -431,64 +323,72 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                 st2(sS + r * XS + c + 2, a.z, a.w);
             }
         }
+        if (tid < 64) sRow[tid] = sRow[64 + tid] = 0.0f;
         __syncthreads();
         float aQ[NT][4], aKp[NT][4], aKm[NT][4];   // dQ, dK+, dK- (see the file header)
         zero(aQ);
         zero(aKp);
         zero(aKm);
-        // dbeta partial sums of this lane's two rows, reduced over the quad and
-        // the four column warps of the row block
-        auto add_dbeta = [&](float s0, float s1) {
+        // per-row partial sums of this lane's two rows, reduced over the quad and
+        // the four column warps of the row block into v[r]
+        auto add_rows = [&](float *v, float s0, float s1) {
             s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
             s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
             s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
             s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
             if (t == 0) {
-                atomicAdd(&sDBeta[r0], s0);
-                atomicAdd(&sDBeta[r1], s1);
+                atomicAdd(&v[r0], s0);
+                atomicAdd(&v[r1], s1);
             }
         };
+        // du_T = T^T du, kept in fp32 until u is known (T lower: rows r >= 16R
+        // of T reach rows of block R)
+        float dut[NT][4];
+        zero(dut);
+        wmma16::mma_rows<NT, true, false>(dut, tv, PadView{sDU, XS}, 16 * R, n0, 16 * R, 64);
         {
-            // du_T = T^T du (T lower: rows r >= 16R of T reach rows of block R)
-            float d[NT][4];
-            zero(d);
-            mma_rows<NT, true, false>(d, sTb, LS, sDU, XS, 16 * R, n0, 16 * R, 64);
             float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
                 const int c = n0 + 8 * j + 2 * t;
-                st2(sDUT + r0 * XS + c, d[j][0], d[j][1]);
-                st2(sDUT + r1 * XS + c, d[j][2], d[j][3]);
+                st2(sDUT + r0 * XS + c, dut[j][0], dut[j][1]);
+                st2(sDUT + r1 * XS + c, dut[j][2], dut[j][3]);
                 // dV = beta du_T; dbeta += du_T . v
                 if (r0 < len) {
                     const float2 v = ld2(p.v + tok(r0) * D + c);
-                    s0 += d[j][0] * v.x + d[j][1] * v.y;
+                    s0 += dut[j][0] * v.x + dut[j][1] * v.y;
                     *reinterpret_cast<float2 *>(p.dv + tok(r0) * D + c) =
-                        make_float2(sBeta[r0] * d[j][0], sBeta[r0] * d[j][1]);
+                        make_float2(sBeta[r0] * dut[j][0], sBeta[r0] * dut[j][1]);
                 }
                 if (r1 < len) {
                     const float2 v = ld2(p.v + tok(r1) * D + c);
-                    s1 += d[j][2] * v.x + d[j][3] * v.y;
+                    s1 += dut[j][2] * v.x + dut[j][3] * v.y;
                     *reinterpret_cast<float2 *>(p.dv + tok(r1) * D + c) =
-                        make_float2(sBeta[r1] * d[j][2], sBeta[r1] * d[j][3]);
+                        make_float2(sBeta[r1] * dut[j][2], sBeta[r1] * dut[j][3]);
                 }
             }
-            add_dbeta(s0, s1);
+            add_rows(sDBeta, s0, s1);
         }
         __syncthreads();
         {
-            // u~ = beta V - Bk S
+            // u~ = beta V - Bk S; sRow[r] = sum_j du_T u~ (fp32)
             float d[NT][4];
             zero(d);
             mma_rows<NT, false, false>(d, sBK, XS, sS, XS, 16 * R, n0, 0, D);
+            float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
                 const int c = n0 + 8 * j + 2 * t;
                 const float2 v0 = r0 < len ? ld2(p.v + tok(r0) * D + c) : make_float2(0.f, 0.f);
                 const float2 v1 = r1 < len ? ld2(p.v + tok(r1) * D + c) : make_float2(0.f, 0.f);
-                st2(sUT + r0 * XS + c, sBeta[r0] * v0.x - d[j][0], sBeta[r0] * v0.y - d[j][1]);
-                st2(sUT + r1 * XS + c, sBeta[r1] * v1.x - d[j][2], sBeta[r1] * v1.y - d[j][3]);
+                const float u00 = sBeta[r0] * v0.x - d[j][0], u01 = sBeta[r0] * v0.y - d[j][1];
+                const float u10 = sBeta[r1] * v1.x - d[j][2], u11 = sBeta[r1] * v1.y - d[j][3];
+                st2(sUT + r0 * XS + c, u00, u01);
+                st2(sUT + r1 * XS + c, u10, u11);
+                s0 += dut[j][0] * u00 + dut[j][1] * u01;
+                s1 += dut[j][2] * u10 + dut[j][3] * u11;
             }
+            add_rows(sRow, s0, s1);
             // d(Q e^b) = scale dO S^T: dQ gets e^b times it
             zero(d);
             mma_rows<NT, false, true>(d, sDO, XS, sS, XS, 16 * R, n0, 0, D);
@@ -503,7 +403,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
             // dBk = -du_T S^T: dK+ gets beta e^b dBk; dbeta += dBk . (K e^b)
             zero(d);
             mma_rows<NT, false, true>(d, sDUT, XS, sS, XS, 16 * R, n0, 0, D);
-            float s0 = 0.0f, s1 = 0.0f;
+            s0 = s1 = 0.0f;
 #pragma unroll
             for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -518,48 +418,51 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                     if (hr) s1 += sum;
                     else s0 += sum;
                 }
-            add_dbeta(s0, s1);
+            add_rows(sDBeta, s0, s1);
         }
         __syncthreads();
 
-        // ---- 3. u = T u~, dT = du u~^T (strictly lower), dP = scale tril(dO u^T),
-        // then dS' in: d(K e^{b_L - b}) = u dS'^T, d e^{b_L} = rowsum(dS' o S)
+        // ---- 3. u = T u~; the A part of dbeta; dA = -strict_tril(du_T u^T)
+        // (so G_A = diag(beta) dA) and dP = scale tril(dO u^T); dS' in:
+        // d(K e^{b_L - b}) = u dS'^T, d e^{b_L} = rowsum(dS' o S)
         bf16 *sU = sBK;                                             // 64 x D
-        bf16 *sDT = sDUT;                                           // 64 x 64
-        bf16 *sGP = sDU;                                            // 64 x 64, written after dT
+        bf16 *sGP = sDU;                                            // 64 x 64
+        bf16 *sGA = sUT;                                            // 64 x 64, after u
         {
             float d[NT][4];
             zero(d);
-            mma_rows<NT, false, false>(d, sTb, LS, sUT, XS, 16 * R, n0, 0, 16 * R + 16);
+            wmma16::mma_rows<NT, false, false>(d, tv, PadView{sUT, XS}, 16 * R, n0, 0, 16 * R + 16);
+            float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
                 const int c = n0 + 8 * j + 2 * t;
                 st2(sU + r0 * XS + c, d[j][0], d[j][1]);
                 st2(sU + r1 * XS + c, d[j][2], d[j][3]);
+                s0 += dut[j][0] * d[j][0] + dut[j][1] * d[j][1];
+                s1 += dut[j][2] * d[j][2] + dut[j][3] * d[j][3];
             }
-            float e2[2][4] = {};
-            if (cq <= R)
-                for (int k = 0; k < D; k += 16)
-                    mma_step<false, true>(e2, sDU, XS, sUT, XS, 16 * R, 16 * cq, k);
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int i = 16 * cq + 8 * j + 2 * t;
-                st2(sDT + r0 * LS + i, i < r0 ? e2[j][0] : 0.0f, i + 1 < r0 ? e2[j][1] : 0.0f);
-                st2(sDT + r1 * LS + i, i < r1 ? e2[j][2] : 0.0f, i + 1 < r1 ? e2[j][3] : 0.0f);
-            }
+            add_rows(sRow + 64, s0, s1);
         }
         __syncthreads();
+        // dbeta_r += sum_i dA_ri (K * K)_ri = -(1/beta_r) sum_j du_T_rj (A u)_rj,
+        // and A u = u~ - u because (I + A) u = u~
+        // (a beta that underflowed to 0 leaves the row's beta-logit gradient 0 anyway)
+        if (tid < len && sBeta[tid] > 0.0f) sDBeta[tid] -= (sRow[tid] - sRow[64 + tid]) / sBeta[tid];
         {
-            float e2[2][4] = {};
+            float e2[2][4] = {}, f2[2][4] = {};
             if (cq <= R)
-                for (int k = 0; k < D; k += 16)
+                for (int k = 0; k < D; k += 16) {
                     mma_step<false, true>(e2, sDO, XS, sU, XS, 16 * R, 16 * cq, k);
+                    mma_step<false, true>(f2, sDUT, XS, sU, XS, 16 * R, 16 * cq, k);
+                }
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int i = 16 * cq + 8 * j + 2 * t;
-                const float s = p.scale;
+                const float s = p.scale, b0 = -sBeta[r0], b1 = -sBeta[r1];
                 st2(sGP + r0 * LS + i, i <= r0 ? s * e2[j][0] : 0.0f, i + 1 <= r0 ? s * e2[j][1] : 0.0f);
                 st2(sGP + r1 * LS + i, i <= r1 ? s * e2[j][2] : 0.0f, i + 1 <= r1 ? s * e2[j][3] : 0.0f);
+                st2(sGA + r0 * LS + i, i < r0 ? b0 * f2[j][0] : 0.0f, i + 1 < r0 ? b0 * f2[j][1] : 0.0f);
+                st2(sGA + r1 * LS + i, i < r1 ? b1 * f2[j][2] : 0.0f, i + 1 < r1 ? b1 * f2[j][3] : 0.0f);
             }
             // dS' in, and d e^{b_L}_c = sum_j dS'_cj S_cj: row c is D/4 float4
             // units on D/4 consecutive lanes
@@ -605,51 +508,12 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         }
         __syncthreads();
 
-        // ---- 4. dA = -T^T dT T^T (strictly lower); G_A = diag(beta) dA;
-        // dbeta += sum_i dA_ri (K * K)_ri
-        bf16 *sX = sUT;                                             // 64 x 64
-        bf16 *sGA = sDO;                                            // 64 x 64
-        {
-            // X = T^T dT: op(A)[i][r] = T[r][i], nonzero for r >= i
-            float e2[2][4] = {};
-            for (int k = 16 * R; k < 64; k += 16)
-                mma_step<true, false>(e2, sTb, LS, sDT, LS, 16 * R, 16 * cq, k);
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int i = 16 * cq + 8 * j + 2 * t;
-                st2(sX + r0 * LS + i, e2[j][0], e2[j][1]);
-                st2(sX + r1 * LS + i, e2[j][2], e2[j][3]);
-            }
-        }
-        __syncthreads();
-        {
-            // dA = -X T^T: op(B)[a][i] = T[i][a], nonzero for a <= i
-            float e2[2][4] = {};
-            if (cq <= R)
-                for (int k = 0; k < 16 * cq + 16; k += 16)
-                    mma_step<false, true>(e2, sX, LS, sTb, LS, 16 * R, 16 * cq, k);
-            float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int e1 = 0; e1 < 2; ++e1) {
-                    const int i = 16 * cq + 8 * j + 2 * t + e1;
-                    const float da0 = i < r0 ? -e2[j][e1] : 0.0f, da1 = i < r1 ? -e2[j][2 + e1] : 0.0f;
-                    if (i < r0) s0 += da0 * __bfloat162float(sKK[r0 * LS + i]);
-                    if (i < r1) s1 += da1 * __bfloat162float(sKK[r1 * LS + i]);
-                    sGA[r0 * LS + i] = __float2bfloat16_rn(sBeta[r0] * da0);
-                    sGA[r1 * LS + i] = __float2bfloat16_rn(sBeta[r1] * da1);
-                }
-            add_dbeta(s0, s1);
-        }
-        __syncthreads();
-
         // ---- 5. through the decayed scores Q * K (gradient dP) and K * K
         // (gradient G_A).  Operands scaled once per row: K_e = k e^{b_e(I) - b}
         // (to the end of the row's block), Q_s, K_s = (q, k) e^{b - b_s(R)} (from
         // the start of the row's block); middle factors m(R, I) = e^{b_s(R) - b_e(I)}.
         bf16 *sKe = reinterpret_cast<bf16 *>(U + L::O_DUT);
-        bf16 *sQs = reinterpret_cast<bf16 *>(U + L::O_UT);
+        bf16 *sQs = reinterpret_cast<bf16 *>(U + L::O_DO);
         bf16 *sKs2 = reinterpret_cast<bf16 *>(U + L::O_BK);
         for (int e = tid; e < 64 * D / 2; e += kNT) {
             const int r = e / (D / 2), c = 2 * (e % (D / 2)), Rb = r >> 4;
@@ -871,7 +735,7 @@ cudaError_t launch_delta_bwd_channel(const BwdChannelArgs &a, cudaStream_t s) {
     Params p{static_cast<const bf16 *>(a.q), static_cast<const bf16 *>(a.k),
              static_cast<const bf16 *>(a.v), static_cast<const bf16 *>(a.beta_logits),
              static_cast<const bf16 *>(a.gate_logits), static_cast<const bf16 *>(a.d_o),
-             a.table, a.states, a.dstates, a.du, a.dq, a.dk, a.dv, a.d_beta_logits,
+             a.table, a.states, a.dstates, a.du, a.tiles, a.dq, a.dk, a.dv, a.d_beta_logits,
              a.d_gate_logits, a.n_tasks, a.H, a.scale, a.flags};
     if (a.D == 64) return launch_d<64>(p, s);
     if (a.D == 128) return launch_d<128>(p, s);

@@ -236,6 +236,7 @@ struct IntraParams {
     const __nv_bfloat16 *gate_scalar;  // [ntok][H] with a scalar gate (ungated kernel), else null
     const int32_t *cu_seqlens;         // [N + 1]
     uint8_t *records;       // [slots][H] records
+    uint8_t *t_out;         // null, or [slots][H] T tiles (8 KB) for the backward pass
     unsigned *err;
     int64_t n_tasks;        // slots * H
     int N, H, ntok;
@@ -1169,6 +1170,8 @@ __device__ __forceinline__ void intra_run(const CUtensorMap &tm_q, const CUtenso
             bulk_store_hint(rec + Rec::WQ, wq, 4 * L::tile64, pol);
             bulk_store_hint(rec + Rec::AQ, aqk, 8192, pol);
             if (GATED || scalar) bulk_store_hint(rec + Rec::GEND, sgend, 4 * D, pol);
+            // the backward pass's copy of T: rows 0..63 of [T; T], a 64-row tile
+            if (p.t_out) bulk_store_hint(p.t_out + ((int64_t)cur.w * H + h) * 8192, t16, 8192, pol);
             bulk_commit();
             if constexpr (FUSED) fst[F_PUB] = (int64_t)cur.w * H + h;
         }
@@ -1603,7 +1606,7 @@ template <int D, bool GATED, bool SCALAR>
 cudaError_t launch_t(const TcLaunch &x, cudaStream_t s) {
     IntraParams p{static_cast<const __nv_bfloat16 *>(x.a->beta_logits),
                   SCALAR ? static_cast<const __nv_bfloat16 *>(x.a->gate_logits) : nullptr,
-                  x.a->cu_seqlens, x.records,
+                  x.a->cu_seqlens, x.records, x.a->t_out,
                   x.err, x.slots * x.a->H, x.a->N, x.a->H, x.a->ntok, x.a->flags};
     using L = Layout<D, GATED>;
     // Shared memory caps the CTAs per SM at CTAS_PER_SM, which keeps their
@@ -1639,7 +1642,7 @@ cudaError_t launch_fused_t(const TcLaunch &x, cudaStream_t s, int grid) {
     const PrefillArgs &a = *x.a;
     IntraParams p{static_cast<const __nv_bfloat16 *>(a.beta_logits),
                   SCALAR ? static_cast<const __nv_bfloat16 *>(a.gate_logits) : nullptr,
-                  a.cu_seqlens, x.records, x.err, x.slots * a.H, a.N, a.H, a.ntok, a.flags};
+                  a.cu_seqlens, x.records, a.t_out, x.err, x.slots * a.H, a.N, a.H, a.ntok, a.flags};
     FusedSched fs;
     fs.flags = x.flags;
     fs.counters = x.counters;

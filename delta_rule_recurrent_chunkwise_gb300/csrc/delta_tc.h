@@ -60,13 +60,15 @@ cudaError_t launch_delta_inter128(const TcLaunch &x, cudaStream_t s);
 
 // Per-chunk gradients of the chunkwise backward pass (bf16, d = dk = dv in
 // {64, 128}, a decay per key channel, per token or none): every (chunk,
-// head) from its inputs, its starting state, the reverse chain's dS' and du.
+// head) from its inputs, its starting state, the reverse chain's dS' and du,
+// and the forward pass's T.
 struct BwdChannelArgs {
     const void *q, *k, *v, *beta_logits, *gate_logits, *d_o;
     const int2 *table;        // [slots] {first token, length}
     const float *states;      // [slots][H][D][D] S at each chunk start
     const float *dstates;     // [slots][H][D][D] dS' of each chunk
     const float *du;          // [slots][H][64][D] du of each chunk
+    const uint8_t *tiles;     // [slots][H] T of each chunk, 8 KB bf16 swizzled tiles
     float *dq, *dk, *dv, *d_beta_logits, *d_gate_logits;
     int64_t n_tasks;
     int H, D;

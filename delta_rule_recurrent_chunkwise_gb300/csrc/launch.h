@@ -24,6 +24,9 @@ struct PrefillArgs {
     // start of every chunk, fp32 [slot][H][dk][dv] (slot as in the chunk
     // table), or null.  With it, o may be null (no output written).
     float *chunk_states = nullptr;
+    // Backward pass only: the UT matrix T = (I + A)^{-1} of every chunk,
+    // bf16, one 64 x 64 row-swizzled tile (8 KB) per (slot, head), or null.
+    uint8_t *t_out = nullptr;
     // Tokens per chunk of the recurrence: 64, or 128 on the tensor-core path
     // with dk = dv = 64 (the records stay per 64 tokens; the recurrence pairs
     // them).
