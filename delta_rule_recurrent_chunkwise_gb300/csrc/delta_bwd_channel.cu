@@ -121,7 +121,8 @@ struct Lay {
     static constexpr int U = ROW + 512;
     // union region, phases 2-3 (the largest)
     static constexpr int O_DO = 0, O_DU = XB, O_DUT = 2 * XB, O_UT = 3 * XB, O_BK = 4 * XB;
-    static constexpr int O_S = 5 * XB, U_BYTES = 5 * XB + SB;
+    // phase 5: the alpha table (fp32 [64][FS]) in the S / dS' slot
+    static constexpr int O_S = 5 * XB, U_BYTES = 5 * XB + (SB > 64 * FS * 4 ? SB : 64 * FS * 4);
     static constexpr int BYTES = U + U_BYTES;
     // phase 6 (dQ, dK and db in fp32) fits inside the union region
     static_assert(3 * 64 * FS * 4 <= U_BYTES, "phase 6");
@@ -515,6 +516,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         bf16 *sKe = reinterpret_cast<bf16 *>(U + L::O_DUT);
         bf16 *sQs = reinterpret_cast<bf16 *>(U + L::O_DO);
         bf16 *sKs2 = reinterpret_cast<bf16 *>(U + L::O_BK);
+        float *sAl = reinterpret_cast<float *>(U + L::O_S);   // alpha_t = e^{b_t - b_(t-1)}, fp32 [64][FS]
         for (int e = tid; e < 64 * D / 2; e += kNT) {
             const int r = e / (D / 2), c = 2 * (e % (D / 2)), Rb = r >> 4;
             const float2 kv = ld2(sK + r * XS + c), qv = ld2(sQ + r * XS + c);
@@ -523,6 +525,8 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
             st2(sKe + r * XS + c, kv.x * ex2(be.x - b.x), kv.y * ex2(be.y - b.y));
             st2(sQs + r * XS + c, qv.x * f0, qv.y * f1);
             st2(sKs2 + r * XS + c, kv.x * f0, kv.y * f1);
+            const float2 bp = r > 0 ? b2at(r - 1, c) : make_float2(0.0f, 0.0f);
+            *reinterpret_cast<float2 *>(sAl + r * FS + c) = make_float2(ex2(b.x - bp.x), ex2(b.y - bp.y));
         }
         for (int e = tid; e < 6 * D; e += kNT) {
             const int pi = e / D, c = e % D;
@@ -585,37 +589,37 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
             }
         }
         {
-            // diagonal blocks exactly, e^{b_r - b_i} taken directly (exponent <= 0):
+            // diagonal blocks exactly, e^{b_r - b_i} as a running product of the
+            // per-token decays alpha_t = e^{b_t - b_(t-1)} (all <= 1):
             //   dQ_rc  += sum_{16R <= i <= r} dP_ri k_ic e^{b_rc - b_ic}
             //   dK+_rc += sum_{16R <= i <  r} G_A,ri k_ic e^{b_rc - b_ic}
             //   dK-_ic += sum_{i <= r < 16R+16} (dP_ri q_rc + G_A,ri k_rc) e^{b_rc - b_ic}
             // (per lane 34 (row, partner) steps whatever g)
+            auto al2 = [&](int r, int c) { return *reinterpret_cast<const float2 *>(sAl + r * FS + c); };
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
                 const int r = r0 + 8 * hr;
-                float br[2 * NT];
+                float f[2 * NT];   // e^{b_r - b_i} at the current partner i, i from r down
 #pragma unroll
-                for (int j = 0; j < NT; ++j) {
-                    const float2 b2 = b2at(r, n0 + 8 * j + 2 * t);
-                    br[2 * j] = b2.x;
-                    br[2 * j + 1] = b2.y;
-                }
-                for (int i = 16 * R; i <= r; ++i) {
+                for (int j = 0; j < 2 * NT; ++j) f[j] = 1.0f;
+                for (int i = r; i >= 16 * R; --i) {
                     const float gp = __bfloat162float(sGP[r * LS + i]);
                     const float ga = __bfloat162float(sGA[r * LS + i]);
 #pragma unroll
                     for (int j = 0; j < NT; ++j) {
                         const int c = n0 + 8 * j + 2 * t;
-                        const float2 kv = ld2(sK + i * XS + c);
-                        const float2 bi = b2at(i, c);
-                        const float w0 = kv.x * ex2(br[2 * j] - bi.x);
-                        const float w1 = kv.y * ex2(br[2 * j + 1] - bi.y);
+                        const float2 kv = ld2(sK + i * XS + c), al = al2(i, c);
+                        const float w0 = kv.x * f[2 * j], w1 = kv.y * f[2 * j + 1];
                         aQ[j][2 * hr] = fmaf(gp, w0, aQ[j][2 * hr]);
                         aQ[j][2 * hr + 1] = fmaf(gp, w1, aQ[j][2 * hr + 1]);
                         aKp[j][2 * hr] = fmaf(ga, w0, aKp[j][2 * hr]);
                         aKp[j][2 * hr + 1] = fmaf(ga, w1, aKp[j][2 * hr + 1]);
+                        f[2 * j] *= al.x;   // e^{b_r - b_(i-1)}
+                        f[2 * j + 1] *= al.y;
                     }
                 }
+#pragma unroll
+                for (int j = 0; j < 2 * NT; ++j) f[j] = 1.0f;   // e^{b_rr - b_r}, rr from r up
                 for (int rr = r; rr < 16 * R + 16; ++rr) {
                     const float gp = __bfloat162float(sGP[rr * LS + r]);
                     const float ga = __bfloat162float(sGA[rr * LS + r]);
@@ -623,10 +627,13 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                     for (int j = 0; j < NT; ++j) {
                         const int c = n0 + 8 * j + 2 * t;
                         const float2 qv = ld2(sQ + rr * XS + c), kv = ld2(sK + rr * XS + c);
-                        const float2 b2 = b2at(rr, c);
-                        const float w0 = ex2(b2.x - br[2 * j]), w1 = ex2(b2.y - br[2 * j + 1]);
-                        aKm[j][2 * hr] = fmaf(fmaf(gp, qv.x, ga * kv.x), w0, aKm[j][2 * hr]);
-                        aKm[j][2 * hr + 1] = fmaf(fmaf(gp, qv.y, ga * kv.y), w1, aKm[j][2 * hr + 1]);
+                        if (rr > r) {
+                            const float2 al = al2(rr, c);
+                            f[2 * j] *= al.x;
+                            f[2 * j + 1] *= al.y;
+                        }
+                        aKm[j][2 * hr] = fmaf(fmaf(gp, qv.x, ga * kv.x), f[2 * j], aKm[j][2 * hr]);
+                        aKm[j][2 * hr + 1] = fmaf(fmaf(gp, qv.y, ga * kv.y), f[2 * j + 1], aKm[j][2 * hr + 1]);
                     }
                 }
             }
