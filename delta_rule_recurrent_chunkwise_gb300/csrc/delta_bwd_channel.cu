@@ -169,7 +169,10 @@ __device__ __forceinline__ void column_scan(float *x, float *seg, bool reverse) 
     __syncthreads();
 }
 
-template <int D>
+// DECAY = false (no gate): every decay factor is 1, the decayed scores are
+// plain products (diagonal blocks included, on the tensor cores) and there
+// is no decay gradient.
+template <int D, bool DECAY>
 __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
     using L = Lay<D>;
     constexpr int XS = L::XS, LS = L::LS, FS = L::FS;
@@ -237,7 +240,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
             const bool ok = r < len;
             float xq[CPL], xk[CPL], lg[CPL];
             const bf16 *pq = p.q + tok(ok ? r : 0) * D, *pk = p.k + tok(ok ? r : 0) * D;
-            const float gs = (ok && p.gate_logits && scalar_gate)
+            const float gs = (DECAY && ok && scalar_gate)
                                  ? log_decay_f(__bfloat162float(p.gate_logits[tok(r)])) : 0.0f;
 #pragma unroll
             for (int m = 0; m < P2; ++m) {
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                 xq[2 * m] = a.x; xq[2 * m + 1] = a.y;
                 xk[2 * m] = b.x; xk[2 * m + 1] = b.y;
                 float2 gl = make_float2(gs, gs);
-                if (ok && p.gate_logits && !scalar_gate) {
+                if (DECAY && ok && !scalar_gate) {
                     const float2 gg = ld2(p.gate_logits + tok(r) * D + c);
                     gl = make_float2(log_decay_f(gg.x), log_decay_f(gg.y));
                 }
@@ -279,11 +282,13 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         if (tid < 64) sDBeta[tid] = 0.0f;
         if (tid < D) sDBL[tid] = sDGL[tid] = 0.0f;
         __syncthreads();
-        column_scan<D, FS>(sB, sSeg, false);
+        if constexpr (DECAY) column_scan<D, FS>(sB, sSeg, false);
         prefetch_task(task + gridDim.x);
         // sB[r][c] = b_rc / ln 2 from here on; b at the token before block R
         auto bs = [&](int Rb, int c) { return Rb == 0 ? 0.0f : sB[(16 * Rb - 1) * FS + c]; };
         auto b2at = [&](int r, int c) { return *reinterpret_cast<const float2 *>(sB + r * FS + c); };
+        // 2^x of a decay exponent; exactly 1 without decay (its loads then go unused)
+        auto ex2d = [&](float x) { if constexpr (DECAY) return ex2(x); else return 1.0f; };
 
         // ---- 1. T = (I + A)^{-1} from the forward pass (bf16, one 64-row
         // swizzled tile of 8 KB: one 16-byte unit per thread)
@@ -308,8 +313,8 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                 const float be = sBeta[r];
                 const float2 k0 = ld2(sK + r * XS + c), k1 = ld2(sK + r * XS + c + 2);
                 const float4 b = *reinterpret_cast<const float4 *>(sB + r * FS + c);
-                st2(sBK + r * XS + c, be * k0.x * ex2(b.x), be * k0.y * ex2(b.y));
-                st2(sBK + r * XS + c + 2, be * k1.x * ex2(b.z), be * k1.y * ex2(b.w));
+                st2(sBK + r * XS + c, be * k0.x * ex2d(b.x), be * k0.y * ex2d(b.y));
+                st2(sBK + r * XS + c + 2, be * k1.x * ex2d(b.z), be * k1.y * ex2d(b.w));
             }
             for (int e = tid; e < 64 * D / 8; e += kNT) {
                 const int r = e / (D / 8), c = 8 * (e % (D / 8));
@@ -398,8 +403,8 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
 #pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {
                     const float2 b = b2at(r0 + 8 * hr, n0 + 8 * j + 2 * t);
-                    aQ[j][2 * hr] = p.scale * ex2(b.x) * d[j][2 * hr];
-                    aQ[j][2 * hr + 1] = p.scale * ex2(b.y) * d[j][2 * hr + 1];
+                    aQ[j][2 * hr] = p.scale * ex2d(b.x) * d[j][2 * hr];
+                    aQ[j][2 * hr + 1] = p.scale * ex2d(b.y) * d[j][2 * hr + 1];
                 }
             // dBk = -du_T S^T: dK+ gets beta e^b dBk; dbeta += dBk . (K e^b)
             zero(d);
@@ -411,7 +416,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                 for (int hr = 0; hr < 2; ++hr) {
                     const int r = r0 + 8 * hr, c = n0 + 8 * j + 2 * t;
                     const float2 b = b2at(r, c), kv = ld2(sK + r * XS + c);
-                    const float e0 = ex2(b.x), e1 = ex2(b.y);
+                    const float e0 = ex2d(b.x), e1 = ex2d(b.y);
                     const float dbk0 = -d[j][2 * hr], dbk1 = -d[j][2 * hr + 1];
                     aKp[j][2 * hr] = sBeta[r] * e0 * dbk0;
                     aKp[j][2 * hr + 1] = sBeta[r] * e1 * dbk1;
@@ -490,10 +495,11 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                 const int c = n0 + 8 * j + 2 * t;
                 const float2 bl = b2at(63, c), b0 = b2at(r0, c), b1 = b2at(r1, c);
                 const float2 k0 = ld2(sK + r0 * XS + c), k1 = ld2(sK + r1 * XS + c);
-                aKm[j][0] = ex2(bl.x - b0.x) * d[j][0];
-                aKm[j][1] = ex2(bl.y - b0.y) * d[j][1];
-                aKm[j][2] = ex2(bl.x - b1.x) * d[j][2];
-                aKm[j][3] = ex2(bl.y - b1.y) * d[j][3];
+                aKm[j][0] = ex2d(bl.x - b0.x) * d[j][0];
+                aKm[j][1] = ex2d(bl.y - b0.y) * d[j][1];
+                aKm[j][2] = ex2d(bl.x - b1.x) * d[j][2];
+                aKm[j][3] = ex2d(bl.y - b1.y) * d[j][3];
+                if constexpr (!DECAY) continue;   // no d b_L without a gate
                 float sx = k0.x * aKm[j][0] + k1.x * aKm[j][2];
                 float sy = k0.y * aKm[j][1] + k1.y * aKm[j][3];
 #pragma unroll
@@ -513,11 +519,12 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         // (gradient G_A).  Operands scaled once per row: K_e = k e^{b_e(I) - b}
         // (to the end of the row's block), Q_s, K_s = (q, k) e^{b - b_s(R)} (from
         // the start of the row's block); middle factors m(R, I) = e^{b_s(R) - b_e(I)}.
-        bf16 *sKe = reinterpret_cast<bf16 *>(U + L::O_DUT);
-        bf16 *sQs = reinterpret_cast<bf16 *>(U + L::O_DO);
-        bf16 *sKs2 = reinterpret_cast<bf16 *>(U + L::O_BK);
+        // (without decay they are K and Q themselves, and every factor is 1)
+        bf16 *sKe = DECAY ? reinterpret_cast<bf16 *>(U + L::O_DUT) : sK;
+        bf16 *sQs = DECAY ? reinterpret_cast<bf16 *>(U + L::O_DO) : sQ;
+        bf16 *sKs2 = DECAY ? reinterpret_cast<bf16 *>(U + L::O_BK) : sK;
         float *sAl = reinterpret_cast<float *>(U + L::O_S);   // alpha_t = e^{b_t - b_(t-1)}, fp32 [64][FS]
-        for (int e = tid; e < 64 * D / 2; e += kNT) {
+        for (int e = tid; e < (DECAY ? 64 * D / 2 : 0); e += kNT) {
             const int r = e / (D / 2), c = 2 * (e % (D / 2)), Rb = r >> 4;
             const float2 kv = ld2(sK + r * XS + c), qv = ld2(sQ + r * XS + c);
             const float2 b = b2at(r, c), be = b2at(16 * Rb + 15, c);
@@ -528,7 +535,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
             const float2 bp = r > 0 ? b2at(r - 1, c) : make_float2(0.0f, 0.0f);
             *reinterpret_cast<float2 *>(sAl + r * FS + c) = make_float2(ex2(b.x - bp.x), ex2(b.y - bp.y));
         }
-        for (int e = tid; e < 6 * D; e += kNT) {
+        for (int e = tid; e < (DECAY ? 6 * D : 0); e += kNT) {
             const int pi = e / D, c = e % D;
             const int Rb = pi < 1 ? 1 : pi < 3 ? 2 : 3, Ib = pi - Rb * (Rb - 1) / 2;
             sMF[pi * D + c] = ex2(bs(Rb, c) - sB[(16 * Ib + 15) * FS + c]);
@@ -536,7 +543,8 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         __syncthreads();
         auto mf = [&](int Rb, int Ib, int c) { return sMF[(Rb * (Rb - 1) / 2 + Ib) * D + c]; };
         {
-            // off-diagonal blocks, two n8 tiles at a time.  Rows of block R:
+            // off-diagonal blocks (without decay also the diagonal ones, as
+            // plain products), two n8 tiles at a time.  Rows of block R:
             //   dQ  += e^{b_r - b_s(R)} sum_{I<R} m(R,I) (dP[R,I] K_e[I])
             //   dK+ += e^{b_r - b_s(R)} sum_{I<R} m(R,I) (G_A[R,I] K_e[I])
             // rows of block I = R of this warp:
@@ -545,30 +553,40 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
             for (int j = 0; j < NT; j += 2) {
                 const int nb = n0 + 8 * j;
                 float sq[2][4] = {}, sa[2][4] = {}, sm2[2][4] = {};
-                for (int Ib = 0; Ib < R; ++Ib) {
-                    float tq[2][4] = {}, ta[2][4] = {};
-                    mma_step<false, false>(tq, sGP, LS, sKe, XS, 16 * R, nb, 16 * Ib);
-                    mma_step<false, false>(ta, sGA, LS, sKe, XS, 16 * R, nb, 16 * Ib);
+                for (int Ib = 0; Ib < R + (DECAY ? 0 : 1); ++Ib) {
+                    if constexpr (DECAY) {
+                        float tq[2][4] = {}, ta[2][4] = {};
+                        mma_step<false, false>(tq, sGP, LS, sKe, XS, 16 * R, nb, 16 * Ib);
+                        mma_step<false, false>(ta, sGA, LS, sKe, XS, 16 * R, nb, 16 * Ib);
 #pragma unroll
-                    for (int jj = 0; jj < 2; ++jj)
+                        for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float m = mf(R, Ib, nb + 8 * jj + 2 * t + (e & 1));
-                            sq[jj][e] = fmaf(m, tq[jj][e], sq[jj][e]);
-                            sa[jj][e] = fmaf(m, ta[jj][e], sa[jj][e]);
-                        }
+                            for (int e = 0; e < 4; ++e) {
+                                const float m = mf(R, Ib, nb + 8 * jj + 2 * t + (e & 1));
+                                sq[jj][e] = fmaf(m, tq[jj][e], sq[jj][e]);
+                                sa[jj][e] = fmaf(m, ta[jj][e], sa[jj][e]);
+                            }
+                    } else {
+                        mma_step<false, false>(sq, sGP, LS, sKe, XS, 16 * R, nb, 16 * Ib);
+                        mma_step<false, false>(sa, sGA, LS, sKe, XS, 16 * R, nb, 16 * Ib);
+                    }
                 }
-                for (int Rb = R + 1; Rb < 4; ++Rb) {
-                    float tb[2][4] = {};
-                    mma_step<true, false>(tb, sGP, LS, sQs, XS, 16 * R, nb, 16 * Rb);
-                    mma_step<true, false>(tb, sGA, LS, sKs2, XS, 16 * R, nb, 16 * Rb);
+                for (int Rb = R + (DECAY ? 1 : 0); Rb < 4; ++Rb) {
+                    if constexpr (DECAY) {
+                        float tb[2][4] = {};
+                        mma_step<true, false>(tb, sGP, LS, sQs, XS, 16 * R, nb, 16 * Rb);
+                        mma_step<true, false>(tb, sGA, LS, sKs2, XS, 16 * R, nb, 16 * Rb);
 #pragma unroll
-                    for (int jj = 0; jj < 2; ++jj)
+                        for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float m = mf(Rb, R, nb + 8 * jj + 2 * t + (e & 1));
-                            sm2[jj][e] = fmaf(m, tb[jj][e], sm2[jj][e]);
-                        }
+                            for (int e = 0; e < 4; ++e) {
+                                const float m = mf(Rb, R, nb + 8 * jj + 2 * t + (e & 1));
+                                sm2[jj][e] = fmaf(m, tb[jj][e], sm2[jj][e]);
+                            }
+                    } else {
+                        mma_step<true, false>(sm2, sGP, LS, sQs, XS, 16 * R, nb, 16 * Rb);
+                        mma_step<true, false>(sm2, sGA, LS, sKs2, XS, 16 * R, nb, 16 * Rb);
+                    }
                 }
 #pragma unroll
                 for (int jj = 0; jj < 2; ++jj) {
@@ -579,8 +597,8 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                     for (int e = 0; e < 4; ++e) {
                         const float2 b = b2at(r0 + 8 * (e >> 1), c);
                         const float bb = (e & 1) ? b.y : b.x;
-                        const float fr = ex2(bb - ((e & 1) ? bsr.y : bsr.x));
-                        const float fc = ex2(((e & 1) ? ber.y : ber.x) - bb);
+                        const float fr = ex2d(bb - ((e & 1) ? bsr.y : bsr.x));
+                        const float fc = ex2d(((e & 1) ? ber.y : ber.x) - bb);
                         aQ[j + jj][e] = fmaf(fr, sq[jj][e], aQ[j + jj][e]);
                         aKp[j + jj][e] = fmaf(fr, sa[jj][e], aKp[j + jj][e]);
                         aKm[j + jj][e] = fmaf(fc, sm2[jj][e], aKm[j + jj][e]);
@@ -588,7 +606,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                 }
             }
         }
-        {
+        if constexpr (DECAY) {
             // diagonal blocks exactly, e^{b_r - b_i} as a running product of the
             // per-token decays alpha_t = e^{b_t - b_(t-1)} (all <= 1):
             //   dQ_rc  += sum_{16R <= i <= r} dP_ri k_ic e^{b_rc - b_ic}
@@ -654,11 +672,12 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                 const float m0 = aKm[j][2 * hr], m1 = aKm[j][2 * hr + 1];
                 *reinterpret_cast<float2 *>(sFQ + r * FS + c) = make_float2(dq0, dq1);
                 *reinterpret_cast<float2 *>(sFK + r * FS + c) = make_float2(p0 + m0, p1 + m1);
-                *reinterpret_cast<float2 *>(sDB + r * FS + c) =
-                    make_float2(qv.x * dq0 + kv.x * (p0 - m0), qv.y * dq1 + kv.y * (p1 - m1));
+                if constexpr (DECAY)
+                    *reinterpret_cast<float2 *>(sDB + r * FS + c) =
+                        make_float2(qv.x * dq0 + kv.x * (p0 - m0), qv.y * dq1 + kv.y * (p1 - m1));
             }
         __syncthreads();
-        if (tid < D && p.gate_logits)
+        if (DECAY && tid < D)
             sDB[63 * FS + tid] += sDBL[tid] + ex2(sB[63 * FS + tid]) * sDGL[tid];
 #pragma unroll 1
         for (int rr = 0; rr < 4; ++rr) {
@@ -687,7 +706,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
             const float be = sBeta[tid];
             p.d_beta_logits[tok(tid)] = sDBeta[tid] * be * (1.0f - be);
         }
-        if (p.gate_logits) {
+        if constexpr (DECAY) {
             __syncthreads();
             column_scan<D, FS>(sDB, sSeg, true);   // d log alpha_t = sum_{r >= t} db_r
             // log alpha = -softplus(x): dx = -d(log alpha) sigmoid(x)
@@ -718,19 +737,19 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
     }
 }
 
-template <int D>
+template <int D, bool DECAY>
 cudaError_t launch_d(const Params &p, cudaStream_t s) {
     int dev = 0, sms = 0;
     cudaError_t e;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     constexpr int bytes = Lay<D>::BYTES;
-    if ((e = cudaFuncSetAttribute(delta_bwd_channel_kernel<D>,
+    if ((e = cudaFuncSetAttribute(delta_bwd_channel_kernel<D, DECAY>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
         return e;
     const int64_t grid = p.n_tasks < sms ? p.n_tasks : sms;
     if (grid > 0) {
-        delta_bwd_channel_kernel<D><<<(unsigned)grid, kNT, bytes, s>>>(p);
+        delta_bwd_channel_kernel<D, DECAY><<<(unsigned)grid, kNT, bytes, s>>>(p);
         e = cudaGetLastError();
     }
     return e;
@@ -744,8 +763,9 @@ cudaError_t launch_delta_bwd_channel(const BwdChannelArgs &a, cudaStream_t s) {
              static_cast<const bf16 *>(a.gate_logits), static_cast<const bf16 *>(a.d_o),
              a.table, a.states, a.dstates, a.du, a.tiles, a.dq, a.dk, a.dv, a.d_beta_logits,
              a.d_gate_logits, a.n_tasks, a.H, a.scale, a.flags};
-    if (a.D == 64) return launch_d<64>(p, s);
-    if (a.D == 128) return launch_d<128>(p, s);
+    const bool decay = a.gate_logits != nullptr;
+    if (a.D == 64) return decay ? launch_d<64, true>(p, s) : launch_d<64, false>(p, s);
+    if (a.D == 128) return decay ? launch_d<128, true>(p, s) : launch_d<128, false>(p, s);
     return cudaErrorInvalidValue;
 }
 
