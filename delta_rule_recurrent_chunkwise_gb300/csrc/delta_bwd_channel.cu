@@ -91,6 +91,19 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// 16 bytes global -> shared without a register round trip (zeros when
+// !valid; src must still be a mapped address), and the wait for all of this
+// thread's outstanding copies.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(wmma16::saddr(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_l2(const void *p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
 }
@@ -135,7 +148,7 @@ struct Params {
     const int2 *table;        // [slots] {first token, length}
     const float *states;      // [slots][H][D][D] S at each chunk start
     const float *dstates;     // [slots][H][D][D] dS' of each chunk
-    const float *du;          // [slots][H][64][D] du of each chunk
+    const bf16 *du;           // [slots][H][64][D] du of each chunk (bf16)
     const uint8_t *tiles;     // [slots][H] T of each chunk (8 KB bf16 swizzled tiles)
     float *dq, *dk, *dv, *d_beta_logits, *d_gate_logits;
     int64_t n_tasks;
@@ -199,7 +212,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
     const int r0 = 16 * R + g, r1 = r0 + 8;   // this lane's two output rows
 
     // inputs of task nt into L2 (one 128-byte line per request): the token
-    // rows of q, k, v, dO and per-channel gate logits, then S, dS' and du
+    // rows of q, k, v, dO and per-channel gate logits, then S, dS', du and T
     auto prefetch_task = [&](int64_t nt) {
         if (nt >= p.n_tasks) return;
         const int64_t ns = nt / H;
@@ -216,10 +229,13 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
             prefetch_l2(base + ((int64_t)(e.x + r) * H + nh) * D + l * 64);
         }
         const int64_t so = (ns * H + nh) * (int64_t)(D * D), uo = (ns * H + nh) * (int64_t)(64 * D);
-        for (int u = tid; u < D * D / 32 * 2 + 64 * D / 32; u += kNT) {
-            const float *q = u < D * D / 32 ? p.states + so + u * 32
-                           : u < D * D / 16 ? p.dstates + so + (u - D * D / 32) * 32
-                                            : p.du + uo + (u - D * D / 16) * 32;
+        constexpr int LSS = D * D / 32, LU = 64 * D / 64, LT = 8192 / 128;   // lines
+        for (int u = tid; u < 2 * LSS + LU + LT; u += kNT) {
+            const void *q = u < LSS ? (const void *)(p.states + so + u * 32)
+                          : u < 2 * LSS ? (const void *)(p.dstates + so + (u - LSS) * 32)
+                          : u < 2 * LSS + LU ? (const void *)(p.du + uo + (u - 2 * LSS) * 64)
+                                             : (const void *)(p.tiles + (ns * H + nh) * (int64_t)8192 +
+                                                              (u - 2 * LSS - LU) * 128);
             prefetch_l2(q);
         }
     };
@@ -232,26 +248,59 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         const int t0 = te.x, len = te.y;
         if (len <= 0) continue;
         auto tok = [&](int r) { return ((int64_t)(t0 + r) * H + h); };
+        bf16 *sDO = reinterpret_cast<bf16 *>(U + L::O_DO), *sDU = reinterpret_cast<bf16 *>(U + L::O_DU);
+
+        // The benchmark's bf16 operands go straight to shared memory by async
+        // copies, in flight through phase 0: T (8 KB, one 16-byte unit per
+        // thread), dO (rows past the end zero) and du, 64 x D each.
+        static_assert(kNT * 16 == 8192, "one unit of T per thread");
+        cp_async16(smem + L::TR + tid * 16, p.tiles + (slot * H + h) * (int64_t)8192 + tid * 16, true);
+        {
+            const bf16 *gdu = p.du + (slot * H + h) * (int64_t)(64 * D);
+#pragma unroll
+            for (int k = 0; k < 64 * D / 8 / kNT; ++k) {
+                const int e = tid + k * kNT, r = e / (D / 8), c = 8 * (e % (D / 8));
+                cp_async16(sDO + r * XS + c, p.d_o + tok(r < len ? r : 0) * D + c, r < len);
+                cp_async16(sDU + r * XS + c, gdu + r * D + c, true);
+            }
+        }
 
         // ---- 0. q^, k^ (silu, L2 norm), beta, log2 alpha; b = prefix sums.
-        // Lanes take channel pairs 2 lane + 64 m.
+        // Lanes take channel pairs 2 lane + 64 m; the warp's four rows are
+        // loaded first (bf16 pairs kept packed).
+        __nv_bfloat162 rq[4][P2], rk[4][P2], rg[4][P2];
+        float rgs[4], rbl[4];
+        const __nv_bfloat162 z2 = __floats2bfloat162_rn(0.0f, 0.0f);
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+            const int r = w + 16 * rr;
+            const bool ok = r < len;
+            const int64_t o = tok(ok ? r : 0) * D;
+            using bfp = const __nv_bfloat162 *;
+#pragma unroll
+            for (int m = 0; m < P2; ++m) {
+                const int c = 2 * lane + 64 * m;
+                rq[rr][m] = ok ? *reinterpret_cast<bfp>(p.q + o + c) : z2;
+                rk[rr][m] = ok ? *reinterpret_cast<bfp>(p.k + o + c) : z2;
+                rg[rr][m] = (DECAY && ok && !scalar_gate) ? *reinterpret_cast<bfp>(p.gate_logits + o + c) : z2;
+            }
+            rgs[rr] = (DECAY && ok && scalar_gate) ? __bfloat162float(p.gate_logits[tok(r)]) : 0.0f;
+            rbl[rr] = ok ? __bfloat162float(p.beta_logits[tok(r)]) : 0.0f;
+        }
+#pragma unroll
         for (int rr = 0; rr < 4; ++rr) {
             const int r = w + 16 * rr;
             const bool ok = r < len;
             float xq[CPL], xk[CPL], lg[CPL];
-            const bf16 *pq = p.q + tok(ok ? r : 0) * D, *pk = p.k + tok(ok ? r : 0) * D;
-            const float gs = (DECAY && ok && scalar_gate)
-                                 ? log_decay_f(__bfloat162float(p.gate_logits[tok(r)])) : 0.0f;
+            const float gs = (DECAY && ok && scalar_gate) ? log_decay_f(rgs[rr]) : 0.0f;
 #pragma unroll
             for (int m = 0; m < P2; ++m) {
-                const int c = 2 * lane + 64 * m;
-                const float2 a = ok ? ld2(pq + c) : make_float2(0.0f, 0.0f);
-                const float2 b = ok ? ld2(pk + c) : make_float2(0.0f, 0.0f);
+                const float2 a = __bfloat1622float2(rq[rr][m]), b = __bfloat1622float2(rk[rr][m]);
                 xq[2 * m] = a.x; xq[2 * m + 1] = a.y;
                 xk[2 * m] = b.x; xk[2 * m + 1] = b.y;
                 float2 gl = make_float2(gs, gs);
                 if (DECAY && ok && !scalar_gate) {
-                    const float2 gg = ld2(p.gate_logits + tok(r) * D + c);
+                    const float2 gg = __bfloat1622float2(rg[rr][m]);
                     gl = make_float2(log_decay_f(gg.x), log_decay_f(gg.y));
                 }
                 lg[2 * m] = gl.x * kLog2e;
@@ -276,8 +325,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
 #pragma unroll
             for (int m = 0; m < P2; ++m)
                 *reinterpret_cast<float2 *>(sB + r * FS + 2 * lane + 64 * m) = make_float2(lg[2 * m], lg[2 * m + 1]);
-            if (lane == 0)
-                sBeta[r] = ok ? sigmoid_f(__bfloat162float(p.beta_logits[tok(r)])) : 0.0f;
+            if (lane == 0) sBeta[r] = ok ? sigmoid_f(rbl[rr]) : 0.0f;
         }
         if (tid < 64) sDBeta[tid] = 0.0f;
         if (tid < D) sDBL[tid] = sDGL[tid] = 0.0f;
@@ -291,44 +339,40 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         auto ex2d = [&](float x) { if constexpr (DECAY) return ex2(x); else return 1.0f; };
 
         // ---- 1. T = (I + A)^{-1} from the forward pass (bf16, one 64-row
-        // swizzled tile of 8 KB: one 16-byte unit per thread)
-        static_assert(kNT * 16 == 8192, "one unit of T per thread");
-        *reinterpret_cast<uint4 *>(smem + L::TR + tid * 16) =
-            *reinterpret_cast<const uint4 *>(p.tiles + (slot * H + h) * (int64_t)8192 + tid * 16);
+        // swizzled tile, already on its way)
         const wmma16::RsView tv{smem + L::TR, 64, 0};
 
-        // ---- 2. dO, du, S and Bk in; du_T = T^T du; u~, d(Q e^b), dBk
-        bf16 *sDO = reinterpret_cast<bf16 *>(U + L::O_DO), *sDU = reinterpret_cast<bf16 *>(U + L::O_DU);
+        // ---- 2. S and Bk in (dO, du by the async copies); du_T = T^T du;
+        // u~, d(Q e^b), dBk
         bf16 *sDUT = reinterpret_cast<bf16 *>(U + L::O_DUT), *sUT = reinterpret_cast<bf16 *>(U + L::O_UT);
         bf16 *sBK = reinterpret_cast<bf16 *>(U + L::O_BK), *sS = reinterpret_cast<bf16 *>(U + L::O_S);
         const float *gS = p.states + (slot * H + h) * (int64_t)(D * D);
         const float *gDS = p.dstates + (slot * H + h) * (int64_t)(D * D);
         {
-            const float *gdu = p.du + (slot * H + h) * (int64_t)(64 * D);
+            // S: every load of this thread first, then the bf16 stores
+            constexpr int NS = D * D / 4 / kNT;
+            float4 sv[NS];
+#pragma unroll
+            for (int k = 0; k < NS; ++k) {
+                const int e = tid + k * kNT;
+                sv[k] = *reinterpret_cast<const float4 *>(gS + (e / (D / 4)) * D + 4 * (e % (D / 4)));
+            }
             for (int e = tid; e < 64 * D / 4; e += kNT) {
                 const int r = e / (D / 4), c = 4 * (e % (D / 4));
-                const float4 a = *reinterpret_cast<const float4 *>(gdu + r * D + c);
-                st2(sDU + r * XS + c, a.x, a.y);
-                st2(sDU + r * XS + c + 2, a.z, a.w);
                 const float be = sBeta[r];
                 const float2 k0 = ld2(sK + r * XS + c), k1 = ld2(sK + r * XS + c + 2);
                 const float4 b = *reinterpret_cast<const float4 *>(sB + r * FS + c);
                 st2(sBK + r * XS + c, be * k0.x * ex2d(b.x), be * k0.y * ex2d(b.y));
                 st2(sBK + r * XS + c + 2, be * k1.x * ex2d(b.z), be * k1.y * ex2d(b.w));
             }
-            for (int e = tid; e < 64 * D / 8; e += kNT) {
-                const int r = e / (D / 8), c = 8 * (e % (D / 8));
-                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4 *>(sDO + r * XS + c) =
-                    r < len ? *reinterpret_cast<const uint4 *>(p.d_o + tok(r) * D + c) : z;
-            }
-            for (int e = tid; e < D * D / 4; e += kNT) {
-                const int r = e / (D / 4), c = 4 * (e % (D / 4));
-                const float4 a = *reinterpret_cast<const float4 *>(gS + r * D + c);
-                st2(sS + r * XS + c, a.x, a.y);
-                st2(sS + r * XS + c + 2, a.z, a.w);
+#pragma unroll
+            for (int k = 0; k < NS; ++k) {
+                const int e = tid + k * kNT, r = e / (D / 4), c = 4 * (e % (D / 4));
+                st2(sS + r * XS + c, sv[k].x, sv[k].y);
+                st2(sS + r * XS + c + 2, sv[k].z, sv[k].w);
             }
         }
+        cp_async_wait_all();   // T, dO, du in (made visible to all by the barrier below)
         if (tid < 64) sRow[tid] = sRow[64 + tid] = 0.0f;
         __syncthreads();
         float aQ[NT][4], aKp[NT][4], aKm[NT][4];   // dQ, dK+, dK- (see the file header)

@@ -37,7 +37,7 @@ struct ChainParams {
     const int32_t *cu;
     const float *d_final_S;
     float *dstates;           // [slots][H][D][D]: dS' of every chunk
-    float *du;                // null, or [slots][H][64][D]: du of every chunk
+    __nv_bfloat16 *du;        // null, or [slots][H][64][D]: du of every chunk (bf16)
     float *d_init_S;
     unsigned *err;
     int H, ntok;
@@ -193,15 +193,14 @@ __global__ void __launch_bounds__(ChainCfg<D>::NT, 1) delta_bwd_chain_kernel(Cha
             wmma16::zero(du);
             wmma16::mma_rows<NT_DU, true, false>(du, aq, dO, 16 * Ru, nu, 16 * Ru, 64);
             wmma16::mma_rows_c<0, D, NT_DU, false, false>(du, kt, dSp, 16 * Ru, nu);
-            float *gdu = p.du ? p.du + ((slot0 + c) * H + h) * (int64_t)(64 * D) : nullptr;
+            bf16 *gdu = p.du ? p.du + ((slot0 + c) * H + h) * (int64_t)(64 * D) : nullptr;
 #pragma unroll
             for (int j = 0; j < NT_DU; ++j)
 #pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {
                     const int r = 16 * Ru + g + 8 * hr, col = nu + 8 * j + 2 * t;
                     wmma16::st2(sDU + r * XS + col, du[j][2 * hr], du[j][2 * hr + 1]);
-                    if (gdu)
-                        *reinterpret_cast<float2 *>(gdu + r * D + col) = make_float2(du[j][2 * hr], du[j][2 * hr + 1]);
+                    if (gdu) wmma16::st2(gdu + r * D + col, du[j][2 * hr], du[j][2 * hr + 1]);
                 }
         }
         __syncthreads();
@@ -246,7 +245,7 @@ ChunkWs chunk_ws(int N, int ntok, int H, int D) {
     w.fwd = a256(delta_tc_workspace_bytes(N, ntok, H, D, D, 64, true));
     w.states = a256(slots * H * D * D * sizeof(float));
     w.dstates = w.states;
-    w.du = a256(slots * H * 64 * D * sizeof(float));
+    w.du = a256(slots * H * 64 * D * 2);   // du of every chunk, bf16
     w.tiles = a256(slots * H * 8192);   // T of every chunk (bf16 64 x 64)
     w.total = w.fwd + w.states + w.dstates + w.du + w.tiles;
     return w;
@@ -279,7 +278,7 @@ cudaError_t launch_delta_backward_chunked(const BwdArgs &a, cudaStream_t s) {
     uint8_t *base = static_cast<uint8_t *>(a.workspace);
     float *states = reinterpret_cast<float *>(base + w.fwd);
     float *dstates = reinterpret_cast<float *>(base + w.fwd + w.states);
-    float *du = reinterpret_cast<float *>(base + w.fwd + w.states + w.dstates);
+    __nv_bfloat16 *du = reinterpret_cast<__nv_bfloat16 *>(base + w.fwd + w.states + w.dstates);
     uint8_t *tiles = base + w.fwd + w.states + w.dstates + w.du;
     unsigned *err = device_error_word();
     if (!err) return cudaErrorInvalidValue;

@@ -67,7 +67,7 @@ struct BwdChannelArgs {
     const int2 *table;        // [slots] {first token, length}
     const float *states;      // [slots][H][D][D] S at each chunk start
     const float *dstates;     // [slots][H][D][D] dS' of each chunk
-    const float *du;          // [slots][H][64][D] du of each chunk
+    const __nv_bfloat16 *du;  // [slots][H][64][D] du of each chunk (bf16)
     const uint8_t *tiles;     // [slots][H] T of each chunk, 8 KB bf16 swizzled tiles
     float *dq, *dk, *dv, *d_beta_logits, *d_gate_logits;
     int64_t n_tasks;
