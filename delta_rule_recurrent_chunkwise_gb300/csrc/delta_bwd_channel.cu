@@ -147,7 +147,8 @@ struct Params {
     const bf16 *q, *k, *v, *beta_logits, *gate_logits, *d_o;
     const int2 *table;        // [slots] {first token, length}
     const float *states;      // [slots][H][D][D] S at each chunk start
-    const float *dstates;     // [slots][H][D][D] dS' of each chunk
+    const float *dstates;     // [slots][H][D][D] dS' of each chunk (fp32; with decay only)
+    const bf16 *dstates16;    // [slots][H][D][D] dS' of each chunk (bf16)
     const bf16 *du;           // [slots][H][64][D] du of each chunk (bf16)
     const uint8_t *tiles;     // [slots][H] T of each chunk (8 KB bf16 swizzled tiles)
     float *dq, *dk, *dv, *d_beta_logits, *d_gate_logits;
@@ -478,6 +479,16 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         bf16 *sU = sBK;                                             // 64 x D
         bf16 *sGP = sDU;                                            // 64 x 64
         bf16 *sGA = sUT;                                            // 64 x 64, after u
+        if constexpr (!DECAY) {
+            // dS' (bf16, from the chain) into the S slot, in flight through 3a
+            // and 3b (with decay it is staged from fp32 in 3b, beside S)
+            const bf16 *gds16 = p.dstates16 + (slot * H + h) * (int64_t)(D * D);
+#pragma unroll
+            for (int k = 0; k < D * D / 8 / kNT; ++k) {
+                const int e = tid + k * kNT, r = e / (D / 8), c = 8 * (e % (D / 8));
+                cp_async16(sS + r * XS + c, gds16 + r * D + c, true);
+            }
+        }
         {
             float d[NT][4];
             zero(d);
@@ -514,20 +525,23 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                 st2(sGA + r0 * LS + i, i < r0 ? b0 * f2[j][0] : 0.0f, i + 1 < r0 ? b0 * f2[j][1] : 0.0f);
                 st2(sGA + r1 * LS + i, i < r1 ? b1 * f2[j][2] : 0.0f, i + 1 < r1 ? b1 * f2[j][3] : 0.0f);
             }
-            // dS' in, and d e^{b_L}_c = sum_j dS'_cj S_cj: row c is D/4 float4
-            // units on D/4 consecutive lanes
-            for (int u = tid; u < D * D / 4; u += kNT) {
-                const int c = u / (D / 4), j = 4 * (u % (D / 4));
-                const float4 ds = *reinterpret_cast<const float4 *>(gDS + c * D + j);
-                const float4 sv = *reinterpret_cast<const float4 *>(gS + c * D + j);
-                float acc = ds.x * sv.x + ds.y * sv.y + ds.z * sv.z + ds.w * sv.w;
+            if constexpr (DECAY) {
+                // dS' in, and d e^{b_L}_c = sum_j dS'_cj S_cj: row c is D/4 float4
+                // units on D/4 consecutive lanes
+                for (int u = tid; u < D * D / 4; u += kNT) {
+                    const int c = u / (D / 4), j = 4 * (u % (D / 4));
+                    const float4 ds = *reinterpret_cast<const float4 *>(gDS + c * D + j);
+                    const float4 sv = *reinterpret_cast<const float4 *>(gS + c * D + j);
+                    float acc = ds.x * sv.x + ds.y * sv.y + ds.z * sv.z + ds.w * sv.w;
 #pragma unroll
-                for (int o = D / 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                if (u % (D / 4) == 0) sDGL[c] = acc;
-                st2(sS + c * XS + j, ds.x, ds.y);
-                st2(sS + c * XS + j + 2, ds.z, ds.w);
+                    for (int o = D / 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                    if (u % (D / 4) == 0) sDGL[c] = acc;
+                    st2(sS + c * XS + j, ds.x, ds.y);
+                    st2(sS + c * XS + j + 2, ds.z, ds.w);
+                }
             }
         }
+        cp_async_wait_all();   // dS' in (made visible to all by the barrier below)
         __syncthreads();
         {
             // K~ = K e^{b_L - b}: dK- gets e^{b_L - b} u dS'^T; d b_L += sum_i k~ (u dS'^T)
@@ -723,19 +737,31 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         __syncthreads();
         if (DECAY && tid < D)
             sDB[63 * FS + tid] += sDBL[tid] + ex2(sB[63 * FS + tid]) * sDGL[tid];
-#pragma unroll 1
+        __nv_bfloat162 xr[4][2][P2];   // raw q, k of the warp's rows, loaded first
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+            const int r = w + 16 * rr;
+#pragma unroll
+            for (int which = 0; which < 2; ++which)
+#pragma unroll
+                for (int m = 0; m < P2; ++m)
+                    xr[rr][which][m] = r < len ? *reinterpret_cast<const __nv_bfloat162 *>(
+                                                     (which ? p.k : p.q) + tok(r) * D + 2 * lane + 64 * m)
+                                               : __floats2bfloat162_rn(0.0f, 0.0f);
+        }
+#pragma unroll
         for (int rr = 0; rr < 4; ++rr) {
             const int r = w + 16 * rr;
             if (r >= len) continue;
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
-                const bf16 *raw = (which ? p.k : p.q) + tok(r) * D;
                 const float *src = (which ? sFK : sFQ) + r * FS;
                 float x[CPL], d[CPL];
 #pragma unroll
                 for (int m = 0; m < P2; ++m) {
                     const int c = 2 * lane + 64 * m;
-                    const float2 xv = ld2(raw + c), dv = *reinterpret_cast<const float2 *>(src + c);
+                    const float2 xv = __bfloat1622float2(xr[rr][which][m]);
+                    const float2 dv = *reinterpret_cast<const float2 *>(src + c);
                     x[2 * m] = xv.x; x[2 * m + 1] = xv.y;
                     d[2 * m] = dv.x; d[2 * m + 1] = dv.y;
                 }
@@ -755,13 +781,22 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
             column_scan<D, FS>(sDB, sSeg, true);   // d log alpha_t = sum_{r >= t} db_r
             // log alpha = -softplus(x): dx = -d(log alpha) sigmoid(x)
             if (!scalar_gate) {
-                for (int e = tid; e < len * D / 2; e += kNT) {
-                    const int r = e / (D / 2), c = 2 * (e % (D / 2));
-                    const int64_t o = tok(r) * D + c;
-                    const float2 gg = ld2(p.gate_logits + o);
+                constexpr int NG = 64 * D / 2 / kNT;   // bf16 pairs per thread, loaded first
+                __nv_bfloat162 gg[NG];
+#pragma unroll
+                for (int k = 0; k < NG; ++k) {
+                    const int e = tid + k * kNT, r = e / (D / 2), c = 2 * (e % (D / 2));
+                    gg[k] = r < len ? *reinterpret_cast<const __nv_bfloat162 *>(p.gate_logits + tok(r) * D + c)
+                                    : __floats2bfloat162_rn(0.0f, 0.0f);
+                }
+#pragma unroll
+                for (int k = 0; k < NG; ++k) {
+                    const int e = tid + k * kNT, r = e / (D / 2), c = 2 * (e % (D / 2));
+                    if (r >= len) continue;
+                    const float2 gv = __bfloat1622float2(gg[k]);
                     const float2 dl = *reinterpret_cast<const float2 *>(sDB + r * FS + c);
-                    *reinterpret_cast<float2 *>(p.d_gate_logits + o) =
-                        make_float2(-dl.x * sigmoid_f(gg.x), -dl.y * sigmoid_f(gg.y));
+                    *reinterpret_cast<float2 *>(p.d_gate_logits + tok(r) * D + c) =
+                        make_float2(-dl.x * sigmoid_f(gv.x), -dl.y * sigmoid_f(gv.y));
                 }
             } else {
                 for (int r = w; r < len; r += kNT / 32) {
@@ -805,7 +840,7 @@ cudaError_t launch_delta_bwd_channel(const BwdChannelArgs &a, cudaStream_t s) {
     Params p{static_cast<const bf16 *>(a.q), static_cast<const bf16 *>(a.k),
              static_cast<const bf16 *>(a.v), static_cast<const bf16 *>(a.beta_logits),
              static_cast<const bf16 *>(a.gate_logits), static_cast<const bf16 *>(a.d_o),
-             a.table, a.states, a.dstates, a.du, a.tiles, a.dq, a.dk, a.dv, a.d_beta_logits,
+             a.table, a.states, a.dstates, a.dstates16, a.du, a.tiles, a.dq, a.dk, a.dv, a.d_beta_logits,
              a.d_gate_logits, a.n_tasks, a.H, a.scale, a.flags};
     const bool decay = a.gate_logits != nullptr;
     if (a.D == 64) return decay ? launch_d<64, true>(p, s) : launch_d<64, false>(p, s);

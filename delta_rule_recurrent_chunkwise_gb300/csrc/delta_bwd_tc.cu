@@ -36,7 +36,8 @@ struct ChainParams {
     const __nv_bfloat16 *d_o;
     const int32_t *cu;
     const float *d_final_S;
-    float *dstates;           // [slots][H][D][D]: dS' of every chunk
+    float *dstates;           // [slots][H][D][D]: dS' of every chunk (fp32; gated)
+    __nv_bfloat16 *dstates16; // [slots][H][D][D]: dS' of every chunk (bf16; no gate)
     __nv_bfloat16 *du;        // null, or [slots][H][64][D]: du of every chunk (bf16)
     float *d_init_S;
     unsigned *err;
@@ -170,12 +171,16 @@ __global__ void __launch_bounds__(ChainCfg<D>::NT, 1) delta_bwd_chain_kernel(Cha
         const PadView dSp{sDS, XS}, dU{sDU, XS};
         // 1. dS' of chunk c out (fp32) and in (bf16 operand); this chunk's dO in
         float *dst = p.dstates + ((slot0 + c) * H + h) * (int64_t)(D * D);
+        bf16 *dst16 = p.dstates16 + ((slot0 + c) * H + h) * (int64_t)(D * D);
 #pragma unroll
         for (int j = 0; j < NT_DS; ++j)
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
                 const int r = 16 * Rs + g + 8 * hr, col = ns + 8 * j + 2 * t;
-                *reinterpret_cast<float2 *>(dst + r * D + col) = make_float2(ds[j][2 * hr], ds[j][2 * hr + 1]);
+                if (p.gend)   // gated: fp32 (the per-chunk kernel also forms rowsum(dS' o S))
+                    *reinterpret_cast<float2 *>(dst + r * D + col) = make_float2(ds[j][2 * hr], ds[j][2 * hr + 1]);
+                else
+                    wmma16::st2(dst16 + r * D + col, ds[j][2 * hr], ds[j][2 * hr + 1]);
                 wmma16::st2(sDS + r * XS + col, ds[j][2 * hr], ds[j][2 * hr + 1]);
             }
         store_do(c);
@@ -236,7 +241,7 @@ __global__ void __launch_bounds__(ChainCfg<D>::NT, 1) delta_bwd_chain_kernel(Cha
 size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct ChunkWs {
-    size_t fwd, states, dstates, du, tiles, total;
+    size_t fwd, states, dstates, dstates16, du, tiles, total;
 };
 
 ChunkWs chunk_ws(int N, int ntok, int H, int D) {
@@ -245,9 +250,10 @@ ChunkWs chunk_ws(int N, int ntok, int H, int D) {
     w.fwd = a256(delta_tc_workspace_bytes(N, ntok, H, D, D, 64, true));
     w.states = a256(slots * H * D * D * sizeof(float));
     w.dstates = w.states;
+    w.dstates16 = a256(slots * H * D * D * 2);
     w.du = a256(slots * H * 64 * D * 2);   // du of every chunk, bf16
     w.tiles = a256(slots * H * 8192);   // T of every chunk (bf16 64 x 64)
-    w.total = w.fwd + w.states + w.dstates + w.du + w.tiles;
+    w.total = w.fwd + w.states + w.dstates + w.dstates16 + w.du + w.tiles;
     return w;
 }
 
@@ -278,8 +284,9 @@ cudaError_t launch_delta_backward_chunked(const BwdArgs &a, cudaStream_t s) {
     uint8_t *base = static_cast<uint8_t *>(a.workspace);
     float *states = reinterpret_cast<float *>(base + w.fwd);
     float *dstates = reinterpret_cast<float *>(base + w.fwd + w.states);
-    __nv_bfloat16 *du = reinterpret_cast<__nv_bfloat16 *>(base + w.fwd + w.states + w.dstates);
-    uint8_t *tiles = base + w.fwd + w.states + w.dstates + w.du;
+    __nv_bfloat16 *dstates16 = reinterpret_cast<__nv_bfloat16 *>(base + w.fwd + w.states + w.dstates);
+    __nv_bfloat16 *du = reinterpret_cast<__nv_bfloat16 *>(base + w.fwd + w.states + w.dstates + w.dstates16);
+    uint8_t *tiles = base + w.fwd + w.states + w.dstates + w.dstates16 + w.du;
     unsigned *err = device_error_word();
     if (!err) return cudaErrorInvalidValue;
 
@@ -296,7 +303,7 @@ cudaError_t launch_delta_backward_chunked(const BwdArgs &a, cudaStream_t s) {
     // 2. dS from the last chunk to the first
     const uint8_t *records = base + tile::Workspace::table_bytes(a.N, a.ntok);
     ChainParams cp{records, static_cast<const __nv_bfloat16 *>(a.d_o), a.cu_seqlens, a.d_final_S,
-                   dstates, du, a.d_init_S, err, a.H, a.ntok, a.scale,
+                   dstates, dstates16, du, a.d_init_S, err, a.H, a.ntok, a.scale,
                    a.gate_logits != nullptr};
     e = D == 64 ? launch_chain<64>(cp, a.N, a.H, s) : launch_chain<128>(cp, a.N, a.H, s);
     if (e != cudaSuccess) return e;
@@ -305,7 +312,7 @@ cudaError_t launch_delta_backward_chunked(const BwdArgs &a, cudaStream_t s) {
     const int64_t n_tasks = tile::Workspace::slots(a.N, a.ntok) * a.H;
     const int2 *table = reinterpret_cast<const int2 *>(base);
     BwdChannelArgs ca{a.q, a.k, a.v, a.beta_logits, a.gate_logits, a.d_o, table, states, dstates,
-                      du, tiles, a.dq, a.dk_out, a.dv_out, a.d_beta_logits,
+                      dstates16, du, tiles, a.dq, a.dk_out, a.dv_out, a.d_beta_logits,
                       a.gate_logits ? a.d_gate_logits : nullptr, n_tasks, a.H, D, a.scale, a.flags};
     return launch_delta_bwd_channel(ca, s);
 }

@@ -66,7 +66,8 @@ struct BwdChannelArgs {
     const void *q, *k, *v, *beta_logits, *gate_logits, *d_o;
     const int2 *table;        // [slots] {first token, length}
     const float *states;      // [slots][H][D][D] S at each chunk start
-    const float *dstates;     // [slots][H][D][D] dS' of each chunk
+    const float *dstates;     // [slots][H][D][D] dS' of each chunk (fp32; gated only)
+    const __nv_bfloat16 *dstates16;  // [slots][H][D][D] dS' of each chunk (bf16)
     const __nv_bfloat16 *du;  // [slots][H][64][D] du of each chunk (bf16)
     const uint8_t *tiles;     // [slots][H] T of each chunk, 8 KB bf16 swizzled tiles
     float *dq, *dk, *dv, *d_beta_logits, *d_gate_logits;
