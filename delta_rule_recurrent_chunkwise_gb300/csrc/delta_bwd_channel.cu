@@ -207,6 +207,11 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
     const int H = p.H;
     const bool scalar_gate = (p.flags & kGateScalar) != 0;
     const bool silu = (p.flags & kSiluQK) != 0;
+    // the additive rule: u = v (beta = 1, no delta term: W = 0, A = 0, T = I),
+    // so K enters only through the scores and the state update, and there
+    // is no beta gradient; wd (0 or 1) weighs every term of the delta part
+    const bool additive = (p.flags & kAdditive) != 0;
+    const float wd = additive ? 0.0f : 1.0f;
     // this warp's output block of a 64 x D product: rows 16R .. 16R + 15,
     // columns n0 .. n0 + D/4 - 1; of a 64 x 64 product: columns 16 cq ..
     const int R = w >> 2, cq = w & 3, n0 = cq * (D / 4);
@@ -286,7 +291,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                 rg[rr][m] = (DECAY && ok && !scalar_gate) ? *reinterpret_cast<bfp>(p.gate_logits + o + c) : z2;
             }
             rgs[rr] = (DECAY && ok && scalar_gate) ? __bfloat162float(p.gate_logits[tok(r)]) : 0.0f;
-            rbl[rr] = ok ? __bfloat162float(p.beta_logits[tok(r)]) : 0.0f;
+            rbl[rr] = (ok && !additive) ? __bfloat162float(p.beta_logits[tok(r)]) : 0.0f;
         }
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) {
@@ -326,7 +331,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
 #pragma unroll
             for (int m = 0; m < P2; ++m)
                 *reinterpret_cast<float2 *>(sB + r * FS + 2 * lane + 64 * m) = make_float2(lg[2 * m], lg[2 * m + 1]);
-            if (lane == 0) sBeta[r] = ok ? sigmoid_f(rbl[rr]) : 0.0f;
+            if (lane == 0) sBeta[r] = ok ? (additive ? 1.0f : sigmoid_f(rbl[rr])) : 0.0f;
         }
         if (tid < 64) sDBeta[tid] = 0.0f;
         if (tid < D) sDBL[tid] = sDGL[tid] = 0.0f;
@@ -360,7 +365,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
             }
             for (int e = tid; e < 64 * D / 4; e += kNT) {
                 const int r = e / (D / 4), c = 4 * (e % (D / 4));
-                const float be = sBeta[r];
+                const float be = wd * sBeta[r];   // Bk = 0 for the additive rule
                 const float2 k0 = ld2(sK + r * XS + c), k1 = ld2(sK + r * XS + c + 2);
                 const float4 b = *reinterpret_cast<const float4 *>(sB + r * FS + c);
                 st2(sBK + r * XS + c, be * k0.x * ex2d(b.x), be * k0.y * ex2d(b.y));
@@ -463,8 +468,8 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                     const float2 b = b2at(r, c), kv = ld2(sK + r * XS + c);
                     const float e0 = ex2d(b.x), e1 = ex2d(b.y);
                     const float dbk0 = -d[j][2 * hr], dbk1 = -d[j][2 * hr + 1];
-                    aKp[j][2 * hr] = sBeta[r] * e0 * dbk0;
-                    aKp[j][2 * hr + 1] = sBeta[r] * e1 * dbk1;
+                    aKp[j][2 * hr] = wd * sBeta[r] * e0 * dbk0;
+                    aKp[j][2 * hr + 1] = wd * sBeta[r] * e1 * dbk1;
                     const float sum = dbk0 * kv.x * e0 + dbk1 * kv.y * e1;
                     if (hr) s1 += sum;
                     else s0 += sum;
@@ -508,7 +513,8 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         // dbeta_r += sum_i dA_ri (K * K)_ri = -(1/beta_r) sum_j du_T_rj (A u)_rj,
         // and A u = u~ - u because (I + A) u = u~
         // (a beta that underflowed to 0 leaves the row's beta-logit gradient 0 anyway)
-        if (tid < len && sBeta[tid] > 0.0f) sDBeta[tid] -= (sRow[tid] - sRow[64 + tid]) / sBeta[tid];
+        if (tid < len && sBeta[tid] > 0.0f && !additive)
+            sDBeta[tid] -= (sRow[tid] - sRow[64 + tid]) / sBeta[tid];
         {
             float e2[2][4] = {}, f2[2][4] = {};
             if (cq <= R)
@@ -519,7 +525,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int i = 16 * cq + 8 * j + 2 * t;
-                const float s = p.scale, b0 = -sBeta[r0], b1 = -sBeta[r1];
+                const float s = p.scale, b0 = -wd * sBeta[r0], b1 = -wd * sBeta[r1];
                 st2(sGP + r0 * LS + i, i <= r0 ? s * e2[j][0] : 0.0f, i + 1 <= r0 ? s * e2[j][1] : 0.0f);
                 st2(sGP + r1 * LS + i, i <= r1 ? s * e2[j][2] : 0.0f, i + 1 <= r1 ? s * e2[j][3] : 0.0f);
                 st2(sGA + r0 * LS + i, i < r0 ? b0 * f2[j][0] : 0.0f, i + 1 < r0 ? b0 * f2[j][1] : 0.0f);
@@ -774,7 +780,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         }
         if (tid < len) {
             const float be = sBeta[tid];
-            p.d_beta_logits[tok(tid)] = sDBeta[tid] * be * (1.0f - be);
+            p.d_beta_logits[tok(tid)] = additive ? 0.0f : sDBeta[tid] * be * (1.0f - be);
         }
         if constexpr (DECAY) {
             __syncthreads();

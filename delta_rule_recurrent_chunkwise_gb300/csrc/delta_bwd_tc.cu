@@ -1,5 +1,5 @@
 // delta_bwd_tc.cu -- chunkwise backward pass of the delta rule (bf16 I/O,
-// dk = dv in {64, 128}, any gate): the forward pass with its records, the
+// dk = dv in {64, 128}, any gate, either update rule): the forward pass with its records, the
 // reverse chain over the chunks, then the per-chunk gradients
 // (delta_bwd_channel.cu).
 //
@@ -271,7 +271,7 @@ cudaError_t launch_chain(const ChainParams &cp, int N, int H, cudaStream_t s) {
 }  // namespace
 
 bool delta_bwd_chunked_supported(const BwdArgs &a) {
-    return a.bf16 && a.dk == a.dv && (a.dk == 64 || a.dk == 128) && !(a.flags & kAdditive);
+    return a.bf16 && a.dk == a.dv && (a.dk == 64 || a.dk == 128);
 }
 
 size_t delta_bwd_chunked_workspace_bytes(int N, int ntok, int H, int D) {

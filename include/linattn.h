@@ -242,7 +242,7 @@ la_status la_decode_step_slots(const void *q, const void *k, const void *v,
  * every chunk start, du per chunk; or, token-serial, checkpoints and
  * per-token column sums); LA_ERR_INVALID_ARG if smaller or missing.
  * dk, dv in {64, 128}.  Two forms, chosen from the arguments: chunkwise
- * (io = LA_BF16, dk = dv, without LA_ADDITIVE; any gate) -- the
+ * (io = LA_BF16, dk = dv; any gate, either update rule) -- the
  * tensor-core forward pass, a reverse pass over the chunks for the state
  * gradient, then every (chunk, head) in parallel; token-serial otherwise.
  * Sums over value columns inside a thread block use shared-memory atomics,

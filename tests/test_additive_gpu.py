@@ -87,3 +87,34 @@ def test_additive_backward(cuda_lib, gate):
     for n in ("dq", "dk", "dv", "d_gate_logits", "d_init_S"):
         assert rel_err(got[n].cpu().numpy(), ref[n]) <= 1e-4, n
     assert float(got["d_beta_logits"].abs().max()) == 0.0
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("gate", ["none", "channel", "scalar"])
+def test_additive_backward_chunkwise(cuda_lib, d, gate):
+    """bf16, dk = dv: the chunkwise backward (beta = 1, W = 0, T = I), ragged
+    lengths with an empty sequence, initial states and a final-state
+    gradient, against the oracle."""
+    la = cuda_lib
+    dev = torch.device("cuda")
+    inp = wl.prefill_inputs([150, 0, 70, 64], 2, d, d, torch.bfloat16, gate != "none", seed=84,
+                            init_state=True, scalar_gate=gate == "scalar")
+    f = la.LA_ADDITIVE | la.LA_L2NORM_K | (la.LA_GATE_SCALAR if gate == "scalar" else 0)
+    of = oracle.ADDITIVE | oracle.L2NORM_K | (oracle.SCALAR_GATE if gate == "scalar" else 0)
+    g = torch.Generator().manual_seed(85)
+    d_o = torch.randn(inp["v"].shape, generator=g).to(torch.bfloat16)
+    d_fS = torch.randn(inp["init_S"].shape, generator=g) * 0.1
+    gl = None if inp["gate_logits"] is None else inp["gate_logits"].to(dev)
+    t = {n: inp[n].to(dev) for n in ("q", "k", "v", "init_S")}
+    got = la.la_backward_delta(t["q"], t["k"], t["v"], None, gl, d_o.to(dev),
+                               inp["cu_seqlens"].to(dev), d_final_S=d_fS.to(dev), flags=f,
+                               init_S=t["init_S"], cu_seqlens_host=inp["cu_seqlens"])
+    assert la.la_check_device() == la.LA_OK
+    ref = oracle.delta_backward(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), None,
+                                None if inp["gate_logits"] is None else f64(inp["gate_logits"]),
+                                inp["cu_seqlens"].numpy(), f64(d_o), f64(d_fS), flags=of,
+                                init_S=f64(inp["init_S"]))
+    names = ("dq", "dk", "dv", "d_init_S") + (("d_gate_logits",) if gate != "none" else ())
+    for n in names:
+        assert rel_err(got[n].cpu().numpy(), ref[n]) <= TOL[torch.bfloat16], n
+    assert float(got["d_beta_logits"].abs().max()) == 0.0

@@ -145,3 +145,18 @@ def test_backward_channel_flags_and_scale_d128(cuda_lib):
     got = _run(la, inp, d_o, d_fS, flags, scale=0.6)
     ref = _oracle(inp, d_o, d_fS, oflags, scale=0.6)
     _compare(got, ref, TOL[torch.bfloat16])
+
+
+def test_backward_varlen_shape_sampled_heads(cuda_lib):
+    """The varlen prefill shape (65 536 packed tokens of seeded lengths, 16
+    heads, d = 128, a decay per key channel, bf16; ragged last chunks): the
+    whole backward on the GPU, the oracle on one head of every sequence."""
+    la = cuda_lib
+    w = wl.workload("varlen_prefill")
+    inp = wl.inputs_for(w, seed=0, init_state=True)
+    d_o, d_fS = _grad_inputs(inp, w.dtype, seed=80)
+    got = _run(la, inp, d_o, d_fS, la.LA_L2NORM_K)
+    heads = [11]
+    ref = _oracle(inp, d_o, d_fS, oracle.L2NORM_K, heads=heads)
+    sub = {n: (None if v is None else v[:, heads]) for n, v in got.items()}
+    _compare(sub, ref, TOL[w.dtype])
