@@ -255,10 +255,11 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         if (len <= 0) continue;
         auto tok = [&](int r) { return ((int64_t)(t0 + r) * H + h); };
         bf16 *sDO = reinterpret_cast<bf16 *>(U + L::O_DO), *sDU = reinterpret_cast<bf16 *>(U + L::O_DU);
+        bf16 *sV = reinterpret_cast<bf16 *>(U + L::O_UT);   // V, until u~ replaces it in place
 
         // The benchmark's bf16 operands go straight to shared memory by async
         // copies, in flight through phase 0: T (8 KB, one 16-byte unit per
-        // thread), dO (rows past the end zero) and du, 64 x D each.
+        // thread), dO and V (rows past the end zero) and du, 64 x D each.
         static_assert(kNT * 16 == 8192, "one unit of T per thread");
         cp_async16(smem + L::TR + tid * 16, p.tiles + (slot * H + h) * (int64_t)8192 + tid * 16, true);
         {
@@ -267,6 +268,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
             for (int k = 0; k < 64 * D / 8 / kNT; ++k) {
                 const int e = tid + k * kNT, r = e / (D / 8), c = 8 * (e % (D / 8));
                 cp_async16(sDO + r * XS + c, p.d_o + tok(r < len ? r : 0) * D + c, r < len);
+                cp_async16(sV + r * XS + c, p.v + tok(r < len ? r : 0) * D + c, r < len);
                 cp_async16(sDU + r * XS + c, gdu + r * D + c, true);
             }
         }
@@ -411,13 +413,13 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                 st2(sDUT + r1 * XS + c, dut[j][2], dut[j][3]);
                 // dV = beta du_T; dbeta += du_T . v
                 if (r0 < len) {
-                    const float2 v = ld2(p.v + tok(r0) * D + c);
+                    const float2 v = ld2(sV + r0 * XS + c);
                     s0 += dut[j][0] * v.x + dut[j][1] * v.y;
                     *reinterpret_cast<float2 *>(p.dv + tok(r0) * D + c) =
                         make_float2(sBeta[r0] * dut[j][0], sBeta[r0] * dut[j][1]);
                 }
                 if (r1 < len) {
-                    const float2 v = ld2(p.v + tok(r1) * D + c);
+                    const float2 v = ld2(sV + r1 * XS + c);
                     s1 += dut[j][2] * v.x + dut[j][3] * v.y;
                     *reinterpret_cast<float2 *>(p.dv + tok(r1) * D + c) =
                         make_float2(sBeta[r1] * dut[j][2], sBeta[r1] * dut[j][3]);
@@ -435,8 +437,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
                 const int c = n0 + 8 * j + 2 * t;
-                const float2 v0 = r0 < len ? ld2(p.v + tok(r0) * D + c) : make_float2(0.f, 0.f);
-                const float2 v1 = r1 < len ? ld2(p.v + tok(r1) * D + c) : make_float2(0.f, 0.f);
+                const float2 v0 = ld2(sV + r0 * XS + c), v1 = ld2(sV + r1 * XS + c);   // (zero past the end)
                 const float u00 = sBeta[r0] * v0.x - d[j][0], u01 = sBeta[r0] * v0.y - d[j][1];
                 const float u10 = sBeta[r1] * v1.x - d[j][2], u11 = sBeta[r1] * v1.y - d[j][3];
                 st2(sUT + r0 * XS + c, u00, u01);
