@@ -160,3 +160,22 @@ def test_backward_varlen_shape_sampled_heads(cuda_lib):
     ref = _oracle(inp, d_o, d_fS, oracle.L2NORM_K, heads=heads)
     sub = {n: (None if v is None else v[:, heads]) for n, v in got.items()}
     _compare(sub, ref, TOL[w.dtype])
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_many_short_sequences(cuda_lib, d):
+    """130 sequences of 1..100 tokens (most shorter than a chunk, some
+    spanning two, some empty), scalar gate at d = 64 and per-channel at 128:
+    every chunk slot and tail of the chunkwise backward."""
+    la = cuda_lib
+    g = torch.Generator().manual_seed(86)
+    lens = torch.randint(0, 101, (130,), generator=g).tolist()
+    scalar = d == 64
+    inp = wl.prefill_inputs(lens, 2, d, d, torch.bfloat16, True, seed=87, init_state=True,
+                            scalar_gate=scalar)
+    d_o, d_fS = _grad_inputs(inp, torch.bfloat16, seed=88)
+    flags = la.LA_L2NORM_K | (la.LA_GATE_SCALAR if scalar else 0)
+    oflags = oracle.L2NORM_K | (oracle.SCALAR_GATE if scalar else 0)
+    got = _run(la, inp, d_o, d_fS, flags)
+    ref = _oracle(inp, d_o, d_fS, oflags)
+    _compare(got, ref, TOL[torch.bfloat16])
