@@ -59,7 +59,17 @@ namespace {
 
 using tile::C;
 using bf16 = __nv_bfloat16;
-constexpr int kNT = 512;              // threads per CTA: 16 warps
+// Threads per CTA and CTAs per SM: at d = 128 one CTA of 16 warps per SM;
+// at d = 64 two CTAs of 8 warps, so that one task's barrier waits overlap
+// the other's work (114.7 KB of shared memory and 256 x 128 registers each).
+// The warps tile a 64 x D output as 4 row blocks x CG column groups.
+template <int D>
+struct Cfg {
+    static constexpr int NTH = D == 64 ? 256 : 512, CTAS = D == 64 ? 2 : 1;
+    static constexpr int NW = NTH / 32, CG = NW / 4;
+    static constexpr int NT = D / (8 * CG);   // n8 tiles of a warp's 16 x D/CG block
+    static constexpr int RPW = 64 / NW;       // rows per warp in row-wise passes
+};
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ------------------------------------------------------------ warp products
@@ -129,8 +139,8 @@ struct Lay {
     static constexpr int DBL = DBETA + 256;              // fp32 [D]: d b_L
     static constexpr int DGL = DBL + 4 * D;              // fp32 [D]: d e^{b_L}
     static constexpr int MF = DGL + 4 * D;               // fp32 [6][D]: middle factors
-    static constexpr int SEG = MF + 24 * D;              // fp32 [kNT / D][D]: scan totals
-    static constexpr int ROW = SEG + 4 * kNT;            // fp32 [2][64]: du_T . u~, du_T . u
+    static constexpr int SEG = MF + 24 * D;              // fp32 [threads / D][D]: scan totals
+    static constexpr int ROW = SEG + 4 * Cfg<D>::NTH;    // fp32 [2][64]: du_T . u~, du_T . u
     static constexpr int U = ROW + 512;
     // union region, phases 2-3 (the largest)
     static constexpr int O_DO = 0, O_DU = XB, O_DUT = 2 * XB, O_UT = 3 * XB, O_BK = 4 * XB;
@@ -142,6 +152,7 @@ struct Lay {
     static_assert(LB <= XB, "dP and G_A fit in a 64 x D slot");
 };
 static_assert(Lay<128>::BYTES <= 232448, "shared memory at d = 128");
+static_assert(2 * (Lay<64>::BYTES + 1024) <= 233472, "two CTAs per SM at d = 64");
 
 struct Params {
     const bf16 *q, *k, *v, *beta_logits, *gate_logits, *d_o;
@@ -160,9 +171,9 @@ struct Params {
 
 // Inclusive prefix sums down the 64 rows of each of the D columns of
 // x (fp32 [64][LDX]), in place; reverse = suffix sums.  All threads of the CTA.
-template <int D, int LDX>
+template <int D, int LDX, int NTH>
 __device__ __forceinline__ void column_scan(float *x, float *seg, bool reverse) {
-    constexpr int NS = kNT / D, RS = 64 / NS;   // segments per column, rows per segment
+    constexpr int NS = NTH / D, RS = 64 / NS;   // segments per column, rows per segment
     const int c = threadIdx.x % D, s = threadIdx.x / D;
     float run = 0.0f;
 #pragma unroll
@@ -187,12 +198,13 @@ __device__ __forceinline__ void column_scan(float *x, float *seg, bool reverse) 
 // plain products (diagonal blocks included, on the tensor cores) and there
 // is no decay gradient.
 template <int D, bool DECAY>
-__global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
+__global__ void __launch_bounds__(Cfg<D>::NTH, Cfg<D>::CTAS) delta_bwd_channel_kernel(Params p) {
     using L = Lay<D>;
+    constexpr int kNT = Cfg<D>::NTH, NW = Cfg<D>::NW, CG = Cfg<D>::CG, RPW = Cfg<D>::RPW;
     constexpr int XS = L::XS, LS = L::LS, FS = L::FS;
     constexpr int CPL = D / 32;          // channels per lane in row-wise passes
     constexpr int P2 = D / 64;           // ... as pairs 2 lane + 64 m
-    constexpr int NT = D / 32;           // n8 tiles of a warp's 16 x D/4 output block
+    constexpr int NT = Cfg<D>::NT;       // n8 tiles of a warp's 16 x D/CG output block
     extern __shared__ __align__(1024) uint8_t smem[];
     bf16 *sQ = reinterpret_cast<bf16 *>(smem + L::Q), *sK = reinterpret_cast<bf16 *>(smem + L::K);
     float *sB = reinterpret_cast<float *>(smem + L::B);
@@ -213,8 +225,8 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
     const bool additive = (p.flags & kAdditive) != 0;
     const float wd = additive ? 0.0f : 1.0f;
     // this warp's output block of a 64 x D product: rows 16R .. 16R + 15,
-    // columns n0 .. n0 + D/4 - 1; of a 64 x 64 product: columns 16 cq ..
-    const int R = w >> 2, cq = w & 3, n0 = cq * (D / 4);
+    // columns n0 .. n0 + D/CG - 1; of a 64 x 64 product: columns 64/CG cq ..
+    const int R = w / CG, cq = w % CG, n0 = cq * (D / CG);
     const int r0 = 16 * R + g, r1 = r0 + 8;   // this lane's two output rows
 
     // inputs of task nt into L2 (one 128-byte line per request): the token
@@ -260,8 +272,11 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         // The benchmark's bf16 operands go straight to shared memory by async
         // copies, in flight through phase 0: T (8 KB, one 16-byte unit per
         // thread), dO and V (rows past the end zero) and du, 64 x D each.
-        static_assert(kNT * 16 == 8192, "one unit of T per thread");
-        cp_async16(smem + L::TR + tid * 16, p.tiles + (slot * H + h) * (int64_t)8192 + tid * 16, true);
+#pragma unroll
+        for (int k = 0; k < 512 / kNT; ++k) {
+            const int u = tid + k * kNT;
+            cp_async16(smem + L::TR + u * 16, p.tiles + (slot * H + h) * (int64_t)8192 + u * 16, true);
+        }
         {
             const bf16 *gdu = p.du + (slot * H + h) * (int64_t)(64 * D);
 #pragma unroll
@@ -276,12 +291,12 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         // ---- 0. q^, k^ (silu, L2 norm), beta, log2 alpha; b = prefix sums.
         // Lanes take channel pairs 2 lane + 64 m; the warp's four rows are
         // loaded first (bf16 pairs kept packed).
-        __nv_bfloat162 rq[4][P2], rk[4][P2], rg[4][P2];
-        float rgs[4], rbl[4];
+        __nv_bfloat162 rq[RPW][P2], rk[RPW][P2], rg[RPW][P2];
+        float rgs[RPW], rbl[RPW];
         const __nv_bfloat162 z2 = __floats2bfloat162_rn(0.0f, 0.0f);
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-            const int r = w + 16 * rr;
+        for (int rr = 0; rr < RPW; ++rr) {
+            const int r = w + NW * rr;
             const bool ok = r < len;
             const int64_t o = tok(ok ? r : 0) * D;
             using bfp = const __nv_bfloat162 *;
@@ -296,8 +311,8 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
             rbl[rr] = (ok && !additive) ? __bfloat162float(p.beta_logits[tok(r)]) : 0.0f;
         }
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-            const int r = w + 16 * rr;
+        for (int rr = 0; rr < RPW; ++rr) {
+            const int r = w + NW * rr;
             const bool ok = r < len;
             float xq[CPL], xk[CPL], lg[CPL];
             const float gs = (DECAY && ok && scalar_gate) ? log_decay_f(rgs[rr]) : 0.0f;
@@ -338,7 +353,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         if (tid < 64) sDBeta[tid] = 0.0f;
         if (tid < D) sDBL[tid] = sDGL[tid] = 0.0f;
         __syncthreads();
-        if constexpr (DECAY) column_scan<D, FS>(sB, sSeg, false);
+        if constexpr (DECAY) column_scan<D, FS, kNT>(sB, sSeg, false);
         prefetch_task(task + gridDim.x);
         // sB[r][c] = b_rc / ln 2 from here on; b at the token before block R
         auto bs = [&](int Rb, int c) { return Rb == 0 ? 0.0f : sB[(16 * Rb - 1) * FS + c]; };
@@ -517,20 +532,25 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         if (tid < len && sBeta[tid] > 0.0f && !additive)
             sDBeta[tid] -= (sRow[tid] - sRow[64 + tid]) / sBeta[tid];
         {
-            float e2[2][4] = {}, f2[2][4] = {};
-            if (cq <= R)
-                for (int k = 0; k < D; k += 16) {
-                    mma_step<false, true>(e2, sDO, XS, sU, XS, 16 * R, 16 * cq, k);
-                    mma_step<false, true>(f2, sDUT, XS, sU, XS, 16 * R, 16 * cq, k);
-                }
+            // 64 x 64 products: this warp's columns in 16-wide steps
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int i = 16 * cq + 8 * j + 2 * t;
-                const float s = p.scale, b0 = -wd * sBeta[r0], b1 = -wd * sBeta[r1];
-                st2(sGP + r0 * LS + i, i <= r0 ? s * e2[j][0] : 0.0f, i + 1 <= r0 ? s * e2[j][1] : 0.0f);
-                st2(sGP + r1 * LS + i, i <= r1 ? s * e2[j][2] : 0.0f, i + 1 <= r1 ? s * e2[j][3] : 0.0f);
-                st2(sGA + r0 * LS + i, i < r0 ? b0 * f2[j][0] : 0.0f, i + 1 < r0 ? b0 * f2[j][1] : 0.0f);
-                st2(sGA + r1 * LS + i, i < r1 ? b1 * f2[j][2] : 0.0f, i + 1 < r1 ? b1 * f2[j][3] : 0.0f);
+            for (int jp = 0; jp < 64 / (16 * CG); ++jp) {
+                const int c0 = (64 / CG) * cq + 16 * jp;
+                float e2[2][4] = {}, f2[2][4] = {};
+                if (c0 <= 16 * R)   // blocks right of the diagonal block are zero
+                    for (int k = 0; k < D; k += 16) {
+                        mma_step<false, true>(e2, sDO, XS, sU, XS, 16 * R, c0, k);
+                        mma_step<false, true>(f2, sDUT, XS, sU, XS, 16 * R, c0, k);
+                    }
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int i = c0 + 8 * j + 2 * t;
+                    const float s = p.scale, b0 = -wd * sBeta[r0], b1 = -wd * sBeta[r1];
+                    st2(sGP + r0 * LS + i, i <= r0 ? s * e2[j][0] : 0.0f, i + 1 <= r0 ? s * e2[j][1] : 0.0f);
+                    st2(sGP + r1 * LS + i, i <= r1 ? s * e2[j][2] : 0.0f, i + 1 <= r1 ? s * e2[j][3] : 0.0f);
+                    st2(sGA + r0 * LS + i, i < r0 ? b0 * f2[j][0] : 0.0f, i + 1 < r0 ? b0 * f2[j][1] : 0.0f);
+                    st2(sGA + r1 * LS + i, i < r1 ? b1 * f2[j][2] : 0.0f, i + 1 < r1 ? b1 * f2[j][3] : 0.0f);
+                }
             }
             if constexpr (DECAY) {
                 // dS' in, and d e^{b_L}_c = sum_j dS'_cj S_cj: row c is D/4 float4
@@ -744,10 +764,10 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         __syncthreads();
         if (DECAY && tid < D)
             sDB[63 * FS + tid] += sDBL[tid] + ex2(sB[63 * FS + tid]) * sDGL[tid];
-        __nv_bfloat162 xr[4][2][P2];   // raw q, k of the warp's rows, loaded first
+        __nv_bfloat162 xr[RPW][2][P2];   // raw q, k of the warp's rows, loaded first
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-            const int r = w + 16 * rr;
+        for (int rr = 0; rr < RPW; ++rr) {
+            const int r = w + NW * rr;
 #pragma unroll
             for (int which = 0; which < 2; ++which)
 #pragma unroll
@@ -757,8 +777,8 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                                                : __floats2bfloat162_rn(0.0f, 0.0f);
         }
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-            const int r = w + 16 * rr;
+        for (int rr = 0; rr < RPW; ++rr) {
+            const int r = w + NW * rr;
             if (r >= len) continue;
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
@@ -785,7 +805,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
         }
         if constexpr (DECAY) {
             __syncthreads();
-            column_scan<D, FS>(sDB, sSeg, true);   // d log alpha_t = sum_{r >= t} db_r
+            column_scan<D, FS, kNT>(sDB, sSeg, true);   // d log alpha_t = sum_{r >= t} db_r
             // log alpha = -softplus(x): dx = -d(log alpha) sigmoid(x)
             if (!scalar_gate) {
                 constexpr int NG = 64 * D / 2 / kNT;   // bf16 pairs per thread, loaded first
@@ -806,7 +826,7 @@ __global__ void __launch_bounds__(kNT, 1) delta_bwd_channel_kernel(Params p) {
                         make_float2(-dl.x * sigmoid_f(gv.x), -dl.y * sigmoid_f(gv.y));
                 }
             } else {
-                for (int r = w; r < len; r += kNT / 32) {
+                for (int r = w; r < len; r += NW) {
                     float s = 0.0f;
 #pragma unroll
                     for (int m = 0; m < P2; ++m) {
@@ -833,9 +853,10 @@ cudaError_t launch_d(const Params &p, cudaStream_t s) {
     if ((e = cudaFuncSetAttribute(delta_bwd_channel_kernel<D, DECAY>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
         return e;
-    const int64_t grid = p.n_tasks < sms ? p.n_tasks : sms;
+    const int64_t slots = (int64_t)sms * Cfg<D>::CTAS;
+    const int64_t grid = p.n_tasks < slots ? p.n_tasks : slots;
     if (grid > 0) {
-        delta_bwd_channel_kernel<D, DECAY><<<(unsigned)grid, kNT, bytes, s>>>(p);
+        delta_bwd_channel_kernel<D, DECAY><<<(unsigned)grid, Cfg<D>::NTH, bytes, s>>>(p);
         e = cudaGetLastError();
     }
     return e;
