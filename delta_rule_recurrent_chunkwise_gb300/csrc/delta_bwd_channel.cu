@@ -201,6 +201,7 @@ template <int D, bool DECAY>
 __global__ void __launch_bounds__(Cfg<D>::NTH, Cfg<D>::CTAS) delta_bwd_channel_kernel(Params p) {
     using L = Lay<D>;
     constexpr int kNT = Cfg<D>::NTH, NW = Cfg<D>::NW, CG = Cfg<D>::CG, RPW = Cfg<D>::RPW;
+    static_assert(kNT % D == 0, "a thread's 16-byte units of S and dS' lie in one row");
     constexpr int XS = L::XS, LS = L::LS, FS = L::FS;
     constexpr int CPL = D / 32;          // channels per lane in row-wise passes
     constexpr int P2 = D / 64;           // ... as pairs 2 lane + 64 m
@@ -278,13 +279,14 @@ __global__ void __launch_bounds__(Cfg<D>::NTH, Cfg<D>::CTAS) delta_bwd_channel_k
             cp_async16(smem + L::TR + u * 16, p.tiles + (slot * H + h) * (int64_t)8192 + u * 16, true);
         }
         {
+            // (du by 16-byte units, unit e = row e % 64 of column group e / 64)
             const bf16 *gdu = p.du + (slot * H + h) * (int64_t)(64 * D);
 #pragma unroll
             for (int k = 0; k < 64 * D / 8 / kNT; ++k) {
                 const int e = tid + k * kNT, r = e / (D / 8), c = 8 * (e % (D / 8));
                 cp_async16(sDO + r * XS + c, p.d_o + tok(r < len ? r : 0) * D + c, r < len);
                 cp_async16(sV + r * XS + c, p.v + tok(r < len ? r : 0) * D + c, r < len);
-                cp_async16(sDU + r * XS + c, gdu + r * D + c, true);
+                cp_async16(sDU + (e % 64) * XS + 8 * (e / 64), gdu + 8 * e, true);
             }
         }
 
@@ -372,14 +374,12 @@ __global__ void __launch_bounds__(Cfg<D>::NTH, Cfg<D>::CTAS) delta_bwd_channel_k
         const float *gS = p.states + (slot * H + h) * (int64_t)(D * D);
         const float *gDS = p.dstates + (slot * H + h) * (int64_t)(D * D);
         {
-            // S: every load of this thread first, then the bf16 stores
+            // S: every load of this thread first, then the bf16 stores (S by
+            // 16-byte units: unit e is row e % D of column group e / D)
             constexpr int NS = D * D / 4 / kNT;
             float4 sv[NS];
 #pragma unroll
-            for (int k = 0; k < NS; ++k) {
-                const int e = tid + k * kNT;
-                sv[k] = *reinterpret_cast<const float4 *>(gS + (e / (D / 4)) * D + 4 * (e % (D / 4)));
-            }
+            for (int k = 0; k < NS; ++k) sv[k] = reinterpret_cast<const float4 *>(gS)[tid + k * kNT];
             for (int e = tid; e < 64 * D / 4; e += kNT) {
                 const int r = e / (D / 4), c = 4 * (e % (D / 4));
                 const float be = wd * sBeta[r];   // Bk = 0 for the additive rule
@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(Cfg<D>::NTH, Cfg<D>::CTAS) delta_bwd_channel_k
             }
 #pragma unroll
             for (int k = 0; k < NS; ++k) {
-                const int e = tid + k * kNT, r = e / (D / 4), c = 4 * (e % (D / 4));
+                const int e = tid + k * kNT, r = e % D, c = 4 * (e / D);
                 st2(sS + r * XS + c, sv[k].x, sv[k].y);
                 st2(sS + r * XS + c + 2, sv[k].z, sv[k].w);
             }
@@ -506,8 +506,8 @@ __global__ void __launch_bounds__(Cfg<D>::NTH, Cfg<D>::CTAS) delta_bwd_channel_k
             const bf16 *gds16 = p.dstates16 + (slot * H + h) * (int64_t)(D * D);
 #pragma unroll
             for (int k = 0; k < D * D / 8 / kNT; ++k) {
-                const int e = tid + k * kNT, r = e / (D / 8), c = 8 * (e % (D / 8));
-                cp_async16(sS + r * XS + c, gds16 + r * D + c, true);
+                const int e = tid + k * kNT;   // row e % D of column group e / D
+                cp_async16(sS + (e % D) * XS + 8 * (e / D), gds16 + 8 * e, true);
             }
         }
         {
@@ -553,19 +553,20 @@ __global__ void __launch_bounds__(Cfg<D>::NTH, Cfg<D>::CTAS) delta_bwd_channel_k
                 }
             }
             if constexpr (DECAY) {
-                // dS' in, and d e^{b_L}_c = sum_j dS'_cj S_cj: row c is D/4 float4
-                // units on D/4 consecutive lanes
+                // dS' in, and d e^{b_L}_c = sum_j dS'_cj S_cj.  Both come by
+                // 16-byte units (unit u: row u % D, columns 4 (u / D) ..): the
+                // thread's units all lie in row tid % D (the thread count is a
+                // multiple of D), whose kNT / D threads add their sums
+                float acc = 0.0f;
                 for (int u = tid; u < D * D / 4; u += kNT) {
-                    const int c = u / (D / 4), j = 4 * (u % (D / 4));
-                    const float4 ds = *reinterpret_cast<const float4 *>(gDS + c * D + j);
-                    const float4 sv = *reinterpret_cast<const float4 *>(gS + c * D + j);
-                    float acc = ds.x * sv.x + ds.y * sv.y + ds.z * sv.z + ds.w * sv.w;
-#pragma unroll
-                    for (int o = D / 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                    if (u % (D / 4) == 0) sDGL[c] = acc;
+                    const int c = u % D, j = 4 * (u / D);
+                    const float4 ds = reinterpret_cast<const float4 *>(gDS)[u];
+                    const float4 sv = reinterpret_cast<const float4 *>(gS)[u];
+                    acc += ds.x * sv.x + ds.y * sv.y + ds.z * sv.z + ds.w * sv.w;
                     st2(sS + c * XS + j, ds.x, ds.y);
                     st2(sS + c * XS + j + 2, ds.z, ds.w);
                 }
+                atomicAdd(&sDGL[tid % D], acc);
             }
         }
         cp_async_wait_all();   // dS' in (made visible to all by the barrier below)

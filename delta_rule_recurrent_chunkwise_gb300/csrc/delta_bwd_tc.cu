@@ -15,9 +15,9 @@
 //   the tensor-core forward pass, keeping its records (-W, Q e^b, U, K~, Aq,
 //     e^{b_L}), T of every chunk, and the state at every chunk start;
 //   delta_bwd_chain_kernel   one CTA per (head, sequence): dS from the last
-//                            chunk to the first, dS in registers, the record
-//                            tiles read in place; stores dS' and du of every
-//                            chunk;
+//                            chunk to the first on tcgen05, dS in TMEM, the
+//                            record tiles as the products' operands in place;
+//                            stores dS' and du of every chunk;
 //   delta_bwd_channel_kernel every (chunk, head) in parallel: the gradients of
 //                            the chunk's inputs and the prologue's derivatives.
 
@@ -25,7 +25,6 @@
 #include "delta_tc.h"
 #include "launch.h"
 #include "tc_tile.cuh"
-#include "warp_mma.cuh"
 
 namespace la {
 namespace {
@@ -36,57 +35,80 @@ struct ChainParams {
     const __nv_bfloat16 *d_o;
     const int32_t *cu;
     const float *d_final_S;
-    float *dstates;           // [slots][H][D][D]: dS' of every chunk (fp32; gated)
-    __nv_bfloat16 *dstates16; // [slots][H][D][D]: dS' of every chunk (bf16; no gate)
-    __nv_bfloat16 *du;        // null, or [slots][H][64][D]: du of every chunk (bf16)
+    // per (slot, head), by 16-byte units (tile::unit_at):
+    float *dstates;           // [slots][H] D x D: dS' of every chunk (fp32; gated)
+    __nv_bfloat16 *dstates16; // [slots][H] D x D: dS' of every chunk (bf16; no gate)
+    __nv_bfloat16 *du;        // null, or [slots][H] 64 x D: du of every chunk (bf16)
     float *d_init_S;
     unsigned *err;
     int H, ntok;
     float scale;
-    bool gend;                // records carry e^{b_L} (gated); else it is 1
 };
 
-// One CTA of 16 warps per (head, sequence).  Shared memory (bytes): two
-// record buffers (the operands of one chunk copied from its record: [-W ;
-// Q e^b] as a 128-row swizzled tile, K e^{b_L - b} as a 64-row one, Aq, and
-// e^{b_L}), two buffers of scale dO, the bf16 copy of dS' and du, barriers.
+// One CTA of 11 warps per (head, sequence).  Shared memory (bytes, from a
+// 1024-aligned base): NB record buffers (the operands of one chunk copied
+// from its record: [-W ; Q e^b] as a 128-row swizzled tile, K e^{b_L - b}
+// as a 64-row one, Aq, e^{b_L}), NB bf16 tiles of scale dO, the bf16
+// operand tiles of dS' and du, barriers.  TMEM: dS (fp32, M = D rows) in
+// columns 0 .. D-1, du (M = 64) in columns D .. 2D-1.
 template <int D> struct ChainCfg {
-    static constexpr int NT = 512;
-    static constexpr int XS = D + 8;                      // bf16 stride of dO, du, dS'
-    static constexpr int WQB = 128 * D * 2, KB = 64 * D * 2, AQB = 64 * 64 * 2, GB = 4 * D;
-    static constexpr int TX = WQB + KB + AQB + GB;        // bytes a record copy delivers
-    static constexpr int BUF = (TX + 1023) & ~1023;
-    static constexpr int DO = 2 * BUF, DOB = 64 * XS * 2;
-    static constexpr int DS = DO + 2 * DOB, DU = DS + D * XS * 2, BARS = DU + 64 * XS * 2;
-    static constexpr int BYTES = BARS + 64;
-    // warp tiles: du (64 x D) in 4 row blocks x 4 column groups; dS (D x D)
-    // in D/16 row blocks x 16/(D/16) column groups
-    static constexpr int NT_DU = D / 32;
-    static constexpr int CG = 16 / (D / 16), NT_DS = D / CG / 8;
-    static constexpr int DO_UNITS = 64 * D / 8 / NT;     // 16-byte units of dO per thread
+    static constexpr int NB = D == 64 ? 4 : 2;            // record and dO buffers
+    static constexpr int NT = 11 * 32;
+    static constexpr int W_DO = 8, N_DO = 2, W_ISSUER = 10;   // dO warps 8, 9; issuing warp
+    static constexpr uint32_t WQB = 128 * D * 2, KB = 64 * D * 2, AQB = 64 * 64 * 2, GB = 4 * D;
+    static constexpr uint32_t TX = WQB + KB + AQB + GB;   // bytes a record copy delivers
+    static constexpr uint32_t BUF = (TX + 1023) & ~1023u;
+    static constexpr uint32_t DOB = 64 * D * 2;           // scale dO, bf16 [64][D] tile
+    static constexpr uint32_t DO = NB * BUF;
+    static constexpr uint32_t DS = DO + NB * DOB;         // dS', bf16 [D][D] tile
+    static constexpr uint32_t DU = DS + D * D * 2;        // du, bf16 [64][D] tile
+    static constexpr uint32_t BARS = DU + 64 * D * 2;
+    static constexpr uint32_t BYTES = BARS + 256;
+    static constexpr uint32_t TDS = 0, TDU = D, TCOLS = 2 * D;
+    static constexpr int DO_UNITS = 64 * D / 8 / (32 * N_DO);   // 16-byte units of dO per staging thread
+    static_assert(BYTES + 1024 <= 232448, "shared memory budget");
 };
 
-// Reverse pass over the chunks of one (head, sequence).  dS (fp32) stays in
-// registers for the whole sequence; per chunk c, last to first:
-//   store dS' (= dS) of chunk c;  du = Aq^T dO' + K~ dS';
-//   dS = Diag(e^{b_L}) dS' + (Q e^b)^T dO' + (-W)^T du
-// with bf16 operands (dS' and du rounded for the products only) read by
-// ldmatrix straight from the record tiles.  Chunk c - 1's record arrives by
-// bulk copy into the other buffer while chunk c computes.
-template <int D>
+// mbarrier slots: per step, then per buffer (REC: record copy landed; DO:
+// dO tile written; FREE: every product reading the buffer has completed)
+enum : int {
+    CB_DSREADY = 0, CB_DU, CB_DUREADY, CB_DS, CB_END, CB_REC0,
+    CB_DO0 = CB_REC0 + 4, CB_FREE0 = CB_DO0 + 4, CB_COUNT = CB_FREE0 + 4
+};
+
+// Reverse pass over the chunks of one (head, sequence) on the tensor cores.
+// Step i handles chunk c = nc - 1 - i; dS (fp32) stays in TMEM throughout:
+//   readback warps  dS' (TMEM) -> global (fp32 gated, else bf16) and its bf16
+//                   operand tile; gated: dS' *= e^{b_L} back into TMEM
+//   issuer          du = Aq^T dO' (ahead, as soon as the chunk's record and
+//                   dO' are in) + K~ dS'                          commit "du"
+//                   dS += (Q e^b)^T dO'
+//   readback warps  du (TMEM) -> bf16 operand tile and global
+//   issuer          dS += (-W)^T du                               commit "ds"
+// with dO' = scale dO rounded to bf16 by two staging warps, up to NB - 1
+// chunks ahead.  Only dS' -> du -> dS is sequential: two product round trips
+// per chunk.  Every mbarrier phase is chained so that no waiter can fall two
+// phases behind: a phase of DSREADY / DUREADY / DU / DS needs the previous
+// phase's waiter to have gone on; a buffer's REC / DO / FREE phase for use
+// u + 1 needs its use u to have been waited for.  Every wait is bounded.
+// (11 warps, not 13 with four staging warps: an SM sub-partition's 16 K
+// registers then hold three warps of up to 168 registers, where the gated
+// d = 128 readback -- a row's 64 dS' columns and their scaled copies --
+// needs more than the 128 that four warps would leave.)
+template <int D, bool GATED>
 __global__ void __launch_bounds__(ChainCfg<D>::NT, 1) delta_bwd_chain_kernel(ChainParams p) {
     using namespace tc;
+    using namespace tile;
     using L = ChainCfg<D>;
-    using Rec = tile::Record<D>;
-    using wmma16::PadView;
-    using wmma16::RsView;
-    using bf16 = __nv_bfloat16;
-    constexpr int XS = L::XS, NT_DU = L::NT_DU, NT_DS = L::NT_DS;
-    extern __shared__ __align__(1024) uint8_t smem[];
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BARS);
-    bf16 *sDS = reinterpret_cast<bf16 *>(smem + L::DS), *sDU = reinterpret_cast<bf16 *>(smem + L::DU);
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    const int g = lane >> 2, t = lane & 3;
+    using Rec = Record<D>;
+    constexpr int NB = L::NB, HALF = D / 2;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::BARS);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + CB_COUNT);
+    uint8_t *sds = sm + L::DS, *sdu = sm + L::DU;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, qd = warp & 3;
     const int h = blockIdx.x, n = blockIdx.y, H = p.H;
     int t_begin = p.cu[n], t_end = p.cu[n + 1];
     if (t_begin < 0 || t_end < t_begin || t_end > p.ntok) {
@@ -96,144 +118,251 @@ __global__ void __launch_bounds__(ChainCfg<D>::NT, 1) delta_bwd_chain_kernel(Cha
     const int nc = (t_end - t_begin + C - 1) / C;
     const int64_t slot0 = (int64_t)(t_begin / C) + n;
     const int64_t sbase = ((int64_t)n * H + h) * D * D;
-    // this warp's blocks: du rows 16 Ru, columns nu ..; dS rows 16 Rs, columns ns ..
-    const int Ru = w >> 2, nu = (w & 3) * (D / 4);
-    const int Rs = w / L::CG, ns = (w % L::CG) * (D / L::CG);
+    auto rec_buf = [&](int i) { return sm + (uint32_t)(i % NB) * L::BUF; };
+    auto do_buf = [&](int i) { return sm + L::DO + (uint32_t)(i % NB) * L::DOB; };
+    auto use_par = [](int i) { return (uint32_t)(i / NB) & 1u; };
+    auto gend_of = [&](int i) { return reinterpret_cast<const float *>(rec_buf(i) + L::WQB + L::KB + L::AQB); };
+    // step i's record (chunk nc - 1 - i) into buffer i % NB: [-W ; Q e^b],
+    // rows 64..127 of each 64-column block of [U ; K~], Aq, e^{b_L}
+    auto issue_rec = [&](int i) {
+        uint8_t *buf = rec_buf(i);
+        uint64_t *bar = &bars[CB_REC0 + i % NB];
+        const uint8_t *rec = p.records + ((slot0 + (nc - 1 - i)) * H + h) * (int64_t)Rec::BYTES;
+        fence_proxy_async();
+        mbar_arrive_expect_tx(bar, L::TX);
+        bulk_load(buf, rec + Rec::WQ, L::WQB, bar);
+#pragma unroll
+        for (int cb = 0; cb < D / 64; ++cb)
+            bulk_load(buf + L::WQB + cb * 8192, rec + Rec::UK + cb * 16384 + 8192, 8192, bar);
+        bulk_load(buf + L::WQB + L::KB, rec + Rec::AQ, L::AQB, bar);
+        bulk_load(buf + L::WQB + L::KB + L::AQB, rec + Rec::GEND, L::GB, bar);
+    };
+    // a wait whose outcome is the same in every lane of the warp (the TMEM
+    // accesses after it are warp-collective)
+    auto wwait = [&](int bar, uint32_t parity, unsigned code) {
+        return __all_sync(0xffffffffu, mbar_wait(&bars[bar], parity, p.err, code));
+    };
+    auto warp_arrive = [&](int bar) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[bar]);
+    };
 
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+        mbar_init(&bars[CB_DSREADY], 8);
+        mbar_init(&bars[CB_DU], 1);
+        mbar_init(&bars[CB_DUREADY], 8);
+        mbar_init(&bars[CB_DS], 1);
+        mbar_init(&bars[CB_END], 1);
+        for (int b = 0; b < NB; ++b) {
+            mbar_init(&bars[CB_REC0 + b], 1);
+            mbar_init(&bars[CB_DO0 + b], L::N_DO);
+            mbar_init(&bars[CB_FREE0 + b], 1);
+        }
         fence_mbar_init();
     }
+    if (warp == 0) {
+        tmem_alloc(tslot, L::TCOLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
     __syncthreads();
-    auto issue = [&](int c) {   // thread 0: chunk c's record into buffer c & 1
-        uint8_t *buf = smem + (c & 1) * L::BUF;
-        const uint8_t *rec = p.records + ((slot0 + c) * H + h) * (int64_t)Rec::BYTES;
-        fence_proxy_async();
-        mbar_arrive_expect_tx(&bars[c & 1], L::TX);
-        bulk_load(buf, rec + Rec::WQ, L::WQB, &bars[c & 1]);
-#pragma unroll
-        for (int cb = 0; cb < D / 64; ++cb)   // rows 64..127 of each 64-column block of [U ; K~]
-            bulk_load(buf + L::WQB + cb * 8192, rec + Rec::UK + cb * 16384 + 8192, 8192, &bars[c & 1]);
-        bulk_load(buf + L::WQB + L::KB, rec + Rec::AQ, L::AQB, &bars[c & 1]);
-        bulk_load(buf + L::WQB + L::KB + L::AQB, rec + Rec::GEND, L::GB, &bars[c & 1]);
-    };
-    // this thread's 16-byte units of scale * dO (rows past the end are zero)
-    uint4 rdo[L::DO_UNITS];
-    auto load_do = [&](int c) {
-        const int tok0 = t_begin + c * C, len = min(C, t_end - tok0);
-#pragma unroll
-        for (int k = 0; k < L::DO_UNITS; ++k) {
-            const int u = tid + L::NT * k, r = u / (D / 8), c8 = (u % (D / 8)) * 8;
-            rdo[k] = r < len ? *reinterpret_cast<const uint4 *>(p.d_o + ((int64_t)(tok0 + r) * H + h) * D + c8)
-                             : make_uint4(0u, 0u, 0u, 0u);
-        }
-    };
-    auto store_do = [&](int c) {
-        bf16 *dst = reinterpret_cast<bf16 *>(smem + L::DO + (c & 1) * L::DOB);
-#pragma unroll
-        for (int k = 0; k < L::DO_UNITS; ++k) {
-            const int u = tid + L::NT * k, r = u / (D / 8), c8 = (u % (D / 8)) * 8;
-            float v[8];
-            tile::unpack8(rdo[k], v);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] *= p.scale;
-            *reinterpret_cast<uint4 *>(dst + r * XS + c8) = tile::pack8(v);
-        }
-    };
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);  // this warp's lane quarter
 
-    // dS' of the last chunk: the final state's gradient
-    float ds[NT_DS][4];
+    if (warp == L::W_ISSUER) {
+        // ================================================= issuer
+        if (lane == 0 && nc > 0) {
+            constexpr uint32_t id_aq = idesc_bf16(64, D, true, true);   // Aq^T dO'
+            constexpr uint32_t id_k = idesc_bf16(64, D, false, true);   // K~ dS'
+            constexpr uint32_t id_s = idesc_bf16(D, D, true, true);     // (Q e^b)^T dO', (-W)^T du
+            const uint64_t bS = mdesc(sds, D, 0, 0), bU = mdesc(sdu, C, 0, 0);
+            int issued = 0, waited = 0;
+            for (; issued < NB && issued < nc; ++issued) issue_rec(issued);
+            for (int i = 0; i < nc; ++i) {
+                const int b = i % NB;
+                const uint8_t *rb = rec_buf(i);
+                if (!mbar_wait(&bars[CB_REC0 + b], use_par(i), p.err, 40)) break;
+                waited = i + 1;
+                if (!mbar_wait(&bars[CB_DO0 + b], use_par(i), p.err, 41)) break;
+                tc_fence_after();
+                const uint64_t bO = mdesc(do_buf(i), C, 0, 0);
+                const uint64_t aA = mdesc(rb + L::WQB + L::KB, C, 0, 0);
 #pragma unroll
-    for (int j = 0; j < NT_DS; ++j)
+                for (int s4 = 0; s4 < 4; ++s4)
+                    mma_bf16(tmem + L::TDU, dstep(aA, s4 * 128), dstep(bO, s4 * 128), id_aq, s4 > 0 ? 1u : 0u);
+                // dS' of this chunk in TMEM (scaled) and as the bf16 tile
+                if (!mbar_wait(&bars[CB_DSREADY], (uint32_t)i & 1u, p.err, 42)) break;
+                tc_fence_after();
+                const uint64_t aK = kdesc(rb + L::WQB, C, 0, 0);
 #pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-            const int r = 16 * Rs + g + 8 * hr, col = ns + 8 * j + 2 * t;
-            const float2 v = p.d_final_S ? *reinterpret_cast<const float2 *>(p.d_final_S + sbase + r * D + col)
-                                         : make_float2(0.0f, 0.0f);
-            ds[j][2 * hr] = v.x;
-            ds[j][2 * hr + 1] = v.y;
-        }
-    if (nc > 0) {
-        if (tid == 0) issue(nc - 1);
-        load_do(nc - 1);
-    }
-    // chunk c is use (nc - 1 - c) / 2 of buffer c & 1: its phase parity
-    auto parity = [&](int c) { return (uint32_t)(((nc - 1 - c) >> 1) & 1); };
-    int pending = nc > 0 ? nc - 1 : -1;   // a record copy issued and not yet waited for
-    for (int c = nc - 1; c >= 0; --c) {
-        const int b = c & 1;
-        const uint8_t *buf = smem + b * L::BUF;
-        const RsView wq{buf, 128, 0}, qe{buf, 128, 64}, kt{buf + L::WQB, 64, 0};
-        const RsView aq{buf + L::WQB + L::KB, 64, 0};
-        const float *gend = reinterpret_cast<const float *>(buf + L::WQB + L::KB + L::AQB);
-        const PadView dO{reinterpret_cast<const bf16 *>(smem + L::DO + b * L::DOB), XS};
-        const PadView dSp{sDS, XS}, dU{sDU, XS};
-        // 1. dS' of chunk c out (fp32) and in (bf16 operand); this chunk's dO in
-        float *dst = p.dstates + ((slot0 + c) * H + h) * (int64_t)(D * D);
-        bf16 *dst16 = p.dstates16 + ((slot0 + c) * H + h) * (int64_t)(D * D);
+                for (int s = 0; s < D / 16; ++s)
+                    mma_bf16(tmem + L::TDU, dstep(aK, kstep_units(C, s)), dstep(bS, s * 128), id_k, 1);
+                mma_commit(&bars[CB_DU]);
+                const uint64_t aQ = mdesc(rb, 128, 64, 0);
 #pragma unroll
-        for (int j = 0; j < NT_DS; ++j)
+                for (int s4 = 0; s4 < 4; ++s4)
+                    mma_bf16(tmem + L::TDS, dstep(aQ, s4 * 128), dstep(bO, s4 * 128), id_s, 1);
+                // step i - 1's products have completed (its "ds" phase came before
+                // this step's DSREADY): its buffer takes step i + NB - 1
+                if (i >= 1 && issued < nc) issue_rec(issued++);
+                if (!mbar_wait(&bars[CB_DUREADY], (uint32_t)i & 1u, p.err, 43)) break;
+                tc_fence_after();
+                const uint64_t aW = mdesc(rb, 128, 0, 0);
 #pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const int r = 16 * Rs + g + 8 * hr, col = ns + 8 * j + 2 * t;
-                if (p.gend)   // gated: fp32 (the per-chunk kernel also forms rowsum(dS' o S))
-                    *reinterpret_cast<float2 *>(dst + r * D + col) = make_float2(ds[j][2 * hr], ds[j][2 * hr + 1]);
-                else
-                    wmma16::st2(dst16 + r * D + col, ds[j][2 * hr], ds[j][2 * hr + 1]);
-                wmma16::st2(sDS + r * XS + col, ds[j][2 * hr], ds[j][2 * hr + 1]);
+                for (int s4 = 0; s4 < 4; ++s4)
+                    mma_bf16(tmem + L::TDS, dstep(aW, s4 * 128), dstep(bU, s4 * 128), id_s, 1);
+                mma_commit(&bars[CB_DS]);
+                mma_commit(&bars[CB_FREE0 + b]);
             }
-        store_do(c);
-        const bool ok = mbar_wait(&bars[b], parity(c), p.err, 15u);
-        if (__syncthreads_or(!ok)) break;
-        pending = -1;
-        if (c > 0) {
-            if (tid == 0) issue(c - 1);
-            pending = c - 1;
-            load_do(c - 1);
+            // every product issued has completed before TMEM is released
+            mma_commit(&bars[CB_END]);
+            mbar_wait(&bars[CB_END], 0, p.err, 44);
+            // record copies still in flight (only after a failed wait); at
+            // most one per buffer
+            for (int j = waited; j < issued; ++j) mbar_wait(&bars[CB_REC0 + j % NB], use_par(j), nullptr, 0u);
         }
-        // 2. du = Aq^T dO' + K~ dS' (Aq lower: rows r >= i of Aq reach column i)
-        {
-            float du[NT_DU][4];
-            wmma16::zero(du);
-            wmma16::mma_rows<NT_DU, true, false>(du, aq, dO, 16 * Ru, nu, 16 * Ru, 64);
-            wmma16::mma_rows_c<0, D, NT_DU, false, false>(du, kt, dSp, 16 * Ru, nu);
-            bf16 *gdu = p.du ? p.du + ((slot0 + c) * H + h) * (int64_t)(64 * D) : nullptr;
+    } else if (warp < 8) {
+        // ================================================= readback warps
+        const int c0 = (warp >> 2) * HALF;              // this warp's column half
+        const int srow = tile::acc_row(D, qd, lane);    // dS row (key channel), or -1
+        const int urow = tile::acc_row(C, qd, lane);    // du row (token), or -1
+        bool ok = true;
+        float v[HALF];                                   // row srow of dS', columns c0 ..
+        for (int i = 0; i < nc && ok; ++i) {
+            const int c = nc - 1 - i;
+            if (i == 0) {
+                // dS' of the last chunk: the final state's gradient
 #pragma unroll
-            for (int j = 0; j < NT_DU; ++j)
-#pragma unroll
-                for (int hr = 0; hr < 2; ++hr) {
-                    const int r = 16 * Ru + g + 8 * hr, col = nu + 8 * j + 2 * t;
-                    wmma16::st2(sDU + r * XS + col, du[j][2 * hr], du[j][2 * hr + 1]);
-                    if (gdu) wmma16::st2(gdu + r * D + col, du[j][2 * hr], du[j][2 * hr + 1]);
+                for (int cb = 0; cb < HALF; cb += 4) {
+                    const float4 f = (srow >= 0 && p.d_final_S)
+                                         ? *reinterpret_cast<const float4 *>(p.d_final_S + sbase + (int64_t)srow * D + c0 + cb)
+                                         : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    v[cb] = f.x; v[cb + 1] = f.y; v[cb + 2] = f.z; v[cb + 3] = f.w;
                 }
-        }
-        __syncthreads();
-        // 3. dS = Diag(e^{b_L}) dS' + (Q e^b)^T dO' + (-W)^T du
-        {
-            const float g0 = p.gend ? gend[16 * Rs + g] : 1.0f;
-            const float g1 = p.gend ? gend[16 * Rs + g + 8] : 1.0f;
+            } else {
+                if (!(ok = wwait(CB_DS, (uint32_t)(i - 1) & 1u, 45))) break;
+                tc_fence_after();
 #pragma unroll
-            for (int j = 0; j < NT_DS; ++j) {
-                ds[j][0] *= g0; ds[j][1] *= g0;
-                ds[j][2] *= g1; ds[j][3] *= g1;
+                for (int cb = 0; cb < HALF; cb += 32)
+                    tmem_ld32(tq + L::TDS + c0 + cb, *reinterpret_cast<float(*)[32]>(v + cb));
             }
-            wmma16::mma_rows_c<0, 64, NT_DS, true, false>(ds, qe, dO, 16 * Rs, ns);
-            wmma16::mma_rows_c<0, 64, NT_DS, true, false>(ds, wq, dU, 16 * Rs, ns);
+            if (srow >= 0) {
+#pragma unroll
+                for (int cb = 0; cb < HALF; cb += 8) tile::st_bf16x8(sds, D, srow, c0 + cb, v + cb);
+            }
+            if (GATED) {
+                // dS' * e^{b_L} back into TMEM, to accumulate the chunk's products on
+                if (!(ok = wwait(CB_REC0 + i % NB, use_par(i), 46))) break;
+                const float gd = srow >= 0 ? gend_of(i)[srow] : 1.0f;
+#pragma unroll
+                for (int cb = 0; cb < HALF; cb += 16) {
+                    float x[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) x[j] = v[cb + j] * gd;
+                    tmem_st16(tq + L::TDS + c0 + cb, x);
+                }
+            } else if (i == 0) {
+#pragma unroll
+                for (int cb = 0; cb < HALF; cb += 16)
+                    tmem_st16(tq + L::TDS + c0 + cb, *reinterpret_cast<float(*)[16]>(v + cb));
+            }
+            fence_proxy_async();
+            warp_arrive(CB_DSREADY);
+            // dS' of chunk c out, for the per-chunk gradients, while du is formed
+            // (16-byte units by column group: each store is a contiguous run)
+            if (srow >= 0) {
+                const int64_t o = ((slot0 + c) * H + h) * (int64_t)(D * D);
+                if (GATED) {   // fp32: the per-chunk kernel also forms rowsum(dS' o S)
+                    float4 *dst = reinterpret_cast<float4 *>(p.dstates + o);
+#pragma unroll
+                    for (int cb = 0; cb < HALF; cb += 4)
+                        dst[unit_at(D, srow, (c0 + cb) / 4)] = make_float4(v[cb], v[cb + 1], v[cb + 2], v[cb + 3]);
+                } else {
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.dstates16 + o);
+#pragma unroll
+                    for (int cb = 0; cb < HALF; cb += 8) dst[unit_at(D, srow, (c0 + cb) / 8)] = pack8(v + cb);
+                }
+            }
+            // du of the chunk -> bf16 operand tile and global
+            if (!(ok = wwait(CB_DU, (uint32_t)i & 1u, 47))) break;
+            tc_fence_after();
+            float u[HALF];
+#pragma unroll
+            for (int cb = 0; cb < HALF; cb += 32)
+                tmem_ld32(tq + L::TDU + c0 + cb, *reinterpret_cast<float(*)[32]>(u + cb));
+            if (urow >= 0) {
+#pragma unroll
+                for (int cb = 0; cb < HALF; cb += 8) tile::st_bf16x8(sdu, C, urow, c0 + cb, u + cb);
+            }
+            fence_proxy_async();
+            warp_arrive(CB_DUREADY);
+            if (urow >= 0 && p.du) {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.du + ((slot0 + c) * H + h) * (int64_t)(C * D));
+#pragma unroll
+                for (int cb = 0; cb < HALF; cb += 8) dst[unit_at(C, urow, (c0 + cb) / 8)] = pack8(u + cb);
+            }
+        }
+        // the gradient of the initial state: dS after chunk 0's step
+        if (ok && p.d_init_S) {
+            if (nc > 0) {
+                if (wwait(CB_DS, (uint32_t)(nc - 1) & 1u, 48)) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int cb = 0; cb < HALF; cb += 32)
+                        tmem_ld32(tq + L::TDS + c0 + cb, *reinterpret_cast<float(*)[32]>(v + cb));
+                } else {
+                    ok = false;
+                }
+            } else {
+#pragma unroll
+                for (int cb = 0; cb < HALF; cb += 4) {
+                    const float4 f = (srow >= 0 && p.d_final_S)
+                                         ? *reinterpret_cast<const float4 *>(p.d_final_S + sbase + (int64_t)srow * D + c0 + cb)
+                                         : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    v[cb] = f.x; v[cb + 1] = f.y; v[cb + 2] = f.z; v[cb + 3] = f.w;
+                }
+            }
+            if (ok && srow >= 0) {
+                float4 *dst = reinterpret_cast<float4 *>(p.d_init_S + sbase + (int64_t)srow * D + c0);
+#pragma unroll
+                for (int cb = 0; cb < HALF; cb += 4) dst[cb / 4] = make_float4(v[cb], v[cb + 1], v[cb + 2], v[cb + 3]);
+            }
+        }
+    } else {
+        // ================================================= dO staging warps (8, 9)
+        const int st = tid - 32 * L::W_DO;   // 0 .. 63
+        for (int j = 0; j < nc; ++j) {
+            const int b = j % NB;
+            // the buffer's previous use (step j - NB) has finished
+            if (j >= NB && !wwait(CB_FREE0 + b, use_par(j - NB), 49)) break;
+            const int tok0 = t_begin + (nc - 1 - j) * C, len = min(C, t_end - tok0);
+            uint4 r[L::DO_UNITS];
+#pragma unroll
+            for (int k = 0; k < L::DO_UNITS; ++k) {
+                const int un = st + 32 * L::N_DO * k, row = un / (D / 8), c8 = (un % (D / 8)) * 8;
+                r[k] = row < len ? *reinterpret_cast<const uint4 *>(p.d_o + ((int64_t)(tok0 + row) * H + h) * D + c8)
+                                 : make_uint4(0u, 0u, 0u, 0u);
+            }
+            uint8_t *dst = do_buf(j);
+#pragma unroll
+            for (int k = 0; k < L::DO_UNITS; ++k) {
+                const int un = st + 32 * L::N_DO * k, row = un / (D / 8), c8 = (un % (D / 8)) * 8;
+                float x[8];
+                tile::unpack8(r[k], x);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] *= p.scale;
+                *reinterpret_cast<uint4 *>(dst + tile::rs_off(C, row, c8)) = tile::pack8(x);
+            }
+            fence_proxy_async();
+            warp_arrive(CB_DO0 + b);
         }
     }
-    // a copy still in flight (only after a failed wait): let it land first
-    if (pending >= 0) mbar_wait(&bars[pending & 1], parity(pending), nullptr, 0u);
-    if (p.d_init_S) {
-#pragma unroll
-        for (int j = 0; j < NT_DS; ++j)
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const int r = 16 * Rs + g + 8 * hr, col = ns + 8 * j + 2 * t;
-                *reinterpret_cast<float2 *>(p.d_init_S + sbase + r * D + col) =
-                    make_float2(ds[j][2 * hr], ds[j][2 * hr + 1]);
-            }
-    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, L::TCOLS);
 }
 
 // ------------------------------------------------------------------ host
@@ -257,20 +386,26 @@ ChunkWs chunk_ws(int N, int ntok, int H, int D) {
     return w;
 }
 
-template <int D>
+template <int D, bool GATED>
 cudaError_t launch_chain(const ChainParams &cp, int N, int H, cudaStream_t s) {
     using L = ChainCfg<D>;
-    const size_t smem = (size_t)L::BYTES;
-    cudaError_t e = cudaFuncSetAttribute(delta_bwd_chain_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const size_t smem = (size_t)L::BYTES + 1024;   // + alignment of the base
+    auto kern = delta_bwd_chain_kernel<D, GATED>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    delta_bwd_chain_kernel<D><<<dim3(H, N), L::NT, smem, s>>>(cp);
+    kern<<<dim3(H, N), L::NT, smem, s>>>(cp);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 bool delta_bwd_chunked_supported(const BwdArgs &a) {
+    // the kernels move rows in 16-byte units (null pointers pass)
+    auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    const void *ptrs[] = {a.q, a.k, a.v, a.beta_logits, a.gate_logits, a.d_o, a.d_final_S, a.init_S,
+                          a.dq, a.dk_out, a.dv_out, a.d_beta_logits, a.d_gate_logits, a.d_init_S};
+    for (const void *p : ptrs)
+        if (!al16(p)) return false;
     return a.bf16 && a.dk == a.dv && (a.dk == 64 || a.dk == 128);
 }
 
@@ -303,9 +438,10 @@ cudaError_t launch_delta_backward_chunked(const BwdArgs &a, cudaStream_t s) {
     // 2. dS from the last chunk to the first
     const uint8_t *records = base + tile::Workspace::table_bytes(a.N, a.ntok);
     ChainParams cp{records, static_cast<const __nv_bfloat16 *>(a.d_o), a.cu_seqlens, a.d_final_S,
-                   dstates, dstates16, du, a.d_init_S, err, a.H, a.ntok, a.scale,
-                   a.gate_logits != nullptr};
-    e = D == 64 ? launch_chain<64>(cp, a.N, a.H, s) : launch_chain<128>(cp, a.N, a.H, s);
+                   dstates, dstates16, du, a.d_init_S, err, a.H, a.ntok, a.scale};
+    const bool gated = a.gate_logits != nullptr;   // records carry e^{b_L}; else it is 1
+    if (D == 64) e = gated ? launch_chain<64, true>(cp, a.N, a.H, s) : launch_chain<64, false>(cp, a.N, a.H, s);
+    else e = gated ? launch_chain<128, true>(cp, a.N, a.H, s) : launch_chain<128, false>(cp, a.N, a.H, s);
     if (e != cudaSuccess) return e;
 
     // 3. every (chunk, head): the gradients, through the prologue

@@ -148,12 +148,13 @@ __global__ void __launch_bounds__(NT, 1) delta_inter_kernel(InterParams p) {
     auto acc = [&](int c) { return (uint32_t)(TC::ACC + (c & 1) * D); };
     const int64_t sbase = ((int64_t)n * H + h) * D * D;
     // 16 consecutive fp32 state entries (row srow, columns col..col+15) at the
-    // start of chunk c, for the backward pass
+    // start of chunk c, for the backward pass (16-byte units by column group,
+    // so the warp's lanes, on consecutive rows, store contiguous runs)
     auto store_state = [&](int c, int srow, int col, const float *v) {
-        float4 *dst = reinterpret_cast<float4 *>(
-            p.states + (((slot0 + c) * H + h) * D + srow) * (int64_t)D + col);
+        float4 *dst = reinterpret_cast<float4 *>(p.states + ((slot0 + c) * H + h) * (int64_t)(D * D));
 #pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        for (int i = 0; i < 4; ++i)
+            dst[unit_at(D, srow, col / 4 + i)] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
     };
     // one lane of each warp arrives once the warp's work is ordered before it
     auto warp_arrive = [&](uint64_t *bar) {

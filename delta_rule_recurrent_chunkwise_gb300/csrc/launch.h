@@ -63,9 +63,10 @@ struct BwdArgs {
 };
 size_t delta_bwd_workspace_bytes(int N, int ntok, int H, int dk, int dv);
 cudaError_t launch_delta_backward(const BwdArgs &a, cudaStream_t s);
-// Chunkwise form (bf16, dk = dv in {64, 128}, any gate, not additive): the
-// tensor-core forward with chunk states, a reverse dS chain and a parallel
-// per-chunk gradient kernel that also takes the prologue's derivatives.
+// Chunkwise form (bf16, dk = dv in {64, 128}, any gate, either rule, every
+// tensor 16-byte aligned): the tensor-core forward with chunk states, a
+// reverse dS chain and a parallel per-chunk gradient kernel that also takes
+// the prologue's derivatives.
 bool delta_bwd_chunked_supported(const BwdArgs &a);
 size_t delta_bwd_chunked_workspace_bytes(int N, int ntok, int H, int D);
 cudaError_t launch_delta_backward_chunked(const BwdArgs &a, cudaStream_t s);

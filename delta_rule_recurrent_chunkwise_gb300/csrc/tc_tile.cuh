@@ -88,6 +88,17 @@ __device__ __forceinline__ void tmem_cols(uint32_t taddr, float (&v)[NC]) {
     else tmem_ld16(taddr, v);
 }
 
+// The backward pass's per-chunk matrices in the workspace -- the state and
+// its gradient at every chunk start (fp32 [D][D]), that gradient in bf16
+// ([D][D]) and du (bf16 [64][D]) -- are stored by 16-byte units (4 fp32 or
+// 8 bf16 of one row), one column of units after another: unit (row r, column
+// group g) at index g * rows + r.  A warp whose lanes hold consecutive rows
+// (a TMEM lane quarter) then stores one contiguous run of units at a time,
+// where row-major storage would have each lane write its own row.
+__host__ __device__ __forceinline__ int64_t unit_at(int rows, int r, int g) {
+    return (int64_t)g * rows + r;
+}
+
 // Per-(chunk, head) record written by the intra-chunk kernel and read by the
 // inter-chunk kernel, byte-for-byte the shared-memory image of its operands:
 //   WQ    [-W ; Q e^{b}]                 128-row RS tile (W = T (beta K e^{b}));

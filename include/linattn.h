@@ -242,9 +242,10 @@ la_status la_decode_step_slots(const void *q, const void *k, const void *v,
  * every chunk start, du per chunk; or, token-serial, checkpoints and
  * per-token column sums); LA_ERR_INVALID_ARG if smaller or missing.
  * dk, dv in {64, 128}.  Two forms, chosen from the arguments: chunkwise
- * (io = LA_BF16, dk = dv; any gate, either update rule) -- the
- * tensor-core forward pass, a reverse pass over the chunks for the state
- * gradient, then every (chunk, head) in parallel; token-serial otherwise.
+ * (io = LA_BF16, dk = dv, every tensor 16-byte aligned; any gate, either
+ * update rule) -- the tensor-core forward pass, a reverse pass over the
+ * chunks for the state gradient (tensor cores, the gradient held in tensor
+ * memory), then every (chunk, head) in parallel; token-serial otherwise.
  * Sums over value columns inside a thread block use shared-memory atomics,
  * so the last bits of dq, dk, d_beta_logits and d_gate_logits may differ
  * between runs. */
