@@ -510,10 +510,11 @@ def run_ours(args, rank, world, dev, dist):
             for bname, wname, kern in (
                     ("gpt2_backward", HEADLINE,
                      "chunkwise: forward with records, T and chunk states; reverse dS "
-                     "chain; per-chunk gradient kernel (bf16 mma.sync)"),
+                     "chain (tcgen05, dS in TMEM); per-chunk gradient kernel (bf16 mma.sync)"),
                     ("gated_backward", "gated_prefill",
                      "chunkwise: forward with records, T and chunk states; reverse dS "
-                     "chain; per-chunk gradient kernel with per-channel decay (bf16 mma.sync)")):
+                     "chain (tcgen05, dS in TMEM); per-chunk gradient kernel with per-channel "
+                     "decay (bf16 mma.sync)")):
                 bw = wl.workload(wname)
                 b_in = wl.inputs_for(bw, seed=rank_seed(rank))
                 bt = {n: (None if b_in[n] is None else b_in[n].to(dev))

@@ -179,3 +179,24 @@ def test_backward_many_short_sequences(cuda_lib, d):
     got = _run(la, inp, d_o, d_fS, flags)
     ref = _oracle(inp, d_o, d_fS, oflags)
     _compare(got, ref, TOL[torch.bfloat16])
+
+
+def test_backward_unaligned_tensor_takes_token_serial(cuda_lib):
+    """A tensor that is not 16-byte aligned (here d_final_S, one float into a
+    larger buffer) sends a bf16 call that the chunkwise form would take to
+    the token-serial kernels instead; the gradients still match the oracle."""
+    la = cuda_lib
+    dev = torch.device("cuda")
+    inp = wl.prefill_inputs([130, 64], 2, 64, 64, torch.bfloat16, True, seed=75, init_state=True)
+    d_o, d_fS = _grad_inputs(inp, torch.bfloat16, seed=76)
+    buf = torch.zeros(d_fS.numel() + 1, device=dev)
+    d_fS_odd = buf[1:].view(d_fS.shape)
+    d_fS_odd.copy_(d_fS.to(dev))
+    assert d_fS_odd.data_ptr() % 16 != 0
+    t = {n: inp[n].to(dev) for n in ("q", "k", "v", "beta_logits", "gate_logits", "init_S")}
+    out = la.la_backward_delta(t["q"], t["k"], t["v"], t["beta_logits"], t["gate_logits"],
+                               d_o.to(dev), inp["cu_seqlens"].to(dev), d_final_S=d_fS_odd,
+                               init_S=t["init_S"], cu_seqlens_host=inp["cu_seqlens"])
+    assert la.la_check_device() == la.LA_OK
+    got = {n: (None if v is None else v.cpu().numpy()) for n, v in out.items()}
+    _compare(got, _oracle(inp, d_o, d_fS, oracle.L2NORM_K), TOL[torch.bfloat16])
