@@ -67,6 +67,7 @@ template <int D> struct ChainCfg {
     static constexpr uint32_t TDS = 0, TDU = D, TCOLS = 2 * D;
     static constexpr int DO_UNITS = 64 * D / 8 / (32 * N_DO);   // 16-byte units of dO per staging thread
     static_assert(BYTES + 1024 <= 232448, "shared memory budget");
+    static_assert(NB <= 4, "four mbarrier slots per kind of buffer");
 };
 
 // mbarrier slots: per step, then per buffer (REC: record copy landed; DO:
