@@ -531,9 +531,33 @@ def run_ours(args, rank, world, dev, dist):
                                          want_d_init_S=False, workspace=bws,
                                          cu_seqlens_host=b_in["cu_seqlens"], stream=stream)
 
+                # the training pair: the forward that keeps what the gradients
+                # need (outputs written), then the gradients from it
+                o_tr = torch.empty((bw.ntok, bw.H, bw.dv), dtype=bw.dtype, device=dev)
+
+                def train_forward():
+                    la.la_prefill_delta_train(bt["q"], bt["k"], bt["v"], bt["beta_logits"],
+                                              bt["gate_logits"], o_tr, bt["cu_seqlens"], bws,
+                                              cu_seqlens_host=b_in["cu_seqlens"], stream=stream)
+
+                def saved_backward():
+                    la.la_backward_delta_saved(bt["q"], bt["k"], bt["v"], bt["beta_logits"],
+                                               bt["gate_logits"], d_o, bt["cu_seqlens"], bws,
+                                               want_d_init_S=False,
+                                               cu_seqlens_host=b_in["cu_seqlens"], stream=stream)
+
+                def train_step():
+                    train_forward()
+                    saved_backward()
+
                 with clocks.load():
                     bms = time_steps(backward_step, 3, 2, flush, stream, barrier)
+                    tms = time_steps(train_step, 3, 2, flush, stream, barrier)
+                    train_forward()
+                    sms_ = time_steps(saved_backward, 3, 2, flush, stream, barrier)
                 b_ms = mor(statistics.median(bms))
+                t_ms = mor(statistics.median(tms))
+                s_ms = mor(statistics.median(sms_))
                 nb = backward_algo_bytes(bw)
                 extra[bname] = {
                     "tokens_per_s": bw.ntok * world / (b_ms / 1e3), "ms": b_ms,
@@ -541,8 +565,12 @@ def run_ours(args, rank, world, dev, dist):
                     "algorithmic_bytes": nb,
                     "workload": f"{len(bw.lengths)} x {bw.lengths[0]} tokens, H={bw.H}, "
                                 f"d={bw.dk}, {'per-channel gate' if bw.gated else 'no gate'}",
-                    "kernel": kern}
-                del bt, d_o, bws
+                    "kernel": kern,
+                    "train_step_ms": t_ms,
+                    "train_step_note": "la_prefill_delta_train (outputs, and the records, T and "
+                                       "chunk-start states kept) + la_backward_delta_saved",
+                    "saved_backward_ms": s_ms}
+                del bt, d_o, bws, o_tr
             result["secondary"] = extra
     result["clocks"] = clocks.summary()
     return result

@@ -10,8 +10,8 @@ Functions (same names as the C ABI):
   la_prefill_linear, la_prefill_delta, la_prefill_delta_workspace_size,
   la_prefill_delta_launches,
   la_prefill_delta_static, la_decode_step, la_decode_step_slots,
-  la_backward_delta, la_check_device, la_selftest_wait_timeout,
-  la_status_string.
+  la_backward_delta, la_prefill_delta_train, la_backward_delta_saved,
+  la_check_device, la_selftest_wait_timeout, la_status_string.
 """
 from __future__ import annotations
 
@@ -29,7 +29,8 @@ LA_L2NORM_K, LA_L2NORM_Q, LA_SILU_QK, LA_GATE_SCALAR, LA_ADDITIVE = 1, 2, 4, 8, 
 EXPORTED = ("la_prefill_linear", "la_prefill_delta", "la_prefill_delta_workspace_size",
             "la_prefill_delta_launches",
             "la_prefill_delta_static", "la_decode_step", "la_decode_step_slots",
-            "la_backward_delta", "la_backward_delta_workspace_size", "la_check_device",
+            "la_backward_delta", "la_backward_delta_workspace_size",
+            "la_prefill_delta_train", "la_backward_delta_saved", "la_check_device",
             "la_selftest_wait_timeout", "la_status_string")
 
 
@@ -67,6 +68,9 @@ def library():
                                              vp, ip, vp, vp]
         lib.la_backward_delta.argtypes = [vp, vp, vp, vp, vp, vp, vp, ip, vp, vp, ip, ip, ip, ip,
                                           ip, fp, u, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        lib.la_prefill_delta_train.argtypes = [vp, vp, vp, vp, vp, vp, ip, vp, vp, ip, ip, ip,
+                                               ip, ip, fp, u, vp, vp, vp, sz, vp]
+        lib.la_backward_delta_saved.argtypes = lib.la_backward_delta.argtypes
         lib.la_backward_delta_workspace_size.argtypes = [ip, ip, ip, ip, ip]
         lib.la_backward_delta_workspace_size.restype = sz
         lib.la_check_device.argtypes = [vp]
@@ -75,6 +79,7 @@ def library():
         lib.la_status_string.restype = ctypes.c_char_p
         for f in ("la_prefill_linear", "la_prefill_delta", "la_prefill_delta_static",
                   "la_decode_step", "la_decode_step_slots", "la_backward_delta",
+                  "la_prefill_delta_train", "la_backward_delta_saved",
                   "la_check_device", "la_selftest_wait_timeout"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
@@ -230,6 +235,50 @@ def la_backward_delta(q, k, v, beta_logits, gate_logits, d_o, cu_seqlens, d_fina
     (None unless want_d_init_S).  Rows of tokens outside every sequence are
     zero here (the library leaves them untouched; they are allocated zeroed
     unless cu_seqlens_host shows the sequences cover every row)."""
+    return _backward("la_backward_delta", q, k, v, beta_logits, gate_logits, d_o, cu_seqlens,
+                     d_final_S, scale, flags, init_S, want_d_init_S, workspace, cu_seqlens_host,
+                     stream)
+
+
+def la_prefill_delta_train(q, k, v, beta_logits, gate_logits, o, cu_seqlens, saved, scale=1.0,
+                           flags=LA_L2NORM_K, init_S=None, final_S=None, cu_seqlens_host=None,
+                           stream=None):
+    """la_prefill_delta (chunk 64) that also keeps what the gradients need in
+    `saved`, a device buffer of la_backward_delta_workspace_size(...) bytes,
+    for la_backward_delta_saved.  bf16 with dk = dv in {64, 128} only."""
+    import torch
+    _check(dict(q=q, k=k, v=v, o=o, beta_logits=beta_logits, gate_logits=gate_logits),
+           dtype=q.dtype, device=q.device)
+    _check(dict(cu_seqlens=cu_seqlens), dtype=torch.int32, device=q.device)
+    _check(dict(init_S=init_S, final_S=final_S), dtype=torch.float32, device=q.device)
+    _check(dict(saved=saved), device=q.device)
+    ntok, H, dk = q.shape
+    dv = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    hold, hptr = _host_cu(cu_seqlens_host)
+    rc = library().la_prefill_delta_train(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(beta_logits), _ptr(gate_logits), _ptr(o), _io(q),
+        _ptr(cu_seqlens), hptr, N, ntok, H, dk, dv, float(scale), int(flags), _ptr(init_S),
+        _ptr(final_S), _ptr(saved), saved.numel() * saved.element_size(), _stream(stream))
+    if rc != LA_OK:
+        raise LinAttnError(rc, "la_prefill_delta_train")
+    return o
+
+
+def la_backward_delta_saved(q, k, v, beta_logits, gate_logits, d_o, cu_seqlens, saved,
+                            d_final_S=None, scale=1.0, flags=LA_L2NORM_K, init_S=None,
+                            want_d_init_S=True, cu_seqlens_host=None, stream=None):
+    """la_backward_delta from the tensors la_prefill_delta_train kept in
+    `saved` (pass that call's inputs); the forward is not recomputed."""
+    if saved is None:
+        raise ValueError("saved: the buffer la_prefill_delta_train filled")
+    return _backward("la_backward_delta_saved", q, k, v, beta_logits, gate_logits, d_o,
+                     cu_seqlens, d_final_S, scale, flags, init_S, want_d_init_S, saved,
+                     cu_seqlens_host, stream)
+
+
+def _backward(fn, q, k, v, beta_logits, gate_logits, d_o, cu_seqlens, d_final_S, scale, flags,
+              init_S, want_d_init_S, workspace, cu_seqlens_host, stream):
     import torch
     _check(dict(q=q, k=k, v=v, d_o=d_o, beta_logits=beta_logits, gate_logits=gate_logits),
            dtype=q.dtype, device=q.device)
@@ -251,14 +300,14 @@ def la_backward_delta(q, k, v, beta_logits, gate_logits, d_o, cu_seqlens, d_fina
         workspace = torch.empty(la_backward_delta_workspace_size(N, ntok, H, dk, dv),
                                 dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size()
-    rc = library().la_backward_delta(
+    rc = getattr(library(), fn)(
         _ptr(q), _ptr(k), _ptr(v), _ptr(beta_logits), _ptr(gate_logits), _ptr(d_o),
         _ptr(d_final_S), _io(q), _ptr(cu_seqlens), hptr, N, ntok, H, dk, dv, float(scale),
         int(flags), _ptr(init_S), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
         _ptr(out["d_beta_logits"]), _ptr(out["d_gate_logits"]), _ptr(out["d_init_S"]),
         _ptr(workspace), ws_bytes, _stream(stream))
     if rc != LA_OK:
-        raise LinAttnError(rc, "la_backward_delta")
+        raise LinAttnError(rc, fn)
     return out
 
 

@@ -234,6 +234,51 @@ la_status la_backward_delta(const void *q, const void *k, const void *v, const v
     return from_cuda(la::launch_delta_backward(a, static_cast<cudaStream_t>(stream)));
 }
 
+la_status la_prefill_delta_train(const void *q, const void *k, const void *v,
+                                 const void *beta_logits, const void *gate_logits, void *o,
+                                 la_dtype io, const int32_t *cu_seqlens,
+                                 const int32_t *cu_seqlens_host, int N, int ntok, int H, int dk,
+                                 int dv, float scale, unsigned flags, const float *init_S,
+                                 float *final_S, void *saved, size_t saved_bytes, void *stream) {
+    if (la_status st = check_delta_args(q, k, v, beta_logits, gate_logits, o, io, cu_seqlens,
+                                        cu_seqlens_host, N, ntok, H, dk, dv, 64, scale, flags))
+        return st;
+    if (io != LA_BF16 || dk != dv) return LA_ERR_UNSUPPORTED;
+    const size_t need = la::delta_bwd_workspace_bytes(N, ntok, H, dk, dv);
+    if (!saved || saved_bytes < need || (reinterpret_cast<uintptr_t>(saved) & 255u))
+        return LA_ERR_INVALID_ARG;
+    la::PrefillArgs a{q, k, v, beta_logits, gate_logits, o, cu_seqlens, N, ntok, H, dk, dv, scale,
+                      flags, init_S, nullptr, final_S, nullptr, true, saved, saved_bytes};
+    if (!la::delta_train_supported(a)) return LA_ERR_UNSUPPORTED;
+    return from_cuda(la::launch_delta_train_forward(a, static_cast<cudaStream_t>(stream)));
+}
+
+la_status la_backward_delta_saved(const void *q, const void *k, const void *v,
+                                  const void *beta_logits, const void *gate_logits,
+                                  const void *d_o, const float *d_final_S, la_dtype io,
+                                  const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                                  int N, int ntok, int H, int dk, int dv, float scale,
+                                  unsigned flags, const float *init_S, float *dq, float *dk_out,
+                                  float *dv_out, float *d_beta_logits, float *d_gate_logits,
+                                  float *d_init_S, void *saved, size_t saved_bytes, void *stream) {
+    if (la_status st = check_delta_args(q, k, v, beta_logits, gate_logits, d_o, io, cu_seqlens,
+                                        cu_seqlens_host, N, ntok, H, dk, dv, 64, scale, flags))
+        return st;
+    if (!dq || !dk_out || !dv_out || !d_beta_logits || (gate_logits && !d_gate_logits))
+        return LA_ERR_INVALID_ARG;
+    if (io != LA_BF16 || dk != dv) return LA_ERR_UNSUPPORTED;   // as la_prefill_delta_train
+    const size_t need = la::delta_bwd_workspace_bytes(N, ntok, H, dk, dv);
+    if (!saved || saved_bytes < need || (reinterpret_cast<uintptr_t>(saved) & 255u))
+        return LA_ERR_INVALID_ARG;
+    la::BwdArgs a{q, k, v, beta_logits, gate_logits, d_o, d_final_S, init_S, cu_seqlens, N, ntok,
+                  H, dk, dv, scale, flags, dq, dk_out, dv_out, d_beta_logits, d_gate_logits,
+                  d_init_S, saved, true};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // unaligned gradient tensors: the token-serial form, recomputing the forward
+    if (!la::delta_bwd_chunked_supported(a)) return from_cuda(la::launch_delta_backward(a, s));
+    return from_cuda(la::launch_delta_backward_saved(a, s));
+}
+
 la_status la_selftest_wait_timeout(void *stream) {
     unsigned *err = la::device_error_word();
     if (!err) return LA_ERR_CUDA;

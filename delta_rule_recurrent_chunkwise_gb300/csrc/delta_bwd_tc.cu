@@ -414,44 +414,109 @@ size_t delta_bwd_chunked_workspace_bytes(int N, int ntok, int H, int D) {
     return chunk_ws(N, ntok, H, D).total;
 }
 
-cudaError_t launch_delta_backward_chunked(const BwdArgs &a, cudaStream_t s) {
+namespace {
+
+// The backward workspace's regions after the forward's own workspace.
+struct ChunkPtrs {
+    uint8_t *base;
+    float *states, *dstates;
+    __nv_bfloat16 *dstates16, *du;
+    uint8_t *tiles;
+};
+
+ChunkPtrs chunk_ptrs(void *workspace, const ChunkWs &w) {
+    ChunkPtrs c;
+    c.base = static_cast<uint8_t *>(workspace);
+    c.states = reinterpret_cast<float *>(c.base + w.fwd);
+    c.dstates = reinterpret_cast<float *>(c.base + w.fwd + w.states);
+    c.dstates16 = reinterpret_cast<__nv_bfloat16 *>(c.base + w.fwd + w.states + w.dstates);
+    c.du = reinterpret_cast<__nv_bfloat16 *>(c.base + w.fwd + w.states + w.dstates + w.dstates16);
+    c.tiles = c.base + w.fwd + w.states + w.dstates + w.dstates16 + w.du;
+    return c;
+}
+
+// The forward pass with everything the gradients need kept in the backward
+// workspace: its records and chunk table, T of every chunk and the state at
+// every chunk start.  f.o and f.final_S are written when given.
+PrefillArgs saving_forward_args(const PrefillArgs &f) {
+    const ChunkWs w = chunk_ws(f.N, f.ntok, f.H, f.dk);
+    const ChunkPtrs c = chunk_ptrs(f.workspace, w);
+    PrefillArgs pa = f;
+    pa.workspace = c.base;
+    pa.workspace_bytes = w.fwd;
+    pa.chunk = tile::C;
+    pa.chunk_states = c.states;
+    pa.t_out = c.tiles;
+    return pa;
+}
+
+// The reverse chain and the per-chunk gradients from a workspace that holds
+// the forward's saved tensors.
+cudaError_t launch_gradients(const BwdArgs &a, cudaStream_t s) {
     const int D = a.dk;
     const ChunkWs w = chunk_ws(a.N, a.ntok, a.H, D);
-    uint8_t *base = static_cast<uint8_t *>(a.workspace);
-    float *states = reinterpret_cast<float *>(base + w.fwd);
-    float *dstates = reinterpret_cast<float *>(base + w.fwd + w.states);
-    __nv_bfloat16 *dstates16 = reinterpret_cast<__nv_bfloat16 *>(base + w.fwd + w.states + w.dstates);
-    __nv_bfloat16 *du = reinterpret_cast<__nv_bfloat16 *>(base + w.fwd + w.states + w.dstates + w.dstates16);
-    uint8_t *tiles = base + w.fwd + w.states + w.dstates + w.dstates16 + w.du;
+    const ChunkPtrs c = chunk_ptrs(a.workspace, w);
     unsigned *err = device_error_word();
     if (!err) return cudaErrorInvalidValue;
 
-    // 1. the forward pass, keeping its records and the state at every chunk start
-    PrefillArgs pa{a.q, a.k, a.v, a.beta_logits, a.gate_logits, nullptr, a.cu_seqlens, a.N,
-                   a.ntok, a.H, D, D, a.scale, a.flags, a.init_S, nullptr, nullptr, nullptr,
-                   true, base, w.fwd};
-    pa.chunk_states = states;
-    pa.t_out = tiles;
-    if (!delta_tc_supported(pa)) return cudaErrorInvalidValue;
-    cudaError_t e = launch_delta_tc(pa, s);
-    if (e != cudaSuccess) return e;
-
-    // 2. dS from the last chunk to the first
-    const uint8_t *records = base + tile::Workspace::table_bytes(a.N, a.ntok);
+    // dS from the last chunk to the first
+    const uint8_t *records = c.base + tile::Workspace::table_bytes(a.N, a.ntok);
     ChainParams cp{records, static_cast<const __nv_bfloat16 *>(a.d_o), a.cu_seqlens, a.d_final_S,
-                   dstates, dstates16, du, a.d_init_S, err, a.H, a.ntok, a.scale};
+                   c.dstates, c.dstates16, c.du, a.d_init_S, err, a.H, a.ntok, a.scale};
     const bool gated = a.gate_logits != nullptr;   // records carry e^{b_L}; else it is 1
+    cudaError_t e;
     if (D == 64) e = gated ? launch_chain<64, true>(cp, a.N, a.H, s) : launch_chain<64, false>(cp, a.N, a.H, s);
     else e = gated ? launch_chain<128, true>(cp, a.N, a.H, s) : launch_chain<128, false>(cp, a.N, a.H, s);
     if (e != cudaSuccess) return e;
 
-    // 3. every (chunk, head): the gradients, through the prologue
+    // every (chunk, head): the gradients, through the prologue
     const int64_t n_tasks = tile::Workspace::slots(a.N, a.ntok) * a.H;
-    const int2 *table = reinterpret_cast<const int2 *>(base);
-    BwdChannelArgs ca{a.q, a.k, a.v, a.beta_logits, a.gate_logits, a.d_o, table, states, dstates,
-                      dstates16, du, tiles, a.dq, a.dk_out, a.dv_out, a.d_beta_logits,
-                      a.gate_logits ? a.d_gate_logits : nullptr, n_tasks, a.H, D, a.scale, a.flags};
+    const int2 *table = reinterpret_cast<const int2 *>(c.base);
+    BwdChannelArgs ca{a.q, a.k, a.v, a.beta_logits, a.gate_logits, a.d_o, table, c.states,
+                      c.dstates, c.dstates16, c.du, c.tiles, a.dq, a.dk_out, a.dv_out,
+                      a.d_beta_logits, a.gate_logits ? a.d_gate_logits : nullptr, n_tasks, a.H, D,
+                      a.scale, a.flags};
     return launch_delta_bwd_channel(ca, s);
+}
+
+}  // namespace
+
+cudaError_t launch_delta_backward_chunked(const BwdArgs &a, cudaStream_t s) {
+    // 1. the forward pass, keeping what the gradients need (no output)
+    PrefillArgs f{a.q, a.k, a.v, a.beta_logits, a.gate_logits, nullptr, a.cu_seqlens, a.N,
+                  a.ntok, a.H, a.dk, a.dk, a.scale, a.flags, a.init_S, nullptr, nullptr, nullptr,
+                  true, a.workspace, 0};
+    const PrefillArgs pa = saving_forward_args(f);
+    if (!delta_tc_supported(pa)) return cudaErrorInvalidValue;
+    cudaError_t e = launch_delta_tc(pa, s);
+    // 2, 3. the reverse chain, then every (chunk, head) in parallel
+    return e != cudaSuccess ? e : launch_gradients(a, s);
+}
+
+bool delta_train_supported(const PrefillArgs &a) {
+    return a.bf16 && a.dk == a.dv && (a.dk == 64 || a.dk == 128) &&
+           delta_tc_supported(saving_forward_args(a));
+}
+
+cudaError_t launch_delta_train_forward(const PrefillArgs &a, cudaStream_t s) {
+    const PrefillArgs pa = saving_forward_args(a);
+    if (!delta_tc_supported(pa)) return cudaErrorInvalidValue;
+    return launch_delta_tc(pa, s);
+}
+
+cudaError_t launch_delta_backward_saved(const BwdArgs &a, cudaStream_t s) {
+    // The chunk table is rebuilt from this call's cu_seqlens, so the per-chunk
+    // kernel's token rows stay inside the tensors whatever the workspace held.
+    PrefillArgs f{a.q, a.k, a.v, a.beta_logits, a.gate_logits, nullptr, a.cu_seqlens, a.N,
+                  a.ntok, a.H, a.dk, a.dk, a.scale, a.flags, a.init_S, nullptr, nullptr, nullptr,
+                  true, a.workspace, 0};
+    const PrefillArgs pa = saving_forward_args(f);
+    TcLaunch x{};
+    x.a = &pa;
+    x.slots = tile::Workspace::slots(a.N, a.ntok);
+    x.table = static_cast<int2 *>(pa.workspace);
+    cudaError_t e = launch_chunk_table(x, s);
+    return e != cudaSuccess ? e : launch_gradients(a, s);
 }
 
 }  // namespace la

@@ -70,6 +70,13 @@ cudaError_t launch_delta_backward(const BwdArgs &a, cudaStream_t s);
 bool delta_bwd_chunked_supported(const BwdArgs &a);
 size_t delta_bwd_chunked_workspace_bytes(int N, int ntok, int H, int D);
 cudaError_t launch_delta_backward_chunked(const BwdArgs &a, cudaStream_t s);
+// The same split for training: the forward pass (a.workspace = a backward
+// workspace of delta_bwd_workspace_bytes) writing o and final_S as asked and
+// keeping the records, T and the chunk-start states there; then the
+// gradients from that workspace, without the forward recomputation.
+bool delta_train_supported(const PrefillArgs &a);
+cudaError_t launch_delta_train_forward(const PrefillArgs &a, cudaStream_t s);
+cudaError_t launch_delta_backward_saved(const BwdArgs &a, cudaStream_t s);
 
 // fp32 SIMT chunk kernels (any I/O dtype).
 cudaError_t launch_linear_simt(const PrefillArgs &a, cudaStream_t s);

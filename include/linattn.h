@@ -259,6 +259,50 @@ la_status la_backward_delta(const void *q, const void *k, const void *v, const v
                             float *d_gate_logits, float *d_init_S, void *workspace,
                             size_t workspace_bytes, void *stream);
 
+/* Training pair: the forward pass that keeps what the gradients need, and
+ * the gradients without recomputing that forward.  (The page motivates the
+ * chunked form by training, section DeltaNet (Parallelizing Linear
+ * Transformers with Delta Rule); it has no such interface.  la_backward_delta
+ * runs the forward again inside the call; a training step that has just run
+ * it pays for it twice.)
+ *
+ * la_prefill_delta_train: the outputs of la_prefill_delta at chunk = 64 (o,
+ * and final_S when given), from the same tensor-core kernels, plus the
+ * per-chunk records, each chunk's T = (I + A)^{-1} and the fp32 state at
+ * every chunk start, kept in `saved`: a buffer of
+ * la_backward_delta_workspace_size(N, ntok, H, dk, dv) bytes, 256-byte
+ * aligned, owned by the caller and left untouched by the library between the
+ * two calls.  Arguments otherwise as la_prefill_delta.  Configurations: those
+ * of the chunkwise backward (io = LA_BF16, dk = dv in {64, 128}, every tensor
+ * 16-byte aligned); LA_ERR_UNSUPPORTED otherwise (use la_prefill_delta and
+ * la_backward_delta there); LA_ERR_INVALID_ARG for a missing, small or
+ * misaligned `saved`. */
+la_status la_prefill_delta_train(const void *q, const void *k, const void *v,
+                                 const void *beta_logits, const void *gate_logits, void *o,
+                                 la_dtype io, const int32_t *cu_seqlens,
+                                 const int32_t *cu_seqlens_host, int N, int ntok, int H, int dk,
+                                 int dv, float scale, unsigned flags, const float *init_S,
+                                 float *final_S, void *saved, size_t saved_bytes, void *stream);
+
+/* la_backward_delta_saved: the gradients of la_backward_delta, with the same
+ * arguments and outputs, taking the forward's tensors from `saved` as the
+ * preceding la_prefill_delta_train left them (pass that call's q, k, v,
+ * beta_logits, gate_logits, cu_seqlens, scale, flags and init_S; the results
+ * are undefined otherwise, though every access stays inside the given
+ * tensors).  The reverse chain and the per-chunk kernels read `saved` and
+ * write only its scratch part (dS' and du of every chunk), so the call may be
+ * repeated on the same saved tensors.  If the gradient tensors are not all
+ * 16-byte aligned, it runs la_backward_delta's token-serial form instead,
+ * which recomputes the forward in the same buffer. */
+la_status la_backward_delta_saved(const void *q, const void *k, const void *v,
+                                  const void *beta_logits, const void *gate_logits,
+                                  const void *d_o, const float *d_final_S, la_dtype io,
+                                  const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                                  int N, int ntok, int H, int dk, int dv, float scale,
+                                  unsigned flags, const float *init_S, float *dq, float *dk_out,
+                                  float *dv_out, float *d_beta_logits, float *d_gate_logits,
+                                  float *d_init_S, void *saved, size_t saved_bytes, void *stream);
+
 /* Synchronises `stream`, then reports (and clears) any error raised on the
  * current device since the previous check: LA_ERR_TIMEOUT if a bounded
  * in-kernel wait gave up, LA_ERR_INVALID_ARG if a kernel found cu_seqlens

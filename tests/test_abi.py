@@ -210,6 +210,41 @@ def test_backward_checks_arguments_and_workspace(lib):
     assert b(*odd, *outs, FAKE, need, None) == la.LA_ERR_UNSUPPORTED
 
 
+def test_training_pair_checks_arguments_and_saved_buffer(lib):
+    """la_prefill_delta_train / la_backward_delta_saved: the forward call's
+    checks, the chunkwise configurations only (bf16, dk = dv), and a saved
+    buffer of la_backward_delta_workspace_size bytes, 256-byte aligned, all
+    before any launch."""
+    N, ntok, H, d = 2, 40, 4, 64
+    need = la.la_backward_delta_workspace_size(N, ntok, H, d, d)
+    MIS = ctypes.c_void_p(0x1000 + 128)   # not 256-byte aligned
+    t = lib.la_prefill_delta_train
+    fwd = (FAKE, FAKE, FAKE, FAKE, None, FAKE)
+    tail = (1.0, la.LA_L2NORM_K, None, None)
+    assert t(*fwd, la.LA_BF16, FAKE, None, N, ntok, H, d, d, *tail, None, need, None) == \
+        la.LA_ERR_INVALID_ARG                                                       # no buffer
+    assert t(*fwd, la.LA_BF16, FAKE, None, N, ntok, H, d, d, *tail, FAKE, need - 1, None) == \
+        la.LA_ERR_INVALID_ARG                                                       # too small
+    assert t(*fwd, la.LA_BF16, FAKE, None, N, ntok, H, d, d, *tail, MIS, need, None) == \
+        la.LA_ERR_INVALID_ARG                                                       # misaligned
+    assert t(*fwd, la.LA_F32, FAKE, None, N, ntok, H, d, d, *tail, FAKE, need, None) == \
+        la.LA_ERR_UNSUPPORTED                                                       # fp32 I/O
+    assert t(*fwd, la.LA_BF16, FAKE, None, N, ntok, H, d, 128, *tail, FAKE, need, None) == \
+        la.LA_ERR_UNSUPPORTED                                                       # dk != dv
+    assert t(*fwd[:5], None, la.LA_BF16, FAKE, None, N, ntok, H, d, d, *tail, FAKE, need,
+             None) == la.LA_ERR_INVALID_ARG                                          # no o
+    b = lib.la_backward_delta_saved
+    head = (FAKE, FAKE, FAKE, FAKE, None, FAKE, None, la.LA_BF16, FAKE, None, N, ntok, H, d, d,
+            1.0, la.LA_L2NORM_K, None)
+    outs = (FAKE, FAKE, FAKE, FAKE, None, None)
+    assert b(*head, *outs, None, need, None) == la.LA_ERR_INVALID_ARG
+    assert b(*head, *outs, FAKE, need - 1, None) == la.LA_ERR_INVALID_ARG
+    assert b(*head, *outs, MIS, need, None) == la.LA_ERR_INVALID_ARG
+    assert b(*head, None, *outs[1:], FAKE, need, None) == la.LA_ERR_INVALID_ARG  # no dq
+    f32 = head[:7] + (la.LA_F32,) + head[8:]
+    assert b(*f32, *outs, FAKE, need, None) == la.LA_ERR_UNSUPPORTED
+
+
 def test_launch_count_query(lib):
     """la_prefill_delta_launches: 1 for the CUDA-core path, 1 or 2 for the
     tensor-core path (2 wherever no device can hold the one-launch grid, as
