@@ -11,7 +11,8 @@ Functions (same names as the C ABI):
   la_prefill_delta_launches,
   la_prefill_delta_static, la_decode_step, la_decode_step_slots,
   la_backward_delta, la_prefill_delta_train, la_backward_delta_saved,
-  la_check_device, la_selftest_wait_timeout, la_status_string.
+  la_check_device, la_selftest_wait_timeout, la_status_string;
+and delta_rule, a torch.autograd.Function over the training pair.
 """
 from __future__ import annotations
 
@@ -275,6 +276,61 @@ def la_backward_delta_saved(q, k, v, beta_logits, gate_logits, d_o, cu_seqlens, 
     return _backward("la_backward_delta_saved", q, k, v, beta_logits, gate_logits, d_o,
                      cu_seqlens, d_final_S, scale, flags, init_S, want_d_init_S, saved,
                      cu_seqlens_host, stream)
+
+
+_DeltaRuleFn = None
+
+
+def delta_rule(q, k, v, beta_logits, gate_logits, cu_seqlens, scale=1.0, flags=LA_L2NORM_K,
+               init_S=None, cu_seqlens_host=None):
+    """Differentiable delta-rule prefill for torch training: returns
+    (o, final_S); the forward is la_prefill_delta_train, the backward
+    la_backward_delta_saved from the buffer the forward filled (one buffer per
+    call, held until the backward).  bf16 q, k, v, beta_logits, gate_logits
+    (or None) with dk = dv in {64, 128}; init_S fp32 or None.  Gradients
+    reach every tensor input that requires one, cast to its dtype."""
+    global _DeltaRuleFn
+    if _DeltaRuleFn is None:
+        import torch
+
+        class _Fn(torch.autograd.Function):
+            @staticmethod
+            def forward(ctx, q, k, v, beta_logits, gate_logits, init_S, cu_seqlens, scale, flags,
+                        cu_host):
+                ntok, H, dk = q.shape
+                N = cu_seqlens.numel() - 1
+                saved = torch.empty(la_backward_delta_workspace_size(N, ntok, H, dk, v.shape[2]),
+                                    dtype=torch.uint8, device=q.device)
+                o = torch.empty_like(v)
+                final_S = torch.empty((N, H, dk, v.shape[2]), dtype=torch.float32,
+                                      device=q.device)
+                la_prefill_delta_train(q, k, v, beta_logits, gate_logits, o, cu_seqlens, saved,
+                                       scale=scale, flags=flags, init_S=init_S, final_S=final_S,
+                                       cu_seqlens_host=cu_host)
+                ctx.save_for_backward(q, k, v, beta_logits, gate_logits, init_S, cu_seqlens,
+                                      saved)
+                ctx.scale, ctx.flags, ctx.cu_host = scale, flags, cu_host
+                return o, final_S
+
+            @staticmethod
+            def backward(ctx, d_o, d_final_S):
+                q, k, v, beta_logits, gate_logits, init_S, cu_seqlens, saved = ctx.saved_tensors
+                if d_o is None:
+                    d_o = torch.zeros_like(v)
+                g = la_backward_delta_saved(
+                    q, k, v, beta_logits, gate_logits, d_o.to(q.dtype).contiguous(), cu_seqlens,
+                    saved, d_final_S=None if d_final_S is None else d_final_S.float().contiguous(),
+                    scale=ctx.scale, flags=ctx.flags, init_S=init_S,
+                    want_d_init_S=init_S is not None, cu_seqlens_host=ctx.cu_host)
+                cast = lambda x, like: None if x is None or like is None else x.to(like.dtype)
+                return (cast(g["dq"], q), cast(g["dk"], k), cast(g["dv"], v),
+                        cast(g["d_beta_logits"], beta_logits),
+                        cast(g["d_gate_logits"], gate_logits), cast(g["d_init_S"], init_S),
+                        None, None, None, None)
+
+        _DeltaRuleFn = _Fn
+    return _DeltaRuleFn.apply(q, k, v, beta_logits, gate_logits, init_S, cu_seqlens, float(scale),
+                              int(flags), cu_seqlens_host)
 
 
 def _backward(fn, q, k, v, beta_logits, gate_logits, d_o, cu_seqlens, d_final_S, scale, flags,

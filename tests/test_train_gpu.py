@@ -129,3 +129,34 @@ def test_train_forward_refuses_fp32(cuda_lib):
         la.la_prefill_delta_train(t["q"], t["k"], t["v"], t["beta_logits"], None,
                                   torch.empty_like(t["v"]), inp["cu_seqlens"].to(dev), saved)
     assert e.value.status == la.LA_ERR_UNSUPPORTED
+
+
+def test_delta_rule_autograd(cuda_lib):
+    """delta_rule as a torch.autograd.Function: a loss over o and final_S
+    back-propagates to every input the same gradients la_backward_delta
+    returns for that loss's output gradients (cast to each input's dtype)."""
+    la = cuda_lib
+    dev = torch.device("cuda")
+    inp = wl.prefill_inputs([150, 64, 9], 2, 64, 64, torch.bfloat16, True, seed=97,
+                            init_state=True)
+    leaves = {n: inp[n].to(dev).requires_grad_(True) for n in NAMES}
+    cu = inp["cu_seqlens"].to(dev)
+    o, fS = la.delta_rule(leaves["q"], leaves["k"], leaves["v"], leaves["beta_logits"],
+                          leaves["gate_logits"], cu, init_S=leaves["init_S"],
+                          cu_seqlens_host=inp["cu_seqlens"])
+    d_o, d_fS = _grad_inputs(inp, torch.bfloat16, seed=98)
+    loss = (o.float() * d_o.to(dev).float()).sum() + (fS * d_fS.to(dev)).sum()
+    loss.backward()
+    assert la.la_check_device() == la.LA_OK
+    t = {n: inp[n].to(dev) for n in NAMES}
+    ref = la.la_backward_delta(t["q"], t["k"], t["v"], t["beta_logits"], t["gate_logits"],
+                               d_o.to(dev), cu, d_final_S=d_fS.to(dev), init_S=t["init_S"],
+                               cu_seqlens_host=inp["cu_seqlens"])
+    pairs = (("q", "dq"), ("k", "dk"), ("v", "dv"), ("beta_logits", "d_beta_logits"),
+             ("gate_logits", "d_gate_logits"), ("init_S", "d_init_S"))
+    for leaf, name in pairs:
+        g = leaves[leaf].grad
+        assert g is not None and g.dtype == leaves[leaf].dtype, leaf
+        # bf16 inputs get the fp32 gradient rounded to bf16 (relative 2^-9)
+        bar = 1e-5 if g.dtype == torch.float32 else 4e-3
+        assert rel_err(g.float().cpu().numpy(), ref[name].cpu().numpy()) <= bar, leaf
