@@ -182,14 +182,17 @@ class Model:
     def run(self):
         ready = {n: (lambda: True) for n in self.roles}
         finished = set()
-        for _ in range(200000):
+        # every role runs at a speed drawn per run (some 50 times slower than
+        # others), so that schedules starving one role are common
+        speed = {n: self.rng.choice((0.02, 1.0)) for n in self.roles}
+        for _ in range(400000):
             live = [n for n in self.roles if n not in finished and ready[n]()]
             workers = [n for n in self.roles if n not in finished and n not in ("tensor", "copy")]
             if not workers:
                 assert not self.copies
                 return
             assert live, f"deadlock: {self.waiting}"
-            n = self.rng.choice(live)
+            n = self.rng.choices(live, weights=[speed[x] for x in live])[0]
             self.waiting.pop(n, None)
             try:
                 ready[n] = next(self.roles[n])
