@@ -160,3 +160,30 @@ def test_delta_rule_autograd(cuda_lib):
         # bf16 inputs get the fp32 gradient rounded to bf16 (relative 2^-9)
         bar = 1e-5 if g.dtype == torch.float32 else 4e-3
         assert rel_err(g.float().cpu().numpy(), ref[name].cpu().numpy()) <= bar, leaf
+
+
+def test_delta_rule_autograd_optional_inputs(cuda_lib):
+    """delta_rule's optional pieces: the additive rule with no beta, a
+    scalar gate at d = 128, no initial state, and a loss on o alone (so no
+    final-state gradient reaches the backward)."""
+    la = cuda_lib
+    dev = torch.device("cuda")
+    inp = wl.prefill_inputs([130, 7, 64], 2, 128, 128, torch.bfloat16, True, seed=99,
+                            scalar_gate=True)
+    names = ("q", "k", "v", "gate_logits")
+    leaves = {n: inp[n].to(dev).requires_grad_(True) for n in names}
+    cu = inp["cu_seqlens"].to(dev)
+    flags = la.LA_ADDITIVE | la.LA_GATE_SCALAR | la.LA_L2NORM_K
+    o, fS = la.delta_rule(leaves["q"], leaves["k"], leaves["v"], None, leaves["gate_logits"], cu,
+                          flags=flags, cu_seqlens_host=inp["cu_seqlens"])
+    g = torch.Generator().manual_seed(100)
+    d_o = torch.randn(inp["v"].shape, generator=g).to(torch.bfloat16)
+    (o.float() * d_o.to(dev).float()).sum().backward()
+    assert la.la_check_device() == la.LA_OK
+    t = {n: inp[n].to(dev) for n in names}
+    ref = la.la_backward_delta(t["q"], t["k"], t["v"], None, t["gate_logits"], d_o.to(dev), cu,
+                               flags=flags, cu_seqlens_host=inp["cu_seqlens"])
+    for leaf, name in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("gate_logits", "d_gate_logits")):
+        got = leaves[leaf].grad
+        assert got is not None and got.dtype == torch.bfloat16, leaf
+        assert rel_err(got.float().cpu().numpy(), ref[name].cpu().numpy()) <= 4e-3, leaf
